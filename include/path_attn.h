@@ -1,0 +1,145 @@
+/*
+ * path_attn.h — C ABI of the GB300 (sm_103a) PaTH attention library.
+ *
+ * PaTH attention (Yang et al., "PaTH Attention: Position Encoding via Accumulating Householder
+ * Transformations", arXiv 2505.16381v2; reading notes at cc.laoqi.cc/papers/2505.16381/v2/r1):
+ *
+ *   H_t        = I - beta_t w_t w_t^T                          (notes §2.1)
+ *   logit(i,j) = scale * k_j^T H_{j+1} H_{j+2} ... H_i q_i       (j <= i; H_j excluded, H_i included)
+ *              + sum_{s=j+1..i} log f_s                         (optional PaTH-FoX gate, notes §2.5)
+ *   o_i        = sum_{j<=i} softmax_j(logit(i,.)) v_j,  lse_i = log sum_{j<=i} exp(logit(i,j))
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensor arguments are DEVICE pointers into memory the caller owns (cudaMalloc, PyTorch,
+ *    ...).  The library allocates nothing, frees nothing, and keeps no state between calls
+ *    other than a per-device attribute cache.  Calls are reentrant.
+ *  - Layouts are dense row-major: q,k,v,w,o,dO,dq,dk,dv,dw are [batch][heads][seqlen][head_dim];
+ *    beta, log_f, lse, dbeta are [batch][heads][seqlen].  Decode vectors are
+ *    [batch][heads][head_dim], beta_t is [batch][heads], caches are
+ *    [batch][heads][capacity][head_dim].
+ *  - Element type of q,k,v,w,o,dO,dq,dk,dv,dw and of the caches: the descriptor's dtype
+ *    (PATH_BF16 or PATH_FP32).  beta, log_f, lse, dbeta are always float32.  Arithmetic
+ *    accumulates in fp32.
+ *  - Every tensor pointer must be 16-byte aligned.  Workspace ("ws") pointers must be 256-byte
+ *    aligned and hold at least the size returned by the matching *_workspace_size function.
+ *  - beta is clamped to [0, 2] inside the kernels (the range of the 2*sigmoid parameterisation,
+ *    notes §2.1/§2.2).  Inputs already in range are used unchanged; dbeta is the gradient with
+ *    respect to the clamped value.  w is used as given (it is not renormalised).
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).  Work is
+ *    enqueued asynchronously; faults inside kernels surface at the caller's next sync.
+ *  - Errors: every argument is validated before any CUDA call; on a validation error nothing
+ *    is launched and a status below is returned.  Launch failures return PATH_ERR_CUDA.
+ *    No exception crosses the ABI.
+ */
+#ifndef PATH_ATTN_H
+#define PATH_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PATH_OK = 0,
+  PATH_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer, bad enum */
+  PATH_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim != 64, chunk value, ...) */
+  PATH_ERR_WORKSPACE = 3,    /* ws_bytes smaller than the required workspace */
+  PATH_ERR_CAPACITY = 4,     /* decode: t + 1 > capacity */
+  PATH_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+  PATH_ERR_INTERNAL = 6
+} path_status_t;
+
+typedef enum { PATH_BF16 = 0, PATH_FP32 = 1 } path_dtype_t;
+
+typedef struct {
+  int batch;      /* > 0 */
+  int heads;      /* > 0 */
+  int seqlen;     /* L > 0 */
+  int head_dim;   /* d; 64 is supported */
+  int dtype;      /* path_dtype_t of q,k,v,w,o (and dO,dq,dk,dv,dw in the backward) */
+  float scale;    /* multiplies the Householder-path logit; the forget bias is added unscaled */
+  int chunk;      /* UT chunk size B; 0 lets the library choose (see path_attn_chunk) */
+} path_attn_desc_t;
+
+typedef struct {
+  int batch;       /* > 0 */
+  int heads;       /* > 0 */
+  int head_dim;    /* 64 */
+  int capacity;    /* rows allocated per (batch, head) in each cache */
+  int cache_dtype; /* path_dtype_t of the caches and of q_t,k_t,v_t,w_t,o_t */
+  float scale;     /* logit multiplier */
+} path_decode_desc_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* path_status_string(int status);
+
+/* Chunk size B used by the forward (for_backward = 0) or backward (1) pass for this
+ * descriptor, or minus a path_status_t if the descriptor is invalid/unsupported. Host only. */
+int path_attn_chunk(const path_attn_desc_t* desc, int for_backward);
+
+/* Bytes of workspace path_attn_fwd (for_backward = 0) or path_attn_bwd (for_backward = 1)
+ * needs for this descriptor; 0 if the descriptor is invalid.  Host only, no CUDA call. */
+size_t path_attn_workspace_size(const path_attn_desc_t* desc, int for_backward);
+
+/*
+ * Forward pass: o and lse for every (batch, head, row).
+ *
+ * Steps (notes §2.6–§2.7): per chunk of B positions, the UT transform
+ * U = (I + strictLower(D W W^T))^{-1} D by forward substitution; the boundary-adjusted queries
+ * Q<- = Q - lower(Q W^T) U W, keys K-> = K - (U strictLower(W K^T))^T W and chunk transform
+ * F = I - W^T U^T W; the diagonal chunk from lower(Q K^T) - lower(Q W^T) U strictLower(W K^T);
+ * then, per query chunk, a right-to-left scan over earlier chunks (scores Z K->^T, online
+ * softmax, O += P V, Z <- Z F^T).
+ *
+ * log_f: forget-gate log values (<= 0) or NULL for plain PaTH.
+ * o: output, desc dtype.  lse: float32 natural-log log-sum-exp per row (the backward needs it).
+ * ws/ws_bytes: scratch of at least path_attn_workspace_size(desc, 0) bytes; its contents on
+ * entry are ignored and on exit are unspecified.
+ */
+int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                  const void* w, const float* beta, const float* log_f, void* o, float* lse,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass: gradients of sum(dO * o) with respect to q, k, v, w and beta, given the
+ * forward's o and lse for the same inputs.  The pages give no backward; this is the exact
+ * derivative of the forward definition, evaluated blockwise: recomputed per-chunk UT
+ * quantities, a descending scan that stores the transported queries Z_c, an ascending adjoint
+ * scan G_c = dS_c K->_c + G_{c-1} F_c with dF_c += G_{c-1}^T Z_c, then the chain rule through
+ * the per-chunk UT quantities.
+ *
+ * dq,dk,dv,dw: desc dtype outputs (overwritten).  dbeta: float32 (overwritten).
+ * log_f and dlog_f must be NULL (the forget-gate gradient is not implemented:
+ * PATH_ERR_UNSUPPORTED otherwise).
+ * ws: at least path_attn_workspace_size(desc, 1) bytes.
+ */
+int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                  const void* w, const float* beta, const float* log_f, const void* o,
+                  const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dw,
+                  float* dbeta, float* dlog_f, void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace path_decode_step needs for any t < capacity; 0 if invalid. Host only. */
+size_t path_decode_workspace_size(const path_decode_desc_t* desc);
+
+/*
+ * One decode step at position t (notes §2.8, Eq. (1)).  On entry rows 0..t-1 of each cache
+ * hold the keys/values of earlier positions, keys already transported to position t-1.
+ * The step
+ *   1. rewrites every cached key in place: k_j <- k_j - beta_t (w_t . k_j) w_t   (j < t),
+ *   2. appends k_t and v_t unchanged at row t,
+ *   3. writes o_t = sum_j softmax_j(scale k_j . q_t) v_j over j = 0..t.
+ * Requires 0 <= t and t + 1 <= capacity (else PATH_ERR_CAPACITY).
+ * q_t,k_t,v_t,w_t,o_t: [batch][heads][head_dim] in cache_dtype; beta_t: [batch][heads] float32.
+ * ws: at least path_decode_workspace_size(desc) bytes (per-split partial softmax states).
+ */
+int path_decode_step(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int t,
+                     const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                     const float* beta_t, void* o_t, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATH_ATTN_H */

@@ -1,0 +1,148 @@
+// C ABI of the PaTH attention library: argument validation, workspace layout and kernel
+// dispatch.  Declared in include/path_attn.h.
+#include "../../include/path_attn.h"
+#include "internal.h"
+
+#include <math.h>
+#include <stdint.h>
+
+using namespace pathattn;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validates a descriptor; on success fills g for the requested pass.
+int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
+  if (!d) return PATH_ERR_INVALID_ARG;
+  if (d->batch <= 0 || d->heads <= 0 || d->seqlen <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
+  if (d->dtype != PATH_BF16 && d->dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
+  if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
+  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  const long long BH = (long long)d->batch * d->heads;
+  if (BH > 65535) return PATH_ERR_UNSUPPORTED;
+  int B;
+  if (for_backward) {
+    B = 32;
+  } else {
+    if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
+    B = d->chunk ? d->chunk : 64;
+  }
+  const long long nc = (d->seqlen + B - 1) / B;
+  if (nc > 65535) return PATH_ERR_UNSUPPORTED;
+  if (g) {
+    g->BH = (int)BH;
+    g->L = d->seqlen;
+    g->B = B;
+    g->nc = (int)nc;
+    g->Lp = (int)(nc * B);
+    g->scale = d->scale;
+  }
+  return PATH_OK;
+}
+
+#define CHECK_PTR(p)                         \
+  do {                                       \
+    if (!(p)) return PATH_ERR_INVALID_ARG;   \
+    if (!aligned((p), 16)) return PATH_ERR_INVALID_ARG; \
+  } while (0)
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA; }
+
+}  // namespace
+
+#define PATH_API __attribute__((visibility("default")))
+extern "C" {
+
+PATH_API const char* path_status_string(int status) {
+  switch (status) {
+    case PATH_OK: return "PATH_OK";
+    case PATH_ERR_INVALID_ARG: return "PATH_ERR_INVALID_ARG: invalid argument (null/misaligned pointer, bad size or enum)";
+    case PATH_ERR_UNSUPPORTED: return "PATH_ERR_UNSUPPORTED: valid but unsupported configuration";
+    case PATH_ERR_WORKSPACE: return "PATH_ERR_WORKSPACE: workspace too small";
+    case PATH_ERR_CAPACITY: return "PATH_ERR_CAPACITY: decode position exceeds cache capacity";
+    case PATH_ERR_CUDA: return "PATH_ERR_CUDA: CUDA launch or runtime error";
+    case PATH_ERR_INTERNAL: return "PATH_ERR_INTERNAL: internal error";
+    default: return "unknown path_status_t";
+  }
+}
+
+PATH_API int path_attn_chunk(const path_attn_desc_t* desc, int for_backward) {
+  Geom g;
+  const int rc = check_desc(desc, for_backward, &g);
+  return rc == PATH_OK ? g.B : -rc;
+}
+
+PATH_API size_t path_attn_workspace_size(const path_attn_desc_t* desc, int for_backward) {
+  Geom g;
+  if (check_desc(desc, for_backward, &g) != PATH_OK) return 0;
+  return for_backward ? bwd_ws_layout(g).total : fwd_ws_layout(g, 4).total;
+}
+
+PATH_API int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                  const void* w, const float* beta, const float* log_f, void* o, float* lse,
+                  void* ws, size_t ws_bytes, void* stream) {
+  Geom g;
+  int rc = check_desc(desc, 0, &g);
+  if (rc != PATH_OK) return rc;
+  CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o); CHECK_PTR(lse);
+  if (log_f && !aligned(log_f, 16)) return PATH_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  const FwdWs lay = fwd_ws_layout(g, 4);
+  if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool bf = desc->dtype == PATH_BF16;
+  char* wsb = (char*)ws;
+  rc = cuda_status(launch_prep_simt(bf, g, q, k, v, w, beta, log_f, wsb, lay, true, st));
+  if (rc != PATH_OK) return rc;
+  return cuda_status(launch_main_simt(bf, g, v, log_f, wsb, lay, o, lse, st));
+}
+
+PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                  const void* w, const float* beta, const float* log_f, const void* o,
+                  const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dw,
+                  float* dbeta, float* dlog_f, void* ws, size_t ws_bytes, void* stream) {
+  Geom g;
+  int rc = check_desc(desc, 1, &g);
+  if (rc != PATH_OK) return rc;
+  CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o);
+  CHECK_PTR(lse); CHECK_PTR(dO); CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dw);
+  CHECK_PTR(dbeta);
+  if (log_f || dlog_f) return PATH_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  const BwdWs lay = bwd_ws_layout(g);
+  if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+  return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,
+                                     dk, dv, dw, dbeta, (char*)ws, lay, (cudaStream_t)stream));
+}
+
+PATH_API size_t path_decode_workspace_size(const path_decode_desc_t* d) {
+  if (!d || d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim != kHeadDim) return 0;
+  if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return 0;
+  const long long BH = (long long)d->batch * d->heads;
+  if (BH > 65535) return 0;
+  return decode_ws_bytes((int)BH);
+}
+
+PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* v_cache, int t,
+                     const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                     const float* beta_t, void* o_t, void* ws, size_t ws_bytes, void* stream) {
+  if (!d) return PATH_ERR_INVALID_ARG;
+  if (d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
+  if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
+  if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
+  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  const long long BH = (long long)d->batch * d->heads;
+  if (BH > 65535) return PATH_ERR_UNSUPPORTED;
+  if (t < 0) return PATH_ERR_INVALID_ARG;
+  if ((long long)t + 1 > d->capacity) return PATH_ERR_CAPACITY;
+  CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(q_t); CHECK_PTR(k_t); CHECK_PTR(v_t);
+  CHECK_PTR(w_t); CHECK_PTR(beta_t); CHECK_PTR(o_t);
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  if (ws_bytes < decode_ws_bytes((int)BH)) return PATH_ERR_WORKSPACE;
+  return cuda_status(launch_decode(d->cache_dtype == PATH_BF16, (int)BH, d->capacity, t, d->scale,
+                                   k_cache, v_cache, q_t, k_t, v_t, w_t, beta_t, o_t, (float*)ws,
+                                   (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pathattn {
+
+constexpr int kHeadDim = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Largest number of persistent CTAs the backward main kernel runs (each owns a slab of
+// transported-query scratch).  8 per SM on a 152-SM GB300.
+constexpr int kBwdMaxCtas = 1216;
+// Largest number of sequence splits of one decode step.
+constexpr int kDecodeMaxSplits = 128;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Problem geometry derived from a descriptor.
+struct Geom {
+  int BH;       // batch * heads
+  int L;        // sequence length
+  int B;        // chunk size
+  int nc;       // number of chunks = ceil(L / B)
+  int Lp;       // padded length nc * B
+  float scale;
+};
+
+// Byte offsets of the forward workspace.  Element type "E" of ql/kr/f is float32 for the SIMT
+// path and bf16 for the tensor-core path (esize).
+struct FwdWs {
+  size_t ql, kr, f;            // Q<- [BH][Lp][64], K-> [BH][Lp][64], F [BH][nc][64][64]
+  size_t dm, dl, dacc;         // diagonal-chunk softmax state: max (log2 domain), sum, acc[64]
+  size_t fa, fr, ft;           // forget gate: local inclusive prefix, local exclusive suffix, chunk total
+  size_t total;
+};
+
+inline FwdWs fwd_ws_layout(const Geom& g, size_t esize) {
+  FwdWs w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  const size_t rows = (size_t)g.BH * g.Lp;
+  w.ql = take(rows * kHeadDim * esize);
+  w.kr = take(rows * kHeadDim * esize);
+  w.f = take((size_t)g.BH * g.nc * kHeadDim * kHeadDim * esize);
+  w.dm = take(rows * 4);
+  w.dl = take(rows * 4);
+  w.dacc = take(rows * kHeadDim * 4);
+  w.fa = take(rows * 4);
+  w.fr = take(rows * 4);
+  w.ft = take((size_t)g.BH * g.nc * 4);
+  w.total = off;
+  return w;
+}
+
+// Backward workspace: the forward layout (fp32 elements) followed by fp32 gradient
+// accumulators and the per-CTA transported-query scratch.
+struct BwdWs {
+  FwdWs fw;
+  size_t Dv;                   // D_i = dO_i . o_i            [BH][Lp]
+  size_t dql, dkr, dv;         // dQ<-, dK->, dV accumulators [BH][Lp][64] fp32
+  size_t df;                   // dF accumulators             [BH][nc][64][64] fp32
+  size_t zs;                   // Z scratch                   [nctas][Lp][64] fp32
+  int nctas;
+  size_t total;
+};
+
+inline int bwd_num_ctas(const Geom& g) {
+  const long tiles = (long)g.BH * g.nc;
+  return (int)(tiles < kBwdMaxCtas ? tiles : kBwdMaxCtas);
+}
+
+inline BwdWs bwd_ws_layout(const Geom& g) {
+  BwdWs w{};
+  w.fw = fwd_ws_layout(g, 4);
+  size_t off = w.fw.total;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  const size_t rows = (size_t)g.BH * g.Lp;
+  w.Dv = take(rows * 4);
+  w.dql = take(rows * kHeadDim * 4);
+  w.dkr = take(rows * kHeadDim * 4);
+  w.dv = take(rows * kHeadDim * 4);
+  w.df = take((size_t)g.BH * g.nc * kHeadDim * kHeadDim * 4);
+  w.nctas = bwd_num_ctas(g);
+  w.zs = take((size_t)w.nctas * g.Lp * kHeadDim * 4);
+  w.total = off;
+  return w;
+}
+
+inline size_t decode_ws_bytes(int BH) {
+  return align_up((size_t)BH * kDecodeMaxSplits * (kHeadDim + 2) * 4, 256);
+}
+
+// ---- launchers (return cudaGetLastError() of their launches) ----
+
+// SIMT (fp32 arithmetic) forward.  is_bf16 selects the input element type.
+cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
+                             const void* v, const void* w, const float* beta, const float* logf,
+                             char* ws, const FwdWs& lay, bool with_diag, cudaStream_t st);
+cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
+                             char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
+
+// SIMT backward.
+cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
+                            const void* v, const void* w, const float* beta, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            void* dw, float* dbeta, char* ws, const BwdWs& lay, cudaStream_t st);
+
+// Decode step.
+cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
+                          const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, void* o, float* partials, cudaStream_t st);
+
+}  // namespace pathattn

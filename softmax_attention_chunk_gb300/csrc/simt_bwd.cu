@@ -1,0 +1,521 @@
+// SIMT (fp32 CUDA-core) backward of PaTH attention.
+//
+// The pages give no backward; this is the exact derivative of the blockwise forward of the
+// PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6–§2.7.  With Z_{b,c} the query chunk b
+// transported to the right edge of key chunk c (Z_{b,b-1} = Q<-_b, Z_{b,c-1} = Z_{b,c} F_c^T):
+//   dV_c  += P^T dO_b,   dK->_c += scale dS^T Z_{b,c},
+//   G_{b,c} = scale dS K->_c + G_{b,c-1} F_c  (ascending c, G_{b,-1} = 0),
+//   dF_c  += G_{b,c-1}^T Z_{b,c},   dQ<-_b = G_{b,b-1},
+// followed per chunk by the chain rule through the diagonal-chunk logits and the UT quantities
+// (Q<-, K->, F, X = U strictLower(W K^T), U = (I + strictLower(D W W^T))^{-1} D).
+#include "internal.h"
+#include "dev_common.cuh"
+
+#include <type_traits>
+
+namespace pathattn {
+namespace {
+
+constexpr int NT = 256;
+constexpr int D = kHeadDim;
+constexpr int DS = D + 1;
+
+// D_i = dO_i . o_i (one warp per row); padded rows get 0.
+template <typename T>
+__global__ void __launch_bounds__(NT) bwd_dot_kernel(Geom g, const T* __restrict__ o,
+                                                     const T* __restrict__ dO, float* __restrict__ Dv) {
+  const long warp = ((long)blockIdx.x * NT + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const long rows = (long)g.BH * g.Lp;
+  if (warp >= rows) return;
+  const int bh = (int)(warp / g.Lp), i = (int)(warp % g.Lp);
+  float acc = 0.f;
+  if (i < g.L) {
+    const size_t off = ((size_t)bh * g.L + i) * D;
+    acc = to_f(o[off + lane]) * to_f(dO[off + lane]) + to_f(o[off + lane + 32]) * to_f(dO[off + lane + 32]);
+  }
+  acc = group_sum<32>(acc);
+  if (lane == 0) Dv[warp] = acc;
+}
+
+template <int B>
+struct BwdMainSmem {
+  static constexpr int BS = B + 1;
+  static constexpr int kZ = 0, kK = kZ + B * DS, kV = kK + B * DS, kF = kV + B * DS;
+  static constexpr int kdO = kF + D * DS, kG = kdO + B * DS, kGn = kG + B * DS;
+  static constexpr int kP = kGn + B * DS, kdS = kP + B * BS, kLse = kdS + B * BS, kDv = kLse + B;
+  static constexpr int total = kDv + B;
+  static constexpr size_t bytes = (size_t)total * 4;
+};
+
+// Persistent CTAs; tile n (heaviest first) is query chunk b = nc-1 - n/BH of head n%BH.
+template <typename T, int B>
+__global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
+    Geom g, const T* __restrict__ v, const float* __restrict__ lse, const T* __restrict__ dO,
+    const float* __restrict__ Dv, const float* __restrict__ ql, const float* __restrict__ kr,
+    const float* __restrict__ f, float* __restrict__ dql, float* __restrict__ dkr,
+    float* __restrict__ dvacc, float* __restrict__ dfacc, float* __restrict__ zs) {
+  extern __shared__ float sm[];
+  using S = BwdMainSmem<B>;
+  constexpr int BS = S::BS;
+  float* sZ = sm + S::kZ;
+  float* sK = sm + S::kK;
+  float* sV = sm + S::kV;
+  float* sF = sm + S::kF;
+  float* sdO = sm + S::kdO;
+  float* sG = sm + S::kG;
+  float* sGn = sm + S::kGn;
+  float* sP = sm + S::kP;
+  float* sdS = sm + S::kdS;
+  float* sLse = sm + S::kLse;
+  float* sDv = sm + S::kDv;
+
+  const int tid = threadIdx.x;
+  float* myz = zs + (size_t)blockIdx.x * g.Lp * D;
+  const long ntiles = (long)g.BH * g.nc;
+  const float scl2 = g.scale * kLog2e;
+
+  for (long n = blockIdx.x; n < ntiles; n += gridDim.x) {
+    const int b = g.nc - 1 - (int)(n / g.BH);
+    const int bh = (int)(n % g.BH);
+    const size_t brow = (size_t)bh * g.Lp + (size_t)b * B;
+    if (b == 0) {
+      for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = 0.f;
+      continue;
+    }
+    // ---- pass 1: Z_{b,c} for c = b-1 .. 0, stored in this CTA's scratch slab ----
+    for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = ql[brow * D + idx];
+    __syncthreads();
+    for (int c = b - 1; c >= 0; --c) {
+      for (int idx = tid; idx < B * D; idx += NT) myz[(size_t)c * B * D + idx] = sZ[(idx / D) * DS + idx % D];
+      if (c == 0) break;
+      const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
+      for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
+      __syncthreads();
+      for (int idx = tid; idx < B * D; idx += NT) {
+        const int i = idx / D, nn = idx % D;
+        float a = 0.f;
+        for (int kk = 0; kk < D; ++kk) a += sZ[i * DS + kk] * sF[nn * DS + kk];
+        sGn[i * DS + nn] = a;
+      }
+      __syncthreads();
+      for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = sGn[(idx / D) * DS + idx % D];
+      __syncthreads();
+    }
+    // ---- pass 2: ascending adjoint scan ----
+    for (int idx = tid; idx < B * D; idx += NT) {
+      const int i = idx / D, cc = idx % D, gi = b * B + i;
+      sdO[i * DS + cc] = gi < g.L ? to_f(dO[((size_t)bh * g.L + gi) * D + cc]) : 0.f;
+      sG[i * DS + cc] = 0.f;
+    }
+    for (int i = tid; i < B; i += NT) {
+      const int gi = b * B + i;
+      sLse[i] = gi < g.L ? lse[(size_t)bh * g.L + gi] * kLog2e : INFINITY;  // padded rows: P = 0
+      sDv[i] = Dv[brow + i];
+    }
+    __syncthreads();  // also orders pass-1 scratch writes before the reads below
+    for (int c = 0; c < b; ++c) {
+      const size_t crow = (size_t)bh * g.Lp + (size_t)c * B;
+      const size_t vrow = (size_t)bh * g.L + (size_t)c * B;
+      for (int idx = tid; idx < B * D; idx += NT) {
+        const int r = idx / D, cc = idx % D;
+        sZ[r * DS + cc] = myz[(size_t)c * B * D + idx];
+        sK[r * DS + cc] = kr[crow * D + idx];
+        sV[r * DS + cc] = to_f(v[vrow * D + idx]);
+      }
+      const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
+      for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
+      __syncthreads();
+      // P and dS
+      for (int idx = tid; idx < B * B; idx += NT) {
+        const int i = idx / B, j = idx % B;
+        float s = 0.f, dp = 0.f;
+        for (int kk = 0; kk < D; ++kk) {
+          s += sZ[i * DS + kk] * sK[j * DS + kk];
+          dp += sdO[i * DS + kk] * sV[j * DS + kk];
+        }
+        const float p = fast_exp2(s * scl2 - sLse[i]);
+        sP[i * BS + j] = p;
+        sdS[i * BS + j] = p * (dp - sDv[i]);
+      }
+      __syncthreads();
+      // dV_c += P^T dO ; dK->_c += scale dS^T Z ; G_new = scale dS K + G F_c
+      for (int idx = tid; idx < B * D; idx += NT) {
+        const int j = idx / D, cc = idx % D;
+        float a = 0.f, bk = 0.f;
+        for (int i = 0; i < B; ++i) {
+          a += sP[i * BS + j] * sdO[i * DS + cc];
+          bk += sdS[i * BS + j] * sZ[i * DS + cc];
+        }
+        atomicAdd(dvacc + (crow + j) * D + cc, a);
+        atomicAdd(dkr + (crow + j) * D + cc, g.scale * bk);
+      }
+      for (int idx = tid; idx < B * D; idx += NT) {
+        const int i = idx / D, nn = idx % D;
+        float a = 0.f;
+        for (int j = 0; j < B; ++j) a += sdS[i * BS + j] * sK[j * DS + nn];
+        a *= g.scale;
+        if (c > 0)
+          for (int kk = 0; kk < D; ++kk) a += sG[i * DS + kk] * sF[kk * DS + nn];
+        sGn[i * DS + nn] = a;
+      }
+      if (c > 0) {  // dF_c += G_{b,c-1}^T Z_{b,c}
+        float* dfc = dfacc + ((size_t)bh * g.nc + c) * D * D;
+        for (int idx = tid; idx < D * D; idx += NT) {
+          const int nn = idx / D, cc = idx % D;
+          float a = 0.f;
+          for (int i = 0; i < B; ++i) a += sG[i * DS + nn] * sZ[i * DS + cc];
+          atomicAdd(dfc + idx, a);
+        }
+      }
+      __syncthreads();
+      float* t = sG; sG = sGn; sGn = t;
+    }
+    for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = sG[(idx / D) * DS + idx % D];
+    __syncthreads();
+  }
+}
+
+template <int B>
+struct PrepBwdSmem {
+  static constexpr int BS = B + 1;
+  static constexpr int nBD = 11, nBB = 11;
+  static constexpr int kBD = 0, kBB = kBD + nBD * B * DS, kdF = kBB + nBB * B * BS;
+  static constexpr int kVec = kdF + D * DS;
+  static constexpr int total = kVec + 4 * B;
+  static constexpr size_t bytes = (size_t)total * 4;
+};
+
+// One CTA per (chunk c, head bh): diagonal-chunk attention backward and the chain rule through
+// Q<- = Q - lower(QW^T) U W, K-> = K - X^T W, F = I - W^T U^T W, X = U strictLower(W K^T),
+// S_d = lower(QK^T) - lower(QW^T) X, U = Y D with Y = (I + strictLower(D W W^T))^{-1}.
+template <typename T, int B>
+__global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
+    Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ lse,
+    const T* __restrict__ dO, const float* __restrict__ Dv, const float* __restrict__ dql,
+    const float* __restrict__ dkr, const float* __restrict__ dvacc, const float* __restrict__ dfacc,
+    T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, T* __restrict__ dw,
+    float* __restrict__ dbeta) {
+  extern __shared__ float sm[];
+  using S = PrepBwdSmem<B>;
+  constexpr int BS = S::BS;
+  float* bd = sm + S::kBD;
+  float* sW = bd + 0 * B * DS;
+  float* sQ = bd + 1 * B * DS;
+  float* sK = bd + 2 * B * DS;
+  float* sV = bd + 3 * B * DS;   // later E3 = M1^T dQ<- + W dF^T
+  float* sdO = bd + 4 * B * DS;
+  float* sdQl = bd + 5 * B * DS;
+  float* sdKr = bd + 6 * B * DS;
+  float* sgQ = bd + 7 * B * DS;
+  float* sgK = bd + 8 * B * DS;
+  float* sgW = bd + 9 * B * DS;
+  float* sY1 = bd + 10 * B * DS;  // U W
+  float* bb = sm + S::kBB;
+  float* sY = bb + 0 * B * BS;    // T^{-1}
+  float* sU = bb + 1 * B * BS;
+  float* sM1 = bb + 2 * B * BS;
+  float* sN2 = bb + 3 * B * BS;
+  float* sX = bb + 4 * B * BS;
+  float* sG = bb + 5 * B * BS;
+  float* sdS = bb + 6 * B * BS;
+  float* sgU = bb + 7 * B * BS;
+  float* sgX = bb + 8 * B * BS;   // later gN = strictLower(gT)
+  float* sT1 = bb + 9 * B * BS;   // QK^T -> P -> gN2
+  float* sT2 = bb + 10 * B * BS;  // dP -> gM1 -> gY Y^T
+  float* sdF = sm + S::kdF;
+  float* sBeta = sm + S::kVec;
+  float* sLse = sBeta + B;
+  float* sDv = sLse + B;
+  float* sgB = sDv + B;
+
+  const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int row0 = c * B;
+  const size_t in_row = (size_t)bh * g.L;
+  const size_t ws_row = (size_t)bh * g.Lp + row0;
+  const float scl2 = g.scale * kLog2e;
+
+  // 1. loads
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D, gi = row0 + r;
+    const bool ok = gi < g.L;
+    const size_t off = (in_row + gi) * D + cc;
+    sW[r * DS + cc] = ok ? to_f(w[off]) : 0.f;
+    sQ[r * DS + cc] = ok ? to_f(q[off]) : 0.f;
+    sK[r * DS + cc] = ok ? to_f(k[off]) : 0.f;
+    sV[r * DS + cc] = ok ? to_f(v[off]) : 0.f;
+    sdO[r * DS + cc] = ok ? to_f(dO[off]) : 0.f;
+    sdQl[r * DS + cc] = dql[(ws_row + r) * D + cc];
+    sdKr[r * DS + cc] = dkr[(ws_row + r) * D + cc];
+  }
+  const float* dfc = dfacc + ((size_t)bh * g.nc + c) * D * D;
+  for (int idx = tid; idx < D * D; idx += NT) sdF[(idx / D) * DS + idx % D] = dfc[idx];
+  for (int r = tid; r < B; r += NT) {
+    const int gi = row0 + r;
+    const bool ok = gi < g.L;
+    sBeta[r] = ok ? clamp_beta(beta[in_row + gi]) : 0.f;
+    sLse[r] = ok ? lse[in_row + gi] * kLog2e : INFINITY;
+    sDv[r] = Dv[ws_row + r];
+    sgB[r] = 0.f;
+  }
+  __syncthreads();
+
+  // 2. G = strictLower(WW^T), M1 = lower(QW^T), N2 = strictLower(WK^T), QK^T, dP = dO V^T
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float gg = 0.f, m1 = 0.f, n2 = 0.f, qk = 0.f, dp = 0.f;
+    for (int kk = 0; kk < D; ++kk) {
+      const float wi = sW[i * DS + kk], wj = sW[j * DS + kk], qi = sQ[i * DS + kk], kj = sK[j * DS + kk];
+      gg += wi * wj;
+      m1 += qi * wj;
+      n2 += wi * kj;
+      qk += qi * kj;
+      dp += sdO[i * DS + kk] * sV[j * DS + kk];
+    }
+    sG[i * BS + j] = j < i ? gg : 0.f;
+    sM1[i * BS + j] = j <= i ? m1 : 0.f;
+    sN2[i * BS + j] = j < i ? n2 : 0.f;
+    sT1[i * BS + j] = qk;
+    sT2[i * BS + j] = dp;
+  }
+  __syncthreads();
+
+  // 3. Y = T^{-1} by forward substitution: Y_i = e_i - beta_i sum_{m<i} G_im Y_m ; U = Y diag(beta)
+  for (int i = 0; i < B; ++i) {
+    if (tid < B) {
+      const int cc = tid;
+      float val = 0.f;
+      if (cc <= i) {
+        float acc = 0.f;
+        for (int m = cc; m < i; ++m) acc += sG[i * BS + m] * sY[m * BS + cc];
+        val = (cc == i ? 1.f : 0.f) - sBeta[i] * acc;
+      }
+      sY[i * BS + cc] = val;
+    }
+    __syncthreads();
+  }
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    sU[i * BS + j] = sY[i * BS + j] * sBeta[j];
+  }
+  __syncthreads();
+
+  // 4. X = U N2 ; Y1 = U W
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float a = 0.f;
+    for (int m = j + 1; m <= i; ++m) a += sU[i * BS + m] * sN2[m * BS + j];
+    sX[i * BS + j] = a;
+  }
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int i = idx / D, cc = idx % D;
+    float a = 0.f;
+    for (int m = 0; m <= i; ++m) a += sU[i * BS + m] * sW[m * DS + cc];
+    sY1[i * DS + cc] = a;
+  }
+  __syncthreads();
+
+  // 5. diagonal logits, P, dS (bilinear-part gradient = scale * P (dP - D))
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float p = 0.f;
+    if (j <= i && row0 + i < g.L) {
+      float s = sT1[i * BS + j];
+      for (int m = j + 1; m <= i; ++m) s -= sM1[i * BS + m] * sX[m * BS + j];
+      p = fast_exp2(s * scl2 - sLse[i]);
+    }
+    sT1[i * BS + j] = p;
+    sdS[i * BS + j] = g.scale * p * (sT2[i * BS + j] - sDv[i]);
+  }
+  __syncthreads();
+
+  // 6. dv (final), gQ, gK, gM1 = lower(-dS X^T - dQ<- Y1^T), gX = -M1^T dS - W dK->^T
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D, gi = row0 + r;
+    float a = 0.f, gq = sdQl[r * DS + cc], gk = sdKr[r * DS + cc];
+    for (int i = 0; i < B; ++i) {
+      a += sT1[i * BS + r] * sdO[i * DS + cc];
+      gq += sdS[r * BS + i] * sK[i * DS + cc];
+      gk += sdS[i * BS + r] * sQ[i * DS + cc];
+    }
+    if (gi < g.L) dv[(in_row + gi) * D + cc] = from_f<T>(dvacc[(ws_row + r) * D + cc] + a);
+    sgQ[r * DS + cc] = gq;
+    sgK[r * DS + cc] = gk;
+  }
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, m = idx % B;
+    float gm = 0.f;
+    if (m <= i) {
+      for (int j = 0; j < B; ++j) gm -= sdS[i * BS + j] * sX[m * BS + j];
+      for (int cc = 0; cc < D; ++cc) gm -= sdQl[i * DS + cc] * sY1[m * DS + cc];
+    }
+    sT2[i * BS + m] = gm;
+    // gX (row i plays m, column m plays j)
+    float gx = 0.f;
+    for (int r = 0; r < B; ++r) gx -= sM1[r * BS + i] * sdS[r * BS + m];
+    for (int cc = 0; cc < D; ++cc) gx -= sW[i * DS + cc] * sdKr[m * DS + cc];
+    sgX[i * BS + m] = gx;
+  }
+  __syncthreads();
+
+  // 7a. E3 = M1^T dQ<- + W dF^T  (into sV)
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int m = idx / D, cc = idx % D;
+    float a = 0.f;
+    for (int i = m; i < B; ++i) a += sM1[i * BS + m] * sdQl[i * DS + cc];
+    for (int n = 0; n < D; ++n) a += sW[m * DS + n] * sdF[cc * DS + n];
+    sV[m * DS + cc] = a;
+  }
+  __syncthreads();
+
+  // 7b. gU = lower(-E3 W^T + gX N2^T); gW = -U^T E3 - X dK-> - Y1 dF + gM1^T Q; gQ += gM1 W
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float a = 0.f;
+    if (j <= i) {
+      for (int cc = 0; cc < D; ++cc) a -= sV[i * DS + cc] * sW[j * DS + cc];
+      for (int m = 0; m < B; ++m) a += sgX[i * BS + m] * sN2[j * BS + m];
+    }
+    sgU[i * BS + j] = a;
+  }
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D;
+    float a = 0.f, gq = 0.f;
+    for (int i = r; i < B; ++i) a -= sU[i * BS + r] * sV[i * DS + cc];
+    for (int m = 0; m < B; ++m) {
+      a -= sX[r * BS + m] * sdKr[m * DS + cc];
+      a += sT2[m * BS + r] * sQ[m * DS + cc];
+      gq += sT2[r * BS + m] * sW[m * DS + cc];
+    }
+    for (int n = 0; n < D; ++n) a -= sY1[r * DS + n] * sdF[n * DS + cc];
+    sgW[r * DS + cc] = a;
+    sgQ[r * DS + cc] += gq;
+  }
+  __syncthreads();
+
+  // 8. gN2 = strictLower(U^T gX) into sT1; dbeta_j += sum_i gU_ij Y_ij
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float a = 0.f;
+    if (j < i)
+      for (int m = i; m < B; ++m) a += sU[m * BS + i] * sgX[m * BS + j];
+    sT1[i * BS + j] = a;
+  }
+  if (tid < B) {
+    float a = 0.f;
+    for (int i = tid; i < B; ++i) a += sgU[i * BS + tid] * sY[i * BS + tid];
+    sgB[tid] += a;
+  }
+  __syncthreads();
+
+  // 9. gW += gN2 K ; gK += gN2^T W ; A1 = gY Y^T with gY = gU diag(beta) (into sT2)
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D;
+    float a = 0.f, b2 = 0.f;
+    for (int m = 0; m < B; ++m) {
+      a += sT1[r * BS + m] * sK[m * DS + cc];
+      b2 += sT1[m * BS + r] * sW[m * DS + cc];
+    }
+    sgW[r * DS + cc] += a;
+    sgK[r * DS + cc] += b2;
+  }
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float a = 0.f;
+    for (int kk = 0; kk < B; ++kk) a += sgU[i * BS + kk] * sBeta[kk] * sY[j * BS + kk];
+    sT2[i * BS + j] = a;
+  }
+  __syncthreads();
+
+  // 10. gN = strictLower(-Y^T A1) into sgX
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float a = 0.f;
+    if (j < i)
+      for (int kk = 0; kk < B; ++kk) a -= sY[kk * BS + i] * sT2[kk * BS + j];
+    sgX[i * BS + j] = a;
+  }
+  __syncthreads();
+
+  // 11. N = strictLower(D G): dbeta_i += sum_{j<i} gN_ij G_ij ; gG = D gN ; gW += (gG + gG^T) W
+  if (tid < B) {
+    float a = 0.f;
+    for (int j = 0; j < tid; ++j) a += sgX[tid * BS + j] * sG[tid * BS + j];
+    sgB[tid] += a;
+  }
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D;
+    float a = 0.f;
+    for (int m = 0; m < B; ++m)
+      a += (sBeta[r] * sgX[r * BS + m] + sBeta[m] * sgX[m * BS + r]) * sW[m * DS + cc];
+    sgW[r * DS + cc] += a;
+  }
+  __syncthreads();
+
+  // 12. outputs
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D, gi = row0 + r;
+    if (gi < g.L) {
+      const size_t off = (in_row + gi) * D + cc;
+      dq[off] = from_f<T>(sgQ[r * DS + cc]);
+      dk[off] = from_f<T>(sgK[r * DS + cc]);
+      dw[off] = from_f<T>(sgW[r * DS + cc]);
+    }
+  }
+  for (int r = tid; r < B; r += NT)
+    if (row0 + r < g.L) dbeta[in_row + row0 + r] = sgB[r];
+}
+
+template <typename T, int B>
+cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                  const float* beta, const void* o, const float* lse, const void* dO, void* dq,
+                  void* dk, void* dv, void* dw, float* dbeta, char* ws, const BwdWs& lay,
+                  cudaStream_t st) {
+  cudaError_t e;
+  const size_t rows = (size_t)g.BH * g.Lp;
+  if ((e = cudaMemsetAsync(ws + lay.dkr, 0, rows * D * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(ws + lay.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(ws + lay.df, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
+  const long nwarps = (long)rows;
+  bwd_dot_kernel<T><<<(unsigned)((nwarps * 32 + NT - 1) / NT), NT, 0, st>>>(
+      g, (const T*)o, (const T*)dO, (float*)(ws + lay.Dv));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_prep_simt(std::is_same<T, __nv_bfloat16>::value, g, q, k, v, w, beta, nullptr, ws,
+                            lay.fw, false, st)) != cudaSuccess)
+    return e;
+  {
+    auto kern = bwd_main_simt_kernel<T, B>;
+    const size_t smem = BwdMainSmem<B>::bytes;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    kern<<<lay.nctas, NT, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
+                                      (const float*)(ws + lay.fw.ql), (const float*)(ws + lay.fw.kr),
+                                      (const float*)(ws + lay.fw.f), (float*)(ws + lay.dql),
+                                      (float*)(ws + lay.dkr), (float*)(ws + lay.dv), (float*)(ws + lay.df),
+                                      (float*)(ws + lay.zs));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    auto kern = prep_bwd_simt_kernel<T, B>;
+    const size_t smem = PrepBwdSmem<B>::bytes;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    kern<<<dim3(g.nc, g.BH), NT, smem, st>>>(
+        g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, lse, (const T*)dO,
+        (const float*)(ws + lay.Dv), (const float*)(ws + lay.dql), (const float*)(ws + lay.dkr),
+        (const float*)(ws + lay.dv), (const float*)(ws + lay.df), (T*)dq, (T*)dk, (T*)dv, (T*)dw, dbeta);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
+                            const void* v, const void* w, const float* beta, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            void* dw, float* dbeta, char* ws, const BwdWs& lay, cudaStream_t st) {
+  if (g.B != 32) return cudaErrorInvalidValue;
+  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, st)
+                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, st);
+}
+
+}  // namespace pathattn

@@ -1,0 +1,402 @@
+// SIMT (fp32 CUDA-core) forward of PaTH attention: per-chunk UT preparation and the
+// right-to-left chunk scan.  Used for the fp32 mode and as the correctness path.
+//
+// Method: PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6 (UT representation,
+// full-matrix logits) and §2.7 (boundary-adjusted Q/K, chunk transforms, right-to-left scan).
+#include "internal.h"
+#include "dev_common.cuh"
+
+namespace pathattn {
+namespace {
+
+constexpr int NT = 256;
+constexpr int D = kHeadDim;
+constexpr int DS = D + 1;  // padded smem row stride of [rows][64] matrices
+
+template <int B>
+struct PrepSmem {
+  static constexpr int BS = B + 1;
+  static constexpr int kW = 0, kQ = kW + B * DS, kK = kQ + B * DS, kV = kK + B * DS;
+  static constexpr int kU = kV + B * DS, kM1 = kU + B * BS, kX = kM1 + B * BS, kT = kX + B * BS;
+  static constexpr int kBeta = kT + B * BS, kLf = kBeta + B, kA = kLf + B;
+  static constexpr int total = kA + B;
+  static constexpr size_t bytes = (size_t)total * 4;
+};
+
+// One CTA per (chunk c, head bh).  Writes Q<-, K->, F, the diagonal-chunk softmax state and
+// the chunk-local forget-gate sums.  Rows beyond L are padding with q=k=v=w=0, beta=0
+// (H = I), log f = 0.
+template <typename T, int B>
+__global__ void __launch_bounds__(NT) prep_simt_kernel(
+    Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ logf,
+    float* __restrict__ ql, float* __restrict__ kr, float* __restrict__ f, float* __restrict__ dm,
+    float* __restrict__ dl, float* __restrict__ dacc, float* __restrict__ fa,
+    float* __restrict__ fr, float* __restrict__ ft, int with_diag) {
+  extern __shared__ float sm[];
+  using S = PrepSmem<B>;
+  constexpr int BS = S::BS;
+  float* sW = sm + S::kW;
+  float* sQ = sm + S::kQ;
+  float* sK = sm + S::kK;
+  float* sV = sm + S::kV;
+  float* sU = sm + S::kU;
+  float* sM1 = sm + S::kM1;
+  float* sX = sm + S::kX;
+  float* sT = sm + S::kT;
+  float* sBeta = sm + S::kBeta;
+  float* sLf = sm + S::kLf;
+  float* sA = sm + S::kA;
+
+  const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int row0 = c * B;
+  const size_t in_row = (size_t)bh * g.L;
+  const size_t ws_row = (size_t)bh * g.Lp + row0;
+
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int r = idx / D, cc = idx % D, gi = row0 + r;
+    const bool ok = gi < g.L;
+    const size_t off = (in_row + gi) * D + cc;
+    sW[r * DS + cc] = ok ? to_f(w[off]) : 0.f;
+    sQ[r * DS + cc] = ok ? to_f(q[off]) : 0.f;
+    sK[r * DS + cc] = ok ? to_f(k[off]) : 0.f;
+    if (with_diag) sV[r * DS + cc] = ok ? to_f(v[off]) : 0.f;
+  }
+  for (int r = tid; r < B; r += NT) {
+    const int gi = row0 + r;
+    const bool ok = gi < g.L;
+    sBeta[r] = ok ? clamp_beta(beta[in_row + gi]) : 0.f;
+    sLf[r] = (ok && logf) ? logf[in_row + gi] : 0.f;
+  }
+  __syncthreads();
+
+  // G = strictLower(W W^T) into sT; chunk-local inclusive forget prefix into sA.
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    if (j < i)
+      for (int kk = 0; kk < D; ++kk) acc += sW[i * DS + kk] * sW[j * DS + kk];
+    sT[i * BS + j] = acc;
+  }
+  if (tid == 0) {
+    float a = 0.f;
+    for (int r = 0; r < B; ++r) { a += sLf[r]; sA[r] = a; }
+  }
+  __syncthreads();
+
+  // U = (I + strictLower(D G))^{-1} D by forward substitution:
+  // row i of U = beta_i (e_i - sum_{m<i} G_im U_m).  U is lower triangular.
+  for (int i = 0; i < B; ++i) {
+    if (tid < B) {
+      const int cc = tid;
+      float val = 0.f;
+      if (cc <= i) {
+        float acc = (cc == i) ? 1.f : 0.f;
+        for (int m = cc; m < i; ++m) acc -= sT[i * BS + m] * sU[m * BS + cc];
+        val = sBeta[i] * acc;
+      }
+      sU[i * BS + cc] = val;
+    }
+    __syncthreads();
+  }
+
+  // M1 = lower(Q W^T)
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    if (j <= i)
+      for (int kk = 0; kk < D; ++kk) acc += sQ[i * DS + kk] * sW[j * DS + kk];
+    sM1[i * BS + j] = acc;
+  }
+  __syncthreads();
+  // A = M1 U (lower) into sT
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    if (j <= i)
+      for (int m = j; m <= i; ++m) acc += sM1[i * BS + m] * sU[m * BS + j];
+    sT[i * BS + j] = acc;
+  }
+  __syncthreads();
+  // Q<- = Q - A W   (query moved to the chunk's left edge)
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int i = idx / D, cc = idx % D;
+    float acc = sQ[i * DS + cc];
+    for (int m = 0; m <= i; ++m) acc -= sT[i * BS + m] * sW[m * DS + cc];
+    ql[(ws_row + i) * D + cc] = acc;
+  }
+  __syncthreads();
+  // N2 = strictLower(W K^T) into sT
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    if (j < i)
+      for (int kk = 0; kk < D; ++kk) acc += sW[i * DS + kk] * sK[j * DS + kk];
+    sT[i * BS + j] = acc;
+  }
+  __syncthreads();
+  // X = U N2 : X_ij = sum_{j<m<=i} U_im N2_mj
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    for (int m = j + 1; m <= i; ++m) acc += sU[i * BS + m] * sT[m * BS + j];
+    sX[i * BS + j] = acc;
+  }
+  __syncthreads();
+  // K-> = K - X^T W   (key moved to the chunk's right edge)
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int j = idx / D, cc = idx % D;
+    float acc = sK[j * DS + cc];
+    for (int m = j + 1; m < B; ++m) acc -= sX[m * BS + j] * sW[m * DS + cc];
+    kr[(ws_row + j) * D + cc] = acc;
+  }
+  // S_d = lower(Q K^T) - M1 X  into sT (diagonal-chunk logits before scale/bias)
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    float acc = 0.f;
+    if (j <= i) {
+      for (int kk = 0; kk < D; ++kk) acc += sQ[i * DS + kk] * sK[j * DS + kk];
+      for (int m = j + 1; m <= i; ++m) acc -= sM1[i * BS + m] * sX[m * BS + j];
+    }
+    sT[i * BS + j] = acc;
+  }
+  __syncthreads();
+
+  // Y = U^T W into sQ (Q is no longer needed)
+  for (int idx = tid; idx < B * D; idx += NT) {
+    const int m = idx / D, cc = idx % D;
+    float acc = 0.f;
+    for (int i = m; i < B; ++i) acc += sU[i * BS + m] * sW[i * DS + cc];
+    sQ[m * DS + cc] = acc;
+  }
+
+  if (with_diag) {
+    // Diagonal-chunk attention partial state per row (log2 domain).
+    constexpr int NSUB = NT / B;
+    const int r = tid / NSUB, sub = tid % NSUB;
+    const float scl = g.scale * kLog2e;
+    float mx = -INFINITY;
+    for (int j = sub; j < B; j += NSUB) {
+      float s = -INFINITY;
+      if (j <= r && row0 + j < g.L) s = sT[r * BS + j] * scl + (sA[r] - sA[j]) * kLog2e;
+      sT[r * BS + j] = s;
+      mx = fmaxf(mx, s);
+    }
+    mx = group_max<NSUB>(mx);
+    float l = 0.f;
+    for (int j = sub; j < B; j += NSUB) {
+      const float s = sT[r * BS + j];
+      const float p = (s == -INFINITY) ? 0.f : fast_exp2(s - mx);
+      sT[r * BS + j] = p;
+      l += p;
+    }
+    l = group_sum<NSUB>(l);
+    __syncwarp();
+    for (int cc = sub; cc < D; cc += NSUB) {
+      float acc = 0.f;
+      for (int j = 0; j <= r; ++j) acc += sT[r * BS + j] * sV[j * DS + cc];
+      dacc[(ws_row + r) * D + cc] = acc;
+    }
+    if (sub == 0) {
+      dm[ws_row + r] = mx;
+      dl[ws_row + r] = l;
+    }
+  }
+  __syncthreads();
+
+  // F = I - W^T Y = I - W^T U^T W  (the chunk's transform H_first ... H_last)
+  float* fout = f + ((size_t)bh * g.nc + c) * D * D;
+  for (int idx = tid; idx < D * D; idx += NT) {
+    const int n = idx / D, cc = idx % D;
+    float acc = (n == cc) ? 1.f : 0.f;
+    for (int m = 0; m < B; ++m) acc -= sW[m * DS + n] * sQ[m * DS + cc];
+    fout[idx] = acc;
+  }
+  if (logf) {
+    const float tot = sA[B - 1];
+    for (int r = tid; r < B; r += NT) {
+      fa[ws_row + r] = sA[r];
+      fr[ws_row + r] = tot - sA[r];
+    }
+    if (tid == 0) ft[(size_t)bh * g.nc + c] = tot;
+  }
+}
+
+template <int B>
+struct MainSmem {
+  static constexpr int BS = B + 1;
+  static constexpr int kZ = 0, kZn = kZ + B * DS, kK = kZn + B * DS, kV = kK + B * DS;
+  static constexpr int kF = kV + B * DS, kP = kF + D * DS, kR = kP + B * BS;
+  static constexpr int total = kR + B;
+  static constexpr size_t bytes = (size_t)total * 4;
+};
+
+// One CTA per (query chunk b, head bh): starts from the diagonal-chunk state and scans the
+// earlier chunks right to left: S = Z K->_c^T, online softmax, O += P V_c, Z <- Z F_c^T.
+template <typename T, int B>
+__global__ void __launch_bounds__(NT) main_simt_kernel(
+    Geom g, const T* __restrict__ v, const float* __restrict__ ql, const float* __restrict__ kr,
+    const float* __restrict__ f, const float* __restrict__ dm, const float* __restrict__ dl,
+    const float* __restrict__ dacc, const float* __restrict__ fa, const float* __restrict__ fr,
+    const float* __restrict__ ft, int fox, T* __restrict__ o, float* __restrict__ lse) {
+  extern __shared__ float sm[];
+  using S = MainSmem<B>;
+  constexpr int BS = S::BS;
+  constexpr int NSUB = NT / B;
+  constexpr int OC = D / NSUB;
+  constexpr int SC = B / NSUB;
+  float* sZ = sm + S::kZ;
+  float* sZn = sm + S::kZn;
+  float* sK = sm + S::kK;
+  float* sV = sm + S::kV;
+  float* sF = sm + S::kF;
+  float* sP = sm + S::kP;
+  float* sR = sm + S::kR;
+
+  const int b = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int r = tid / NSUB, sub = tid % NSUB;
+  const size_t wrow = (size_t)bh * g.Lp + (size_t)b * B;
+  const float scl = g.scale * kLog2e;
+
+  for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = ql[wrow * D + idx];
+  float m = dm[wrow + r];
+  float l = (sub == 0) ? dl[wrow + r] : 0.f;
+  float acc[OC];
+#pragma unroll
+  for (int u = 0; u < OC; ++u) acc[u] = dacc[(wrow + r) * D + sub + NSUB * u];
+  const float arow = fox ? fa[wrow + r] : 0.f;
+  float Rsum = 0.f;
+  __syncthreads();
+
+  for (int c = b - 1; c >= 0; --c) {
+    const size_t crow = (size_t)bh * g.Lp + (size_t)c * B;
+    const size_t vrow = (size_t)bh * g.L + (size_t)c * B;  // chunk c < b is always full
+    for (int idx = tid; idx < B * D; idx += NT) {
+      const int rr = idx / D, cc = idx % D;
+      sK[rr * DS + cc] = kr[crow * D + idx];
+      sV[rr * DS + cc] = to_f(v[vrow * D + idx]);
+    }
+    const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
+    for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
+    for (int j = tid; j < B; j += NT) sR[j] = fox ? fr[crow + j] : 0.f;
+    const float Tc = fox ? ft[(size_t)bh * g.nc + c] : 0.f;
+    __syncthreads();
+
+    float s[SC];
+    float mx = -INFINITY;
+    const float rowbias = (arow + Rsum) * kLog2e;
+#pragma unroll
+    for (int u = 0; u < SC; ++u) {
+      const int j = sub + NSUB * u;
+      float dot = 0.f;
+#pragma unroll 16
+      for (int kk = 0; kk < D; ++kk) dot += sZ[r * DS + kk] * sK[j * DS + kk];
+      s[u] = dot * scl + rowbias + sR[j] * kLog2e;
+      mx = fmaxf(mx, s[u]);
+    }
+    mx = group_max<NSUB>(mx);
+    const float mnew = fmaxf(m, mx);
+    const float corr = fast_exp2(m - mnew);
+    m = mnew;
+    l *= corr;
+#pragma unroll
+    for (int u = 0; u < OC; ++u) acc[u] *= corr;
+#pragma unroll
+    for (int u = 0; u < SC; ++u) {
+      const float p = fast_exp2(s[u] - m);
+      l += p;
+      sP[r * BS + sub + NSUB * u] = p;
+    }
+    // Z' = Z F_c^T
+#pragma unroll
+    for (int u = 0; u < OC; ++u) {
+      const int n = sub + NSUB * u;
+      float dot = 0.f;
+#pragma unroll 16
+      for (int kk = 0; kk < D; ++kk) dot += sZ[r * DS + kk] * sF[n * DS + kk];
+      sZn[r * DS + n] = dot;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < OC; ++u) {
+      const int cc = sub + NSUB * u;
+      float a = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < B; ++j) a += sP[r * BS + j] * sV[j * DS + cc];
+      acc[u] += a;
+    }
+    Rsum += Tc;
+    __syncthreads();
+    float* t = sZ; sZ = sZn; sZn = t;
+  }
+
+  l = group_sum<NSUB>(l);
+  const int gi = b * B + r;
+  if (gi < g.L) {
+    const float inv = 1.f / l;
+    const size_t orow = (size_t)bh * g.L + gi;
+#pragma unroll
+    for (int u = 0; u < OC; ++u) o[orow * D + sub + NSUB * u] = from_f<T>(acc[u] * inv);
+    if (sub == 0) lse[orow] = (m + log2f(l)) * kLn2;
+  }
+}
+
+template <typename T, int B>
+cudaError_t prep_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                   const float* beta, const float* logf, char* ws, const FwdWs& lay,
+                   bool with_diag, cudaStream_t st) {
+  auto kern = prep_simt_kernel<T, B>;
+  const size_t smem = PrepSmem<B>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(g.nc, g.BH);
+  kern<<<grid, NT, smem, st>>>(g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, logf,
+                               (float*)(ws + lay.ql), (float*)(ws + lay.kr), (float*)(ws + lay.f),
+                               (float*)(ws + lay.dm), (float*)(ws + lay.dl), (float*)(ws + lay.dacc),
+                               (float*)(ws + lay.fa), (float*)(ws + lay.fr), (float*)(ws + lay.ft),
+                               with_diag ? 1 : 0);
+  return cudaGetLastError();
+}
+
+template <typename T, int B>
+cudaError_t main_t(const Geom& g, const void* v, const float* logf, char* ws, const FwdWs& lay,
+                   void* o, float* lse, cudaStream_t st) {
+  auto kern = main_simt_kernel<T, B>;
+  const size_t smem = MainSmem<B>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(g.nc, g.BH);
+  kern<<<grid, NT, smem, st>>>(g, (const T*)v, (const float*)(ws + lay.ql), (const float*)(ws + lay.kr),
+                               (const float*)(ws + lay.f), (const float*)(ws + lay.dm),
+                               (const float*)(ws + lay.dl), (const float*)(ws + lay.dacc),
+                               (const float*)(ws + lay.fa), (const float*)(ws + lay.fr),
+                               (const float*)(ws + lay.ft), logf ? 1 : 0, (T*)o, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
+                             const void* v, const void* w, const float* beta, const float* logf,
+                             char* ws, const FwdWs& lay, bool with_diag, cudaStream_t st) {
+  if (g.B == 32)
+    return is_bf16 ? prep_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
+                   : prep_t<float, 32>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
+  if (g.B == 64)
+    return is_bf16 ? prep_t<__nv_bfloat16, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
+                   : prep_t<float, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
+                             char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st) {
+  if (g.B == 32)
+    return is_bf16 ? main_t<__nv_bfloat16, 32>(g, v, logf, ws, lay, o, lse, st)
+                   : main_t<float, 32>(g, v, logf, ws, lay, o, lse, st);
+  if (g.B == 64)
+    return is_bf16 ? main_t<__nv_bfloat16, 64>(g, v, logf, ws, lay, o, lse, st)
+                   : main_t<float, 64>(g, v, logf, ws, lay, o, lse, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pathattn

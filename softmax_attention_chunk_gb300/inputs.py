@@ -68,7 +68,7 @@ def _normal_rows(seed, name, bh, rows, d, dtype, scale=1.0, mean=0.0):
 
 
 def _unit_rows(seed, name, bh, rows, d, dtype):
-    x = torch.randn(rows, d, generator=_gen(seed, name, bh), dtype=torch.float64)
+    x = torch.randn(rows, d, generator=_gen(seed, name, bh), dtype=torch.float32).double()
     x = x / x.norm(dim=-1, keepdim=True)
     return x.to(dtype)
 
@@ -84,6 +84,18 @@ def _beta_row(seed, bh, rows, near2_frac, prefix=""):
     return beta.clamp(max=BETA_MAX_BELOW_2)
 
 
+def _parallel(fn, n):
+    """Runs fn(i) for i < n on a thread pool (torch kernels release the GIL)."""
+    if n <= 8:
+        for i in range(n):
+            fn(i)
+        return
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 4)) as ex:
+        list(ex.map(fn, range(n)))
+
+
 def gen_path_inputs(batch, heads, seqlen, head_dim, dtype="bf16", seed=1000, near2_frac=0.0,
                     fox=False, with_dO=False, heads_subset=None, **_unused):
     """Inputs of the forward/backward workload.
@@ -96,32 +108,30 @@ def gen_path_inputs(batch, heads, seqlen, head_dim, dtype="bf16", seed=1000, nea
     d, L = head_dim, seqlen
     sd = 1.0 / math.sqrt(d)
     hs = _heads(batch, heads, heads_subset)
-    out = {k: [] for k in ("q", "k", "v", "w", "beta")}
-    if fox:
-        out["log_f"] = []
-    if with_dO:
-        out["dO"] = []
-    for bh in hs:
-        out["q"].append(_normal_rows(seed, "q", bh, L, d, tdt, sd))
-        out["k"].append(_normal_rows(seed, "k", bh, L, d, tdt, sd))
-        out["v"].append(_normal_rows(seed, "v", bh, L, d, tdt, sd))
-        out["w"].append(_unit_rows(seed, "w", bh, L, d, tdt))
-        out["beta"].append(_beta_row(seed, bh, L, near2_frac))
+    n = len(hs)
+    res = {key: torch.empty(n, L, d, dtype=tdt) for key in ("q", "k", "v", "w")}
+    res["beta"] = torch.empty(n, L, dtype=torch.float32)
+    res["log_f"] = torch.empty(n, L, dtype=torch.float32) if fox else None
+    res["dO"] = torch.empty(n, L, d, dtype=tdt) if with_dO else None
+
+    def one(idx):
+        bh = hs[idx]
+        res["q"][idx] = _normal_rows(seed, "q", bh, L, d, tdt, sd)
+        res["k"][idx] = _normal_rows(seed, "k", bh, L, d, tdt, sd)
+        res["v"][idx] = _normal_rows(seed, "v", bh, L, d, tdt, sd)
+        res["w"][idx] = _unit_rows(seed, "w", bh, L, d, tdt)
+        res["beta"][idx] = _beta_row(seed, bh, L, near2_frac)
         if fox:
             xf = torch.randn(L, generator=_gen(seed, "xf", bh), dtype=torch.float64) + 2.0
-            out["log_f"].append(torch.log(torch.sigmoid(xf)).to(torch.float32))
+            res["log_f"][idx] = torch.log(torch.sigmoid(xf)).to(torch.float32)
         if with_dO:
-            out["dO"].append(_normal_rows(seed, "dO", bh, L, d, tdt, 1.0))
-    res = {}
-    for key, lst in out.items():
-        t = torch.stack(lst, 0)
-        if heads_subset is None:
-            t = t.reshape(batch, heads, *t.shape[1:])
-        res[key] = t
-    if not fox:
-        res["log_f"] = None
-    if not with_dO:
-        res["dO"] = None
+            res["dO"][idx] = _normal_rows(seed, "dO", bh, L, d, tdt, 1.0)
+
+    _parallel(one, n)
+    if heads_subset is None:
+        for key, t in list(res.items()):
+            if t is not None:
+                res[key] = t.reshape(batch, heads, *t.shape[1:])
     return res
 
 
@@ -139,19 +149,25 @@ def gen_decode_inputs(batch, heads, head_dim, t0, steps, dtype="bf16", seed=1004
     cap = t0 + steps if capacity is None else capacity
     sd = 1.0 / math.sqrt(d)
     hs = _heads(batch, heads, heads_subset)
-    kc = torch.zeros(len(hs), cap, d, dtype=tdt)
-    vc = torch.zeros(len(hs), cap, d, dtype=tdt)
-    sq, sk, sv, sw, sb = [], [], [], [], []
-    for n, bh in enumerate(hs):
+    n = len(hs)
+    kc = torch.zeros(n, cap, d, dtype=tdt)
+    vc = torch.zeros(n, cap, d, dtype=tdt)
+    sq, sk, sv, sw = (torch.empty(n, steps, d, dtype=tdt) for _ in range(4))
+    sb = torch.empty(n, steps, dtype=torch.float32)
+
+    def one(idx):
+        bh = hs[idx]
         if t0 > 0:
-            kc[n, :t0] = _normal_rows(seed, "kc", bh, t0, d, tdt, sd)
-            vc[n, :t0] = _normal_rows(seed, "vc", bh, t0, d, tdt, sd)
-        sq.append(_normal_rows(seed, "sq", bh, steps, d, tdt, sd))
-        sk.append(_normal_rows(seed, "sk", bh, steps, d, tdt, sd))
-        sv.append(_normal_rows(seed, "sv", bh, steps, d, tdt, sd))
-        sw.append(_unit_rows(seed, "sw", bh, steps, d, tdt))
-        sb.append(_beta_row(seed, bh, steps, 0.0, prefix="s"))
-    step = lambda lst: torch.stack(lst, 1)  # [steps, n, ...]
+            kc[idx, :t0] = _normal_rows(seed, "kc", bh, t0, d, tdt, sd)
+            vc[idx, :t0] = _normal_rows(seed, "vc", bh, t0, d, tdt, sd)
+        sq[idx] = _normal_rows(seed, "sq", bh, steps, d, tdt, sd)
+        sk[idx] = _normal_rows(seed, "sk", bh, steps, d, tdt, sd)
+        sv[idx] = _normal_rows(seed, "sv", bh, steps, d, tdt, sd)
+        sw[idx] = _unit_rows(seed, "sw", bh, steps, d, tdt)
+        sb[idx] = _beta_row(seed, bh, steps, 0.0, prefix="s")
+
+    _parallel(one, n)
+    step = lambda x: x.transpose(0, 1).contiguous()  # [steps, n, ...]
     res = dict(k_cache=kc, v_cache=vc, q=step(sq), k=step(sk), v=step(sv), w=step(sw), beta=step(sb))
     if heads_subset is None:
         res["k_cache"] = kc.reshape(batch, heads, cap, d)

@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 CPU oracle, element by
+element, on the same seeded inputs.  Sizes span several chunks and ragged tails.
+
+Tolerances (stated by the workload definitions): max abs error <= 1e-4 in the fp32 mode and
+<= 2e-2 on bf16 outputs.  Gradients use max abs <= tol * max(1, max |ref|) per tensor.  The
+bf16 cases additionally require relative Frobenius error <= 2e-2 so that an error of the order of
+the (small) outputs themselves cannot pass.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from softmax_attention_chunk_gb300.inputs import gen_decode_inputs, gen_path_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def flat(x):
+    return None if x is None else x.reshape(-1, *x.shape[2:])
+
+
+def np64(x):
+    return x.detach().double().cpu().numpy()
+
+
+def check(got, ref, tol, name, rel=None):
+    got = np64(got).reshape(ref.shape)
+    err = np.abs(got - ref).max()
+    assert err <= tol, f"{name}: max abs err {err:.3e} > {tol:.1e}"
+    if rel is not None:
+        r = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert r <= rel, f"{name}: rel fro err {r:.3e} > {rel:.1e}"
+    return err
+
+
+def run_fwd(inp, scale, chunk=0):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=scale, chunk=chunk)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_fwd(inp, scale):
+    return orc.fwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]),
+                   flat(inp["log_f"]), scale)
+
+
+@pytest.mark.parametrize("chunk", [0, 32, 64])
+def test_fwd_pr1_tiny_fp32(cuda_lib, chunk):
+    """Batch 1, 2 heads, L=128, d=64, fp32: max abs <= 1e-4."""
+    from softmax_attention_chunk_gb300.inputs import CONFIGS
+
+    cfg = CONFIGS["pr1_tiny_fwd"]
+    inp = gen_path_inputs(**cfg)
+    o, lse = run_fwd(inp, cfg["scale"], chunk)
+    o_ref, lse_ref = oracle_fwd(inp, cfg["scale"])
+    check(o, o_ref, 1e-4, "o")
+    check(lse, lse_ref, 1e-4, "lse")
+
+
+@pytest.mark.parametrize("L", [1, 2, 31, 33, 64, 65, 130, 257])
+@pytest.mark.parametrize("fox", [False, True])
+def test_fwd_ragged_fp32(cuda_lib, L, fox):
+    inp = gen_path_inputs(2, 2, L, 64, "fp32", seed=100 + L, fox=fox)
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(o, o_ref, 1e-4, "o")
+    check(lse, lse_ref, 1e-4, "lse")
+
+
+def test_fwd_large_logits_fp32(cuda_lib):
+    """scale = 16 gives logits of std ~2: exercises the online-softmax rescaling."""
+    inp = gen_path_inputs(1, 3, 300, 64, "fp32", seed=5, near2_frac=0.2)
+    o, lse = run_fwd(inp, 16.0)
+    o_ref, lse_ref = oracle_fwd(inp, 16.0)
+    check(o, o_ref, 1e-4, "o")
+    check(lse, lse_ref, 1e-4, "lse")
+
+
+def test_fwd_beta_edges_fp32(cuda_lib):
+    """beta = 0 (identity), exactly 2 (reflection), and out-of-range values (clamped to [0, 2])."""
+    inp = gen_path_inputs(1, 2, 150, 64, "fp32", seed=6)
+    b = inp["beta"].clone()
+    b[..., 0::5] = 2.0
+    b[..., 1::5] = 0.0
+    b[..., 2::7] = 2.5
+    b[..., 3::11] = -0.5
+    inp["beta"] = b
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(o, o_ref, 1e-4, "o")
+    check(lse, lse_ref, 1e-4, "lse")
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_fwd_bf16_near_reflection(cuda_lib, fox):
+    inp = gen_path_inputs(2, 2, 700, 64, "bf16", seed=8, near2_frac=0.05, fox=fox)
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(o, o_ref, 2e-2, "o", rel=2e-2)
+    check(lse, lse_ref, 2e-2, "lse")
+
+
+def run_bwd(inp, scale):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], None, scale=scale)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=scale)
+    torch.cuda.synchronize()
+    return g
+
+
+def check_grads(inp, g, scale, tol, rel=None):
+    ref = orc.bwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]), None,
+                  scale, flat(inp["dO"]))
+    for key in ("dq", "dk", "dv", "dw", "dbeta"):
+        r = ref[key]
+        check(flat(g[key]), r, tol * max(1.0, np.abs(r).max()), key, rel=rel)
+
+
+@pytest.mark.parametrize("L", [1, 31, 32, 33, 100, 129])
+def test_bwd_fp32(cuda_lib, L):
+    inp = gen_path_inputs(1, 2, L, 64, "fp32", seed=200 + L, with_dO=True, near2_frac=0.1)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 1e-4)
+
+
+def test_bwd_fp32_scaled(cuda_lib):
+    inp = gen_path_inputs(1, 2, 160, 64, "fp32", seed=31, with_dO=True)
+    g = run_bwd(inp, 4.0)
+    check_grads(inp, g, 4.0, 1e-4)
+
+
+def test_bwd_bf16(cuda_lib):
+    inp = gen_path_inputs(2, 2, 300, 64, "bf16", seed=32, with_dO=True, near2_frac=0.05)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
+
+
+def test_bwd_rejects_forget_gate(cuda_lib):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(1, 1, 64, 64, "fp32", seed=3, with_dO=True, fox=True)
+    t = {k: v.to(DEV) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"])
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], log_f=t["log_f"])
+
+
+@pytest.mark.parametrize("dtype,t0,steps,tol", [("fp32", 0, 40, 1e-4), ("fp32", 3000, 5, 1e-4),
+                                                ("bf16", 0, 30, 2e-2), ("bf16", 5000, 6, 2e-2)])
+def test_decode_steps(cuda_lib, dtype, t0, steps, tol):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    B, H, d = 2, 2, 64
+    di = gen_decode_inputs(B, H, d, t0=t0, steps=steps, dtype=dtype, seed=40 + t0)
+    kc, vc = di["k_cache"].to(DEV), di["v_cache"].to(DEV)
+    kref = np64(di["k_cache"]).reshape(B * H, -1, d).copy()
+    vref = np64(di["v_cache"]).reshape(B * H, -1, d).copy()
+    for s in range(steps):
+        args = [di[n][s].to(DEV) for n in ("q", "k", "v", "w", "beta")]
+        o_t = pa.decode_step(kc, vc, t0 + s, *args, scale=1.0)
+        torch.cuda.synchronize()
+        o_r = orc.decode_step(kref, vref, t0 + s, *[flat(di[n][s]) for n in ("q", "k", "v", "w", "beta")], 1.0)
+        check(o_t.reshape(B * H, d), o_r, tol, f"o_t step {s}", rel=2e-2 if dtype == "bf16" else None)
+    n = t0 + steps
+    check(kc.reshape(B * H, -1, d)[:, :n], kref[:, :n], tol, "rewritten keys")
+    check(vc.reshape(B * H, -1, d)[:, :n], vref[:, :n], 0.0, "values")
+
+
+def test_decode_matches_forward_rows(cuda_lib):
+    """Decoding a sequence token by token from an empty cache gives the forward's rows."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    L = 70
+    inp = gen_path_inputs(1, 2, L, 64, "fp32", seed=77)
+    o_f, _ = run_fwd(inp, 1.0)
+    kc = torch.zeros(1, 2, L, 64, device=DEV)
+    vc = torch.zeros_like(kc)
+    rows = []
+    for t in range(L):
+        sl = lambda x: x[:, :, t].contiguous().to(DEV)
+        rows.append(pa.decode_step(kc, vc, t, sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["w"]),
+                                   sl(inp["beta"]), scale=1.0))
+    o_d = torch.stack(rows, 2)
+    assert (o_d - o_f).abs().max().item() <= 1e-4
