@@ -54,7 +54,7 @@ _lib.path_attn_bwd.argtypes = [_DP] + [_vp] * 15 + [_vp, _sz, _vp]
 _lib.path_decode_workspace_size.restype = _sz
 _lib.path_decode_workspace_size.argtypes = [_DDP]
 _lib.path_decode_step.restype = _i
-_lib.path_decode_step.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _vp, _sz, _vp]
+_lib.path_decode_step.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
 
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_decode_workspace_size", "path_decode_step")
