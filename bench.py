@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the PaTH attention library on one GB300 (or N, one process each).
+
+Step = one forward + backward pass of PaTH attention over batch 32, 32 heads, head dim 64,
+L = 4096, bf16 inputs (q, k, v, w, dO; beta fp32, 5 % of beta in [1.95, 2)), i.e. every step
+of the fwd/bwd hot path.  The decode workload (batch 32, 32 heads, cache 32768 -> 33023 bf16,
+256 steps) is measured in the same run and reported under "decode".
+
+Metric: fwd+bwd TFLOP/s with FLOPs counted per head as
+  fwd 2 L^2 d + L^2 d^2 / B_fwd,  bwd 5 L^2 d + 2 L^2 d^2 / B_bwd
+at the chunk sizes the kernels use (the FlashAttention-convention count, fwd 2 L^2 d + bwd
+5 L^2 d, is reported beside it).  Decode: HBM GB/s counting 3 x t x d x 2 bytes per head per step
+(read K, write K, read V).
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from softmax_attention_chunk_gb300.inputs import CONFIGS, gen_decode_inputs, gen_path_inputs  # noqa: E402
+
+METRIC = "PaTH fwd+bwd TFLOP/s (B32 H32 d64 L4K) vs bf16 peak; decode HBM GB/s"
+FWD_CFG = "fig1_fwd_l4096"
+DEC_CFG = "decode_b32h32_t32768"
+L2_BYTES = 129 * 2**20
+WORKLOAD = ("PaTH fwd+bwd, batch 32, 32 heads, d=64, L=4096, bf16 (beta fp32, 5% near-reflection beta), "
+            "per rank")
+FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # FP32 FMA lanes x 2 x max SM clock
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def fwd_flops_per_head(L, d, B):
+    return 2 * L * L * d + L * L * d * d / B
+
+
+def bwd_flops_per_head(L, d, B):
+    return 5 * L * L * d + 2 * L * L * d * d / B
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline_sample(cfg, B_f, B_b, budget_s=15.0, max_heads=16):
+    """The fp64 oracle, as it stands, on whole heads of the same workload (fwd + bwd)."""
+    from oracle import oracle as orc
+
+    L, d = cfg["seqlen"], cfg["head_dim"]
+    flops = 0.0
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_heads and (time.perf_counter() - t0) < budget_s:
+        x = gen_path_inputs(**cfg, with_dO=True, heads_subset=[n])
+        orc.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, cfg["scale"])
+        orc.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, cfg["scale"], x["dO"])
+        flops += fwd_flops_per_head(L, d, B_f) + bwd_flops_per_head(L, d, B_b)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {cfg['batch'] * cfg['heads']} heads (L={L}, fwd+bwd, fp64, input generation "
+                      f"included), {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+
+    cfg = dict(CONFIGS[FWD_CFG])
+    from softmax_attention_chunk_gb300 import build_lib  # noqa: F401  (chunk sizes only; no GPU)
+    B_f, B_b = chunk_sizes()
+    L, d = cfg["seqlen"], cfg["head_dim"]
+    per_step = fwd_flops_per_head(L, d, B_f) + bwd_flops_per_head(L, d, B_b)
+
+    def step(h):
+        x = gen_path_inputs(**cfg, with_dO=True, heads_subset=[h])
+        orc.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, cfg["scale"])
+        orc.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, cfg["scale"], x["dO"])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "chunk_fwd": B_f, "chunk_bwd": B_b},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": "one (batch, head) of the B32 H32 L4096 workload per step, fwd+bwd fp64"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def chunk_sizes():
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    cfg = CONFIGS[FWD_CFG]
+    desc = pa.path_attn_desc_t(cfg["batch"], cfg["heads"], cfg["seqlen"], cfg["head_dim"], pa.PATH_BF16,
+                               cfg["scale"], 0)
+    return pa.path_attn_chunk(desc, 0), pa.path_attn_chunk(desc, 1)
+
+
+def ev():
+    e = torch.cuda.Event(enable_timing=True)
+    e.record()
+    return e
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    pk = peaks()
+    cfg = dict(CONFIGS[FWD_CFG])
+    cfg["seed"] = cfg["seed"] + 7919 * rank  # each rank owns its own (batch, head) problems
+    Bt, H, L, d = cfg["batch"], cfg["heads"], cfg["seqlen"], cfg["head_dim"]
+    BH = Bt * H
+    B_f, B_b = chunk_sizes()
+    dev = torch.device("cuda", local)
+
+    host = gen_path_inputs(**cfg, with_dO=True)
+    host = {k: v.pin_memory() for k, v in host.items() if v is not None}
+    x = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+    torch.cuda.synchronize()
+    q, k, v, w, beta, dO = (x[n] for n in ("q", "k", "v", "w", "beta", "dO"))
+    desc = pa.make_desc(q, cfg["scale"])
+    ws_f = pa.workspace(desc, 0, dev)
+    ws_b = pa.workspace(desc, 1, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(Bt, H, L, dtype=torch.float32, device=dev)
+    grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q), dw=torch.empty_like(q),
+                 dbeta=torch.empty_like(beta))
+
+    def step(evs=None):
+        marks = [ev()] if evs is not None else None
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse), phases=pa.PATH_FWD_PREPARE)
+        if marks is not None: marks.append(ev())
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse), phases=pa.PATH_FWD_SCAN)
+        if marks is not None: marks.append(ev())
+        for ph in (pa.PATH_BWD_PREPARE, pa.PATH_BWD_SCAN, pa.PATH_BWD_FINISH):
+            pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads, phases=ph)
+            if marks is not None: marks.append(ev())
+        if evs is not None:
+            evs.append(marks)
+
+    for _ in range(args.warmup):
+        step()
+    clocks = Clocks(local)
+    barrier(ws)
+    clocks.start()
+    evs = []
+    for _ in range(args.steps):
+        step(evs)
+    barrier(ws)
+    clocks_rec = clocks.stop()
+    phase_names = ["fwd_prepare", "fwd_scan", "bwd_prepare", "bwd_scan", "bwd_finish"]
+    phase_ms = {n: statistics.mean(m[i].elapsed_time(m[i + 1]) for m in evs) for i, n in enumerate(phase_names)}
+    total_ms = evs[0][0].elapsed_time(evs[-1][-1])
+    total_ms = max_over_ranks(total_ms, ws)
+    ms_step = total_ms / args.steps
+    flops_step = BH * (fwd_flops_per_head(L, d, B_f) + bwd_flops_per_head(L, d, B_b))
+    fa_flops_step = BH * 7 * L * L * d
+    value = ws * flops_step / (ms_step * 1e-3) / 1e12
+
+    # dominant kernel roofline (the scan phases each run one kernel)
+    dom = max(("fwd_scan", "bwd_scan"), key=lambda n: phase_ms[n])
+    npairs_f = (math.ceil(L / B_f) * (math.ceil(L / B_f) - 1)) // 2
+    npairs_b = (math.ceil(L / B_b) * (math.ceil(L / B_b) - 1)) // 2
+    alg = {"fwd_scan": BH * npairs_f * (4 * B_f * B_f * d + 2 * B_f * d * d),
+           "bwd_scan": BH * npairs_b * (10 * B_b * B_b * d + 4 * B_b * d * d)}
+    achieved = alg[dom] / (phase_ms[dom] * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": FP32_SIMT_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_PEAK_TFLOPS, "traffic": None,
+                "peak_source": "FP32 CUDA-core peak 152 SM x 128 lanes x 2 flop x 2070 MHz"}
+
+    # end-to-end through the public API: pinned host inputs in, outputs and gradients out
+    outs_h = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+              "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    for n, t in grads.items():
+        outs_h[n] = torch.empty_like(t, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+
+    def e2e_step():
+        for n, t in host.items():
+            x[n].copy_(t, non_blocking=True)
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse))
+        pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads)
+        outs_h["o"].copy_(o, non_blocking=True)
+        outs_h["lse"].copy_(lse, non_blocking=True)
+        for n, t in grads.items():
+            outs_h[n].copy_(t, non_blocking=True)
+
+    e2e_step()
+    barrier(ws)
+    e0 = ev()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1 = ev()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, ws)
+    e2e = {"value": ws * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+    del ws_b, grads, x, host, outs_h
+    torch.cuda.empty_cache()
+
+    dec = None if args.no_decode else run_decode(args, pa, dev, rank, ws, pk)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(dict(CONFIGS[FWD_CFG]), B_f, B_b)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD,
+                           "chunk_fwd": B_f, "chunk_bwd": B_b, "flops_per_step": flops_step,
+                           "l2": "inputs larger than L2 (6 x 512 MiB per step)"},
+                "frac_of_bf16_peak": value / ws / pk["bf16"],
+                "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
+                "phase_ms": phase_ms, "roofline": roofline, "e2e": e2e, "clocks": clocks_rec,
+                "gpu_launches": 6 * args.steps, "memset_ops": 3 * args.steps,
+                "peaks": pk, "decode": dec, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_decode(args, pa, dev, rank, ws, pk):
+    cfg = dict(CONFIGS[DEC_CFG])
+    cfg["seed"] += 7919 * rank
+    Bt, H, d, t0 = cfg["batch"], cfg["heads"], cfg["head_dim"], cfg["t0"]
+    steps = args.decode_steps
+    di = gen_decode_inputs(**{**cfg, "steps": steps})
+    kc0 = di["k_cache"].to(dev)
+    vc0 = di["v_cache"].to(dev)
+    kc, vc = kc0.clone(), vc0.clone()
+    sx = {n: di[n].to(dev) for n in ("q", "k", "v", "w", "beta")}
+    del di
+    desc = pa.make_decode_desc(kc, cfg["scale"])
+    wsd = pa.decode_workspace(desc, dev)
+    o = torch.empty(Bt, H, d, dtype=kc.dtype, device=dev)
+    for s in range(3):  # warm-up on the copy, then restore the pristine cache
+        pa.decode_step(kc, vc, t0 + s, *(sx[n][s] for n in ("q", "k", "v", "w", "beta")), scale=cfg["scale"],
+                       ws=wsd, out=o)
+    kc.copy_(kc0)
+    vc.copy_(vc0)
+    clocks = Clocks(dev.index)
+    barrier(ws)
+    clocks.start()
+    marks = [ev()]
+    for s in range(steps):
+        pa.decode_step(kc, vc, t0 + s, *(sx[n][s] for n in ("q", "k", "v", "w", "beta")), scale=cfg["scale"],
+                       ws=wsd, out=o)
+        marks.append(ev())
+    barrier(ws)
+    crec = clocks.stop()
+    per = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
+    total_ms = max_over_ranks(sum(per), ws)
+    nbytes = sum(Bt * H * 3 * (t0 + s) * d * 2 for s in range(steps))
+    gbs = ws * nbytes / (total_ms * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "tokens_per_s": ws * Bt * steps / (total_ms * 1e-3),
+            "ms_per_step": total_ms / steps, "steps": steps, "frac_of_hbm": gbs / ws / pk["hbm"],
+            "roofline": {"kernel": "decode step (split + combine)", "bound": "hbm", "achieved": gbs / ws,
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / ws / pk["hbm"], "traffic": None},
+            "clocks": crec, "gpu_launches": 2 * steps,
+            "workload": "decode, batch 32, 32 heads, d=64, cache 32768 -> 33023 bf16, 256 steps"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

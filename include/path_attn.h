@@ -120,6 +120,33 @@ int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, co
                   const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dw,
                   float* dbeta, float* dlog_f, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * The same two passes split into their phases, so that a caller can time or overlap them.
+ * path_attn_fwd(...) is path_attn_fwd_phases(PATH_FWD_ALL, ...); path_attn_bwd likewise.
+ * Phases must run in the listed order on one stream with the same arguments and the same
+ * workspace, and nothing else may use that workspace in between.  Arguments, validation and
+ * errors are those of the full call (every pointer is checked whatever the phase);
+ * phases == 0 or an unknown bit gives PATH_ERR_INVALID_ARG.
+ *   forward:  PREPARE = per-chunk UT transform, Q<-, K->, F and diagonal-chunk softmax state
+ *             into ws;  SCAN = right-to-left chunk scan writing o and lse.
+ *   backward: PREPARE = zero the accumulators, D_i = dO_i . o_i, recompute the per-chunk UT
+ *             quantities;  SCAN = descending Z pass and ascending adjoint scan (accumulates
+ *             dV, dK->, dF, writes dQ<- in ws);  FINISH = diagonal-chunk and UT backward
+ *             writing dq, dk, dv, dw, dbeta.
+ */
+enum { PATH_FWD_PREPARE = 1, PATH_FWD_SCAN = 2, PATH_FWD_ALL = 3 };
+enum { PATH_BWD_PREPARE = 1, PATH_BWD_SCAN = 2, PATH_BWD_FINISH = 4, PATH_BWD_ALL = 7 };
+
+int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q, const void* k,
+                         const void* v, const void* w, const float* beta, const float* log_f,
+                         void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, const void* q, const void* k,
+                         const void* v, const void* w, const float* beta, const float* log_f,
+                         const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                         void* dv, void* dw, float* dbeta, float* dlog_f, void* ws,
+                         size_t ws_bytes, void* stream);
+
 /* Bytes of workspace path_decode_step needs for any t < capacity; 0 if invalid. Host only. */
 size_t path_decode_workspace_size(const path_decode_desc_t* desc);
 

@@ -79,12 +79,14 @@ PATH_API size_t path_attn_workspace_size(const path_attn_desc_t* desc, int for_b
   return for_backward ? bwd_ws_layout(g).total : fwd_ws_layout(g, 4).total;
 }
 
-PATH_API int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
-                  const void* w, const float* beta, const float* log_f, void* o, float* lse,
-                  void* ws, size_t ws_bytes, void* stream) {
+PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q,
+                                  const void* k, const void* v, const void* w, const float* beta,
+                                  const float* log_f, void* o, float* lse, void* ws,
+                                  size_t ws_bytes, void* stream) {
   Geom g;
   int rc = check_desc(desc, 0, &g);
   if (rc != PATH_OK) return rc;
+  if (phases <= 0 || (phases & ~PATH_FWD_ALL)) return PATH_ERR_INVALID_ARG;
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o); CHECK_PTR(lse);
   if (log_f && !aligned(log_f, 16)) return PATH_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
@@ -93,18 +95,33 @@ PATH_API int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const vo
   cudaStream_t st = (cudaStream_t)stream;
   const bool bf = desc->dtype == PATH_BF16;
   char* wsb = (char*)ws;
-  rc = cuda_status(launch_prep_simt(bf, g, q, k, v, w, beta, log_f, wsb, lay, true, st));
-  if (rc != PATH_OK) return rc;
-  return cuda_status(launch_main_simt(bf, g, v, log_f, wsb, lay, o, lse, st));
+  if (phases & PATH_FWD_PREPARE) {
+    rc = cuda_status(launch_prep_simt(bf, g, q, k, v, w, beta, log_f, wsb, lay, true, st));
+    if (rc != PATH_OK) return rc;
+  }
+  if (phases & PATH_FWD_SCAN) {
+    rc = cuda_status(launch_main_simt(bf, g, v, log_f, wsb, lay, o, lse, st));
+    if (rc != PATH_OK) return rc;
+  }
+  return PATH_OK;
 }
 
-PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
-                  const void* w, const float* beta, const float* log_f, const void* o,
-                  const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dw,
-                  float* dbeta, float* dlog_f, void* ws, size_t ws_bytes, void* stream) {
+PATH_API int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                           const void* w, const float* beta, const float* log_f, void* o, float* lse,
+                           void* ws, size_t ws_bytes, void* stream) {
+  return path_attn_fwd_phases(PATH_FWD_ALL, desc, q, k, v, w, beta, log_f, o, lse, ws, ws_bytes, stream);
+}
+
+PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, const void* q,
+                                  const void* k, const void* v, const void* w, const float* beta,
+                                  const float* log_f, const void* o, const float* lse,
+                                  const void* dO, void* dq, void* dk, void* dv, void* dw,
+                                  float* dbeta, float* dlog_f, void* ws, size_t ws_bytes,
+                                  void* stream) {
   Geom g;
   int rc = check_desc(desc, 1, &g);
   if (rc != PATH_OK) return rc;
+  if (phases <= 0 || (phases & ~PATH_BWD_ALL)) return PATH_ERR_INVALID_ARG;
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o);
   CHECK_PTR(lse); CHECK_PTR(dO); CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dw);
   CHECK_PTR(dbeta);
@@ -113,7 +130,15 @@ PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const vo
   const BwdWs lay = bwd_ws_layout(g);
   if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,
-                                     dk, dv, dw, dbeta, (char*)ws, lay, (cudaStream_t)stream));
+                                     dk, dv, dw, dbeta, (char*)ws, lay, phases, (cudaStream_t)stream));
+}
+
+PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
+                           const void* w, const float* beta, const float* log_f, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv, void* dw,
+                           float* dbeta, float* dlog_f, void* ws, size_t ws_bytes, void* stream) {
+  return path_attn_bwd_phases(PATH_BWD_ALL, desc, q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw,
+                              dbeta, dlog_f, ws, ws_bytes, stream);
 }
 
 PATH_API size_t path_decode_workspace_size(const path_decode_desc_t* d) {

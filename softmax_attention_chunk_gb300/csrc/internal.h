@@ -104,11 +104,13 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
-// SIMT backward.
+// SIMT backward.  phases: bit 0 = prepare (zero accumulators, D_i, recomputed UT quantities),
+// bit 1 = adjoint chunk scan, bit 2 = per-chunk UT backward writing the gradients.
 cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                             const void* v, const void* w, const float* beta, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                            void* dw, float* dbeta, char* ws, const BwdWs& lay, cudaStream_t st);
+                            void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
+                            cudaStream_t st);
 
 // Decode step.
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,

@@ -471,9 +471,10 @@ template <typename T, int B>
 cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                   const float* beta, const void* o, const float* lse, const void* dO, void* dq,
                   void* dk, void* dv, void* dw, float* dbeta, char* ws, const BwdWs& lay,
-                  cudaStream_t st) {
+                  int phases, cudaStream_t st) {
   cudaError_t e;
   const size_t rows = (size_t)g.BH * g.Lp;
+  if (phases & 1) {
   if ((e = cudaMemsetAsync(ws + lay.dkr, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.df, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
@@ -484,7 +485,8 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
   if ((e = launch_prep_simt(std::is_same<T, __nv_bfloat16>::value, g, q, k, v, w, beta, nullptr, ws,
                             lay.fw, false, st)) != cudaSuccess)
     return e;
-  {
+  }
+  if (phases & 2) {
     auto kern = bwd_main_simt_kernel<T, B>;
     const size_t smem = BwdMainSmem<B>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
@@ -495,7 +497,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
                                       (float*)(ws + lay.zs));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
+  if (phases & 4) {
     auto kern = prep_bwd_simt_kernel<T, B>;
     const size_t smem = PrepBwdSmem<B>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
@@ -512,10 +514,11 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
 cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                             const void* v, const void* w, const float* beta, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                            void* dw, float* dbeta, char* ws, const BwdWs& lay, cudaStream_t st) {
+                            void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
+                            cudaStream_t st) {
   if (g.B != 32) return cudaErrorInvalidValue;
-  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, st)
-                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, st);
+  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st)
+                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st);
 }
 
 }  // namespace pathattn

@@ -51,13 +51,21 @@ _lib.path_attn_fwd.restype = _i
 _lib.path_attn_fwd.argtypes = [_DP] + [_vp] * 8 + [_vp, _sz, _vp]
 _lib.path_attn_bwd.restype = _i
 _lib.path_attn_bwd.argtypes = [_DP] + [_vp] * 15 + [_vp, _sz, _vp]
+_lib.path_attn_fwd_phases.restype = _i
+_lib.path_attn_fwd_phases.argtypes = [_i, _DP] + [_vp] * 8 + [_vp, _sz, _vp]
+_lib.path_attn_bwd_phases.restype = _i
+_lib.path_attn_bwd_phases.argtypes = [_i, _DP] + [_vp] * 15 + [_vp, _sz, _vp]
 _lib.path_decode_workspace_size.restype = _sz
 _lib.path_decode_workspace_size.argtypes = [_DDP]
 _lib.path_decode_step.restype = _i
 _lib.path_decode_step.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
 
+PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
+PATH_BWD_PREPARE, PATH_BWD_SCAN, PATH_BWD_FINISH, PATH_BWD_ALL = 1, 2, 4, 7
+
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
-            "path_attn_bwd", "path_decode_workspace_size", "path_decode_step")
+            "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
+            "path_decode_step")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -82,6 +90,17 @@ def path_attn_bwd(desc, q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw, dbe
                   ws_bytes, stream) -> int:
     return _lib.path_attn_bwd(ctypes.byref(desc), q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw,
                               dbeta, dlog_f, ws, ws_bytes, stream)
+
+
+def path_attn_fwd_phases(phases, desc, q, k, v, w, beta, log_f, o, lse, ws, ws_bytes, stream) -> int:
+    return _lib.path_attn_fwd_phases(int(phases), ctypes.byref(desc), q, k, v, w, beta, log_f, o, lse, ws,
+                                     ws_bytes, stream)
+
+
+def path_attn_bwd_phases(phases, desc, q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw, dbeta, dlog_f,
+                         ws, ws_bytes, stream) -> int:
+    return _lib.path_attn_bwd_phases(int(phases), ctypes.byref(desc), q, k, v, w, beta, log_f, o, lse, dO, dq,
+                                     dk, dv, dw, dbeta, dlog_f, ws, ws_bytes, stream)
 
 
 def path_decode_workspace_size(desc: path_decode_desc_t) -> int:
@@ -131,7 +150,7 @@ def workspace(desc, for_backward, device):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None):
+def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None, phases=PATH_FWD_ALL):
     """o [B,H,L,d] (dtype of q) and lse [B,H,L] float32."""
     desc = make_desc(q, scale, chunk)
     for name, t in (("k", k), ("v", v), ("w", w)):
@@ -144,13 +163,14 @@ def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None):
         ws = workspace(desc, 0, q.device)
     o, lse = out if out is not None else (torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32,
                                                                            device=q.device))
-    rc = path_attn_fwd(desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse), _p(ws),
-                       ws.numel(), _stream())
+    rc = path_attn_fwd_phases(phases, desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse),
+                              _p(ws), ws.numel(), _stream())
     _check(rc, "path_attn_fwd")
     return o, lse
 
 
-def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, out=None):
+def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, out=None,
+        phases=PATH_BWD_ALL):
     """Gradients dict dq, dk, dv, dw (dtype of q) and dbeta (float32)."""
     desc = make_desc(q, scale, chunk)
     for name, t in (("k", k), ("v", v), ("w", w), ("o", o), ("dO", dO)):
@@ -162,9 +182,9 @@ def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, o
     if out is None:
         out = dict(dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
                    dw=torch.empty_like(q), dbeta=torch.empty_like(beta))
-    rc = path_attn_bwd(desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse), _p(dO),
-                       _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dw"]), _p(out["dbeta"]), None,
-                       _p(ws), ws.numel(), _stream())
+    rc = path_attn_bwd_phases(phases, desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse),
+                              _p(dO), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dw"]),
+                              _p(out["dbeta"]), None, _p(ws), ws.numel(), _stream())
     _check(rc, "path_attn_bwd")
     return out
 

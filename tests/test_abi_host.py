@@ -1,0 +1,160 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function
+include/path_attn.h declares, and rejects bad arguments with the documented status before any
+CUDA call.  Every call below fails validation, so nothing is ever launched (fake pointers are
+never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "path_attn.h")
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from softmax_attention_chunk_gb300 import build_lib
+
+    build_lib.build()
+    from softmax_attention_chunk_gb300 import path_attn
+
+    return path_attn
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\**\s+(path_[a-z_]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_path_calls():
+    fns = declared_functions()
+    for f in ("path_attn_fwd", "path_attn_bwd", "path_decode_step"):
+        assert f in fns
+
+
+def test_library_exports_every_declared_symbol(pa):
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    for f in declared_functions():
+        assert hasattr(lib, f), f
+    assert sorted(pa.EXPORTED) == declared_functions()
+
+
+def desc(pa, **kw):
+    d = dict(batch=1, heads=2, seqlen=100, head_dim=64, dtype=pa.PATH_FP32, scale=1.0, chunk=0)
+    d.update(kw)
+    return pa.path_attn_desc_t(d["batch"], d["heads"], d["seqlen"], d["head_dim"], d["dtype"], d["scale"],
+                               d["chunk"])
+
+
+FAKE = 1 << 20  # aligned, never dereferenced
+
+
+def test_status_strings(pa):
+    for s in range(7):
+        assert pa.path_status_string(s).startswith(pa.STATUS_NAMES[s])
+    assert "unknown" in pa.path_status_string(99)
+
+
+def test_descriptor_validation(pa):
+    assert pa.path_attn_chunk(desc(pa), 0) == 64
+    assert pa.path_attn_chunk(desc(pa, chunk=32), 0) == 32
+    assert pa.path_attn_chunk(desc(pa), 1) > 0
+    assert pa.path_attn_chunk(desc(pa, head_dim=128), 0) == -2          # unsupported
+    assert pa.path_attn_chunk(desc(pa, head_dim=0), 0) == -1            # invalid
+    assert pa.path_attn_chunk(desc(pa, seqlen=0), 0) == -1
+    assert pa.path_attn_chunk(desc(pa, dtype=7), 0) == -1
+    assert pa.path_attn_chunk(desc(pa, chunk=48), 0) == -2
+    assert pa.path_attn_chunk(desc(pa, scale=float("nan")), 0) == -1
+    assert pa.path_attn_workspace_size(desc(pa, head_dim=32), 0) == 0
+    assert pa.path_attn_workspace_size(desc(pa), 0) > 0
+    assert pa.path_attn_workspace_size(desc(pa), 1) > pa.path_attn_workspace_size(desc(pa), 0)
+    # workspace grows with the problem
+    assert pa.path_attn_workspace_size(desc(pa, seqlen=1000), 0) > pa.path_attn_workspace_size(desc(pa), 0)
+
+
+def fwd_args(pa, d, ws_bytes=None, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, w=FAKE, beta=FAKE, log_f=None, o=FAKE, lse=FAKE, ws=FAKE,
+             ws_bytes=pa.path_attn_workspace_size(d, 0) if ws_bytes is None else ws_bytes, stream=None)
+    a.update(over)
+    return a
+
+
+def call_fwd(pa, d, **a):
+    return pa.path_attn_fwd(d, a["q"], a["k"], a["v"], a["w"], a["beta"], a["log_f"], a["o"], a["lse"], a["ws"],
+                            a["ws_bytes"], a["stream"])
+
+
+def test_fwd_argument_errors(pa):
+    d = desc(pa)
+    ok_bytes = pa.path_attn_workspace_size(d, 0)
+    assert call_fwd(pa, d, **fwd_args(pa, d, ws_bytes=ok_bytes - 1)) == 3          # workspace
+    assert call_fwd(pa, d, **fwd_args(pa, d, q=None, ws_bytes=0)) == 1             # null
+    assert call_fwd(pa, d, **fwd_args(pa, d, k=FAKE + 8, ws_bytes=0)) == 1         # misaligned
+    assert call_fwd(pa, d, **fwd_args(pa, d, ws=FAKE + 16, ws_bytes=0)) == 1       # ws not 256-aligned
+    assert call_fwd(pa, d, **fwd_args(pa, d, log_f=FAKE + 4, ws_bytes=0)) == 1
+    assert call_fwd(pa, desc(pa, head_dim=128), **fwd_args(pa, d)) == 2
+    assert pa._lib.path_attn_fwd(None, *([FAKE] * 8), FAKE, 0, None) == 1
+    for bad in (0, 4, 8):
+        assert pa.path_attn_fwd_phases(bad, d, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 0, None) in (1, 3)
+    assert pa.path_attn_fwd_phases(0, d, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ok_bytes, None) == 1
+
+
+def test_bwd_argument_errors(pa):
+    d = desc(pa)
+    n = pa.path_attn_workspace_size(d, 1)
+    args = [FAKE] * 6 + [None] + [FAKE] * 3 + [FAKE] * 5  # q k v w beta o? see order below
+    # order: q,k,v,w,beta,log_f,o,lse,dO,dq,dk,dv,dw,dbeta,dlog_f,ws,ws_bytes,stream
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE]
+    assert pa.path_attn_bwd(d, *base, n - 1, None) == 3
+    with_logf = list(base); with_logf[5] = FAKE
+    assert pa.path_attn_bwd(d, *with_logf, n, None) == 2   # forget-gate gradient unsupported
+    with_dlogf = list(base); with_dlogf[14] = FAKE
+    assert pa.path_attn_bwd(d, *with_dlogf, n, None) == 2
+    null_dw = list(base); null_dw[12] = None
+    assert pa.path_attn_bwd(d, *null_dw, n, None) == 1
+    assert pa.path_attn_bwd_phases(8, d, *base, n, None) == 1
+    del args
+
+
+def test_decode_argument_errors(pa):
+    dd = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_BF16, 1.0)
+    n = pa.path_decode_workspace_size(dd)
+    assert n > 0
+    vec = [FAKE] * 6
+    assert pa.path_decode_step(dd, FAKE, FAKE, 100, *vec, FAKE, n, None) == 4     # t + 1 > capacity
+    assert pa.path_decode_step(dd, FAKE, FAKE, -1, *vec, FAKE, n, None) == 1
+    assert pa.path_decode_step(dd, FAKE, FAKE, 5, *vec, FAKE, n - 1, None) == 3
+    assert pa.path_decode_step(dd, None, FAKE, 5, *vec, FAKE, n, None) == 1
+    bad = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
+    assert pa.path_decode_workspace_size(bad) == 0
+    assert pa.path_decode_step(bad, FAKE, FAKE, 5, *vec, FAKE, n, None) == 2
+
+
+def test_torch_wrapper_rejects_bad_tensors(pa):
+    q = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        pa.fwd(q, q, q, q, torch.zeros(1, 1, 8), scale=1.0)  # CPU tensors are refused before any call
+
+
+def test_input_generator_subsets_are_exact():
+    from softmax_attention_chunk_gb300.inputs import gen_decode_inputs, gen_path_inputs
+
+    full = gen_path_inputs(2, 3, 50, 64, "bf16", seed=4, near2_frac=0.3, fox=True, with_dO=True)
+    sub = gen_path_inputs(2, 3, 50, 64, "bf16", seed=4, near2_frac=0.3, fox=True, with_dO=True,
+                          heads_subset=[4, 1])
+    for key in ("q", "k", "v", "w", "beta", "log_f", "dO"):
+        f = full[key].reshape(6, *full[key].shape[2:])
+        assert torch.equal(f[[4, 1]], sub[key]), key
+    b = full["beta"]
+    assert float(b.min()) > 0 and float(b.max()) < 2
+    assert float(b.max()) >= 1.95  # the near-reflection tail is present
+    w = full["w"].double()
+    assert torch.allclose(w.norm(dim=-1), torch.ones(2, 3, 50, dtype=torch.float64), atol=1e-2)
+    dfull = gen_decode_inputs(1, 3, 64, t0=10, steps=4, dtype="fp32", seed=2)
+    dsub = gen_decode_inputs(1, 3, 64, t0=10, steps=4, dtype="fp32", seed=2, heads_subset=[2])
+    assert torch.equal(dfull["k_cache"][0, 2], dsub["k_cache"][0])
+    assert torch.equal(dfull["q"][:, 0, 2], dsub["q"][:, 0])
+    assert torch.all(dfull["k_cache"][:, :, 10:] == 0)
