@@ -165,6 +165,29 @@ int path_decode_step(const path_decode_desc_t* desc, void* k_cache, void* v_cach
                      const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                      const float* beta_t, void* o_t, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * path_decode_step without a workspace argument.  The paper has no counterpart: this exists
+ * for callers that cannot allocate device memory when they decode — code running inside
+ * another runtime's memory pool without access to its allocator, plugins that may only use
+ * the buffers handed to them, or serving loops that forbid allocation after start-up.
+ *
+ * Same arguments, semantics and results as path_decode_step, minus ws/ws_bytes.  The per-split
+ * partial softmax states live in a fixed 16 MiB array inside the library, present on every
+ * GPU that loads it until the process exits.  Limit: batch * heads <= PATH_DECODE_NOALLOC_MAX_HEADS,
+ * otherwise PATH_ERR_WORKSPACE is returned and nothing runs.  The call itself allocates
+ * nothing (no cudaMalloc, no library allocator).
+ *  - The first call made with a given device current looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *  - All calls on a device share the one array: calls that may overlap on the GPU (different
+ *    streams without ordering between them) race and give wrong results.  Calls ordered on one
+ *    stream are safe.  Nothing in the array needs to start at zero: each call overwrites the
+ *    parts it reads.
+ */
+#define PATH_DECODE_NOALLOC_MAX_HEADS 496
+int path_decode_step_noalloc(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int t,
+                             const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                             const float* beta_t, void* o_t, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -59,13 +59,16 @@ _lib.path_decode_workspace_size.restype = _sz
 _lib.path_decode_workspace_size.argtypes = [_DDP]
 _lib.path_decode_step.restype = _i
 _lib.path_decode_step.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
+_lib.path_decode_step_noalloc.restype = _i
+_lib.path_decode_step_noalloc.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp]
+PATH_DECODE_NOALLOC_MAX_HEADS = 496
 
 PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
 PATH_BWD_PREPARE, PATH_BWD_SCAN, PATH_BWD_FINISH, PATH_BWD_ALL = 1, 2, 4, 7
 
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
-            "path_decode_step")
+            "path_decode_step", "path_decode_step_noalloc")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -110,6 +113,11 @@ def path_decode_workspace_size(desc: path_decode_desc_t) -> int:
 def path_decode_step(desc, k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, o_t, ws, ws_bytes, stream) -> int:
     return _lib.path_decode_step(ctypes.byref(desc), k_cache, v_cache, int(t), q_t, k_t, v_t, w_t, beta_t,
                                  o_t, ws, ws_bytes, stream)
+
+
+def path_decode_step_noalloc(desc, k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, o_t, stream) -> int:
+    return _lib.path_decode_step_noalloc(ctypes.byref(desc), k_cache, v_cache, int(t), q_t, k_t, v_t, w_t,
+                                         beta_t, o_t, stream)
 
 
 # ---------------- torch-tensor wrappers ----------------
