@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling on a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
     return ap.parse_args()
 
 
@@ -222,6 +224,10 @@ def run_ours(args):
     pk = peaks()
     cfg = dict(CONFIGS[FWD_CFG])
     cfg["seed"] = cfg["seed"] + 7919 * rank  # each rank owns its own (batch, head) problems
+    if args.batch:
+        cfg["batch"] = args.batch
+    if args.heads:
+        cfg["heads"] = args.heads
     Bt, H, L, d = cfg["batch"], cfg["heads"], cfg["seqlen"], cfg["head_dim"]
     BH = Bt * H
     B_f, B_b = chunk_sizes()
@@ -322,7 +328,7 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": WORKLOAD,
+                "config": {"workload": WORKLOAD if (Bt, H) == (32, 32) else f"{WORKLOAD}; batch {Bt}, {H} heads",
                            "chunk_fwd": B_f, "chunk_bwd": B_b, "flops_per_step": flops_step,
                            "l2": "inputs larger than L2 (6 x 512 MiB per step)"},
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
