@@ -36,6 +36,7 @@ struct FwdWs {
   size_t ql, kr, f;            // Q<- [BH][Lp][64], K-> [BH][Lp][64], F [BH][nc][64][64]
   size_t dm, dl, dacc;         // diagonal-chunk softmax state: max (log2 domain), sum, acc[64]
   size_t fa, fr, ft;           // forget gate: local inclusive prefix, local exclusive suffix, chunk total
+  size_t err;                  // int: first timeout code of a tensor-core kernel (0 = none)
   size_t total;
 };
 
@@ -53,6 +54,7 @@ inline FwdWs fwd_ws_layout(const Geom& g, size_t esize) {
   w.fa = take(rows * 4);
   w.fr = take(rows * 4);
   w.ft = take((size_t)g.BH * g.nc * 4);
+  w.err = take(4);
   w.total = off;
   return w;
 }
@@ -103,6 +105,14 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
                              char* ws, const FwdWs& lay, bool with_diag, cudaStream_t st);
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
+
+// Preparation for the tensor-core scan: bf16 inputs, chunk 64, Q<-/K->/F written as bf16.
+cudaError_t launch_prep_bf16_out(const Geom& g, const void* q, const void* k, const void* v,
+                                 const void* w, const float* beta, const float* logf, char* ws,
+                                 const FwdWs& lay, cudaStream_t st);
+// tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
+cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
+                           const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
 // SIMT backward.  phases: bit 0 = prepare (zero accumulators, D_i, recomputed UT quantities),
 // bit 1 = adjoint chunk scan, bit 2 = per-chunk UT backward writing the gradients.

@@ -26,11 +26,11 @@ struct PrepSmem {
 // One CTA per (chunk c, head bh).  Writes Q<-, K->, F, the diagonal-chunk softmax state and
 // the chunk-local forget-gate sums.  Rows beyond L are padding with q=k=v=w=0, beta=0
 // (H = I), log f = 0.
-template <typename T, int B>
+template <typename T, int B, typename OutT>
 __global__ void __launch_bounds__(NT) prep_simt_kernel(
     Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ logf,
-    float* __restrict__ ql, float* __restrict__ kr, float* __restrict__ f, float* __restrict__ dm,
+    OutT* __restrict__ ql, OutT* __restrict__ kr, OutT* __restrict__ f, float* __restrict__ dm,
     float* __restrict__ dl, float* __restrict__ dacc, float* __restrict__ fa,
     float* __restrict__ fr, float* __restrict__ ft, int with_diag) {
   extern __shared__ float sm[];
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
     const int i = idx / D, cc = idx % D;
     float acc = sQ[i * DS + cc];
     for (int m = 0; m <= i; ++m) acc -= sT[i * BS + m] * sW[m * DS + cc];
-    ql[(ws_row + i) * D + cc] = acc;
+    ql[(ws_row + i) * D + cc] = from_f<OutT>(acc);
   }
   __syncthreads();
   // N2 = strictLower(W K^T) into sT
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
     const int j = idx / D, cc = idx % D;
     float acc = sK[j * DS + cc];
     for (int m = j + 1; m < B; ++m) acc -= sX[m * BS + j] * sW[m * DS + cc];
-    kr[(ws_row + j) * D + cc] = acc;
+    kr[(ws_row + j) * D + cc] = from_f<OutT>(acc);
   }
   // S_d = lower(Q K^T) - M1 X  into sT (diagonal-chunk logits before scale/bias)
   for (int idx = tid; idx < B * B; idx += NT) {
@@ -205,12 +205,12 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   __syncthreads();
 
   // F = I - W^T Y = I - W^T U^T W  (the chunk's transform H_first ... H_last)
-  float* fout = f + ((size_t)bh * g.nc + c) * D * D;
+  OutT* fout = f + ((size_t)bh * g.nc + c) * D * D;
   for (int idx = tid; idx < D * D; idx += NT) {
     const int n = idx / D, cc = idx % D;
     float acc = (n == cc) ? 1.f : 0.f;
     for (int m = 0; m < B; ++m) acc -= sW[m * DS + n] * sQ[m * DS + cc];
-    fout[idx] = acc;
+    fout[idx] = from_f<OutT>(acc);
   }
   if (logf) {
     const float tot = sA[B - 1];
@@ -341,17 +341,17 @@ __global__ void __launch_bounds__(NT) main_simt_kernel(
   }
 }
 
-template <typename T, int B>
+template <typename T, int B, typename OutT = float>
 cudaError_t prep_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                    const float* beta, const float* logf, char* ws, const FwdWs& lay,
                    bool with_diag, cudaStream_t st) {
-  auto kern = prep_simt_kernel<T, B>;
+  auto kern = prep_simt_kernel<T, B, OutT>;
   const size_t smem = PrepSmem<B>::bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(g.nc, g.BH);
   kern<<<grid, NT, smem, st>>>(g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, logf,
-                               (float*)(ws + lay.ql), (float*)(ws + lay.kr), (float*)(ws + lay.f),
+                               (OutT*)(ws + lay.ql), (OutT*)(ws + lay.kr), (OutT*)(ws + lay.f),
                                (float*)(ws + lay.dm), (float*)(ws + lay.dl), (float*)(ws + lay.dacc),
                                (float*)(ws + lay.fa), (float*)(ws + lay.fr), (float*)(ws + lay.ft),
                                with_diag ? 1 : 0);
@@ -386,6 +386,13 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
     return is_bf16 ? prep_t<__nv_bfloat16, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
                    : prep_t<float, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prep_bf16_out(const Geom& g, const void* q, const void* k, const void* v,
+                                 const void* w, const float* beta, const float* logf, char* ws,
+                                 const FwdWs& lay, cudaStream_t st) {
+  if (g.B != 64) return cudaErrorInvalidValue;
+  return prep_t<__nv_bfloat16, 64, __nv_bfloat16>(g, q, k, v, w, beta, logf, ws, lay, true, st);
 }
 
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
