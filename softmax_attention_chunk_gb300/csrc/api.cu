@@ -34,10 +34,11 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
     if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
     B = d->chunk ? d->chunk : 64;
   }
+  // The tensor-core path scans 64-row key chunks and 128-row query tiles.
+  if (uses_tensor_cores(d, for_backward)) B = 64;
   long long nc = (d->seqlen + B - 1) / B;
-  // The tensor-core forward scans 128-row query tiles (two chunks): pad to an even chunk count.
-  if (uses_tensor_cores(d, for_backward)) nc += nc & 1;
-  if (nc > 65535 || nc * B > (1LL << 30)) return PATH_ERR_UNSUPPORTED;
+  if (uses_tensor_cores(d, for_backward)) nc = (d->seqlen + 127) / 128 * 2;
+  if (nc * (B / 32) > 65535 || nc * B > (1LL << 30)) return PATH_ERR_UNSUPPORTED;
   if (g) {
     g->BH = (int)BH;
     g->L = d->seqlen;
@@ -49,9 +50,13 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
   return PATH_OK;
 }
 
-// Forward workspace layout of the path this descriptor takes.
-FwdWs fwd_layout(const path_attn_desc_t* d, const Geom& g) {
-  return fwd_ws_layout(g, uses_tensor_cores(d, 0) ? 2 : 4);
+TcWs tc_layout(const path_attn_desc_t* d, bool for_backward) {
+  return tc_ws_layout(d->batch * d->heads, d->seqlen, d->scale, for_backward);
+}
+
+// Forward workspace size of the path this descriptor takes.
+size_t fwd_ws_total(const path_attn_desc_t* d, const Geom& g) {
+  return uses_tensor_cores(d, 0) ? tc_layout(d, false).total : fwd_ws_layout(g, 4).total;
 }
 
 #define CHECK_PTR(p)                         \
@@ -89,7 +94,7 @@ PATH_API int path_attn_chunk(const path_attn_desc_t* desc, int for_backward) {
 PATH_API size_t path_attn_workspace_size(const path_attn_desc_t* desc, int for_backward) {
   Geom g;
   if (check_desc(desc, for_backward, &g) != PATH_OK) return 0;
-  return for_backward ? bwd_ws_layout(g).total : fwd_layout(desc, g).total;
+  return for_backward ? bwd_ws_layout(g).total : fwd_ws_total(desc, g);
 }
 
 PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q,
@@ -103,24 +108,31 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o); CHECK_PTR(lse);
   if (log_f && !aligned(log_f, 16)) return PATH_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
-  const FwdWs lay = fwd_layout(desc, g);
-  if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+  if (ws_bytes < fwd_ws_total(desc, g)) return PATH_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   const bool bf = desc->dtype == PATH_BF16;
-  const bool tcp = uses_tensor_cores(desc, 0);
   char* wsb = (char*)ws;
+  if (uses_tensor_cores(desc, 0)) {
+    const TcWs tw = tc_layout(desc, false);
+    if (phases & PATH_FWD_PREPARE) {
+      rc = cuda_status(launch_prep_simt(true, tw.g32, q, k, v, w, beta, log_f, wsb, tw.p32, true, st));
+      if (rc == PATH_OK) rc = cuda_status(launch_merge64(tw, v, log_f, wsb, true, st));
+      if (rc != PATH_OK) return rc;
+    }
+    if (phases & PATH_FWD_SCAN) {
+      rc = cuda_status(cudaMemsetAsync(wsb + tw.p64.err, 0, sizeof(int), st));
+      if (rc == PATH_OK) rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, st));
+      if (rc != PATH_OK) return rc;
+    }
+    return PATH_OK;
+  }
+  const FwdWs lay = fwd_ws_layout(g, 4);
   if (phases & PATH_FWD_PREPARE) {
-    rc = cuda_status(tcp ? launch_prep_bf16_out(g, q, k, v, w, beta, log_f, wsb, lay, st)
-                         : launch_prep_simt(bf, g, q, k, v, w, beta, log_f, wsb, lay, true, st));
+    rc = cuda_status(launch_prep_simt(bf, g, q, k, v, w, beta, log_f, wsb, lay, true, st));
     if (rc != PATH_OK) return rc;
   }
   if (phases & PATH_FWD_SCAN) {
-    if (tcp) {
-      rc = cuda_status(cudaMemsetAsync(wsb + lay.err, 0, sizeof(int), st));
-      if (rc != PATH_OK) return rc;
-    }
-    rc = cuda_status(tcp ? launch_scan_tc(g, v, log_f, wsb, lay, o, lse, st)
-                         : launch_main_simt(bf, g, v, log_f, wsb, lay, o, lse, st));
+    rc = cuda_status(launch_main_simt(bf, g, v, log_f, wsb, lay, o, lse, st));
     if (rc != PATH_OK) return rc;
   }
   return PATH_OK;

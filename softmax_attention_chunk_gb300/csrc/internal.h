@@ -40,9 +40,9 @@ struct FwdWs {
   size_t total;
 };
 
-inline FwdWs fwd_ws_layout(const Geom& g, size_t esize) {
+inline FwdWs fwd_ws_layout(const Geom& g, size_t esize, size_t base = 0) {
   FwdWs w{};
-  size_t off = 0;
+  size_t off = base;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t rows = (size_t)g.BH * g.Lp;
   w.ql = take(rows * kHeadDim * esize);
@@ -93,6 +93,57 @@ inline BwdWs bwd_ws_layout(const Geom& g) {
   return w;
 }
 
+// Workspace of the bf16 tensor-core path.  The UT preparation runs at chunk 32 (fp32 results,
+// p32); a merge kernel forms the chunk-64 operands of the tcgen05 kernels (bf16 Q<-, K->, F and
+// the fp32 diagonal-chunk softmax / forget-gate state, p64).  Lp is a multiple of 128.
+struct TcWs {
+  Geom g32, g64;
+  FwdWs p32, p64;
+  // backward only
+  size_t Dv;                       // D_i                                [BH][Lp]
+  size_t dql64, dkr64, dv, df64;   // chunk-64 gradients (fp32; dkr64/dv/df64 accumulate)
+  size_t dql32, dkr32, df32;       // chunk-32 gradients for the UT backward (fp32)
+  size_t zs;                       // transported queries Z, bf16 swizzled 128x64 tiles
+  size_t total;
+};
+
+inline Geom tc_geom(int BH, int L, float scale, int B) {
+  Geom g;
+  g.BH = BH;
+  g.L = L;
+  g.Lp = (L + 127) / 128 * 128;
+  g.B = B;
+  g.nc = g.Lp / B;
+  g.scale = scale;
+  return g;
+}
+
+inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
+  TcWs w{};
+  w.g32 = tc_geom(BH, L, scale, 32);
+  w.g64 = tc_geom(BH, L, scale, 64);
+  w.p32 = fwd_ws_layout(w.g32, 4, 0);
+  w.p64 = fwd_ws_layout(w.g64, 2, w.p32.total);
+  size_t off = w.p64.total;
+  if (for_backward) {
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t rows = (size_t)BH * w.g64.Lp;
+    const size_t nt = (size_t)w.g64.Lp / 128;
+    w.Dv = take(rows * 4);
+    w.dql64 = take(rows * kHeadDim * 4);
+    w.dkr64 = take(rows * kHeadDim * 4);
+    w.dv = take(rows * kHeadDim * 4);
+    w.df64 = take((size_t)BH * w.g64.nc * kHeadDim * kHeadDim * 4);
+    w.dql32 = take(rows * kHeadDim * 4);
+    w.dkr32 = take(rows * kHeadDim * 4);
+    w.df32 = take((size_t)BH * w.g32.nc * kHeadDim * kHeadDim * 4);
+    // tile T of a head has at most 2T+1 steps: sum over tiles <= nt^2 tiles of 16 KB
+    w.zs = take((size_t)BH * nt * nt * 128 * 128);
+  }
+  w.total = off;
+  return w;
+}
+
 inline size_t decode_ws_bytes(int BH) {
   return align_up((size_t)BH * kDecodeMaxSplits * (kHeadDim + 2) * 4, 256);
 }
@@ -106,10 +157,9 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
-// Preparation for the tensor-core scan: bf16 inputs, chunk 64, Q<-/K->/F written as bf16.
-cudaError_t launch_prep_bf16_out(const Geom& g, const void* q, const void* k, const void* v,
-                                 const void* w, const float* beta, const float* logf, char* ws,
-                                 const FwdWs& lay, cudaStream_t st);
+// Merge of adjacent chunk-32 preparation results into chunk-64 operands (tensor-core path).
+cudaError_t launch_merge64(const TcWs& w, const void* v, const float* logf, char* ws, bool with_diag,
+                           cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, cudaStream_t st);

@@ -388,13 +388,6 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prep_bf16_out(const Geom& g, const void* q, const void* k, const void* v,
-                                 const void* w, const float* beta, const float* logf, char* ws,
-                                 const FwdWs& lay, cudaStream_t st) {
-  if (g.B != 64) return cudaErrorInvalidValue;
-  return prep_t<__nv_bfloat16, 64, __nv_bfloat16>(g, q, k, v, w, beta, logf, ws, lay, true, st);
-}
-
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st) {
   if (g.B == 32)
