@@ -12,10 +12,10 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// bf16 forwards with the default (or 64) chunk run the tcgen05 scan; fp32 and chunk 32 run the
-// SIMT kernels.  The backward is SIMT.
-bool uses_tensor_cores(const path_attn_desc_t* d, int for_backward) {
-  return !for_backward && d->dtype == PATH_BF16 && (d->chunk == 0 || d->chunk == 64);
+// bf16 with the default (or 64) chunk runs the tcgen05 kernels; fp32 and chunk 32 run the
+// SIMT kernels.
+bool uses_tensor_cores(const path_attn_desc_t* d, int /*for_backward*/) {
+  return d->dtype == PATH_BF16 && (d->chunk == 0 || d->chunk == 64);
 }
 
 // Validates a descriptor; on success fills g for the requested pass.
@@ -27,13 +27,8 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
   if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
   const long long BH = (long long)d->batch * d->heads;
   if (BH > 65535) return PATH_ERR_UNSUPPORTED;
-  int B;
-  if (for_backward) {
-    B = 32;
-  } else {
-    if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
-    B = d->chunk ? d->chunk : 64;
-  }
+  if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
+  int B = for_backward ? 32 : (d->chunk ? d->chunk : 64);
   // The tensor-core path scans 64-row key chunks and 128-row query tiles.
   if (uses_tensor_cores(d, for_backward)) B = 64;
   long long nc = (d->seqlen + B - 1) / B;
@@ -94,7 +89,8 @@ PATH_API int path_attn_chunk(const path_attn_desc_t* desc, int for_backward) {
 PATH_API size_t path_attn_workspace_size(const path_attn_desc_t* desc, int for_backward) {
   Geom g;
   if (check_desc(desc, for_backward, &g) != PATH_OK) return 0;
-  return for_backward ? bwd_ws_layout(g).total : fwd_ws_total(desc, g);
+  if (for_backward) return uses_tensor_cores(desc, 1) ? tc_layout(desc, true).total : bwd_ws_layout(g).total;
+  return fwd_ws_total(desc, g);
 }
 
 PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q,
@@ -159,6 +155,12 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
   CHECK_PTR(dbeta);
   if (log_f || dlog_f) return PATH_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  if (uses_tensor_cores(desc, 1)) {
+    const TcWs tw = tc_layout(desc, true);
+    if (ws_bytes < tw.total) return PATH_ERR_WORKSPACE;
+    return cuda_status(launch_bwd_tc(tw, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, (char*)ws, phases,
+                                     (cudaStream_t)stream));
+  }
   const BwdWs lay = bwd_ws_layout(g);
   if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,

@@ -1,0 +1,617 @@
+// Tensor-core backward of PaTH attention (bf16 operands, fp32 accumulation).
+//
+// The pages give no backward; this is the exact derivative of the blockwise forward of the
+// PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6–§2.7, on 128-row query tiles and
+// 64-row key chunks.  For query tile T the forward visits key chunks c_0 > c_1 > ... with the
+// transported queries Z_0 = Q<-_T, Z_{n+1} = Z_n F_{c_n}^T.  The backward
+//   1. (zchain) recomputes and stores every Z_n of every tile (bf16, swizzled 128x64 images);
+//   2. (scan) walks the steps in reverse (ascending c) with G_{nsteps} = 0:
+//        P = exp(scale Z_n K->_c^T - lse), dP = dO V_c^T, dS = scale P (dP - D)
+//        dV_c += P^T dO,  dK->_c += dS^T Z_n,  dF_c += G_{n+1}^T Z_n,
+//        G_n = dS K->_c + G_{n+1} F_c,     dQ<-_T = G_0,
+//      the chunk sums dV, dK->, dF being added across tiles with bulk fp32 reductions;
+//   3. (convert) maps the chunk-64 gradients onto the chunk-32 quantities the UT backward
+//      works with, including the block of b-rows against a-keys inside each 64-chunk.
+#include "internal.h"
+#include "dev_common.cuh"
+#include "tc_common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace pathattn {
+
+bool make_map_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);  // fwd_tc.cu
+
+namespace {
+using namespace tc;
+
+constexpr int BQ = 128;
+constexpr int BK = 64;
+constexpr int D = kHeadDim;
+constexpr uint32_t ZTILE = BQ * 128;  // bytes of one 128x64 bf16 tile
+
+__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int step_chunk(bool has_partial, int T, int n) {
+  return has_partial ? 2 * T - n : 2 * T - 1 - n;
+}
+
+// ============================ Z chain ============================
+constexpr int ZC_NSTAGE = 3;
+struct __align__(1024) ZcSmem {
+  uint8_t z[2][ZTILE];
+  uint8_t f[ZC_NSTAGE][BK * 128];
+  uint64_t full[ZC_NSTAGE], empty[ZC_NSTAGE];
+  uint64_t z_init, z_ready, zp_full;
+  uint32_t tmem_base;
+};
+
+struct ZcParams {
+  int L, Lp, nc, BH, ntiles;
+  uint8_t* zs;
+  int* err;
+};
+
+__global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ CUtensorMap tm_ql,
+                                                        const __grid_constant__ CUtensorMap tm_f,
+                                                        const ZcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  ZcSmem& s = *reinterpret_cast<ZcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
+  const int bh = (int)(blockIdx.x % p.BH);
+  const bool has_partial = (2 * T + 1) * BK < p.L;
+  const int nsteps = (has_partial ? 1 : 0) + 2 * T;
+  uint8_t* zbase = p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * ZTILE;
+  if (nsteps == 0) return;
+
+  if (tid == 0) {
+    for (int k = 0; k < ZC_NSTAGE; ++k) {
+      mbar_init(&s.full[k], 1);
+      mbar_init(&s.empty[k], 1);
+    }
+    mbar_init(&s.z_init, 1);
+    mbar_init(&s.z_ready, 1);
+    mbar_init(&s.zp_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 4) tmem_alloc(&s.tmem_base, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.z_init, ZTILE);
+      tma_load_2d(s.z[0], &tm_ql, 0, bh * p.Lp + T * BQ, &s.z_init);
+      const int nmma = nsteps - 1;
+      for (int m = 0; m < nmma && m < ZC_NSTAGE; ++m) {
+        mbar_arrive_expect_tx(&s.full[m], BK * 128);
+        tma_load_2d(s.f[m], &tm_f, 0, (bh * p.nc + step_chunk(has_partial, T, m)) * D, &s.full[m]);
+      }
+      const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+      for (int n = 0; n < nmma; ++n) {
+        const int st = n % ZC_NSTAGE;
+        if (!mbar_wait(&s.full[st], (n / ZC_NSTAGE) & 1, p.err, 11)) break;
+        if (!mbar_wait(&s.z_ready, n & 1, p.err, 12)) break;
+        tc_fence_after();
+        const uint32_t za = smem_u32(s.z[n & 1]), fa = smem_u32(s.f[st]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tb, sdesc_sw128(za + 32 * k, 1024, 16), sdesc_sw128(fa + 32 * k, 1024, 16), idesc, k > 0);
+        mma_commit(&s.empty[st]);
+        mma_commit(&s.zp_full);
+        const int m = n + ZC_NSTAGE;
+        if (m < nmma) {
+          if (!mbar_wait(&s.empty[st], (n / ZC_NSTAGE) & 1, p.err, 13)) break;
+          mbar_arrive_expect_tx(&s.full[st], BK * 128);
+          tma_load_2d(s.f[st], &tm_f, 0, (bh * p.nc + step_chunk(has_partial, T, m)) * D, &s.full[st]);
+        }
+      }
+    }
+  } else {
+    const int r = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    bool ok = mbar_wait(&s.z_init, 0, p.err, 14);
+    for (int n = 0; ok && n < nsteps; ++n) {
+      uint8_t* cur = s.z[n & 1];
+      fence_proxy_async_smem();
+      wg_sync();
+      if (r == 0) {
+        bulk_store(zbase + (size_t)n * ZTILE, cur, ZTILE);
+        bulk_commit();
+        if (n + 1 < nsteps) mbar_arrive(&s.z_ready);
+      }
+      if (n + 1 == nsteps) break;
+      if (!mbar_wait(&s.zp_full, n & 1, p.err, 15)) { ok = false; break; }
+      tc_fence_after();
+      uint8_t* nxt = s.z[(n + 1) & 1];
+      if (r == 0) bulk_wait_read0();  // the store of step n-1 read `nxt`
+      wg_sync();
+      const bool active = !(has_partial && n == 0 && r < 64);
+      uint32_t a[32], b[32];
+      tmem_ld32(tb + lane_off, a);
+      tmem_ld32(tb + lane_off + 32, b);
+      tmem_ld_wait();
+      uint8_t* row = nxt + r * 128;
+      if (active) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* src = (q < 4) ? (a + 8 * q) : (b + 8 * (q - 4));
+          uint4 pk;
+          pk.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+          pk.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+          pk.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+          pk.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = pk;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(cur + r * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) reinterpret_cast<uint4*>(row)[q] = src[q];
+      }
+      tc_fence_before();
+    }
+    if (r == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tb, 64);
+  }
+}
+
+// ============================ adjoint scan ============================
+constexpr int BS_NSTAGE = 2;
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DK = 256, TM_DF = 320;
+
+struct __align__(1024) BsStage {
+  uint8_t z[ZTILE];        // Z_n
+  uint8_t kr[BK * 128];    // K->_c
+  uint8_t v[BK * 128];     // V_c
+  uint8_t f[BK * 128];     // F_c
+};
+struct __align__(1024) BsSmem {
+  uint8_t dO[ZTILE];
+  BsStage st[BS_NSTAGE];
+  uint8_t ps[ZTILE];       // P  (bf16, rows x keys)
+  uint8_t ds[ZTILE];       // dS (bf16, rows x keys), scale included
+  uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d)
+  float stash[64 * D];     // fp32 G_1 of the lower rows (tile with a partial step)
+  float stg[3][64 * D];    // dV, dK->, dF of the step (fp32, row-major) for the bulk reductions
+  uint64_t full[BS_NSTAGE], empty[BS_NSTAGE];
+  uint64_t do_full, sp_full, ps_ready, g_full;
+  uint32_t tmem_base;
+};
+
+struct BsParams {
+  int L, Lp, nc, BH, ntiles;
+  float scale, scl;
+  const float* lse;
+  const float* Dv;
+  const uint8_t* zs;
+  float* dql;   // [BH][Lp][64]  dQ<- (written)
+  float* dkr;   // [BH][Lp][64]  dK-> (accumulated)
+  float* dv;    // [BH][Lp][64]  dV   (accumulated)
+  float* df;    // [BH][nc][64][64] dF (accumulated)
+  int* err;
+};
+
+__device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const float* x) {
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 pk;
+    pk.x = pack_bf16(x[8 * q], x[8 * q + 1]);
+    pk.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
+    pk.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
+    pk.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
+    *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = pk;
+  }
+}
+
+__global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
+                                                            const __grid_constant__ CUtensorMap tm_kr,
+                                                            const __grid_constant__ CUtensorMap tm_v,
+                                                            const __grid_constant__ CUtensorMap tm_f,
+                                                            const BsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  BsSmem& s = *reinterpret_cast<BsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
+  const int bh = (int)(blockIdx.x % p.BH);
+  const bool has_partial = (2 * T + 1) * BK < p.L;
+  const int nsteps = (has_partial ? 1 : 0) + 2 * T;
+  const uint8_t* zbase = p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * ZTILE;
+
+  if (nsteps == 0) {  // no earlier chunk: dQ<- of the tile is zero
+    for (int idx = tid; idx < BQ * D; idx += blockDim.x)
+      p.dql[((size_t)bh * p.Lp + (size_t)T * BQ) * D + idx] = 0.f;
+    return;
+  }
+  if (tid == 0) {
+    for (int k = 0; k < BS_NSTAGE; ++k) {
+      mbar_init(&s.full[k], 1);
+      mbar_init(&s.empty[k], 1);
+    }
+    mbar_init(&s.do_full, 1);
+    mbar_init(&s.sp_full, 1);
+    mbar_init(&s.ps_ready, 128);
+    mbar_init(&s.g_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) tmem_alloc(&s.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+
+  if (warp == 4) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&s.do_full, ZTILE);
+      tma_load_2d(s.dO, &tm_do, 0, bh * p.L + T * BQ, &s.do_full);
+      for (int k = 0; k < nsteps; ++k) {
+        const int si = k % BS_NSTAGE;
+        if (k >= BS_NSTAGE && !mbar_wait(&s.empty[si], ((k / BS_NSTAGE) - 1) & 1, p.err, 21)) break;
+        const int n = nsteps - 1 - k;
+        const int c = step_chunk(has_partial, T, n);
+        BsStage& S = s.st[si];
+        mbar_arrive_expect_tx(&s.full[si], ZTILE + 3 * BK * 128);
+        bulk_load(S.z, zbase + (size_t)n * ZTILE, ZTILE, &s.full[si]);
+        tma_load_2d(S.kr, &tm_kr, 0, bh * p.Lp + c * BK, &s.full[si]);
+        tma_load_2d(S.v, &tm_v, 0, bh * p.L + c * BK, &s.full[si]);
+        tma_load_2d(S.f, &tm_f, 0, (bh * p.nc + c) * D, &s.full[si]);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t i_rk = idesc_bf16(128, 64, 0, 0);   // [128 x 64] = A(K-major) B(K-major)^T
+      const uint32_t i_rm = idesc_bf16(128, 64, 0, 1);   // [128 x 64] = A(K-major) B(MN-major)
+      const uint32_t i_tt = idesc_bf16(64, 64, 1, 1);    // [64 x 64]  = A(MN-major)^T-style product
+      const uint32_t a_do = smem_u32(s.dO), a_ps = smem_u32(s.ps), a_ds = smem_u32(s.ds), a_gs = smem_u32(s.gs);
+      bool ok = mbar_wait(&s.do_full, 0, p.err, 22);
+      for (int k = 0; ok && k < nsteps; ++k) {
+        const int si = k % BS_NSTAGE;
+        const int n = nsteps - 1 - k;
+        const bool partial = has_partial && n == 0;
+        if (!mbar_wait(&s.full[si], (k / BS_NSTAGE) & 1, p.err, 23)) { ok = false; break; }
+        tc_fence_after();
+        const BsStage& S = s.st[si];
+        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v), a_f = smem_u32(S.f);
+        // S = Z K->^T, dP = dO V^T
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tb + TM_S, sdesc_sw128(a_z + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 32 * kk, 1024, 16), i_rk, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tb + TM_DP, sdesc_sw128(a_do + 32 * kk, 1024, 16), sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
+        mma_commit(&s.sp_full);
+        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
+        tc_fence_after();
+        // dV = P^T dO, dK-> = dS^T Z  (M = 64 keys, K = 128 rows)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tb + TM_DV, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tb + TM_DK, sdesc_sw128(a_ds + 2048 * kk, 1024, 0), sdesc_sw128(a_z + 2048 * kk, 1024, 0), i_tt, kk > 0);
+        // G_n = dS K->_c + G_{n+1} F_c
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tb + TM_G, sdesc_sw128(a_ds + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 2048 * kk, 1024, 0), i_rm, kk > 0);
+        if (k > 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tb + TM_G, sdesc_sw128(a_gs + 32 * kk, 1024, 16), sdesc_sw128(a_f + 2048 * kk, 1024, 0), i_rm, 1);
+          // dF_c = G_{n+1}^T Z_n over the rows that crossed chunk c
+          const uint32_t off = partial ? 64 * 128 : 0;
+          const int nk = partial ? 4 : 8;
+          for (int kk = 0; kk < nk; ++kk)
+            mma_ss(tb + TM_DF, sdesc_sw128(a_gs + off + 2048 * kk, 1024, 0),
+                   sdesc_sw128(a_z + off + 2048 * kk, 1024, 0), i_tt, kk > 0);
+        }
+        mma_commit(&s.empty[si]);
+        mma_commit(&s.g_full);
+      }
+    }
+  } else {
+    // ---------------- warpgroup: thread r owns query row r of the tile ----------------
+    const int r = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int grow = T * BQ + r;
+    const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
+    const float lse2 = grow < p.L ? p.lse[(size_t)bh * p.L + grow] * kLog2e : INFINITY;
+    const float Dr = p.Dv[wrow];
+    if (r < 64)
+      for (int j = 0; j < D; ++j) s.stash[r * D + j] = 0.f;
+    for (int k = 0; k < nsteps; ++k) {
+      const int n = nsteps - 1 - k;
+      const bool partial = has_partial && n == 0;
+      const int c = step_chunk(has_partial, T, n);
+      const bool active = !(partial && r < 64);
+      if (!mbar_wait(&s.sp_full, k & 1, p.err, 25)) break;
+      tc_fence_after();
+      {
+        uint32_t sa[32], sb[32], da[32], db[32];
+        tmem_ld32(tb + lane_off + TM_S, sa);
+        tmem_ld32(tb + lane_off + TM_S + 32, sb);
+        tmem_ld32(tb + lane_off + TM_DP, da);
+        tmem_ld32(tb + lane_off + TM_DP + 32, db);
+        tmem_ld_wait();
+        float pv[64], dsv[64];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
+          const float p1 = active ? fast_exp2(fmaf(__uint_as_float(sb[j]), p.scl, -lse2)) : 0.f;
+          pv[j] = p0;
+          pv[32 + j] = p1;
+          dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+          dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
+        }
+        store_row_bf16_sw(s.ps, r, pv);
+        store_row_bf16_sw(s.ds, r, dsv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.ps_ready);
+      if (!mbar_wait(&s.g_full, k & 1, p.err, 26)) break;
+      tc_fence_after();
+      // G_n
+      {
+        uint32_t ga[32], gb[32];
+        tmem_ld32(tb + lane_off + TM_G, ga);
+        tmem_ld32(tb + lane_off + TM_G + 32, gb);
+        tmem_ld_wait();
+        float g[64];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] = __uint_as_float(ga[j]);
+          g[32 + j] = __uint_as_float(gb[j]);
+        }
+        if (partial && r < 64) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) g[j] = s.stash[r * D + j];
+        }
+        if (has_partial && n == 1 && r < 64) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) s.stash[r * D + j] = g[j];
+        }
+        if (n == 0) {
+          float4* dst = reinterpret_cast<float4*>(p.dql + wrow * D);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[j] = make_float4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
+        } else {
+          store_row_bf16_sw(s.gs, r, g);
+        }
+      }
+      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions
+      if (r == 0) bulk_wait_read0();
+      wg_sync();
+      {
+        const int mrow = 16 * warp + lane;  // M=64 accumulator: row 16w+l sits in lane l of warp w
+        uint32_t a[32], b[32];
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          if (t == 2 && k == 0) break;
+          const uint32_t col = t == 0 ? TM_DV : (t == 1 ? TM_DK : TM_DF);
+          tmem_ld32(tb + lane_off + col, a);
+          tmem_ld32(tb + lane_off + col + 32, b);
+          tmem_ld_wait();
+          if (lane < 16) {
+            float4* dst = reinterpret_cast<float4*>(s.stg[t] + mrow * D);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              dst[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                                   __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
+              dst[8 + j] = make_float4(__uint_as_float(b[4 * j]), __uint_as_float(b[4 * j + 1]),
+                                       __uint_as_float(b[4 * j + 2]), __uint_as_float(b[4 * j + 3]));
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      wg_sync();
+      if (r == 0) {
+        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK;
+        bulk_reduce_add_f32(p.dv + crow * D, s.stg[0], BK * D * 4);
+        bulk_reduce_add_f32(p.dkr + crow * D, s.stg[1], BK * D * 4);
+        if (k > 0) bulk_reduce_add_f32(p.df + ((size_t)bh * p.nc + c) * D * D, s.stg[2], D * D * 4);
+        bulk_commit();
+      }
+    }
+    if (r == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+// ============================ chunk-64 -> chunk-32 gradients ============================
+// With a, b the two 32-chunks of 64-chunk c (row-vector conventions as in the merge):
+//   Q<-64 = [Q<-32_a ; Q<-32_b F_a^T]  =>  dQ<-32_a = dQ<-64_a,  dQ<-32_b = dQ<-64_b F_a,
+//                                          dF_a += dQ<-64_b^T Q<-32_b
+//   K->64 = [K->32_a F_b ; K->32_b]    =>  dK->32_b = dK->64_b,  dK->32_a = dK->64_a F_b^T,
+//                                          dF_b += K->32_a^T dK->64_a
+//   F64 = F_a F_b                      =>  dF_a += dF64 F_b^T,  dF_b += F_a^T dF64
+// plus the attention block of b-rows against a-keys (logits Q<-32_b K->32_a^T), whose
+// gradients go to dQ<-32_b, dK->32_a and dV_a.
+constexpr int CV_NT = 256;
+constexpr int DS = D + 1;
+struct CvSmem {
+  float fa[D * DS], fb[D * DS], dF[D * DS];
+  float qb[32 * DS], ka[32 * DS], dqb[32 * DS], dka[32 * DS], dob[32 * DS], va[32 * DS];
+  float p[32 * 33], ds[32 * 33];
+};
+
+__global__ void __launch_bounds__(CV_NT) convert_kernel(
+    Geom g, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
+    const float* __restrict__ Dv, const float* __restrict__ ql32, const float* __restrict__ kr32,
+    const float* __restrict__ f32, const float* __restrict__ dql64, const float* __restrict__ dkr64,
+    const float* __restrict__ df64, float* __restrict__ dv, float* __restrict__ dql32, float* __restrict__ dkr32,
+    float* __restrict__ df32) {
+  extern __shared__ float smraw[];
+  CvSmem& s = *reinterpret_cast<CvSmem*>(smraw);
+  const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int nc32 = g.Lp / 32, nc64 = g.Lp / 64;
+  const size_t row0 = (size_t)bh * g.Lp + (size_t)c * 64;
+  const float* Fa = f32 + ((size_t)bh * nc32 + 2 * c) * D * D;
+  const float* Fb = Fa + D * D;
+  const float* dF64 = df64 + ((size_t)bh * nc64 + c) * D * D;
+  for (int idx = tid; idx < D * D; idx += CV_NT) {
+    const int i = idx / D, j = idx % D;
+    s.fa[i * DS + j] = Fa[idx];
+    s.fb[i * DS + j] = Fb[idx];
+    s.dF[i * DS + j] = dF64[idx];
+  }
+  for (int idx = tid; idx < 32 * D; idx += CV_NT) {
+    const int r = idx / D, cc = idx % D;
+    s.qb[r * DS + cc] = ql32[(row0 + 32 + r) * D + cc];
+    s.ka[r * DS + cc] = kr32[(row0 + r) * D + cc];
+    s.dqb[r * DS + cc] = dql64[(row0 + 32 + r) * D + cc];
+    s.dka[r * DS + cc] = dkr64[(row0 + r) * D + cc];
+    const int gb = c * 64 + 32 + r, ga = c * 64 + r;
+    s.dob[r * DS + cc] = gb < g.L ? __bfloat162float(dO[((size_t)bh * g.L + gb) * D + cc]) : 0.f;
+    s.va[r * DS + cc] = ga < g.L ? __bfloat162float(v[((size_t)bh * g.L + ga) * D + cc]) : 0.f;
+  }
+  __syncthreads();
+  // cross block: rows of b (i) against keys of a (j)
+  for (int idx = tid; idx < 32 * 32; idx += CV_NT) {
+    const int i = idx / 32, j = idx % 32;
+    const int gi = c * 64 + 32 + i;
+    float sdot = 0.f, dp = 0.f;
+#pragma unroll 16
+    for (int k = 0; k < D; ++k) {
+      sdot += s.qb[i * DS + k] * s.ka[j * DS + k];
+      dp += s.dob[i * DS + k] * s.va[j * DS + k];
+    }
+    float pij = 0.f;
+    if (gi < g.L) pij = fast_exp2(sdot * g.scale * kLog2e - lse[(size_t)bh * g.L + gi] * kLog2e);
+    s.p[i * 33 + j] = pij;
+    s.ds[i * 33 + j] = g.scale * pij * (dp - Dv[row0 + 32 + i]);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < 32 * D; idx += CV_NT) {
+    const int r = idx / D, n = idx % D;
+    // dQ<-32: rows a copy, rows b = dQ<-64_b F_a + dS K->32_a
+    dql32[(row0 + r) * D + n] = dql64[(row0 + r) * D + n];
+    float qb = 0.f;
+#pragma unroll 16
+    for (int k = 0; k < D; ++k) qb += s.dqb[r * DS + k] * s.fa[k * DS + n];
+    for (int j = 0; j < 32; ++j) qb += s.ds[r * 33 + j] * s.ka[j * DS + n];
+    dql32[(row0 + 32 + r) * D + n] = qb;
+    // dK->32: rows b copy, rows a = dK->64_a F_b^T + dS^T Q<-32_b
+    dkr32[(row0 + 32 + r) * D + n] = dkr64[(row0 + 32 + r) * D + n];
+    float ka = 0.f;
+#pragma unroll 16
+    for (int k = 0; k < D; ++k) ka += s.dka[r * DS + k] * s.fb[n * DS + k];
+    for (int i = 0; i < 32; ++i) ka += s.ds[i * 33 + r] * s.qb[i * DS + n];
+    dkr32[(row0 + r) * D + n] = ka;
+    // dV rows of a gain P^T dO_b
+    float va = 0.f;
+    for (int i = 0; i < 32; ++i) va += s.p[i * 33 + r] * s.dob[i * DS + n];
+    dv[(row0 + r) * D + n] += va;
+  }
+  float* dFa = df32 + ((size_t)bh * nc32 + 2 * c) * D * D;
+  float* dFb = dFa + D * D;
+  for (int idx = tid; idx < D * D; idx += CV_NT) {
+    const int n = idx / D, k = idx % D;
+    float a = 0.f, b = 0.f;
+#pragma unroll 16
+    for (int m = 0; m < D; ++m) {
+      a += s.dF[n * DS + m] * s.fb[k * DS + m];   // dF64 F_b^T
+      b += s.fa[m * DS + n] * s.dF[m * DS + k];   // F_a^T dF64
+    }
+    for (int i = 0; i < 32; ++i) {
+      a += s.dqb[i * DS + n] * s.qb[i * DS + k];  // dQ<-64_b^T Q<-32_b
+      b += s.ka[i * DS + n] * s.dka[i * DS + k];  // K->32_a^T dK->64_a
+    }
+    dFa[idx] = a;
+    dFb[idx] = b;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
+                          const float* beta, const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st) {
+  cudaError_t e;
+  const Geom& g = w.g64;
+  const size_t rows = (size_t)g.BH * g.Lp;
+  const int nt = g.Lp / BQ;
+  int* err = (int*)(ws + w.p64.err);
+  if (phases & 1) {
+    if ((e = cudaMemsetAsync(ws + w.dkr64, 0, rows * D * 4, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws + w.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws + w.df64, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_dot(w.g32, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
+    if ((e = launch_prep_simt(true, w.g32, q, k, v, wv, beta, nullptr, ws, w.p32, false, st)) != cudaSuccess) return e;
+    if ((e = launch_merge64(w, v, nullptr, ws, false, st)) != cudaSuccess) return e;
+    CUtensorMap m_ql, m_f;
+    if (!make_map_rows64(&m_ql, ws + w.p64.ql, rows, BQ) ||
+        !make_map_rows64(&m_f, ws + w.p64.f, (uint64_t)g.BH * g.nc * D, D))
+      return cudaErrorInvalidValue;
+    ZcParams zp{g.L, g.Lp, g.nc, g.BH, nt, (uint8_t*)(ws + w.zs), err};
+    const size_t smem = sizeof(ZcSmem) + 1024;
+    if ((e = cudaFuncSetAttribute(zchain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    zchain_tc_kernel<<<(unsigned)((long)nt * g.BH), 160, smem, st>>>(m_ql, m_f, zp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (phases & 2) {
+    CUtensorMap m_do, m_kr, m_v, m_f;
+    if (!make_map_rows64(&m_do, dO, (uint64_t)g.BH * g.L, BQ) ||
+        !make_map_rows64(&m_kr, ws + w.p64.kr, rows, BK) || !make_map_rows64(&m_v, v, (uint64_t)g.BH * g.L, BK) ||
+        !make_map_rows64(&m_f, ws + w.p64.f, (uint64_t)g.BH * g.nc * D, D))
+      return cudaErrorInvalidValue;
+    BsParams bp;
+    bp.L = g.L;
+    bp.Lp = g.Lp;
+    bp.nc = g.nc;
+    bp.BH = g.BH;
+    bp.ntiles = nt;
+    bp.scale = g.scale;
+    bp.scl = g.scale * kLog2e;
+    bp.lse = lse;
+    bp.Dv = (const float*)(ws + w.Dv);
+    bp.zs = (const uint8_t*)(ws + w.zs);
+    bp.dql = (float*)(ws + w.dql64);
+    bp.dkr = (float*)(ws + w.dkr64);
+    bp.dv = (float*)(ws + w.dv);
+    bp.df = (float*)(ws + w.df64);
+    bp.err = err;
+    const size_t smem = sizeof(BsSmem) + 1024;
+    if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), 192, smem, st>>>(m_do, m_kr, m_v, m_f, bp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (phases & 4) {
+    const size_t smem = sizeof(CvSmem);
+    if ((e = cudaFuncSetAttribute(convert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    convert_kernel<<<dim3(g.nc, g.BH), CV_NT, smem, st>>>(
+        g, (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO, lse, (const float*)(ws + w.Dv),
+        (const float*)(ws + w.p32.ql), (const float*)(ws + w.p32.kr), (const float*)(ws + w.p32.f),
+        (const float*)(ws + w.dql64), (const float*)(ws + w.dkr64), (const float*)(ws + w.df64), (float*)(ws + w.dv),
+        (float*)(ws + w.dql32), (float*)(ws + w.dkr32), (float*)(ws + w.df32));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_prep_bwd(w.g32, q, k, v, wv, beta, lse, dO, (const float*)(ws + w.Dv), (const float*)(ws + w.dql32),
+                             (const float*)(ws + w.dkr32), (const float*)(ws + w.dv), (const float*)(ws + w.df32), dq,
+                             dk, dv, dw, dbeta, st)) != cudaSuccess)
+      return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace pathattn

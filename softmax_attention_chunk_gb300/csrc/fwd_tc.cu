@@ -289,6 +289,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
 }
 
+}  // namespace
+
 // ---------------- host side ----------------
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -316,7 +318,6 @@ bool make_map_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
 
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, cudaStream_t st) {

@@ -172,6 +172,19 @@ cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const vo
                             void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
                             cudaStream_t st);
 
+// bf16 helpers shared by the tensor-core backward: D_i = dO_i . o_i, and the chunk-32 UT
+// backward (diagonal blocks + chain rule through the UT quantities) writing the gradients.
+cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* Dv, cudaStream_t st);
+cudaError_t launch_prep_bwd(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                            const float* beta, const float* lse, const void* dO, const float* Dv,
+                            const float* dql, const float* dkr, const float* dvacc, const float* dfacc,
+                            void* dq, void* dk, void* dv, void* dw, float* dbeta, cudaStream_t st);
+// Tensor-core backward (bf16).  phases: 1 = prepare (accumulators, D_i, chunk-32 UT quantities,
+// chunk-64 merge, Z chain), 2 = adjoint scan, 4 = chunk conversion + UT backward.
+cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
+                          const float* beta, const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st);
+
 // Decode step.
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
                           const void* q, const void* k, const void* v, const void* w,
