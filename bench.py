@@ -40,6 +40,48 @@ L2_BYTES = 129 * 2**20
 WORKLOAD = ("PaTH fwd+bwd, batch 32, 32 heads, d=64, L=4096, bf16 (beta fp32, 5% near-reflection beta), "
             "per rank")
 FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # FP32 FMA lanes x 2 x max SM clock
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rate
+D = 64
+
+
+# Algorithmic multiply-adds of the kernels of the bf16 tensor-core path (2 flops each).
+def prep32_macs(diag, B=32):
+    return (7 + diag) * B * B * D + 3 * B ** 3 + D * D * B
+
+
+def merge64_macs(diag):
+    return D ** 3 + 2 * 32 * D * D + diag * (2 * 32 * 32 * D)
+
+
+def convert_macs():
+    return 2 * 32 * 32 * D + 2 * 32 * D * D + 3 * 32 * D * 32 + 2 * D ** 3 + 2 * D * D * 32
+
+
+def ut_bwd32_macs(B=32):
+    return 21 * B * B * D + 8 * B ** 3 + 2 * B * D * D
+
+
+def tiles_steps(L):
+    """(number of 128-row query tiles, sum over tiles of scan steps) for one head."""
+    nt = (L + 127) // 128
+    steps = sum(2 * t + (1 if (2 * t + 1) * 64 < L else 0) for t in range(nt))
+    return nt, steps
+
+
+def phase_roofline(L, BH, pk):
+    """Per phase of the fwd+bwd step: (algorithmic flops per launch, bound, peak TFLOP/s)."""
+    nc32, nc64 = (L + 127) // 128 * 4, (L + 127) // 128 * 2
+    nt, steps = tiles_steps(L)
+    npairs = nc64 * (nc64 - 1) // 2
+    tf32 = pk["bf16"] * TF32_OVER_BF16
+    return {
+        "fwd_prepare": (2 * BH * (nc32 * prep32_macs(1) + nc64 * merge64_macs(1)), "tensor(tf32)", tf32),
+        "fwd_scan": (BH * npairs * (4 * 64 * 64 * D + 2 * 64 * D * D), "tensor", pk["bf16"]),
+        "bwd_prepare": (2 * BH * (nc32 * prep32_macs(0) + nc64 * merge64_macs(0) + (steps - nt) * 128 * D * D),
+                        "tensor(tf32)", tf32),
+        "bwd_scan": (BH * npairs * (10 * 64 * 64 * D + 4 * 64 * D * D), "tensor", pk["bf16"]),
+        "bwd_finish": (2 * BH * (nc64 * convert_macs() + nc32 * ut_bwd32_macs()), "tensor(tf32)", tf32),
+    }
 
 
 def parse():
@@ -277,16 +319,27 @@ def run_ours(args):
     fa_flops_step = BH * 7 * L * L * d
     value = ws * flops_step / (ms_step * 1e-3) / 1e12
 
-    # dominant kernel roofline (the scan phases each run one kernel)
-    dom = max(("fwd_scan", "bwd_scan"), key=lambda n: phase_ms[n])
-    npairs_f = (math.ceil(L / B_f) * (math.ceil(L / B_f) - 1)) // 2
-    npairs_b = (math.ceil(L / B_b) * (math.ceil(L / B_b) - 1)) // 2
-    alg = {"fwd_scan": BH * npairs_f * (4 * B_f * B_f * d + 2 * B_f * d * d),
-           "bwd_scan": BH * npairs_b * (10 * B_b * B_b * d + 4 * B_b * d * d)}
-    achieved = alg[dom] / (phase_ms[dom] * 1e-3) / 1e12
-    roofline = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": FP32_SIMT_PEAK_TFLOPS,
-                "unit": "TFLOP/s", "frac": achieved / FP32_SIMT_PEAK_TFLOPS, "traffic": None,
-                "peak_source": "FP32 CUDA-core peak 152 SM x 128 lanes x 2 flop x 2070 MHz"}
+    # roofline per phase; the dominant phase is reported as "roofline"
+    pr = phase_roofline(L, BH, pk)
+    phases = {}
+    for n, ms in phase_ms.items():
+        fl, bound, peak = pr[n]
+        ach = fl / (ms * 1e-3) / 1e12
+        phases[n] = {"ms": ms, "share": ms / sum(phase_ms.values()), "flops": fl, "achieved": ach,
+                     "bound": bound, "peak": peak, "frac": ach / peak}
+    dom = max(phase_ms, key=lambda n: phase_ms[n])
+    kernels = {"fwd_prepare": "prep_simt_kernel (UT, chunk 32) + merge64_kernel",
+               "fwd_scan": "fwd_scan_tc_kernel (tcgen05)",
+               "bwd_prepare": "bwd_dot + prep_simt_kernel + merge64_kernel + zchain_tc_kernel",
+               "bwd_scan": "bwd_scan_tc_kernel (tcgen05)",
+               "bwd_finish": "convert_kernel + prep_bwd_simt_kernel (UT backward)"}
+    d = phases[dom]
+    roofline = {"kernel": f"{dom}: {kernels[dom]}", "bound": "tensor", "achieved": d["achieved"], "peak": d["peak"],
+                "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
+                "peak_source": ("measured bf16 dense" if d["bound"] == "tensor" else
+                                "measured bf16 dense x nominal TF32/bf16 ratio 1.1/2.25") + f" ({pk['src']})"}
+    scan_roofline = {n: {"achieved": phases[n]["achieved"], "peak": phases[n]["peak"], "frac": phases[n]["frac"],
+                         "unit": "TFLOP/s", "of": "measured bf16 dense"} for n in ("fwd_scan", "bwd_scan")}
 
     # end-to-end through the public API: pinned host inputs in, outputs and gradients out
     outs_h = {"o": torch.empty_like(o, device="cpu").pin_memory(),
@@ -333,8 +386,8 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (6 x 512 MiB per step)"},
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
-                "phase_ms": phase_ms, "roofline": roofline, "e2e": e2e, "clocks": clocks_rec,
-                "gpu_launches": 6 * args.steps, "memset_ops": 3 * args.steps,
+                "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "e2e": e2e,
+                "clocks": clocks_rec, "gpu_launches": 10 * args.steps, "memset_ops": 5 * args.steps,
                 "peaks": pk, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:

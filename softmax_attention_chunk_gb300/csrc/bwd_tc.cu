@@ -15,6 +15,7 @@
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
+#include "smem_mm.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -483,60 +484,40 @@ __global__ void __launch_bounds__(CV_NT) convert_kernel(
     s.va[r * DS + cc] = ga < g.L ? __bfloat162float(v[((size_t)bh * g.L + ga) * D + cc]) : 0.f;
   }
   __syncthreads();
-  // cross block: rows of b (i) against keys of a (j)
+  // cross block: rows of b (i) against keys of a (j): logits into p, dP into ds
+  smem_mm<32, 32, D, false, true, true>(s.qb, DS, s.ka, DS, [&](int i, int j, float x) { s.p[i * 33 + j] = x; });
+  smem_mm<32, 32, D, false, true, true>(s.dob, DS, s.va, DS, [&](int i, int j, float x) { s.ds[i * 33 + j] = x; });
+  __syncthreads();
   for (int idx = tid; idx < 32 * 32; idx += CV_NT) {
     const int i = idx / 32, j = idx % 32;
     const int gi = c * 64 + 32 + i;
-    float sdot = 0.f, dp = 0.f;
-#pragma unroll 16
-    for (int k = 0; k < D; ++k) {
-      sdot += s.qb[i * DS + k] * s.ka[j * DS + k];
-      dp += s.dob[i * DS + k] * s.va[j * DS + k];
-    }
     float pij = 0.f;
-    if (gi < g.L) pij = fast_exp2(sdot * g.scale * kLog2e - lse[(size_t)bh * g.L + gi] * kLog2e);
+    if (gi < g.L) pij = fast_exp2(s.p[i * 33 + j] * g.scale * kLog2e - lse[(size_t)bh * g.L + gi] * kLog2e);
     s.p[i * 33 + j] = pij;
-    s.ds[i * 33 + j] = g.scale * pij * (dp - Dv[row0 + 32 + i]);
+    s.ds[i * 33 + j] = g.scale * pij * (s.ds[i * 33 + j] - Dv[row0 + 32 + i]);
   }
   __syncthreads();
+  // dQ<-32: rows a copy, rows b = dQ<-64_b F_a + dS K->32_a
+  // dK->32: rows b copy, rows a = dK->64_a F_b^T + dS^T Q<-32_b ;  dV rows of a += P^T dO_b
   for (int idx = tid; idx < 32 * D; idx += CV_NT) {
     const int r = idx / D, n = idx % D;
-    // dQ<-32: rows a copy, rows b = dQ<-64_b F_a + dS K->32_a
     dql32[(row0 + r) * D + n] = dql64[(row0 + r) * D + n];
-    float qb = 0.f;
-#pragma unroll 16
-    for (int k = 0; k < D; ++k) qb += s.dqb[r * DS + k] * s.fa[k * DS + n];
-    for (int j = 0; j < 32; ++j) qb += s.ds[r * 33 + j] * s.ka[j * DS + n];
-    dql32[(row0 + 32 + r) * D + n] = qb;
-    // dK->32: rows b copy, rows a = dK->64_a F_b^T + dS^T Q<-32_b
     dkr32[(row0 + 32 + r) * D + n] = dkr64[(row0 + 32 + r) * D + n];
-    float ka = 0.f;
-#pragma unroll 16
-    for (int k = 0; k < D; ++k) ka += s.dka[r * DS + k] * s.fb[n * DS + k];
-    for (int i = 0; i < 32; ++i) ka += s.ds[i * 33 + r] * s.qb[i * DS + n];
-    dkr32[(row0 + r) * D + n] = ka;
-    // dV rows of a gain P^T dO_b
-    float va = 0.f;
-    for (int i = 0; i < 32; ++i) va += s.p[i * 33 + r] * s.dob[i * DS + n];
-    dv[(row0 + r) * D + n] += va;
   }
+  float* qout = dql32 + (row0 + 32) * D;
+  float* kout = dkr32 + row0 * D;
+  smem_mm<32, D, D, false, false, true>(s.dqb, DS, s.fa, DS, [&](int i, int n, float x) { qout[i * D + n] = x; });
+  smem_mm<32, D, 32, false, false, true>(s.ds, 33, s.ka, DS, [&](int i, int n, float x) { qout[i * D + n] += x; });
+  smem_mm<32, D, D, false, true, true>(s.dka, DS, s.fb, DS, [&](int j, int n, float x) { kout[j * D + n] = x; });
+  smem_mm<32, D, 32, true, false, true>(s.ds, 33, s.qb, DS, [&](int j, int n, float x) { kout[j * D + n] += x; });
+  smem_mm<32, D, 32, true, false, true>(s.p, 33, s.dob, DS, [&](int j, int n, float x) { dv[(row0 + j) * D + n] += x; });
+  // dF_a = dF64 F_b^T + dQ<-64_b^T Q<-32_b ;  dF_b = F_a^T dF64 + K->32_a^T dK->64_a
   float* dFa = df32 + ((size_t)bh * nc32 + 2 * c) * D * D;
   float* dFb = dFa + D * D;
-  for (int idx = tid; idx < D * D; idx += CV_NT) {
-    const int n = idx / D, k = idx % D;
-    float a = 0.f, b = 0.f;
-#pragma unroll 16
-    for (int m = 0; m < D; ++m) {
-      a += s.dF[n * DS + m] * s.fb[k * DS + m];   // dF64 F_b^T
-      b += s.fa[m * DS + n] * s.dF[m * DS + k];   // F_a^T dF64
-    }
-    for (int i = 0; i < 32; ++i) {
-      a += s.dqb[i * DS + n] * s.qb[i * DS + k];  // dQ<-64_b^T Q<-32_b
-      b += s.ka[i * DS + n] * s.dka[i * DS + k];  // K->32_a^T dK->64_a
-    }
-    dFa[idx] = a;
-    dFb[idx] = b;
-  }
+  smem_mm<D, D, D, false, true, true>(s.dF, DS, s.fb, DS, [&](int n, int k, float x) { dFa[n * D + k] = x; });
+  smem_mm<D, D, 32, true, false, true>(s.dqb, DS, s.qb, DS, [&](int n, int k, float x) { dFa[n * D + k] += x; });
+  smem_mm<D, D, D, true, false, true>(s.fa, DS, s.dF, DS, [&](int n, int k, float x) { dFb[n * D + k] = x; });
+  smem_mm<D, D, 32, true, false, true>(s.ka, DS, s.dka, DS, [&](int n, int k, float x) { dFb[n * D + k] += x; });
 }
 
 }  // namespace

@@ -10,6 +10,7 @@
 // gain T_b.  (PaTH reading notes, cc.laoqi.cc/papers/2505.16381, §2.6 interval form and §2.7.)
 #include "internal.h"
 #include "dev_common.cuh"
+#include "smem_mm.cuh"
 
 namespace pathattn {
 namespace {
@@ -23,6 +24,7 @@ struct MergeSmem {
   float fa[D * DS], fb[D * DS];
   float qb[H32 * DS], ka[H32 * DS], va[H32 * DS];
   float p[H32 * (H32 + 1)];
+  float corr[H32];
 };
 
 template <typename T>
@@ -58,31 +60,19 @@ __global__ void __launch_bounds__(NT) merge64_kernel(
 
   // F64 = F_a F_b
   __nv_bfloat16* fo = f64 + ((size_t)bh * nc64 + c) * D * D;
-  for (int idx = tid; idx < D * D; idx += NT) {
-    const int n = idx / D, k = idx % D;
-    float a = 0.f;
-#pragma unroll 16
-    for (int m = 0; m < D; ++m) a += s.fa[n * DS + m] * s.fb[m * DS + k];
-    fo[idx] = __float2bfloat16_rn(a);
-  }
-  // Q<-64 and K->64
-  for (int idx = tid; idx < 64 * D; idx += NT) {
+  smem_mm<D, D, D, false, false, true>(s.fa, DS, s.fb, DS, [&](int n, int k, float x) { fo[n * D + k] = __float2bfloat16_rn(x); });
+  // Q<-64 = [Q<-32_a ; Q<-32_b F_a^T],  K->64 = [K->32_a F_b ; K->32_b]
+  for (int idx = tid; idx < 32 * D; idx += NT) {
     const int r = idx / D, cc = idx % D;
-    float qv, kv;
-    if (r < 32) {
-      qv = ql32[(row0 + r) * D + cc];
-      kv = 0.f;
-#pragma unroll 16
-      for (int m = 0; m < D; ++m) kv += s.ka[r * DS + m] * s.fb[m * DS + cc];
-    } else {
-      qv = 0.f;
-#pragma unroll 16
-      for (int k = 0; k < D; ++k) qv += s.qb[(r - 32) * DS + k] * s.fa[cc * DS + k];
-      kv = kr32[(row0 + r) * D + cc];
-    }
-    ql64[(row0 + r) * D + cc] = __float2bfloat16_rn(qv);
-    kr64[(row0 + r) * D + cc] = __float2bfloat16_rn(kv);
+    ql64[(row0 + r) * D + cc] = __float2bfloat16_rn(ql32[(row0 + r) * D + cc]);
+    kr64[(row0 + 32 + r) * D + cc] = __float2bfloat16_rn(kr32[(row0 + 32 + r) * D + cc]);
   }
+  smem_mm<H32, D, D, false, true, true>(s.qb, DS, s.fa, DS, [&](int r, int n, float x) {
+    ql64[(row0 + 32 + r) * D + n] = __float2bfloat16_rn(x);
+  });
+  smem_mm<H32, D, D, false, false, true>(s.ka, DS, s.fb, DS, [&](int r, int n, float x) {
+    kr64[(row0 + r) * D + n] = __float2bfloat16_rn(x);
+  });
   const float Ta = fox ? ft32[(size_t)bh * nc32 + 2 * c] : 0.f;
   const float Tb = fox ? ft32[(size_t)bh * nc32 + 2 * c + 1] : 0.f;
   if (fox) {
@@ -100,6 +90,8 @@ __global__ void __launch_bounds__(NT) merge64_kernel(
     dl64[row0 + r] = dl32[row0 + r];
   }
   // rows of b: merge the block against the keys of a
+  smem_mm<H32, H32, D, false, true, true>(s.qb, DS, s.ka, DS, [&](int i, int j, float x) { s.p[i * (H32 + 1) + j] = x; });
+  __syncthreads();
   constexpr int NSUB = NT / H32;  // 8 threads per row
   const int r = tid / NSUB, sub = tid % NSUB;
   const size_t wr = row0 + 32 + r;
@@ -110,10 +102,7 @@ __global__ void __launch_bounds__(NT) merge64_kernel(
 #pragma unroll
   for (int u = 0; u < H32 / NSUB; ++u) {
     const int j = sub + NSUB * u;
-    float dot = 0.f;
-#pragma unroll 16
-    for (int k = 0; k < D; ++k) dot += s.qb[r * DS + k] * s.ka[j * DS + k];
-    float x = dot * scl;
+    float x = s.p[r * (H32 + 1) + j] * scl;
     if (fox) x += (arow + fr32[row0 + j]) * kLog2e;
     if (c * 64 + j >= g.L) x = -INFINITY;  // (never: chunk a is full when b has rows)
     sv[u] = x;
@@ -131,17 +120,16 @@ __global__ void __launch_bounds__(NT) merge64_kernel(
     ls += pj;
   }
   ls = group_sum<NSUB>(ls);
-  __syncwarp();
-  for (int cc = sub; cc < D; cc += NSUB) {
-    float a = dacc32[wr * D + cc] * corr;
-#pragma unroll 8
-    for (int j = 0; j < H32; ++j) a += s.p[r * (H32 + 1) + j] * s.va[j * DS + cc];
-    dacc64[wr * D + cc] = a;
-  }
   if (sub == 0) {
+    s.corr[r] = corr;
     dm64[wr] = mnew;
     dl64[wr] = dl32[wr] * corr + ls;
   }
+  __syncthreads();
+  smem_mm<H32, D, H32, false, false, true>(s.p, H32 + 1, s.va, DS, [&](int i, int cc, float x) {
+    const size_t w2 = row0 + 32 + i;
+    dacc64[w2 * D + cc] = dacc32[w2 * D + cc] * s.corr[i] + x;
+  });
 }
 
 }  // namespace

@@ -10,6 +10,7 @@
 // (Q<-, K->, F, X = U strictLower(W K^T), U = (I + strictLower(D W W^T))^{-1} D).
 #include "internal.h"
 #include "dev_common.cuh"
+#include "smem_mm.cuh"
 
 #include <type_traits>
 
@@ -261,24 +262,14 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   }
   __syncthreads();
 
+  // bf16 inputs: products on TF32 tensor cores; fp32 inputs: exact fp32 loops
+  constexpr bool TC = std::is_same<T, __nv_bfloat16>::value;
   // 2. G = strictLower(WW^T), M1 = lower(QW^T), N2 = strictLower(WK^T), QK^T, dP = dO V^T
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float gg = 0.f, m1 = 0.f, n2 = 0.f, qk = 0.f, dp = 0.f;
-    for (int kk = 0; kk < D; ++kk) {
-      const float wi = sW[i * DS + kk], wj = sW[j * DS + kk], qi = sQ[i * DS + kk], kj = sK[j * DS + kk];
-      gg += wi * wj;
-      m1 += qi * wj;
-      n2 += wi * kj;
-      qk += qi * kj;
-      dp += sdO[i * DS + kk] * sV[j * DS + kk];
-    }
-    sG[i * BS + j] = j < i ? gg : 0.f;
-    sM1[i * BS + j] = j <= i ? m1 : 0.f;
-    sN2[i * BS + j] = j < i ? n2 : 0.f;
-    sT1[i * BS + j] = qk;
-    sT2[i * BS + j] = dp;
-  }
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sW, DS, [&](int i, int j, float x) { sG[i * BS + j] = j < i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sW, DS, [&](int i, int j, float x) { sM1[i * BS + j] = j <= i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sK, DS, [&](int i, int j, float x) { sN2[i * BS + j] = j < i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sK, DS, [&](int i, int j, float x) { sT1[i * BS + j] = x; });
+  smem_mm<B, B, D, false, true, TC>(sdO, DS, sV, DS, [&](int i, int j, float x) { sT2[i * BS + j] = x; });
   __syncthreads();
 
   // 3. Y = T^{-1} by forward substitution: Y_i = e_i - beta_i sum_{m<i} G_im Y_m ; U = Y diag(beta)
@@ -302,155 +293,92 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   __syncthreads();
 
   // 4. X = U N2 ; Y1 = U W
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float a = 0.f;
-    for (int m = j + 1; m <= i; ++m) a += sU[i * BS + m] * sN2[m * BS + j];
-    sX[i * BS + j] = a;
-  }
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int i = idx / D, cc = idx % D;
-    float a = 0.f;
-    for (int m = 0; m <= i; ++m) a += sU[i * BS + m] * sW[m * DS + cc];
-    sY1[i * DS + cc] = a;
-  }
+  smem_mm<B, B, B, false, false, TC>(sU, BS, sN2, BS, [&](int i, int j, float x) { sX[i * BS + j] = x; });
+  smem_mm<B, D, B, false, false, TC>(sU, BS, sW, DS, [&](int i, int cc, float x) { sY1[i * DS + cc] = x; });
   __syncthreads();
 
-  // 5. diagonal logits, P, dS (bilinear-part gradient = scale * P (dP - D))
+  // 5. diagonal logits S_d = QK^T - M1 X (owned elements of sT1), then P and dS (scale included)
+  smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) { sT1[i * BS + j] -= x; });
+  __syncthreads();
   for (int idx = tid; idx < B * B; idx += NT) {
     const int i = idx / B, j = idx % B;
     float p = 0.f;
-    if (j <= i && row0 + i < g.L) {
-      float s = sT1[i * BS + j];
-      for (int m = j + 1; m <= i; ++m) s -= sM1[i * BS + m] * sX[m * BS + j];
-      p = fast_exp2(s * scl2 - sLse[i]);
-    }
+    if (j <= i && row0 + i < g.L) p = fast_exp2(sT1[i * BS + j] * scl2 - sLse[i]);
     sT1[i * BS + j] = p;
     sdS[i * BS + j] = g.scale * p * (sT2[i * BS + j] - sDv[i]);
   }
   __syncthreads();
 
-  // 6. dv (final), gQ, gK, gM1 = lower(-dS X^T - dQ<- Y1^T), gX = -M1^T dS - W dK->^T
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int r = idx / D, cc = idx % D, gi = row0 + r;
-    float a = 0.f, gq = sdQl[r * DS + cc], gk = sdKr[r * DS + cc];
-    for (int i = 0; i < B; ++i) {
-      a += sT1[i * BS + r] * sdO[i * DS + cc];
-      gq += sdS[r * BS + i] * sK[i * DS + cc];
-      gk += sdS[i * BS + r] * sQ[i * DS + cc];
-    }
-    if (gi < g.L) dv[(in_row + gi) * D + cc] = from_f<T>(dvacc[(ws_row + r) * D + cc] + a);
-    sgQ[r * DS + cc] = gq;
-    sgK[r * DS + cc] = gk;
-  }
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, m = idx % B;
-    float gm = 0.f;
-    if (m <= i) {
-      for (int j = 0; j < B; ++j) gm -= sdS[i * BS + j] * sX[m * BS + j];
-      for (int cc = 0; cc < D; ++cc) gm -= sdQl[i * DS + cc] * sY1[m * DS + cc];
-    }
-    sT2[i * BS + m] = gm;
-    // gX (row i plays m, column m plays j)
-    float gx = 0.f;
-    for (int r = 0; r < B; ++r) gx -= sM1[r * BS + i] * sdS[r * BS + m];
-    for (int cc = 0; cc < D; ++cc) gx -= sW[i * DS + cc] * sdKr[m * DS + cc];
-    sgX[i * BS + m] = gx;
-  }
+  // 6. dv (final) = dV acc + P^T dO ; gQ = dQ<- + dS K ; gK = dK-> + dS^T Q ;
+  //    gM1 = lower(-dS X^T - dQ<- Y1^T) (sT2) ; gX = -M1^T dS - W dK->^T
+  smem_mm<B, D, B, true, false, TC>(sT1, BS, sdO, DS, [&](int r, int cc, float x) {
+    if (row0 + r < g.L) dv[(in_row + row0 + r) * D + cc] = from_f<T>(dvacc[(ws_row + r) * D + cc] + x);
+  });
+  smem_mm<B, D, B, false, false, TC>(sdS, BS, sK, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] = sdQl[r * DS + cc] + x; });
+  smem_mm<B, D, B, true, false, TC>(sdS, BS, sQ, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] = sdKr[r * DS + cc] + x; });
+  smem_mm<B, B, B, false, true, TC>(sdS, BS, sX, BS, [&](int i, int m, float x) { sT2[i * BS + m] = -x; });
+  smem_mm<B, B, B, true, false, TC>(sM1, BS, sdS, BS, [&](int i, int m, float x) { sgX[i * BS + m] = -x; });
+  smem_mm<B, B, D, false, true, TC>(sdQl, DS, sY1, DS, [&](int i, int m, float x) {
+    sT2[i * BS + m] = m <= i ? sT2[i * BS + m] - x : 0.f;
+  });
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sdKr, DS, [&](int i, int m, float x) { sgX[i * BS + m] -= x; });
   __syncthreads();
 
   // 7a. E3 = M1^T dQ<- + W dF^T  (into sV)
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int m = idx / D, cc = idx % D;
-    float a = 0.f;
-    for (int i = m; i < B; ++i) a += sM1[i * BS + m] * sdQl[i * DS + cc];
-    for (int n = 0; n < D; ++n) a += sW[m * DS + n] * sdF[cc * DS + n];
-    sV[m * DS + cc] = a;
-  }
+  smem_mm<B, D, B, true, false, TC>(sM1, BS, sdQl, DS, [&](int m, int cc, float x) { sV[m * DS + cc] = x; });
+  smem_mm<B, D, D, false, true, TC>(sW, DS, sdF, DS, [&](int m, int cc, float x) { sV[m * DS + cc] += x; });
   __syncthreads();
 
   // 7b. gU = lower(-E3 W^T + gX N2^T); gW = -U^T E3 - X dK-> - Y1 dF + gM1^T Q; gQ += gM1 W
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float a = 0.f;
-    if (j <= i) {
-      for (int cc = 0; cc < D; ++cc) a -= sV[i * DS + cc] * sW[j * DS + cc];
-      for (int m = 0; m < B; ++m) a += sgX[i * BS + m] * sN2[j * BS + m];
-    }
-    sgU[i * BS + j] = a;
-  }
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int r = idx / D, cc = idx % D;
-    float a = 0.f, gq = 0.f;
-    for (int i = r; i < B; ++i) a -= sU[i * BS + r] * sV[i * DS + cc];
-    for (int m = 0; m < B; ++m) {
-      a -= sX[r * BS + m] * sdKr[m * DS + cc];
-      a += sT2[m * BS + r] * sQ[m * DS + cc];
-      gq += sT2[r * BS + m] * sW[m * DS + cc];
-    }
-    for (int n = 0; n < D; ++n) a -= sY1[r * DS + n] * sdF[n * DS + cc];
-    sgW[r * DS + cc] = a;
-    sgQ[r * DS + cc] += gq;
-  }
+  smem_mm<B, B, D, false, true, TC>(sV, DS, sW, DS, [&](int i, int j, float x) { sgU[i * BS + j] = -x; });
+  smem_mm<B, B, B, false, true, TC>(sgX, BS, sN2, BS, [&](int i, int j, float x) {
+    sgU[i * BS + j] = j <= i ? sgU[i * BS + j] + x : 0.f;
+  });
+  smem_mm<B, D, B, true, false, TC>(sU, BS, sV, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] = -x; });
+  smem_mm<B, D, B, false, false, TC>(sX, BS, sdKr, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, D, D, false, false, TC>(sY1, DS, sdF, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, D, B, true, false, TC>(sT2, BS, sQ, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
+  smem_mm<B, D, B, false, false, TC>(sT2, BS, sW, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] += x; });
   __syncthreads();
 
   // 8. gN2 = strictLower(U^T gX) into sT1; dbeta_j += sum_i gU_ij Y_ij
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float a = 0.f;
-    if (j < i)
-      for (int m = i; m < B; ++m) a += sU[m * BS + i] * sgX[m * BS + j];
-    sT1[i * BS + j] = a;
-  }
+  smem_mm<B, B, B, true, false, TC>(sU, BS, sgX, BS, [&](int i, int j, float x) { sT1[i * BS + j] = j < i ? x : 0.f; });
   if (tid < B) {
     float a = 0.f;
     for (int i = tid; i < B; ++i) a += sgU[i * BS + tid] * sY[i * BS + tid];
     sgB[tid] += a;
   }
   __syncthreads();
+  // gY = gU diag(beta) (in place)
+  for (int idx = tid; idx < B * B; idx += NT) {
+    const int i = idx / B, j = idx % B;
+    sgU[i * BS + j] *= sBeta[j];
+  }
+  __syncthreads();
 
-  // 9. gW += gN2 K ; gK += gN2^T W ; A1 = gY Y^T with gY = gU diag(beta) (into sT2)
+  // 9. gW += gN2 K ; gK += gN2^T W ; A1 = gY Y^T (into sT2)
+  smem_mm<B, D, B, false, false, TC>(sT1, BS, sK, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
+  smem_mm<B, D, B, true, false, TC>(sT1, BS, sW, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] += x; });
+  smem_mm<B, B, B, false, true, TC>(sgU, BS, sY, BS, [&](int i, int j, float x) { sT2[i * BS + j] = x; });
+  __syncthreads();
+
+  // 10. gN = strictLower(-Y^T A1) into sgX ; W scaled by beta into sY1 (free now)
+  smem_mm<B, B, B, true, false, TC>(sY, BS, sT2, BS, [&](int i, int j, float x) { sgX[i * BS + j] = j < i ? -x : 0.f; });
   for (int idx = tid; idx < B * D; idx += NT) {
     const int r = idx / D, cc = idx % D;
-    float a = 0.f, b2 = 0.f;
-    for (int m = 0; m < B; ++m) {
-      a += sT1[r * BS + m] * sK[m * DS + cc];
-      b2 += sT1[m * BS + r] * sW[m * DS + cc];
-    }
-    sgW[r * DS + cc] += a;
-    sgK[r * DS + cc] += b2;
-  }
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float a = 0.f;
-    for (int kk = 0; kk < B; ++kk) a += sgU[i * BS + kk] * sBeta[kk] * sY[j * BS + kk];
-    sT2[i * BS + j] = a;
+    sY1[r * DS + cc] = sBeta[r] * sW[r * DS + cc];
   }
   __syncthreads();
 
-  // 10. gN = strictLower(-Y^T A1) into sgX
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float a = 0.f;
-    if (j < i)
-      for (int kk = 0; kk < B; ++kk) a -= sY[kk * BS + i] * sT2[kk * BS + j];
-    sgX[i * BS + j] = a;
-  }
-  __syncthreads();
-
-  // 11. N = strictLower(D G): dbeta_i += sum_{j<i} gN_ij G_ij ; gG = D gN ; gW += (gG + gG^T) W
+  // 11. N = strictLower(D G): dbeta_i += sum_{j<i} gN_ij G_ij ; gG = D gN ;
+  //     gW += gG W + gG^T W = diag(beta) (gN W) + gN^T (diag(beta) W)
   if (tid < B) {
     float a = 0.f;
     for (int j = 0; j < tid; ++j) a += sgX[tid * BS + j] * sG[tid * BS + j];
     sgB[tid] += a;
   }
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int r = idx / D, cc = idx % D;
-    float a = 0.f;
-    for (int m = 0; m < B; ++m)
-      a += (sBeta[r] * sgX[r * BS + m] + sBeta[m] * sgX[m * BS + r]) * sW[m * DS + cc];
-    sgW[r * DS + cc] += a;
-  }
+  smem_mm<B, D, B, false, false, TC>(sgX, BS, sW, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += sBeta[r] * x; });
+  smem_mm<B, D, B, true, false, TC>(sgX, BS, sY1, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
   __syncthreads();
 
   // 12. outputs

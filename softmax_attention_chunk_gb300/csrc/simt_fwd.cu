@@ -5,6 +5,9 @@
 // full-matrix logits) and §2.7 (boundary-adjusted Q/K, chunk transforms, right-to-left scan).
 #include "internal.h"
 #include "dev_common.cuh"
+#include "smem_mm.cuh"
+
+#include <type_traits>
 
 namespace pathattn {
 namespace {
@@ -18,7 +21,8 @@ struct PrepSmem {
   static constexpr int BS = B + 1;
   static constexpr int kW = 0, kQ = kW + B * DS, kK = kQ + B * DS, kV = kK + B * DS;
   static constexpr int kU = kV + B * DS, kM1 = kU + B * BS, kX = kM1 + B * BS, kT = kX + B * BS;
-  static constexpr int kBeta = kT + B * BS, kLf = kBeta + B, kA = kLf + B;
+  static constexpr int kR = kT + B * BS;
+  static constexpr int kBeta = kR + B * DS, kLf = kBeta + B, kA = kLf + B;
   static constexpr int total = kA + B;
   static constexpr size_t bytes = (size_t)total * 4;
 };
@@ -44,9 +48,12 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   float* sM1 = sm + S::kM1;
   float* sX = sm + S::kX;
   float* sT = sm + S::kT;
+  float* sR = sm + S::kR;
   float* sBeta = sm + S::kBeta;
   float* sLf = sm + S::kLf;
   float* sA = sm + S::kA;
+  // bf16 inputs: products on TF32 tensor cores; fp32 inputs: exact fp32 loops
+  constexpr bool TC = std::is_same<T, __nv_bfloat16>::value;
 
   const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
   const int row0 = c * B;
@@ -71,13 +78,7 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   __syncthreads();
 
   // G = strictLower(W W^T) into sT; chunk-local inclusive forget prefix into sA.
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    if (j < i)
-      for (int kk = 0; kk < D; ++kk) acc += sW[i * DS + kk] * sW[j * DS + kk];
-    sT[i * BS + j] = acc;
-  }
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sW, DS, [&](int i, int j, float x) { sT[i * BS + j] = j < i ? x : 0.f; });
   if (tid == 0) {
     float a = 0.f;
     for (int r = 0; r < B; ++r) { a += sLf[r]; sA[r] = a; }
@@ -101,74 +102,32 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   }
 
   // M1 = lower(Q W^T)
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    if (j <= i)
-      for (int kk = 0; kk < D; ++kk) acc += sQ[i * DS + kk] * sW[j * DS + kk];
-    sM1[i * BS + j] = acc;
-  }
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sW, DS, [&](int i, int j, float x) { sM1[i * BS + j] = j <= i ? x : 0.f; });
   __syncthreads();
   // A = M1 U (lower) into sT
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    if (j <= i)
-      for (int m = j; m <= i; ++m) acc += sM1[i * BS + m] * sU[m * BS + j];
-    sT[i * BS + j] = acc;
-  }
+  smem_mm<B, B, B, false, false, TC>(sM1, BS, sU, BS, [&](int i, int j, float x) { sT[i * BS + j] = x; });
   __syncthreads();
   // Q<- = Q - A W   (query moved to the chunk's left edge)
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int i = idx / D, cc = idx % D;
-    float acc = sQ[i * DS + cc];
-    for (int m = 0; m <= i; ++m) acc -= sT[i * BS + m] * sW[m * DS + cc];
-    ql[(ws_row + i) * D + cc] = from_f<OutT>(acc);
-  }
+  smem_mm<B, D, B, false, false, TC>(sT, BS, sW, DS, [&](int i, int j, float x) {
+    ql[(ws_row + i) * D + j] = from_f<OutT>(sQ[i * DS + j] - x);
+  });
   __syncthreads();
   // N2 = strictLower(W K^T) into sT
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    if (j < i)
-      for (int kk = 0; kk < D; ++kk) acc += sW[i * DS + kk] * sK[j * DS + kk];
-    sT[i * BS + j] = acc;
-  }
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sK, DS, [&](int i, int j, float x) { sT[i * BS + j] = j < i ? x : 0.f; });
   __syncthreads();
-  // X = U N2 : X_ij = sum_{j<m<=i} U_im N2_mj
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    for (int m = j + 1; m <= i; ++m) acc += sU[i * BS + m] * sT[m * BS + j];
-    sX[i * BS + j] = acc;
-  }
+  // X = U N2
+  smem_mm<B, B, B, false, false, TC>(sU, BS, sT, BS, [&](int i, int j, float x) { sX[i * BS + j] = x; });
   __syncthreads();
-  // K-> = K - X^T W   (key moved to the chunk's right edge)
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int j = idx / D, cc = idx % D;
-    float acc = sK[j * DS + cc];
-    for (int m = j + 1; m < B; ++m) acc -= sX[m * BS + j] * sW[m * DS + cc];
-    kr[(ws_row + j) * D + cc] = from_f<OutT>(acc);
-  }
-  // S_d = lower(Q K^T) - M1 X  into sT (diagonal-chunk logits before scale/bias)
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    float acc = 0.f;
-    if (j <= i) {
-      for (int kk = 0; kk < D; ++kk) acc += sQ[i * DS + kk] * sK[j * DS + kk];
-      for (int m = j + 1; m <= i; ++m) acc -= sM1[i * BS + m] * sX[m * BS + j];
-    }
-    sT[i * BS + j] = acc;
-  }
+  // K-> = K - X^T W   (key moved to the chunk's right edge);  S_d <- Q K^T
+  smem_mm<B, D, B, true, false, TC>(sX, BS, sW, DS, [&](int j, int n, float x) {
+    kr[(ws_row + j) * D + n] = from_f<OutT>(sK[j * DS + n] - x);
+  });
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sK, DS, [&](int i, int j, float x) { sT[i * BS + j] = x; });
+  // Y = U^T W into sR
+  smem_mm<B, D, B, true, false, TC>(sU, BS, sW, DS, [&](int m, int n, float x) { sR[m * DS + n] = x; });
+  // S_d -= M1 X   (same element ownership as the Q K^T product above: no barrier needed)
+  smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) { sT[i * BS + j] -= x; });
   __syncthreads();
-
-  // Y = U^T W into sQ (Q is no longer needed)
-  for (int idx = tid; idx < B * D; idx += NT) {
-    const int m = idx / D, cc = idx % D;
-    float acc = 0.f;
-    for (int i = m; i < B; ++i) acc += sU[i * BS + m] * sW[i * DS + cc];
-    sQ[m * DS + cc] = acc;
-  }
 
   if (with_diag) {
     // Diagonal-chunk attention partial state per row (log2 domain).
@@ -191,27 +150,19 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
       l += p;
     }
     l = group_sum<NSUB>(l);
-    __syncwarp();
-    for (int cc = sub; cc < D; cc += NSUB) {
-      float acc = 0.f;
-      for (int j = 0; j <= r; ++j) acc += sT[r * BS + j] * sV[j * DS + cc];
-      dacc[(ws_row + r) * D + cc] = acc;
-    }
     if (sub == 0) {
       dm[ws_row + r] = mx;
       dl[ws_row + r] = l;
     }
+    __syncthreads();
+    smem_mm<B, D, B, false, false, TC>(sT, BS, sV, DS, [&](int i, int cc, float x) { dacc[(ws_row + i) * D + cc] = x; });
   }
-  __syncthreads();
 
   // F = I - W^T Y = I - W^T U^T W  (the chunk's transform H_first ... H_last)
   OutT* fout = f + ((size_t)bh * g.nc + c) * D * D;
-  for (int idx = tid; idx < D * D; idx += NT) {
-    const int n = idx / D, cc = idx % D;
-    float acc = (n == cc) ? 1.f : 0.f;
-    for (int m = 0; m < B; ++m) acc -= sW[m * DS + n] * sQ[m * DS + cc];
-    fout[idx] = from_f<OutT>(acc);
-  }
+  smem_mm<D, D, B, true, false, TC>(sW, DS, sR, DS, [&](int n, int kk, float x) {
+    fout[n * D + kk] = from_f<OutT>((n == kk ? 1.f : 0.f) - x);
+  });
   if (logf) {
     const float tot = sA[B - 1];
     for (int r = tid; r < B; r += NT) {

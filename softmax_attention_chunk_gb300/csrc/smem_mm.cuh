@@ -1,0 +1,68 @@
+// Block-level product of small fp32 matrices held in shared memory, used by the per-chunk UT
+// kernels (32x32, 32x64, 64x64 operands).  C = op(A) op(B) with
+//   op(A)(i,k) = TA ? A[k*lda + i] : A[i*lda + k]    (M x K)
+//   op(B)(k,j) = TB ? B[j*ldb + k] : B[k*ldb + j]    (K x N)
+// and every result element handed to epi(i, j, value).  The operands' zeros encode the
+// triangular masks of the UT algebra, so products run over the full K range.
+//
+// TC = true runs 16x8x8 TF32 warp MMAs (fp32 accumulate; operands rounded to TF32, relative
+// 2^-11), the bf16 path's choice: these products are too small and too dependent for tcgen05's
+// 64/128-row tiles and TMEM round trips.  TC = false is a plain fp32 loop (fp32 mode).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pathattn {
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <int M, int N, int K, bool TA, bool TB, bool TC, typename Epi>
+__device__ __forceinline__ void smem_mm(const float* A, int lda, const float* B, int ldb, Epi epi) {
+  auto LA = [&](int i, int k) { return TA ? A[k * lda + i] : A[i * lda + k]; };
+  auto LB = [&](int k, int j) { return TB ? B[j * ldb + k] : B[k * ldb + j]; };
+  const int tid = threadIdx.x;
+  if constexpr (TC) {
+    static_assert(M % 16 == 0 && N % 8 == 0 && K % 8 == 0, "tile shape");
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int nwarps = blockDim.x >> 5;
+    constexpr int TN = N / 8, NT = (M / 16) * TN;
+    for (int tile = warp; tile < NT; tile += nwarps) {
+      const int i0 = (tile / TN) * 16, j0 = (tile % TN) * 8;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        const uint32_t a[4] = {to_tf32(LA(i0 + g, k0 + t)), to_tf32(LA(i0 + g + 8, k0 + t)),
+                               to_tf32(LA(i0 + g, k0 + t + 4)), to_tf32(LA(i0 + g + 8, k0 + t + 4))};
+        const uint32_t b[2] = {to_tf32(LB(k0 + t, j0 + g)), to_tf32(LB(k0 + t + 4, j0 + g))};
+        mma_m16n8k8_tf32(c, a, b);
+      }
+      epi(i0 + g, j0 + 2 * t, c[0]);
+      epi(i0 + g, j0 + 2 * t + 1, c[1]);
+      epi(i0 + g + 8, j0 + 2 * t, c[2]);
+      epi(i0 + g + 8, j0 + 2 * t + 1, c[3]);
+    }
+  } else {
+    for (int idx = tid; idx < M * N; idx += blockDim.x) {
+      const int i = idx / N, j = idx % N;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < K; ++k) acc += LA(i, k) * LB(k, j);
+      epi(i, j, acc);
+    }
+  }
+}
+
+}  // namespace pathattn
