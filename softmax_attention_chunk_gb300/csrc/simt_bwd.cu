@@ -180,9 +180,9 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
 template <int B>
 struct PrepBwdSmem {
   static constexpr int BS = B + 1;
-  static constexpr int nBD = 11, nBB = 11;
-  static constexpr int kBD = 0, kBB = kBD + nBD * B * DS, kdF = kBB + nBB * B * BS;
-  static constexpr int kVec = kdF + D * DS;
+  static constexpr int nBD = 8, nBB = 11;
+  static constexpr int kBD = 0, kBB = kBD + nBD * B * DS;
+  static constexpr int kVec = kBB + nBB * B * BS;
   static constexpr int total = kVec + 4 * B;
   static constexpr size_t bytes = (size_t)total * 4;
 };
@@ -205,14 +205,13 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   float* sW = bd + 0 * B * DS;
   float* sQ = bd + 1 * B * DS;
   float* sK = bd + 2 * B * DS;
-  float* sV = bd + 3 * B * DS;   // later E3 = M1^T dQ<- + W dF^T
-  float* sdO = bd + 4 * B * DS;
-  float* sdQl = bd + 5 * B * DS;
-  float* sdKr = bd + 6 * B * DS;
-  float* sgQ = bd + 7 * B * DS;
-  float* sgK = bd + 8 * B * DS;
-  float* sgW = bd + 9 * B * DS;
-  float* sY1 = bd + 10 * B * DS;  // U W
+  float* sV = bd + 3 * B * DS;    // V, then Y1 = U W (step 4), then diag(beta) W (step 10)
+  float* sdO = bd + 4 * B * DS;   // dO, then E3 = M1^T dQ<- + W dF^T (step 7a)
+  float* sgQ = bd + 5 * B * DS;
+  float* sgK = bd + 6 * B * DS;
+  float* sgW = bd + 7 * B * DS;
+  float* sY1 = sV;
+  float* sE3 = sdO;
   float* bb = sm + S::kBB;
   float* sY = bb + 0 * B * BS;    // T^{-1}
   float* sU = bb + 1 * B * BS;
@@ -225,7 +224,6 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   float* sgX = bb + 8 * B * BS;   // later gN = strictLower(gT)
   float* sT1 = bb + 9 * B * BS;   // QK^T -> P -> gN2
   float* sT2 = bb + 10 * B * BS;  // dP -> gM1 -> gY Y^T
-  float* sdF = sm + S::kdF;
   float* sBeta = sm + S::kVec;
   float* sLse = sBeta + B;
   float* sDv = sLse + B;
@@ -247,11 +245,11 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     sK[r * DS + cc] = ok ? to_f(k[off]) : 0.f;
     sV[r * DS + cc] = ok ? to_f(v[off]) : 0.f;
     sdO[r * DS + cc] = ok ? to_f(dO[off]) : 0.f;
-    sdQl[r * DS + cc] = dql[(ws_row + r) * D + cc];
-    sdKr[r * DS + cc] = dkr[(ws_row + r) * D + cc];
   }
-  const float* dfc = dfacc + ((size_t)bh * g.nc + c) * D * D;
-  for (int idx = tid; idx < D * D; idx += NT) sdF[(idx / D) * DS + idx % D] = dfc[idx];
+  // dQ<-, dK-> rows and dF of this chunk are read in place (global, row stride D)
+  const float* gdQl = dql + ws_row * D;
+  const float* gdKr = dkr + ws_row * D;
+  const float* gdF = dfacc + ((size_t)bh * g.nc + c) * D * D;
   for (int r = tid; r < B; r += NT) {
     const int gi = row0 + r;
     const bool ok = gi < g.L;
@@ -273,18 +271,40 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   __syncthreads();
 
   // 3. Y = T^{-1} by forward substitution: Y_i = e_i - beta_i sum_{m<i} G_im Y_m ; U = Y diag(beta)
-  for (int i = 0; i < B; ++i) {
-    if (tid < B) {
+  if constexpr (B == 32) {
+    // one warp, lane = column: the column of Y lives in registers
+    if (tid < 32) {
       const int cc = tid;
-      float val = 0.f;
-      if (cc <= i) {
-        float acc = 0.f;
-        for (int m = cc; m < i; ++m) acc += sG[i * BS + m] * sY[m * BS + cc];
-        val = (cc == i ? 1.f : 0.f) - sBeta[i] * acc;
+      float y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int m = 0; m + 1 < i; m += 2) {
+          a0 += sG[i * BS + m] * y[m];
+          a1 += sG[i * BS + m + 1] * y[m + 1];
+        }
+        if (i & 1) a0 += sG[i * BS + i - 1] * y[i - 1];
+        y[i] = (cc == i ? 1.f : 0.f) - sBeta[i] * (a0 + a1);
       }
-      sY[i * BS + cc] = val;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sY[i * BS + cc] = y[i];
     }
     __syncthreads();
+  } else {
+    for (int i = 0; i < B; ++i) {
+      if (tid < B) {
+        const int cc = tid;
+        float val = 0.f;
+        if (cc <= i) {
+          float acc = 0.f;
+          for (int m = cc; m < i; ++m) acc += sG[i * BS + m] * sY[m * BS + cc];
+          val = (cc == i ? 1.f : 0.f) - sBeta[i] * acc;
+        }
+        sY[i * BS + cc] = val;
+      }
+      __syncthreads();
+    }
   }
   for (int idx = tid; idx < B * B; idx += NT) {
     const int i = idx / B, j = idx % B;
@@ -314,29 +334,29 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   smem_mm<B, D, B, true, false, TC>(sT1, BS, sdO, DS, [&](int r, int cc, float x) {
     if (row0 + r < g.L) dv[(in_row + row0 + r) * D + cc] = from_f<T>(dvacc[(ws_row + r) * D + cc] + x);
   });
-  smem_mm<B, D, B, false, false, TC>(sdS, BS, sK, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] = sdQl[r * DS + cc] + x; });
-  smem_mm<B, D, B, true, false, TC>(sdS, BS, sQ, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] = sdKr[r * DS + cc] + x; });
+  smem_mm<B, D, B, false, false, TC>(sdS, BS, sK, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] = gdQl[r * D + cc] + x; });
+  smem_mm<B, D, B, true, false, TC>(sdS, BS, sQ, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] = gdKr[r * D + cc] + x; });
   smem_mm<B, B, B, false, true, TC>(sdS, BS, sX, BS, [&](int i, int m, float x) { sT2[i * BS + m] = -x; });
   smem_mm<B, B, B, true, false, TC>(sM1, BS, sdS, BS, [&](int i, int m, float x) { sgX[i * BS + m] = -x; });
-  smem_mm<B, B, D, false, true, TC>(sdQl, DS, sY1, DS, [&](int i, int m, float x) {
+  smem_mm<B, B, D, false, true, TC>(gdQl, D, sY1, DS, [&](int i, int m, float x) {
     sT2[i * BS + m] = m <= i ? sT2[i * BS + m] - x : 0.f;
   });
-  smem_mm<B, B, D, false, true, TC>(sW, DS, sdKr, DS, [&](int i, int m, float x) { sgX[i * BS + m] -= x; });
+  smem_mm<B, B, D, false, true, TC>(sW, DS, gdKr, D, [&](int i, int m, float x) { sgX[i * BS + m] -= x; });
   __syncthreads();
 
-  // 7a. E3 = M1^T dQ<- + W dF^T  (into sV)
-  smem_mm<B, D, B, true, false, TC>(sM1, BS, sdQl, DS, [&](int m, int cc, float x) { sV[m * DS + cc] = x; });
-  smem_mm<B, D, D, false, true, TC>(sW, DS, sdF, DS, [&](int m, int cc, float x) { sV[m * DS + cc] += x; });
+  // 7a. E3 = M1^T dQ<- + W dF^T  (into the slot of dO, free after step 6)
+  smem_mm<B, D, B, true, false, TC>(sM1, BS, gdQl, D, [&](int m, int cc, float x) { sE3[m * DS + cc] = x; });
+  smem_mm<B, D, D, false, true, TC>(sW, DS, gdF, D, [&](int m, int cc, float x) { sE3[m * DS + cc] += x; });
   __syncthreads();
 
   // 7b. gU = lower(-E3 W^T + gX N2^T); gW = -U^T E3 - X dK-> - Y1 dF + gM1^T Q; gQ += gM1 W
-  smem_mm<B, B, D, false, true, TC>(sV, DS, sW, DS, [&](int i, int j, float x) { sgU[i * BS + j] = -x; });
+  smem_mm<B, B, D, false, true, TC>(sE3, DS, sW, DS, [&](int i, int j, float x) { sgU[i * BS + j] = -x; });
   smem_mm<B, B, B, false, true, TC>(sgX, BS, sN2, BS, [&](int i, int j, float x) {
     sgU[i * BS + j] = j <= i ? sgU[i * BS + j] + x : 0.f;
   });
-  smem_mm<B, D, B, true, false, TC>(sU, BS, sV, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] = -x; });
-  smem_mm<B, D, B, false, false, TC>(sX, BS, sdKr, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
-  smem_mm<B, D, D, false, false, TC>(sY1, DS, sdF, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, D, B, true, false, TC>(sU, BS, sE3, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] = -x; });
+  smem_mm<B, D, B, false, false, TC>(sX, BS, gdKr, D, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, D, D, false, false, TC>(sY1, DS, gdF, D, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
   smem_mm<B, D, B, true, false, TC>(sT2, BS, sQ, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
   smem_mm<B, D, B, false, false, TC>(sT2, BS, sW, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] += x; });
   __syncthreads();

@@ -87,18 +87,40 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
 
   // U = (I + strictLower(D G))^{-1} D by forward substitution:
   // row i of U = beta_i (e_i - sum_{m<i} G_im U_m).  U is lower triangular.
-  for (int i = 0; i < B; ++i) {
-    if (tid < B) {
+  if constexpr (B == 32) {
+    // one warp, lane = column: the column of U lives in registers
+    if (tid < 32) {
       const int cc = tid;
-      float val = 0.f;
-      if (cc <= i) {
-        float acc = (cc == i) ? 1.f : 0.f;
-        for (int m = cc; m < i; ++m) acc -= sT[i * BS + m] * sU[m * BS + cc];
-        val = sBeta[i] * acc;
+      float u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float a0 = (cc == i) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+        for (int m = 0; m + 1 < i; m += 2) {
+          a0 -= sT[i * BS + m] * u[m];
+          a1 -= sT[i * BS + m + 1] * u[m + 1];
+        }
+        if (i & 1) a0 -= sT[i * BS + i - 1] * u[i - 1];
+        u[i] = sBeta[i] * (a0 + a1);
       }
-      sU[i * BS + cc] = val;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sU[i * BS + cc] = u[i];
     }
     __syncthreads();
+  } else {
+    for (int i = 0; i < B; ++i) {
+      if (tid < B) {
+        const int cc = tid;
+        float val = 0.f;
+        if (cc <= i) {
+          float acc = (cc == i) ? 1.f : 0.f;
+          for (int m = cc; m < i; ++m) acc -= sT[i * BS + m] * sU[m * BS + cc];
+          val = sBeta[i] * acc;
+        }
+        sU[i * BS + cc] = val;
+      }
+      __syncthreads();
+    }
   }
 
   // M1 = lower(Q W^T)
