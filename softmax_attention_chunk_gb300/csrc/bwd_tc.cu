@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   ZcSmem& s = *reinterpret_cast<ZcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heaviest tiles (largest T) of all heads first
   const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
   const bool has_partial = (2 * T + 1) * BK < p.L;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 
 // ============================ adjoint scan ============================
 constexpr int BS_NSTAGE = 2;
+constexpr int SROW = D + 4;  // staging row stride (floats): 16-byte aligned, spreads rows over banks
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DK = 256, TM_DF = 320;
 
 struct __align__(1024) BsStage {
@@ -182,7 +184,7 @@ struct __align__(1024) BsSmem {
   uint8_t ds[ZTILE];       // dS (bf16, rows x keys), scale included
   uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d)
   float stash[64 * D];     // fp32 G_1 of the lower rows (tile with a partial step)
-  float stg[3][64 * D];    // dV, dK->, dF of the step (fp32, row-major) for the bulk reductions
+  float stg[3][64 * SROW]; // dV, dK->, dF of the step (fp32 rows padded to SROW) for the bulk reductions
   uint64_t full[BS_NSTAGE], empty[BS_NSTAGE];
   uint64_t do_full, sp_full, ps_ready, g_full;
   uint32_t tmem_base;
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   BsSmem& s = *reinterpret_cast<BsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heaviest tiles (largest T) of all heads first
   const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
   const bool has_partial = (2 * T + 1) * BK < p.L;
@@ -390,11 +393,11 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
           store_row_bf16_sw(s.gs, r, g);
         }
       }
-      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions
-      if (r == 0) bulk_wait_read0();
-      wg_sync();
+      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions, one 256-byte row per
+      // owning thread (M=64 accumulator: row 16w+l sits in lane l of warp w)
+      const int mrow = 16 * warp + lane;
+      if (lane < 16) bulk_wait_read0();  // this thread's reductions of the previous step read its rows
       {
-        const int mrow = 16 * warp + lane;  // M=64 accumulator: row 16w+l sits in lane l of warp w
         uint32_t a[32], b[32];
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
           tmem_ld32(tb + lane_off + col + 32, b);
           tmem_ld_wait();
           if (lane < 16) {
-            float4* dst = reinterpret_cast<float4*>(s.stg[t] + mrow * D);
+            float4* dst = reinterpret_cast<float4*>(s.stg[t] + mrow * SROW);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               dst[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
@@ -417,16 +420,15 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      wg_sync();
-      if (r == 0) {
-        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK;
-        bulk_reduce_add_f32(p.dv + crow * D, s.stg[0], BK * D * 4);
-        bulk_reduce_add_f32(p.dkr + crow * D, s.stg[1], BK * D * 4);
-        if (k > 0) bulk_reduce_add_f32(p.df + ((size_t)bh * p.nc + c) * D * D, s.stg[2], D * D * 4);
+      if (lane < 16) {
+        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK + mrow;
+        bulk_reduce_add_f32(p.dv + crow * D, s.stg[0] + mrow * SROW, D * 4);
+        bulk_reduce_add_f32(p.dkr + crow * D, s.stg[1] + mrow * SROW, D * 4);
+        if (k > 0) bulk_reduce_add_f32(p.df + (((size_t)bh * p.nc + c) * D + mrow) * D, s.stg[2] + mrow * SROW, D * 4);
         bulk_commit();
       }
     }
-    if (r == 0) bulk_wait0();
+    if (lane < 16) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();

@@ -33,7 +33,8 @@ constexpr int D = kHeadDim;
 constexpr int NSTAGE = 3;
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t COL_S = 0, COL_Z = 64, COL_O = 128, COL_P = 192;
+// S double-buffered (P of step n is written over S of step n), one Z' buffer, O.
+constexpr uint32_t COL_S0 = 0, COL_Z = 128, COL_O = 192;
 constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
 
 struct __align__(1024) ScanSmem {
@@ -41,7 +42,9 @@ struct __align__(1024) ScanSmem {
   uint8_t kf[NSTAGE][128 * 128];      // rows 0-63: K->_c, rows 64-127: F_c
   uint8_t v[NSTAGE][BK * 128];        // V_c
   uint64_t full[NSTAGE], empty[NSTAGE];
-  uint64_t s_full, p_ready, o_done, z_init;
+  // p_ready alternates by step parity: a thread may arrive for step n+1 before a slower one has
+  // arrived for step n (the next score MMA only waits for z_ready), never two steps ahead.
+  uint64_t s_full[2], z_ready, p_ready[2], pv_done, o_done, z_init;
   uint32_t tmem_base;
 };
 
@@ -67,7 +70,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);  // heaviest tiles first
+  // heaviest tiles (largest T) of all heads first
+  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
   const int bh = (int)(blockIdx.x % p.BH);
   const bool has_partial = (2 * T + 1) * BK < p.L;
   const int nsteps = (has_partial ? 1 : 0) + 2 * T;
@@ -77,8 +81,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       mbar_init(&s.full[k], 1);
       mbar_init(&s.empty[k], 1);
     }
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_ready, 128);
+    mbar_init(&s.s_full[0], 1);
+    mbar_init(&s.s_full[1], 1);
+    mbar_init(&s.z_ready, 128);
+    mbar_init(&s.p_ready[0], 128);
+    mbar_init(&s.p_ready[1], 128);
+    mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_done, 1);
     mbar_init(&s.z_init, 1);
     fence_barrier_init();
@@ -110,38 +118,46 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
+    // order: S(n), Z'(n) as soon as Z(n) is in shared memory; then O += P(n-1) V(n-1).
     if (lane == 0 && nsteps > 0) {
-      const uint32_t idesc_sz = idesc_bf16(128, 128, 0, 0);
+      const uint32_t idesc_n64 = idesc_bf16(128, 64, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
       const uint32_t zaddr = smem_u32(s.z);
       bool ok = mbar_wait(&s.z_init, 0, p.err, 2);
+      auto issue_pv = [&](int m) {
+        const uint32_t va = smem_u32(s.v[m % NSTAGE]);
+        const uint32_t pcol = COL_S0 + 64 * (m & 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tb + COL_O, tb + pcol + 8 * k, sdesc_sw128(va + 2048 * k, 1024, 0), idesc_pv, 1);
+        mma_commit(&s.empty[m % NSTAGE]);
+        mma_commit(&s.pv_done);
+      };
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&s.full[st], (n / NSTAGE) & 1, p.err, 3)) { ok = false; break; }
-        if (n > 0) {
-          if (!mbar_wait(&s.p_ready, (n - 1) & 1, p.err, 4)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t va = smem_u32(s.v[(n - 1) % NSTAGE]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tb + COL_O, tb + COL_P + 8 * k, sdesc_sw128(va + 2048 * k, 1024, 0), idesc_pv, 1);
-          mma_commit(&s.empty[(n - 1) % NSTAGE]);
-        } else {
-          tc_fence_after();
-        }
-        const uint32_t kfa = smem_u32(s.kf[st]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tb + COL_S, sdesc_sw128(zaddr + 32 * k, 1024, 16), sdesc_sw128(kfa + 32 * k, 1024, 16),
-                 idesc_sz, k > 0 ? 1u : 0u);
-        mma_commit(&s.s_full);
-      }
-      if (ok && mbar_wait(&s.p_ready, (nsteps - 1) & 1, p.err, 5)) {
+        if (n > 0 && !mbar_wait(&s.z_ready, (n - 1) & 1, p.err, 4)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t va = smem_u32(s.v[(nsteps - 1) % NSTAGE]);
+        const uint32_t kfa = smem_u32(s.kf[st]);
+        const uint32_t scol = COL_S0 + 64 * (n & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tb + COL_O, tb + COL_P + 8 * k, sdesc_sw128(va + 2048 * k, 1024, 0), idesc_pv, 1);
+          mma_ss(tb + scol, sdesc_sw128(zaddr + 32 * k, 1024, 16), sdesc_sw128(kfa + 32 * k, 1024, 16),
+                 idesc_n64, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tb + COL_Z, sdesc_sw128(zaddr + 32 * k, 1024, 16),
+                 sdesc_sw128(kfa + 64 * 128 + 32 * k, 1024, 16), idesc_n64, k > 0 ? 1u : 0u);
+        mma_commit(&s.s_full[n & 1]);
+        if (n > 0) {
+          if (!mbar_wait(&s.p_ready[(n - 1) & 1], ((n - 1) >> 1) & 1, p.err, 5)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(n - 1);
+        }
+      }
+      if (ok && mbar_wait(&s.p_ready[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, p.err, 5)) {
+        tc_fence_after();
+        issue_pv(nsteps - 1);
         mma_commit(&s.o_done);
       }
     }
@@ -166,14 +182,37 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     float R = 0.f;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
-      if (!mbar_wait(&s.s_full, n & 1, p.err, 6)) { ok = false; break; }
+      if (!mbar_wait(&s.s_full[n & 1], (n >> 1) & 1, p.err, 6)) { ok = false; break; }
       tc_fence_after();
       const int c = has_partial ? 2 * T - n : 2 * T - 1 - n;
       const bool active = !(has_partial && n == 0 && r < 64);
-      // scores (log2 domain, in place in the load registers)
+      const uint32_t scol = COL_S0 + 64 * (n & 1);
       uint32_t buf2[32];
-      tmem_ld32(tb + lane_off + COL_S, buf);
-      tmem_ld32(tb + lane_off + COL_S + 32, buf2);
+      // transport first: Z <- Z F_c^T (bf16) so that the next score MMA can start
+      if (n + 1 < nsteps) {
+        if (active) {
+          tmem_ld32(tb + lane_off + COL_Z, buf);
+          tmem_ld32(tb + lane_off + COL_Z + 32, buf2);
+          tmem_ld_wait();
+          uint8_t* zrow = s.z + r * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = (q < 4) ? (buf + 8 * q) : (buf2 + 8 * (q - 4));
+            uint4 pk;
+            pk.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
+            pk.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
+            pk.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
+            pk.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
+            *reinterpret_cast<uint4*>(zrow + ((q ^ (r & 7)) * 16)) = pk;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&s.z_ready);
+      }
+      // scores (log2 domain, in place in the load registers)
+      tmem_ld32(tb + lane_off + scol, buf);
+      tmem_ld32(tb + lane_off + scol + 32, buf2);
       tmem_ld_wait();
       const float rb = (arow + R) * kLog2e;
       float mx = -INFINITY;
@@ -196,6 +235,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const float mnew = fmaxf(m, mx);
       const bool resc = mnew > m + kTau;
       if (__any_sync(0xffffffffu, resc)) {
+        // O holds P(n-1) V(n-1) only once that MMA has completed
+        if (n > 0 && !mbar_wait(&s.pv_done, (n - 1) & 1, p.err, 8)) { ok = false; break; }
+        tc_fence_after();
         const float corr = resc ? fast_exp2(m - mnew) : 1.f;
         if (resc) m = mnew;
         l *= corr;
@@ -209,7 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           tmem_st32(tb + lane_off + COL_O + h * 32, ob);
         }
       }
-      // probabilities, packed bf16 pairs (key 2j in the low half) into TMEM
+      // probabilities, packed bf16 pairs (key 2j in the low half), written over S(n)
       float ls = 0.f;
       {
         uint32_t pk[32];
@@ -223,33 +265,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           pk[j] = pack_bf16(p0, p1);
           pk[16 + j] = pack_bf16(p2, p3);
         }
-        tmem_st32(tb + lane_off + COL_P, pk);
+        tmem_st32(tb + lane_off + scol, pk);
       }
       l += ls;
-      // transport: Z <- Z F_c^T, rounded to bf16, into the swizzled Z tile
-      if (active) {
-        if (n + 1 < nsteps) {
-          tmem_ld32(tb + lane_off + COL_Z, buf);
-          tmem_ld32(tb + lane_off + COL_Z + 32, buf2);
-          tmem_ld_wait();
-          uint8_t* zrow = s.z + r * 128;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t* src = (q < 4) ? (buf + 8 * q) : (buf2 + 8 * (q - 4));
-            uint4 pk;
-            pk.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
-            pk.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
-            pk.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
-            pk.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
-            *reinterpret_cast<uint4*>(zrow + ((q ^ (r & 7)) * 16)) = pk;
-          }
-        }
-        if (p.fox) R += p.ft[(size_t)bh * p.nc + c];
-      }
-      fence_proxy_async_smem();
+      if (active && p.fox) R += p.ft[(size_t)bh * p.nc + c];
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_ready);
+      mbar_arrive(&s.p_ready[n & 1]);
     }
     // ---------------- epilogue ----------------
     if (nsteps > 0) {
