@@ -77,8 +77,8 @@ def phase_roofline(L, BH, pk):
     return {
         "fwd_prepare": (2 * BH * (nc32 * prep32_macs(1) + nc64 * merge64_macs(1)), "tensor(tf32)", tf32),
         "fwd_scan": (BH * npairs * (4 * 64 * 64 * D + 2 * 64 * D * D), "tensor", pk["bf16"]),
-        "bwd_prepare": (2 * BH * (nc32 * prep32_macs(0) + nc64 * merge64_macs(0) + (steps - nt) * 128 * D * D),
-                        "tensor(tf32)", tf32),
+        # the forward's preparation is reused: the backward prepare phase runs D_i and the Z chain
+        "bwd_prepare": (2 * BH * (steps - nt) * 128 * D * D, "tensor", pk["bf16"]),
         "bwd_scan": (BH * npairs * (10 * 64 * 64 * D + 4 * 64 * D * D), "tensor", pk["bf16"]),
         "bwd_finish": (2 * BH * (nc64 * convert_macs() + nc32 * ut_bwd32_macs()), "tensor(tf32)", tf32),
     }
@@ -281,20 +281,23 @@ def run_ours(args):
     torch.cuda.synchronize()
     q, k, v, w, beta, dO = (x[n] for n in ("q", "k", "v", "w", "beta", "dO"))
     desc = pa.make_desc(q, cfg["scale"])
-    ws_f = pa.workspace(desc, 0, dev)
     ws_b = pa.workspace(desc, 1, dev)
     o = torch.empty_like(q)
     lse = torch.empty(Bt, H, L, dtype=torch.float32, device=dev)
     grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q), dw=torch.empty_like(q),
                  dbeta=torch.empty_like(beta))
 
+    # Training step: the forward runs in the backward's workspace and the backward reuses its
+    # per-chunk preparation (PATH_BWD_REUSE_FWD), as a training framework keeps forward state.
+    bwd_phases = (pa.PATH_BWD_PREPARE | pa.PATH_BWD_REUSE_FWD, pa.PATH_BWD_SCAN, pa.PATH_BWD_FINISH)
+
     def step(evs=None):
         marks = [ev()] if evs is not None else None
-        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse), phases=pa.PATH_FWD_PREPARE)
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_PREPARE)
         if marks is not None: marks.append(ev())
-        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse), phases=pa.PATH_FWD_SCAN)
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_SCAN)
         if marks is not None: marks.append(ev())
-        for ph in (pa.PATH_BWD_PREPARE, pa.PATH_BWD_SCAN, pa.PATH_BWD_FINISH):
+        for ph in bwd_phases:
             pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads, phases=ph)
             if marks is not None: marks.append(ev())
         if evs is not None:
@@ -330,7 +333,7 @@ def run_ours(args):
     dom = max(phase_ms, key=lambda n: phase_ms[n])
     kernels = {"fwd_prepare": "prep_simt_kernel (UT, chunk 32) + merge64_kernel",
                "fwd_scan": "fwd_scan_tc_kernel (tcgen05)",
-               "bwd_prepare": "bwd_dot + prep_simt_kernel + merge64_kernel + zchain_tc_kernel",
+               "bwd_prepare": "bwd_dot + zchain_tc_kernel (forward preparation reused)",
                "bwd_scan": "bwd_scan_tc_kernel (tcgen05)",
                "bwd_finish": "convert_kernel + prep_bwd_simt_kernel (UT backward)"}
     d = phases[dom]
@@ -352,8 +355,9 @@ def run_ours(args):
     def e2e_step():
         for n, t in host.items():
             x[n].copy_(t, non_blocking=True)
-        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_f, out=(o, lse))
-        pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads)
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse))
+        pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads,
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD)
         outs_h["o"].copy_(o, non_blocking=True)
         outs_h["lse"].copy_(lse, non_blocking=True)
         for n, t in grads.items():
@@ -387,7 +391,7 @@ def run_ours(args):
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
                 "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "e2e": e2e,
-                "clocks": clocks_rec, "gpu_launches": 10 * args.steps, "memset_ops": 5 * args.steps,
+                "clocks": clocks_rec, "gpu_launches": 8 * args.steps, "memset_ops": 5 * args.steps,
                 "peaks": pk, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -136,6 +136,12 @@ int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, co
  */
 enum { PATH_FWD_PREPARE = 1, PATH_FWD_SCAN = 2, PATH_FWD_ALL = 3 };
 enum { PATH_BWD_PREPARE = 1, PATH_BWD_SCAN = 2, PATH_BWD_FINISH = 4, PATH_BWD_ALL = 7 };
+/* Optional bit for path_attn_bwd_phases(PREPARE): the workspace already holds the forward's
+ * per-chunk preparation for exactly these inputs and descriptor, because path_attn_fwd was run
+ * with this same workspace (sized by path_attn_workspace_size(desc, 1)) and nothing used it since.
+ * PREPARE then skips recomputing it (the bf16 tensor-core path; ignored by the fp32 path).  If the
+ * statement is false the gradients are wrong; nothing detects it. */
+enum { PATH_BWD_REUSE_FWD = 8 };
 
 int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q, const void* k,
                          const void* v, const void* w, const float* beta, const float* log_f,

@@ -149,7 +149,7 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
   Geom g;
   int rc = check_desc(desc, 1, &g);
   if (rc != PATH_OK) return rc;
-  if (phases <= 0 || (phases & ~PATH_BWD_ALL)) return PATH_ERR_INVALID_ARG;
+  if ((phases & PATH_BWD_ALL) == 0 || (phases & ~(PATH_BWD_ALL | PATH_BWD_REUSE_FWD))) return PATH_ERR_INVALID_ARG;
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o);
   CHECK_PTR(lse); CHECK_PTR(dO); CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dw);
   CHECK_PTR(dbeta);
@@ -164,7 +164,8 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
   const BwdWs lay = bwd_ws_layout(g);
   if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,
-                                     dk, dv, dw, dbeta, (char*)ws, lay, phases, (cudaStream_t)stream));
+                                     dk, dv, dw, dbeta, (char*)ws, lay, phases & PATH_BWD_ALL,
+                                     (cudaStream_t)stream));
 }
 
 PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,

@@ -180,7 +180,8 @@ cudaError_t launch_prep_bwd(const Geom& g, const void* q, const void* k, const v
                             const float* dql, const float* dkr, const float* dvacc, const float* dfacc,
                             void* dq, void* dk, void* dv, void* dw, float* dbeta, cudaStream_t st);
 // Tensor-core backward (bf16).  phases: 1 = prepare (accumulators, D_i, chunk-32 UT quantities,
-// chunk-64 merge, Z chain), 2 = adjoint scan, 4 = chunk conversion + UT backward.
+// chunk-64 merge, Z chain), 2 = adjoint scan, 4 = chunk conversion + UT backward; with bit 8
+// the prepare phase keeps the forward's preparation found in ws.
 cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
                           const float* beta, const void* o, const float* lse, const void* dO, void* dq, void* dk,
                           void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st);

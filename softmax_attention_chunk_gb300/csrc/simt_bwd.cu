@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
 
   // bf16 inputs: products on TF32 tensor cores; fp32 inputs: exact fp32 loops
   constexpr bool TC = std::is_same<T, __nv_bfloat16>::value;
-  // 2. G = strictLower(WW^T), M1 = lower(QW^T), N2 = strictLower(WK^T), QK^T, dP = dO V^T
+  // P2. G = strictLower(WW^T), M1 = lower(QW^T), N2 = strictLower(WK^T), QK^T (sT1), dP = dO V^T (sT2)
   smem_mm<B, B, D, false, true, TC>(sW, DS, sW, DS, [&](int i, int j, float x) { sG[i * BS + j] = j < i ? x : 0.f; });
   smem_mm<B, B, D, false, true, TC>(sQ, DS, sW, DS, [&](int i, int j, float x) { sM1[i * BS + j] = j <= i ? x : 0.f; });
   smem_mm<B, B, D, false, true, TC>(sW, DS, sK, DS, [&](int i, int j, float x) { sN2[i * BS + j] = j < i ? x : 0.f; });
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   smem_mm<B, B, D, false, true, TC>(sdO, DS, sV, DS, [&](int i, int j, float x) { sT2[i * BS + j] = x; });
   __syncthreads();
 
-  // 3. Y = T^{-1} by forward substitution: Y_i = e_i - beta_i sum_{m<i} G_im Y_m ; U = Y diag(beta)
+  // P3. Y = T^{-1} by forward substitution: Y_i = e_i - beta_i sum_{m<i} G_im Y_m ; U = Y diag(beta)
   if constexpr (B == 32) {
     // one warp, lane = column: the column of Y lives in registers
     if (tid < 32) {
@@ -287,10 +287,13 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
         if (i & 1) a0 += sG[i * BS + i - 1] * y[i - 1];
         y[i] = (cc == i ? 1.f : 0.f) - sBeta[i] * (a0 + a1);
       }
+      const float bc = sBeta[cc];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sY[i * BS + cc] = y[i];
+      for (int i = 0; i < 32; ++i) {
+        sY[i * BS + cc] = y[i];
+        sU[i * BS + cc] = y[i] * bc;
+      }
     }
-    __syncthreads();
   } else {
     for (int i = 0; i < B; ++i) {
       if (tid < B) {
@@ -305,32 +308,30 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
       }
       __syncthreads();
     }
-  }
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    sU[i * BS + j] = sY[i * BS + j] * sBeta[j];
+    for (int idx = tid; idx < B * B; idx += NT) {
+      const int i = idx / B, j = idx % B;
+      sU[i * BS + j] = sY[i * BS + j] * sBeta[j];
+    }
   }
   __syncthreads();
 
-  // 4. X = U N2 ; Y1 = U W
+  // P4. X = U N2 ; Y1 = U W (into V's slot) ; E3 = M1^T dQ<- + W dF^T (into dO's slot needs dO
+  //     until P6, so E3 waits); then the diagonal logits and, in the same epilogue, P and dS
   smem_mm<B, B, B, false, false, TC>(sU, BS, sN2, BS, [&](int i, int j, float x) { sX[i * BS + j] = x; });
   smem_mm<B, D, B, false, false, TC>(sU, BS, sW, DS, [&](int i, int cc, float x) { sY1[i * DS + cc] = x; });
   __syncthreads();
 
-  // 5. diagonal logits S_d = QK^T - M1 X (owned elements of sT1), then P and dS (scale included)
-  smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) { sT1[i * BS + j] -= x; });
-  __syncthreads();
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
+  // P5. S_d = QK^T - M1 X ; P = exp(scale S_d - lse) on j <= i ; dS = scale P (dP - D)
+  smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) {
     float p = 0.f;
-    if (j <= i && row0 + i < g.L) p = fast_exp2(sT1[i * BS + j] * scl2 - sLse[i]);
+    if (j <= i && row0 + i < g.L) p = fast_exp2((sT1[i * BS + j] - x) * scl2 - sLse[i]);
     sT1[i * BS + j] = p;
     sdS[i * BS + j] = g.scale * p * (sT2[i * BS + j] - sDv[i]);
-  }
+  });
   __syncthreads();
 
-  // 6. dv (final) = dV acc + P^T dO ; gQ = dQ<- + dS K ; gK = dK-> + dS^T Q ;
-  //    gM1 = lower(-dS X^T - dQ<- Y1^T) (sT2) ; gX = -M1^T dS - W dK->^T
+  // P6. dv (final) = dV acc + P^T dO ; gQ = dQ<- + dS K ; gK = dK-> + dS^T Q ;
+  //     gM1 = lower(-dS X^T - dQ<- Y1^T) (sT2) ; gX = -M1^T dS - W dK->^T
   smem_mm<B, D, B, true, false, TC>(sT1, BS, sdO, DS, [&](int r, int cc, float x) {
     if (row0 + r < g.L) dv[(in_row + row0 + r) * D + cc] = from_f<T>(dvacc[(ws_row + r) * D + cc] + x);
   });
@@ -344,54 +345,47 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   smem_mm<B, B, D, false, true, TC>(sW, DS, gdKr, D, [&](int i, int m, float x) { sgX[i * BS + m] -= x; });
   __syncthreads();
 
-  // 7a. E3 = M1^T dQ<- + W dF^T  (into the slot of dO, free after step 6)
+  // P7. E3 = M1^T dQ<- + W dF^T (into dO's slot, free now); gN2 = strictLower(U^T gX) (sT1, P free)
   smem_mm<B, D, B, true, false, TC>(sM1, BS, gdQl, D, [&](int m, int cc, float x) { sE3[m * DS + cc] = x; });
   smem_mm<B, D, D, false, true, TC>(sW, DS, gdF, D, [&](int m, int cc, float x) { sE3[m * DS + cc] += x; });
-  __syncthreads();
-
-  // 7b. gU = lower(-E3 W^T + gX N2^T); gW = -U^T E3 - X dK-> - Y1 dF + gM1^T Q; gQ += gM1 W
-  smem_mm<B, B, D, false, true, TC>(sE3, DS, sW, DS, [&](int i, int j, float x) { sgU[i * BS + j] = -x; });
-  smem_mm<B, B, B, false, true, TC>(sgX, BS, sN2, BS, [&](int i, int j, float x) {
-    sgU[i * BS + j] = j <= i ? sgU[i * BS + j] + x : 0.f;
-  });
-  smem_mm<B, D, B, true, false, TC>(sU, BS, sE3, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] = -x; });
-  smem_mm<B, D, B, false, false, TC>(sX, BS, gdKr, D, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, B, B, true, false, TC>(sU, BS, sgX, BS, [&](int i, int j, float x) { sT1[i * BS + j] = j < i ? x : 0.f; });
+  // gW = -X dK-> - Y1 dF + gM1^T Q (the -U^T E3 term follows in P8) ; gQ += gM1 W
+  smem_mm<B, D, B, false, false, TC>(sX, BS, gdKr, D, [&](int r, int cc, float x) { sgW[r * DS + cc] = -x; });
   smem_mm<B, D, D, false, false, TC>(sY1, DS, gdF, D, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
   smem_mm<B, D, B, true, false, TC>(sT2, BS, sQ, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
   smem_mm<B, D, B, false, false, TC>(sT2, BS, sW, DS, [&](int r, int cc, float x) { sgQ[r * DS + cc] += x; });
   __syncthreads();
 
-  // 8. gN2 = strictLower(U^T gX) into sT1; dbeta_j += sum_i gU_ij Y_ij
-  smem_mm<B, B, B, true, false, TC>(sU, BS, sgX, BS, [&](int i, int j, float x) { sT1[i * BS + j] = j < i ? x : 0.f; });
+  // P8. gU = lower(-E3 W^T + gX N2^T); gW -= U^T E3; gW += gN2 K; gK += gN2^T W
+  smem_mm<B, B, D, false, true, TC>(sE3, DS, sW, DS, [&](int i, int j, float x) { sgU[i * BS + j] = -x; });
+  smem_mm<B, B, B, false, true, TC>(sgX, BS, sN2, BS, [&](int i, int j, float x) {
+    sgU[i * BS + j] = j <= i ? sgU[i * BS + j] + x : 0.f;
+  });
+  smem_mm<B, D, B, true, false, TC>(sU, BS, sE3, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] -= x; });
+  smem_mm<B, D, B, false, false, TC>(sT1, BS, sK, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
+  smem_mm<B, D, B, true, false, TC>(sT1, BS, sW, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] += x; });
+  __syncthreads();
+
+  // P9. dbeta_j += sum_i gU_ij Y_ij ; A1 = gY Y^T = gU diag(beta) Y^T = gU U^T (into sT2)
   if (tid < B) {
     float a = 0.f;
     for (int i = tid; i < B; ++i) a += sgU[i * BS + tid] * sY[i * BS + tid];
     sgB[tid] += a;
   }
-  __syncthreads();
-  // gY = gU diag(beta) (in place)
-  for (int idx = tid; idx < B * B; idx += NT) {
-    const int i = idx / B, j = idx % B;
-    sgU[i * BS + j] *= sBeta[j];
-  }
-  __syncthreads();
-
-  // 9. gW += gN2 K ; gK += gN2^T W ; A1 = gY Y^T (into sT2)
-  smem_mm<B, D, B, false, false, TC>(sT1, BS, sK, DS, [&](int r, int cc, float x) { sgW[r * DS + cc] += x; });
-  smem_mm<B, D, B, true, false, TC>(sT1, BS, sW, DS, [&](int r, int cc, float x) { sgK[r * DS + cc] += x; });
-  smem_mm<B, B, B, false, true, TC>(sgU, BS, sY, BS, [&](int i, int j, float x) { sT2[i * BS + j] = x; });
-  __syncthreads();
-
-  // 10. gN = strictLower(-Y^T A1) into sgX ; W scaled by beta into sY1 (free now)
-  smem_mm<B, B, B, true, false, TC>(sY, BS, sT2, BS, [&](int i, int j, float x) { sgX[i * BS + j] = j < i ? -x : 0.f; });
+  smem_mm<B, B, B, false, true, TC>(sgU, BS, sU, BS, [&](int i, int j, float x) { sT2[i * BS + j] = x; });
+  // diag(beta) W into Y1's slot (free now)
   for (int idx = tid; idx < B * D; idx += NT) {
     const int r = idx / D, cc = idx % D;
     sY1[r * DS + cc] = sBeta[r] * sW[r * DS + cc];
   }
   __syncthreads();
 
-  // 11. N = strictLower(D G): dbeta_i += sum_{j<i} gN_ij G_ij ; gG = D gN ;
-  //     gW += gG W + gG^T W = diag(beta) (gN W) + gN^T (diag(beta) W)
+  // P10. gN = strictLower(-Y^T A1) into sgX
+  smem_mm<B, B, B, true, false, TC>(sY, BS, sT2, BS, [&](int i, int j, float x) { sgX[i * BS + j] = j < i ? -x : 0.f; });
+  __syncthreads();
+
+  // P11. N = strictLower(D G): dbeta_i += sum_{j<i} gN_ij G_ij ; gG = D gN ;
+  //      gW += gG W + gG^T W = diag(beta) (gN W) + gN^T (diag(beta) W)
   if (tid < B) {
     float a = 0.f;
     for (int j = 0; j < tid; ++j) a += sgX[tid * BS + j] * sG[tid * BS + j];

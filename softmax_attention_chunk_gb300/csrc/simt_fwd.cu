@@ -22,7 +22,8 @@ struct PrepSmem {
   static constexpr int kW = 0, kQ = kW + B * DS, kK = kQ + B * DS, kV = kK + B * DS;
   static constexpr int kU = kV + B * DS, kM1 = kU + B * BS, kX = kM1 + B * BS, kT = kX + B * BS;
   static constexpr int kR = kT + B * BS;
-  static constexpr int kBeta = kR + B * DS, kLf = kBeta + B, kA = kLf + B;
+  static constexpr int kG = kR + B * DS, kN2 = kG + B * BS, kAM = kN2 + B * BS;
+  static constexpr int kBeta = kAM + B * BS, kLf = kBeta + B, kA = kLf + B;
   static constexpr int total = kA + B;
   static constexpr size_t bytes = (size_t)total * 4;
 };
@@ -49,6 +50,9 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   float* sX = sm + S::kX;
   float* sT = sm + S::kT;
   float* sR = sm + S::kR;
+  float* sG = sm + S::kG;
+  float* sN2 = sm + S::kN2;
+  float* sAM = sm + S::kAM;
   float* sBeta = sm + S::kBeta;
   float* sLf = sm + S::kLf;
   float* sA = sm + S::kA;
@@ -77,15 +81,19 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   }
   __syncthreads();
 
-  // G = strictLower(W W^T) into sT; chunk-local inclusive forget prefix into sA.
-  smem_mm<B, B, D, false, true, TC>(sW, DS, sW, DS, [&](int i, int j, float x) { sT[i * BS + j] = j < i ? x : 0.f; });
-  if (tid == 0) {
+  // Phase 1 (independent products of the inputs): G = strictLower(W W^T), M1 = lower(Q W^T),
+  // N2 = strictLower(W K^T), Q K^T (start of the diagonal logits); chunk-local forget prefix.
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sW, DS, [&](int i, int j, float x) { sG[i * BS + j] = j < i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sW, DS, [&](int i, int j, float x) { sM1[i * BS + j] = j <= i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sW, DS, sK, DS, [&](int i, int j, float x) { sN2[i * BS + j] = j < i ? x : 0.f; });
+  smem_mm<B, B, D, false, true, TC>(sQ, DS, sK, DS, [&](int i, int j, float x) { sT[i * BS + j] = x; });
+  if (tid == NT - 1) {
     float a = 0.f;
     for (int r = 0; r < B; ++r) { a += sLf[r]; sA[r] = a; }
   }
   __syncthreads();
 
-  // U = (I + strictLower(D G))^{-1} D by forward substitution:
+  // Phase 2: U = (I + strictLower(D G))^{-1} D by forward substitution:
   // row i of U = beta_i (e_i - sum_{m<i} G_im U_m).  U is lower triangular.
   if constexpr (B == 32) {
     // one warp, lane = column: the column of U lives in registers
@@ -97,10 +105,10 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
         float a0 = (cc == i) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
         for (int m = 0; m + 1 < i; m += 2) {
-          a0 -= sT[i * BS + m] * u[m];
-          a1 -= sT[i * BS + m + 1] * u[m + 1];
+          a0 -= sG[i * BS + m] * u[m];
+          a1 -= sG[i * BS + m + 1] * u[m + 1];
         }
-        if (i & 1) a0 -= sT[i * BS + i - 1] * u[i - 1];
+        if (i & 1) a0 -= sG[i * BS + i - 1] * u[i - 1];
         u[i] = sBeta[i] * (a0 + a1);
       }
 #pragma unroll
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
         float val = 0.f;
         if (cc <= i) {
           float acc = (cc == i) ? 1.f : 0.f;
-          for (int m = cc; m < i; ++m) acc -= sT[i * BS + m] * sU[m * BS + cc];
+          for (int m = cc; m < i; ++m) acc -= sG[i * BS + m] * sU[m * BS + cc];
           val = sBeta[i] * acc;
         }
         sU[i * BS + cc] = val;
@@ -123,32 +131,27 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
     }
   }
 
-  // M1 = lower(Q W^T)
-  smem_mm<B, B, D, false, true, TC>(sQ, DS, sW, DS, [&](int i, int j, float x) { sM1[i * BS + j] = j <= i ? x : 0.f; });
+  // Phase 3: A = M1 U, X = U N2, Y = U^T W
+  smem_mm<B, B, B, false, false, TC>(sM1, BS, sU, BS, [&](int i, int j, float x) { sAM[i * BS + j] = x; });
+  smem_mm<B, B, B, false, false, TC>(sU, BS, sN2, BS, [&](int i, int j, float x) { sX[i * BS + j] = x; });
+  smem_mm<B, D, B, true, false, TC>(sU, BS, sW, DS, [&](int m, int n, float x) { sR[m * DS + n] = x; });
   __syncthreads();
-  // A = M1 U (lower) into sT
-  smem_mm<B, B, B, false, false, TC>(sM1, BS, sU, BS, [&](int i, int j, float x) { sT[i * BS + j] = x; });
-  __syncthreads();
-  // Q<- = Q - A W   (query moved to the chunk's left edge)
-  smem_mm<B, D, B, false, false, TC>(sT, BS, sW, DS, [&](int i, int j, float x) {
+
+  // Phase 4: Q<- = Q - A W (left edge), K-> = K - X^T W (right edge),
+  //          S_d = lower(Q K^T) - M1 X (same element owners as Q K^T), F = I - W^T Y
+  smem_mm<B, D, B, false, false, TC>(sAM, BS, sW, DS, [&](int i, int j, float x) {
     ql[(ws_row + i) * D + j] = from_f<OutT>(sQ[i * DS + j] - x);
   });
-  __syncthreads();
-  // N2 = strictLower(W K^T) into sT
-  smem_mm<B, B, D, false, true, TC>(sW, DS, sK, DS, [&](int i, int j, float x) { sT[i * BS + j] = j < i ? x : 0.f; });
-  __syncthreads();
-  // X = U N2
-  smem_mm<B, B, B, false, false, TC>(sU, BS, sT, BS, [&](int i, int j, float x) { sX[i * BS + j] = x; });
-  __syncthreads();
-  // K-> = K - X^T W   (key moved to the chunk's right edge);  S_d <- Q K^T
   smem_mm<B, D, B, true, false, TC>(sX, BS, sW, DS, [&](int j, int n, float x) {
     kr[(ws_row + j) * D + n] = from_f<OutT>(sK[j * DS + n] - x);
   });
-  smem_mm<B, B, D, false, true, TC>(sQ, DS, sK, DS, [&](int i, int j, float x) { sT[i * BS + j] = x; });
-  // Y = U^T W into sR
-  smem_mm<B, D, B, true, false, TC>(sU, BS, sW, DS, [&](int m, int n, float x) { sR[m * DS + n] = x; });
-  // S_d -= M1 X   (same element ownership as the Q K^T product above: no barrier needed)
   smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) { sT[i * BS + j] -= x; });
+  {
+    OutT* fout = f + ((size_t)bh * g.nc + c) * D * D;
+    smem_mm<D, D, B, true, false, TC>(sW, DS, sR, DS, [&](int n, int kk, float x) {
+      fout[n * D + kk] = from_f<OutT>((n == kk ? 1.f : 0.f) - x);
+    });
+  }
   __syncthreads();
 
   if (with_diag) {
@@ -180,11 +183,6 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
     smem_mm<B, D, B, false, false, TC>(sT, BS, sV, DS, [&](int i, int cc, float x) { dacc[(ws_row + i) * D + cc] = x; });
   }
 
-  // F = I - W^T Y = I - W^T U^T W  (the chunk's transform H_first ... H_last)
-  OutT* fout = f + ((size_t)bh * g.nc + c) * D * D;
-  smem_mm<D, D, B, true, false, TC>(sW, DS, sR, DS, [&](int n, int kk, float x) {
-    fout[n * D + kk] = from_f<OutT>((n == kk ? 1.f : 0.f) - x);
-  });
   if (logf) {
     const float tot = sA[B - 1];
     for (int r = tid; r < B; r += NT) {

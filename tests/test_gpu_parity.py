@@ -189,3 +189,23 @@ def test_decode_matches_forward_rows(cuda_lib):
                                    sl(inp["beta"]), scale=1.0))
     o_d = torch.stack(rows, 2)
     assert (o_d - o_f).abs().max().item() <= 1e-4
+
+
+def test_bwd_reusing_forward_preparation(cuda_lib):
+    """PATH_BWD_REUSE_FWD: forward run in the backward's workspace, backward skips recomputing
+    the preparation; gradients equal the plain backward's (up to reduction order) and the oracle's."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(2, 2, 333, 64, "bf16", seed=44, with_dO=True, near2_frac=0.05)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    desc = pa.make_desc(t["q"], 1.0)
+    ws = pa.workspace(desc, 1, DEV)
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], None, 1.0, ws=ws)
+    g_plain = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], 1.0)
+    g_reuse = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], 1.0, ws=ws,
+                     phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD)
+    torch.cuda.synchronize()
+    for key in ("dq", "dk", "dv", "dw", "dbeta"):
+        a, b = g_plain[key].float(), g_reuse[key].float()
+        assert (a - b).abs().max().item() <= 1e-2 * max(1.0, a.abs().max().item()), key
+    check_grads(inp, g_reuse, 1.0, 2e-2, rel=3e-2)
