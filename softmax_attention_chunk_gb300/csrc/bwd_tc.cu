@@ -60,9 +60,8 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   ZcSmem& s = *reinterpret_cast<ZcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest tiles (largest T) of all heads first
-  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  int bh, T;
+  tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
   const bool has_partial = (2 * T + 1) * BK < p.L;
   const int nsteps = (has_partial ? 1 : 0) + 2 * T;
   uint8_t* zbase = p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * ZTILE;
@@ -186,7 +185,7 @@ struct __align__(1024) BsSmem {
   float stash[64 * D];     // fp32 G_1 of the lower rows (tile with a partial step)
   float stg[3][64 * SROW]; // dV, dK->, dF of the step (fp32 rows padded to SROW) for the bulk reductions
   uint64_t full[BS_NSTAGE], empty[BS_NSTAGE];
-  uint64_t do_full, sp_full, ps_ready, g_full;
+  uint64_t do_full, sp_full, ps_ready, g_full, g_free;
   uint32_t tmem_base;
 };
 
@@ -216,7 +215,10 @@ __device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const fl
   }
 }
 
-__global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
+// Warp roles: 0-3 softmax side (P, dS of a step), 4 TMA/bulk producer, 5 MMA issuer,
+// 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions of the previous step).
+constexpr int BS_THREADS = 320;
+__global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
                                                             const __grid_constant__ CUtensorMap tm_kr,
                                                             const __grid_constant__ CUtensorMap tm_v,
                                                             const __grid_constant__ CUtensorMap tm_f,
@@ -224,9 +226,8 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   BsSmem& s = *reinterpret_cast<BsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest tiles (largest T) of all heads first
-  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  int bh, T;
+  tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
   const bool has_partial = (2 * T + 1) * BK < p.L;
   const int nsteps = (has_partial ? 1 : 0) + 2 * T;
   const uint8_t* zbase = p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * ZTILE;
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
     mbar_init(&s.sp_full, 1);
     mbar_init(&s.ps_ready, 128);
     mbar_init(&s.g_full, 1);
+    mbar_init(&s.g_free, 128);
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -296,6 +298,8 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
           mma_ss(tb + TM_DP, sdesc_sw128(a_do + 32 * kk, 1024, 16), sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
         mma_commit(&s.sp_full);
         if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
+        // the gradient side has read G/dV/dK->/dF of the previous step and written G_{n+1}
+        if (k > 0 && !mbar_wait(&s.g_free, (k - 1) & 1, p.err, 27)) { ok = false; break; }
         tc_fence_after();
         // dV = P^T dO, dK-> = dS^T Z  (M = 64 keys, K = 128 rows)
 #pragma unroll
@@ -323,47 +327,58 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
         mma_commit(&s.g_full);
       }
     }
-  } else {
-    // ---------------- warpgroup: thread r owns query row r of the tile ----------------
+  } else if (warp < 4) {
+    // ---------------- softmax side: thread r owns query row r of the tile ----------------
     const int r = tid;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const int grow = T * BQ + r;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
     const float lse2 = grow < p.L ? p.lse[(size_t)bh * p.L + grow] * kLog2e : INFINITY;
     const float Dr = p.Dv[wrow];
-    if (r < 64)
-      for (int j = 0; j < D; ++j) s.stash[r * D + j] = 0.f;
+    for (int k = 0; k < nsteps; ++k) {
+      const int n = nsteps - 1 - k;
+      const bool partial = has_partial && n == 0;
+      const bool active = !(partial && r < 64);
+      if (!mbar_wait(&s.sp_full, k & 1, p.err, 25)) break;
+      tc_fence_after();
+      uint32_t sa[32], sb[32], da[32], db[32];
+      tmem_ld32(tb + lane_off + TM_S, sa);
+      tmem_ld32(tb + lane_off + TM_S + 32, sb);
+      tmem_ld32(tb + lane_off + TM_DP, da);
+      tmem_ld32(tb + lane_off + TM_DP + 32, db);
+      tmem_ld_wait();
+      float pv[64], dsv[64];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
+        const float p1 = active ? fast_exp2(fmaf(__uint_as_float(sb[j]), p.scl, -lse2)) : 0.f;
+        pv[j] = p0;
+        pv[32 + j] = p1;
+        dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+        dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
+      }
+      // the MMAs of the previous step read the P / dS tiles
+      if (k > 0 && !mbar_wait(&s.g_full, (k - 1) & 1, p.err, 26)) break;
+      store_row_bf16_sw(s.ps, r, pv);
+      store_row_bf16_sw(s.ds, r, dsv);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.ps_ready);
+    }
+  } else if (warp >= 6) {
+    // ---------------- gradient side: thread owns query row rg = 32 (warp % 4) + lane ----------------
+    const int q4 = warp & 3;
+    const int rg = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + rg;
+    const int mrow = 16 * q4 + lane;  // M=64 accumulators: row 16q+l sits in lane l of quarter q
+    if (rg < 64)
+      for (int j = 0; j < D; ++j) s.stash[rg * D + j] = 0.f;
     for (int k = 0; k < nsteps; ++k) {
       const int n = nsteps - 1 - k;
       const bool partial = has_partial && n == 0;
       const int c = step_chunk(has_partial, T, n);
-      const bool active = !(partial && r < 64);
-      if (!mbar_wait(&s.sp_full, k & 1, p.err, 25)) break;
-      tc_fence_after();
-      {
-        uint32_t sa[32], sb[32], da[32], db[32];
-        tmem_ld32(tb + lane_off + TM_S, sa);
-        tmem_ld32(tb + lane_off + TM_S + 32, sb);
-        tmem_ld32(tb + lane_off + TM_DP, da);
-        tmem_ld32(tb + lane_off + TM_DP + 32, db);
-        tmem_ld_wait();
-        float pv[64], dsv[64];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
-          const float p1 = active ? fast_exp2(fmaf(__uint_as_float(sb[j]), p.scl, -lse2)) : 0.f;
-          pv[j] = p0;
-          pv[32 + j] = p1;
-          dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
-          dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
-        }
-        store_row_bf16_sw(s.ps, r, pv);
-        store_row_bf16_sw(s.ds, r, dsv);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&s.ps_ready);
-      if (!mbar_wait(&s.g_full, k & 1, p.err, 26)) break;
+      if (!mbar_wait(&s.g_full, k & 1, p.err, 28)) break;
       tc_fence_after();
       // G_n
       {
@@ -377,25 +392,23 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
           g[j] = __uint_as_float(ga[j]);
           g[32 + j] = __uint_as_float(gb[j]);
         }
-        if (partial && r < 64) {
+        if (partial && rg < 64) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) g[j] = s.stash[r * D + j];
+          for (int j = 0; j < 64; ++j) g[j] = s.stash[rg * D + j];
         }
-        if (has_partial && n == 1 && r < 64) {
+        if (has_partial && n == 1 && rg < 64) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) s.stash[r * D + j] = g[j];
+          for (int j = 0; j < 64; ++j) s.stash[rg * D + j] = g[j];
         }
         if (n == 0) {
           float4* dst = reinterpret_cast<float4*>(p.dql + wrow * D);
 #pragma unroll
           for (int j = 0; j < 16; ++j) dst[j] = make_float4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
         } else {
-          store_row_bf16_sw(s.gs, r, g);
+          store_row_bf16_sw(s.gs, rg, g);
         }
       }
-      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions, one 256-byte row per
-      // owning thread (M=64 accumulator: row 16w+l sits in lane l of warp w)
-      const int mrow = 16 * warp + lane;
+      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions, one 256-byte row per thread
       if (lane < 16) bulk_wait_read0();  // this thread's reductions of the previous step read its rows
       {
         uint32_t a[32], b[32];
@@ -420,6 +433,7 @@ __global__ void __launch_bounds__(192, 1) bwd_scan_tc_kernel(const __grid_consta
       }
       fence_proxy_async_smem();
       tc_fence_before();
+      mbar_arrive(&s.g_free);
       if (lane < 16) {
         const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK + mrow;
         bulk_reduce_add_f32(p.dv + crow * D, s.stg[0] + mrow * SROW, D * 4);
@@ -578,7 +592,7 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     const size_t smem = sizeof(BsSmem) + 1024;
     if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), 192, smem, st>>>(m_do, m_kr, m_v, m_f, bp);
+    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), BS_THREADS, smem, st>>>(m_do, m_kr, m_v, m_f, bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {

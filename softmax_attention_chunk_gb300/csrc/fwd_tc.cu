@@ -70,9 +70,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest tiles (largest T) of all heads first
-  const int T = p.ntiles - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  int bh, T;
+  tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
   const bool has_partial = (2 * T + 1) * BK < p.L;
   const int nsteps = (has_partial ? 1 : 0) + 2 * T;
 

@@ -143,6 +143,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t sbo, uin
   return d;
 }
 
+// ---------------- tile schedule ----------------
+// Maps a linear CTA index onto (head, query tile): heads are taken in groups of kHeadGroup; inside
+// a group the heaviest tiles (largest T, most steps) of all its heads come first.  A group's
+// operands and fp32 accumulators stay L2-resident, and tiles of one head start at different times.
+constexpr int kHeadGroup = 16;
+__device__ __forceinline__ void tile_of_block(int blk, int ntiles, int BH, int& bh, int& T) {
+  const int per_group = ntiles * kHeadGroup;
+  const int grp = blk / per_group, within = blk % per_group;
+  const int gsize = min(kHeadGroup, BH - grp * kHeadGroup);
+  T = ntiles - 1 - within / gsize;
+  bh = grp * kHeadGroup + within % gsize;
+}
+
 // ---------------- tcgen05: TMEM <-> registers ----------------
 // 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
