@@ -111,13 +111,12 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
   if (uses_tensor_cores(desc, 0)) {
     const TcWs tw = tc_layout(desc, false);
     if (phases & PATH_FWD_PREPARE) {
-      rc = cuda_status(launch_prep_simt(true, tw.g32, q, k, v, w, beta, log_f, wsb, tw.p32, true, st));
-      if (rc == PATH_OK) rc = cuda_status(launch_merge64(tw, v, log_f, wsb, true, st));
+      rc = cuda_status(cudaMemsetAsync(wsb + tw.p64.err, 0, sizeof(int), st));
+      if (rc == PATH_OK) rc = cuda_status(launch_ut_prep64(tw.g64, q, k, v, w, beta, log_f, wsb, tw.p64, true, st));
       if (rc != PATH_OK) return rc;
     }
     if (phases & PATH_FWD_SCAN) {
-      rc = cuda_status(cudaMemsetAsync(wsb + tw.p64.err, 0, sizeof(int), st));
-      if (rc == PATH_OK) rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, st));
+      rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, st));
       if (rc != PATH_OK) return rc;
     }
     return PATH_OK;

@@ -552,9 +552,10 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaMemsetAsync(ws + w.df64, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
     if ((e = launch_bwd_dot(w.g32, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
-    if (!(phases & 8)) {  // 8: the forward's chunk-32 / chunk-64 preparation is already in ws
-      if ((e = launch_prep_simt(true, w.g32, q, k, v, wv, beta, nullptr, ws, w.p32, false, st)) != cudaSuccess) return e;
-      if ((e = launch_merge64(w, v, nullptr, ws, false, st)) != cudaSuccess) return e;
+    // chunk-32 fp32 UT quantities for the chunk conversion of the finish phase
+    if ((e = launch_prep_simt(true, w.g32, q, k, v, wv, beta, nullptr, ws, w.p32, false, st)) != cudaSuccess) return e;
+    if (!(phases & 8)) {  // 8: the forward's chunk-64 preparation is already in ws
+      if ((e = launch_ut_prep64(w.g64, q, k, v, wv, beta, nullptr, ws, w.p64, false, st)) != cudaSuccess) return e;
     }
     CUtensorMap m_ql, m_f;
     if (!make_map_rows64(&m_ql, ws + w.p64.ql, rows, BQ) ||

@@ -93,9 +93,9 @@ inline BwdWs bwd_ws_layout(const Geom& g) {
   return w;
 }
 
-// Workspace of the bf16 tensor-core path.  The UT preparation runs at chunk 32 (fp32 results,
-// p32); a merge kernel forms the chunk-64 operands of the tcgen05 kernels (bf16 Q<-, K->, F and
-// the fp32 diagonal-chunk softmax / forget-gate state, p64).  Lp is a multiple of 128.
+// Workspace of the bf16 tensor-core path (Lp a multiple of 128).  p64: chunk-64 operands of the
+// tcgen05 kernels (bf16 Q<-, K->, F; fp32 diagonal-chunk softmax and forget-gate state).
+// p32: chunk-32 fp32 UT quantities used by the backward's chunk conversion.
 struct TcWs {
   Geom g32, g64;
   FwdWs p32, p64;
@@ -122,10 +122,12 @@ inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
   TcWs w{};
   w.g32 = tc_geom(BH, L, scale, 32);
   w.g64 = tc_geom(BH, L, scale, 64);
-  w.p32 = fwd_ws_layout(w.g32, 4, 0);
-  w.p64 = fwd_ws_layout(w.g64, 2, w.p32.total);
+  // p64 first: the forward and backward layouts place it at the same offsets
+  w.p64 = fwd_ws_layout(w.g64, 2, 0);
   size_t off = w.p64.total;
   if (for_backward) {
+    w.p32 = fwd_ws_layout(w.g32, 4, off);
+    off = w.p32.total;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t rows = (size_t)BH * w.g64.Lp;
     const size_t nt = (size_t)w.g64.Lp / 128;
@@ -157,9 +159,11 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
-// Merge of adjacent chunk-32 preparation results into chunk-64 operands (tensor-core path).
-cudaError_t launch_merge64(const TcWs& w, const void* v, const float* logf, char* ws, bool with_diag,
-                           cudaStream_t st);
+// tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
+// tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.
+cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                             const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
+                             cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, cudaStream_t st);
