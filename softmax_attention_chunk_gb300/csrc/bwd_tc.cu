@@ -10,12 +10,11 @@
 //        dV_c += P^T dO,  dK->_c += dS^T Z_n,  dF_c += G_{n+1}^T Z_n,
 //        G_n = dS K->_c + G_{n+1} F_c,     dQ<-_T = G_0,
 //      the chunk sums dV, dK->, dF being added across tiles with bulk fp32 reductions;
-//   3. (convert) maps the chunk-64 gradients onto the chunk-32 quantities the UT backward
-//      works with, including the block of b-rows against a-keys inside each 64-chunk.
+//   3. (finish) the per-chunk UT backward (ut_bwd_tc.cu) adds the diagonal chunk and takes
+//      dQ<-, dK->, dF back to q, k, w, beta.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
-#include "smem_mm.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -452,90 +451,6 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
   }
 }
 
-// ============================ chunk-64 -> chunk-32 gradients ============================
-// With a, b the two 32-chunks of 64-chunk c (row-vector conventions as in the merge):
-//   Q<-64 = [Q<-32_a ; Q<-32_b F_a^T]  =>  dQ<-32_a = dQ<-64_a,  dQ<-32_b = dQ<-64_b F_a,
-//                                          dF_a += dQ<-64_b^T Q<-32_b
-//   K->64 = [K->32_a F_b ; K->32_b]    =>  dK->32_b = dK->64_b,  dK->32_a = dK->64_a F_b^T,
-//                                          dF_b += K->32_a^T dK->64_a
-//   F64 = F_a F_b                      =>  dF_a += dF64 F_b^T,  dF_b += F_a^T dF64
-// plus the attention block of b-rows against a-keys (logits Q<-32_b K->32_a^T), whose
-// gradients go to dQ<-32_b, dK->32_a and dV_a.
-constexpr int CV_NT = 256;
-constexpr int DS = D + 1;
-struct CvSmem {
-  float fa[D * DS], fb[D * DS], dF[D * DS];
-  float qb[32 * DS], ka[32 * DS], dqb[32 * DS], dka[32 * DS], dob[32 * DS], va[32 * DS];
-  float p[32 * 33], ds[32 * 33];
-};
-
-__global__ void __launch_bounds__(CV_NT) convert_kernel(
-    Geom g, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ dO, const float* __restrict__ lse,
-    const float* __restrict__ Dv, const float* __restrict__ ql32, const float* __restrict__ kr32,
-    const float* __restrict__ f32, const float* __restrict__ dql64, const float* __restrict__ dkr64,
-    const float* __restrict__ df64, float* __restrict__ dv, float* __restrict__ dql32, float* __restrict__ dkr32,
-    float* __restrict__ df32) {
-  extern __shared__ float smraw[];
-  CvSmem& s = *reinterpret_cast<CvSmem*>(smraw);
-  const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-  const int nc32 = g.Lp / 32, nc64 = g.Lp / 64;
-  const size_t row0 = (size_t)bh * g.Lp + (size_t)c * 64;
-  const float* Fa = f32 + ((size_t)bh * nc32 + 2 * c) * D * D;
-  const float* Fb = Fa + D * D;
-  const float* dF64 = df64 + ((size_t)bh * nc64 + c) * D * D;
-  for (int idx = tid; idx < D * D; idx += CV_NT) {
-    const int i = idx / D, j = idx % D;
-    s.fa[i * DS + j] = Fa[idx];
-    s.fb[i * DS + j] = Fb[idx];
-    s.dF[i * DS + j] = dF64[idx];
-  }
-  for (int idx = tid; idx < 32 * D; idx += CV_NT) {
-    const int r = idx / D, cc = idx % D;
-    s.qb[r * DS + cc] = ql32[(row0 + 32 + r) * D + cc];
-    s.ka[r * DS + cc] = kr32[(row0 + r) * D + cc];
-    s.dqb[r * DS + cc] = dql64[(row0 + 32 + r) * D + cc];
-    s.dka[r * DS + cc] = dkr64[(row0 + r) * D + cc];
-    const int gb = c * 64 + 32 + r, ga = c * 64 + r;
-    s.dob[r * DS + cc] = gb < g.L ? __bfloat162float(dO[((size_t)bh * g.L + gb) * D + cc]) : 0.f;
-    s.va[r * DS + cc] = ga < g.L ? __bfloat162float(v[((size_t)bh * g.L + ga) * D + cc]) : 0.f;
-  }
-  __syncthreads();
-  // cross block: rows of b (i) against keys of a (j): logits into p, dP into ds
-  smem_mm<32, 32, D, false, true, true>(s.qb, DS, s.ka, DS, [&](int i, int j, float x) { s.p[i * 33 + j] = x; });
-  smem_mm<32, 32, D, false, true, true>(s.dob, DS, s.va, DS, [&](int i, int j, float x) { s.ds[i * 33 + j] = x; });
-  __syncthreads();
-  for (int idx = tid; idx < 32 * 32; idx += CV_NT) {
-    const int i = idx / 32, j = idx % 32;
-    const int gi = c * 64 + 32 + i;
-    float pij = 0.f;
-    if (gi < g.L) pij = fast_exp2(s.p[i * 33 + j] * g.scale * kLog2e - lse[(size_t)bh * g.L + gi] * kLog2e);
-    s.p[i * 33 + j] = pij;
-    s.ds[i * 33 + j] = g.scale * pij * (s.ds[i * 33 + j] - Dv[row0 + 32 + i]);
-  }
-  __syncthreads();
-  // dQ<-32: rows a copy, rows b = dQ<-64_b F_a + dS K->32_a
-  // dK->32: rows b copy, rows a = dK->64_a F_b^T + dS^T Q<-32_b ;  dV rows of a += P^T dO_b
-  for (int idx = tid; idx < 32 * D; idx += CV_NT) {
-    const int r = idx / D, n = idx % D;
-    dql32[(row0 + r) * D + n] = dql64[(row0 + r) * D + n];
-    dkr32[(row0 + 32 + r) * D + n] = dkr64[(row0 + 32 + r) * D + n];
-  }
-  float* qout = dql32 + (row0 + 32) * D;
-  float* kout = dkr32 + row0 * D;
-  smem_mm<32, D, D, false, false, true>(s.dqb, DS, s.fa, DS, [&](int i, int n, float x) { qout[i * D + n] = x; });
-  smem_mm<32, D, 32, false, false, true>(s.ds, 33, s.ka, DS, [&](int i, int n, float x) { qout[i * D + n] += x; });
-  smem_mm<32, D, D, false, true, true>(s.dka, DS, s.fb, DS, [&](int j, int n, float x) { kout[j * D + n] = x; });
-  smem_mm<32, D, 32, true, false, true>(s.ds, 33, s.qb, DS, [&](int j, int n, float x) { kout[j * D + n] += x; });
-  smem_mm<32, D, 32, true, false, true>(s.p, 33, s.dob, DS, [&](int j, int n, float x) { dv[(row0 + j) * D + n] += x; });
-  // dF_a = dF64 F_b^T + dQ<-64_b^T Q<-32_b ;  dF_b = F_a^T dF64 + K->32_a^T dK->64_a
-  float* dFa = df32 + ((size_t)bh * nc32 + 2 * c) * D * D;
-  float* dFb = dFa + D * D;
-  smem_mm<D, D, D, false, true, true>(s.dF, DS, s.fb, DS, [&](int n, int k, float x) { dFa[n * D + k] = x; });
-  smem_mm<D, D, 32, true, false, true>(s.dqb, DS, s.qb, DS, [&](int n, int k, float x) { dFa[n * D + k] += x; });
-  smem_mm<D, D, D, true, false, true>(s.fa, DS, s.dF, DS, [&](int n, int k, float x) { dFb[n * D + k] = x; });
-  smem_mm<D, D, 32, true, false, true>(s.ka, DS, s.dka, DS, [&](int n, int k, float x) { dFb[n * D + k] += x; });
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
@@ -551,9 +466,7 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaMemsetAsync(ws + w.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(ws + w.df64, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
-    if ((e = launch_bwd_dot(w.g32, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
-    // chunk-32 fp32 UT quantities for the chunk conversion of the finish phase
-    if ((e = launch_prep_simt(true, w.g32, q, k, v, wv, beta, nullptr, ws, w.p32, false, st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_dot(g, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
     if (!(phases & 8)) {  // 8: the forward's chunk-64 preparation is already in ws
       if ((e = launch_ut_prep64(w.g64, q, k, v, wv, beta, nullptr, ws, w.p64, false, st)) != cudaSuccess) return e;
     }
@@ -597,18 +510,9 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {
-    const size_t smem = sizeof(CvSmem);
-    if ((e = cudaFuncSetAttribute(convert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-      return e;
-    convert_kernel<<<dim3(g.nc, g.BH), CV_NT, smem, st>>>(
-        g, (const __nv_bfloat16*)v, (const __nv_bfloat16*)dO, lse, (const float*)(ws + w.Dv),
-        (const float*)(ws + w.p32.ql), (const float*)(ws + w.p32.kr), (const float*)(ws + w.p32.f),
-        (const float*)(ws + w.dql64), (const float*)(ws + w.dkr64), (const float*)(ws + w.df64), (float*)(ws + w.dv),
-        (float*)(ws + w.dql32), (float*)(ws + w.dkr32), (float*)(ws + w.df32));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_prep_bwd(w.g32, q, k, v, wv, beta, lse, dO, (const float*)(ws + w.Dv), (const float*)(ws + w.dql32),
-                             (const float*)(ws + w.dkr32), (const float*)(ws + w.dv), (const float*)(ws + w.df32), dq,
-                             dk, dv, dw, dbeta, st)) != cudaSuccess)
+    if ((e = launch_ut_bwd64(g, q, k, v, wv, beta, lse, dO, (const float*)(ws + w.Dv), (const float*)(ws + w.dql64),
+                             (const float*)(ws + w.dkr64), (const float*)(ws + w.dv), (const float*)(ws + w.df64), dq,
+                             dk, dv, dw, dbeta, err, st)) != cudaSuccess)
       return e;
   }
   return cudaSuccess;

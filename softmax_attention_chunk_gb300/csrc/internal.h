@@ -95,14 +95,12 @@ inline BwdWs bwd_ws_layout(const Geom& g) {
 
 // Workspace of the bf16 tensor-core path (Lp a multiple of 128).  p64: chunk-64 operands of the
 // tcgen05 kernels (bf16 Q<-, K->, F; fp32 diagonal-chunk softmax and forget-gate state).
-// p32: chunk-32 fp32 UT quantities used by the backward's chunk conversion.
 struct TcWs {
-  Geom g32, g64;
-  FwdWs p32, p64;
+  Geom g64;
+  FwdWs p64;
   // backward only
   size_t Dv;                       // D_i                                [BH][Lp]
   size_t dql64, dkr64, dv, df64;   // chunk-64 gradients (fp32; dkr64/dv/df64 accumulate)
-  size_t dql32, dkr32, df32;       // chunk-32 gradients for the UT backward (fp32)
   size_t zs;                       // transported queries Z, bf16 swizzled 128x64 tiles
   size_t total;
 };
@@ -120,14 +118,11 @@ inline Geom tc_geom(int BH, int L, float scale, int B) {
 
 inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
   TcWs w{};
-  w.g32 = tc_geom(BH, L, scale, 32);
   w.g64 = tc_geom(BH, L, scale, 64);
   // p64 first: the forward and backward layouts place it at the same offsets
   w.p64 = fwd_ws_layout(w.g64, 2, 0);
   size_t off = w.p64.total;
   if (for_backward) {
-    w.p32 = fwd_ws_layout(w.g32, 4, off);
-    off = w.p32.total;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t rows = (size_t)BH * w.g64.Lp;
     const size_t nt = (size_t)w.g64.Lp / 128;
@@ -136,9 +131,6 @@ inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
     w.dkr64 = take(rows * kHeadDim * 4);
     w.dv = take(rows * kHeadDim * 4);
     w.df64 = take((size_t)BH * w.g64.nc * kHeadDim * kHeadDim * 4);
-    w.dql32 = take(rows * kHeadDim * 4);
-    w.dkr32 = take(rows * kHeadDim * 4);
-    w.df32 = take((size_t)BH * w.g32.nc * kHeadDim * kHeadDim * 4);
     // tile T of a head has at most 2T+1 steps: sum over tiles <= nt^2 tiles of 16 KB
     w.zs = take((size_t)BH * nt * nt * 128 * 128);
   }
@@ -176,13 +168,14 @@ cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const vo
                             void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
                             cudaStream_t st);
 
-// bf16 helpers shared by the tensor-core backward: D_i = dO_i . o_i, and the chunk-32 UT
-// backward (diagonal blocks + chain rule through the UT quantities) writing the gradients.
+// D_i = dO_i . o_i for the bf16 tensor-core backward.
 cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* Dv, cudaStream_t st);
-cudaError_t launch_prep_bwd(const Geom& g, const void* q, const void* k, const void* v, const void* w,
-                            const float* beta, const float* lse, const void* dO, const float* Dv,
-                            const float* dql, const float* dkr, const float* dvacc, const float* dfacc,
-                            void* dq, void* dk, void* dv, void* dw, float* dbeta, cudaStream_t st);
+// tcgen05 UT backward at chunk 64: diagonal-chunk attention backward and the chain rule through
+// the per-chunk UT quantities, writing dq, dk, dv, dw, dbeta.
+cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                            const float* beta, const float* lse, const void* dO, const float* Dv, const float* dql,
+                            const float* dkr, const float* dvacc, const float* df, void* dq, void* dk, void* dv,
+                            void* dw, float* dbeta, int* err, cudaStream_t st);
 // Tensor-core backward (bf16).  phases: 1 = prepare (accumulators, D_i, chunk-32 UT quantities,
 // chunk-64 merge, Z chain), 2 = adjoint scan, 4 = chunk conversion + UT backward; with bit 8
 // the prepare phase keeps the forward's preparation found in ws.

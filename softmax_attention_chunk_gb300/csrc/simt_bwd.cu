@@ -460,22 +460,6 @@ cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep_bwd(const Geom& g, const void* q, const void* k, const void* v, const void* w,
-                            const float* beta, const float* lse, const void* dO, const float* Dv,
-                            const float* dql, const float* dkr, const float* dvacc, const float* dfacc,
-                            void* dq, void* dk, void* dv, void* dw, float* dbeta, cudaStream_t st) {
-  if (g.B != 32) return cudaErrorInvalidValue;
-  using T = __nv_bfloat16;
-  auto kern = prep_bwd_simt_kernel<T, 32>;
-  const size_t smem = PrepBwdSmem<32>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3(g.nc, g.BH), NT, smem, st>>>(g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, lse,
-                                            (const T*)dO, Dv, dql, dkr, dvacc, dfacc, (T*)dq, (T*)dk, (T*)dv,
-                                            (T*)dw, dbeta);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                             const void* v, const void* w, const float* beta, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
