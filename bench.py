@@ -39,26 +39,13 @@ DEC_CFG = "decode_b32h32_t32768"
 L2_BYTES = 129 * 2**20
 WORKLOAD = ("PaTH fwd+bwd, batch 32, 32 heads, d=64, L=4096, bf16 (beta fp32, 5% near-reflection beta), "
             "per rank")
-FP32_SIMT_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # FP32 FMA lanes x 2 x max SM clock
-TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rate
 D = 64
 
 
-# Algorithmic multiply-adds of the kernels of the bf16 tensor-core path (2 flops each).
-def prep32_macs(diag, B=32):
-    return (7 + diag) * B * B * D + 3 * B ** 3 + D * D * B
-
-
-def merge64_macs(diag):
-    return D ** 3 + 2 * 32 * D * D + diag * (2 * 32 * 32 * D)
-
-
-def convert_macs():
-    return 2 * 32 * 32 * D + 2 * 32 * D * D + 3 * 32 * D * 32 + 2 * D ** 3 + 2 * D * D * 32
-
-
-def ut_bwd32_macs(B=32):
-    return 21 * B * B * D + 8 * B ** 3 + 2 * B * D * D
+# Algorithmic multiply-adds of the per-chunk UT kernels of the bf16 tensor-core path (2 flops
+# each): every product is a 64 x 64 x 64 tcgen05 MMA.
+UT_PREP64_MMAS = 12  # G, M1, N2, QK^T; M1 U, U N2, U^T W; A W, X^T W, M1 X, W^T Y; P V
+UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule through U, X, M1, N2, G
 
 
 def tiles_steps(L):
@@ -70,17 +57,16 @@ def tiles_steps(L):
 
 def phase_roofline(L, BH, pk):
     """Per phase of the fwd+bwd step: (algorithmic flops per launch, bound, peak TFLOP/s)."""
-    nc32, nc64 = (L + 127) // 128 * 4, (L + 127) // 128 * 2
+    nc64 = (L + 127) // 128 * 2
     nt, steps = tiles_steps(L)
     npairs = nc64 * (nc64 - 1) // 2
-    tf32 = pk["bf16"] * TF32_OVER_BF16
     return {
-        "fwd_prepare": (2 * BH * (nc32 * prep32_macs(1) + nc64 * merge64_macs(1)), "tensor(tf32)", tf32),
+        "fwd_prepare": (2 * BH * nc64 * UT_PREP64_MMAS * 64 ** 3, "tensor", pk["bf16"]),
         "fwd_scan": (BH * npairs * (4 * 64 * 64 * D + 2 * 64 * D * D), "tensor", pk["bf16"]),
         # the forward's preparation is reused: the backward prepare phase runs D_i and the Z chain
         "bwd_prepare": (2 * BH * (steps - nt) * 128 * D * D, "tensor", pk["bf16"]),
         "bwd_scan": (BH * npairs * (10 * 64 * 64 * D + 4 * 64 * D * D), "tensor", pk["bf16"]),
-        "bwd_finish": (2 * BH * (nc64 * convert_macs() + nc32 * ut_bwd32_macs()), "tensor(tf32)", tf32),
+        "bwd_finish": (2 * BH * nc64 * UT_BWD64_MMAS * 64 ** 3, "tensor", pk["bf16"]),
     }
 
 
@@ -331,16 +317,15 @@ def run_ours(args):
         phases[n] = {"ms": ms, "share": ms / sum(phase_ms.values()), "flops": fl, "achieved": ach,
                      "bound": bound, "peak": peak, "frac": ach / peak}
     dom = max(phase_ms, key=lambda n: phase_ms[n])
-    kernels = {"fwd_prepare": "prep_simt_kernel (UT, chunk 32) + merge64_kernel",
+    kernels = {"fwd_prepare": "ut_prep64_kernel (tcgen05 UT preparation)",
                "fwd_scan": "fwd_scan_tc_kernel (tcgen05)",
                "bwd_prepare": "bwd_dot + zchain_tc_kernel (forward preparation reused)",
                "bwd_scan": "bwd_scan_tc_kernel (tcgen05)",
-               "bwd_finish": "convert_kernel + prep_bwd_simt_kernel (UT backward)"}
+               "bwd_finish": "ut_bwd64_kernel (tcgen05 UT backward)"}
     d = phases[dom]
     roofline = {"kernel": f"{dom}: {kernels[dom]}", "bound": "tensor", "achieved": d["achieved"], "peak": d["peak"],
                 "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
-                "peak_source": ("measured bf16 dense" if d["bound"] == "tensor" else
-                                "measured bf16 dense x nominal TF32/bf16 ratio 1.1/2.25") + f" ({pk['src']})"}
+                "peak_source": f"bf16 dense ({pk['src']})"}
     scan_roofline = {n: {"achieved": phases[n]["achieved"], "peak": phases[n]["peak"], "frac": phases[n]["frac"],
                          "unit": "TFLOP/s", "of": "measured bf16 dense"} for n in ("fwd_scan", "bwd_scan")}
 
@@ -391,7 +376,7 @@ def run_ours(args):
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
                 "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "e2e": e2e,
-                "clocks": clocks_rec, "gpu_launches": 8 * args.steps, "memset_ops": 5 * args.steps,
+                "clocks": clocks_rec, "gpu_launches": 6 * args.steps, "memset_ops": 5 * args.steps,
                 "peaks": pk, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:

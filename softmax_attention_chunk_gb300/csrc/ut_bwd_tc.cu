@@ -16,7 +16,11 @@
 //   gW = -U^T E3 - X dK-> - Y1 dF + gM1^T Q + gN2 K + diag(beta) gN W + gN^T diag(beta) W
 //   dbeta_j = sum_i gU_ij Y_ij + sum_{m<j} gN_jm G_jm
 // Every product is an M=64 N=64 K=64 tcgen05 MMA on 64x64 bf16 tiles (128-byte swizzled),
-// K-major or MN-major per operand; accumulators gQ, gK, gW stay in TMEM across phases.
+// K-major or MN-major per operand.  The schedule keeps at most four 64-column accumulators in
+// TMEM (256 columns) and thirteen tiles in shared memory (Q and K are re-read by TMA after their
+// slots have served other operands), so that two CTAs share an SM and hide each other's phase
+// latencies.  Accumulator rows are read with the 16x32bx2 shape: every thread of a warp holds
+// 32 columns of one of the warp's 16 rows.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
@@ -27,7 +31,7 @@
 
 namespace pathattn {
 
-bool make_map_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);  // fwd_tc.cu
+bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads);  // fwd_tc.cu
 
 namespace {
 using namespace tc;
@@ -35,30 +39,32 @@ using namespace tc;
 constexpr int B = 64;
 constexpr int D = kHeadDim;
 constexpr uint32_t TILE = 64 * 128;
-constexpr int GS = 65;
-// TMEM columns: temporaries 0..319, persistent accumulators gW, gQ, gK
-constexpr uint32_t C_GW = 320, C_GQ = 384, C_GK = 448;
+constexpr uint32_t C0 = 0, C1 = 64, C2 = 128, C3 = 192;  // TMEM accumulator columns
 
-// Tile slots (a slot is reused once its first tenant is dead).
+// Shared-memory tile slots.  A slot takes a new tenant once every MMA and thread that reads the
+// previous one has finished (phases in brackets).
 enum {
-  T_W, T_Q, T_K,
-  T_V,   // V (P2), then E3 (P7..P8)
-  T_DO,  // dO (P2, P6), then gN2 (P7..P8)
-  T_DQ,  // dQ<- (P6, P7), then gU (P8..P9)
-  T_DK,  // dK-> (P6, P7), then A1 (P9..P10)
-  T_DF,  // dF (P7), then gN (P10..P11)
-  T_M1,  // M1 (P5..P7), then diag(beta) gN (P10..P11)
-  T_N2, T_U, T_Y, T_X,
-  T_Y1,  // Y1 (P6, P7), then diag(beta) W (P9..P11)
-  T_P,   // P (P6), then gX (P6..P8)
-  T_DS, T_GM1, NTILES
+  S_W,   // W [all]
+  S_Q,   // Q [P2] | G fp32 low half [P2-P3] | P [P5-P6] | gM1 [P6-P7] | gU [P8-P9]
+  S_K,   // K [P2] | G fp32 high half [P2-P3] | dS [P5-P8] | diag(beta) W [P8-P11]
+  S_V,   // V [P4] | dF [P4-P7] | gN2 [P7-P8] | A1 [P9-P10]
+  S_DO,  // dO [P4-P6] | gX [P6-P8] | gU.*Y fp32 low half [P8-P9] | diag(beta) gN [P10-P11]
+  S_M1,  // M1 [P2-P7] | gU.*Y fp32 high half [P8-P9]
+  S_N2,  // N2 [P2-P8] | gN [P10-P11]
+  S_U,   // U [P3-P9]
+  S_Y,   // Y [P3-P10]
+  S_DQ,  // dQ<- [P3-P7] | E3 [P7-P8]
+  S_DK,  // dK-> [P3-P6]
+  S_X,   // X [P4-P6] | Q again [P7-P8]
+  S_Y1,  // Y1 [P4-P6] | K again [P7-P8]
+  NSLOT
 };
-constexpr int T_E3 = T_V, T_GN2 = T_DO, T_GU = T_DQ, T_A1 = T_DK, T_GN = T_DF, T_GNB = T_M1, T_BW = T_Y1, T_GX = T_P;
+constexpr int S_G = S_Q, S_P = S_Q, S_GM1 = S_Q, S_GU = S_Q, S_DS = S_K, S_BW = S_K, S_DF = S_V, S_GN2 = S_V,
+              S_A1 = S_V, S_GX = S_DO, S_SCR = S_DO, S_GNB = S_DO, S_GN = S_N2, S_E3 = S_DQ, S_Q2 = S_X,
+              S_K2 = S_Y1;
 
 struct __align__(1024) UbSmem {
-  uint8_t t[NTILES][TILE];
-  float g[B * GS];   // G (strictly lower, fp32)
-  float y[B * GS];   // Y (fp32) for dbeta
+  uint8_t t[NSLOT][TILE];
   float beta[B], lse2[B], dv[B], gb[B];
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
@@ -82,15 +88,30 @@ struct UbParams {
   int* err;
 };
 
-__device__ __forceinline__ void store_bf16_row(__nv_bfloat16* dst, const float* x) {
+// fp32 64x64 matrix over two adjacent slots, element (r, m) at r * 64 + (m ^ 4 (r mod 8)):
+// rows of a warp's 16-byte stores fall on different banks, 4-column groups stay contiguous.
+__device__ __forceinline__ int f32_idx(int r, int m) { return r * 64 + (m ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ void store_bf16_half(__nv_bfloat16* dst, const float* x) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
+  for (int q = 0; q < 4; ++q)
     d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
                        pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
 }
+__device__ __forceinline__ void load_f32_half(const float* src, float* x) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 v = s4[q];
+    x[4 * q] = v.x;
+    x[4 * q + 1] = v.y;
+    x[4 * q + 2] = v.z;
+    x[4 * q + 3] = v.w;
+  }
+}
 
-__global__ void __launch_bounds__(128, 1) ut_bwd64_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v,
                                                          const __grid_constant__ CUtensorMap tm_w,
@@ -104,30 +125,33 @@ __global__ void __launch_bounds__(128, 1) ut_bwd64_kernel(const __grid_constant_
   const size_t in_row = (size_t)bh * p.L;
   const size_t ws_row = (size_t)bh * p.Lp + row0;
   const bool lead = tid == 0;
-  const int i = 16 * warp + lane;  // M=64 accumulator row of this thread (lanes < 16)
-  const bool has_row = lane < 16;
-  const bool row_ok = has_row && row0 + i < p.L;
+  // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
+  const int i = 16 * warp + (lane & 15), h = lane >> 4;
+  const bool row_ok = row0 + i < p.L;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   auto ta = [&](int slot) { return smem_u32(s.t[slot]); };
+  float* sg = reinterpret_cast<float*>(s.t[S_G]);
+  float* scr = reinterpret_cast<float*>(s.t[S_SCR]);
 
   if (lead) {
     mbar_init(&s.bar_in, 1);
     mbar_init(&s.bar_mma, 1);
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&s.tmem_base, 512);
+  if (warp == 1) tmem_alloc(&s.tmem_base, 256);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   uint32_t mph = 0;
-  // Issues the MMAs of one phase (lead thread), then every thread waits for them.
-  auto run = [&](auto issue, int code) {
+  auto issue = [&](auto fn) {  // the lead thread issues one phase's MMAs and commits them
     if (lead) {
       tc_fence_after();
-      issue();
+      fn();
       mma_commit(&s.bar_mma);
     }
+  };
+  auto wait_mma = [&](int code) {
     mbar_wait(&s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
@@ -138,15 +162,14 @@ __global__ void __launch_bounds__(128, 1) ut_bwd64_kernel(const __grid_constant_
     __syncthreads();
   };
 
-  // ---- loads ----
+  // ---- loads: W, Q, K, V, dO by TMA (rows >= L read as zero) ----
   if (lead) {
-    const int y0 = (int)(in_row + row0);
     mbar_arrive_expect_tx(&s.bar_in, 5 * TILE);
-    tma_load_2d(s.t[T_W], &tm_w, 0, y0, &s.bar_in);
-    tma_load_2d(s.t[T_Q], &tm_q, 0, y0, &s.bar_in);
-    tma_load_2d(s.t[T_K], &tm_k, 0, y0, &s.bar_in);
-    tma_load_2d(s.t[T_V], &tm_v, 0, y0, &s.bar_in);
-    tma_load_2d(s.t[T_DO], &tm_do, 0, y0, &s.bar_in);
+    tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_K], &tm_k, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_V], &tm_v, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_DO], &tm_do, 0, row0, bh, &s.bar_in);
   }
   if (tid < B) {
     const int gi = row0 + tid;
@@ -155,291 +178,284 @@ __global__ void __launch_bounds__(128, 1) ut_bwd64_kernel(const __grid_constant_
     s.lse2[tid] = ok ? p.lse[in_row + gi] * kLog2e : INFINITY;
     s.dv[tid] = p.Dv[ws_row + tid];
   }
-  {  // dQ<-, dK->, dF as bf16 operand tiles (2 threads per row, 32 columns each)
-    const int r = tid >> 1, h = tid & 1;
-    const bool ok = row0 + r < p.L;
-    float x[64];
-    const float* dqs = p.dql + (ws_row + r) * D;
-    const float* dks = p.dkr + (ws_row + r) * D;
-    const float* dfs = p.df + (((size_t)bh * p.nc + c) * D + r) * D;
-    for (int j = 0; j < 64; ++j) x[j] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[32 * h + j] = ok ? dqs[32 * h + j] : 0.f;
-    // each thread writes its 4 chunks of 16 bytes (8 bf16) of the row
-#pragma unroll
-    for (int qq = 4 * h; qq < 4 * h + 4; ++qq)
-      *reinterpret_cast<uint4*>(s.t[T_DQ] + r * 128 + ((qq ^ (r & 7)) * 16)) =
-          make_uint4(pack_bf16(x[8 * qq], x[8 * qq + 1]), pack_bf16(x[8 * qq + 2], x[8 * qq + 3]),
-                     pack_bf16(x[8 * qq + 4], x[8 * qq + 5]), pack_bf16(x[8 * qq + 6], x[8 * qq + 7]));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[32 * h + j] = ok ? dks[32 * h + j] : 0.f;
-#pragma unroll
-    for (int qq = 4 * h; qq < 4 * h + 4; ++qq)
-      *reinterpret_cast<uint4*>(s.t[T_DK] + r * 128 + ((qq ^ (r & 7)) * 16)) =
-          make_uint4(pack_bf16(x[8 * qq], x[8 * qq + 1]), pack_bf16(x[8 * qq + 2], x[8 * qq + 3]),
-                     pack_bf16(x[8 * qq + 4], x[8 * qq + 5]), pack_bf16(x[8 * qq + 6], x[8 * qq + 7]));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[32 * h + j] = dfs[32 * h + j];
-#pragma unroll
-    for (int qq = 4 * h; qq < 4 * h + 4; ++qq)
-      *reinterpret_cast<uint4*>(s.t[T_DF] + r * 128 + ((qq ^ (r & 7)) * 16)) =
-          make_uint4(pack_bf16(x[8 * qq], x[8 * qq + 1]), pack_bf16(x[8 * qq + 2], x[8 * qq + 3]),
-                     pack_bf16(x[8 * qq + 4], x[8 * qq + 5]), pack_bf16(x[8 * qq + 6], x[8 * qq + 7]));
-  }
   mbar_wait(&s.bar_in, 0, p.err, 41);
-  if (row0 + B > p.L) {  // rows beyond L are zero
-    for (int r = tid; r < B; r += 128)
-      if (row0 + r >= p.L)
-        for (int si = 0; si < 5; ++si) {
-          const int slot = si == 0 ? T_W : si == 1 ? T_Q : si == 2 ? T_K : si == 3 ? T_V : T_DO;
-          for (int qq = 0; qq < 8; ++qq) reinterpret_cast<uint4*>(s.t[slot] + r * 128)[qq] = make_uint4(0, 0, 0, 0);
-        }
-  }
   publish();
 
-  // ---- P2: G, M1, N2, QK^T, dP ----
-  run([&] {
-    mma64(tb + 0, ta(T_W), 0, ta(T_W), 0, 0);
-    mma64(tb + 64, ta(T_Q), 0, ta(T_W), 0, 0);
-    mma64(tb + 128, ta(T_W), 0, ta(T_K), 0, 0);
-    mma64(tb + 192, ta(T_Q), 0, ta(T_K), 0, 0);
-    mma64(tb + 256, ta(T_DO), 0, ta(T_V), 0, 0);
-  }, 42);
+  // ---- P2: G = W W^T, M1 = Q W^T, N2 = W K^T, Q K^T ----
+  issue([&] {
+    mma64(tb + C0, ta(S_W), 0, ta(S_W), 0, 0);
+    mma64(tb + C1, ta(S_Q), 0, ta(S_W), 0, 0);
+    mma64(tb + C2, ta(S_W), 0, ta(S_K), 0, 0);
+    mma64(tb + C3, ta(S_Q), 0, ta(S_K), 0, 0);
+  });
+  wait_mma(42);
   {
-    float x[64];
-    ld_row(tb, lane_off, 0, x);
-    if (has_row) {
+    float x[32];
+    ld_half(tb, lane_off, C0, x);  // G, strictly lower, fp32 into the slots of Q and K
 #pragma unroll
-      for (int j = 0; j < 64; ++j) s.g[i * GS + j] = j < i ? x[j] : 0.f;
+    for (int q = 0; q < 8; ++q) {
+      const int j = 32 * h + 4 * q;
+      *reinterpret_cast<float4*>(sg + f32_idx(i, j)) =
+          make_float4(j < i ? x[4 * q] : 0.f, j + 1 < i ? x[4 * q + 1] : 0.f, j + 2 < i ? x[4 * q + 2] : 0.f,
+                      j + 3 < i ? x[4 * q + 3] : 0.f);
     }
-    ld_row(tb, lane_off, 64, x);
-    if (has_row) {
+    ld_half(tb, lane_off, C1, x);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = j <= i ? x[j] : 0.f;
-      put_row(s.t[T_M1], i, x);
-    }
-    ld_row(tb, lane_off, 128, x);
-    if (has_row) {
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
+    put_half(s.t[S_M1], i, h, x);
+    ld_half(tb, lane_off, C2, x);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = j < i ? x[j] : 0.f;
-      put_row(s.t[T_N2], i, x);
-    }
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
+    put_half(s.t[S_N2], i, h, x);
   }
   publish();
 
-  // ---- P3: Y = T^{-1} (fp32 forward substitution, lane = column), U = Y diag(beta) ----
+  // ---- P3: Y = (I + strictLower(D G))^{-1} by forward substitution (warps 0-1, lane = column),
+  //      U = Y D; warps 2-3 meanwhile turn dQ<- and dK-> into bf16 operand tiles ----
   if (warp < 2) {
     const int cc = 32 * warp + lane;
     float yc[64];
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      float a0 = 0.f, a1 = 0.f;
+    for (int r = 0; r < 64; ++r) yc[r] = 0.f;  // G_rm = 0 for m >= r: unsolved entries add nothing
 #pragma unroll
-      for (int m = 0; m + 1 < r; m += 2) {
-        a0 += s.g[r * GS + m] * yc[m];
-        a1 += s.g[r * GS + m + 1] * yc[m + 1];
+    for (int r = 0; r < 64; ++r) {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int m = 0; m < r; m += 4) {
+        const float4 gv = *reinterpret_cast<const float4*>(sg + f32_idx(r, m));
+        a0 += gv.x * yc[m];
+        a1 += gv.y * yc[m + 1];
+        a2 += gv.z * yc[m + 2];
+        a3 += gv.w * yc[m + 3];
       }
-      if (r & 1) a0 += s.g[r * GS + r - 1] * yc[r - 1];
-      yc[r] = (cc == r ? 1.f : 0.f) - s.beta[r] * (a0 + a1);
+      yc[r] = (cc == r ? 1.f : 0.f) - s.beta[r] * ((a0 + a1) + (a2 + a3));
     }
     const float bc = s.beta[cc];
 #pragma unroll
     for (int r = 0; r < 64; ++r) {
-      s.y[r * GS + cc] = yc[r];
-      *reinterpret_cast<__nv_bfloat16*>(s.t[T_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r]);
-      *reinterpret_cast<__nv_bfloat16*>(s.t[T_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r] * bc);
+      *reinterpret_cast<__nv_bfloat16*>(s.t[S_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r]);
+      *reinterpret_cast<__nv_bfloat16*>(s.t[S_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r] * bc);
     }
-  }
-  publish();
-
-  // ---- P4: X = U N2, Y1 = U W ----
-  run([&] {
-    mma64(tb + 0, ta(T_U), 0, ta(T_N2), 1, 0);
-    mma64(tb + 64, ta(T_U), 0, ta(T_W), 1, 0);
-  }, 43);
-  {
-    float x[64];
-    ld_row(tb, lane_off, 0, x);
-    if (has_row) put_row(s.t[T_X], i, x);
-    ld_row(tb, lane_off, 64, x);
-    if (has_row) put_row(s.t[T_Y1], i, x);
-  }
-  publish();
-
-  // ---- P5: S_d = QK^T - M1 X ; P ; dS = scale P (dP - D) ----
-  run([&] { mma64(tb + 192, ta(T_M1), 0, ta(T_X), 1, 1, 1); }, 44);
-  {
-    float sx[64], dp[64];
-    ld_row(tb, lane_off, 192, sx);
-    ld_row(tb, lane_off, 256, dp);
-    if (has_row) {
+  } else {
+    const int r = tid - 64;
+    const bool ok = row0 + r < p.L;
+    float x[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float pj = (j <= i && row_ok) ? fast_exp2(sx[j] * p.scl - s.lse2[i]) : 0.f;
-        sx[j] = pj;
-        dp[j] = p.scale * pj * (dp[j] - s.dv[i]);
-      }
-      put_row(s.t[T_P], i, sx);
-      put_row(s.t[T_DS], i, dp);
+    for (int hh = 0; hh < 2; ++hh) {
+      if (ok) load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, x);
+      else
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      put_half(s.t[S_DQ], r, hh, x);
+      if (ok) load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, x);
+      else
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      put_half(s.t[S_DK], r, hh, x);
     }
   }
   publish();
 
-  // ---- P6: dvp = P^T dO ; gQ = dS K ; gK = dS^T Q ; gM1 = -dS X^T - dQ<- Y1^T ; gX = -M1^T dS - W dK->^T ----
-  run([&] {
-    mma64(tb + 0, ta(T_P), 1, ta(T_DO), 1, 0);
-    mma64(tb + C_GQ, ta(T_DS), 0, ta(T_K), 1, 0);
-    mma64(tb + C_GK, ta(T_DS), 1, ta(T_Q), 1, 0);
-    mma64(tb + 64, ta(T_DS), 0, ta(T_X), 0, 0, 1);
-    mma64(tb + 64, ta(T_DQ), 0, ta(T_Y1), 0, 1, 1);
-    mma64(tb + 128, ta(T_M1), 1, ta(T_DS), 1, 0, 1);
-    mma64(tb + 128, ta(T_W), 0, ta(T_DK), 0, 1, 1);
-  }, 45);
+  // ---- P4: X = U N2, Y1 = U W, dP = dO V^T ----
+  issue([&] {
+    mma64(tb + C0, ta(S_U), 0, ta(S_N2), 1, 0);
+    mma64(tb + C1, ta(S_U), 0, ta(S_W), 1, 0);
+    mma64(tb + C2, ta(S_DO), 0, ta(S_V), 0, 0);
+  });
+  wait_mma(43);
   {
-    float x[64];
-    ld_row(tb, lane_off, 0, x);
+    float x[32];
+    ld_half(tb, lane_off, C0, x);
+    put_half(s.t[S_X], i, h, x);
+    ld_half(tb, lane_off, C1, x);
+    put_half(s.t[S_Y1], i, h, x);
+    // dF as a bf16 tile in V's slot: row tid/2, half tid%2
+    const int r = tid >> 1, hh = tid & 1;
+    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D + 32 * hh, x);
+    put_half(s.t[S_DF], r, hh, x);
+  }
+  publish();
+
+  // ---- P5: S_d = Q K^T - M1 X ; P ; dS = scale P (dP - D_i) ----
+  issue([&] { mma64(tb + C3, ta(S_M1), 0, ta(S_X), 1, 1, 1); });
+  wait_mma(44);
+  {
+    float sx[32], dp[32];
+    ld_half(tb, lane_off, C3, sx);
+    ld_half(tb, lane_off, C2, dp);
+    const float l2 = s.lse2[i], dvi = s.dv[i];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float pj = (32 * h + j <= i && row_ok) ? fast_exp2(sx[j] * p.scl - l2) : 0.f;
+      sx[j] = pj;
+      dp[j] = p.scale * pj * (dp[j] - dvi);
+    }
+    put_half(s.t[S_P], i, h, sx);
+    put_half(s.t[S_DS], i, h, dp);
+  }
+  publish();
+
+  // ---- P6: dV_diag = P^T dO ; gM1 = -dS X^T - dQ<- Y1^T ; gX = -M1^T dS - W dK->^T ;
+  //          gW = -X dK-> - Y1 dF ----
+  issue([&] {
+    mma64(tb + C0, ta(S_P), 1, ta(S_DO), 1, 0);
+    mma64(tb + C1, ta(S_DS), 0, ta(S_X), 0, 0, 1);
+    mma64(tb + C1, ta(S_DQ), 0, ta(S_Y1), 0, 1, 1);
+    mma64(tb + C2, ta(S_M1), 1, ta(S_DS), 1, 0, 1);
+    mma64(tb + C2, ta(S_W), 0, ta(S_DK), 0, 1, 1);
+    mma64(tb + C3, ta(S_X), 0, ta(S_DK), 1, 0, 1);
+    mma64(tb + C3, ta(S_Y1), 0, ta(S_DF), 1, 1, 1);
+  });
+  wait_mma(45);
+  if (lead) {  // X and Y1 are consumed: Q and K come back into their slots
+    mbar_arrive_expect_tx(&s.bar_in, 2 * TILE);
+    tma_load_3d(s.t[S_Q2], &tm_q, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_K2], &tm_k, 0, row0, bh, &s.bar_in);
+  }
+  {
+    float x[32], a[32];
+    ld_half(tb, lane_off, C0, x);
     if (row_ok) {
-      const size_t orow = in_row + row0 + i;
-      const float* acc = p.dvacc + (ws_row + i) * D;
+      load_f32_half(p.dvacc + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] += acc[j];
-      store_bf16_row(p.dv + orow * D, x);
+      for (int j = 0; j < 32; ++j) x[j] += a[j];
+      store_bf16_half(p.dv + (in_row + row0 + i) * D + 32 * h, x);
     }
-    ld_row(tb, lane_off, 64, x);
-    if (has_row) {
+    ld_half(tb, lane_off, C1, x);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = j <= i ? x[j] : 0.f;
-      put_row(s.t[T_GM1], i, x);
-    }
-    ld_row(tb, lane_off, 128, x);
-    if (has_row) put_row(s.t[T_GX], i, x);
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
+    put_half(s.t[S_GM1], i, h, x);
+    ld_half(tb, lane_off, C2, x);
+    put_half(s.t[S_GX], i, h, x);
   }
   publish();
 
-  // ---- P7: E3 = M1^T dQ<- + W dF^T ; gN2 = U^T gX ; gW = -X dK-> - Y1 dF + gM1^T Q ; gQ += gM1 W ----
-  run([&] {
-    mma64(tb + 0, ta(T_M1), 1, ta(T_DQ), 1, 0);
-    mma64(tb + 0, ta(T_W), 0, ta(T_DF), 0, 1);
-    mma64(tb + 64, ta(T_U), 1, ta(T_GX), 1, 0);
-    mma64(tb + C_GW, ta(T_X), 0, ta(T_DK), 1, 0, 1);
-    mma64(tb + C_GW, ta(T_Y1), 0, ta(T_DF), 1, 1, 1);
-    mma64(tb + C_GW, ta(T_GM1), 1, ta(T_Q), 1, 1);
-    mma64(tb + C_GQ, ta(T_GM1), 0, ta(T_W), 1, 1);
-  }, 46);
+  // ---- P7: gQ = dS K + gM1 W ; E3 = M1^T dQ<- + W dF^T ; gN2 = U^T gX ; gW += gM1^T Q ----
+  if (lead) mbar_wait(&s.bar_in, 1, p.err, 46);
+  issue([&] {
+    mma64(tb + C0, ta(S_DS), 0, ta(S_K2), 1, 0);
+    mma64(tb + C0, ta(S_GM1), 0, ta(S_W), 1, 1);
+    mma64(tb + C1, ta(S_M1), 1, ta(S_DQ), 1, 0);
+    mma64(tb + C1, ta(S_W), 0, ta(S_DF), 0, 1);
+    mma64(tb + C2, ta(S_U), 1, ta(S_GX), 1, 0);
+    mma64(tb + C3, ta(S_GM1), 1, ta(S_Q2), 1, 1);
+  });
+  wait_mma(47);
   {
-    float x[64];
-    ld_row(tb, lane_off, 0, x);
-    if (has_row) put_row(s.t[T_E3], i, x);
-    ld_row(tb, lane_off, 64, x);
-    if (has_row) {
+    float x[32], a[32];
+    ld_half(tb, lane_off, C0, x);
+    if (row_ok) {
+      load_f32_half(p.dql + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = j < i ? x[j] : 0.f;
-      put_row(s.t[T_GN2], i, x);
+      for (int j = 0; j < 32; ++j) x[j] += a[j];
+      store_bf16_half(p.dq + (in_row + row0 + i) * D + 32 * h, x);
     }
+    ld_half(tb, lane_off, C1, x);
+    put_half(s.t[S_E3], i, h, x);
+    ld_half(tb, lane_off, C2, x);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
+    put_half(s.t[S_GN2], i, h, x);
   }
   publish();
 
-  // ---- P8: gU = -E3 W^T + gX N2^T ; gW += -U^T E3 + gN2 K ; gK += gN2^T W ----
-  run([&] {
-    mma64(tb + 0, ta(T_E3), 0, ta(T_W), 0, 0, 1);
-    mma64(tb + 0, ta(T_GX), 0, ta(T_N2), 0, 1);
-    mma64(tb + C_GW, ta(T_U), 1, ta(T_E3), 1, 1, 1);
-    mma64(tb + C_GW, ta(T_GN2), 0, ta(T_K), 1, 1);
-    mma64(tb + C_GK, ta(T_GN2), 1, ta(T_W), 1, 1);
-  }, 47);
+  // ---- P8: gK = dS^T Q + gN2^T W ; gU = -E3 W^T + gX N2^T ; gW += -U^T E3 + gN2 K ----
+  issue([&] {
+    mma64(tb + C0, ta(S_DS), 1, ta(S_Q2), 1, 0);
+    mma64(tb + C0, ta(S_GN2), 1, ta(S_W), 1, 1);
+    mma64(tb + C1, ta(S_E3), 0, ta(S_W), 0, 0, 1);
+    mma64(tb + C1, ta(S_GX), 0, ta(S_N2), 0, 1);
+    mma64(tb + C3, ta(S_U), 1, ta(S_E3), 1, 1, 1);
+    mma64(tb + C3, ta(S_GN2), 0, ta(S_K2), 1, 1);
+  });
+  wait_mma(48);
   {
-    float x[64];
-    ld_row(tb, lane_off, 0, x);
-    if (has_row) {
+    float x[32], a[32];
+    ld_half(tb, lane_off, C0, x);
+    if (row_ok) {
+      load_f32_half(p.dkr + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = j <= i ? x[j] : 0.f;
-      put_row(s.t[T_GU], i, x);
-      // gU .* Y in place of Y (its fp32 copy has no other use); column sums give dbeta
-#pragma unroll
-      for (int j = 0; j < 64; ++j) s.y[i * GS + j] *= x[j];
+      for (int j = 0; j < 32; ++j) x[j] += a[j];
+      store_bf16_half(p.dk + (in_row + row0 + i) * D + 32 * h, x);
     }
-  }
-  // diag(beta) W (Y1's slot is free now)
-  if (tid < B) {
-    float x[64];
-    get_row(s.t[T_W], tid, x);
-    const float bt = s.beta[tid];
+    ld_half(tb, lane_off, C1, x);
 #pragma unroll
-    for (int j = 0; j < 64; ++j) x[j] *= bt;
-    put_row(s.t[T_BW], tid, x);
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
+    put_half(s.t[S_GU], i, h, x);
+    // gU .* Y (fp32) for the column sums that give dbeta
+    get_half(s.t[S_Y], i, h, a);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(scr + f32_idx(i, 32 * h + 4 * q)) =
+          make_float4(x[4 * q] * a[4 * q], x[4 * q + 1] * a[4 * q + 1], x[4 * q + 2] * a[4 * q + 2],
+                      x[4 * q + 3] * a[4 * q + 3]);
+    // diag(beta) W
+    get_half(s.t[S_W], i, h, x);
+    const float bi = s.beta[i];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] *= bi;
+    put_half(s.t[S_BW], i, h, x);
   }
   publish();
 
-  // ---- P9: A1 = gU U^T ; dbeta_j = sum_i gU_ij Y_ij ----
-  run([&] { mma64(tb + 64, ta(T_GU), 0, ta(T_U), 0, 0); }, 48);
+  // ---- P9: A1 = gU U^T ; G again (for dbeta) ; dbeta_j = sum_i gU_ij Y_ij ----
+  issue([&] {
+    mma64(tb + C0, ta(S_GU), 0, ta(S_U), 0, 0);
+    mma64(tb + C2, ta(S_W), 0, ta(S_W), 0, 0);
+  });
   if (tid < B) {
     float acc = 0.f;
-    for (int r = tid; r < B; ++r) acc += s.y[r * GS + tid];
+    for (int r = tid; r < B; ++r) acc += scr[f32_idx(r, tid)];
     s.gb[tid] = acc;
   }
+  wait_mma(49);
   {
-    float x[64];
-    ld_row(tb, lane_off, 64, x);
-    if (has_row) put_row(s.t[T_A1], i, x);
+    float x[32];
+    ld_half(tb, lane_off, C0, x);
+    put_half(s.t[S_A1], i, h, x);
   }
   publish();
 
   // ---- P10: gN = strictLower(-Y^T A1) ; dbeta_i += sum_{j<i} gN_ij G_ij ----
-  run([&] { mma64(tb + 128, ta(T_Y), 1, ta(T_A1), 1, 0, 1); }, 49);
+  issue([&] { mma64(tb + C1, ta(S_Y), 1, ta(S_A1), 1, 0, 1); });
+  wait_mma(50);
   {
-    float x[64];
-    ld_row(tb, lane_off, 128, x);
-    if (has_row) {
-      float acc = 0.f;
+    float x[32], g[32];
+    ld_half(tb, lane_off, C1, x);
+    ld_half(tb, lane_off, C2, g);
+    float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        x[j] = j < i ? x[j] : 0.f;
-        acc += x[j] * s.g[i * GS + j];
-      }
-      s.gb[i] += acc;
-      put_row(s.t[T_GN], i, x);
-      const float bi = s.beta[i];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] *= bi;
-      put_row(s.t[T_GNB], i, x);
+    for (int j = 0; j < 32; ++j) {
+      x[j] = 32 * h + j < i ? x[j] : 0.f;
+      acc += x[j] * g[j];
     }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+    if (h == 0) s.gb[i] += acc;
+    put_half(s.t[S_GN], i, h, x);
+    const float bi = s.beta[i];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] *= bi;
+    put_half(s.t[S_GNB], i, h, x);
   }
   publish();
 
-  // ---- P11: gW += diag(beta) gN W + gN^T diag(beta) W ----
-  run([&] {
-    mma64(tb + C_GW, ta(T_GNB), 0, ta(T_W), 1, 1);
-    mma64(tb + C_GW, ta(T_GN), 1, ta(T_BW), 1, 1);
-  }, 50);
-
-  // ---- outputs ----
+  // ---- P11: gW += diag(beta) gN W + gN^T diag(beta) W ; outputs dw, dbeta ----
+  issue([&] {
+    mma64(tb + C3, ta(S_GNB), 0, ta(S_W), 1, 1);
+    mma64(tb + C3, ta(S_GN), 1, ta(S_BW), 1, 1);
+  });
+  wait_mma(51);
   {
-    float x[64];
-    const size_t orow = in_row + row0 + i;
-    ld_row(tb, lane_off, C_GQ, x);
-    if (row_ok) {
-      const float* a = p.dql + (ws_row + i) * D;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] += a[j];
-      store_bf16_row(p.dq + orow * D, x);
-    }
-    ld_row(tb, lane_off, C_GK, x);
-    if (row_ok) {
-      const float* a = p.dkr + (ws_row + i) * D;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] += a[j];
-      store_bf16_row(p.dk + orow * D, x);
-    }
-    ld_row(tb, lane_off, C_GW, x);
-    if (row_ok) store_bf16_row(p.dw + orow * D, x);
+    float x[32];
+    ld_half(tb, lane_off, C3, x);
+    if (row_ok) store_bf16_half(p.dw + (in_row + row0 + i) * D + 32 * h, x);
   }
-  __syncthreads();
-  if (tid < B && row0 + tid < p.L) p.dbeta[in_row + row0 + tid] = s.gb[tid];
   tc_fence_before();
   __syncthreads();
+  if (tid < B && row0 + tid < p.L) p.dbeta[in_row + row0 + tid] = s.gb[tid];
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tb, 512);
+    tmem_dealloc(tb, 256);
   }
 }
 
@@ -451,9 +467,9 @@ cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const v
                             void* dw, float* dbeta, int* err, cudaStream_t st) {
   if (g.B != 64) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv, mw, mdo;
-  const uint64_t rows = (uint64_t)g.BH * g.L;
-  if (!make_map_rows64(&mq, q, rows, B) || !make_map_rows64(&mk, k, rows, B) || !make_map_rows64(&mv, v, rows, B) ||
-      !make_map_rows64(&mw, w, rows, B) || !make_map_rows64(&mdo, dO, rows, B))
+  if (!make_map_head_rows64(&mq, q, g.L, g.BH) || !make_map_head_rows64(&mk, k, g.L, g.BH) ||
+      !make_map_head_rows64(&mv, v, g.L, g.BH) || !make_map_head_rows64(&mw, w, g.L, g.BH) ||
+      !make_map_head_rows64(&mdo, dO, g.L, g.BH))
     return cudaErrorInvalidValue;
   UbParams p;
   p.L = g.L;
@@ -477,6 +493,9 @@ cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const v
   p.err = err;
   const size_t smem = sizeof(UbSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(ut_bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ut_bwd64_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   ut_bwd64_kernel<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, mdo, p);
   return cudaGetLastError();

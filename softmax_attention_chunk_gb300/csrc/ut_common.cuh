@@ -60,6 +60,41 @@ __device__ __forceinline__ void ld_row(uint32_t tb, uint32_t lane_off, uint32_t 
   }
 }
 
+// Half rows: 32 columns (half h) of row r of a swizzled bf16 tile.
+__device__ __forceinline__ void put_half(uint8_t* tile, int r, int h, const float* x) {
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 pk;
+    pk.x = pack_bf16(x[8 * q], x[8 * q + 1]);
+    pk.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
+    pk.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
+    pk.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
+    *reinterpret_cast<uint4*>(row + (((4 * h + q) ^ (r & 7)) * 16)) = pk;
+  }
+}
+__device__ __forceinline__ void get_half(const uint8_t* tile, int r, int h, float* x) {
+  const uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 pk = *reinterpret_cast<const uint4*>(row + (((4 * h + q) ^ (r & 7)) * 16));
+    const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[8 * q + 2 * e] = __uint_as_float(wv[e] << 16);
+      x[8 * q + 2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+    }
+  }
+}
+// This thread's half row of an M=64 accumulator at TMEM column col: row 16 * warp + lane % 16,
+// columns col + 32 * (lane / 16) .. + 31.
+__device__ __forceinline__ void ld_half(uint32_t tb, uint32_t lane_off, uint32_t col, float* x) {
+  uint32_t a[32];
+  tmem_ld16x2(tb + lane_off + col, a);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(a[j]);
+}
 
 }  // namespace tc
 }  // namespace pathattn
