@@ -165,9 +165,18 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 }
 
 // ============================ adjoint scan ============================
+// Per step k (chunk c, transported queries Z_n, n = nsteps - 1 - k) the MMA issuer runs
+//   S_{k+1} = Z K->^T, dP_{k+1} = dO V^T          (one step ahead, for the softmax side)
+//   [dK->_c ; dF_c] = [dS^T ; G_{n+1}^T] Z_n      (one M=128 MMA: dS and G tiles are adjacent and
+//                                                  form one MN-major operand with LBO = one tile)
+//   G_n = dS K->_c + G_{n+1} F_c
+//   dV_c = P^T dO
+// with the dV / [dK->; dF] accumulators double-buffered in TMEM, so that the gradient side drains
+// step k while step k+1 computes.
 constexpr int BS_NSTAGE = 2;
 constexpr int SROW = D + 4;  // staging row stride (floats): 16-byte aligned, spreads rows over banks
-constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DK = 256, TM_DF = 320;
+// TMEM columns: S, dP, G_n, accumulator buffers (dV at +0, [dK->; dF] at +64), G_0 of a partial step
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_ACC0 = 192, TM_ACC1 = 320, TM_G2 = 448;
 
 struct __align__(1024) BsStage {
   uint8_t z[ZTILE];        // Z_n
@@ -176,15 +185,15 @@ struct __align__(1024) BsStage {
   uint8_t f[BK * 128];     // F_c
 };
 struct __align__(1024) BsSmem {
-  uint8_t dO[ZTILE];
-  BsStage st[BS_NSTAGE];
   uint8_t ps[ZTILE];       // P  (bf16, rows x keys)
   uint8_t ds[ZTILE];       // dS (bf16, rows x keys), scale included
-  uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d)
-  float stash[64 * D];     // fp32 G_1 of the lower rows (tile with a partial step)
-  float stg[3][64 * SROW]; // dV, dK->, dF of the step (fp32 rows padded to SROW) for the bulk reductions
+  uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d); follows ds (stacked operand)
+  uint8_t dO[ZTILE];
+  BsStage st[BS_NSTAGE];
+  float stg_v[BK * SROW];    // dV of a step (fp32 rows) for the bulk reductions
+  float stg_kf[BQ * SROW];   // dK-> (rows 0-63) and dF (rows 64-127) of a step
   uint64_t full[BS_NSTAGE], empty[BS_NSTAGE];
-  uint64_t do_full, sp_full, ps_ready, g_full, g_free;
+  uint64_t do_full, sp_full, ps_ready, g_full, gs_ready, acc_full[2], acc_free[2];
   uint32_t tmem_base;
 };
 
@@ -215,7 +224,7 @@ __device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const fl
 }
 
 // Warp roles: 0-3 softmax side (P, dS of a step), 4 TMA/bulk producer, 5 MMA issuer,
-// 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions of the previous step).
+// 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions).
 constexpr int BS_THREADS = 320;
 __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
                                                             const __grid_constant__ CUtensorMap tm_kr,
@@ -245,7 +254,11 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     mbar_init(&s.sp_full, 1);
     mbar_init(&s.ps_ready, 128);
     mbar_init(&s.g_full, 1);
-    mbar_init(&s.g_free, 128);
+    mbar_init(&s.gs_ready, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.acc_full[b], 1);
+      mbar_init(&s.acc_free[b], 128);
+    }
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -277,18 +290,12 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     if (lane == 0) {
       const uint32_t i_rk = idesc_bf16(128, 64, 0, 0);   // [128 x 64] = A(K-major) B(K-major)^T
       const uint32_t i_rm = idesc_bf16(128, 64, 0, 1);   // [128 x 64] = A(K-major) B(MN-major)
-      const uint32_t i_tt = idesc_bf16(64, 64, 1, 1);    // [64 x 64]  = A(MN-major)^T-style product
+      const uint32_t i_tt = idesc_bf16(64, 64, 1, 1);    // [64 x 64]  = A(MN-major) B(MN-major)
+      const uint32_t i_st = idesc_bf16(128, 64, 1, 1);   // [128 x 64] = A(MN-major, two atoms) B(MN-major)
       const uint32_t a_do = smem_u32(s.dO), a_ps = smem_u32(s.ps), a_ds = smem_u32(s.ds), a_gs = smem_u32(s.gs);
-      bool ok = mbar_wait(&s.do_full, 0, p.err, 22);
-      for (int k = 0; ok && k < nsteps; ++k) {
-        const int si = k % BS_NSTAGE;
-        const int n = nsteps - 1 - k;
-        const bool partial = has_partial && n == 0;
-        if (!mbar_wait(&s.full[si], (k / BS_NSTAGE) & 1, p.err, 23)) { ok = false; break; }
-        tc_fence_after();
-        const BsStage& S = s.st[si];
-        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v), a_f = smem_u32(S.f);
-        // S = Z K->^T, dP = dO V^T
+      auto issue_sdp = [&](int k) {  // S and dP of step k
+        const BsStage& S = s.st[k % BS_NSTAGE];
+        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tb + TM_S, sdesc_sw128(a_z + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 32 * kk, 1024, 16), i_rk, kk > 0);
@@ -296,34 +303,57 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tb + TM_DP, sdesc_sw128(a_do + 32 * kk, 1024, 16), sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
         mma_commit(&s.sp_full);
-        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
-        // the gradient side has read G/dV/dK->/dF of the previous step and written G_{n+1}
-        if (k > 0 && !mbar_wait(&s.g_free, (k - 1) & 1, p.err, 27)) { ok = false; break; }
+      };
+      bool ok = mbar_wait(&s.do_full, 0, p.err, 22) && mbar_wait(&s.full[0], 0, p.err, 23);
+      if (ok) {
         tc_fence_after();
-        // dV = P^T dO, dK-> = dS^T Z  (M = 64 keys, K = 128 rows)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb + TM_DV, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb + TM_DK, sdesc_sw128(a_ds + 2048 * kk, 1024, 0), sdesc_sw128(a_z + 2048 * kk, 1024, 0), i_tt, kk > 0);
-        // G_n = dS K->_c + G_{n+1} F_c
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tb + TM_G, sdesc_sw128(a_ds + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 2048 * kk, 1024, 0), i_rm, kk > 0);
-        if (k > 0) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tb + TM_G, sdesc_sw128(a_gs + 32 * kk, 1024, 16), sdesc_sw128(a_f + 2048 * kk, 1024, 0), i_rm, 1);
-          // dF_c = G_{n+1}^T Z_n over the rows that crossed chunk c
+        issue_sdp(0);
+      }
+      for (int k = 0; ok && k < nsteps; ++k) {
+        const int si = k % BS_NSTAGE, b = k & 1;
+        const int n = nsteps - 1 - k;
+        const bool partial = has_partial && n == 0;
+        // the softmax side has read S/dP of step k and written its P / dS tiles
+        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
+        if (k + 1 < nsteps) {
+          if (!mbar_wait(&s.full[(k + 1) % BS_NSTAGE], ((k + 1) / BS_NSTAGE) & 1, p.err, 23)) { ok = false; break; }
+          tc_fence_after();
+          issue_sdp(k + 1);
+        }
+        // G_{n+1} is in gs (zero before the first step) and G_{n+1} has left TM_G
+        if (!mbar_wait(&s.gs_ready, k & 1, p.err, 27)) { ok = false; break; }
+        // the gradient side has drained accumulator buffer b (step k - 2)
+        if (k >= 2 && !mbar_wait(&s.acc_free[b], ((k - 2) >> 1) & 1, p.err, 29)) { ok = false; break; }
+        tc_fence_after();
+        const BsStage& S = s.st[si];
+        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_f = smem_u32(S.f);
+        const uint32_t acc = b ? TM_ACC1 : TM_ACC0;
+        // [dK->; dF] = [dS^T; G_{n+1}^T] Z_n over the rows that crossed chunk c (rows 64-127 at a
+        // partial step, where dS of rows 0-63 is zero anyway)
+        {
           const uint32_t off = partial ? 64 * 128 : 0;
           const int nk = partial ? 4 : 8;
           for (int kk = 0; kk < nk; ++kk)
-            mma_ss(tb + TM_DF, sdesc_sw128(a_gs + off + 2048 * kk, 1024, 0),
-                   sdesc_sw128(a_z + off + 2048 * kk, 1024, 0), i_tt, kk > 0);
+            mma_ss(tb + acc + 64, sdesc_sw128(a_ds + off + 2048 * kk, 1024, ZTILE),
+                   sdesc_sw128(a_z + off + 2048 * kk, 1024, 0), i_st, kk > 0);
         }
-        mma_commit(&s.empty[si]);
+        // G_n = dS K->_c + G_{n+1} F_c  (a partial step keeps G_1 of rows 0-63 in TM_G)
+        const uint32_t tg = partial ? TM_G2 : TM_G;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tb + tg, sdesc_sw128(a_ds + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 2048 * kk, 1024, 0), i_rm, kk > 0);
+        if (k > 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tb + tg, sdesc_sw128(a_gs + 32 * kk, 1024, 16), sdesc_sw128(a_f + 2048 * kk, 1024, 0), i_rm, 1);
+        }
         mma_commit(&s.g_full);
+        // dV = P^T dO  (M = 64 keys, K = 128 rows)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tb + acc, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
+        mma_commit(&s.acc_full[b]);
+        mma_commit(&s.empty[si]);
       }
     }
   } else if (warp < 4) {
@@ -356,8 +386,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
         dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
       }
-      // the MMAs of the previous step read the P / dS tiles
-      if (k > 0 && !mbar_wait(&s.g_full, (k - 1) & 1, p.err, 26)) break;
+      // the MMAs of step k-1 have read the P / dS tiles
+      if (k > 0 && !mbar_wait(&s.acc_full[(k - 1) & 1], ((k - 1) >> 1) & 1, p.err, 26)) break;
       store_row_bf16_sw(s.ps, r, pv);
       store_row_bf16_sw(s.ds, r, dsv);
       fence_proxy_async_smem();
@@ -370,20 +400,28 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     const int rg = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + rg;
-    const int mrow = 16 * q4 + lane;  // M=64 accumulators: row 16q+l sits in lane l of quarter q
-    if (rg < 64)
-      for (int j = 0; j < D; ++j) s.stash[rg * D + j] = 0.f;
+    const int vrow = 16 * q4 + (lane & 15), vh = lane >> 4;  // dV (M=64) half row of this thread
+    {  // G_{nsteps} = 0
+      uint4* row = reinterpret_cast<uint4*>(s.gs + rg * 128);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+      mbar_arrive(&s.gs_ready);
+    }
     for (int k = 0; k < nsteps; ++k) {
       const int n = nsteps - 1 - k;
       const bool partial = has_partial && n == 0;
       const int c = step_chunk(has_partial, T, n);
+      const int b = k & 1;
+      const uint32_t acc = b ? TM_ACC1 : TM_ACC0;
       if (!mbar_wait(&s.g_full, k & 1, p.err, 28)) break;
       tc_fence_after();
-      // G_n
+      // G_n (rows 0-63 of a partial step keep G_1)
       {
+        const uint32_t tg = (partial && rg >= 64) ? TM_G2 : TM_G;
         uint32_t ga[32], gb[32];
-        tmem_ld32(tb + lane_off + TM_G, ga);
-        tmem_ld32(tb + lane_off + TM_G + 32, gb);
+        tmem_ld32(tb + lane_off + tg, ga);
+        tmem_ld32(tb + lane_off + tg + 32, gb);
         tmem_ld_wait();
         float g[64];
 #pragma unroll
@@ -391,13 +429,9 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           g[j] = __uint_as_float(ga[j]);
           g[32 + j] = __uint_as_float(gb[j]);
         }
-        if (partial && rg < 64) {
+        if (partial && rg < 64 && k == 0) {  // a tile whose only step is the partial one: G_1 = 0
 #pragma unroll
-          for (int j = 0; j < 64; ++j) g[j] = s.stash[rg * D + j];
-        }
-        if (has_partial && n == 1 && rg < 64) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) s.stash[rg * D + j] = g[j];
+          for (int j = 0; j < 64; ++j) g[j] = 0.f;
         }
         if (n == 0) {
           float4* dst = reinterpret_cast<float4*>(p.dql + wrow * D);
@@ -405,43 +439,51 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           for (int j = 0; j < 16; ++j) dst[j] = make_float4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
         } else {
           store_row_bf16_sw(s.gs, rg, g);
+          fence_proxy_async_smem();
         }
+        tc_fence_before();
+        mbar_arrive(&s.gs_ready);
       }
-      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions, one 256-byte row per thread
-      if (lane < 16) bulk_wait_read0();  // this thread's reductions of the previous step read its rows
+      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions
+      if (!mbar_wait(&s.acc_full[b], (k >> 1) & 1, p.err, 30)) break;
+      tc_fence_after();
+      bulk_wait_read0();  // this thread's reductions of the previous step have read their rows
+      __syncwarp();
       {
-        uint32_t a[32], b[32];
+        uint32_t a[32], bb[32];
+        tmem_ld32(tb + lane_off + acc + 64, a);
+        tmem_ld32(tb + lane_off + acc + 96, bb);
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(s.stg_kf + rg * SROW);
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          if (t == 2 && k == 0) break;
-          const uint32_t col = t == 0 ? TM_DV : (t == 1 ? TM_DK : TM_DF);
-          tmem_ld32(tb + lane_off + col, a);
-          tmem_ld32(tb + lane_off + col + 32, b);
-          tmem_ld_wait();
-          if (lane < 16) {
-            float4* dst = reinterpret_cast<float4*>(s.stg[t] + mrow * SROW);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              dst[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                                   __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
-              dst[8 + j] = make_float4(__uint_as_float(b[4 * j]), __uint_as_float(b[4 * j + 1]),
-                                       __uint_as_float(b[4 * j + 2]), __uint_as_float(b[4 * j + 3]));
-            }
-          }
+        for (int j = 0; j < 8; ++j) {
+          dst[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                               __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
+          dst[8 + j] = make_float4(__uint_as_float(bb[4 * j]), __uint_as_float(bb[4 * j + 1]),
+                                   __uint_as_float(bb[4 * j + 2]), __uint_as_float(bb[4 * j + 3]));
         }
+        tmem_ld16x2(tb + lane_off + acc, a);
+        tmem_ld_wait();
+        float4* dv = reinterpret_cast<float4*>(s.stg_v + vrow * SROW + 32 * vh);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dv[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                              __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&s.g_free);
-      if (lane < 16) {
-        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK + mrow;
-        bulk_reduce_add_f32(p.dv + crow * D, s.stg[0] + mrow * SROW, D * 4);
-        bulk_reduce_add_f32(p.dkr + crow * D, s.stg[1] + mrow * SROW, D * 4);
-        if (k > 0) bulk_reduce_add_f32(p.df + (((size_t)bh * p.nc + c) * D + mrow) * D, s.stg[2] + mrow * SROW, D * 4);
+      mbar_arrive(&s.acc_free[b]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      {
+        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK;
+        if (rg < 64) bulk_reduce_add_f32(p.dkr + (crow + rg) * D, s.stg_kf + rg * SROW, D * 4);
+        else if (k > 0)
+          bulk_reduce_add_f32(p.df + (((size_t)bh * p.nc + c) * D + (rg - 64)) * D, s.stg_kf + rg * SROW, D * 4);
+        if (vh == 0) bulk_reduce_add_f32(p.dv + (crow + vrow) * D, s.stg_v + vrow * SROW, D * 4);
         bulk_commit();
       }
     }
-    if (lane < 16) bulk_wait0();
+    bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
