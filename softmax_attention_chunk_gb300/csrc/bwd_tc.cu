@@ -114,8 +114,10 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
   } else {
     const int r = tid;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // every thread runs every step (wg_sync needs all of them); after a timed-out wait (error
+    // recorded) the remaining waits are skipped
     bool ok = mbar_wait(&s.z_init, 0, p.err, 14);
-    for (int n = 0; ok && n < nsteps; ++n) {
+    for (int n = 0; n < nsteps; ++n) {
       uint8_t* cur = s.z[n & 1];
       fence_proxy_async_smem();
       wg_sync();
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
         if (n + 1 < nsteps) mbar_arrive(&s.z_ready);
       }
       if (n + 1 == nsteps) break;
-      if (!mbar_wait(&s.zp_full, n & 1, p.err, 15)) { ok = false; break; }
+      ok = ok && mbar_wait(&s.zp_full, n & 1, p.err, 15);
       tc_fence_after();
       uint8_t* nxt = s.z[(n + 1) & 1];
       if (r == 0) bulk_wait_read0();  // the store of step n-1 read `nxt`

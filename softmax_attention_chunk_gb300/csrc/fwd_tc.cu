@@ -6,13 +6,22 @@
 // Z <- Z F_c^T carries the queries across chunk c.
 //
 // GB300 mapping (one CTA = one 128-row query tile = two 64-row UT chunks; 2 CTAs per SM):
-//   * warp 4 streams [K->_c ; F_c] (one 128x64 tile) and V_c with TMA into a 3-stage ring;
-//   * warp 5 issues the MMAs: one M=128 N=128 K=64 MMA gives the scores S and the transported
-//     queries Z' = Z F_c^T together (the B operand stacks K->_c over F_c), and an M=128 N=64
-//     K=64 MMA with P read from TMEM accumulates O += P V_c;
-//   * warps 0-3 (one thread per query row / TMEM lane) run the online softmax on S (lazy
-//     rescaling of O when the running max grows by more than 8 in log2 units), write P to TMEM
-//     and Z' (rounded to bf16) to the swizzled shared-memory Z tile for the next step.
+//   * warp 8 streams [K->_c ; F_c] (one 128x64 tile) and V_c with TMA into a 3-stage ring;
+//   * warp 9 issues the MMAs, all with the A operand in TMEM: one N=128 MMA gives the scores
+//     S = Z K->_c^T and the transported queries Z' = Z F_c^T together (the B tile stacks K->_c
+//     over F_c) from the bf16 Z held in TMEM, and O += P V_c reads P from TMEM; shared memory
+//     only supplies the B tiles;
+//   * warps 0-7 run the softmax, two threads per query row (TMEM lane): warps w and w+4 share
+//     the lanes of quarter w and take the column halves 0-31 and 32-63 of S, Z', O and the
+//     matching halves of Z and P.  Each step a thread first turns its half of Z' into bf16 Z
+//     (TMEM to registers to TMEM) and reads its half of S, which frees both for the next
+//     MMAs, then runs the online softmax.  The two halves of a row share the running max: it
+//     only changes when some row's scores exceed it by more than 8 (log2 units, lazy
+//     rescaling of O); one barrier-reduction per step tells all threads whether that happened,
+//     and only then do the halves exchange their maxima through shared memory.  The softmax
+//     is instruction-issue bound: without a forget gate the maximum is taken over the raw
+//     scores (3-input max), and the scaling, the max subtraction and the row sums use paired
+//     fp32 instructions.
 // The upper chunk of the tile first meets the lower chunk as an ordinary earlier chunk (the
 // "partial" step: lower rows masked, only upper rows transported), then all 128 rows scan
 // together.  The diagonal chunks come from the preparation kernel as softmax partial states.
@@ -31,20 +40,21 @@ constexpr int BQ = 128;
 constexpr int BK = 64;
 constexpr int D = kHeadDim;
 constexpr int NSTAGE = 3;
-constexpr int NTHREADS = 192;
+constexpr int NSOFT = 256;  // softmax threads: two per query row
+constexpr int NTHREADS = NSOFT + 64;
 constexpr uint32_t TMEM_COLS = 256;
-// S double-buffered (P of step n is written over S of step n), one Z' buffer, O.
-constexpr uint32_t COL_S0 = 0, COL_Z = 128, COL_O = 192;
+// TMEM: scores S, transported queries Z' (fp32), output O, probabilities P (bf16 pairs), transported
+// queries Z (bf16 pairs, A operand of the score and transport MMAs).
+constexpr uint32_t COL_S = 0, COL_ZP = 64, COL_O = 128, COL_P = 192, COL_Z = 224;
 constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
 
 struct __align__(1024) ScanSmem {
-  uint8_t z[BQ * 128];                // Z tile, bf16, 128-byte swizzled rows
+  uint8_t z0[BQ * 128];               // Q<- tile (bf16, 128-byte swizzled rows): the first Z
   uint8_t kf[NSTAGE][128 * 128];      // rows 0-63: K->_c, rows 64-127: F_c
   uint8_t v[NSTAGE][BK * 128];        // V_c
+  float xm[2][BQ];                    // per-half row maxima / sums exchanged between the halves
   uint64_t full[NSTAGE], empty[NSTAGE];
-  // p_ready alternates by step parity: a thread may arrive for step n+1 before a slower one has
-  // arrived for step n (the next score MMA only waits for z_ready), never two steps ahead.
-  uint64_t s_full[2], z_ready, p_ready[2], pv_done, o_done, z_init;
+  uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done;
   uint32_t tmem_base;
 };
 
@@ -57,12 +67,74 @@ struct ScanParams {
   const float* fa;
   const float* fr;
   const float* ft;
-  int fox;
   __nv_bfloat16* o;
   float* lse;
   int* err;
 };
 
+// Paired fp32 arithmetic (two lanes of a 64-bit register per instruction) and 3-input max/min.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Barrier 1 over the softmax threads; returns whether q held for any of them.
+__device__ __forceinline__ bool softmax_any(bool q) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pq, pr;\n\t"
+      "setp.ne.u32 pq, %1, 0;\n\t"
+      "bar.red.or.pred pr, 1, 256, pq;\n\t"
+      "selp.u32 %0, 1, 0, pr;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)q)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+template <bool FOX>
 __global__ void __launch_bounds__(NTHREADS, 2)
     fwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_ql, const __grid_constant__ CUtensorMap tm_kr,
                        const __grid_constant__ CUtensorMap tm_f, const __grid_constant__ CUtensorMap tm_v,
@@ -80,23 +152,21 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       mbar_init(&s.full[k], 1);
       mbar_init(&s.empty[k], 1);
     }
-    mbar_init(&s.s_full[0], 1);
-    mbar_init(&s.s_full[1], 1);
-    mbar_init(&s.z_ready, 128);
-    mbar_init(&s.p_ready[0], 128);
-    mbar_init(&s.p_ready[1], 128);
+    mbar_init(&s.z_init, 1);
+    mbar_init(&s.z_ready, NSOFT);
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.p_ready, NSOFT);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_done, 1);
-    mbar_init(&s.z_init, 1);
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(&s.tmem_base, TMEM_COLS);
+  if (warp == 9) tmem_alloc(&s.tmem_base, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && nsteps > 0) {
       prefetch_tmap(&tm_ql);
@@ -104,7 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       prefetch_tmap(&tm_f);
       prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(&s.z_init, BQ * 128);
-      tma_load_2d(s.z, &tm_ql, 0, bh * p.Lp + T * BQ, &s.z_init);
+      tma_load_2d(s.z0, &tm_ql, 0, bh * p.Lp + T * BQ, &s.z_init);
       for (int n = 0; n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (n >= NSTAGE && !mbar_wait(&s.empty[st], ((n / NSTAGE) - 1) & 1, p.err, 1)) break;
@@ -115,196 +185,226 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         tma_load_2d(s.v[st], &tm_v, 0, bh * p.L + c * BK, &s.full[st]);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
-    // order: S(n), Z'(n) as soon as Z(n) is in shared memory; then O += P(n-1) V(n-1).
+    // order: S(n), Z'(n) once Z(n) is in TMEM and S(n-1), Z'(n-1) have been read; then
+    // O += P(n-1) V(n-1) once P(n-1) is written.
     if (lane == 0 && nsteps > 0) {
-      const uint32_t idesc_n64 = idesc_bf16(128, 64, 0, 0);
+      // S and Z' come from one N=128 MMA: the stage tile stacks K->_c (rows 0-63) over F_c, and
+      // the S and Z' TMEM blocks are adjacent.  Descriptors advance by plain 64-bit adds (the
+      // start-address field counts 16-byte units).
+      const uint32_t idesc_sz = idesc_bf16(128, 128, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
-      const uint32_t zaddr = smem_u32(s.z);
-      bool ok = mbar_wait(&s.z_init, 0, p.err, 2);
+      // stage st of the kf / v rings lies st * 16 KB / st * 8 KB after stage 0
+      const uint64_t dkf0 = sdesc_sw128(smem_u32(s.kf[0]), 1024, 16);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(s.v[0]), 1024, 0);
+      bool ok = true;
       auto issue_pv = [&](int m) {
-        const uint32_t va = smem_u32(s.v[m % NSTAGE]);
-        const uint32_t pcol = COL_S0 + 64 * (m & 1);
+        const uint64_t d0 = dv0 + (uint64_t)(512 * (m % NSTAGE));
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tb + COL_O, tb + pcol + 8 * k, sdesc_sw128(va + 2048 * k, 1024, 0), idesc_pv, 1);
+        for (int k = 0; k < 4; ++k) mma_ts(tb + COL_O, tb + COL_P + 8 * k, d0 + (uint64_t)(128 * k), idesc_pv, 1);
         mma_commit(&s.empty[m % NSTAGE]);
         mma_commit(&s.pv_done);
       };
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&s.full[st], (n / NSTAGE) & 1, p.err, 3)) { ok = false; break; }
-        if (n > 0 && !mbar_wait(&s.z_ready, (n - 1) & 1, p.err, 4)) { ok = false; break; }
+        if (!mbar_wait(&s.z_ready, n & 1, p.err, 4)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kfa = smem_u32(s.kf[st]);
-        const uint32_t scol = COL_S0 + 64 * (n & 1);
+        const uint64_t d0 = dkf0 + (uint64_t)(1024 * st);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tb + scol, sdesc_sw128(zaddr + 32 * k, 1024, 16), sdesc_sw128(kfa + 32 * k, 1024, 16),
-                 idesc_n64, k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tb + COL_Z, sdesc_sw128(zaddr + 32 * k, 1024, 16),
-                 sdesc_sw128(kfa + 64 * 128 + 32 * k, 1024, 16), idesc_n64, k > 0 ? 1u : 0u);
-        mma_commit(&s.s_full[n & 1]);
+        for (int k = 0; k < 4; ++k) mma_ts(tb + COL_S, tb + COL_Z + 8 * k, d0 + (uint64_t)(2 * k), idesc_sz, k > 0 ? 1u : 0u);
+        mma_commit(&s.s_full);
         if (n > 0) {
-          if (!mbar_wait(&s.p_ready[(n - 1) & 1], ((n - 1) >> 1) & 1, p.err, 5)) { ok = false; break; }
+          if (!mbar_wait(&s.p_ready, (n - 1) & 1, p.err, 5)) { ok = false; break; }
           tc_fence_after();
           issue_pv(n - 1);
         }
       }
-      if (ok && mbar_wait(&s.p_ready[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, p.err, 5)) {
+      if (ok && mbar_wait(&s.p_ready, (nsteps - 1) & 1, p.err, 5)) {
         tc_fence_after();
         issue_pv(nsteps - 1);
         mma_commit(&s.o_done);
       }
     }
   } else {
-    // ---------------- softmax / transport warpgroup: thread r owns query row r ----------------
-    const int r = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ---------------- softmax / transport: thread (r, h) owns columns 32h..32h+31 of row r ----------------
+    const int q4 = warp & 3, h = warp >> 2;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t c_s = tb + lane_off + COL_S + 32 * h, c_zp = tb + lane_off + COL_ZP + 32 * h;
+    const uint32_t c_o = tb + lane_off + COL_O + 32 * h, c_p = tb + lane_off + COL_P + 16 * h;
+    const uint32_t c_z = tb + lane_off + COL_Z + 16 * h;
     const int grow = T * BQ + r;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
-    float m = p.dm[wrow], l = p.dl[wrow];
-    uint32_t buf[32];
+    float m = p.dm[wrow], l = h == 0 ? p.dl[wrow] : 0.f;  // l: this half's share of the row sum
+    uint32_t x[32];
+    bool ok = true;
     if (nsteps > 0) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
+      tmem_st32(c_o, x);
+      // Z_0 = Q<- of the tile: shared memory (swizzled rows) -> TMEM
+      ok = mbar_wait(&s.z_init, 0, p.err, 2);  // (on a timeout the tile below is garbage; err is set)
+      const uint8_t* zrow = s.z0 + r * 128;
+      uint32_t z16[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) buf[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
-        tmem_st32(tb + lane_off + COL_O + h * 32, buf);
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(zrow + (((4 * h + q) ^ (r & 7)) * 16));
+        z16[4 * q] = v.x;
+        z16[4 * q + 1] = v.y;
+        z16[4 * q + 2] = v.z;
+        z16[4 * q + 3] = v.w;
       }
+      tmem_st16(c_z, z16);
       tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.z_ready);
     }
-    const float arow = p.fox ? p.fa[wrow] : 0.f;
+    const float arow = FOX ? p.fa[wrow] : 0.f;
     float R = 0.f;
-    bool ok = true;
+    // Every softmax thread runs every step (the per-step barrier needs all of them); after a
+    // wait has timed out (error recorded) the remaining waits are skipped.
     for (int n = 0; n < nsteps; ++n) {
-      if (!mbar_wait(&s.s_full[n & 1], (n >> 1) & 1, p.err, 6)) { ok = false; break; }
+      ok = ok && mbar_wait(&s.s_full, n & 1, p.err, 6);
       tc_fence_after();
       const int c = has_partial ? 2 * T - n : 2 * T - 1 - n;
       const bool active = !(has_partial && n == 0 && r < 64);
-      const uint32_t scol = COL_S0 + 64 * (n & 1);
-      uint32_t buf2[32];
-      // transport first: Z <- Z F_c^T (bf16) so that the next score MMA can start
-      if (n + 1 < nsteps) {
-        if (active) {
-          tmem_ld32(tb + lane_off + COL_Z, buf);
-          tmem_ld32(tb + lane_off + COL_Z + 32, buf2);
-          tmem_ld_wait();
-          uint8_t* zrow = s.z + r * 128;
+      // transport first: Z <- bf16(Z F_c^T) into TMEM, so that the next MMAs can start
+      if (n + 1 < nsteps && active) {
+        tmem_ld32(c_zp, x);
+        tmem_ld_wait();
+        uint32_t z16[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t* src = (q < 4) ? (buf + 8 * q) : (buf2 + 8 * (q - 4));
-            uint4 pk;
-            pk.x = pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1]));
-            pk.y = pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3]));
-            pk.z = pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5]));
-            pk.w = pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7]));
-            *reinterpret_cast<uint4*>(zrow + ((q ^ (r & 7)) * 16)) = pk;
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&s.z_ready);
+        for (int j = 0; j < 16; ++j) z16[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+        tmem_st16(c_z, z16);
       }
-      // scores (log2 domain, in place in the load registers)
-      tmem_ld32(tb + lane_off + scol, buf);
-      tmem_ld32(tb + lane_off + scol + 32, buf2);
+      tmem_ld32(c_s, x);
       tmem_ld_wait();
-      const float rb = (arow + R) * kLog2e;
-      float mx = -INFINITY;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.z_ready);  // Z(n+1) written, S(n) and Z'(n) read
+      // this half's maximum of the log2-domain scores x = scl s (+ forget-gate terms); without a
+      // forget gate x is a plain multiple of the raw score, so its maximum comes from the raw
+      // maximum (minimum for a negative scale) and x itself is folded into the exponent below
+      float mxh;
+      if (FOX) {
+        const float rb = (arow + R) * kLog2e;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float x0 = fmaf(__uint_as_float(buf[j]), p.scl, rb);
-        float x1 = fmaf(__uint_as_float(buf2[j]), p.scl, rb);
-        if (p.fox) {
-          x0 += __ldg(p.fr + (size_t)bh * p.Lp + (size_t)c * BK + j) * kLog2e;
-          x1 += __ldg(p.fr + (size_t)bh * p.Lp + (size_t)c * BK + 32 + j) * kLog2e;
+        for (int j = 0; j < 32; ++j) {
+          float xv = fmaf(__uint_as_float(x[j]), p.scl, rb);
+          xv += __ldg(p.fr + (size_t)bh * p.Lp + (size_t)c * BK + 32 * h + j) * kLog2e;
+          mx4[j & 3] = fmaxf(mx4[j & 3], xv);
+          x[j] = __float_as_uint(xv);
         }
-        if (!active) {
-          x0 = -INFINITY;
-          x1 = -INFINITY;
+        mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      } else {
+        float e0, e1;
+        if (p.scl >= 0.f) {
+          e0 = e1 = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            e0 = max3(e0, __uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+            e1 = max3(e1, __uint_as_float(x[2 * j + 2]), __uint_as_float(x[2 * j + 3]));
+          }
+          mxh = fmaxf(e0, e1) * p.scl;
+        } else {
+          e0 = e1 = INFINITY;
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            e0 = min3(e0, __uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+            e1 = min3(e1, __uint_as_float(x[2 * j + 2]), __uint_as_float(x[2 * j + 3]));
+          }
+          mxh = fminf(e0, e1) * p.scl;
         }
-        mx = fmaxf(mx, fmaxf(x0, x1));
-        buf[j] = __float_as_uint(x0);
-        buf2[j] = __float_as_uint(x1);
       }
-      const float mnew = fmaxf(m, mx);
-      const bool resc = mnew > m + kTau;
-      if (__any_sync(0xffffffffu, resc)) {
-        // O holds P(n-1) V(n-1) only once that MMA has completed
-        if (n > 0 && !mbar_wait(&s.pv_done, (n - 1) & 1, p.err, 8)) { ok = false; break; }
-        tc_fence_after();
-        const float corr = resc ? fast_exp2(m - mnew) : 1.f;
-        if (resc) m = mnew;
-        l *= corr;
-        uint32_t ob[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld32(tb + lane_off + COL_O + h * 32, ob);
+      if (!active) mxh = -INFINITY;
+      if (softmax_any(mxh > m + kTau)) {
+        // some row needs a larger reference: the halves agree on the row maximum first
+        s.xm[h][r] = mxh;
+        softmax_sync();
+        const float mnew = fmaxf(m, fmaxf(s.xm[0][r], s.xm[1][r]));
+        softmax_sync();
+        if (mnew > m + kTau) {
+          // O holds P(n-1) V(n-1) only once that MMA has completed
+          if (n > 0) ok = ok && mbar_wait(&s.pv_done, (n - 1) & 1, p.err, 8);
+          tc_fence_after();
+          const float corr = fast_exp2(m - mnew);
+          m = mnew;
+          l *= corr;
+          uint32_t ob[32];
+          tmem_ld32(c_o, ob);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(__uint_as_float(ob[j]) * corr);
-          tmem_st32(tb + lane_off + COL_O + h * 32, ob);
+          tmem_st32(c_o, ob);
         }
       }
-      // probabilities, packed bf16 pairs (key 2j in the low half), written over S(n)
-      float ls = 0.f;
-      {
-        uint32_t pk[32];
+      // probabilities, packed bf16 pairs (key 2j in the low half); exponents and row sums by
+      // paired fp32 instructions
+      uint32_t pk[16];
+      if (active) {
+        uint64_t acc[2] = {0ull, 0ull};
+        const uint64_t nm = f2(-m, -m), sc = f2(p.scl, p.scl);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float p0 = fast_exp2(__uint_as_float(buf[2 * j]) - m);
-          const float p1 = fast_exp2(__uint_as_float(buf[2 * j + 1]) - m);
-          const float p2 = fast_exp2(__uint_as_float(buf2[2 * j]) - m);
-          const float p3 = fast_exp2(__uint_as_float(buf2[2 * j + 1]) - m);
-          ls += (p0 + p1) + (p2 + p3);
+          const uint64_t xx = f2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+          float a0, a1;
+          f2_split(FOX ? f2_add(xx, nm) : f2_fma(xx, sc, nm), a0, a1);
+          const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+          acc[j & 1] = f2_add(acc[j & 1], f2(p0, p1));
           pk[j] = pack_bf16(p0, p1);
-          pk[16 + j] = pack_bf16(p2, p3);
         }
-        tmem_st32(tb + lane_off + scol, pk);
+        float s0, s1, s2, s3;
+        f2_split(acc[0], s0, s1);
+        f2_split(acc[1], s2, s3);
+        l += (s0 + s1) + (s2 + s3);
+        if (FOX) R += p.ft[(size_t)bh * p.nc + c];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
       }
-      l += ls;
-      if (active && p.fox) R += p.ft[(size_t)bh * p.nc + c];
+      // P(n-1) has been consumed by its MMA before P(n) replaces it
+      if (n > 0) ok = ok && mbar_wait(&s.pv_done, (n - 1) & 1, p.err, 9);
+      tmem_st16(c_p, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&s.p_ready[n & 1]);
+      mbar_arrive(&s.p_ready);
     }
     // ---------------- epilogue ----------------
     if (nsteps > 0) {
       if (ok) ok = mbar_wait(&s.o_done, 0, p.err, 7);
       tc_fence_after();
     }
-    const float inv = 1.f / l;
-    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.L + (grow < p.L ? grow : 0)) * D);
+    s.xm[h][r] = l;
+    softmax_sync();
+    const float lt = s.xm[0][r] + s.xm[1][r];
+    const float inv = 1.f / lt;
+    if (nsteps > 0) {
+      tmem_ld32(c_o, x);
+      tmem_ld_wait();
+    } else {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (nsteps > 0) {
-        tmem_ld32(tb + lane_off + COL_O + h * 32, buf);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) buf[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
-      }
-      if (grow < p.L) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 pk;
-          pk.x = pack_bf16(__uint_as_float(buf[8 * q]) * inv, __uint_as_float(buf[8 * q + 1]) * inv);
-          pk.y = pack_bf16(__uint_as_float(buf[8 * q + 2]) * inv, __uint_as_float(buf[8 * q + 3]) * inv);
-          pk.z = pack_bf16(__uint_as_float(buf[8 * q + 4]) * inv, __uint_as_float(buf[8 * q + 5]) * inv);
-          pk.w = pack_bf16(__uint_as_float(buf[8 * q + 6]) * inv, __uint_as_float(buf[8 * q + 7]) * inv);
-          dst[h * 4 + q] = pk;
-        }
-      }
+      for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
     }
-    if (grow < p.L) p.lse[(size_t)bh * p.L + grow] = (m + log2f(l)) * kLn2;
+    if (grow < p.L) {
+      uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.L + grow) * D + 32 * h);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 pk;
+        pk.x = pack_bf16(__uint_as_float(x[8 * q]) * inv, __uint_as_float(x[8 * q + 1]) * inv);
+        pk.y = pack_bf16(__uint_as_float(x[8 * q + 2]) * inv, __uint_as_float(x[8 * q + 3]) * inv);
+        pk.z = pack_bf16(__uint_as_float(x[8 * q + 4]) * inv, __uint_as_float(x[8 * q + 5]) * inv);
+        pk.w = pack_bf16(__uint_as_float(x[8 * q + 6]) * inv, __uint_as_float(x[8 * q + 7]) * inv);
+        dst[q] = pk;
+      }
+      if (h == 0) p.lse[(size_t)bh * p.L + grow] = (m + log2f(lt)) * kLn2;
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tb, TMEM_COLS);
   }
@@ -374,15 +474,15 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   p.fa = (const float*)(ws + lay.fa);
   p.fr = (const float*)(ws + lay.fr);
   p.ft = (const float*)(ws + lay.ft);
-  p.fox = logf ? 1 : 0;
   p.o = (__nv_bfloat16*)o;
   p.lse = lse;
   p.err = (int*)(ws + lay.err);
   const size_t smem = sizeof(ScanSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = logf ? fwd_scan_tc_kernel<true> : fwd_scan_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long ntiles = (long)p.ntiles * g.BH;
-  fwd_scan_tc_kernel<<<(unsigned)ntiles, NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
+  kern<<<(unsigned)ntiles, NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
   return cudaGetLastError();
 }
 

@@ -35,14 +35,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up after a bounded number of
-// polls (seconds), records `code` in *err and returns false, so that a broken pipeline ends
-// the kernel instead of hanging the GPU.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity to complete, spinning on try_wait (which itself
+// suspends the thread in hardware for a while).  Gives up after about 2 s (global timer; a
+// hard cap on the polls as well), records `code` in *err and returns false, so that a broken
+// pipeline ends the kernel instead of hanging the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < (1u << 24); ++i) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(128);
+    if ((i & 1023u) == 0 && global_ns() - t0 > 2000000000ull) break;
   }
   if (err) atomicCAS(err, 0, code);
   return false;
