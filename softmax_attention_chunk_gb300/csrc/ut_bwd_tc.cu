@@ -45,16 +45,16 @@ constexpr uint32_t C0 = 0, C1 = 64, C2 = 128, C3 = 192;  // TMEM accumulator col
 // previous one has finished (phases in brackets).
 enum {
   S_W,   // W [all]
-  S_Q,   // Q [P2] | G fp32 low half [P2-P3] | P [P5-P6] | gM1 [P6-P7] | gU [P8-P9]
-  S_K,   // K [P2] | G fp32 high half [P2-P3] | dS [P5-P8] | diag(beta) W [P8-P11]
+  S_Q,   // Q [P2] | L fp32 low half [P2-P3] | P [P5-P6] | gM1 [P6-P7] | gU [P8-P9]
+  S_K,   // K [P2] | L fp32 high half [P2-P3] | dS [P5-P8] | diag(beta) W [P8-P11]
   S_V,   // V [P4] | dF [P4-P7] | gN2 [P7-P8] | A1 [P9-P10]
   S_DO,  // dO [P4-P6] | gX [P6-P8] | gU.*Y fp32 low half [P8-P9] | diag(beta) gN [P10-P11]
   S_M1,  // M1 [P2-P7] | gU.*Y fp32 high half [P8-P9]
   S_N2,  // N2 [P2-P8] | gN [P10-P11]
   S_U,   // U [P3-P9]
   S_Y,   // Y [P3-P10]
-  S_DQ,  // dQ<- [P3-P7] | E3 [P7-P8]
-  S_DK,  // dK-> [P3-P6]
+  S_DQ,  // dQ<- [P4-P7] | E3 [P7-P8]
+  S_DK,  // dK-> [P4-P6]
   S_X,   // X [P4-P6] | Q again [P7-P8]
   S_Y1,  // Y1 [P4-P6] | K again [P7-P8]
   NSLOT
@@ -87,29 +87,6 @@ struct UbParams {
   float* dbeta;
   int* err;
 };
-
-// fp32 64x64 matrix over two adjacent slots, element (r, m) at r * 64 + (m ^ 4 (r mod 8)):
-// rows of a warp's 16-byte stores fall on different banks, 4-column groups stay contiguous.
-__device__ __forceinline__ int f32_idx(int r, int m) { return r * 64 + (m ^ ((r & 7) << 2)); }
-
-__device__ __forceinline__ void store_bf16_half(__nv_bfloat16* dst, const float* x) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
-                       pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
-}
-__device__ __forceinline__ void load_f32_half(const float* src, float* x) {
-  const float4* s4 = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 v = s4[q];
-    x[4 * q] = v.x;
-    x[4 * q + 1] = v.y;
-    x[4 * q + 2] = v.z;
-    x[4 * q + 3] = v.w;
-  }
-}
 
 __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
@@ -191,13 +168,14 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   wait_mma(42);
   {
     float x[32];
-    ld_half(tb, lane_off, C0, x);  // G, strictly lower, fp32 into the slots of Q and K
+    ld_half(tb, lane_off, C0, x);  // L = strictLower(diag(beta) G), fp32 into the slots of Q and K
+    const float bi = s.beta[i];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int j = 32 * h + 4 * q;
       *reinterpret_cast<float4*>(sg + f32_idx(i, j)) =
-          make_float4(j < i ? x[4 * q] : 0.f, j + 1 < i ? x[4 * q + 1] : 0.f, j + 2 < i ? x[4 * q + 2] : 0.f,
-                      j + 3 < i ? x[4 * q + 3] : 0.f);
+          make_float4(j < i ? bi * x[4 * q] : 0.f, j + 1 < i ? bi * x[4 * q + 1] : 0.f,
+                      j + 2 < i ? bi * x[4 * q + 2] : 0.f, j + 3 < i ? bi * x[4 * q + 3] : 0.f);
     }
     ld_half(tb, lane_off, C1, x);
 #pragma unroll
@@ -210,48 +188,17 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   }
   publish();
 
-  // ---- P3: Y = (I + strictLower(D G))^{-1} by forward substitution (warps 0-1, lane = column),
-  //      U = Y D; warps 2-3 meanwhile turn dQ<- and dK-> into bf16 operand tiles ----
+  // ---- P3: Y = (I + strictLower(D G))^{-1} by forward substitution (warps 0-1, lane = column);
+  //      Y and U = Y D as bf16 tiles ----
   if (warp < 2) {
     const int cc = 32 * warp + lane;
-    float yc[64];
-#pragma unroll
-    for (int r = 0; r < 64; ++r) yc[r] = 0.f;  // G_rm = 0 for m >= r: unsolved entries add nothing
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-      for (int m = 0; m < r; m += 4) {
-        const float4 gv = *reinterpret_cast<const float4*>(sg + f32_idx(r, m));
-        a0 += gv.x * yc[m];
-        a1 += gv.y * yc[m + 1];
-        a2 += gv.z * yc[m + 2];
-        a3 += gv.w * yc[m + 3];
-      }
-      yc[r] = (cc == r ? 1.f : 0.f) - s.beta[r] * ((a0 + a1) + (a2 + a3));
-    }
+    float y[64];
+    ut_solve_column(sg, cc, y);
     const float bc = s.beta[cc];
 #pragma unroll
     for (int r = 0; r < 64; ++r) {
-      *reinterpret_cast<__nv_bfloat16*>(s.t[S_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r]);
-      *reinterpret_cast<__nv_bfloat16*>(s.t[S_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(yc[r] * bc);
-    }
-  } else {
-    const int r = tid - 64;
-    const bool ok = row0 + r < p.L;
-    float x[32];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (ok) load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, x);
-      else
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = 0.f;
-      put_half(s.t[S_DQ], r, hh, x);
-      if (ok) load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, x);
-      else
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = 0.f;
-      put_half(s.t[S_DK], r, hh, x);
+      *reinterpret_cast<__nv_bfloat16*>(s.t[S_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r]);
+      *reinterpret_cast<__nv_bfloat16*>(s.t[S_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r] * bc);
     }
   }
   publish();
@@ -269,10 +216,21 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     put_half(s.t[S_X], i, h, x);
     ld_half(tb, lane_off, C1, x);
     put_half(s.t[S_Y1], i, h, x);
-    // dF as a bf16 tile in V's slot: row tid/2, half tid%2
+    // dF (V's slot), dQ<- and dK-> as bf16 operand tiles: row tid/2, half tid%2
     const int r = tid >> 1, hh = tid & 1;
+    const bool ok = row0 + r < p.L;
+    float y1[32], y2[32];
     load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D + 32 * hh, x);
+    if (ok) {
+      load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, y1);
+      load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, y2);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) y1[j] = y2[j] = 0.f;
+    }
     put_half(s.t[S_DF], r, hh, x);
+    put_half(s.t[S_DQ], r, hh, y1);
+    put_half(s.t[S_DK], r, hh, y2);
   }
   publish();
 

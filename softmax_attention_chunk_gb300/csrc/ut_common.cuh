@@ -95,6 +95,65 @@ __device__ __forceinline__ void ld_half(uint32_t tb, uint32_t lane_off, uint32_t
 #pragma unroll
   for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(a[j]);
 }
+// fp32 64x64 matrix over two adjacent tile slots, element (r, m) at r * 64 + (m ^ 4 (r mod 8)):
+// rows of a warp's 16-byte stores fall on different banks, 4-column groups stay contiguous.
+__device__ __forceinline__ int f32_idx(int r, int m) { return r * 64 + (m ^ ((r & 7) << 2)); }
+
+// 32 fp32 values as bf16 to global memory (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store_bf16_half(__nv_bfloat16* dst, const float* x) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                       pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+}
+// 32 fp32 values from global memory (128 bytes, 16-byte aligned).
+__device__ __forceinline__ void load_f32_half(const float* src, float* x) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 v = s4[q];
+    x[4 * q] = v.x;
+    x[4 * q + 1] = v.y;
+    x[4 * q + 2] = v.z;
+    x[4 * q + 3] = v.w;
+  }
+}
+
+// Forward substitution for the UT transform, one column per thread: returns in y the column cc
+// of Y = (I + L)^{-1}, L = strictLower(diag(beta) G), i.e. row by row
+//   Y_rc = delta_rc - sum_{m<r} L_rm Y_mc,
+// with L the fp32 matrix at sl (f32_idx layout, strictly lower: entries with m >= r are zero).
+// Rows go in blocks of 16: the earlier blocks enter through 16 independent accumulations
+// (16-byte broadcast loads of L), the block itself is substituted row by row.  Everything is
+// unrolled so that y stays in registers.
+__device__ __forceinline__ void ut_solve_column(const float* sl, int cc, float (&y)[64]) {
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    float acc[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16 * b; m += 4) {
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        const float4 lv = *reinterpret_cast<const float4*>(sl + f32_idx(16 * b + rr, m));
+        acc[rr] = fmaf(lv.x, y[m], acc[rr]);
+        acc[rr] = fmaf(lv.y, y[m + 1], acc[rr]);
+        acc[rr] = fmaf(lv.z, y[m + 2], acc[rr]);
+        acc[rr] = fmaf(lv.w, y[m + 3], acc[rr]);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * b + rr;
+      float a = acc[rr];
+#pragma unroll
+      for (int m = 16 * b; m < r; ++m) a = fmaf(sl[f32_idx(r, m)], y[m], a);
+      y[r] = (cc == r ? 1.f : 0.f) - a;
+    }
+  }
+}
 
 }  // namespace tc
 }  // namespace pathattn
