@@ -169,33 +169,37 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 // ============================ adjoint scan ============================
 // Per step k (chunk c, transported queries Z_n, n = nsteps - 1 - k) the MMA issuer runs
 //   S_{k+1} = Z K->^T, dP_{k+1} = dO V^T          (one step ahead, for the softmax side)
-//   [dK->_c ; dF_c] = [dS^T ; G_{n+1}^T] Z_n      (one M=128 MMA: dS and G tiles are adjacent and
-//                                                  form one MN-major operand with LBO = one tile)
-//   G_n = dS K->_c + G_{n+1} F_c
+//   G_n = [dS | G_{n+1}] [K->_c ; F_c]            (one K=128 chain, A from TMEM)
+//   [dK->_c ; dF_c] = [dS^T ; G_{n+1}^T] Z_n      (one M=128 MMA: the dS and G tiles are adjacent
+//                                                  in shared memory and form one MN-major operand)
 //   dV_c = P^T dO
-// with the dV / [dK->; dF] accumulators double-buffered in TMEM, so that the gradient side drains
-// step k while step k+1 computes.
-constexpr int BS_NSTAGE = 2;
+// dO (constant per tile), dS and G_{n+1} are also kept in TMEM as bf16 pairs, so that dP and G
+// read only their B tiles from shared memory; shared-memory bandwidth, not the tensor pipe,
+// bounds these N=64 products.
+constexpr int BS_NSTAGE = 2;   // K->_c, F_c, V_c ring (L2-resident operands)
+constexpr int BS_ZSTAGE = 3;   // Z_n ring (streamed from HBM: one more stage of look-ahead)
 constexpr int SROW = D + 4;  // staging row stride (floats): 16-byte aligned, spreads rows over banks
-// TMEM columns: S, dP, G_n, accumulator buffers (dV at +0, [dK->; dF] at +64), G_0 of a partial step
-constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_ACC0 = 192, TM_ACC1 = 320, TM_G2 = 448;
+// TMEM columns: S, dP, G_n, dV, [dK->; dF], G_0 of a partial step, dO (bf16 pairs), dS | G_{n+1}
+// (bf16 pairs, the A operand of the G chain)
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DKF = 256, TM_G2 = 320, TM_DO = 384,
+                   TM_DSG = 416;
 
 struct __align__(1024) BsStage {
-  uint8_t z[ZTILE];        // Z_n
-  uint8_t kr[BK * 128];    // K->_c
+  uint8_t kr[BK * 128];    // K->_c  } adjacent: the B operand [K->_c ; F_c] of the G chain
+  uint8_t f[BK * 128];     // F_c    }
   uint8_t v[BK * 128];     // V_c
-  uint8_t f[BK * 128];     // F_c
 };
 struct __align__(1024) BsSmem {
   uint8_t ps[ZTILE];       // P  (bf16, rows x keys)
   uint8_t ds[ZTILE];       // dS (bf16, rows x keys), scale included
   uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d); follows ds (stacked operand)
   uint8_t dO[ZTILE];
+  uint8_t z[BS_ZSTAGE][ZTILE];  // Z_n
   BsStage st[BS_NSTAGE];
   float stg_v[BK * SROW];    // dV of a step (fp32 rows) for the bulk reductions
   float stg_kf[BQ * SROW];   // dK-> (rows 0-63) and dF (rows 64-127) of a step
-  uint64_t full[BS_NSTAGE], empty[BS_NSTAGE];
-  uint64_t do_full, sp_full, ps_ready, g_full, gs_ready, acc_full[2], acc_free[2];
+  uint64_t full[BS_NSTAGE], empty[BS_NSTAGE], zfull[BS_ZSTAGE], zempty[BS_ZSTAGE];
+  uint64_t do_full, sp_full, ps_ready, g_full, gs_ready, acc_full, acc_free;
   uint32_t tmem_base;
 };
 
@@ -224,10 +228,17 @@ __device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const fl
     *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = pk;
   }
 }
+// 64 fp32 values as 32 bf16 pairs (column 2j in the low half), the TMEM A-operand layout.
+__device__ __forceinline__ void pack_row_pairs(const float* x, uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+}
 
-// Warp roles: 0-3 softmax side (P, dS of a step), 4 TMA/bulk producer, 5 MMA issuer,
-// 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions).
-constexpr int BS_THREADS = 320;
+// Warp roles: 0-3 softmax side (P, dS of a step), 4 TMA/bulk producer (lane 0: K->, F, V; lane
+// 16: Z), 5 MMA issuer A (S, dP, the G chain), 6-9 gradient side (G_n conversion, dQ<- output,
+// dV/dK->/dF reductions), 10 MMA issuer B ([dK->; dF], dV).  Two issuers because a tcgen05.mma
+// costs tens of cycles to issue from one thread and these products are small (N = 64).
+constexpr int BS_THREADS = 352;
 __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
                                                             const __grid_constant__ CUtensorMap tm_kr,
                                                             const __grid_constant__ CUtensorMap tm_v,
@@ -252,15 +263,17 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       mbar_init(&s.full[k], 1);
       mbar_init(&s.empty[k], 1);
     }
+    for (int k = 0; k < BS_ZSTAGE; ++k) {
+      mbar_init(&s.zfull[k], 1);
+      mbar_init(&s.zempty[k], 2);  // both issuers read Z
+    }
     mbar_init(&s.do_full, 1);
     mbar_init(&s.sp_full, 1);
     mbar_init(&s.ps_ready, 128);
-    mbar_init(&s.g_full, 1);
+    mbar_init(&s.g_full, 2);       // G_n (issuer A) and [dK->; dF] (issuer B) complete
     mbar_init(&s.gs_ready, 128);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s.acc_full[b], 1);
-      mbar_init(&s.acc_free[b], 128);
-    }
+    mbar_init(&s.acc_full, 1);     // issuer B's MMAs of the step complete
+    mbar_init(&s.acc_free, 128);
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -270,92 +283,117 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
   const uint32_t tb = s.tmem_base;
 
   if (warp == 4) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
+    // ---------------- producers ----------------
+    if (lane == 0) {  // K->_c, F_c, V_c (and dO once)
       mbar_arrive_expect_tx(&s.do_full, ZTILE);
       tma_load_2d(s.dO, &tm_do, 0, bh * p.L + T * BQ, &s.do_full);
       for (int k = 0; k < nsteps; ++k) {
         const int si = k % BS_NSTAGE;
         if (k >= BS_NSTAGE && !mbar_wait(&s.empty[si], ((k / BS_NSTAGE) - 1) & 1, p.err, 21)) break;
-        const int n = nsteps - 1 - k;
-        const int c = step_chunk(has_partial, T, n);
+        const int c = step_chunk(has_partial, T, nsteps - 1 - k);
         BsStage& S = s.st[si];
-        mbar_arrive_expect_tx(&s.full[si], ZTILE + 3 * BK * 128);
-        bulk_load(S.z, zbase + (size_t)n * ZTILE, ZTILE, &s.full[si]);
+        mbar_arrive_expect_tx(&s.full[si], 3 * BK * 128);
         tma_load_2d(S.kr, &tm_kr, 0, bh * p.Lp + c * BK, &s.full[si]);
         tma_load_2d(S.v, &tm_v, 0, bh * p.L + c * BK, &s.full[si]);
         tma_load_2d(S.f, &tm_f, 0, (bh * p.nc + c) * D, &s.full[si]);
       }
+    } else if (lane == 16) {  // Z_n
+      for (int k = 0; k < nsteps; ++k) {
+        const int zi = k % BS_ZSTAGE;
+        if (k >= BS_ZSTAGE && !mbar_wait(&s.zempty[zi], ((k / BS_ZSTAGE) - 1) & 1, p.err, 20)) break;
+        mbar_arrive_expect_tx(&s.zfull[zi], ZTILE);
+        bulk_load(s.z[zi], zbase + (size_t)(nsteps - 1 - k) * ZTILE, ZTILE, &s.zfull[zi]);
+      }
     }
   } else if (warp == 5) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer A: S, dP (one step ahead) and the G chain ----------------
     if (lane == 0) {
-      const uint32_t i_rk = idesc_bf16(128, 64, 0, 0);   // [128 x 64] = A(K-major) B(K-major)^T
-      const uint32_t i_rm = idesc_bf16(128, 64, 0, 1);   // [128 x 64] = A(K-major) B(MN-major)
-      const uint32_t i_tt = idesc_bf16(64, 64, 1, 1);    // [64 x 64]  = A(MN-major) B(MN-major)
-      const uint32_t i_st = idesc_bf16(128, 64, 1, 1);   // [128 x 64] = A(MN-major, two atoms) B(MN-major)
-      const uint32_t a_do = smem_u32(s.dO), a_ps = smem_u32(s.ps), a_ds = smem_u32(s.ds), a_gs = smem_u32(s.gs);
+      const uint32_t i_rk = idesc_bf16(128, 64, 0, 0);   // [128 x 64] = A(K-major / TMEM) B(K-major)^T
+      const uint32_t i_rm = idesc_bf16(128, 64, 0, 1);   // [128 x 64] = A(TMEM) B(MN-major)
       auto issue_sdp = [&](int k) {  // S and dP of step k
         const BsStage& S = s.st[k % BS_NSTAGE];
-        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v);
+        const uint32_t a_z = smem_u32(s.z[k % BS_ZSTAGE]), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tb + TM_S, sdesc_sw128(a_z + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 32 * kk, 1024, 16), i_rk, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tb + TM_DP, sdesc_sw128(a_do + 32 * kk, 1024, 16), sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
+          mma_ts(tb + TM_DP, tb + TM_DO + 8 * kk, sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
         mma_commit(&s.sp_full);
       };
-      bool ok = mbar_wait(&s.do_full, 0, p.err, 22) && mbar_wait(&s.full[0], 0, p.err, 23);
+      // phase 0 of gs_ready: dO is in TMEM and G_{nsteps} = 0 is in place
+      bool ok = mbar_wait(&s.gs_ready, 0, p.err, 22) && mbar_wait(&s.full[0], 0, p.err, 23) &&
+                mbar_wait(&s.zfull[0], 0, p.err, 23);
       if (ok) {
         tc_fence_after();
         issue_sdp(0);
       }
       for (int k = 0; ok && k < nsteps; ++k) {
-        const int si = k % BS_NSTAGE, b = k & 1;
+        const int si = k % BS_NSTAGE;
         const int n = nsteps - 1 - k;
         const bool partial = has_partial && n == 0;
-        // the softmax side has read S/dP of step k and written its P / dS tiles
+        // the softmax side has read S/dP of step k and written P, dS
         if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
         if (k + 1 < nsteps) {
-          if (!mbar_wait(&s.full[(k + 1) % BS_NSTAGE], ((k + 1) / BS_NSTAGE) & 1, p.err, 23)) { ok = false; break; }
+          if (!mbar_wait(&s.full[(k + 1) % BS_NSTAGE], ((k + 1) / BS_NSTAGE) & 1, p.err, 23) ||
+              !mbar_wait(&s.zfull[(k + 1) % BS_ZSTAGE], ((k + 1) / BS_ZSTAGE) & 1, p.err, 23)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           issue_sdp(k + 1);
         }
-        // G_{n+1} is in gs (zero before the first step) and G_{n+1} has left TM_G
+        // G_{n+1} is in place (shared memory and TMEM) and G_{n+2} has left TM_G
         if (!mbar_wait(&s.gs_ready, k & 1, p.err, 27)) { ok = false; break; }
-        // the gradient side has drained accumulator buffer b (step k - 2)
-        if (k >= 2 && !mbar_wait(&s.acc_free[b], ((k - 2) >> 1) & 1, p.err, 29)) { ok = false; break; }
         tc_fence_after();
-        const BsStage& S = s.st[si];
-        const uint32_t a_z = smem_u32(S.z), a_kr = smem_u32(S.kr), a_f = smem_u32(S.f);
-        const uint32_t acc = b ? TM_ACC1 : TM_ACC0;
+        // G_n = [dS | G_{n+1}] [K->_c ; F_c]  (a partial step keeps G_1 of rows 0-63 in TM_G)
+        const uint32_t a_kr = smem_u32(s.st[si].kr);
+        const uint32_t tg = partial ? TM_G2 : TM_G;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tb + tg, tb + TM_DSG + 8 * kk, sdesc_sw128(a_kr + 2048 * kk, 1024, 0), i_rm, kk > 0);
+        mma_commit(&s.g_full);
+        mma_commit(&s.empty[si]);
+        mma_commit(&s.zempty[k % BS_ZSTAGE]);
+      }
+    }
+  } else if (warp == 10) {
+    // ---------------- MMA issuer B: [dK->; dF] and dV ----------------
+    if (lane == 0) {
+      const uint32_t i_tt = idesc_bf16(64, 64, 1, 1);    // [64 x 64]  = A(MN-major) B(MN-major)
+      const uint32_t i_st = idesc_bf16(128, 64, 1, 1);   // [128 x 64] = A(MN-major, two atoms) B(MN-major)
+      const uint32_t a_do = smem_u32(s.dO), a_ps = smem_u32(s.ps), a_ds = smem_u32(s.ds);
+      bool ok = mbar_wait(&s.do_full, 0, p.err, 32);
+      for (int k = 0; ok && k < nsteps; ++k) {
+        const int n = nsteps - 1 - k;
+        const bool partial = has_partial && n == 0;
+        const int zi = k % BS_ZSTAGE;
+        // P, dS (shared memory) of step k, G_{n+1} (shared memory), Z_n, and the accumulators of
+        // step k-1 drained
+        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 33) || !mbar_wait(&s.gs_ready, k & 1, p.err, 34) ||
+            !mbar_wait(&s.zfull[zi], (k / BS_ZSTAGE) & 1, p.err, 35) ||
+            (k >= 1 && !mbar_wait(&s.acc_free, (k - 1) & 1, p.err, 29))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_z = smem_u32(s.z[zi]);
         // [dK->; dF] = [dS^T; G_{n+1}^T] Z_n over the rows that crossed chunk c (rows 64-127 at a
         // partial step, where dS of rows 0-63 is zero anyway)
         {
           const uint32_t off = partial ? 64 * 128 : 0;
           const int nk = partial ? 4 : 8;
           for (int kk = 0; kk < nk; ++kk)
-            mma_ss(tb + acc + 64, sdesc_sw128(a_ds + off + 2048 * kk, 1024, ZTILE),
+            mma_ss(tb + TM_DKF, sdesc_sw128(a_ds + off + 2048 * kk, 1024, ZTILE),
                    sdesc_sw128(a_z + off + 2048 * kk, 1024, 0), i_st, kk > 0);
-        }
-        // G_n = dS K->_c + G_{n+1} F_c  (a partial step keeps G_1 of rows 0-63 in TM_G)
-        const uint32_t tg = partial ? TM_G2 : TM_G;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tb + tg, sdesc_sw128(a_ds + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 2048 * kk, 1024, 0), i_rm, kk > 0);
-        if (k > 0) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tb + tg, sdesc_sw128(a_gs + 32 * kk, 1024, 16), sdesc_sw128(a_f + 2048 * kk, 1024, 0), i_rm, 1);
         }
         mma_commit(&s.g_full);
         // dV = P^T dO  (M = 64 keys, K = 128 rows)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb + acc, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
-        mma_commit(&s.acc_full[b]);
-        mma_commit(&s.empty[si]);
+          mma_ss(tb + TM_DV, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
+        mma_commit(&s.acc_full);
+        mma_commit(&s.zempty[zi]);
       }
     }
   } else if (warp < 4) {
@@ -388,11 +426,17 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
         dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
       }
-      // the MMAs of step k-1 have read the P / dS tiles
-      if (k > 0 && !mbar_wait(&s.acc_full[(k - 1) & 1], ((k - 1) >> 1) & 1, p.err, 26)) break;
+      // the MMAs of step k-1 have read P, dS (shared memory) and dS (TMEM): the G chain and
+      // [dK->; dF] (g_full), dV (acc_full)
+      if (k > 0 && (!mbar_wait(&s.g_full, (k - 1) & 1, p.err, 36) || !mbar_wait(&s.acc_full, (k - 1) & 1, p.err, 26)))
+        break;
       store_row_bf16_sw(s.ps, r, pv);
       store_row_bf16_sw(s.ds, r, dsv);
+      uint32_t pk[32];
+      pack_row_pairs(dsv, pk);
+      tmem_st32(tb + lane_off + TM_DSG, pk);
       fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ps_ready);
     }
@@ -403,19 +447,34 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + rg;
     const int vrow = 16 * q4 + (lane & 15), vh = lane >> 4;  // dV (M=64) half row of this thread
-    {  // G_{nsteps} = 0
-      uint4* row = reinterpret_cast<uint4*>(s.gs + rg * 128);
+    {  // dO into TMEM (A operand of dP); G_{nsteps} = 0 in shared memory and TMEM
+      mbar_wait(&s.do_full, 0, p.err, 31);
+      uint32_t buf[32];
+      const uint8_t* row = s.dO + rg * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((q ^ (rg & 7)) * 16));
+        buf[4 * q] = v.x;
+        buf[4 * q + 1] = v.y;
+        buf[4 * q + 2] = v.z;
+        buf[4 * q + 3] = v.w;
+      }
+      tmem_st32(tb + lane_off + TM_DO, buf);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) buf[j] = 0u;
+      tmem_st32(tb + lane_off + TM_DSG + 32, buf);
+      uint4* grow_ = reinterpret_cast<uint4*>(s.gs + rg * 128);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) grow_[q] = make_uint4(0, 0, 0, 0);
       fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
       mbar_arrive(&s.gs_ready);
     }
     for (int k = 0; k < nsteps; ++k) {
       const int n = nsteps - 1 - k;
       const bool partial = has_partial && n == 0;
       const int c = step_chunk(has_partial, T, n);
-      const int b = k & 1;
-      const uint32_t acc = b ? TM_ACC1 : TM_ACC0;
       if (!mbar_wait(&s.g_full, k & 1, p.err, 28)) break;
       tc_fence_after();
       // G_n (rows 0-63 of a partial step keep G_1)
@@ -441,20 +500,22 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           for (int j = 0; j < 16; ++j) dst[j] = make_float4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
         } else {
           store_row_bf16_sw(s.gs, rg, g);
+          uint32_t pk[32];
+          pack_row_pairs(g, pk);
+          tmem_st32(tb + lane_off + TM_DSG + 32, pk);
           fence_proxy_async_smem();
+          tmem_st_wait();
         }
         tc_fence_before();
         mbar_arrive(&s.gs_ready);
       }
       // dV, dK->, dF of this step -> staging -> bulk fp32 reductions
-      if (!mbar_wait(&s.acc_full[b], (k >> 1) & 1, p.err, 30)) break;
-      tc_fence_after();
       bulk_wait_read0();  // this thread's reductions of the previous step have read their rows
       __syncwarp();
       {
         uint32_t a[32], bb[32];
-        tmem_ld32(tb + lane_off + acc + 64, a);
-        tmem_ld32(tb + lane_off + acc + 96, bb);
+        tmem_ld32(tb + lane_off + TM_DKF, a);
+        tmem_ld32(tb + lane_off + TM_DKF + 32, bb);
         tmem_ld_wait();
         float4* dst = reinterpret_cast<float4*>(s.stg_kf + rg * SROW);
 #pragma unroll
@@ -464,7 +525,9 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           dst[8 + j] = make_float4(__uint_as_float(bb[4 * j]), __uint_as_float(bb[4 * j + 1]),
                                    __uint_as_float(bb[4 * j + 2]), __uint_as_float(bb[4 * j + 3]));
         }
-        tmem_ld16x2(tb + lane_off + acc, a);
+        if (!mbar_wait(&s.acc_full, k & 1, p.err, 30)) break;
+        tc_fence_after();
+        tmem_ld16x2(tb + lane_off + TM_DV, a);
         tmem_ld_wait();
         float4* dv = reinterpret_cast<float4*>(s.stg_v + vrow * SROW + 32 * vh);
 #pragma unroll
@@ -473,7 +536,7 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
                               __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
       }
       tc_fence_before();
-      mbar_arrive(&s.acc_free[b]);
+      mbar_arrive(&s.acc_free);
       fence_proxy_async_smem();
       __syncwarp();
       {
