@@ -9,7 +9,7 @@
 //        P = exp(scale Z_n K->_c^T - lse), dP = dO V_c^T, dS = scale P (dP - D)
 //        dV_c += P^T dO,  dK->_c += dS^T Z_n,  dF_c += G_{n+1}^T Z_n,
 //        G_n = dS K->_c + G_{n+1} F_c,     dQ<-_T = G_0,
-//      the chunk sums dV, dK->, dF being added across tiles with bulk fp32 reductions;
+//      the chunk sums dV, dK->, dF being added across tiles with TMA tensor fp32 reductions;
 //   3. (finish) the per-chunk UT backward (ut_bwd_tc.cu) adds the diagonal chunk and takes
 //      dQ<-, dK->, dF back to q, k, w, beta.
 #include "internal.h"
@@ -22,6 +22,7 @@
 namespace pathattn {
 
 bool make_map_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);  // fwd_tc.cu
+bool make_map_f32_rows64(CUtensorMap* m, const void* base, uint64_t rows);                 // fwd_tc.cu
 
 namespace {
 using namespace tc;
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 // bounds these N=64 products.
 constexpr int BS_NSTAGE = 2;   // K->_c, F_c, V_c ring (L2-resident operands)
 constexpr int BS_ZSTAGE = 3;   // Z_n ring (streamed from HBM: one more stage of look-ahead)
-constexpr int SROW = D + 4;  // staging row stride (floats): 16-byte aligned, spreads rows over banks
+constexpr uint32_t BOX = 64 * 128;  // one 64-row x 32-column fp32 box (128-byte swizzled rows)
 // TMEM columns: S, dP, G_n, dV, [dK->; dF], G_0 of a partial step, dO (bf16 pairs), dS | G_{n+1}
 // (bf16 pairs, the A operand of the G chain)
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DKF = 256, TM_G2 = 320, TM_DO = 384,
@@ -196,8 +197,8 @@ struct __align__(1024) BsSmem {
   uint8_t dO[ZTILE];
   uint8_t z[BS_ZSTAGE][ZTILE];  // Z_n
   BsStage st[BS_NSTAGE];
-  float stg_v[BK * SROW];    // dV of a step (fp32 rows) for the bulk reductions
-  float stg_kf[BQ * SROW];   // dK-> (rows 0-63) and dF (rows 64-127) of a step
+  // dK->, dF, dV of a step as fp32 boxes (column halves 0-31 / 32-63) for the tensor reductions
+  uint8_t stg[6][BOX];       // 0,1: dK->   2,3: dF   4,5: dV
   uint64_t full[BS_NSTAGE], empty[BS_NSTAGE], zfull[BS_ZSTAGE], zempty[BS_ZSTAGE];
   uint64_t do_full, sp_full, ps_ready, g_full, gs_ready, acc_full, acc_free;
   uint32_t tmem_base;
@@ -215,6 +216,15 @@ struct BsParams {
   float* df;    // [BH][nc][64][64] dF (accumulated)
   int* err;
 };
+
+// 32 fp32 values as row r of a 128-byte swizzled fp32 box.
+__device__ __forceinline__ void store_box_row(uint8_t* box, int r, const uint32_t* x) {
+  uint8_t* row = box + r * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+}
+__device__ __forceinline__ void grad_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const float* x) {
   uint8_t* row = tile + r * 128;
@@ -243,6 +253,9 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
                                                             const __grid_constant__ CUtensorMap tm_kr,
                                                             const __grid_constant__ CUtensorMap tm_v,
                                                             const __grid_constant__ CUtensorMap tm_f,
+                                                            const __grid_constant__ CUtensorMap tm_rdk,
+                                                            const __grid_constant__ CUtensorMap tm_rdv,
+                                                            const __grid_constant__ CUtensorMap tm_rdf,
                                                             const BsParams p) {
   extern __shared__ uint8_t smem_raw[];
   BsSmem& s = *reinterpret_cast<BsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -471,11 +484,14 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       tc_fence_before();
       mbar_arrive(&s.gs_ready);
     }
+    // Every gradient thread runs every step (grad_sync needs all 128); after a timed-out wait
+    // (error recorded) the remaining waits are skipped.
+    bool ok = true;
     for (int k = 0; k < nsteps; ++k) {
       const int n = nsteps - 1 - k;
       const bool partial = has_partial && n == 0;
       const int c = step_chunk(has_partial, T, n);
-      if (!mbar_wait(&s.g_full, k & 1, p.err, 28)) break;
+      ok = ok && mbar_wait(&s.g_full, k & 1, p.err, 28);
       tc_fence_after();
       // G_n (rows 0-63 of a partial step keep G_1)
       {
@@ -509,42 +525,39 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         tc_fence_before();
         mbar_arrive(&s.gs_ready);
       }
-      // dV, dK->, dF of this step -> staging -> bulk fp32 reductions
-      bulk_wait_read0();  // this thread's reductions of the previous step have read their rows
-      __syncwarp();
+      // dV, dK->, dF of this step -> swizzled fp32 boxes -> six tensor reductions
+      if (rg == 0) bulk_wait_read0();  // the reductions of the previous step have read the boxes
+      grad_sync();
       {
-        uint32_t a[32], bb[32];
+        uint32_t a[32];
         tmem_ld32(tb + lane_off + TM_DKF, a);
-        tmem_ld32(tb + lane_off + TM_DKF + 32, bb);
         tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(s.stg_kf + rg * SROW);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          dst[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                               __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
-          dst[8 + j] = make_float4(__uint_as_float(bb[4 * j]), __uint_as_float(bb[4 * j + 1]),
-                                   __uint_as_float(bb[4 * j + 2]), __uint_as_float(bb[4 * j + 3]));
-        }
-        if (!mbar_wait(&s.acc_full, k & 1, p.err, 30)) break;
+        const int bx = rg < 64 ? 0 : 2, br = rg & 63;
+        store_box_row(s.stg[bx], br, a);
+        tmem_ld32(tb + lane_off + TM_DKF + 32, a);
+        tmem_ld_wait();
+        store_box_row(s.stg[bx + 1], br, a);
+        ok = ok && mbar_wait(&s.acc_full, k & 1, p.err, 30);
         tc_fence_after();
         tmem_ld16x2(tb + lane_off + TM_DV, a);
         tmem_ld_wait();
-        float4* dv = reinterpret_cast<float4*>(s.stg_v + vrow * SROW + 32 * vh);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dv[j] = make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                              __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
+        store_box_row(s.stg[4 + vh], vrow, a);
       }
       tc_fence_before();
       mbar_arrive(&s.acc_free);
       fence_proxy_async_smem();
-      __syncwarp();
-      {
-        const size_t crow = (size_t)bh * p.Lp + (size_t)c * BK;
-        if (rg < 64) bulk_reduce_add_f32(p.dkr + (crow + rg) * D, s.stg_kf + rg * SROW, D * 4);
-        else if (k > 0)
-          bulk_reduce_add_f32(p.df + (((size_t)bh * p.nc + c) * D + (rg - 64)) * D, s.stg_kf + rg * SROW, D * 4);
-        if (vh == 0) bulk_reduce_add_f32(p.dv + (crow + vrow) * D, s.stg_v + vrow * SROW, D * 4);
+      grad_sync();
+      if (rg == 0) {
+        const int crow = bh * p.Lp + c * BK;
+        const int frow = (bh * p.nc + c) * D;
+        tma_reduce_add_2d(&tm_rdk, s.stg[0], 0, crow);
+        tma_reduce_add_2d(&tm_rdk, s.stg[1], 32, crow);
+        if (k > 0) {  // G_{nsteps} = 0: the first step adds nothing to dF
+          tma_reduce_add_2d(&tm_rdf, s.stg[2], 0, frow);
+          tma_reduce_add_2d(&tm_rdf, s.stg[3], 32, frow);
+        }
+        tma_reduce_add_2d(&tm_rdv, s.stg[4], 0, crow);
+        tma_reduce_add_2d(&tm_rdv, s.stg[5], 32, crow);
         bulk_commit();
       }
     }
@@ -589,7 +602,10 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 2) {
-    CUtensorMap m_do, m_kr, m_v, m_f;
+    CUtensorMap m_do, m_kr, m_v, m_f, m_rdk, m_rdv, m_rdf;
+    if (!make_map_f32_rows64(&m_rdk, ws + w.dkr64, rows) || !make_map_f32_rows64(&m_rdv, ws + w.dv, rows) ||
+        !make_map_f32_rows64(&m_rdf, ws + w.df64, (uint64_t)g.BH * g.nc * D))
+      return cudaErrorInvalidValue;
     if (!make_map_rows64(&m_do, dO, (uint64_t)g.BH * g.L, BQ) ||
         !make_map_rows64(&m_kr, ws + w.p64.kr, rows, BK) || !make_map_rows64(&m_v, v, (uint64_t)g.BH * g.L, BK) ||
         !make_map_rows64(&m_f, ws + w.p64.f, (uint64_t)g.BH * g.nc * D, D))
@@ -613,7 +629,8 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     const size_t smem = sizeof(BsSmem) + 1024;
     if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), BS_THREADS, smem, st>>>(m_do, m_kr, m_v, m_f, bp);
+    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), BS_THREADS, smem, st>>>(m_do, m_kr, m_v, m_f, m_rdk, m_rdv,
+                                                                                m_rdf, bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {

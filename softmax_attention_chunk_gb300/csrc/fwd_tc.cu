@@ -439,6 +439,20 @@ bool make_map_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][64] fp32 matrix seen in 64-row x 32-column boxes with 128-byte swizzle (targets of the
+// backward's bulk reductions).
+bool make_map_f32_rows64(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {64, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {32, 64};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [heads][L][64] bf16 tensor seen in 64-row boxes of one head; rows >= L read as zero.
 bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads) {
   auto enc = tensor_map_encoder();

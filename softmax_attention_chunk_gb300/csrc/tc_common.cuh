@@ -253,6 +253,14 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* sme
                "r"(smem_u32(smem_src)), "r"(bytes)
                : "memory");
 }
+// Element-wise fp32 add of a shared-memory box into global memory through a tensor map
+// (the reduction happens at L2); the box is in the map's swizzled layout.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* smem_src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until the shared-memory sources of all committed bulk groups have been read.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
