@@ -15,6 +15,7 @@
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
+#include "ut_common.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -169,7 +170,8 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 
 // ============================ adjoint scan ============================
 // Per step k (chunk c, transported queries Z_n, n = nsteps - 1 - k) the MMA issuer runs
-//   S_{k+1} = Z K->^T, dP_{k+1} = dO V^T          (one step ahead, for the softmax side)
+//   S_{k+1} = Z K->^T, dP_{k+1} = dO V^T          (one step ahead: as soon as the softmax side has
+//                                                  taken S_k, dP_k into registers)
 //   G_n = [dS | G_{n+1}] [K->_c ; F_c]            (one K=128 chain, A from TMEM)
 //   [dK->_c ; dF_c] = [dS^T ; G_{n+1}^T] Z_n      (one M=128 MMA: the dS and G tiles are adjacent
 //                                                  in shared memory and form one MN-major operand)
@@ -177,8 +179,9 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
 // dO (constant per tile), dS and G_{n+1} are also kept in TMEM as bf16 pairs, so that dP and G
 // read only their B tiles from shared memory; shared-memory bandwidth, not the tensor pipe,
 // bounds these N=64 products.
-constexpr int BS_NSTAGE = 2;   // K->_c, F_c, V_c ring (L2-resident operands)
-constexpr int BS_ZSTAGE = 3;   // Z_n ring (streamed from HBM: one more stage of look-ahead)
+constexpr int BS_KSTAGE = 3;   // [K->_c ; F_c] ring (held until the G chain of the step completes)
+constexpr int BS_VSTAGE = 2;   // V_c ring (released once dP of the step completes)
+constexpr int BS_ZSTAGE = 3;   // Z_n ring (streamed from HBM)
 constexpr uint32_t BOX = 64 * 128;  // one 64-row x 32-column fp32 box (128-byte swizzled rows)
 // TMEM columns: S, dP, G_n, dV, [dK->; dF], G_0 of a partial step, dO (bf16 pairs), dS | G_{n+1}
 // (bf16 pairs, the A operand of the G chain)
@@ -188,7 +191,6 @@ constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DKF = 256, 
 struct __align__(1024) BsStage {
   uint8_t kr[BK * 128];    // K->_c  } adjacent: the B operand [K->_c ; F_c] of the G chain
   uint8_t f[BK * 128];     // F_c    }
-  uint8_t v[BK * 128];     // V_c
 };
 struct __align__(1024) BsSmem {
   uint8_t ps[ZTILE];       // P  (bf16, rows x keys)
@@ -196,11 +198,13 @@ struct __align__(1024) BsSmem {
   uint8_t gs[ZTILE];       // G_{n+1} (bf16, rows x d); follows ds (stacked operand)
   uint8_t dO[ZTILE];
   uint8_t z[BS_ZSTAGE][ZTILE];  // Z_n
-  BsStage st[BS_NSTAGE];
+  BsStage st[BS_KSTAGE];
+  uint8_t v[BS_VSTAGE][BK * 128];  // V_c
   // dK->, dF, dV of a step as fp32 boxes (column halves 0-31 / 32-63) for the tensor reductions
   uint8_t stg[6][BOX];       // 0,1: dK->   2,3: dF   4,5: dV
-  uint64_t full[BS_NSTAGE], empty[BS_NSTAGE], zfull[BS_ZSTAGE], zempty[BS_ZSTAGE];
-  uint64_t do_full, sp_full, ps_ready, g_full, gs_ready, acc_full, acc_free;
+  uint64_t full[BS_KSTAGE], empty[BS_KSTAGE], vfull[BS_VSTAGE], vempty[BS_VSTAGE], zfull[BS_ZSTAGE],
+      zempty[BS_ZSTAGE];
+  uint64_t do_full, sp_full, sp_free, ps_ready, g_full, gs_ready, acc_full, acc_free;
   uint32_t tmem_base;
 };
 
@@ -244,11 +248,13 @@ __device__ __forceinline__ void pack_row_pairs(const float* x, uint32_t (&pk)[32
   for (int j = 0; j < 32; ++j) pk[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
 }
 
-// Warp roles: 0-3 softmax side (P, dS of a step), 4 TMA/bulk producer (lane 0: K->, F, V; lane
-// 16: Z), 5 MMA issuer A (S, dP, the G chain), 6-9 gradient side (G_n conversion, dQ<- output,
-// dV/dK->/dF reductions), 10 MMA issuer B ([dK->; dF], dV).  Two issuers because a tcgen05.mma
-// costs tens of cycles to issue from one thread and these products are small (N = 64).
-constexpr int BS_THREADS = 352;
+// Warp roles: 0-3 and 11-14 softmax side (P, dS of a step; two threads per query row, column
+// halves 0-31 / 32-63), 4 TMA/bulk producer (lane 0: K->, F, V; lane 16: Z), 5 MMA issuer A (S,
+// dP, the G chain), 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions),
+// 10 MMA issuer B ([dK->; dF], dV).  Two issuers because a tcgen05.mma costs tens of cycles to
+// issue from one thread and these products are small (N = 64).
+constexpr int BS_THREADS = 480;
+constexpr int BS_NSOFT = 256;
 __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
                                                             const __grid_constant__ CUtensorMap tm_kr,
                                                             const __grid_constant__ CUtensorMap tm_v,
@@ -272,9 +278,13 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     return;
   }
   if (tid == 0) {
-    for (int k = 0; k < BS_NSTAGE; ++k) {
+    for (int k = 0; k < BS_KSTAGE; ++k) {
       mbar_init(&s.full[k], 1);
       mbar_init(&s.empty[k], 1);
+    }
+    for (int k = 0; k < BS_VSTAGE; ++k) {
+      mbar_init(&s.vfull[k], 1);
+      mbar_init(&s.vempty[k], 1);
     }
     for (int k = 0; k < BS_ZSTAGE; ++k) {
       mbar_init(&s.zfull[k], 1);
@@ -282,7 +292,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     }
     mbar_init(&s.do_full, 1);
     mbar_init(&s.sp_full, 1);
-    mbar_init(&s.ps_ready, 128);
+    mbar_init(&s.sp_free, BS_NSOFT);
+    mbar_init(&s.ps_ready, BS_NSOFT);
     mbar_init(&s.g_full, 2);       // G_n (issuer A) and [dK->; dF] (issuer B) complete
     mbar_init(&s.gs_ready, 128);
     mbar_init(&s.acc_full, 1);     // issuer B's MMAs of the step complete
@@ -297,18 +308,25 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
 
   if (warp == 4) {
     // ---------------- producers ----------------
-    if (lane == 0) {  // K->_c, F_c, V_c (and dO once)
+    if (lane == 0) {  // [K->_c ; F_c] (and dO once)
       mbar_arrive_expect_tx(&s.do_full, ZTILE);
       tma_load_2d(s.dO, &tm_do, 0, bh * p.L + T * BQ, &s.do_full);
       for (int k = 0; k < nsteps; ++k) {
-        const int si = k % BS_NSTAGE;
-        if (k >= BS_NSTAGE && !mbar_wait(&s.empty[si], ((k / BS_NSTAGE) - 1) & 1, p.err, 21)) break;
+        const int si = k % BS_KSTAGE;
+        if (k >= BS_KSTAGE && !mbar_wait(&s.empty[si], ((k / BS_KSTAGE) - 1) & 1, p.err, 21)) break;
         const int c = step_chunk(has_partial, T, nsteps - 1 - k);
         BsStage& S = s.st[si];
-        mbar_arrive_expect_tx(&s.full[si], 3 * BK * 128);
+        mbar_arrive_expect_tx(&s.full[si], 2 * BK * 128);
         tma_load_2d(S.kr, &tm_kr, 0, bh * p.Lp + c * BK, &s.full[si]);
-        tma_load_2d(S.v, &tm_v, 0, bh * p.L + c * BK, &s.full[si]);
         tma_load_2d(S.f, &tm_f, 0, (bh * p.nc + c) * D, &s.full[si]);
+      }
+    } else if (lane == 8) {  // V_c
+      for (int k = 0; k < nsteps; ++k) {
+        const int vi = k % BS_VSTAGE;
+        if (k >= BS_VSTAGE && !mbar_wait(&s.vempty[vi], ((k / BS_VSTAGE) - 1) & 1, p.err, 19)) break;
+        const int c = step_chunk(has_partial, T, nsteps - 1 - k);
+        mbar_arrive_expect_tx(&s.vfull[vi], BK * 128);
+        tma_load_2d(s.v[vi], &tm_v, 0, bh * p.L + c * BK, &s.vfull[vi]);
       }
     } else if (lane == 16) {  // Z_n
       for (int k = 0; k < nsteps; ++k) {
@@ -324,8 +342,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       const uint32_t i_rk = idesc_bf16(128, 64, 0, 0);   // [128 x 64] = A(K-major / TMEM) B(K-major)^T
       const uint32_t i_rm = idesc_bf16(128, 64, 0, 1);   // [128 x 64] = A(TMEM) B(MN-major)
       auto issue_sdp = [&](int k) {  // S and dP of step k
-        const BsStage& S = s.st[k % BS_NSTAGE];
-        const uint32_t a_z = smem_u32(s.z[k % BS_ZSTAGE]), a_kr = smem_u32(S.kr), a_v = smem_u32(S.v);
+        const BsStage& S = s.st[k % BS_KSTAGE];
+        const uint32_t a_z = smem_u32(s.z[k % BS_ZSTAGE]), a_kr = smem_u32(S.kr), a_v = smem_u32(s.v[k % BS_VSTAGE]);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tb + TM_S, sdesc_sw128(a_z + 32 * kk, 1024, 16), sdesc_sw128(a_kr + 32 * kk, 1024, 16), i_rk, kk > 0);
@@ -333,22 +351,24 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         for (int kk = 0; kk < 4; ++kk)
           mma_ts(tb + TM_DP, tb + TM_DO + 8 * kk, sdesc_sw128(a_v + 32 * kk, 1024, 16), i_rk, kk > 0);
         mma_commit(&s.sp_full);
+        mma_commit(&s.vempty[k % BS_VSTAGE]);
       };
       // phase 0 of gs_ready: dO is in TMEM and G_{nsteps} = 0 is in place
       bool ok = mbar_wait(&s.gs_ready, 0, p.err, 22) && mbar_wait(&s.full[0], 0, p.err, 23) &&
-                mbar_wait(&s.zfull[0], 0, p.err, 23);
+                mbar_wait(&s.vfull[0], 0, p.err, 23) && mbar_wait(&s.zfull[0], 0, p.err, 23);
       if (ok) {
         tc_fence_after();
         issue_sdp(0);
       }
       for (int k = 0; ok && k < nsteps; ++k) {
-        const int si = k % BS_NSTAGE;
+        const int si = k % BS_KSTAGE;
         const int n = nsteps - 1 - k;
         const bool partial = has_partial && n == 0;
-        // the softmax side has read S/dP of step k and written P, dS
-        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24)) { ok = false; break; }
+        // the softmax side has taken S/dP of step k into registers: issue step k+1's
+        if (!mbar_wait(&s.sp_free, k & 1, p.err, 37)) { ok = false; break; }
         if (k + 1 < nsteps) {
-          if (!mbar_wait(&s.full[(k + 1) % BS_NSTAGE], ((k + 1) / BS_NSTAGE) & 1, p.err, 23) ||
+          if (!mbar_wait(&s.full[(k + 1) % BS_KSTAGE], ((k + 1) / BS_KSTAGE) & 1, p.err, 23) ||
+              !mbar_wait(&s.vfull[(k + 1) % BS_VSTAGE], ((k + 1) / BS_VSTAGE) & 1, p.err, 23) ||
               !mbar_wait(&s.zfull[(k + 1) % BS_ZSTAGE], ((k + 1) / BS_ZSTAGE) & 1, p.err, 23)) {
             ok = false;
             break;
@@ -356,8 +376,12 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           tc_fence_after();
           issue_sdp(k + 1);
         }
-        // G_{n+1} is in place (shared memory and TMEM) and G_{n+2} has left TM_G
-        if (!mbar_wait(&s.gs_ready, k & 1, p.err, 27)) { ok = false; break; }
+        // dS of step k is in TMEM, G_{n+1} is in place (shared memory and TMEM) and G_{n+2} has
+        // left TM_G
+        if (!mbar_wait(&s.ps_ready, k & 1, p.err, 24) || !mbar_wait(&s.gs_ready, k & 1, p.err, 27)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         // G_n = [dS | G_{n+1}] [K->_c ; F_c]  (a partial step keeps G_1 of rows 0-63 in TM_G)
         const uint32_t a_kr = smem_u32(s.st[si].kr);
@@ -409,10 +433,11 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         mma_commit(&s.zempty[zi]);
       }
     }
-  } else if (warp < 4) {
-    // ---------------- softmax side: thread r owns query row r of the tile ----------------
-    const int r = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 4 || warp >= 11) {
+    // ---------------- softmax side: thread (r, h) owns columns 32h..32h+31 of query row r ----------------
+    const int q4 = warp & 3, h = warp < 4 ? 0 : 1;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int grow = T * BQ + r;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
     const float lse2 = grow < p.L ? p.lse[(size_t)bh * p.L + grow] * kLog2e : INFINITY;
@@ -423,31 +448,29 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       const bool active = !(partial && r < 64);
       if (!mbar_wait(&s.sp_full, k & 1, p.err, 25)) break;
       tc_fence_after();
-      uint32_t sa[32], sb[32], da[32], db[32];
-      tmem_ld32(tb + lane_off + TM_S, sa);
-      tmem_ld32(tb + lane_off + TM_S + 32, sb);
-      tmem_ld32(tb + lane_off + TM_DP, da);
-      tmem_ld32(tb + lane_off + TM_DP + 32, db);
+      uint32_t sa[32], da[32];
+      tmem_ld32(tb + lane_off + TM_S + 32 * h, sa);
+      tmem_ld32(tb + lane_off + TM_DP + 32 * h, da);
       tmem_ld_wait();
-      float pv[64], dsv[64];
+      tc_fence_before();
+      mbar_arrive(&s.sp_free);  // S and dP of step k may be overwritten
+      float pv[32], dsv[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
-        const float p1 = active ? fast_exp2(fmaf(__uint_as_float(sb[j]), p.scl, -lse2)) : 0.f;
         pv[j] = p0;
-        pv[32 + j] = p1;
         dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
-        dsv[32 + j] = p.scale * p1 * (__uint_as_float(db[j]) - Dr);
       }
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(dsv[2 * j], dsv[2 * j + 1]);
       // the MMAs of step k-1 have read P, dS (shared memory) and dS (TMEM): the G chain and
       // [dK->; dF] (g_full), dV (acc_full)
       if (k > 0 && (!mbar_wait(&s.g_full, (k - 1) & 1, p.err, 36) || !mbar_wait(&s.acc_full, (k - 1) & 1, p.err, 26)))
         break;
-      store_row_bf16_sw(s.ps, r, pv);
-      store_row_bf16_sw(s.ds, r, dsv);
-      uint32_t pk[32];
-      pack_row_pairs(dsv, pk);
-      tmem_st32(tb + lane_off + TM_DSG, pk);
+      put_half(s.ps, r, h, pv);
+      put_half(s.ds, r, h, dsv);
+      tmem_st16(tb + lane_off + TM_DSG + 16 * h, pk);
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
