@@ -183,10 +183,10 @@ constexpr int BS_KSTAGE = 3;   // [K->_c ; F_c] ring (held until the G chain of 
 constexpr int BS_VSTAGE = 2;   // V_c ring (released once dP of the step completes)
 constexpr int BS_ZSTAGE = 3;   // Z_n ring (streamed from HBM)
 constexpr uint32_t BOX = 64 * 128;  // one 64-row x 32-column fp32 box (128-byte swizzled rows)
-// TMEM columns: S, dP, G_n, dV, [dK->; dF], G_0 of a partial step, dO (bf16 pairs), dS | G_{n+1}
-// (bf16 pairs, the A operand of the G chain)
-constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DV = 192, TM_DKF = 256, TM_G2 = 320, TM_DO = 384,
-                   TM_DSG = 416;
+// TMEM columns: S (also G_0 of a partial step), dP, G_n, [dK->; dF], dV (two buffers), dO (bf16
+// pairs), dS | G_{n+1} (bf16 pairs, the A operand of the G chain)
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_G = 128, TM_DKF = 192, TM_DV = 256, TM_DO = 384, TM_DSG = 416;
+constexpr uint32_t TM_G2 = TM_S;  // the last step issues no next S
 
 struct __align__(1024) BsStage {
   uint8_t kr[BK * 128];    // K->_c  } adjacent: the B operand [K->_c ; F_c] of the G chain
@@ -204,7 +204,7 @@ struct __align__(1024) BsSmem {
   uint8_t stg[6][BOX];       // 0,1: dK->   2,3: dF   4,5: dV
   uint64_t full[BS_KSTAGE], empty[BS_KSTAGE], vfull[BS_VSTAGE], vempty[BS_VSTAGE], zfull[BS_ZSTAGE],
       zempty[BS_ZSTAGE];
-  uint64_t do_full, sp_full, sp_free, ps_ready, g_full, gs_ready, acc_full, acc_free;
+  uint64_t do_full, sp_full, sp_free, ps_ready, g_full, gs_ready, acc_full, dkf_free, dv_free[2];
   uint32_t tmem_base;
 };
 
@@ -297,7 +297,9 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     mbar_init(&s.g_full, 2);       // G_n (issuer A) and [dK->; dF] (issuer B) complete
     mbar_init(&s.gs_ready, 128);
     mbar_init(&s.acc_full, 1);     // issuer B's MMAs of the step complete
-    mbar_init(&s.acc_free, 128);
+    mbar_init(&s.dkf_free, 128);   // the gradient side has read [dK->; dF] of the step
+    mbar_init(&s.dv_free[0], 128); // ... and dV, one barrier per dV buffer (a single one could
+    mbar_init(&s.dv_free[1], 128); // complete step k-1 before issuer B waits for step k-2)
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -405,11 +407,11 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         const int n = nsteps - 1 - k;
         const bool partial = has_partial && n == 0;
         const int zi = k % BS_ZSTAGE;
-        // P, dS (shared memory) of step k, G_{n+1} (shared memory), Z_n, and the accumulators of
-        // step k-1 drained
+        // P, dS (shared memory) of step k, G_{n+1} (shared memory), Z_n, and [dK->; dF] of step
+        // k-1 read out
         if (!mbar_wait(&s.ps_ready, k & 1, p.err, 33) || !mbar_wait(&s.gs_ready, k & 1, p.err, 34) ||
             !mbar_wait(&s.zfull[zi], (k / BS_ZSTAGE) & 1, p.err, 35) ||
-            (k >= 1 && !mbar_wait(&s.acc_free, (k - 1) & 1, p.err, 29))) {
+            (k >= 1 && !mbar_wait(&s.dkf_free, (k - 1) & 1, p.err, 29))) {
           ok = false;
           break;
         }
@@ -425,10 +427,13 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
                    sdesc_sw128(a_z + off + 2048 * kk, 1024, 0), i_st, kk > 0);
         }
         mma_commit(&s.g_full);
-        // dV = P^T dO  (M = 64 keys, K = 128 rows)
+        // dV = P^T dO  (M = 64 keys, K = 128 rows) into buffer k % 2, read out two steps ago
+        if (k >= 2 && !mbar_wait(&s.dv_free[k & 1], ((k - 2) >> 1) & 1, p.err, 38)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tdv = TM_DV + 64 * (k & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tb + TM_DV, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
+          mma_ss(tb + tdv, sdesc_sw128(a_ps + 2048 * kk, 1024, 0), sdesc_sw128(a_do + 2048 * kk, 1024, 0), i_tt, kk > 0);
         mma_commit(&s.acc_full);
         mma_commit(&s.zempty[zi]);
       }
@@ -548,8 +553,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         tc_fence_before();
         mbar_arrive(&s.gs_ready);
       }
-      // dV, dK->, dF of this step -> swizzled fp32 boxes -> six tensor reductions
-      if (rg == 0) bulk_wait_read0();  // the reductions of the previous step have read the boxes
+      // [dK->; dF] of this step -> swizzled fp32 boxes (once the previous reductions have read them)
+      if (rg == 0) bulk_wait_read0();
       grad_sync();
       {
         uint32_t a[32];
@@ -560,14 +565,20 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         tmem_ld32(tb + lane_off + TM_DKF + 32, a);
         tmem_ld_wait();
         store_box_row(s.stg[bx + 1], br, a);
-        ok = ok && mbar_wait(&s.acc_full, k & 1, p.err, 30);
-        tc_fence_after();
-        tmem_ld16x2(tb + lane_off + TM_DV, a);
+      }
+      tc_fence_before();
+      mbar_arrive(&s.dkf_free);
+      // dV of this step (buffer k % 2) -> boxes 4, 5; then the six tensor reductions
+      ok = ok && mbar_wait(&s.acc_full, k & 1, p.err, 30);
+      tc_fence_after();
+      {
+        uint32_t a[32];
+        tmem_ld16x2(tb + lane_off + TM_DV + 64 * (k & 1), a);
         tmem_ld_wait();
         store_box_row(s.stg[4 + vh], vrow, a);
       }
       tc_fence_before();
-      mbar_arrive(&s.acc_free);
+      mbar_arrive(&s.dv_free[k & 1]);
       fence_proxy_async_smem();
       grad_sync();
       if (rg == 0) {
