@@ -56,17 +56,19 @@ def tiles_steps(L):
 
 
 def phase_roofline(L, BH, pk):
-    """Per phase of the fwd+bwd step: (algorithmic flops per launch, bound, peak TFLOP/s)."""
+    """Per phase of the fwd+bwd step: (algorithmic work per launch, bound, peak, unit); work is
+    flops for the tensor-core phases and HBM bytes for the bandwidth-bound one."""
     nc64 = (L + 127) // 128 * 2
-    nt, steps = tiles_steps(L)
+    Lp = nc64 * 64
     npairs = nc64 * (nc64 - 1) // 2
     return {
-        "fwd_prepare": (2 * BH * nc64 * UT_PREP64_MMAS * 64 ** 3, "tensor", pk["bf16"]),
-        "fwd_scan": (BH * npairs * (4 * 64 * 64 * D + 2 * 64 * D * D), "tensor", pk["bf16"]),
-        # the forward's preparation is reused: the backward prepare phase runs D_i and the Z chain
-        "bwd_prepare": (2 * BH * (steps - nt) * 128 * D * D, "tensor", pk["bf16"]),
-        "bwd_scan": (BH * npairs * (10 * 64 * 64 * D + 4 * 64 * D * D), "tensor", pk["bf16"]),
-        "bwd_finish": (2 * BH * nc64 * UT_BWD64_MMAS * 64 ** 3, "tensor", pk["bf16"]),
+        "fwd_prepare": (2 * BH * nc64 * UT_PREP64_MMAS * 64 ** 3, "tensor", pk["bf16"], "TFLOP/s"),
+        "fwd_scan": (BH * npairs * (4 * 64 * 64 * D + 2 * 64 * D * D), "tensor", pk["bf16"], "TFLOP/s"),
+        # the forward's preparation and transported queries are reused: the backward prepare phase
+        # reads o and dO for D_i (bf16), writes D_i and zeroes the fp32 accumulators dK->, dV, dF
+        "bwd_prepare": (BH * (2 * L * D * 2 + Lp * 4 + 2 * Lp * D * 4 + nc64 * D * D * 4), "hbm", pk["hbm"], "GB/s"),
+        "bwd_scan": (BH * npairs * (10 * 64 * 64 * D + 4 * 64 * D * D), "tensor", pk["bf16"], "TFLOP/s"),
+        "bwd_finish": (2 * BH * nc64 * UT_BWD64_MMAS * 64 ** 3, "tensor", pk["bf16"], "TFLOP/s"),
     }
 
 
@@ -273,15 +275,18 @@ def run_ours(args):
     grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q), dw=torch.empty_like(q),
                  dbeta=torch.empty_like(beta))
 
-    # Training step: the forward runs in the backward's workspace and the backward reuses its
-    # per-chunk preparation (PATH_BWD_REUSE_FWD), as a training framework keeps forward state.
-    bwd_phases = (pa.PATH_BWD_PREPARE | pa.PATH_BWD_REUSE_FWD, pa.PATH_BWD_SCAN, pa.PATH_BWD_FINISH)
+    # Training step: the forward runs in the backward's workspace and stores its transported
+    # query tiles (PATH_FWD_STORE_Z); the backward reuses them and the per-chunk preparation
+    # (PATH_BWD_Z_FROM_FWD, PATH_BWD_REUSE_FWD), as a training framework keeps forward state.
+    bwd_phases = (pa.PATH_BWD_PREPARE | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD, pa.PATH_BWD_SCAN,
+                  pa.PATH_BWD_FINISH)
 
     def step(evs=None):
         marks = [ev()] if evs is not None else None
         pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_PREPARE)
         if marks is not None: marks.append(ev())
-        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_SCAN)
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse),
+               phases=pa.PATH_FWD_SCAN | pa.PATH_FWD_STORE_Z)
         if marks is not None: marks.append(ev())
         for ph in bwd_phases:
             pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads, phases=ph)
@@ -312,20 +317,34 @@ def run_ours(args):
     pr = phase_roofline(L, BH, pk)
     phases = {}
     for n, ms in phase_ms.items():
-        fl, bound, peak = pr[n]
-        ach = fl / (ms * 1e-3) / 1e12
-        phases[n] = {"ms": ms, "share": ms / sum(phase_ms.values()), "flops": fl, "achieved": ach,
-                     "bound": bound, "peak": peak, "frac": ach / peak}
+        work, bound, peak, unit = pr[n]
+        ach = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        phases[n] = {"ms": ms, "share": ms / sum(phase_ms.values()), ("flops" if unit == "TFLOP/s" else "bytes"): work,
+                     "achieved": ach, "unit": unit, "bound": bound, "peak": peak, "frac": ach / peak}
     dom = max(phase_ms, key=lambda n: phase_ms[n])
     kernels = {"fwd_prepare": "ut_prep64_kernel (tcgen05 UT preparation)",
                "fwd_scan": "fwd_scan_tc_kernel (tcgen05)",
-               "bwd_prepare": "bwd_dot + zchain_tc_kernel (forward preparation reused)",
+               "bwd_prepare": "bwd_dot_kernel + accumulator memsets (forward preparation and Z tiles reused)",
                "bwd_scan": "bwd_scan_tc_kernel (tcgen05)",
                "bwd_finish": "ut_bwd64_kernel (tcgen05 UT backward)"}
     d = phases[dom]
-    roofline = {"kernel": f"{dom}: {kernels[dom]}", "bound": "tensor", "achieved": d["achieved"], "peak": d["peak"],
-                "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
-                "peak_source": f"bf16 dense ({pk['src']})"}
+    roofline = {"kernel": f"{dom}: {kernels[dom]}", "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "peak_source": (f"bf16 dense ({pk['src']})" if d["bound"] == "tensor" else f"HBM copy ({pk['src']})")}
+
+    # the forward on its own (inference: no transported-query store), against the bf16 peak
+    fw = []
+    for i in range(args.warmup + args.steps):
+        a = ev()
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse))
+        b = ev()
+        if i >= args.warmup:
+            fw.append((a, b))
+    torch.cuda.synchronize()
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fw)
+    fwd_tf = BH * fwd_flops_per_head(L, cfg["head_dim"], B_f) / (fwd_ms * 1e-3) / 1e12
+    forward = {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_bf16_peak": fwd_tf / pk["bf16"],
+               "note": "inference forward (prepare + scan, no Z store), same inputs, after the timed steps"}
     scan_roofline = {n: {"achieved": phases[n]["achieved"], "peak": phases[n]["peak"], "frac": phases[n]["frac"],
                          "unit": "TFLOP/s", "of": "measured bf16 dense"} for n in ("fwd_scan", "bwd_scan")}
 
@@ -340,9 +359,9 @@ def run_ours(args):
     def e2e_step():
         for n, t in host.items():
             x[n].copy_(t, non_blocking=True)
-        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse))
+        pa.fwd(q, k, v, w, beta, None, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z)
         pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, out=grads,
-               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD)
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
         outs_h["o"].copy_(o, non_blocking=True)
         outs_h["lse"].copy_(lse, non_blocking=True)
         for n, t in grads.items():
@@ -375,8 +394,8 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (6 x 512 MiB per step)"},
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
-                "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "e2e": e2e,
-                "clocks": clocks_rec, "gpu_launches": 6 * args.steps, "memset_ops": 5 * args.steps,
+                "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward, "e2e": e2e,
+                "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 5 * args.steps,
                 "peaks": pk, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -142,6 +142,17 @@ enum { PATH_BWD_PREPARE = 1, PATH_BWD_SCAN = 2, PATH_BWD_FINISH = 4, PATH_BWD_AL
  * PREPARE then skips recomputing it (the bf16 tensor-core path; ignored by the fp32 path).  If the
  * statement is false the gradients are wrong; nothing detects it. */
 enum { PATH_BWD_REUSE_FWD = 8 };
+/* Optional bit for path_attn_fwd_phases(SCAN), for a forward that a backward will follow (a
+ * training step): ws must be backward-sized (path_attn_workspace_size(desc, 1), else
+ * PATH_ERR_WORKSPACE), and the scan also stores every transported query tile Z_n (§2.7: the
+ * queries carried across earlier chunks) in ws, which the backward needs.  The bf16
+ * tensor-core path only; ignored by the fp32 path. */
+enum { PATH_FWD_STORE_Z = 4 };
+/* Optional bit for path_attn_bwd_phases(PREPARE): the workspace already holds the transported
+ * query tiles because the forward ran with PATH_FWD_STORE_Z on it (same inputs, descriptor and
+ * workspace, nothing used it since); PREPARE then skips recomputing them.  Same caveat and scope
+ * as PATH_BWD_REUSE_FWD. */
+enum { PATH_BWD_Z_FROM_FWD = 16 };
 
 int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, const void* q, const void* k,
                          const void* v, const void* w, const float* beta, const float* log_f,

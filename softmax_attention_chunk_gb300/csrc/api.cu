@@ -100,7 +100,7 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
   Geom g;
   int rc = check_desc(desc, 0, &g);
   if (rc != PATH_OK) return rc;
-  if (phases <= 0 || (phases & ~PATH_FWD_ALL)) return PATH_ERR_INVALID_ARG;
+  if ((phases & PATH_FWD_ALL) == 0 || (phases & ~(PATH_FWD_ALL | PATH_FWD_STORE_Z))) return PATH_ERR_INVALID_ARG;
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o); CHECK_PTR(lse);
   if (log_f && !aligned(log_f, 16)) return PATH_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
@@ -110,13 +110,19 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
   char* wsb = (char*)ws;
   if (uses_tensor_cores(desc, 0)) {
     const TcWs tw = tc_layout(desc, false);
+    void* zstore = nullptr;
+    if (phases & PATH_FWD_STORE_Z) {  // the backward-sized layout holds the Z store
+      const TcWs twb = tc_layout(desc, true);
+      if (ws_bytes < twb.total) return PATH_ERR_WORKSPACE;
+      zstore = wsb + twb.zs;
+    }
     if (phases & PATH_FWD_PREPARE) {
       rc = cuda_status(cudaMemsetAsync(wsb + tw.p64.err, 0, sizeof(int), st));
       if (rc == PATH_OK) rc = cuda_status(launch_ut_prep64(tw.g64, q, k, v, w, beta, log_f, wsb, tw.p64, true, st));
       if (rc != PATH_OK) return rc;
     }
     if (phases & PATH_FWD_SCAN) {
-      rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, st));
+      rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, zstore, st));
       if (rc != PATH_OK) return rc;
     }
     return PATH_OK;
@@ -148,7 +154,8 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
   Geom g;
   int rc = check_desc(desc, 1, &g);
   if (rc != PATH_OK) return rc;
-  if ((phases & PATH_BWD_ALL) == 0 || (phases & ~(PATH_BWD_ALL | PATH_BWD_REUSE_FWD))) return PATH_ERR_INVALID_ARG;
+  if ((phases & PATH_BWD_ALL) == 0 || (phases & ~(PATH_BWD_ALL | PATH_BWD_REUSE_FWD | PATH_BWD_Z_FROM_FWD)))
+    return PATH_ERR_INVALID_ARG;
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o);
   CHECK_PTR(lse); CHECK_PTR(dO); CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dw);
   CHECK_PTR(dbeta);

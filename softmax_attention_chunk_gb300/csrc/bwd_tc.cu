@@ -624,16 +624,18 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if (!(phases & 8)) {  // 8: the forward's chunk-64 preparation is already in ws
       if ((e = launch_ut_prep64(w.g64, q, k, v, wv, beta, nullptr, ws, w.p64, false, st)) != cudaSuccess) return e;
     }
-    CUtensorMap m_ql, m_f;
-    if (!make_map_rows64(&m_ql, ws + w.p64.ql, rows, BQ) ||
-        !make_map_rows64(&m_f, ws + w.p64.f, (uint64_t)g.BH * g.nc * D, D))
-      return cudaErrorInvalidValue;
-    ZcParams zp{g.L, g.Lp, g.nc, g.BH, nt, (uint8_t*)(ws + w.zs), err};
-    const size_t smem = sizeof(ZcSmem) + 1024;
-    if ((e = cudaFuncSetAttribute(zchain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-      return e;
-    zchain_tc_kernel<<<(unsigned)((long)nt * g.BH), 160, smem, st>>>(m_ql, m_f, zp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!(phases & 16)) {  // 16: the forward stored the transported query tiles in ws
+      CUtensorMap m_ql, m_f;
+      if (!make_map_rows64(&m_ql, ws + w.p64.ql, rows, BQ) ||
+          !make_map_rows64(&m_f, ws + w.p64.f, (uint64_t)g.BH * g.nc * D, D))
+        return cudaErrorInvalidValue;
+      ZcParams zp{g.L, g.Lp, g.nc, g.BH, nt, (uint8_t*)(ws + w.zs), err};
+      const size_t smem = sizeof(ZcSmem) + 1024;
+      if ((e = cudaFuncSetAttribute(zchain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      zchain_tc_kernel<<<(unsigned)((long)nt * g.BH), 160, smem, st>>>(m_ql, m_f, zp);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   if (phases & 2) {
     CUtensorMap m_do, m_kr, m_v, m_f, m_rdk, m_rdv, m_rdf;

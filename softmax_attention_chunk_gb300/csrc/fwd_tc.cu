@@ -52,9 +52,10 @@ struct __align__(1024) ScanSmem {
   uint8_t z0[BQ * 128];               // Q<- tile (bf16, 128-byte swizzled rows): the first Z
   uint8_t kf[NSTAGE][128 * 128];      // rows 0-63: K->_c, rows 64-127: F_c
   uint8_t v[NSTAGE][BK * 128];        // V_c
+  uint8_t zout[BQ * 128];             // Z_{n+1} (swizzled image) on its way to the Z store
   float xm[2][BQ];                    // per-half row maxima / sums exchanged between the halves
   uint64_t full[NSTAGE], empty[NSTAGE];
-  uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done;
+  uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done, zbuf_free;
   uint32_t tmem_base;
 };
 
@@ -69,8 +70,19 @@ struct ScanParams {
   const float* ft;
   __nv_bfloat16* o;
   float* lse;
+  uint8_t* zs;  // if set: every transported query tile Z_n is stored for the backward (bulk copies
+                // of a shared-memory tile image issued by the MMA warp)
   int* err;
 };
+
+// Part of a 128-row bf16 tile in its 128-byte swizzled image (the layout TMA writes and the
+// backward bulk-copies): the four 16-byte chunks 4h..4h+3 of row r.
+__device__ __forceinline__ void put_tile_quarter(uint8_t* tile, int r, int h, const uint32_t* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + q) ^ (r & 7)) * 16)) =
+        make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
 
 // Paired fp32 arithmetic (two lanes of a 64-bit register per instruction) and 3-input max/min.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -141,6 +153,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     mbar_init(&s.p_ready, NSOFT);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_done, 1);
+    mbar_init(&s.zbuf_free, 1);
     fence_barrier_init();
   }
   if (warp == 9) tmem_alloc(&s.tmem_base, TMEM_COLS);
@@ -189,15 +202,26 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mma_commit(&s.empty[m % NSTAGE]);
         mma_commit(&s.pv_done);
       };
+      // Z store of this tile: tile n of the tile's sequence at n * 16 KB (the tiles of earlier query
+      // tiles of the head come first: sum_{t<T} (2t+1) = T^2)
+      uint8_t* zstore = p.zs ? p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * (BQ * 128) : nullptr;
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&s.full[st], (n / NSTAGE) & 1, p.err, 3)) { ok = false; break; }
         if (!mbar_wait(&s.z_ready, n & 1, p.err, 4)) { ok = false; break; }
         tc_fence_after();
+        if (zstore) {  // Z_n (Z_0 straight from the Q<- tile)
+          bulk_store(zstore + (size_t)n * (BQ * 128), n == 0 ? s.z0 : s.zout, BQ * 128);
+          bulk_commit();
+        }
         const uint64_t d0 = dkf0 + (uint64_t)(1024 * st);
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_ts(tb + COL_S, tb + COL_Z + 8 * k, d0 + (uint64_t)(2 * k), idesc_sz, k > 0 ? 1u : 0u);
         mma_commit(&s.s_full);
+        if (zstore && n >= 1) {  // the store buffer may take Z_{n+1}
+          bulk_wait_read0();
+          mbar_arrive(&s.zbuf_free);
+        }
         if (n > 0) {
           if (!mbar_wait(&s.p_ready, (n - 1) & 1, p.err, 5)) { ok = false; break; }
           tc_fence_after();
@@ -209,6 +233,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         issue_pv(nsteps - 1);
         mma_commit(&s.o_done);
       }
+      if (zstore) bulk_wait0();  // the Z store is complete before the CTA exits
     }
   } else {
     // ---------------- softmax / transport: thread (r, h) owns columns 32h..32h+31 of row r ----------------
@@ -261,6 +286,25 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int j = 0; j < 16; ++j) z16[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
         tmem_st16(c_z, z16);
+        if (p.zs) {  // Z_{n+1} into the store buffer once the bulk copy of Z_n has read it
+          if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free, (n - 1) & 1, p.err, 10);
+          put_tile_quarter(s.zout, r, h, z16);
+          fence_proxy_async_smem();
+        }
+      } else if (n + 1 < nsteps && p.zs) {  // rows not transported at the partial step keep Z_0
+        const uint4* src = reinterpret_cast<const uint4*>(s.z0 + r * 128);
+        uint32_t z16[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = src[(4 * h + q) ^ (r & 7)];
+          z16[4 * q] = v.x;
+          z16[4 * q + 1] = v.y;
+          z16[4 * q + 2] = v.z;
+          z16[4 * q + 3] = v.w;
+        }
+        if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free, (n - 1) & 1, p.err, 10);
+        put_tile_quarter(s.zout, r, h, z16);
+        fence_proxy_async_smem();
       }
       tmem_ld32(c_s, x);
       tmem_ld_wait();
@@ -450,7 +494,7 @@ bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t
 }
 
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
-                           const FwdWs& lay, void* o, float* lse, cudaStream_t st) {
+                           const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st) {
   if (g.B != BK || (g.nc & 1) || g.Lp != g.nc * BK) return cudaErrorInvalidValue;
   CUtensorMap m_ql, m_kr, m_f, m_v;
   const uint64_t prow = (uint64_t)g.BH * g.Lp;
@@ -473,6 +517,7 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   p.ft = (const float*)(ws + lay.ft);
   p.o = (__nv_bfloat16*)o;
   p.lse = lse;
+  p.zs = (uint8_t*)zstore;
   p.err = (int*)(ws + lay.err);
   const size_t smem = sizeof(ScanSmem) + 1024;
   auto kern = logf ? fwd_scan_tc_kernel<true> : fwd_scan_tc_kernel<false>;

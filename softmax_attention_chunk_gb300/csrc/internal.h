@@ -158,7 +158,7 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
                              cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
-                           const FwdWs& lay, void* o, float* lse, cudaStream_t st);
+                           const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);
 
 // SIMT backward.  phases: bit 0 = prepare (zero accumulators, D_i, recomputed UT quantities),
 // bit 1 = adjoint chunk scan, bit 2 = per-chunk UT backward writing the gradients.

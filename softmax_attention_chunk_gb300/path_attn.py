@@ -66,6 +66,8 @@ PATH_DECODE_NOALLOC_MAX_HEADS = 496
 PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
 PATH_BWD_PREPARE, PATH_BWD_SCAN, PATH_BWD_FINISH, PATH_BWD_ALL = 1, 2, 4, 7
 PATH_BWD_REUSE_FWD = 8
+PATH_FWD_STORE_Z = 4
+PATH_BWD_Z_FROM_FWD = 16
 
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",

@@ -158,3 +158,21 @@ def test_input_generator_subsets_are_exact():
     assert torch.equal(dfull["k_cache"][0, 2], dsub["k_cache"][0])
     assert torch.equal(dfull["q"][:, 0, 2], dsub["q"][:, 0])
     assert torch.all(dfull["k_cache"][:, :, 10:] == 0)
+
+
+def test_training_step_bits_are_validated(pa):
+    """PATH_FWD_STORE_Z needs a backward-sized workspace on the bf16 tensor-core path; the new bits
+    are accepted only next to a phase, and unknown bits are rejected."""
+    d = desc(pa, dtype=pa.PATH_BF16)
+    f_bytes = pa.path_attn_workspace_size(d, 0)
+    b_bytes = pa.path_attn_workspace_size(d, 1)
+    assert f_bytes < b_bytes
+    fwd = lambda ph, n: pa.path_attn_fwd_phases(ph, d, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, n, None)
+    assert fwd(pa.PATH_FWD_SCAN | pa.PATH_FWD_STORE_Z, b_bytes - 1) == 3   # forward-sized: too small
+    assert fwd(pa.PATH_FWD_STORE_Z, b_bytes) == 1                         # no phase
+    assert fwd(pa.PATH_FWD_ALL | 8, b_bytes) == 1                         # unknown bit
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE]
+    bwd = lambda ph, n: pa.path_attn_bwd_phases(ph, d, *base, n, None)
+    assert bwd(pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD, b_bytes - 1) == 3
+    assert bwd(pa.PATH_BWD_Z_FROM_FWD, b_bytes) == 1
+    assert bwd(pa.PATH_BWD_ALL | 32, b_bytes) == 1

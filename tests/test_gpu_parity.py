@@ -209,3 +209,28 @@ def test_bwd_reusing_forward_preparation(cuda_lib):
         a, b = g_plain[key].float(), g_reuse[key].float()
         assert (a - b).abs().max().item() <= 1e-2 * max(1.0, a.abs().max().item()), key
     check_grads(inp, g_reuse, 1.0, 2e-2, rel=3e-2)
+
+
+@pytest.mark.parametrize("L", [333, 1000])
+def test_training_step_with_stored_transported_queries(cuda_lib, L):
+    """PATH_FWD_STORE_Z + PATH_BWD_Z_FROM_FWD: the forward stores every transported query tile, the
+    backward skips recomputing them; gradients equal the plain backward's (the tiles are the same
+    bf16 values up to MMA accumulation order) and the oracle's."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(2, 2, L, 64, "bf16", seed=45 + L, with_dO=True, near2_frac=0.05)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    desc = pa.make_desc(t["q"], 1.0)
+    o0, lse0 = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], None, 1.0)
+    g_plain = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o0, lse0, t["dO"], 1.0)
+    ws = pa.workspace(desc, 1, DEV)
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], None, 1.0, ws=ws,
+                    phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], 1.0, ws=ws,
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o0) and torch.equal(lse, lse0)  # storing Z leaves the outputs unchanged
+    for key in ("dq", "dk", "dv", "dw", "dbeta"):
+        a, b = g_plain[key].float(), g[key].float()
+        assert (a - b).abs().max().item() <= 1e-2 * max(1.0, a.abs().max().item()), key
+    check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
