@@ -46,6 +46,10 @@ D = 64
 # each): every product is a 64 x 64 x 64 tcgen05 MMA.
 UT_PREP64_MMAS = 12  # G, M1, N2, QK^T; M1 U, U N2, U^T W; A W, X^T W, M1 X, W^T Y; P V
 UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule through U, X, M1, N2, G
+# DRAM bytes per head of one bwd_scan_tc_kernel launch at L = 4096: ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum) of a 16-head launch divided by 16 — the kernel takes heads 16 at a time,
+# so a launch over more heads repeats that traffic per group (profiles/tc_kernels_b1h16_l4096.md).
+BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (428205568 + 82692352) / 16
 
 
 def tiles_steps(L):
@@ -328,8 +332,9 @@ def run_ours(args):
                "bwd_scan": "bwd_scan_tc_kernel (tcgen05)",
                "bwd_finish": "ut_bwd64_kernel (tcgen05 UT backward)"}
     d = phases[dom]
+    traffic = BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 * BH if (dom == "bwd_scan" and L == 4096) else None
     roofline = {"kernel": f"{dom}: {kernels[dom]}", "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
-                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                 "peak_source": (f"bf16 dense ({pk['src']})" if d["bound"] == "tensor" else f"HBM copy ({pk['src']})")}
 
     # the forward on its own (inference: no transported-query store), against the bf16 peak
