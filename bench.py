@@ -47,8 +47,9 @@ D = 64
 UT_PREP64_MMAS = 12  # G, M1, N2, QK^T; M1 U, U N2, U^T W; A W, X^T W, M1 X, W^T Y; P V
 UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule through U, X, M1, N2, G
 # DRAM bytes per head of one bwd_scan_tc_kernel launch at L = 4096: ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum) of a 16-head launch divided by 16 — the kernel takes heads 16 at a time,
-# so a launch over more heads repeats that traffic per group (profiles/tc_kernels_b1h16_l4096.md).
+# dram__bytes_write.sum) of a 16-head launch (batch 1, 16 heads) divided by 16 — the kernel takes
+# heads 16 at a time, so a launch over more heads repeats that traffic per group.  To be retaken
+# whenever the kernel changes.
 BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (428205568 + 82692352) / 16
 
 
