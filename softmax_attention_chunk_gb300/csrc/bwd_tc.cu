@@ -553,8 +553,12 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         tc_fence_before();
         mbar_arrive(&s.gs_ready);
       }
-      // [dK->; dF] of this step -> swizzled fp32 boxes (once the previous reductions have read them)
-      if (rg == 0) bulk_wait_read0();
+      // [dK->; dF] of this step -> swizzled fp32 boxes 0-3 -> four tensor reductions (one bulk
+      // group); dV -> boxes 4, 5 -> two more (a second group).  Each staging waits only for the
+      // group of the previous step that read the same boxes.
+      const int crow = bh * p.Lp + c * BK;
+      const int frow = (bh * p.nc + c) * D;
+      if (rg == 0) bulk_wait_read1();  // the previous step's [dK->; dF] group has read boxes 0-3
       grad_sync();
       {
         uint32_t a[32];
@@ -568,9 +572,22 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       }
       tc_fence_before();
       mbar_arrive(&s.dkf_free);
-      // dV of this step (buffer k % 2) -> boxes 4, 5; then the six tensor reductions
+      fence_proxy_async_smem();
+      grad_sync();
+      if (rg == 0) {
+        tma_reduce_add_2d(&tm_rdk, s.stg[0], 0, crow);
+        tma_reduce_add_2d(&tm_rdk, s.stg[1], 32, crow);
+        if (k > 0) {  // G_{nsteps} = 0: the first step adds nothing to dF
+          tma_reduce_add_2d(&tm_rdf, s.stg[2], 0, frow);
+          tma_reduce_add_2d(&tm_rdf, s.stg[3], 32, frow);
+        }
+        bulk_commit();
+      }
+      // dV of this step (buffer k % 2)
       ok = ok && mbar_wait(&s.acc_full, k & 1, p.err, 30);
       tc_fence_after();
+      if (rg == 0) bulk_wait_read1();  // the previous step's dV group has read boxes 4, 5
+      grad_sync();
       {
         uint32_t a[32];
         tmem_ld16x2(tb + lane_off + TM_DV + 64 * (k & 1), a);
@@ -582,14 +599,6 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       fence_proxy_async_smem();
       grad_sync();
       if (rg == 0) {
-        const int crow = bh * p.Lp + c * BK;
-        const int frow = (bh * p.nc + c) * D;
-        tma_reduce_add_2d(&tm_rdk, s.stg[0], 0, crow);
-        tma_reduce_add_2d(&tm_rdk, s.stg[1], 32, crow);
-        if (k > 0) {  // G_{nsteps} = 0: the first step adds nothing to dF
-          tma_reduce_add_2d(&tm_rdf, s.stg[2], 0, frow);
-          tma_reduce_add_2d(&tm_rdf, s.stg[3], 32, frow);
-        }
         tma_reduce_add_2d(&tm_rdv, s.stg[4], 0, crow);
         tma_reduce_add_2d(&tm_rdv, s.stg[5], 32, crow);
         bulk_commit();
