@@ -277,6 +277,11 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* 
                "r"(x), "r"(y), "r"(smem_u32(smem_src))
                : "memory");
 }
+// Asks the TMA engine to bring `bytes` (a multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until the shared-memory sources of all committed bulk groups have been read.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

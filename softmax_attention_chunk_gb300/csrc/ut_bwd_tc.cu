@@ -139,8 +139,13 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     __syncthreads();
   };
 
-  // ---- loads: W, Q, K, V, dO by TMA (rows >= L read as zero) ----
+  // ---- loads: W, Q, K, V, dO by TMA (rows >= L read as zero); the fp32 gradients that the
+  //      epilogues read later are brought into L2 meanwhile ----
   if (lead) {
+    bulk_prefetch_l2(p.dql + ws_row * D, B * D * 4);
+    bulk_prefetch_l2(p.dkr + ws_row * D, B * D * 4);
+    bulk_prefetch_l2(p.dvacc + ws_row * D, B * D * 4);
+    bulk_prefetch_l2(p.df + ((size_t)bh * p.nc + c) * D * D, D * D * 4);
     mbar_arrive_expect_tx(&s.bar_in, 5 * TILE);
     tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
     tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
