@@ -47,14 +47,14 @@ enum {
   S_W,   // W [all]
   S_Q,   // Q [P2] | L fp32 low half [P2-P3] | P [P5-P6] | gM1 [P6-P7] | gU [P8-P9]
   S_K,   // K [P2] | L fp32 high half [P2-P3] | dS [P5-P8] | diag(beta) W [P8-P11]
-  S_V,   // V [P4] | dF [P4-P7] | gN2 [P7-P8] | A1 [P9-P10]
-  S_DO,  // dO [P4-P6] | gX [P6-P8] | gU.*Y fp32 low half [P8-P9] | diag(beta) gN [P10-P11]
+  S_V,   // V [P3] | dF [P3-P7] | gN2 [P7-P8] | A1 [P9-P10]
+  S_DO,  // dO [P3-P6] | gX [P6-P8] | gU.*Y fp32 low half [P8-P9] | diag(beta) gN [P10-P11]
   S_M1,  // M1 [P2-P7] | gU.*Y fp32 high half [P8-P9]
   S_N2,  // N2 [P2-P8] | gN [P10-P11]
   S_U,   // U [P3-P9]
   S_Y,   // Y [P3-P10]
-  S_DQ,  // dQ<- [P4-P7] | E3 [P7-P8]
-  S_DK,  // dK-> [P4-P6]
+  S_DQ,  // dQ<- [P3-P7] | E3 [P7-P8]
+  S_DK,  // dK-> [P3-P6]
   S_X,   // X [P4-P6] | Q again [P7-P8]
   S_Y1,  // Y1 [P4-P6] | K again [P7-P8]
   NSLOT
@@ -193,8 +193,15 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   }
   publish();
 
-  // ---- P3: Y = (I + strictLower(D G))^{-1} by forward substitution (warps 0-1, lane = column);
-  //      Y and U = Y D as bf16 tiles ----
+  // ---- P3: dP = dO V^T goes to the tensor core first (its accumulator is free).  Warps 0-1 solve
+  //      Y = (I + strictLower(D G))^{-1} by forward substitution (lane = column) and write Y and
+  //      U = Y D as bf16 tiles; meanwhile warps 2-3 (thread = row) write dQ<- and dK-> (zero past
+  //      L) and, once dP has read V, dF into V's slot as bf16 operand tiles ----
+  if (tid == 64) {
+    tc_fence_after();
+    mma64(tb + C2, ta(S_DO), 0, ta(S_V), 0, 0);
+    mma_commit(&s.bar_mma);
+  }
   if (warp < 2) {
     const int cc = 32 * warp + lane;
     float y[64];
@@ -205,14 +212,41 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
       *reinterpret_cast<__nv_bfloat16*>(s.t[S_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r]);
       *reinterpret_cast<__nv_bfloat16*>(s.t[S_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r] * bc);
     }
+  } else {
+    const int r = tid - 64;
+    const bool ok = row0 + r < p.L;
+    float x[32];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (ok) {
+        load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, x);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      }
+      put_half(s.t[S_DQ], r, hh, x);
+      if (ok) {
+        load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, x);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      }
+      put_half(s.t[S_DK], r, hh, x);
+    }
+    float f0[32], f1[32];
+    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D, f0);
+    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D + 32, f1);
+    mbar_wait(&s.bar_mma, mph, p.err, 52);  // dP has read V
+    put_half(s.t[S_DF], r, 0, f0);
+    put_half(s.t[S_DF], r, 1, f1);
   }
+  mph ^= 1;
   publish();
 
-  // ---- P4: X = U N2, Y1 = U W, dP = dO V^T ----
+  // ---- P4: X = U N2, Y1 = U W ----
   issue([&] {
     mma64(tb + C0, ta(S_U), 0, ta(S_N2), 1, 0);
     mma64(tb + C1, ta(S_U), 0, ta(S_W), 1, 0);
-    mma64(tb + C2, ta(S_DO), 0, ta(S_V), 0, 0);
   });
   wait_mma(43);
   {
@@ -221,21 +255,6 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     put_half(s.t[S_X], i, h, x);
     ld_half(tb, lane_off, C1, x);
     put_half(s.t[S_Y1], i, h, x);
-    // dF (V's slot), dQ<- and dK-> as bf16 operand tiles: row tid/2, half tid%2
-    const int r = tid >> 1, hh = tid & 1;
-    const bool ok = row0 + r < p.L;
-    float y1[32], y2[32];
-    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D + 32 * hh, x);
-    if (ok) {
-      load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, y1);
-      load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, y2);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) y1[j] = y2[j] = 0.f;
-    }
-    put_half(s.t[S_DF], r, hh, x);
-    put_half(s.t[S_DQ], r, hh, y1);
-    put_half(s.t[S_DK], r, hh, y2);
   }
   publish();
 
@@ -269,17 +288,17 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     mma64(tb + C3, ta(S_X), 0, ta(S_DK), 1, 0, 1);
     mma64(tb + C3, ta(S_Y1), 0, ta(S_DF), 1, 1, 1);
   });
-  wait_mma(45);
-  if (lead) {  // X and Y1 are consumed: Q and K come back into their slots
-    mbar_arrive_expect_tx(&s.bar_in, 2 * TILE);
-    tma_load_3d(s.t[S_Q2], &tm_q, 0, row0, bh, &s.bar_in);
-    tma_load_3d(s.t[S_K2], &tm_k, 0, row0, bh, &s.bar_in);
-  }
   {
     float x[32], a[32];
+    if (row_ok) load_f32_half(p.dvacc + (ws_row + i) * D + 32 * h, a);  // in flight during the MMAs
+    wait_mma(45);
+    if (lead) {  // X and Y1 are consumed: Q and K come back into their slots
+      mbar_arrive_expect_tx(&s.bar_in, 2 * TILE);
+      tma_load_3d(s.t[S_Q2], &tm_q, 0, row0, bh, &s.bar_in);
+      tma_load_3d(s.t[S_K2], &tm_k, 0, row0, bh, &s.bar_in);
+    }
     ld_half(tb, lane_off, C0, x);
     if (row_ok) {
-      load_f32_half(p.dvacc + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] += a[j];
       store_bf16_half(p.dv + (in_row + row0 + i) * D + 32 * h, x);
@@ -303,12 +322,12 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     mma64(tb + C2, ta(S_U), 1, ta(S_GX), 1, 0);
     mma64(tb + C3, ta(S_GM1), 1, ta(S_Q2), 1, 1);
   });
-  wait_mma(47);
   {
     float x[32], a[32];
+    if (row_ok) load_f32_half(p.dql + (ws_row + i) * D + 32 * h, a);
+    wait_mma(47);
     ld_half(tb, lane_off, C0, x);
     if (row_ok) {
-      load_f32_half(p.dql + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] += a[j];
       store_bf16_half(p.dq + (in_row + row0 + i) * D + 32 * h, x);
@@ -331,12 +350,12 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     mma64(tb + C3, ta(S_U), 1, ta(S_E3), 1, 1, 1);
     mma64(tb + C3, ta(S_GN2), 0, ta(S_K2), 1, 1);
   });
-  wait_mma(48);
   {
     float x[32], a[32];
+    if (row_ok) load_f32_half(p.dkr + (ws_row + i) * D + 32 * h, a);
+    wait_mma(48);
     ld_half(tb, lane_off, C0, x);
     if (row_ok) {
-      load_f32_half(p.dkr + (ws_row + i) * D + 32 * h, a);
 #pragma unroll
       for (int j = 0; j < 32; ++j) x[j] += a[j];
       store_bf16_half(p.dk + (in_row + row0 + i) * D + 32 * h, x);
@@ -366,10 +385,16 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     mma64(tb + C0, ta(S_GU), 0, ta(S_U), 0, 0);
     mma64(tb + C2, ta(S_W), 0, ta(S_W), 0, 0);
   });
-  if (tid < B) {
-    float acc = 0.f;
-    for (int r = tid; r < B; ++r) acc += scr[f32_idx(r, tid)];
-    s.gb[tid] = acc;
+  if (tid < B) {  // column sums; the rows above the diagonal hold exact zeros (gU and Y are lower)
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < B; r += 4) {
+      a0 += scr[f32_idx(r, tid)];
+      a1 += scr[f32_idx(r + 1, tid)];
+      a2 += scr[f32_idx(r + 2, tid)];
+      a3 += scr[f32_idx(r + 3, tid)];
+    }
+    s.gb[tid] = (a0 + a1) + (a2 + a3);
   }
   wait_mma(49);
   {
