@@ -120,36 +120,59 @@ __device__ __forceinline__ void load_f32_half(const float* src, float* x) {
   }
 }
 
-// Forward substitution for the UT transform, one column per thread: returns in y the column cc
-// of Y = (I + L)^{-1}, L = strictLower(diag(beta) G), i.e. row by row
+// Forward substitution for the UT transform, one column per thread of two warps: returns in y
+// the column cc of Y = (I + L)^{-1}, L = strictLower(diag(beta) G), i.e. row by row
 //   Y_rc = delta_rc - sum_{m<r} L_rm Y_mc,
 // with L the fp32 matrix at sl (f32_idx layout, strictly lower: entries with m >= r are zero).
 // Rows go in blocks of 16: the earlier blocks enter through 16 independent accumulations
 // (16-byte broadcast loads of L), the block itself is substituted row by row.  Everything is
-// unrolled so that y stays in registers.
+// unrolled so that y stays in registers.  B0 is the first row block that can be nonzero for
+// every column of the calling warp (Y is unit lower triangular: 0 for columns 0-31, 2 for
+// columns 32-63), so a warp skips the blocks above it.  The sums over the earlier blocks use
+// paired fp32 FMAs (even and odd m in the two lanes of a 64-bit register, added at the end).
+template <int B0>
 __device__ __forceinline__ void ut_solve_column(const float* sl, int cc, float (&y)[64]) {
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
+  for (int r = 0; r < 16 * B0; ++r) y[r] = 0.f;
+#pragma unroll
+  for (int b = B0; b < 4; ++b) {
     float acc[16];
+    if (b > B0) {
+      uint64_t s2[16];
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+      for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
 #pragma unroll
-    for (int m = 0; m < 16 * b; m += 4) {
+      for (int m = 16 * B0; m < 16 * b; m += 4) {
+        const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sl + f32_idx(16 * b + rr, m));
+          s2[rr] = f2_fma(lv.x, y01, s2[rr]);
+          s2[rr] = f2_fma(lv.y, y23, s2[rr]);
+        }
+      }
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
-        const float4 lv = *reinterpret_cast<const float4*>(sl + f32_idx(16 * b + rr, m));
-        acc[rr] = fmaf(lv.x, y[m], acc[rr]);
-        acc[rr] = fmaf(lv.y, y[m + 1], acc[rr]);
-        acc[rr] = fmaf(lv.z, y[m + 2], acc[rr]);
-        acc[rr] = fmaf(lv.w, y[m + 3], acc[rr]);
+        float lo, hi;
+        f2_split(s2[rr], lo, hi);
+        acc[rr] = lo + hi;
       }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
     }
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       const int r = 16 * b + rr;
       float a = acc[rr];
 #pragma unroll
-      for (int m = 16 * b; m < r; ++m) a = fmaf(sl[f32_idx(r, m)], y[m], a);
+      for (int m = 16 * b; m < r; m += 4) {
+        const float4 lv = *reinterpret_cast<const float4*>(sl + f32_idx(r, m));
+        a = fmaf(lv.x, y[m], a);
+        if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
+        if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
+        if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
+      }
       y[r] = (cc == r ? 1.f : 0.f) - a;
     }
   }

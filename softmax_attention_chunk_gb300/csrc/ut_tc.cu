@@ -165,11 +165,12 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
 
 
   // ---- P2: U = (I + strictLower(D G))^{-1} D = Y diag(beta): one column of Y per thread of
-  //      warps 0-1 ----
+  //      warps 0-1 (columns 32-63 are zero above row 32) ----
   if (warp < 2) {
     const int cc = 32 * warp + lane;
     float y[64];
-    ut_solve_column(sg, cc, y);
+    if (warp == 0) ut_solve_column<0>(sg, cc, y);
+    else ut_solve_column<2>(sg, cc, y);
     const float bc = s.beta[cc];
 #pragma unroll
     for (int r = 0; r < 64; ++r)
