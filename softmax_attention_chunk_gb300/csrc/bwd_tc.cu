@@ -229,6 +229,15 @@ __device__ __forceinline__ void store_box_row(uint8_t* box, int r, const uint32_
     *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = make_uint4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
 }
 __device__ __forceinline__ void grad_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+// 16 fp32 values as columns 16q .. 16q+15 of row r of a 128-byte swizzled fp32 box.
+__device__ __forceinline__ void store_box_quarter(uint8_t* box, int r, int q, const uint32_t* x) {
+  uint8_t* row = box + r * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(row + (((4 * q + j) ^ (r & 7)) * 16)) =
+        make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
 
 __device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const float* x) {
   uint8_t* row = tile + r * 128;
@@ -249,9 +258,9 @@ __device__ __forceinline__ void pack_row_pairs(const float* x, uint32_t (&pk)[32
 }
 
 // Warp roles: 0-3 and 11-14 softmax side (P, dS of a step; two threads per query row, column
-// halves 0-31 / 32-63), 4 TMA/bulk producer (lane 0: K->, F, V; lane 16: Z), 5 MMA issuer A (S,
-// dP, the G chain), 6-9 gradient side (G_n conversion, dQ<- output, dV/dK->/dF reductions),
-// 10 MMA issuer B ([dK->; dF], dV).  Two issuers because a tcgen05.mma costs tens of cycles to
+// halves 0-31 / 32-63; then the dV reductions of the previous step), 4 TMA/bulk producer (lane 0:
+// K->, F; lane 8: V; lane 16: Z), 5 MMA issuer A (S, dP, the G chain), 6-9 gradient side (G_n
+// conversion, dQ<- output, dK->/dF reductions), 10 MMA issuer B ([dK->; dF], dV).  Two issuers because a tcgen05.mma costs tens of cycles to
 // issue from one thread and these products are small (N = 64).
 constexpr int BS_THREADS = 480;
 constexpr int BS_NSOFT = 256;
@@ -298,8 +307,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     mbar_init(&s.gs_ready, 128);
     mbar_init(&s.acc_full, 1);     // issuer B's MMAs of the step complete
     mbar_init(&s.dkf_free, 128);   // the gradient side has read [dK->; dF] of the step
-    mbar_init(&s.dv_free[0], 128); // ... and dV, one barrier per dV buffer (a single one could
-    mbar_init(&s.dv_free[1], 128); // complete step k-1 before issuer B waits for step k-2)
+    mbar_init(&s.dv_free[0], BS_NSOFT);  // the softmax side has read dV, one barrier per dV buffer (a
+    mbar_init(&s.dv_free[1], BS_NSOFT);  // single one could complete step k-1 before issuer B waits for k-2)
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -447,11 +456,36 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
     const float lse2 = grow < p.L ? p.lse[(size_t)bh * p.L + grow] * kLog2e : INFINITY;
     const float Dr = p.Dv[wrow];
+    const int vrow = 16 * q4 + (lane & 15), vh = lane >> 4;  // dV (M=64): row, column half
+    // dV of step j (complete) -> columns 16h.. of the fp32 boxes 4, 5 -> two tensor reductions
+    // issued by thread 0 (its own bulk groups: each waits for the previous one to have read the
+    // boxes).  Runs after the step's P and dS are published, in the softmax side's slack.
+    auto stage_dv = [&](int j) {
+      const int crow = bh * p.Lp + step_chunk(has_partial, T, nsteps - 1 - j) * BK;
+      if (tid == 0) bulk_wait_read0();
+      soft_sync();
+      uint32_t a[16];
+      tmem_ld16x2_16(tb + lane_off + TM_DV + 64 * (j & 1) + 16 * h, a);
+      tmem_ld_wait();
+      store_box_quarter(s.stg[4 + vh], vrow, h, a);
+      tc_fence_before();
+      mbar_arrive(&s.dv_free[j & 1]);
+      fence_proxy_async_smem();
+      soft_sync();
+      if (tid == 0) {
+        tma_reduce_add_2d(&tm_rdv, s.stg[4], 0, crow);
+        tma_reduce_add_2d(&tm_rdv, s.stg[5], 32, crow);
+        bulk_commit();
+      }
+    };
+    // Every softmax thread runs every step (soft_sync needs all 256); after a timed-out wait
+    // (error recorded) the remaining waits are skipped.
+    bool ok = true;
     for (int k = 0; k < nsteps; ++k) {
       const int n = nsteps - 1 - k;
       const bool partial = has_partial && n == 0;
       const bool active = !(partial && r < 64);
-      if (!mbar_wait(&s.sp_full, k & 1, p.err, 25)) break;
+      ok = ok && mbar_wait(&s.sp_full, k & 1, p.err, 25);
       tc_fence_after();
       uint32_t sa[32], da[32];
       tmem_ld32(tb + lane_off + TM_S + 32 * h, sa);
@@ -471,8 +505,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(dsv[2 * j], dsv[2 * j + 1]);
       // the MMAs of step k-1 have read P, dS (shared memory) and dS (TMEM): the G chain and
       // [dK->; dF] (g_full), dV (acc_full)
-      if (k > 0 && (!mbar_wait(&s.g_full, (k - 1) & 1, p.err, 36) || !mbar_wait(&s.acc_full, (k - 1) & 1, p.err, 26)))
-        break;
+      if (k > 0) ok = ok && mbar_wait(&s.g_full, (k - 1) & 1, p.err, 36) && mbar_wait(&s.acc_full, (k - 1) & 1, p.err, 26);
+      tc_fence_after();
       put_half(s.ps, r, h, pv);
       put_half(s.ds, r, h, dsv);
       tmem_st16(tb + lane_off + TM_DSG + 16 * h, pk);
@@ -480,14 +514,18 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ps_ready);
+      if (k > 0) stage_dv(k - 1);
     }
+    ok = ok && mbar_wait(&s.acc_full, (nsteps - 1) & 1, p.err, 26);
+    tc_fence_after();
+    stage_dv(nsteps - 1);
+    if (tid == 0) bulk_wait0();
   } else if (warp >= 6) {
     // ---------------- gradient side: thread owns query row rg = 32 (warp % 4) + lane ----------------
     const int q4 = warp & 3;
     const int rg = 32 * q4 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + rg;
-    const int vrow = 16 * q4 + (lane & 15), vh = lane >> 4;  // dV (M=64) half row of this thread
     {  // dO into TMEM (A operand of dP); G_{nsteps} = 0 in shared memory and TMEM
       mbar_wait(&s.do_full, 0, p.err, 31);
       uint32_t buf[32];
@@ -554,11 +592,10 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         mbar_arrive(&s.gs_ready);
       }
       // [dK->; dF] of this step -> swizzled fp32 boxes 0-3 -> four tensor reductions (one bulk
-      // group); dV -> boxes 4, 5 -> two more (a second group).  Each staging waits only for the
-      // group of the previous step that read the same boxes.
+      // group, which the next step's staging waits to have read the boxes).
       const int crow = bh * p.Lp + c * BK;
       const int frow = (bh * p.nc + c) * D;
-      if (rg == 0) bulk_wait_read1();  // the previous step's [dK->; dF] group has read boxes 0-3
+      if (rg == 0) bulk_wait_read0();  // the previous step's [dK->; dF] group has read boxes 0-3
       grad_sync();
       {
         uint32_t a[32];
@@ -581,26 +618,6 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           tma_reduce_add_2d(&tm_rdf, s.stg[2], 0, frow);
           tma_reduce_add_2d(&tm_rdf, s.stg[3], 32, frow);
         }
-        bulk_commit();
-      }
-      // dV of this step (buffer k % 2)
-      ok = ok && mbar_wait(&s.acc_full, k & 1, p.err, 30);
-      tc_fence_after();
-      if (rg == 0) bulk_wait_read1();  // the previous step's dV group has read boxes 4, 5
-      grad_sync();
-      {
-        uint32_t a[32];
-        tmem_ld16x2(tb + lane_off + TM_DV + 64 * (k & 1), a);
-        tmem_ld_wait();
-        store_box_row(s.stg[4 + vh], vrow, a);
-      }
-      tc_fence_before();
-      mbar_arrive(&s.dv_free[k & 1]);
-      fence_proxy_async_smem();
-      grad_sync();
-      if (rg == 0) {
-        tma_reduce_add_2d(&tm_rdv, s.stg[4], 0, crow);
-        tma_reduce_add_2d(&tm_rdv, s.stg[5], 32, crow);
         bulk_commit();
       }
     }
