@@ -29,8 +29,8 @@ def check(got, ref, tol, name, rel=None):
     got = np64(got).reshape(ref.shape)
     err = np.abs(got - ref).max()
     assert err <= tol, f"{name}: max abs err {err:.3e} > {tol:.1e}"
-    if rel is not None:
-        r = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    if rel is not None and np.linalg.norm(ref) > 0:  # a zero reference leaves the max-abs bound
+        r = np.linalg.norm(got - ref) / np.linalg.norm(ref)
         assert r <= rel, f"{name}: rel fro err {r:.3e} > {rel:.1e}"
     return err
 
@@ -142,6 +142,31 @@ def test_bwd_bf16(cuda_lib):
     check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
 
 
+@pytest.mark.parametrize("L", [1, 40, 64, 65, 128, 129, 192, 257])
+def test_bwd_bf16_ragged(cuda_lib, L):
+    """bf16 tensor-core backward at lengths giving a lone partial chunk (1, 40), exact chunk and
+    query-tile multiples (64, 128, 192), a tile whose only step is the partial one (65) and
+    ragged tails after full tiles (129, 257)."""
+    inp = gen_path_inputs(1, 3, L, 64, "bf16", seed=300 + L, with_dO=True, near2_frac=0.05)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
+
+
+def test_bwd_bf16_more_heads_than_a_schedule_group(cuda_lib):
+    """18 heads: the tile schedule takes heads 16 at a time, so the second group is partial."""
+    inp = gen_path_inputs(2, 9, 200, 64, "bf16", seed=77, with_dO=True, near2_frac=0.05)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
+
+
+def test_fwd_bf16_more_heads_than_a_schedule_group(cuda_lib):
+    inp = gen_path_inputs(2, 9, 200, 64, "bf16", seed=78, near2_frac=0.05)
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(flat(o), o_ref, 2e-2, "o", rel=2e-2)
+    check(flat(lse), lse_ref, 2e-2, "lse")
+
+
 def test_bwd_rejects_forget_gate(cuda_lib):
     from softmax_attention_chunk_gb300 import path_attn as pa
 
@@ -211,7 +236,7 @@ def test_bwd_reusing_forward_preparation(cuda_lib):
     check_grads(inp, g_reuse, 1.0, 2e-2, rel=3e-2)
 
 
-@pytest.mark.parametrize("L", [333, 1000])
+@pytest.mark.parametrize("L", [65, 129, 333, 1000])
 def test_training_step_with_stored_transported_queries(cuda_lib, L):
     """PATH_FWD_STORE_Z + PATH_BWD_Z_FROM_FWD: the forward stores every transported query tile, the
     backward skips recomputing them; gradients equal the plain backward's (the tiles are the same
