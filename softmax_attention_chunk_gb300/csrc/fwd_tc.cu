@@ -49,13 +49,14 @@ constexpr uint32_t COL_S = 0, COL_ZP = 64, COL_O = 128, COL_P = 192, COL_Z = 224
 constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
 
 struct __align__(1024) ScanSmem {
-  uint8_t z0[BQ * 128];               // Q<- tile (bf16, 128-byte swizzled rows): the first Z
+  uint8_t z0[BQ * 128];               // Q<- tile (bf16, 128-byte swizzled rows): the first Z; after
+                                      // step 0 the image buffer of the even Z tiles
   uint8_t kf[NSTAGE][128 * 128];      // rows 0-63: K->_c, rows 64-127: F_c
   uint8_t v[NSTAGE][BK * 128];        // V_c
-  uint8_t zout[BQ * 128];             // Z_{n+1} (swizzled image) on its way to the Z store
+  uint8_t zout[BQ * 128];             // image buffer of the odd Z tiles on their way to the Z store
   float xm[2][BQ];                    // per-half row maxima / sums exchanged between the halves
   uint64_t full[NSTAGE], empty[NSTAGE];
-  uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done, zbuf_free;
+  uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done, zbuf_free[2];
   uint32_t tmem_base;
 };
 
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     mbar_init(&s.p_ready, NSOFT);
     mbar_init(&s.pv_done, 1);
     mbar_init(&s.o_done, 1);
-    mbar_init(&s.zbuf_free, 1);
+    mbar_init(&s.zbuf_free[0], 1);
+    mbar_init(&s.zbuf_free[1], 1);
     fence_barrier_init();
   }
   if (warp == 9) tmem_alloc(&s.tmem_base, TMEM_COLS);
@@ -192,17 +194,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         if (!mbar_wait(&s.full[st], (n / NSTAGE) & 1, p.err, 3)) { ok = false; break; }
         if (!mbar_wait(&s.z_ready, n & 1, p.err, 4)) { ok = false; break; }
         tc_fence_after();
-        if (zstore) {  // Z_n (Z_0 straight from the Q<- tile)
-          bulk_store(zstore + (size_t)n * (BQ * 128), n == 0 ? s.z0 : s.zout, BQ * 128);
+        if (zstore) {  // Z_n from image buffer n % 2 (Z_0 is the Q<- tile itself)
+          bulk_store(zstore + (size_t)n * (BQ * 128), (n & 1) ? s.zout : s.z0, BQ * 128);
           bulk_commit();
         }
         const uint64_t d0 = dkf0 + (uint64_t)(1024 * st);
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_ts(tb + COL_S, tb + COL_Z + 8 * k, d0 + (uint64_t)(2 * k), idesc_sz, k > 0 ? 1u : 0u);
         mma_commit(&s.s_full);
-        if (zstore && n >= 1) {  // the store buffer may take Z_{n+1}
-          bulk_wait_read0();
-          mbar_arrive(&s.zbuf_free);
+        if (zstore && n >= 1) {  // the copy of Z_{n-1} has read its buffer, which may take Z_{n+1}
+          bulk_wait_read1();
+          mbar_arrive(&s.zbuf_free[(n - 1) & 1]);
         }
         if (n > 0) {
           if (!mbar_wait(&s.p_ready, (n - 1) & 1, p.err, 5)) { ok = false; break; }
@@ -268,9 +270,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int j = 0; j < 16; ++j) z16[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
         tmem_st16(c_z, z16);
-        if (p.zs) {  // Z_{n+1} into the store buffer once the bulk copy of Z_n has read it
-          if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free, (n - 1) & 1, p.err, 10);
-          put_tile_quarter(s.zout, r, h, z16);
+        if (p.zs) {  // Z_{n+1} into image buffer (n+1) % 2 once the bulk copy of Z_{n-1} has read it
+          if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free[(n + 1) & 1], ((n - 1) >> 1) & 1, p.err, 10);
+          put_tile_quarter((n & 1) ? s.z0 : s.zout, r, h, z16);
           fence_proxy_async_smem();
         }
       } else if (n + 1 < nsteps && p.zs) {  // rows not transported at the partial step keep Z_0
@@ -284,8 +286,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           z16[4 * q + 2] = v.z;
           z16[4 * q + 3] = v.w;
         }
-        if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free, (n - 1) & 1, p.err, 10);
-        put_tile_quarter(s.zout, r, h, z16);
+        if (n >= 1) ok = ok && mbar_wait(&s.zbuf_free[(n + 1) & 1], ((n - 1) >> 1) & 1, p.err, 10);
+        put_tile_quarter((n & 1) ? s.z0 : s.zout, r, h, z16);
         fence_proxy_async_smem();
       }
       tmem_ld32(c_s, x);
