@@ -21,22 +21,65 @@ constexpr int NT = 256;
 constexpr int D = kHeadDim;
 constexpr int DS = D + 1;
 
-// D_i = dO_i . o_i (one warp per row); padded rows get 0.
+// D_i = dO_i . o_i; padded rows get 0.  A row is read by a group of D / VEC lanes with 16-byte
+// loads (VEC elements each), a warp covers DOT_PASSES row groups with all loads issued before the
+// products, so that every thread keeps DOT_PASSES * 32 bytes in flight (the kernel is bound by
+// HBM reads of o and dO).
+constexpr int DOT_PASSES = 2;
+template <typename T>
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b) {
+  if constexpr (std::is_same<T, float>::value) {
+    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+  } else {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 u = __bfloat1622float2(x[j]), v = __bfloat1622float2(y[j]);
+      acc = fmaf(u.x, v.x, acc);
+      acc = fmaf(u.y, v.y, acc);
+    }
+    return acc;
+  }
+}
 template <typename T>
 __global__ void __launch_bounds__(NT) bwd_dot_kernel(Geom g, const T* __restrict__ o,
                                                      const T* __restrict__ dO, float* __restrict__ Dv) {
+  constexpr int VEC = 16 / (int)sizeof(T);
+  constexpr int LPR = D / VEC;   // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp and pass
   const long warp = ((long)blockIdx.x * NT + threadIdx.x) / 32;
-  const int lane = threadIdx.x % 32;
+  const int lane = threadIdx.x % 32, sub = lane / LPR, l = lane % LPR;
   const long rows = (long)g.BH * g.Lp;
-  if (warp >= rows) return;
-  const int bh = (int)(warp / g.Lp), i = (int)(warp % g.Lp);
-  float acc = 0.f;
-  if (i < g.L) {
-    const size_t off = ((size_t)bh * g.L + i) * D;
-    acc = to_f(o[off + lane]) * to_f(dO[off + lane]) + to_f(o[off + lane + 32]) * to_f(dO[off + lane + 32]);
+  const long row0 = warp * (RPW * DOT_PASSES) + sub;
+  uint4 a[DOT_PASSES], b[DOT_PASSES];
+  bool ok[DOT_PASSES];
+#pragma unroll
+  for (int k = 0; k < DOT_PASSES; ++k) {
+    const long row = row0 + (long)k * RPW;
+    const int bh = (int)(row / g.Lp), i = (int)(row % g.Lp);
+    ok[k] = row < rows && i < g.L;
+    a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (ok[k]) {
+      const size_t off = ((size_t)bh * g.L + i) * D + (size_t)l * VEC;
+      a[k] = __ldg(reinterpret_cast<const uint4*>(o + off));
+      b[k] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+    }
   }
-  acc = group_sum<32>(acc);
-  if (lane == 0) Dv[warp] = acc;
+#pragma unroll
+  for (int k = 0; k < DOT_PASSES; ++k) {
+    const long row = row0 + (long)k * RPW;
+    const float acc = group_sum<LPR>(ok[k] ? dot16<T>(a[k], b[k]) : 0.f);
+    if (l == 0 && row < rows) Dv[row] = acc;
+  }
+}
+template <typename T>
+unsigned dot_blocks(const Geom& g) {
+  constexpr int rows_per_block = (NT / 32) * (32 / (D / (16 / (int)sizeof(T)))) * DOT_PASSES;
+  const long rows = (long)g.BH * g.Lp;
+  return (unsigned)((rows + rows_per_block - 1) / rows_per_block);
 }
 
 template <int B>
@@ -420,9 +463,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
   if ((e = cudaMemsetAsync(ws + lay.dkr, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.df, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
-  const long nwarps = (long)rows;
-  bwd_dot_kernel<T><<<(unsigned)((nwarps * 32 + NT - 1) / NT), NT, 0, st>>>(
-      g, (const T*)o, (const T*)dO, (float*)(ws + lay.Dv));
+  bwd_dot_kernel<T><<<dot_blocks<T>(g), NT, 0, st>>>(g, (const T*)o, (const T*)dO, (float*)(ws + lay.Dv));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prep_simt(std::is_same<T, __nv_bfloat16>::value, g, q, k, v, w, beta, nullptr, ws,
                             lay.fw, false, st)) != cudaSuccess)
@@ -454,8 +495,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
 }  // namespace
 
 cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* Dv, cudaStream_t st) {
-  const long nwarps = (long)g.BH * g.Lp;
-  bwd_dot_kernel<__nv_bfloat16><<<(unsigned)((nwarps * 32 + NT - 1) / NT), NT, 0, st>>>(
+  bwd_dot_kernel<__nv_bfloat16><<<dot_blocks<__nv_bfloat16>(g), NT, 0, st>>>(
       g, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, Dv);
   return cudaGetLastError();
 }
