@@ -47,8 +47,9 @@ def lib():
         _lib.oracle_logits.argtypes = [i, i, _P, _P, _P, _P, _P, d, _P]
         _lib.oracle_bwd_head.argtypes = [i, i, _P, _P, _P, _P, _P, _P, d, _P, _P, _P, _P, _P, _P, _P]
         _lib.oracle_decode_step.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P, _P, d, _P, _P]
+        _lib.oracle_prefill_cache.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P]
         for f in ("oracle_fwd_head_rows", "oracle_fwd", "oracle_logits", "oracle_bwd_head",
-                  "oracle_decode_step"):
+                  "oracle_decode_step", "oracle_prefill_cache"):
             getattr(_lib, f).restype = i
     return _lib
 
@@ -138,3 +139,15 @@ def decode_step(k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, scale=1.0, want
                                     _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), float(scale),
                                     _ptr(o), _ptr(lse)))
     return (o, lse) if want_lse else o
+
+
+def prefill_cache(k, v, w, beta, cap):
+    """Prefill -> decode hand-off: fp64 caches [n,cap,d] holding the L prompt tokens after the
+    decode rewrite of every prompt position (row j = H_{L-1}...H_{j+1} k_j, rows >= L zero)."""
+    k, v, w, beta = map(_f64, (k, v, w, beta))
+    n, L, d = k.shape
+    kc = np.zeros((n, cap, d))
+    vc = np.zeros((n, cap, d))
+    _check(lib().oracle_prefill_cache(n, d, int(cap), L, _ptr(kc), _ptr(vc), _ptr(k), _ptr(v),
+                                      _ptr(w), _ptr(beta)))
+    return kc, vc

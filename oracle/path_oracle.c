@@ -25,7 +25,8 @@
  *
  * Backward (absent from the pages): exact reverse-mode derivative of the same walk, per row.
  * Decode: the in-place key rewrite of the notes' §2.8 (Eq. (1)) followed by a plain
- * single-query softmax.
+ * single-query softmax.  Prefill hand-off: the same rewrite applied to the prompt tokens in
+ * order, so that every prompt key ends up transported to the prompt end (§2.8, last paragraph).
  *
  * Parallelism: OpenMP over independent query rows (and heads); no reduction order depends on
  * the thread count except the final sum of per-thread gradient buffers in oracle_bwd.
@@ -287,4 +288,32 @@ int oracle_decode_step(int nheads, int d, int cap, int t, double* kc, double* vc
     free(s); free(p);
   }
   return bad ? -1 : 0;
+}
+
+/* Prefill -> decode hand-off for nheads heads (reading notes §2.8, last paragraph: after a
+ * prefill every key is aligned to the prompt end).  The decode rewrite applied to the L prompt
+ * tokens in order: for t = 0..L-1, k_j <- k_j - beta_t (w_t . k_j) w_t for every j < t, then
+ * row t <- (k_t, v_t).  On return row j of kc holds H_{L-1} ... H_{j+1} k_j.
+ * kc, vc: caches [nheads][cap][d] (rows 0..L-1 written, the rest untouched);
+ * k, v, w: [nheads][L][d]; beta: [nheads][L] (clamped to [0, 2] like everywhere else). */
+int oracle_prefill_cache(int nheads, int d, int cap, int L, double* kc, double* vc,
+                         const double* k, const double* v, const double* w, const double* beta) {
+  if (L < 0 || L > cap) return -2;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int h = 0; h < nheads; ++h) {
+    double* K = kc + (size_t)h * cap * d;
+    double* V = vc + (size_t)h * cap * d;
+    for (int t = 0; t < L; ++t) {
+      const double* wt = w + ((size_t)h * L + t) * d;
+      const double b = clamp_beta(beta[(size_t)h * L + t]);
+      for (int j = 0; j < t; ++j) {
+        double* kj = K + (size_t)j * d;
+        const double a = dot(wt, kj, d);
+        for (int n = 0; n < d; ++n) kj[n] -= b * a * wt[n];
+      }
+      memcpy(K + (size_t)t * d, k + ((size_t)h * L + t) * d, sizeof(double) * d);
+      memcpy(V + (size_t)t * d, v + ((size_t)h * L + t) * d, sizeof(double) * d);
+    }
+  }
+  return 0;
 }

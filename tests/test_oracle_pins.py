@@ -410,3 +410,50 @@ def test_fwd_rows_subset_matches_full():
     o_r, lse_r = orc.fwd_rows(q, k, v, w, beta, logf, 1.0, rows)
     np.testing.assert_array_equal(o_r, o[0, rows])
     np.testing.assert_array_equal(lse_r, lse[0, rows])
+
+
+# ---------------- prefill -> decode hand-off (notes §2.8, last paragraph) ----------------
+
+def test_prefill_cache_rows_are_explicit_suffix_products():
+    """Row j of the handed-off cache is H_{L-1} @ ... @ H_{j+1} k_j, formed as d x d matrices."""
+    rng = np.random.default_rng(41)
+    n, L, d = 2, 7, 5
+    probs = [rand_problem(rng, L, d) for _ in range(n)]
+    k = np.stack([p[1] for p in probs]); v = np.stack([p[2] for p in probs])
+    w = np.stack([p[3] for p in probs]); beta = np.stack([p[4] for p in probs])
+    kc, vc = orc.prefill_cache(k, v, w, beta, cap=L + 3)
+    for h in range(n):
+        for j in range(L):
+            M = np.eye(d)
+            for t in range(j + 1, L):  # H_t multiplies from the left: H_{L-1} ... H_{j+1}
+                M = (np.eye(d) - beta[h, t] * np.outer(w[h, t], w[h, t])) @ M
+            np.testing.assert_allclose(kc[h, j], M @ k[h, j], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(vc[h, :L], v[h])
+        assert not kc[h, L:].any() and not vc[h, L:].any()
+
+
+def test_prefill_then_decode_step_gives_the_forward_row():
+    """Hand off a prompt of L tokens, decode token L: o_L equals row L of the forward over L+1
+    tokens (the forward oracle evaluates the path logits directly)."""
+    rng = np.random.default_rng(42)
+    L, d = 23, 8
+    q, k, v, w, beta, _ = rand_problem(rng, L + 1, d)
+    kc, vc = orc.prefill_cache(k[None, :L], v[None, :L], w[None, :L], beta[None, :L], cap=L + 1)
+    o_dec = orc.decode_step(kc, vc, L, q[None, L], k[None, L], v[None, L], w[None, L], beta[None, L], scale=0.7)
+    o_fwd, _ = orc.fwd(q[None], k[None], v[None], w[None], beta[None], None, 0.7)
+    np.testing.assert_allclose(o_dec[0], o_fwd[0, L], rtol=0, atol=1e-12)
+
+
+def test_prefill_special_cases():
+    """beta = 0 leaves the keys as given; beta = 2 with w = e_0 reflects coordinate 0 once per
+    later token: row j gets (-1)^(L-1-j) on that coordinate and nothing else changes."""
+    rng = np.random.default_rng(43)
+    L, d = 9, 4
+    k = rng.standard_normal((1, L, d)); v = rng.standard_normal((1, L, d))
+    w = np.zeros((1, L, d)); w[..., 0] = 1.0
+    kc, _ = orc.prefill_cache(k, v, w, np.zeros((1, L)), cap=L)
+    np.testing.assert_array_equal(kc[0], k[0])
+    kc, _ = orc.prefill_cache(k, v, w, np.full((1, L), 2.0), cap=L)
+    sign = np.array([(-1.0) ** (L - 1 - j) for j in range(L)])
+    np.testing.assert_allclose(kc[0, :, 0], sign * k[0, :, 0], rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(kc[0, :, 1:], k[0, :, 1:])
