@@ -48,8 +48,9 @@ def lib():
         _lib.oracle_bwd_head.argtypes = [i, i, _P, _P, _P, _P, _P, _P, d, _P, _P, _P, _P, _P, _P, _P]
         _lib.oracle_decode_step.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P, _P, d, _P, _P]
         _lib.oracle_prefill_cache.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P]
+        _lib.oracle_transport_keys.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_int), _P, _P, _P, _P]
         for f in ("oracle_fwd_head_rows", "oracle_fwd", "oracle_logits", "oracle_bwd_head",
-                  "oracle_decode_step", "oracle_prefill_cache"):
+                  "oracle_decode_step", "oracle_prefill_cache", "oracle_transport_keys"):
             getattr(_lib, f).restype = i
     return _lib
 
@@ -151,3 +152,15 @@ def prefill_cache(k, v, w, beta, cap):
     _check(lib().oracle_prefill_cache(n, d, int(cap), L, _ptr(kc), _ptr(vc), _ptr(k), _ptr(v),
                                       _ptr(w), _ptr(beta)))
     return kc, vc
+
+
+def transport_keys(k, w, beta, rows):
+    """Rows of the prefill hand-off one key at a time: [n, len(rows), d] with entry (h, r) equal
+    to H_{L-1}...H_{j+1} k_j of head h, j = rows[r] (O((L - j) d) per row)."""
+    k, w, beta = map(_f64, (k, w, beta))
+    n, L, d = k.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    out = np.zeros((n, len(rows), d))
+    _check(lib().oracle_transport_keys(n, d, L, len(rows), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                       _ptr(k), _ptr(w), _ptr(beta), _ptr(out)))
+    return out

@@ -317,3 +317,27 @@ int oracle_prefill_cache(int nheads, int d, int cap, int L, double* kc, double* 
   }
   return 0;
 }
+
+/* Selected rows of the prefill hand-off, one key at a time (same rewrite as above, restricted to
+ * the keys asked for): out[h][r] = H_{L-1} ... H_{j+1} k_j with j = rows[r], for every head h.
+ * k, w: [nheads][L][d]; beta: [nheads][L]; rows: nrows indices in [0, L); out: [nheads][nrows][d]. */
+int oracle_transport_keys(int nheads, int d, int L, int nrows, const int* rows, const double* k,
+                          const double* w, const double* beta, double* out) {
+  for (int r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= L) return -2;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int h = 0; h < nheads; ++h) {
+    for (int r = 0; r < nrows; ++r) {
+      const int j = rows[r];
+      double* o = out + ((size_t)h * nrows + r) * d;
+      memcpy(o, k + ((size_t)h * L + j) * d, sizeof(double) * d);
+      for (int t = j + 1; t < L; ++t) {
+        const double* wt = w + ((size_t)h * L + t) * d;
+        const double b = clamp_beta(beta[(size_t)h * L + t]);
+        const double a = dot(wt, o, d);
+        for (int n = 0; n < d; ++n) o[n] -= b * a * wt[n];
+      }
+    }
+  }
+  return 0;
+}

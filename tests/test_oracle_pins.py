@@ -457,3 +457,15 @@ def test_prefill_special_cases():
     sign = np.array([(-1.0) ** (L - 1 - j) for j in range(L)])
     np.testing.assert_allclose(kc[0, :, 0], sign * k[0, :, 0], rtol=0, atol=1e-15)
     np.testing.assert_array_equal(kc[0, :, 1:], k[0, :, 1:])
+
+
+def test_transport_keys_are_the_prefill_rows():
+    """The row-at-a-time hand-off (used on full-size prompts) equals the prefill cache rows."""
+    rng = np.random.default_rng(44)
+    n, L, d = 3, 40, 6
+    probs = [rand_problem(rng, L, d) for _ in range(n)]
+    k = np.stack([p[1] for p in probs]); v = np.stack([p[2] for p in probs])
+    w = np.stack([p[3] for p in probs]); beta = np.stack([p[4] for p in probs])
+    kc, _ = orc.prefill_cache(k, v, w, beta, cap=L)
+    rows = [0, 1, 17, 38, 39]
+    np.testing.assert_allclose(orc.transport_keys(k, w, beta, rows), kc[:, rows], rtol=0, atol=1e-13)
