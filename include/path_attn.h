@@ -200,6 +200,29 @@ int path_decode_step(const path_decode_desc_t* desc, void* k_cache, void* v_cach
  *    stream are safe.  Nothing in the array needs to start at zero: each call overwrites the
  *    parts it reads.
  */
+/* Bytes of workspace path_decode_prefill needs for a prompt of prompt_len tokens (the fp32
+ * chunk transforms of the prompt); 0 if the descriptor or prompt_len is invalid. Host only. */
+size_t path_decode_prefill_workspace_size(const path_decode_desc_t* desc, int prompt_len);
+
+/*
+ * Prefill -> decode hand-off (notes §2.8, last paragraph: after a prefill every key must be
+ * aligned to the prompt end, by the block suffix products).  Fills rows 0..prompt_len-1 of each
+ * cache so that path_decode_step can continue at t = prompt_len:
+ *   k_cache row j = H_{L-1} ... H_{j+1} k_j   (H_t = I - beta_t w_t w_t^T, L = prompt_len),
+ *   v_cache row j = v_j,
+ * i.e. exactly what prompt_len calls of path_decode_step from an empty cache would leave there.
+ * Computed blockwise in fp32 (64-row chunks: each key moved to its chunk's end, then through the
+ * later chunks' transforms right to left) and rounded once to cache_dtype.
+ * k, v, w: [batch][heads][prompt_len][head_dim] in cache_dtype; beta: [batch][heads][prompt_len]
+ * float32 (clamped to [0, 2]).  Caches: [batch][heads][capacity][head_dim]; rows >= prompt_len
+ * are not touched.  Requires 0 <= prompt_len <= capacity (else PATH_ERR_CAPACITY); prompt_len = 0
+ * does nothing.  ws: at least path_decode_prefill_workspace_size(desc, prompt_len) bytes,
+ * 256-byte aligned.  Asynchronous on stream.
+ */
+int path_decode_prefill(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int prompt_len,
+                        const void* k, const void* v, const void* w, const float* beta, void* ws,
+                        size_t ws_bytes, void* stream);
+
 #define PATH_DECODE_NOALLOC_MAX_HEADS 496
 int path_decode_step_noalloc(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int t,
                              const void* q_t, const void* k_t, const void* v_t, const void* w_t,

@@ -211,4 +211,48 @@ PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* 
                                    (cudaStream_t)stream));
 }
 
+// Geometry of the prompt of a prefill hand-off: 64-row chunks over prompt_len rows.
+static Geom prefill_geom(const path_decode_desc_t* d, int prompt_len) {
+  Geom g;
+  g.BH = d->batch * d->heads;
+  g.L = prompt_len;
+  g.B = 64;
+  g.nc = (prompt_len + 63) / 64;
+  g.Lp = g.nc * 64;
+  g.scale = d->scale;
+  return g;
+}
+
+static int check_decode_desc(const path_decode_desc_t* d) {
+  if (!d) return PATH_ERR_INVALID_ARG;
+  if (d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
+  if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
+  if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
+  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  if ((long long)d->batch * d->heads > 65535) return PATH_ERR_UNSUPPORTED;
+  return PATH_OK;
+}
+
+PATH_API size_t path_decode_prefill_workspace_size(const path_decode_desc_t* d, int prompt_len) {
+  if (check_decode_desc(d) != PATH_OK || prompt_len < 0 || prompt_len > d->capacity) return 0;
+  return fwd_ws_layout(prefill_geom(d, prompt_len), 4).total;
+}
+
+PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, void* v_cache, int prompt_len,
+                                 const void* k, const void* v, const void* w, const float* beta, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  int rc = check_decode_desc(d);
+  if (rc != PATH_OK) return rc;
+  if (prompt_len < 0) return PATH_ERR_INVALID_ARG;
+  if (prompt_len > d->capacity) return PATH_ERR_CAPACITY;
+  CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta);
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  const Geom g = prefill_geom(d, prompt_len);
+  const FwdWs lay = fwd_ws_layout(g, 4);
+  if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+  if (prompt_len == 0) return PATH_OK;
+  return cuda_status(launch_prefill(d->cache_dtype == PATH_BF16, g, d->capacity, k, v, w, beta, k_cache,
+                                    v_cache, (char*)ws, lay, (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -151,6 +151,13 @@ cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const v
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
+// Prefill -> decode hand-off: rows 0..g.L-1 of the caches ([g.BH][cap][64]) get the prompt keys
+// transported to the prompt end and the prompt values; g.B must be 64; ws holds the fp32
+// forward layout lay = fwd_ws_layout(g, 4).
+cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
+                           const float* beta, void* k_cache, void* v_cache, char* ws, const FwdWs& lay,
+                           cudaStream_t st);
+
 // tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
 // tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,

@@ -61,6 +61,10 @@ _lib.path_decode_step.restype = _i
 _lib.path_decode_step.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
 _lib.path_decode_step_noalloc.restype = _i
 _lib.path_decode_step_noalloc.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp]
+_lib.path_decode_prefill_workspace_size.restype = _sz
+_lib.path_decode_prefill_workspace_size.argtypes = [_DDP, _i]
+_lib.path_decode_prefill.restype = _i
+_lib.path_decode_prefill.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 4 + [_vp, _sz, _vp]
 PATH_DECODE_NOALLOC_MAX_HEADS = 496
 
 PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
@@ -71,7 +75,8 @@ PATH_BWD_Z_FROM_FWD = 16
 
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
-            "path_decode_step", "path_decode_step_noalloc")
+            "path_decode_step", "path_decode_step_noalloc", "path_decode_prefill_workspace_size",
+            "path_decode_prefill")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -121,6 +126,15 @@ def path_decode_step(desc, k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, o_t,
 def path_decode_step_noalloc(desc, k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, o_t, stream) -> int:
     return _lib.path_decode_step_noalloc(ctypes.byref(desc), k_cache, v_cache, int(t), q_t, k_t, v_t, w_t,
                                          beta_t, o_t, stream)
+
+
+def path_decode_prefill_workspace_size(desc: path_decode_desc_t, prompt_len: int) -> int:
+    return _lib.path_decode_prefill_workspace_size(ctypes.byref(desc), int(prompt_len))
+
+
+def path_decode_prefill(desc, k_cache, v_cache, prompt_len, k, v, w, beta, ws, ws_bytes, stream) -> int:
+    return _lib.path_decode_prefill(ctypes.byref(desc), k_cache, v_cache, int(prompt_len), k, v, w, beta, ws,
+                                    ws_bytes, stream)
 
 
 # ---------------- torch-tensor wrappers ----------------
@@ -227,3 +241,24 @@ def decode_step(k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, scale=1.0, ws=N
                           _p(o), _p(ws), ws.numel(), _stream())
     _check(rc, "path_decode_step")
     return o
+
+
+def decode_prefill(k_cache, v_cache, k, v, w, beta, ws=None):
+    """Prefill -> decode hand-off: rows 0..L-1 of the caches [B,H,cap,d] get the prompt keys
+    k,v,w [B,H,L,d] (cache dtype), beta [B,H,L] fp32 transported to the prompt end; decoding then
+    continues at t = L."""
+    desc = make_decode_desc(k_cache, 1.0)
+    B, H, cap, d = k_cache.shape
+    L = k.shape[2]
+    _need(v_cache, k_cache.dtype, k_cache.shape, "v_cache")
+    for name, x in (("k", k), ("v", v), ("w", w)):
+        _need(x, k_cache.dtype, (B, H, L, d), name)
+    _need(beta, torch.float32, (B, H, L), "beta")
+    n = path_decode_prefill_workspace_size(desc, L)
+    if n == 0:
+        raise RuntimeError("invalid decode descriptor or prompt length")
+    if ws is None:
+        ws = torch.empty(n, dtype=torch.uint8, device=k_cache.device)
+    rc = path_decode_prefill(desc, _p(k_cache), _p(v_cache), L, _p(k), _p(v), _p(w), _p(beta), _p(ws), ws.numel(),
+                             _stream())
+    _check(rc, "path_decode_prefill")

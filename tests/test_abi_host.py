@@ -133,6 +133,26 @@ def test_decode_argument_errors(pa):
     assert pa.path_decode_step(bad, FAKE, FAKE, 5, *vec, FAKE, n, None) == 2
 
 
+def test_prefill_argument_errors(pa):
+    """Prefill hand-off: every check runs before any CUDA call (FAKE pointers are never used)."""
+    dd = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_BF16, 1.0)
+    n = pa.path_decode_prefill_workspace_size(dd, 70)
+    assert n > 0 and n > pa.path_decode_prefill_workspace_size(dd, 10) > 0
+    assert pa.path_decode_prefill_workspace_size(dd, 0) > 0            # an empty prompt is valid
+    assert pa.path_decode_prefill_workspace_size(dd, 101) == 0         # longer than the cache
+    assert pa.path_decode_prefill_workspace_size(dd, -1) == 0
+    vec = [FAKE] * 4
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 101, *vec, FAKE, n, None) == 4   # prompt > capacity
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, -1, *vec, FAKE, n, None) == 1
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec, FAKE, n - 1, None) == 3
+    assert pa.path_decode_prefill(dd, None, FAKE, 70, *vec, FAKE, n, None) == 1
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, FAKE, FAKE, FAKE, None, FAKE, n, None) == 1
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 0, *vec, FAKE, n, None) == 0     # nothing to do
+    bad = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
+    assert pa.path_decode_prefill_workspace_size(bad, 10) == 0
+    assert pa.path_decode_prefill(bad, FAKE, FAKE, 10, *vec, FAKE, n, None) == 2
+
+
 def test_torch_wrapper_rejects_bad_tensors(pa):
     q = torch.zeros(1, 1, 8, 64)
     with pytest.raises(ValueError):

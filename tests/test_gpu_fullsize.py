@@ -139,3 +139,26 @@ def test_decode_full_size_sampled_heads(cuda_lib):
     n = t0 + steps
     kg = np64(kc.reshape(B * H, -1, d)[heads, :n])
     assert np.abs(kg - kref[:, :n]).max() <= 2e-2
+
+
+def test_prefill_full_length_sampled_rows(cuda_lib):
+    """Hand-off of a prompt as long as the decode workload's cache (32768 tokens, bf16): sampled
+    rows of every head against the oracle's one-key-at-a-time transport."""
+    cfg = CONFIGS["decode_b32h32_t32768"]
+    L = cfg["t0"]
+    inp = gen_path_inputs(1, 4, L, cfg["head_dim"], "bf16", seed=cfg["seed"] + 5, near2_frac=0.05)
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    cap = L + 16
+    kc = torch.zeros(1, 4, cap, cfg["head_dim"], dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    t = {n: inp[n].to(DEV) for n in ("k", "v", "w", "beta")}
+    pa.decode_prefill(kc, vc, t["k"], t["v"], t["w"], t["beta"])
+    torch.cuda.synchronize()
+    rows = sample_rows(L, np.random.default_rng(9))
+    ref = orc.transport_keys(inp["k"].reshape(4, L, -1), inp["w"].reshape(4, L, -1), inp["beta"].reshape(4, L), rows)
+    got = np64(kc.reshape(4, cap, -1)[:, rows])
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= 2e-2 * np.abs(ref).max() and rel <= 2e-2, (err, rel)
+    assert torch.equal(vc[:, :, :L], t["v"])

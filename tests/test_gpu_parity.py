@@ -259,3 +259,57 @@ def test_training_step_with_stored_transported_queries(cuda_lib, L):
         a, b = g_plain[key].float(), g[key].float()
         assert (a - b).abs().max().item() <= 1e-2 * max(1.0, a.abs().max().item()), key
     check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
+
+
+# ---------------- prefill -> decode hand-off ----------------
+
+def run_prefill(inp, dtype, cap, fill=7.0):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    B, H, L, d = inp["k"].shape
+    kc = torch.full((B, H, cap, d), fill, dtype=tdt, device=DEV)
+    vc = torch.full((B, H, cap, d), fill, dtype=tdt, device=DEV)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    pa.decode_prefill(kc, vc, t["k"], t["v"], t["w"], t["beta"])
+    torch.cuda.synchronize()
+    return kc, vc
+
+
+@pytest.mark.parametrize("dtype,L", [("fp32", 1), ("fp32", 65), ("fp32", 333), ("bf16", 1), ("bf16", 64),
+                                     ("bf16", 200), ("bf16", 1000)])
+def test_prefill_cache_matches_oracle(cuda_lib, dtype, L):
+    """Rows 0..L-1: keys transported to the prompt end (fp32 within 1e-4; bf16 within the bf16
+    tolerance relative to the largest key), values copied exactly; rows >= L untouched."""
+    inp = gen_path_inputs(1, 3, L, 64, dtype, seed=500 + L, near2_frac=0.05)
+    cap = L + 7
+    kc, vc = run_prefill(inp, dtype, cap)
+    kref, vref = orc.prefill_cache(flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]), cap)
+    if dtype == "fp32":
+        check(flat(kc)[:, :L], kref[:, :L], 1e-4, "k_cache")
+    else:
+        check(flat(kc)[:, :L], kref[:, :L], 2e-2 * np.abs(kref).max(), "k_cache", rel=2e-2)
+    check(flat(vc)[:, :L], vref[:, :L], 0.0, "v_cache")
+    assert bool((flat(kc)[:, L:] == 7).all()) and bool((flat(vc)[:, L:] == 7).all())
+
+
+@pytest.mark.parametrize("dtype,L", [("fp32", 130), ("bf16", 300)])
+def test_prefill_then_decode_matches_forward(cuda_lib, dtype, L):
+    """Hand off L prompt tokens, decode four more: each output equals the forward oracle's row."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    steps = 4
+    inp = gen_path_inputs(1, 2, L + steps, 64, dtype, seed=600 + L, near2_frac=0.05)
+    head = {n: inp[n][:, :, :L].contiguous() for n in ("k", "v", "w", "beta")}
+    kc, vc = run_prefill(head, dtype, L + steps)
+    o_ref, _ = orc.fwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]), None, 0.8)
+    t = {n: inp[n].to(DEV) for n in ("q", "k", "v", "w", "beta")}
+    for s in range(steps):
+        pos = L + s
+        o = pa.decode_step(kc, vc, pos, *(t[n][:, :, pos].contiguous() for n in ("q", "k", "v", "w", "beta")),
+                           scale=0.8)
+        torch.cuda.synchronize()
+        if dtype == "fp32":
+            check(flat(o), o_ref[:, pos], 1e-4, f"o[{pos}]")
+        else:
+            check(flat(o), o_ref[:, pos], 2e-2, f"o[{pos}]", rel=2e-2)
