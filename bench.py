@@ -387,6 +387,9 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     dec = None if args.no_decode else run_decode(args, pa, dev, rank, ws, pk)
+    torch.cuda.empty_cache()
+    handoff = None if args.no_decode else run_prefill_handoff(args, pa, dev, pk)
+    torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(dict(CONFIGS[FWD_CFG]), B_f, B_b)
@@ -402,7 +405,7 @@ def run_ours(args):
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
                 "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward, "e2e": e2e,
                 "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 5 * args.steps,
-                "peaks": pk, "decode": dec, "cpu_baseline": cpu}
+                "peaks": pk, "decode": dec, "prefill_handoff": handoff, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -447,6 +450,41 @@ def run_decode(args, pa, dev, rank, ws, pk):
                          "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / ws / pk["hbm"], "traffic": None},
             "clocks": crec, "gpu_launches": 2 * steps,
             "workload": "decode, batch 32, 32 heads, d=64, cache 32768 -> 33023 bf16, 256 steps"}
+
+
+def run_prefill_handoff(args, pa, dev, pk):
+    """Prefill -> decode hand-off of a prompt as long as the decode workload's cache (batch 32,
+    32 heads, 32768 tokens, bf16), inputs drawn on the device; CUDA events around the call."""
+    cfg = CONFIGS[DEC_CFG]
+    Bt, H, d, L = cfg["batch"], cfg["heads"], cfg["head_dim"], cfg["t0"]
+    g = torch.Generator(device=dev).manual_seed(cfg["seed"] + 11)
+    sd = 1.0 / math.sqrt(d)
+    k = (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16)
+    v = (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16)
+    w = torch.randn(Bt, H, L, d, device=dev, generator=g)
+    w = (w / w.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    beta = 2.0 * torch.sigmoid(torch.randn(Bt, H, L, device=dev, generator=g))
+    kc = torch.empty(Bt, H, L + 256, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    desc = pa.make_decode_desc(kc, cfg["scale"])
+    wsp = torch.empty(pa.path_decode_prefill_workspace_size(desc, L), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        pa.decode_prefill(kc, vc, k, v, w, beta, ws=wsp)
+    reps = 3
+    marks = [ev()]
+    for _ in range(reps):
+        pa.decode_prefill(kc, vc, k, v, w, beta, ws=wsp)
+        marks.append(ev())
+    torch.cuda.synchronize()
+    ms = statistics.mean(marks[i].elapsed_time(marks[i + 1]) for i in range(reps))
+    # compulsory HBM bytes: read k, v, w (bf16) and beta, write both cache slabs
+    nbytes = Bt * H * L * (3 * d * 2 + 4 + 2 * d * 2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "tokens_per_s": Bt * L / (ms * 1e-3), "compulsory_bytes": nbytes, "achieved_gbs": gbs,
+            "frac_of_hbm": gbs / pk["hbm"],
+            "bound": "latency: the per-chunk tcgen05 UT preparation (fp32 F from split bf16 products) and the "
+                     "per-head fp32 suffix walk (one CTA per head, chunks right to left)",
+            "gpu_launches": 2, "workload": "prefill -> decode hand-off, batch 32, 32 heads, d=64, prompt 32768 bf16"}
 
 
 def main():

@@ -235,7 +235,7 @@ static int check_decode_desc(const path_decode_desc_t* d) {
 
 PATH_API size_t path_decode_prefill_workspace_size(const path_decode_desc_t* d, int prompt_len) {
   if (check_decode_desc(d) != PATH_OK || prompt_len < 0 || prompt_len > d->capacity) return 0;
-  return fwd_ws_layout(prefill_geom(d, prompt_len), 4).total;
+  return prefill_ws_bytes(prefill_geom(d, prompt_len), d->cache_dtype == PATH_BF16);
 }
 
 PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, void* v_cache, int prompt_len,
@@ -248,11 +248,11 @@ PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, voi
   CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta);
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
   const Geom g = prefill_geom(d, prompt_len);
-  const FwdWs lay = fwd_ws_layout(g, 4);
-  if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+  const bool bf = d->cache_dtype == PATH_BF16;
+  if (ws_bytes < prefill_ws_bytes(g, bf)) return PATH_ERR_WORKSPACE;
   if (prompt_len == 0) return PATH_OK;
-  return cuda_status(launch_prefill(d->cache_dtype == PATH_BF16, g, d->capacity, k, v, w, beta, k_cache,
-                                    v_cache, (char*)ws, lay, (cudaStream_t)stream));
+  return cuda_status(launch_prefill(bf, g, d->capacity, k, v, w, beta, k_cache, v_cache, (char*)ws,
+                                    (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -152,17 +152,19 @@ cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const f
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st);
 
 // Prefill -> decode hand-off: rows 0..g.L-1 of the caches ([g.BH][cap][64]) get the prompt keys
-// transported to the prompt end and the prompt values; g.B must be 64; ws holds the fp32
-// forward layout lay = fwd_ws_layout(g, 4).
+// transported to the prompt end and the prompt values; g.B must be 64; ws holds at least
+// prefill_ws_bytes(g, is_bf16) bytes.
+size_t prefill_ws_bytes(const Geom& g, bool is_bf16);
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
-                           const float* beta, void* k_cache, void* v_cache, char* ws, const FwdWs& lay,
-                           cudaStream_t st);
+                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st);
 
 // tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
-// tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.
+// tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32 set
+// (and no diagonal state) F goes to f32 ([BH][nc][64][64] fp32) instead, from products whose
+// bf16 operands U and U^T W are split into high and low bf16 parts (about 16 significant bits).
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st);
+                             cudaStream_t st, float* f32 = nullptr);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

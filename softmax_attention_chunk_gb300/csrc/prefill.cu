@@ -10,9 +10,11 @@
 //   F_c = I - W_c^T U_c^T W_c = H_{s(c)} ... H_{e(c)}, so H_{e(c)} ... H_{s(c)} = F_c^T,
 // hence k~_j = F_{nc-1}^T ... F_{c+1}^T K->_c row j.  With the suffix products
 //   S_{nc-1} = I,   S_{c-1} = S_c F_c^T,
-// the cache rows of chunk c are K->_c S_c^T.  K-> and F come from the fp32 UT preparation
-// (simt_fwd.cu); here one CTA per head walks the chunks right to left, keeping S in shared
-// memory, all in fp32: 2 * 64^3 multiply-adds per chunk.
+// the cache rows of chunk c are K->_c S_c^T.  For a bf16 cache, K-> (bf16) and F (fp32, from
+// split-precision bf16 products: the long suffix chain must not accumulate bf16 rounding) come
+// from the tcgen05 UT preparation (ut_tc.cu); for an fp32 cache both come from the fp32 SIMT
+// preparation (simt_fwd.cu).  One CTA per head then walks the chunks right to left, keeping S in
+// shared memory, in fp32: 2 * 64^3 multiply-adds per chunk.
 #include "internal.h"
 #include "dev_common.cuh"
 
@@ -31,6 +33,12 @@ struct PrefillSmem {
   float a[CB * LD];  // K->_c, then F_c
   float t[D * LD];   // S_c F_c^T before it replaces S
 };
+
+// Asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned) from global memory into L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
 
 // out[r][n] = sum_m A[r][m] * B[n][m] for the thread's 4 x 4 block (A B^T).
 __device__ __forceinline__ void mm_abt(const float* A, const float* Bm, int r0, int n0, float (&acc)[4][4]) {
@@ -52,9 +60,9 @@ __device__ __forceinline__ void mm_abt(const float* A, const float* Bm, int r0, 
   }
 }
 
-template <typename T>
+template <typename T, typename KR>
 __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, int nc, int cap,
-                                                               const float* __restrict__ kr,
+                                                               const KR* __restrict__ kr,
                                                                const float* __restrict__ f,
                                                                T* __restrict__ k_cache) {
   extern __shared__ float smem_f[];
@@ -64,8 +72,12 @@ __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, in
   for (int e = tid; e < D * D; e += PT) s.s[(e / D) * LD + e % D] = (e / D == e % D) ? 1.f : 0.f;
   for (int c = nc - 1; c >= 0; --c) {
     const int rows = min(CB, L - c * CB);
-    const float* src = kr + ((size_t)bh * Lp + (size_t)c * CB) * D;
-    for (int e = tid; e < CB * D; e += PT) s.a[(e / D) * LD + e % D] = e / D < rows ? src[e] : 0.f;
+    const KR* src = kr + ((size_t)bh * Lp + (size_t)c * CB) * D;
+    if (tid == 0 && c > 0) {  // F_c (used after the first product) and the next step's K-> into L2
+      l2_prefetch(f + ((size_t)bh * nc + c) * D * D, D * D * sizeof(float));
+      l2_prefetch(kr + ((size_t)bh * Lp + (size_t)(c - 1) * CB) * D, CB * D * sizeof(KR));
+    }
+    for (int e = tid; e < CB * D; e += PT) s.a[(e / D) * LD + e % D] = e / D < rows ? to_f(src[e]) : 0.f;
     __syncthreads();
     float acc[4][4];
     mm_abt(s.a, s.s, r0, n0, acc);  // K->_c S_c^T
@@ -93,33 +105,54 @@ __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, in
   }
 }
 
-template <typename T>
-cudaError_t prefill_t(const Geom& g, int cap, const void* k, const void* v, const void* w, const float* beta,
-                      void* k_cache, void* v_cache, char* ws, const FwdWs& lay, cudaStream_t st) {
-  // K-> and F of every chunk in fp32 (the query input is unused here: k stands in for it)
-  cudaError_t e = launch_prep_simt(std::is_same<T, __nv_bfloat16>::value, g, k, k, v, w, beta, nullptr, ws,
-                                   lay, false, st);
-  if (e != cudaSuccess) return e;
+// Workspace of the hand-off: the forward layout of the chosen preparation (bf16 tcgen05 or fp32
+// SIMT), plus the fp32 F array of the bf16 path.
+struct PrefillWs {
+  FwdWs lay;
+  size_t f32, total;
+};
+PrefillWs prefill_ws(const Geom& g, bool is_bf16) {
+  PrefillWs w;
+  w.lay = fwd_ws_layout(g, is_bf16 ? 2 : 4);
+  w.f32 = align_up(w.lay.total, 256);
+  w.total = is_bf16 ? w.f32 + (size_t)g.BH * g.nc * D * D * 4 : w.lay.total;
+  return w;
+}
+
+template <typename T, typename KR>
+cudaError_t transport(const Geom& g, int cap, const KR* kr, const float* f, void* k_cache, cudaStream_t st) {
   const size_t smem = sizeof(PrefillSmem);
-  e = cudaFuncSetAttribute(prefill_transport_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(prefill_transport_kernel<T, KR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  prefill_transport_kernel<T><<<(unsigned)g.BH, PT, smem, st>>>(
-      g.L, g.Lp, g.nc, cap, (const float*)(ws + lay.kr), (const float*)(ws + lay.f), (T*)k_cache);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // values are appended unchanged: rows 0..L-1 of every (batch, head) slab of the cache
-  const size_t row = (size_t)D * sizeof(T);
-  return cudaMemcpy2DAsync(v_cache, (size_t)cap * row, v, (size_t)g.L * row, (size_t)g.L * row, (size_t)g.BH,
-                           cudaMemcpyDeviceToDevice, st);
+  prefill_transport_kernel<T, KR><<<(unsigned)g.BH, PT, smem, st>>>(g.L, g.Lp, g.nc, cap, kr, f, (T*)k_cache);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t prefill_ws_bytes(const Geom& g, bool is_bf16) { return prefill_ws(g, is_bf16).total; }
+
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
-                           const float* beta, void* k_cache, void* v_cache, char* ws, const FwdWs& lay,
-                           cudaStream_t st) {
+                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st) {
   if (g.B != CB) return cudaErrorInvalidValue;
-  return is_bf16 ? prefill_t<__nv_bfloat16>(g, cap, k, v, w, beta, k_cache, v_cache, ws, lay, st)
-                 : prefill_t<float>(g, cap, k, v, w, beta, k_cache, v_cache, ws, lay, st);
+  const PrefillWs pw = prefill_ws(g, is_bf16);
+  cudaError_t e;
+  // K-> and F of every chunk (the query input is unused here: k stands in for it)
+  if (is_bf16) {
+    float* f32 = (float*)(ws + pw.f32);
+    if ((e = cudaMemsetAsync(ws + pw.lay.err, 0, sizeof(int), st)) != cudaSuccess) return e;
+    if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st, f32)) != cudaSuccess) return e;
+    e = transport<__nv_bfloat16>(g, cap, (const __nv_bfloat16*)(ws + pw.lay.kr), f32, k_cache, st);
+  } else {
+    if ((e = launch_prep_simt(false, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
+    e = transport<float>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f), k_cache, st);
+  }
+  if (e != cudaSuccess) return e;
+  // values are appended unchanged: rows 0..L-1 of every (batch, head) slab of the cache
+  const size_t row = (size_t)D * (is_bf16 ? 2 : 4);
+  return cudaMemcpy2DAsync(v_cache, (size_t)cap * row, v, (size_t)g.L * row, (size_t)g.L * row, (size_t)g.BH,
+                           cudaMemcpyDeviceToDevice, st);
 }
 
 }  // namespace pathattn
