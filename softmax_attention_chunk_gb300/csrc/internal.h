@@ -159,12 +159,13 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
                            const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st);
 
 // tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
-// tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32 set
-// (and no diagonal state) F goes to f32 ([BH][nc][64][64] fp32) instead, from products whose
-// bf16 operands U and U^T W are split into high and low bf16 parts (about 16 significant bits).
+// tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32_f
+// (and no diagonal state) F is written in fp32 ([BH][nc][64][64]) at lay.f, which must then have
+// room for it, from products whose bf16 operands U and U^T W are split into high and low bf16
+// parts (about 16 significant bits).
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, float* f32 = nullptr);
+                             cudaStream_t st, bool f32_f = false);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

@@ -140,10 +140,11 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
   cudaError_t e;
   // K-> and F of every chunk (the query input is unused here: k stands in for it)
   if (is_bf16) {
-    float* f32 = (float*)(ws + pw.f32);
-    if ((e = cudaMemsetAsync(ws + pw.lay.err, 0, sizeof(int), st)) != cudaSuccess) return e;
-    if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st, f32)) != cudaSuccess) return e;
-    e = transport<__nv_bfloat16>(g, cap, (const __nv_bfloat16*)(ws + pw.lay.kr), f32, k_cache, st);
+    FwdWs lay = pw.lay;
+    lay.f = pw.f32;  // F in fp32
+    if ((e = cudaMemsetAsync(ws + lay.err, 0, sizeof(int), st)) != cudaSuccess) return e;
+    if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, lay, false, st, true)) != cudaSuccess) return e;
+    e = transport<__nv_bfloat16>(g, cap, (const __nv_bfloat16*)(ws + lay.kr), (const float*)(ws + pw.f32), k_cache, st);
   } else {
     if ((e = launch_prep_simt(false, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
     e = transport<float>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f), k_cache, st);

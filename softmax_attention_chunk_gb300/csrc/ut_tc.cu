@@ -56,10 +56,10 @@ struct UtParams {
   float* fr;
   float* ft;
   int with_diag;
-  float* f32;  // if set (hand-off, no diagonal state): F in fp32 from split-precision products
   int* err;
 };
 
+template <bool F32>
 __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
                                                         const __grid_constant__ CUtensorMap tm_v,
@@ -173,13 +173,18 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     if (warp == 0) ut_solve_column<0>(sg, cc, y);
     else ut_solve_column<2>(sg, cc, y);
     const float bc = s.beta[cc];
+    if constexpr (F32) {  // fp32 F: U = U_hi + U_lo, both bf16 (U_lo in P's slot, unused without the diagonal state)
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      const float uv = y[r] * bc;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-      *reinterpret_cast<__nv_bfloat16*>(s.u + sw128_offset(r, cc)) = hi;
-      // fp32 F: U = U_hi + U_lo, both bf16 (U_lo in P's slot, unused without the diagonal state)
-      if (p.f32) *reinterpret_cast<__nv_bfloat16*>(s.p + sw128_offset(r, cc)) = __float2bfloat16_rn(uv - __bfloat162float(hi));
+      for (int r = 0; r < 64; ++r) {
+        const float uv = y[r] * bc;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
+        *reinterpret_cast<__nv_bfloat16*>(s.u + sw128_offset(r, cc)) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(s.p + sw128_offset(r, cc)) = __float2bfloat16_rn(uv - __bfloat162float(hi));
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < 64; ++r)
+        *reinterpret_cast<__nv_bfloat16*>(s.u + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r] * bc);
     }
   }
   publish();
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     mma64(tb + 0, am1, 0, au, 1, 0);
     mma64(tb + 64, au, 0, an2, 1, 0);
     mma64(tb + 128, au, 1, aw, 1, 0);
-    if (p.f32) mma64(tb + 128, ap, 1, aw, 1, 1);
+    if constexpr (F32) mma64(tb + 128, ap, 1, aw, 1, 1);
   }, 33);
   {
     float x[32];
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     ld_half(tb, lane_off, 64, x);
     put_half(s.x, i, h, x);
     ld_half(tb, lane_off, 128, x);
-    if (p.f32) {  // Y = Y_hi + Y_lo, both bf16 (Y_lo in V's slot, never loaded without the diagonal state)
+    if constexpr (F32) {  // Y = Y_hi + Y_lo, both bf16 (Y_lo in V's slot, never loaded without the diagonal state)
       float lo[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     mma64(tb + 64, ax, 1, aw, 1, 0);
     mma64(tb + 192, am1, 0, ax, 1, 1, /*neg_a=*/1);
     mma64(tb + 128, aw, 1, ay, 1, 0);
-    if (p.f32) mma64(tb + 128, aw, 1, av, 1, 1);
+    if constexpr (F32) mma64(tb + 128, aw, 1, av, 1, 1);
   }, 34);
   {
     float x[32], src[32];
@@ -236,8 +241,9 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     ld_half(tb, lane_off, 128, x);  // F = I - W^T Y, row i
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
-    if (p.f32) {
-      float4* dst = reinterpret_cast<float4*>(p.f32 + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
+    if constexpr (F32) {
+      // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.f) + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
 #pragma unroll
       for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     } else {
@@ -298,8 +304,8 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
 
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, float* f32) {
-  if (g.B != 64 || (f32 && with_diag)) return cudaErrorInvalidValue;
+                             cudaStream_t st, bool f32_f) {
+  if (g.B != 64 || (f32_f && with_diag)) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv, mw;
   if (!make_map_head_rows64(&mq, q, g.L, g.BH) || !make_map_head_rows64(&mk, k, g.L, g.BH) ||
       !make_map_head_rows64(&mv, v, g.L, g.BH) || !make_map_head_rows64(&mw, w, g.L, g.BH))
@@ -322,12 +328,12 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
   p.fr = (float*)(ws + lay.fr);
   p.ft = (float*)(ws + lay.ft);
   p.with_diag = with_diag ? 1 : 0;
-  p.f32 = f32;
   p.err = (int*)(ws + lay.err);
   const size_t smem = sizeof(UtSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(ut_prep64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = f32_f ? ut_prep64_kernel<true> : ut_prep64_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ut_prep64_kernel<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, p);
+  kern<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, p);
   return cudaGetLastError();
 }
 
