@@ -49,8 +49,10 @@ def lib():
         _lib.oracle_decode_step.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P, _P, d, _P, _P]
         _lib.oracle_prefill_cache.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P]
         _lib.oracle_transport_keys.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_int), _P, _P, _P, _P]
+        _lib.oracle_decode_step_fox.argtypes = [i, i, i, i, _P, _P, _P, _P, _P, _P, _P, _P, _P, d, _P, _P]
         for f in ("oracle_fwd_head_rows", "oracle_fwd", "oracle_logits", "oracle_bwd_head",
-                  "oracle_decode_step", "oracle_prefill_cache", "oracle_transport_keys"):
+                  "oracle_decode_step", "oracle_prefill_cache", "oracle_transport_keys",
+                  "oracle_decode_step_fox"):
             getattr(_lib, f).restype = i
     return _lib
 
@@ -164,3 +166,18 @@ def transport_keys(k, w, beta, rows):
     _check(lib().oracle_transport_keys(n, d, L, len(rows), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
                                        _ptr(k), _ptr(w), _ptr(beta), _ptr(out)))
     return out
+
+
+def decode_step_fox(k_cache, v_cache, a_cache, t, q_t, k_t, v_t, w_t, beta_t, logf_t, scale=1.0, want_lse=False):
+    """One PaTH-FoX decode step, in place on the fp64 caches [n,cap,d] and the prefix cache a [n,cap]
+    (a_j = sum_{s<=j} log f_s); returns o_t [n,d] (and lse)."""
+    for c in (k_cache, v_cache, a_cache):
+        assert c.dtype == np.float64 and c.flags.c_contiguous
+    q_t, k_t, v_t, w_t, beta_t, logf_t = map(_f64, (q_t, k_t, v_t, w_t, beta_t, logf_t))
+    n, cap, d = k_cache.shape
+    o = np.zeros((n, d))
+    lse = np.zeros(n) if want_lse else None
+    _check(lib().oracle_decode_step_fox(n, d, cap, int(t), _ptr(k_cache), _ptr(v_cache), _ptr(a_cache), _ptr(q_t),
+                                        _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(logf_t), float(scale),
+                                        _ptr(o), _ptr(lse)))
+    return (o, lse) if want_lse else o

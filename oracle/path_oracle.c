@@ -25,7 +25,8 @@
  *
  * Backward (absent from the pages): exact reverse-mode derivative of the same walk, per row.
  * Decode: the in-place key rewrite of the notes' §2.8 (Eq. (1)) followed by a plain
- * single-query softmax.  Prefill hand-off: the same rewrite applied to the prompt tokens in
+ * single-query softmax; with a forget gate the bias sum_{s=j+1..t} log f_s is carried as prefix
+ * sums per cache row.  Prefill hand-off: the same rewrite applied to the prompt tokens in
  * order, so that every prompt key ends up transported to the prompt end (§2.8, last paragraph).
  *
  * Parallelism: OpenMP over independent query rows (and heads); no reduction order depends on
@@ -340,4 +341,51 @@ int oracle_transport_keys(int nheads, int d, int L, int nrows, const int* rows, 
     }
   }
   return 0;
+}
+
+/* One PaTH-FoX decode step for nheads heads (reading notes §2.8 Eq. (1) with the forget-gate bias
+ * of §2.5): the keys are rewritten exactly as in oracle_decode_step, and the logit of cached key j
+ * gains sum_{s=j+1..t} log f_s.  That sum is carried as prefix sums: ac[h][j] = sum_{s<=j} log f_s,
+ * so the bias is ac[t] - ac[j]; the step stores ac[t] = ac[t-1] + log f_t (ac[-1] = 0).
+ * ac: [nheads][cap] fp64, rows 0..t-1 valid on entry; logf_t: [nheads]; other arguments as in
+ * oracle_decode_step. */
+int oracle_decode_step_fox(int nheads, int d, int cap, int t, double* kc, double* vc, double* ac,
+                           const double* q_t, const double* k_t, const double* v_t, const double* w_t,
+                           const double* beta_t, const double* logf_t, double scale, double* o_t,
+                           double* lse_t) {
+  if (t < 0 || t + 1 > cap) return -2;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int h = 0; h < nheads; ++h) {
+    double* K = kc + (size_t)h * cap * d;
+    double* V = vc + (size_t)h * cap * d;
+    double* A = ac + (size_t)h * cap;
+    const double* w = w_t + (size_t)h * d;
+    const double* q = q_t + (size_t)h * d;
+    const double b = clamp_beta(beta_t[h]);
+    for (int j = 0; j < t; ++j) {
+      double* kj = K + (size_t)j * d;
+      const double a = dot(w, kj, d);
+      for (int n = 0; n < d; ++n) kj[n] -= b * a * w[n];
+    }
+    memcpy(K + (size_t)t * d, k_t + (size_t)h * d, sizeof(double) * d);
+    memcpy(V + (size_t)t * d, v_t + (size_t)h * d, sizeof(double) * d);
+    A[t] = (t > 0 ? A[t - 1] : 0.0) + logf_t[h];
+    double* s = (double*)malloc(sizeof(double) * (t + 1));
+    double* p = (double*)malloc(sizeof(double) * (t + 1));
+    if (!s || !p) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+      for (int j = 0; j <= t; ++j) s[j] = scale * dot(K + (size_t)j * d, q, d) + (A[t] - A[j]);
+      const double l = row_softmax(s, t, p);
+      if (lse_t) lse_t[h] = l;
+      double* o = o_t + (size_t)h * d;
+      for (int n = 0; n < d; ++n) o[n] = 0.0;
+      for (int j = 0; j <= t; ++j)
+        for (int n = 0; n < d; ++n) o[n] += p[j] * V[(size_t)j * d + n];
+    }
+    free(s); free(p);
+  }
+  return bad ? -1 : 0;
 }

@@ -469,3 +469,35 @@ def test_transport_keys_are_the_prefill_rows():
     kc, _ = orc.prefill_cache(k, v, w, beta, cap=L)
     rows = [0, 1, 17, 38, 39]
     np.testing.assert_allclose(orc.transport_keys(k, w, beta, rows), kc[:, rows], rtol=0, atol=1e-13)
+
+
+def test_fox_decode_from_empty_cache_reproduces_forward_rows():
+    """PaTH-FoX decode (key rewrite plus the forget bias carried as prefix sums) gives the FoX
+    forward's rows (whose bias the forward oracle sums along the query walk)."""
+    rng = np.random.default_rng(17)
+    n, L, d = 2, 19, 6
+    q, k, v = (rng.standard_normal((n, L, d)) for _ in range(3))
+    w = rng.standard_normal((n, L, d)); w /= np.linalg.norm(w, axis=-1, keepdims=True)
+    beta = rng.uniform(0, 2, (n, L))
+    logf = np.log(1.0 / (1.0 + np.exp(-(rng.standard_normal((n, L)) + 2.0))))
+    o_f, lse_f = orc.fwd(q, k, v, w, beta, logf, 0.9)
+    kc = np.zeros((n, L, d)); vc = np.zeros((n, L, d)); ac = np.zeros((n, L))
+    for t in range(L):
+        o_t, lse_t = orc.decode_step_fox(kc, vc, ac, t, q[:, t], k[:, t], v[:, t], w[:, t], beta[:, t], logf[:, t],
+                                         0.9, want_lse=True)
+        np.testing.assert_allclose(o_t, o_f[:, t], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse_t, lse_f[:, t], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ac, np.cumsum(logf, axis=1), rtol=0, atol=1e-12)
+
+
+def test_fox_decode_with_zero_log_f_is_plain_decode():
+    rng = np.random.default_rng(18)
+    n, t0, d = 2, 9, 5
+    kc = rng.standard_normal((n, t0 + 1, d)); vc = rng.standard_normal((n, t0 + 1, d))
+    kc2, vc2, ac = kc.copy(), vc.copy(), np.zeros((n, t0 + 1))
+    q, k, v = (rng.standard_normal((n, d)) for _ in range(3))
+    w = rng.standard_normal((n, d)); w /= np.linalg.norm(w, axis=-1, keepdims=True)
+    beta = rng.uniform(0, 2, n)
+    o1 = orc.decode_step(kc, vc, t0, q, k, v, w, beta, 1.3)
+    o2 = orc.decode_step_fox(kc2, vc2, ac, t0, q, k, v, w, beta, np.zeros(n), 1.3)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-14)
