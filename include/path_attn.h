@@ -216,12 +216,30 @@ size_t path_decode_prefill_workspace_size(const path_decode_desc_t* desc, int pr
  * k, v, w: [batch][heads][prompt_len][head_dim] in cache_dtype; beta: [batch][heads][prompt_len]
  * float32 (clamped to [0, 2]).  Caches: [batch][heads][capacity][head_dim]; rows >= prompt_len
  * are not touched.  Requires 0 <= prompt_len <= capacity (else PATH_ERR_CAPACITY); prompt_len = 0
- * does nothing.  ws: at least path_decode_prefill_workspace_size(desc, prompt_len) bytes,
+ * does nothing.  PaTH-FoX: with log_f ([batch][heads][prompt_len] float32) and a_cache
+ * ([batch][heads][capacity] float32) both given, rows 0..prompt_len-1 of a_cache get the inclusive
+ * prefix sums of log_f, as path_decode_step_fox expects; both NULL for plain PaTH (one without the
+ * other is PATH_ERR_INVALID_ARG).  ws: at least path_decode_prefill_workspace_size(desc, prompt_len) bytes,
  * 256-byte aligned.  Asynchronous on stream.
  */
 int path_decode_prefill(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int prompt_len,
-                        const void* k, const void* v, const void* w, const float* beta, void* ws,
-                        size_t ws_bytes, void* stream);
+                        const void* k, const void* v, const void* w, const float* beta, const float* log_f,
+                        float* a_cache, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One PaTH-FoX decode step (notes §2.8 Eq. (1) with the forget gate of §2.5): the key rewrite
+ * and append of path_decode_step, and the logit of cached key j gains
+ *   sum_{s=j+1..t} log f_s = a_t - a_j,
+ * where a_cache ([batch][heads][capacity] float32) holds the prefix sums a_j = sum_{s<=j} log f_s
+ * of the cached rows (rows 0..t-1 on entry; path_decode_prefill with log_f fills them for a
+ * prompt).  The step stores a_t = a_{t-1} + log_f_t (a_{-1} = 0) in row t, then
+ *   o_t = sum_j softmax_j(scale k_j . q_t + a_t - a_j) v_j   over j = 0..t.
+ * log_f_t: [batch][heads] float32 (log of the forget gate, <= 0).  Other arguments, requirements
+ * and errors as path_decode_step (same workspace size).
+ */
+int path_decode_step_fox(const path_decode_desc_t* desc, void* k_cache, void* v_cache, float* a_cache, int t,
+                         const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
+                         const float* log_f_t, void* o_t, void* ws, size_t ws_bytes, void* stream);
 
 #define PATH_DECODE_NOALLOC_MAX_HEADS 496
 int path_decode_step_noalloc(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int t,

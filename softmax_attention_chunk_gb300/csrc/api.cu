@@ -239,20 +239,40 @@ PATH_API size_t path_decode_prefill_workspace_size(const path_decode_desc_t* d, 
 }
 
 PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, void* v_cache, int prompt_len,
-                                 const void* k, const void* v, const void* w, const float* beta, void* ws,
-                                 size_t ws_bytes, void* stream) {
+                                 const void* k, const void* v, const void* w, const float* beta,
+                                 const float* log_f, float* a_cache, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_decode_desc(d);
   if (rc != PATH_OK) return rc;
   if (prompt_len < 0) return PATH_ERR_INVALID_ARG;
   if (prompt_len > d->capacity) return PATH_ERR_CAPACITY;
   CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta);
+  if ((!log_f) != (!a_cache)) return PATH_ERR_INVALID_ARG;
+  if (log_f) { CHECK_PTR(log_f); CHECK_PTR(a_cache); }
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
   const Geom g = prefill_geom(d, prompt_len);
   const bool bf = d->cache_dtype == PATH_BF16;
   if (ws_bytes < prefill_ws_bytes(g, bf)) return PATH_ERR_WORKSPACE;
   if (prompt_len == 0) return PATH_OK;
   return cuda_status(launch_prefill(bf, g, d->capacity, k, v, w, beta, k_cache, v_cache, (char*)ws,
-                                    (cudaStream_t)stream));
+                                    (cudaStream_t)stream, log_f, a_cache));
+}
+
+PATH_API int path_decode_step_fox(const path_decode_desc_t* d, void* k_cache, void* v_cache, float* a_cache, int t,
+                                  const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                                  const float* beta_t, const float* log_f_t, void* o_t, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  int rc = check_decode_desc(d);
+  if (rc != PATH_OK) return rc;
+  if (t < 0) return PATH_ERR_INVALID_ARG;
+  if ((long long)t + 1 > d->capacity) return PATH_ERR_CAPACITY;
+  CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(a_cache); CHECK_PTR(q_t); CHECK_PTR(k_t); CHECK_PTR(v_t);
+  CHECK_PTR(w_t); CHECK_PTR(beta_t); CHECK_PTR(log_f_t); CHECK_PTR(o_t);
+  const int BH = d->batch * d->heads;
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  if (ws_bytes < decode_ws_bytes(BH)) return PATH_ERR_WORKSPACE;
+  return cuda_status(launch_decode(d->cache_dtype == PATH_BF16, BH, d->capacity, t, d->scale, k_cache, v_cache,
+                                   q_t, k_t, v_t, w_t, beta_t, o_t, (float*)ws, (cudaStream_t)stream, a_cache,
+                                   log_f_t));
 }
 
 }  // extern "C"

@@ -60,11 +60,15 @@ template <> struct Vec8<float> {
 
 // grid (nsplit, BH).  Split s covers rows [s*per, min((s+1)*per, t+1)) of its head.
 // Writes partial (m [log2 domain], l, acc[64]) to partials[(bh*kDecodeMaxSplits + s)*(D+2)].
-template <typename T>
+// FOX (PaTH-FoX, notes §2.5): the logit of key j gains sum_{s=j+1..t} log f_s = A_t - a_j, with
+// ac[bh][j] = a_j the prefix sums of log f kept beside the cache; A_t = a_{t-1} + log f_t is
+// stored as row t.
+template <typename T, bool FOX>
 __global__ void __launch_bounds__(NT) decode_split_kernel(
     int cap, int t, int per, float scale, T* __restrict__ kc, T* __restrict__ vc,
     const T* __restrict__ qt, const T* __restrict__ kt, const T* __restrict__ vt,
-    const T* __restrict__ wt, const float* __restrict__ beta_t, float* __restrict__ partials) {
+    const T* __restrict__ wt, const float* __restrict__ beta_t, float* __restrict__ partials,
+    float* __restrict__ ac, const float* __restrict__ logf_t) {
   __shared__ float s_m[GROUPS], s_l[GROUPS];
   __shared__ float s_acc[GROUPS][D + 1];
 
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
   qw = group_sum<LANES>(qw);
   const float bt = clamp_beta(beta_t[bh]);
   const float scl = scale * kLog2e;
+  float At = 0.f;
+  if constexpr (FOX) At = (t > 0 ? ac[hrow + t - 1] : 0.f) + logf_t[bh];
 
   float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
@@ -97,12 +103,15 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
   // Trip count is uniform over the CTA so that every lane reaches the group shuffles.
   for (int base = j0; base < j1; base += GROUPS * UNROLL) {
     Vec8<T> kv[UNROLL], vv[UNROLL];
+    float bias[UNROLL];  // forget-gate bias of the key, log2 domain (FOX)
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int j = base + grp + u * GROUPS;
+      bias[u] = 0.f;
       if (j < t) {
         kv[u].load(kc + (hrow + j) * D + e0);
         vv[u].load(vc + (hrow + j) * D + e0);
+        if constexpr (FOX) bias[u] = (At - ac[hrow + j]) * kLog2e;
       } else if (j == t) {
         kv[u].load(kt + (size_t)bh * D + e0);
         vv[u].load(vt + (size_t)bh * D + e0);
@@ -135,10 +144,13 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
           Vec8<T> kn;
           kn.from_float(kf);
           kn.store(kc + (hrow + j) * D + e0);
-          s = (qk - ba * qw) * scl;
+          s = (qk - ba * qw) * scl + bias[u];
         } else {  // j == t: append the new key and value unchanged
           kv[u].store(kc + (hrow + j) * D + e0);
           vv[u].store(vc + (hrow + j) * D + e0);
+          if constexpr (FOX) {
+            if (lane8 == 0) ac[hrow + t] = At;
+          }
           s = qk * scl;
         }
         float vf[8];
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(int nsplit, const flo
 template <typename T>
 cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, const void* q,
                      const void* k, const void* v, const void* w, const float* beta, void* o,
-                     float* partials, cudaStream_t st) {
+                     float* partials, float* ac, const float* logf_t, cudaStream_t st) {
   const int n = t + 1;
   // Aim for >= ~4 waves of CTAs over 152 SMs while keeping >= 256 rows per split.
   int nsplit = (n + 1023) / 1024;
@@ -210,9 +222,14 @@ cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, co
   if (nsplit < 1) nsplit = 1;
   const int per = (n + nsplit - 1) / nsplit;
   nsplit = (n + per - 1) / per;
-  decode_split_kernel<T><<<dim3(nsplit, BH), NT, 0, st>>>(
-      cap, t, per, scale, (T*)kc, (T*)vc, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta,
-      partials);
+  if (ac)
+    decode_split_kernel<T, true><<<dim3(nsplit, BH), NT, 0, st>>>(
+        cap, t, per, scale, (T*)kc, (T*)vc, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta,
+        partials, ac, logf_t);
+  else
+    decode_split_kernel<T, false><<<dim3(nsplit, BH), NT, 0, st>>>(
+        cap, t, per, scale, (T*)kc, (T*)vc, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta,
+        partials, nullptr, nullptr);
   decode_combine_kernel<T><<<BH, D, 0, st>>>(nsplit, partials, (T*)o);
   return cudaGetLastError();
 }
@@ -221,9 +238,10 @@ cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, co
 
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
                           const void* q, const void* k, const void* v, const void* w,
-                          const float* beta, void* o, float* partials, cudaStream_t st) {
-  return is_bf16 ? decode_t<__nv_bfloat16>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, st)
-                 : decode_t<float>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, st);
+                          const float* beta, void* o, float* partials, cudaStream_t st, float* ac,
+                          const float* logf_t) {
+  return is_bf16 ? decode_t<__nv_bfloat16>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st)
+                 : decode_t<float>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st);
 }
 
 }  // namespace pathattn

@@ -154,9 +154,12 @@ cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const f
 // Prefill -> decode hand-off: rows 0..g.L-1 of the caches ([g.BH][cap][64]) get the prompt keys
 // transported to the prompt end and the prompt values; g.B must be 64; ws holds at least
 // prefill_ws_bytes(g, is_bf16) bytes.
+// With logf and a_cache set (PaTH-FoX), rows 0..g.L-1 of a_cache ([g.BH][cap] fp32) get the
+// inclusive prefix sums of logf ([g.BH][g.L]).
 size_t prefill_ws_bytes(const Geom& g, bool is_bf16);
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
-                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st);
+                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st,
+                           const float* logf = nullptr, float* a_cache = nullptr);
 
 // tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
 // tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32_f
@@ -194,8 +197,11 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
                           void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st);
 
 // Decode step.
+// ac / logf_t (PaTH-FoX, both set or both null): prefix sums of log f beside the cache
+// ([BH][cap] fp32, rows 0..t-1 valid, row t written) and this step's log f ([BH]).
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
                           const void* q, const void* k, const void* v, const void* w,
-                          const float* beta, void* o, float* partials, cudaStream_t st);
+                          const float* beta, void* o, float* partials, cudaStream_t st, float* ac = nullptr,
+                          const float* logf_t = nullptr);
 
 }  // namespace pathattn

@@ -119,6 +119,33 @@ PrefillWs prefill_ws(const Geom& g, bool is_bf16) {
   return w;
 }
 
+// Inclusive prefix sums of log f per head into the forget-gate prefix cache: one CTA of 256
+// threads per head, each thread summing a contiguous segment, then a block scan of the segment
+// totals (fp32; the decode step extends the same running sum).
+__global__ void __launch_bounds__(PT) prefill_logf_prefix_kernel(int L, int cap, const float* __restrict__ logf,
+                                                                 float* __restrict__ ac) {
+  __shared__ float tot[PT];
+  const int tid = threadIdx.x, bh = blockIdx.x;
+  const int seg = (L + PT - 1) / PT, j0 = tid * seg, j1 = min(L, j0 + seg);
+  const float* src = logf + (size_t)bh * L;
+  float s = 0.f;
+  for (int j = j0; j < j1; ++j) s += src[j];
+  tot[tid] = s;
+  __syncthreads();
+  for (int o = 1; o < PT; o <<= 1) {  // inclusive Hillis-Steele scan of the segment totals
+    const float x = tid >= o ? tot[tid - o] : 0.f;
+    __syncthreads();
+    tot[tid] += x;
+    __syncthreads();
+  }
+  float run = tid > 0 ? tot[tid - 1] : 0.f;
+  float* dst = ac + (size_t)bh * cap;
+  for (int j = j0; j < j1; ++j) {
+    run += src[j];
+    dst[j] = run;
+  }
+}
+
 template <typename T, typename KR>
 cudaError_t transport(const Geom& g, int cap, const KR* kr, const float* f, void* k_cache, cudaStream_t st) {
   const size_t smem = sizeof(PrefillSmem);
@@ -134,8 +161,9 @@ cudaError_t transport(const Geom& g, int cap, const KR* kr, const float* f, void
 size_t prefill_ws_bytes(const Geom& g, bool is_bf16) { return prefill_ws(g, is_bf16).total; }
 
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
-                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st) {
-  if (g.B != CB) return cudaErrorInvalidValue;
+                           const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st,
+                           const float* logf, float* a_cache) {
+  if (g.B != CB || (!logf) != (!a_cache)) return cudaErrorInvalidValue;
   const PrefillWs pw = prefill_ws(g, is_bf16);
   cudaError_t e;
   // K-> and F of every chunk (the query input is unused here: k stands in for it)
@@ -150,6 +178,10 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
     e = transport<float>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f), k_cache, st);
   }
   if (e != cudaSuccess) return e;
+  if (logf) {
+    prefill_logf_prefix_kernel<<<(unsigned)g.BH, PT, 0, st>>>(g.L, cap, logf, a_cache);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // values are appended unchanged: rows 0..L-1 of every (batch, head) slab of the cache
   const size_t row = (size_t)D * (is_bf16 ? 2 : 4);
   return cudaMemcpy2DAsync(v_cache, (size_t)cap * row, v, (size_t)g.L * row, (size_t)g.L * row, (size_t)g.BH,

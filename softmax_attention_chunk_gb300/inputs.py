@@ -29,7 +29,7 @@ BETA_MAX_BELOW_2 = float(torch.tensor(2.0, dtype=torch.float32).nextafter(torch.
 
 _TENSOR_IDS = {
     "q": 1, "k": 2, "v": 3, "w": 4, "xbeta": 5, "near2_mask": 6, "near2_val": 7, "xf": 8, "dO": 9,
-    "kc": 11, "vc": 12, "sq": 13, "sk": 14, "sv": 15, "sw": 16, "sxbeta": 17,
+    "kc": 11, "vc": 12, "sq": 13, "sk": 14, "sv": 15, "sw": 16, "sxbeta": 17, "xfc": 18, "sxf": 19,
 }
 
 # The five workloads (sizes and distributions).  Index 1 is run at L=4096 by default; the
@@ -135,14 +135,22 @@ def gen_path_inputs(batch, heads, seqlen, head_dim, dtype="bf16", seed=1000, nea
     return res
 
 
+def _log_f_row(seed, name, bh, rows):
+    """log f = log sigmoid(N(2, 1)), computed in fp64, stored fp32."""
+    xf = torch.randn(rows, generator=_gen(seed, name, bh), dtype=torch.float64) + 2.0
+    return torch.log(torch.sigmoid(xf)).to(torch.float32)
+
+
 def gen_decode_inputs(batch, heads, head_dim, t0, steps, dtype="bf16", seed=1004, capacity=None,
-                      heads_subset=None, **_unused):
+                      heads_subset=None, fox=False, **_unused):
     """Inputs of the decode workload: a cache pre-filled with ``t0`` random entries and
     ``steps`` new tokens per head.
 
     Returns k_cache/v_cache of shape [B,H,capacity,d] (entries >= t0 are zero), per-step
-    q,k,v,w of shape [steps,B,H,d] and beta of shape [steps,B,H].  With ``heads_subset`` the
-    head axes collapse to one axis of the selected flat head indices.
+    q,k,v,w of shape [steps,B,H,d] and beta of shape [steps,B,H].  With ``fox`` also a_cache
+    [B,H,capacity] (fp32 running sums of the pre-filled entries' log f, summed in fp64) and the
+    per-step log_f [steps,B,H].  With ``heads_subset`` the head axes collapse to one axis of the
+    selected flat head indices.
     """
     tdt = TORCH_DTYPES[dtype]
     d = head_dim
@@ -154,6 +162,8 @@ def gen_decode_inputs(batch, heads, head_dim, t0, steps, dtype="bf16", seed=1004
     vc = torch.zeros(n, cap, d, dtype=tdt)
     sq, sk, sv, sw = (torch.empty(n, steps, d, dtype=tdt) for _ in range(4))
     sb = torch.empty(n, steps, dtype=torch.float32)
+    ac = torch.zeros(n, cap, dtype=torch.float32) if fox else None
+    sf = torch.empty(n, steps, dtype=torch.float32) if fox else None
 
     def one(idx):
         bh = hs[idx]
@@ -165,14 +175,24 @@ def gen_decode_inputs(batch, heads, head_dim, t0, steps, dtype="bf16", seed=1004
         sv[idx] = _normal_rows(seed, "sv", bh, steps, d, tdt, sd)
         sw[idx] = _unit_rows(seed, "sw", bh, steps, d, tdt)
         sb[idx] = _beta_row(seed, bh, steps, 0.0, prefix="s")
+        if fox:
+            if t0 > 0:
+                ac[idx, :t0] = torch.cumsum(_log_f_row(seed, "xfc", bh, t0).double(), 0).to(torch.float32)
+            sf[idx] = _log_f_row(seed, "sxf", bh, steps)
 
     _parallel(one, n)
     step = lambda x: x.transpose(0, 1).contiguous()  # [steps, n, ...]
     res = dict(k_cache=kc, v_cache=vc, q=step(sq), k=step(sk), v=step(sv), w=step(sw), beta=step(sb))
+    if fox:
+        res["a_cache"] = ac
+        res["log_f"] = step(sf)
     if heads_subset is None:
         res["k_cache"] = kc.reshape(batch, heads, cap, d)
         res["v_cache"] = vc.reshape(batch, heads, cap, d)
         for key in ("q", "k", "v", "w"):
             res[key] = res[key].reshape(steps, batch, heads, d)
         res["beta"] = res["beta"].reshape(steps, batch, heads)
+        if fox:
+            res["a_cache"] = ac.reshape(batch, heads, cap)
+            res["log_f"] = res["log_f"].reshape(steps, batch, heads)
     return res

@@ -64,7 +64,9 @@ _lib.path_decode_step_noalloc.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp
 _lib.path_decode_prefill_workspace_size.restype = _sz
 _lib.path_decode_prefill_workspace_size.argtypes = [_DDP, _i]
 _lib.path_decode_prefill.restype = _i
-_lib.path_decode_prefill.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 4 + [_vp, _sz, _vp]
+_lib.path_decode_prefill.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
+_lib.path_decode_step_fox.restype = _i
+_lib.path_decode_step_fox.argtypes = [_DDP, _vp, _vp, _vp, _i] + [_vp] * 7 + [_vp, _sz, _vp]
 PATH_DECODE_NOALLOC_MAX_HEADS = 496
 
 PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
@@ -76,7 +78,7 @@ PATH_BWD_Z_FROM_FWD = 16
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
             "path_decode_step", "path_decode_step_noalloc", "path_decode_prefill_workspace_size",
-            "path_decode_prefill")
+            "path_decode_prefill", "path_decode_step_fox")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -132,9 +134,16 @@ def path_decode_prefill_workspace_size(desc: path_decode_desc_t, prompt_len: int
     return _lib.path_decode_prefill_workspace_size(ctypes.byref(desc), int(prompt_len))
 
 
-def path_decode_prefill(desc, k_cache, v_cache, prompt_len, k, v, w, beta, ws, ws_bytes, stream) -> int:
-    return _lib.path_decode_prefill(ctypes.byref(desc), k_cache, v_cache, int(prompt_len), k, v, w, beta, ws,
-                                    ws_bytes, stream)
+def path_decode_prefill(desc, k_cache, v_cache, prompt_len, k, v, w, beta, log_f, a_cache, ws, ws_bytes,
+                        stream) -> int:
+    return _lib.path_decode_prefill(ctypes.byref(desc), k_cache, v_cache, int(prompt_len), k, v, w, beta, log_f,
+                                    a_cache, ws, ws_bytes, stream)
+
+
+def path_decode_step_fox(desc, k_cache, v_cache, a_cache, t, q_t, k_t, v_t, w_t, beta_t, log_f_t, o_t, ws, ws_bytes,
+                         stream) -> int:
+    return _lib.path_decode_step_fox(ctypes.byref(desc), k_cache, v_cache, a_cache, int(t), q_t, k_t, v_t, w_t,
+                                     beta_t, log_f_t, o_t, ws, ws_bytes, stream)
 
 
 # ---------------- torch-tensor wrappers ----------------
@@ -243,10 +252,11 @@ def decode_step(k_cache, v_cache, t, q_t, k_t, v_t, w_t, beta_t, scale=1.0, ws=N
     return o
 
 
-def decode_prefill(k_cache, v_cache, k, v, w, beta, ws=None):
+def decode_prefill(k_cache, v_cache, k, v, w, beta, ws=None, log_f=None, a_cache=None):
     """Prefill -> decode hand-off: rows 0..L-1 of the caches [B,H,cap,d] get the prompt keys
     k,v,w [B,H,L,d] (cache dtype), beta [B,H,L] fp32 transported to the prompt end; decoding then
-    continues at t = L."""
+    continues at t = L.  PaTH-FoX: log_f [B,H,L] and a_cache [B,H,cap] (fp32) together fill the
+    forget-gate prefix cache."""
     desc = make_decode_desc(k_cache, 1.0)
     B, H, cap, d = k_cache.shape
     L = k.shape[2]
@@ -254,11 +264,36 @@ def decode_prefill(k_cache, v_cache, k, v, w, beta, ws=None):
     for name, x in (("k", k), ("v", v), ("w", w)):
         _need(x, k_cache.dtype, (B, H, L, d), name)
     _need(beta, torch.float32, (B, H, L), "beta")
+    if (log_f is None) != (a_cache is None):
+        raise ValueError("log_f and a_cache go together")
+    if log_f is not None:
+        _need(log_f, torch.float32, (B, H, L), "log_f")
+        _need(a_cache, torch.float32, (B, H, cap), "a_cache")
     n = path_decode_prefill_workspace_size(desc, L)
     if n == 0:
         raise RuntimeError("invalid decode descriptor or prompt length")
     if ws is None:
         ws = torch.empty(n, dtype=torch.uint8, device=k_cache.device)
-    rc = path_decode_prefill(desc, _p(k_cache), _p(v_cache), L, _p(k), _p(v), _p(w), _p(beta), _p(ws), ws.numel(),
-                             _stream())
+    rc = path_decode_prefill(desc, _p(k_cache), _p(v_cache), L, _p(k), _p(v), _p(w), _p(beta), _p(log_f),
+                             _p(a_cache), _p(ws), ws.numel(), _stream())
     _check(rc, "path_decode_prefill")
+
+
+def decode_step_fox(k_cache, v_cache, a_cache, t, q_t, k_t, v_t, w_t, beta_t, log_f_t, scale=1.0, ws=None, out=None):
+    """One PaTH-FoX decode step at position t (in place on the caches and the forget-gate prefix
+    cache a_cache [B,H,cap] fp32); returns o_t [B,H,d]."""
+    desc = make_decode_desc(k_cache, scale)
+    B, H, cap, d = k_cache.shape
+    _need(v_cache, k_cache.dtype, k_cache.shape, "v_cache")
+    _need(a_cache, torch.float32, (B, H, cap), "a_cache")
+    for name, x in (("q_t", q_t), ("k_t", k_t), ("v_t", v_t), ("w_t", w_t)):
+        _need(x, k_cache.dtype, (B, H, d), name)
+    _need(beta_t, torch.float32, (B, H), "beta_t")
+    _need(log_f_t, torch.float32, (B, H), "log_f_t")
+    if ws is None:
+        ws = decode_workspace(desc, k_cache.device)
+    o = torch.empty_like(q_t) if out is None else out
+    rc = path_decode_step_fox(desc, _p(k_cache), _p(v_cache), _p(a_cache), t, _p(q_t), _p(k_t), _p(v_t), _p(w_t),
+                              _p(beta_t), _p(log_f_t), _p(o), _p(ws), ws.numel(), _stream())
+    _check(rc, "path_decode_step_fox")
+    return o

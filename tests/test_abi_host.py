@@ -141,16 +141,30 @@ def test_prefill_argument_errors(pa):
     assert pa.path_decode_prefill_workspace_size(dd, 0) > 0            # an empty prompt is valid
     assert pa.path_decode_prefill_workspace_size(dd, 101) == 0         # longer than the cache
     assert pa.path_decode_prefill_workspace_size(dd, -1) == 0
-    vec = [FAKE] * 4
+    vec = [FAKE] * 4 + [None, None]
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 101, *vec, FAKE, n, None) == 4   # prompt > capacity
     assert pa.path_decode_prefill(dd, FAKE, FAKE, -1, *vec, FAKE, n, None) == 1
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec, FAKE, n - 1, None) == 3
     assert pa.path_decode_prefill(dd, None, FAKE, 70, *vec, FAKE, n, None) == 1
-    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, FAKE, FAKE, FAKE, None, FAKE, n, None) == 1
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, FAKE, FAKE, FAKE, None, None, None, FAKE, n, None) == 1
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec[:4], FAKE, None, FAKE, n, None) == 1  # log_f alone
+    assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec[:4], None, FAKE, FAKE, n, None) == 1  # a_cache alone
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 0, *vec, FAKE, n, None) == 0     # nothing to do
     bad = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
     assert pa.path_decode_prefill_workspace_size(bad, 10) == 0
     assert pa.path_decode_prefill(bad, FAKE, FAKE, 10, *vec, FAKE, n, None) == 2
+
+
+def test_fox_decode_argument_errors(pa):
+    dd = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_BF16, 1.0)
+    n = pa.path_decode_workspace_size(dd)
+    vec = [FAKE] * 7
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, FAKE, 100, *vec, FAKE, n, None) == 4     # t + 1 > capacity
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, FAKE, -1, *vec, FAKE, n, None) == 1
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, FAKE, 5, *vec, FAKE, n - 1, None) == 3
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, None, 5, *vec, FAKE, n, None) == 1      # no prefix cache
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, FAKE, 5, *vec[:6], None, FAKE, n, None) == 1  # no o_t
+    assert pa.path_decode_step_fox(dd, FAKE, FAKE, FAKE, 5, *vec[:5], None, FAKE, FAKE, n, None) == 1  # no log f
 
 
 def test_torch_wrapper_rejects_bad_tensors(pa):

@@ -313,3 +313,54 @@ def test_prefill_then_decode_matches_forward(cuda_lib, dtype, L):
             check(flat(o), o_ref[:, pos], 1e-4, f"o[{pos}]")
         else:
             check(flat(o), o_ref[:, pos], 2e-2, f"o[{pos}]", rel=2e-2)
+
+
+# ---------------- PaTH-FoX decode ----------------
+
+@pytest.mark.parametrize("dtype,t0,steps,tol", [("fp32", 0, 30, 1e-4), ("fp32", 3000, 5, 1e-4), ("bf16", 2000, 5, 2e-2)])
+def test_fox_decode_steps(cuda_lib, dtype, t0, steps, tol):
+    """Forget-gate decode against the oracle step by step (outputs, rewritten keys, prefix cache)."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    di = gen_decode_inputs(1, 3, 64, t0=t0, steps=steps, dtype=dtype, seed=71 + t0, fox=True)
+    kc, vc, ac = di["k_cache"].to(DEV), di["v_cache"].to(DEV), di["a_cache"].to(DEV)
+    kref, vref = np64(flat(di["k_cache"])).copy(), np64(flat(di["v_cache"])).copy()
+    aref = np64(flat(di["a_cache"])).copy()
+    for s in range(steps):
+        x = {n: di[n][s].to(DEV) for n in ("q", "k", "v", "w", "beta", "log_f")}
+        o = pa.decode_step_fox(kc, vc, ac, t0 + s, x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], scale=1.0)
+        torch.cuda.synchronize()
+        o_r = orc.decode_step_fox(kref, vref, aref, t0 + s, *(flat(di[n][s]) for n in ("q", "k", "v", "w", "beta")),
+                                  flat(di["log_f"][s]), 1.0)
+        check(flat(o), o_r, tol, f"o[{s}]", rel=2e-2 if dtype == "bf16" else None)
+    n = t0 + steps
+    check(flat(kc)[:, :n], kref[:, :n], tol, "k_cache")
+    check(flat(ac)[:, :n], aref[:, :n], 1e-3, "a_cache")
+
+
+@pytest.mark.parametrize("dtype,L", [("fp32", 130), ("bf16", 300)])
+def test_fox_prefill_then_decode_matches_forward(cuda_lib, dtype, L):
+    """Hand off L FoX prompt tokens (keys and forget-gate prefix sums), decode four more: each
+    output equals the FoX forward oracle's row."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    steps = 4
+    inp = gen_path_inputs(1, 2, L + steps, 64, dtype, seed=700 + L, near2_frac=0.05, fox=True)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    kc = torch.zeros(1, 2, L + steps, 64, dtype=tdt, device=DEV)
+    vc = torch.zeros_like(kc)
+    ac = torch.zeros(1, 2, L + steps, dtype=torch.float32, device=DEV)
+    t = {n: inp[n].to(DEV) for n in ("q", "k", "v", "w", "beta", "log_f")}
+    head = {n: t[n][:, :, :L].contiguous() for n in ("k", "v", "w", "beta", "log_f")}
+    pa.decode_prefill(kc, vc, head["k"], head["v"], head["w"], head["beta"], log_f=head["log_f"], a_cache=ac)
+    o_ref, _ = orc.fwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]),
+                       flat(inp["log_f"]), 0.8)
+    for s in range(steps):
+        pos = L + s
+        o = pa.decode_step_fox(kc, vc, ac, pos, *(t[n][:, :, pos].contiguous() for n in ("q", "k", "v", "w", "beta",
+                                                                                           "log_f")), scale=0.8)
+        torch.cuda.synchronize()
+        if dtype == "fp32":
+            check(flat(o), o_ref[:, pos], 1e-4, f"o[{pos}]")
+        else:
+            check(flat(o), o_ref[:, pos], 2e-2, f"o[{pos}]", rel=2e-2)
