@@ -444,12 +444,35 @@ def run_decode(args, pa, dev, rank, ws, pk):
     total_ms = max_over_ranks(sum(per), ws)
     nbytes = sum(Bt * H * 3 * (t0 + s) * d * 2 for s in range(steps))
     gbs = ws * nbytes / (total_ms * 1e-3) / 1e9
+
+    # PaTH-FoX decode on the same cache: forget-gate prefix sums of the cached rows and a log f per
+    # step (drawn on the device: log sigmoid(N(2, 1))), restored cache, same steps
+    kc.copy_(kc0)
+    vc.copy_(vc0)
+    g = torch.Generator(device=dev).manual_seed(cfg["seed"] + 13)
+    logf = lambda *shape: torch.nn.functional.logsigmoid(torch.randn(*shape, device=dev, generator=g) + 2.0)
+    ac = torch.zeros(Bt, H, kc.shape[2], device=dev)
+    ac[:, :, :t0] = torch.cumsum(logf(Bt, H, t0).double(), dim=2).float()
+    lf = logf(steps, Bt, H)
+    torch.cuda.synchronize()
+    fmarks = [ev()]
+    for s in range(steps):
+        pa.decode_step_fox(kc, vc, ac, t0 + s, *(sx[n][s] for n in ("q", "k", "v", "w", "beta")), lf[s],
+                           scale=cfg["scale"], ws=wsd, out=o)
+        fmarks.append(ev())
+    torch.cuda.synchronize()
+    fox_ms = max_over_ranks(sum(fmarks[i].elapsed_time(fmarks[i + 1]) for i in range(steps)), ws)
+    fox_bytes = nbytes + sum(Bt * H * (t0 + s) * 4 for s in range(steps))  # + the prefix cache
+    fox_gbs = ws * fox_bytes / (fox_ms * 1e-3) / 1e9
     return {"value": gbs, "unit": "GB/s", "tokens_per_s": ws * Bt * steps / (total_ms * 1e-3),
             "ms_per_step": total_ms / steps, "steps": steps, "frac_of_hbm": gbs / ws / pk["hbm"],
             "roofline": {"kernel": "decode step (split + combine)", "bound": "hbm", "achieved": gbs / ws,
                          "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / ws / pk["hbm"], "traffic": None},
             "clocks": crec, "gpu_launches": 2 * steps,
-            "workload": "decode, batch 32, 32 heads, d=64, cache 32768 -> 33023 bf16, 256 steps"}
+            "workload": "decode, batch 32, 32 heads, d=64, cache 32768 -> 33023 bf16, 256 steps",
+            "fox": {"value": fox_gbs, "unit": "GB/s", "ms_per_step": fox_ms / steps,
+                    "frac_of_hbm": fox_gbs / ws / pk["hbm"], "gpu_launches": 2 * steps,
+                    "workload": "PaTH-FoX decode, same cache and steps, forget-gate prefix sums beside the cache"}}
 
 
 def run_prefill_handoff(args, pa, dev, pk):

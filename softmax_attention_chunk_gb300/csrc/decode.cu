@@ -103,15 +103,15 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
   // Trip count is uniform over the CTA so that every lane reaches the group shuffles.
   for (int base = j0; base < j1; base += GROUPS * UNROLL) {
     Vec8<T> kv[UNROLL], vv[UNROLL];
-    float bias[UNROLL];  // forget-gate bias of the key, log2 domain (FOX)
+    float aj[UNROLL];  // prefix sums a_j of the keys (FOX), used once the key is consumed
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int j = base + grp + u * GROUPS;
-      bias[u] = 0.f;
+      aj[u] = 0.f;
       if (j < t) {
         kv[u].load(kc + (hrow + j) * D + e0);
         vv[u].load(vc + (hrow + j) * D + e0);
-        if constexpr (FOX) bias[u] = (At - ac[hrow + j]) * kLog2e;
+        if constexpr (FOX) aj[u] = ac[hrow + j];
       } else if (j == t) {
         kv[u].load(kt + (size_t)bh * D + e0);
         vv[u].load(vt + (size_t)bh * D + e0);
@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
           Vec8<T> kn;
           kn.from_float(kf);
           kn.store(kc + (hrow + j) * D + e0);
-          s = (qk - ba * qw) * scl + bias[u];
+          s = (qk - ba * qw) * scl;
+          if constexpr (FOX) s += (At - aj[u]) * kLog2e;
         } else {  // j == t: append the new key and value unchanged
           kv[u].store(kc + (hrow + j) * D + e0);
           vv[u].store(vc + (hrow + j) * D + e0);
