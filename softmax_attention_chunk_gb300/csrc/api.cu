@@ -159,14 +159,20 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
   CHECK_PTR(q); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta); CHECK_PTR(o);
   CHECK_PTR(lse); CHECK_PTR(dO); CHECK_PTR(dq); CHECK_PTR(dk); CHECK_PTR(dv); CHECK_PTR(dw);
   CHECK_PTR(dbeta);
-  if (log_f || dlog_f) return PATH_ERR_UNSUPPORTED;
+  if (dlog_f && !log_f) return PATH_ERR_INVALID_ARG;
+  if (log_f && !aligned(log_f, 16)) return PATH_ERR_INVALID_ARG;
+  if (dlog_f && !aligned(dlog_f, 16)) return PATH_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
   if (uses_tensor_cores(desc, 1)) {
+    // PaTH-FoX: the tensor-core backward takes the forget gate (dlog f needs a nonzero scale: the
+    // logit gradient is recovered from the scaled one)
+    if (log_f && desc->scale == 0.f) return PATH_ERR_UNSUPPORTED;
     const TcWs tw = tc_layout(desc, true);
     if (ws_bytes < tw.total) return PATH_ERR_WORKSPACE;
     return cuda_status(launch_bwd_tc(tw, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, (char*)ws, phases,
-                                     (cudaStream_t)stream));
+                                     (cudaStream_t)stream, log_f, dlog_f));
   }
+  if (log_f || dlog_f) return PATH_ERR_UNSUPPORTED;  // the fp32 path has no forget-gate backward
   const BwdWs lay = bwd_ws_layout(g);
   if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,

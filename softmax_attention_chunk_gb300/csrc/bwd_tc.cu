@@ -206,6 +206,7 @@ struct __align__(1024) BsSmem {
       zempty[BS_ZSTAGE];
   uint64_t do_full, sp_full, sp_free, ps_ready, g_full, gs_ready, acc_full, dkf_free, dv_free[2];
   uint32_t tmem_base;
+  alignas(16) float fxa[BS_KSTAGE][BK];  // PaTH-FoX: prefix sums A_j of the stage's key chunk
 };
 
 struct BsParams {
@@ -219,6 +220,8 @@ struct BsParams {
   float* dv;    // [BH][Lp][64]  dV   (accumulated)
   float* df;    // [BH][nc][64][64] dF (accumulated)
   int* err;
+  const float* fxa;  // PaTH-FoX: A_i = sum_{s<=i} log f_s        [BH][Lp]
+  float* fxcs;       // PaTH-FoX: column sums of dS' (accumulated) [BH][Lp]
 };
 
 // 32 fp32 values as row r of a 128-byte swizzled fp32 box.
@@ -264,6 +267,25 @@ __device__ __forceinline__ void pack_row_pairs(const float* x, uint32_t (&pk)[32
 // issue from one thread and these products are small (N = 64).
 constexpr int BS_THREADS = 480;
 constexpr int BS_NSOFT = 256;
+
+// Column sums over the warp's 32 rows of the 32 values each lane holds (its row's columns):
+// a reduce-scatter butterfly; on return v[0] of lane l is the sum of column l.
+__device__ __forceinline__ void warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < o; ++j) {
+      const float send = up ? v[j] : v[j + o];
+      const float keep = up ? v[j + o] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
+// FOX (PaTH-FoX, notes §2.5): the logit of (i, j) gains A_i - A_j; the column sums of the
+// step's dS' = P (dP - D) are added into fxcs for dlog f.
+template <bool FOX>
 __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_do,
                                                             const __grid_constant__ CUtensorMap tm_kr,
                                                             const __grid_constant__ CUtensorMap tm_v,
@@ -327,9 +349,10 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         if (k >= BS_KSTAGE && !mbar_wait(&s.empty[si], ((k / BS_KSTAGE) - 1) & 1, p.err, 21)) break;
         const int c = step_chunk(has_partial, T, nsteps - 1 - k);
         BsStage& S = s.st[si];
-        mbar_arrive_expect_tx(&s.full[si], 2 * BK * 128);
+        mbar_arrive_expect_tx(&s.full[si], 2 * BK * 128 + (FOX ? BK * 4 : 0));
         tma_load_2d(S.kr, &tm_kr, 0, bh * p.Lp + c * BK, &s.full[si]);
         tma_load_2d(S.f, &tm_f, 0, (bh * p.nc + c) * D, &s.full[si]);
+        if constexpr (FOX) bulk_load(s.fxa[si], p.fxa + (size_t)bh * p.Lp + (size_t)c * BK, BK * 4, &s.full[si]);
       }
     } else if (lane == 8) {  // V_c
       for (int k = 0; k < nsteps; ++k) {
@@ -456,6 +479,10 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
     const size_t wrow = (size_t)bh * p.Lp + (size_t)T * BQ + r;
     const float lse2 = grow < p.L ? p.lse[(size_t)bh * p.L + grow] * kLog2e : INFINITY;
     const float Dr = p.Dv[wrow];
+    // FOX: exponent offset of the row, A_i log2(e) - lse_i log2(e); the keys' -A_j log2(e) per step
+    const float fox_row = FOX ? p.fxa[wrow] * kLog2e - lse2 : 0.f;
+    const float inv_scale = FOX ? 1.f / p.scale : 0.f;
+    float fox_rowsum = 0.f;  // FOX: this thread's share of its row's sum of dS' (scaled)
     const int vrow = 16 * q4 + (lane & 15), vh = lane >> 4;  // dV (M=64): row, column half
     // dV of step j (complete) -> columns 16h.. of the fp32 boxes 4, 5 -> two tensor reductions
     // issued by thread 0 (its own bulk groups: each waits for the previous one to have read the
@@ -494,11 +521,31 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       tc_fence_before();
       mbar_arrive(&s.sp_free);  // S and dP of step k may be overwritten
       float pv[32], dsv[32];
+      if constexpr (FOX) {
+        // the stage of this step's chunk holds its A_j (its barrier completed before S was issued)
+        const int si = k % BS_KSTAGE;
+        ok = ok && mbar_wait(&s.full[si], (k / BS_KSTAGE) & 1, p.err, 39);
+        const float4* a4 = reinterpret_cast<const float4*>(s.fxa[si] + 32 * h);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
-        pv[j] = p0;
-        dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+        for (int q = 0; q < 8; ++q) {
+          const float4 av = a4[q];
+          const float aj[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * q + e;
+            const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, fmaf(-aj[e], kLog2e, fox_row)))
+                                    : 0.f;
+            pv[j] = p0;
+            dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
+          pv[j] = p0;
+          dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+        }
       }
       uint32_t pk[16];
 #pragma unroll
@@ -514,11 +561,19 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ps_ready);
+      if constexpr (FOX) {  // row sum of dS' kept; column sums over this warp's 32 rows into fxcs
+#pragma unroll
+        for (int j = 0; j < 32; ++j) fox_rowsum += dsv[j];
+        warp_column_sums(dsv, lane);
+        atomicAdd(p.fxcs + (size_t)bh * p.Lp + (size_t)step_chunk(has_partial, T, n) * BK + 32 * h + lane,
+                  dsv[0] * inv_scale);
+      }
       if (k > 0) stage_dv(k - 1);
     }
     ok = ok && mbar_wait(&s.acc_full, (nsteps - 1) & 1, p.err, 26);
     tc_fence_after();
     stage_dv(nsteps - 1);
+    if constexpr (FOX) atomicAdd(p.fxcs + wrow, -fox_rowsum * inv_scale);  // fxcs_m = colsum_m - rowsum_m
     if (tid == 0) bulk_wait0();
   } else if (warp >= 6) {
     // ---------------- gradient side: thread owns query row rg = 32 (warp % 4) + lane ----------------
@@ -635,7 +690,8 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
 
 cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
                           const float* beta, const void* o, const float* lse, const void* dO, void* dq, void* dk,
-                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st) {
+                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st, const float* logf,
+                          float* dlogf) {
   cudaError_t e;
   const Geom& g = w.g64;
   const size_t rows = (size_t)g.BH * g.Lp;
@@ -647,6 +703,10 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaMemsetAsync(ws + w.df64, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
     if ((e = launch_bwd_dot(g, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
+    if (logf) {  // PaTH-FoX: prefix sums of log f, zeroed column sums of dS'
+      if ((e = launch_fox_prefix(g, logf, (float*)(ws + w.fxa), st)) != cudaSuccess) return e;
+      if ((e = cudaMemsetAsync(ws + w.fxcs, 0, rows * 4, st)) != cudaSuccess) return e;
+    }
     if (!(phases & 8)) {  // 8: the forward's chunk-64 preparation is already in ws
       if ((e = launch_ut_prep64(w.g64, q, k, v, wv, beta, nullptr, ws, w.p64, false, st)) != cudaSuccess) return e;
     }
@@ -688,18 +748,22 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     bp.dv = (float*)(ws + w.dv);
     bp.df = (float*)(ws + w.df64);
     bp.err = err;
+    bp.fxa = logf ? (const float*)(ws + w.fxa) : nullptr;
+    bp.fxcs = logf ? (float*)(ws + w.fxcs) : nullptr;
     const size_t smem = sizeof(BsSmem) + 1024;
-    if ((e = cudaFuncSetAttribute(bwd_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+    auto kern = logf ? bwd_scan_tc_kernel<true> : bwd_scan_tc_kernel<false>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return e;
-    bwd_scan_tc_kernel<<<(unsigned)((long)nt * g.BH), BS_THREADS, smem, st>>>(m_do, m_kr, m_v, m_f, m_rdk, m_rdv,
-                                                                                m_rdf, bp);
+    kern<<<(unsigned)((long)nt * g.BH), BS_THREADS, smem, st>>>(m_do, m_kr, m_v, m_f, m_rdk, m_rdv, m_rdf, bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {
+    float* cs = logf ? (float*)(ws + w.fxcs) : nullptr;
     if ((e = launch_ut_bwd64(g, q, k, v, wv, beta, lse, dO, (const float*)(ws + w.Dv), (const float*)(ws + w.dql64),
                              (const float*)(ws + w.dkr64), (const float*)(ws + w.dv), (const float*)(ws + w.df64), dq,
-                             dk, dv, dw, dbeta, err, st)) != cudaSuccess)
+                             dk, dv, dw, dbeta, err, st, logf, cs)) != cudaSuccess)
       return e;
+    if (dlogf && (e = launch_fox_dlogf(g, cs, dlogf, st)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }

@@ -102,6 +102,7 @@ struct TcWs {
   size_t Dv;                       // D_i                                [BH][Lp]
   size_t dql64, dkr64, dv, df64;   // chunk-64 gradients (fp32; dkr64/dv/df64 accumulate)
   size_t zs;                       // transported queries Z, bf16 swizzled 128x64 tiles
+  size_t fxa, fxcs;                // PaTH-FoX: prefix sums of log f, column sums of dS' [BH][Lp]
   size_t total;
 };
 
@@ -133,6 +134,8 @@ inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
     w.df64 = take((size_t)BH * w.g64.nc * kHeadDim * kHeadDim * 4);
     // tile T of a head has at most 2T+1 steps: sum over tiles <= nt^2 tiles of 16 KB
     w.zs = take((size_t)BH * nt * nt * 128 * 128);
+    w.fxa = take(rows * 4);
+    w.fxcs = take(rows * 4);
   }
   w.total = off;
   return w;
@@ -143,6 +146,11 @@ inline size_t decode_ws_bytes(int BH) {
 }
 
 // ---- launchers (return cudaGetLastError() of their launches) ----
+
+// PaTH-FoX backward helpers (one CTA per head): A[bh][i] = sum_{s<=i} log f_s over [0, Lp) (rows
+// >= L keep the total), and dlog f_s = -sum_{m>=s} cs[bh][m] for s < L.
+cudaError_t launch_fox_prefix(const Geom& g, const float* logf, float* A, cudaStream_t st);
+cudaError_t launch_fox_dlogf(const Geom& g, const float* cs, float* dlogf, cudaStream_t st);
 
 // SIMT (fp32 arithmetic) forward.  is_bf16 selects the input element type.
 cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
@@ -188,13 +196,15 @@ cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* 
 cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                             const float* beta, const float* lse, const void* dO, const float* Dv, const float* dql,
                             const float* dkr, const float* dvacc, const float* df, void* dq, void* dk, void* dv,
-                            void* dw, float* dbeta, int* err, cudaStream_t st);
+                            void* dw, float* dbeta, int* err, cudaStream_t st, const float* logf = nullptr,
+                            float* fxcs = nullptr);
 // Tensor-core backward (bf16).  phases: 1 = prepare (accumulators, D_i, chunk-32 UT quantities,
 // chunk-64 merge, Z chain), 2 = adjoint scan, 4 = chunk conversion + UT backward; with bit 8
 // the prepare phase keeps the forward's preparation found in ws.
 cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const void* v, const void* wv,
                           const float* beta, const void* o, const float* lse, const void* dO, void* dq, void* dk,
-                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st);
+                          void* dv, void* dw, float* dbeta, char* ws, int phases, cudaStream_t st, const float* logf = nullptr,
+                          float* dlogf = nullptr);
 
 // Decode step.
 // ac / logf_t (PaTH-FoX, both set or both null): prefix sums of log f beside the cache

@@ -68,6 +68,7 @@ struct __align__(1024) UbSmem {
   float beta[B], lse2[B], dv[B], gb[B];
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
+  float pre[B];  // PaTH-FoX: chunk-local inclusive prefix of log f
 };
 
 struct UbParams {
@@ -86,8 +87,13 @@ struct UbParams {
   __nv_bfloat16* dw;
   float* dbeta;
   int* err;
+  const float* logf;  // PaTH-FoX: log f [BH][L]
+  float* fxcs;        // PaTH-FoX: column sums of dS' (accumulated) [BH][Lp]
 };
 
+// FOX (PaTH-FoX, notes §2.5): the diagonal logits gain pre_i - pre_j (chunk-local prefix sums of
+// log f) and the column sums of the chunk's dS' are added into fxcs.
+template <bool FOX>
 __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v,
@@ -159,6 +165,24 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     s.beta[tid] = ok ? clamp_beta(p.beta[in_row + gi]) : 0.f;
     s.lse2[tid] = ok ? p.lse[in_row + gi] * kLog2e : INFINITY;
     s.dv[tid] = p.Dv[ws_row + tid];
+  }
+  if constexpr (FOX) {
+    if (warp == 3) {  // chunk-local inclusive prefix of log f
+      const int ga = row0 + lane, gb2 = row0 + 32 + lane;
+      float a = ga < p.L ? p.logf[in_row + ga] : 0.f;
+      float b2 = gb2 < p.L ? p.logf[in_row + gb2] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float ta = __shfl_up_sync(0xffffffffu, a, o), tb2 = __shfl_up_sync(0xffffffffu, b2, o);
+        if (lane >= o) {
+          a += ta;
+          b2 += tb2;
+        }
+      }
+      const float tot_a = __shfl_sync(0xffffffffu, a, 31);
+      s.pre[lane] = a;
+      s.pre[32 + lane] = b2 + tot_a;
+    }
   }
   mbar_wait(&s.bar_in, 0, p.err, 41);
   publish();
@@ -269,14 +293,39 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     ld_half(tb, lane_off, C3, sx);
     ld_half(tb, lane_off, C2, dp);
     const float l2 = s.lse2[i], dvi = s.dv[i];
+    const float fox_i = FOX ? s.pre[i] * kLog2e - l2 : -l2;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      const float pj = (32 * h + j <= i && row_ok) ? fast_exp2(sx[j] * p.scl - l2) : 0.f;
+      const float off = FOX ? fmaf(-s.pre[32 * h + j], kLog2e, fox_i) : fox_i;
+      const float pj = (32 * h + j <= i && row_ok) ? fast_exp2(fmaf(sx[j], p.scl, off)) : 0.f;
       sx[j] = pj;
       dp[j] = p.scale * pj * (dp[j] - dvi);
     }
     put_half(s.t[S_P], i, h, sx);
     put_half(s.t[S_DS], i, h, dp);
+    if constexpr (FOX) {
+      // the row's sum of dS' (this half) leaves fxcs_i = colsum_i - rowsum_i ...
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rs += dp[j];
+      atomicAdd(p.fxcs + ws_row + i, -rs / p.scale);
+      // ... and the column sums of dS' over the half-warp's 16 rows (reduce-scatter: lane l keeps
+      // columns 2 (l % 16), 2 (l % 16) + 1 of its half) are added
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < 2 * o; ++j) {
+          const float send = up ? dp[j] : dp[j + 2 * o];
+          const float keep = up ? dp[j + 2 * o] : dp[j];
+          dp[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      const float inv_scale = 1.f / p.scale;
+      float* cs = p.fxcs + ws_row + 32 * h + 2 * (lane & 15);
+      atomicAdd(cs, dp[0] * inv_scale);
+      atomicAdd(cs + 1, dp[1] * inv_scale);
+    }
   }
   publish();
 
@@ -455,7 +504,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
 cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                             const float* beta, const float* lse, const void* dO, const float* Dv, const float* dql,
                             const float* dkr, const float* dvacc, const float* df, void* dq, void* dk, void* dv,
-                            void* dw, float* dbeta, int* err, cudaStream_t st) {
+                            void* dw, float* dbeta, int* err, cudaStream_t st, const float* logf, float* fxcs) {
   if (g.B != 64) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv, mw, mdo;
   if (!make_map_head_rows64(&mq, q, g.L, g.BH) || !make_map_head_rows64(&mk, k, g.L, g.BH) ||
@@ -482,13 +531,16 @@ cudaError_t launch_ut_bwd64(const Geom& g, const void* q, const void* k, const v
   p.dw = (__nv_bfloat16*)dw;
   p.dbeta = dbeta;
   p.err = err;
+  p.logf = logf;
+  p.fxcs = fxcs;
   const size_t smem = sizeof(UbSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(ut_bwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = logf ? ut_bwd64_kernel<true> : ut_bwd64_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ut_bwd64_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  ut_bwd64_kernel<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, mdo, p);
+  kern<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, mdo, p);
   return cudaGetLastError();
 }
 

@@ -205,7 +205,8 @@ def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None, pha
 
 def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, out=None,
         phases=PATH_BWD_ALL):
-    """Gradients dict dq, dk, dv, dw (dtype of q) and dbeta (float32)."""
+    """Gradients dict dq, dk, dv, dw (dtype of q) and dbeta (float32); with log_f (PaTH-FoX) also
+    dlog_f (float32)."""
     desc = make_desc(q, scale, chunk)
     for name, t in (("k", k), ("v", v), ("w", w), ("o", o), ("dO", dO)):
         _need(t, q.dtype, q.shape, name)
@@ -213,12 +214,16 @@ def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, o
     _need(lse, torch.float32, q.shape[:3], "lse")
     if ws is None:
         ws = workspace(desc, 1, q.device)
+    if log_f is not None:
+        _need(log_f, torch.float32, q.shape[:3], "log_f")
     if out is None:
         out = dict(dq=torch.empty_like(q), dk=torch.empty_like(q), dv=torch.empty_like(q),
                    dw=torch.empty_like(q), dbeta=torch.empty_like(beta))
+        if log_f is not None:
+            out["dlog_f"] = torch.empty_like(beta)
     rc = path_attn_bwd_phases(phases, desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse),
                               _p(dO), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dw"]),
-                              _p(out["dbeta"]), None, _p(ws), ws.numel(), _stream())
+                              _p(out["dbeta"]), _p(out.get("dlog_f")), _p(ws), ws.numel(), _stream())
     _check(rc, "path_attn_bwd")
     return out
 

@@ -109,10 +109,14 @@ def test_bwd_argument_errors(pa):
     # order: q,k,v,w,beta,log_f,o,lse,dO,dq,dk,dv,dw,dbeta,dlog_f,ws,ws_bytes,stream
     base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE]
     assert pa.path_attn_bwd(d, *base, n - 1, None) == 3
-    with_logf = list(base); with_logf[5] = FAKE
-    assert pa.path_attn_bwd(d, *with_logf, n, None) == 2   # forget-gate gradient unsupported
+    # forget gate: dlog f without log f is an argument error; the fp32 path and a zero scale have
+    # no forget-gate backward (every check runs before any launch: the pointers here are fake)
     with_dlogf = list(base); with_dlogf[14] = FAKE
-    assert pa.path_attn_bwd(d, *with_dlogf, n, None) == 2
+    assert pa.path_attn_bwd(d, *with_dlogf, n, None) == 1
+    with_logf = list(base); with_logf[5] = FAKE
+    assert pa.path_attn_bwd(d, *with_logf, n, None) == 2  # d is an fp32 descriptor
+    d0 = pa.path_attn_desc_t(d.batch, d.heads, d.seqlen, d.head_dim, pa.PATH_BF16, 0.0, d.chunk)
+    assert pa.path_attn_bwd(d0, *with_logf, pa.path_attn_workspace_size(d0, 1), None) == 2
     null_dw = list(base); null_dw[12] = None
     assert pa.path_attn_bwd(d, *null_dw, n, None) == 1
     assert pa.path_attn_bwd_phases(8, d, *base, n, None) == 1

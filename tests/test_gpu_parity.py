@@ -167,7 +167,8 @@ def test_fwd_bf16_more_heads_than_a_schedule_group(cuda_lib):
     check(flat(lse), lse_ref, 2e-2, "lse")
 
 
-def test_bwd_rejects_forget_gate(cuda_lib):
+def test_fp32_bwd_rejects_forget_gate(cuda_lib):
+    """The fp32 (SIMT) backward has no forget-gate gradient: it refuses log_f."""
     from softmax_attention_chunk_gb300 import path_attn as pa
 
     inp = gen_path_inputs(1, 1, 64, 64, "fp32", seed=3, with_dO=True, fox=True)
@@ -364,3 +365,45 @@ def test_fox_prefill_then_decode_matches_forward(cuda_lib, dtype, L):
             check(flat(o), o_ref[:, pos], 1e-4, f"o[{pos}]")
         else:
             check(flat(o), o_ref[:, pos], 2e-2, f"o[{pos}]", rel=2e-2)
+
+
+
+# ---------------- PaTH-FoX backward (bf16 tensor-core path) ----------------
+
+def check_grads_fox(inp, g, scale, tol, rel):
+    ref = orc.bwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]),
+                  flat(inp["log_f"]), scale, flat(inp["dO"]), want_dlogf=True)
+    for key in ("dq", "dk", "dv", "dw", "dbeta", "dlog_f"):
+        r = ref[key]
+        check(flat(g[key]), r, tol * max(1.0, np.abs(r).max()), key, rel=rel)
+
+
+@pytest.mark.parametrize("L", [1, 64, 65, 200, 333])
+def test_bwd_bf16_fox(cuda_lib, L):
+    """Forget-gate backward: every gradient including dlog f against the oracle (whose dlog f is
+    pinned by finite differences)."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(2, 2, L, 64, "bf16", seed=800 + L, with_dO=True, near2_frac=0.05, fox=True)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=1.0)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=1.0, log_f=t["log_f"])
+    torch.cuda.synchronize()
+    check_grads_fox(inp, g, 1.0, 2e-2, 3e-2)
+
+
+def test_bwd_bf16_fox_training_step_reuse(cuda_lib):
+    """Forget gate through the training-step path: the forward stores the transported queries and
+    the backward reuses them and the preparation."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(2, 9, 300, 64, "bf16", seed=901, with_dO=True, near2_frac=0.05, fox=True)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    desc = pa.make_desc(t["q"], 0.7)
+    ws = pa.workspace(desc, 1, DEV)
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], 0.7, ws=ws,
+                    phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], 0.7, ws=ws, log_f=t["log_f"],
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
+    torch.cuda.synchronize()
+    check_grads_fox(inp, g, 0.7, 2e-2, 3e-2)
