@@ -111,8 +111,10 @@ int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, co
  * the per-chunk UT quantities.
  *
  * dq,dk,dv,dw: desc dtype outputs (overwritten).  dbeta: float32 (overwritten).
- * log_f and dlog_f must be NULL (the forget-gate gradient is not implemented:
- * PATH_ERR_UNSUPPORTED otherwise).
+ * PaTH-FoX (forget gate, notes §2.5): pass the forward's log_f; dlog_f (float32, same shape,
+ * may be NULL) receives dL/dlog f.  dlog_f without log_f is PATH_ERR_INVALID_ARG.  The forget-gate
+ * backward runs on the bf16 tensor-core path only (fp32 descriptors, and scale == 0, return
+ * PATH_ERR_UNSUPPORTED).
  * ws: at least path_attn_workspace_size(desc, 1) bytes.
  */
 int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,
