@@ -338,6 +338,28 @@ def run_ours(args):
                 "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                 "peak_source": (f"bf16 dense ({pk['src']})" if d["bound"] == "tensor" else f"HBM copy ({pk['src']})")}
 
+    # PaTH-FoX training step on the same inputs plus a forget gate (log f = log sigmoid(N(2, 1)),
+    # drawn on the device): forward with the forget bias, backward with dlog f
+    gf = torch.Generator(device=dev).manual_seed(cfg["seed"] + 17)
+    log_f = torch.nn.functional.logsigmoid(torch.randn(beta.shape, device=dev, generator=gf) + 2.0)
+    dlog_f = torch.empty_like(log_f)
+    fox_out = dict(grads, dlog_f=dlog_f)
+    fx = []
+    for i in range(args.warmup + args.steps):
+        a = ev()
+        pa.fwd(q, k, v, w, beta, log_f, cfg["scale"], ws=ws_b, out=(o, lse), phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z)
+        pa.bwd(q, k, v, w, beta, o, lse, dO, cfg["scale"], ws=ws_b, log_f=log_f, out=fox_out,
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
+        b = ev()
+        if i >= args.warmup:
+            fx.append((a, b))
+    torch.cuda.synchronize()
+    fox_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in fx), ws)
+    fox_train = {"ms_per_step": fox_ms, "tflops": ws * flops_step / (fox_ms * 1e-3) / 1e12,
+                 "frac_of_bf16_peak": flops_step / (fox_ms * 1e-3) / 1e12 / pk["bf16"],
+                 "note": "PaTH-FoX training step (forget gate; dlog f included), same workload, same flop count"}
+    del log_f, dlog_f, fox_out
+
     # the forward on its own (inference: no transported-query store), against the bf16 peak
     fw = []
     for i in range(args.warmup + args.steps):
@@ -435,7 +457,8 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (6 x 512 MiB per step)"},
                 "frac_of_bf16_peak": value / ws / pk["bf16"],
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
-                "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward, "e2e": e2e,
+                "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward,
+                "fox_train": fox_train, "e2e": e2e,
                 "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 5 * args.steps,
                 "peaks": pk, "decode": dec, "prefill_handoff": handoff, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
