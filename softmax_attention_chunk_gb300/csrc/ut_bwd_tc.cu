@@ -69,6 +69,7 @@ struct __align__(1024) UbSmem {
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
   float pre[B];  // PaTH-FoX: chunk-local inclusive prefix of log f
+  uint64_t bar_mma2;  // the second issuer's commits (phases whose MMAs two threads issue)
 };
 
 struct UbParams {
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   if (lead) {
     mbar_init(&s.bar_in, 1);
     mbar_init(&s.bar_mma, 1);
+    mbar_init(&s.bar_mma2, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&s.tmem_base, 256);
@@ -133,6 +135,27 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
       fn();
       mma_commit(&s.bar_mma);
     }
+  };
+  // Phases with many products split them over two issuing threads (a tcgen05.mma costs tens of
+  // cycles to issue), by accumulator so that every accumulation chain stays in one thread's order.
+  uint32_t mph2 = 0;
+  auto issue2 = [&](auto fa, auto fb) {
+    if (lead) {
+      tc_fence_after();
+      fa();
+      mma_commit(&s.bar_mma);
+    } else if (tid == 32) {
+      tc_fence_after();
+      fb();
+      mma_commit(&s.bar_mma2);
+    }
+  };
+  auto wait_mma2 = [&](int code) {
+    mbar_wait(&s.bar_mma, mph, p.err, code);
+    mbar_wait(&s.bar_mma2, mph2, p.err, code);
+    mph ^= 1;
+    mph2 ^= 1;
+    tc_fence_after();
   };
   auto wait_mma = [&](int code) {
     mbar_wait(&s.bar_mma, mph, p.err, code);
@@ -188,13 +211,14 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   publish();
 
   // ---- P2: G = W W^T, M1 = Q W^T, N2 = W K^T, Q K^T ----
-  issue([&] {
+  issue2([&] {
     mma64(tb + C0, ta(S_W), 0, ta(S_W), 0, 0);
     mma64(tb + C1, ta(S_Q), 0, ta(S_W), 0, 0);
+  }, [&] {
     mma64(tb + C2, ta(S_W), 0, ta(S_K), 0, 0);
     mma64(tb + C3, ta(S_Q), 0, ta(S_K), 0, 0);
   });
-  wait_mma(42);
+  wait_mma2(42);
   {
     float x[32];
     ld_half(tb, lane_off, C0, x);  // L = strictLower(diag(beta) G), fp32 into the slots of Q and K
@@ -331,10 +355,11 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
 
   // ---- P6: dV_diag = P^T dO ; gM1 = -dS X^T - dQ<- Y1^T ; gX = -M1^T dS - W dK->^T ;
   //          gW = -X dK-> - Y1 dF ----
-  issue([&] {
+  issue2([&] {
     mma64(tb + C0, ta(S_P), 1, ta(S_DO), 1, 0);
     mma64(tb + C1, ta(S_DS), 0, ta(S_X), 0, 0, 1);
     mma64(tb + C1, ta(S_DQ), 0, ta(S_Y1), 0, 1, 1);
+  }, [&] {
     mma64(tb + C2, ta(S_M1), 1, ta(S_DS), 1, 0, 1);
     mma64(tb + C2, ta(S_W), 0, ta(S_DK), 0, 1, 1);
     mma64(tb + C3, ta(S_X), 0, ta(S_DK), 1, 0, 1);
@@ -343,7 +368,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   {
     float x[32], a[32];
     if (row_ok) load_f32_half(p.dvacc + (ws_row + i) * D + 32 * h, a);  // in flight during the MMAs
-    wait_mma(45);
+    wait_mma2(45);
     if (lead) {  // X and Y1 are consumed: Q and K come back into their slots
       mbar_arrive_expect_tx(&s.bar_in, 2 * TILE);
       tma_load_3d(s.t[S_Q2], &tm_q, 0, row0, bh, &s.bar_in);
@@ -365,19 +390,20 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   publish();
 
   // ---- P7: gQ = dS K + gM1 W ; E3 = M1^T dQ<- + W dF^T ; gN2 = U^T gX ; gW += gM1^T Q ----
-  if (lead) mbar_wait(&s.bar_in, 1, p.err, 46);
-  issue([&] {
+  if (lead || tid == 32) mbar_wait(&s.bar_in, 1, p.err, 46);  // both issuers read Q and K again
+  issue2([&] {
     mma64(tb + C0, ta(S_DS), 0, ta(S_K2), 1, 0);
     mma64(tb + C0, ta(S_GM1), 0, ta(S_W), 1, 1);
     mma64(tb + C1, ta(S_M1), 1, ta(S_DQ), 1, 0);
     mma64(tb + C1, ta(S_W), 0, ta(S_DF), 0, 1);
+  }, [&] {
     mma64(tb + C2, ta(S_U), 1, ta(S_GX), 1, 0);
     mma64(tb + C3, ta(S_GM1), 1, ta(S_Q2), 1, 1);
   });
   {
     float x[32], a[32];
     if (row_ok) load_f32_half(p.dql + (ws_row + i) * D + 32 * h, a);
-    wait_mma(47);
+    wait_mma2(47);
     ld_half(tb, lane_off, C0, x);
     if (row_ok) {
 #pragma unroll
@@ -394,18 +420,19 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   publish();
 
   // ---- P8: gK = dS^T Q + gN2^T W ; gU = -E3 W^T + gX N2^T ; gW += -U^T E3 + gN2 K ----
-  issue([&] {
+  issue2([&] {
     mma64(tb + C0, ta(S_DS), 1, ta(S_Q2), 1, 0);
     mma64(tb + C0, ta(S_GN2), 1, ta(S_W), 1, 1);
     mma64(tb + C1, ta(S_E3), 0, ta(S_W), 0, 0, 1);
     mma64(tb + C1, ta(S_GX), 0, ta(S_N2), 0, 1);
+  }, [&] {
     mma64(tb + C3, ta(S_U), 1, ta(S_E3), 1, 1, 1);
     mma64(tb + C3, ta(S_GN2), 0, ta(S_K2), 1, 1);
   });
   {
     float x[32], a[32];
     if (row_ok) load_f32_half(p.dkr + (ws_row + i) * D + 32 * h, a);
-    wait_mma(48);
+    wait_mma2(48);
     ld_half(tb, lane_off, C0, x);
     if (row_ok) {
 #pragma unroll
