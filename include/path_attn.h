@@ -112,9 +112,9 @@ int path_attn_fwd(const path_attn_desc_t* desc, const void* q, const void* k, co
  *
  * dq,dk,dv,dw: desc dtype outputs (overwritten).  dbeta: float32 (overwritten).
  * PaTH-FoX (forget gate, notes §2.5): pass the forward's log_f; dlog_f (float32, same shape,
- * may be NULL) receives dL/dlog f.  dlog_f without log_f is PATH_ERR_INVALID_ARG.  The forget-gate
- * backward runs on the bf16 tensor-core path only (fp32 descriptors, and scale == 0, return
- * PATH_ERR_UNSUPPORTED).
+ * may be NULL) receives dL/dlog f.  dlog_f without log_f is PATH_ERR_INVALID_ARG.  Both paths
+ * take the forget gate; the bf16 tensor-core path recovers the logit gradient from the scaled
+ * one, so there log_f with scale == 0 returns PATH_ERR_UNSUPPORTED (the fp32 path accepts it).
  * ws: at least path_attn_workspace_size(desc, 1) bytes.
  */
 int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,

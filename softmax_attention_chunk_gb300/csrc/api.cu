@@ -172,12 +172,11 @@ PATH_API int path_attn_bwd_phases(int phases, const path_attn_desc_t* desc, cons
     return cuda_status(launch_bwd_tc(tw, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, (char*)ws, phases,
                                      (cudaStream_t)stream, log_f, dlog_f));
   }
-  if (log_f || dlog_f) return PATH_ERR_UNSUPPORTED;  // the fp32 path has no forget-gate backward
   const BwdWs lay = bwd_ws_layout(g);
   if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_bwd_simt(desc->dtype == PATH_BF16, g, q, k, v, w, beta, o, lse, dO, dq,
                                      dk, dv, dw, dbeta, (char*)ws, lay, phases & PATH_BWD_ALL,
-                                     (cudaStream_t)stream));
+                                     (cudaStream_t)stream, log_f, dlog_f));
 }
 
 PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const void* k, const void* v,

@@ -67,6 +67,7 @@ struct BwdWs {
   size_t dql, dkr, dv;         // dQ<-, dK->, dV accumulators [BH][Lp][64] fp32
   size_t df;                   // dF accumulators             [BH][nc][64][64] fp32
   size_t zs;                   // Z scratch                   [nctas][Lp][64] fp32
+  size_t fxa, fxcs;            // PaTH-FoX: prefix sums of log f, colsum - rowsum of dS' [BH][Lp]
   int nctas;
   size_t total;
 };
@@ -89,6 +90,8 @@ inline BwdWs bwd_ws_layout(const Geom& g) {
   w.df = take((size_t)g.BH * g.nc * kHeadDim * kHeadDim * 4);
   w.nctas = bwd_num_ctas(g);
   w.zs = take((size_t)w.nctas * g.Lp * kHeadDim * 4);
+  w.fxa = take(rows * 4);
+  w.fxcs = take(rows * 4);
   w.total = off;
   return w;
 }
@@ -182,12 +185,14 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);
 
 // SIMT backward.  phases: bit 0 = prepare (zero accumulators, D_i, recomputed UT quantities),
-// bit 1 = adjoint chunk scan, bit 2 = per-chunk UT backward writing the gradients.
+// bit 1 = adjoint chunk scan, bit 2 = per-chunk UT backward writing the gradients.  With logf
+// (PaTH-FoX, [BH][L]) the logits carry the forget-gate bias; dlogf (needs logf) receives its
+// gradient at the end of bit 2.
 cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                             const void* v, const void* w, const float* beta, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
-                            cudaStream_t st);
+                            cudaStream_t st, const float* logf = nullptr, float* dlogf = nullptr);
 
 // D_i = dO_i . o_i for the bf16 tensor-core backward.
 cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* Dv, cudaStream_t st);

@@ -8,6 +8,9 @@
 //   dF_c  += G_{b,c-1}^T Z_{b,c},   dQ<-_b = G_{b,b-1},
 // followed per chunk by the chain rule through the diagonal-chunk logits and the UT quantities
 // (Q<-, K->, F, X = U strictLower(W K^T), U = (I + strictLower(D W W^T))^{-1} D).
+// PaTH-FoX (§2.5): the logit of (i, j) gains A_i - A_j (A = prefix sums of log f, formed over the
+// whole sequence by fox_bwd.cu); both scans add colsum_m - rowsum_m of the logit gradient
+// dS' = P (dP - D) into fxcs, from which fox_bwd.cu forms dlog f.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "smem_mm.cuh"
@@ -88,17 +91,19 @@ struct BwdMainSmem {
   static constexpr int kZ = 0, kK = kZ + B * DS, kV = kK + B * DS, kF = kV + B * DS;
   static constexpr int kdO = kF + D * DS, kG = kdO + B * DS, kGn = kG + B * DS;
   static constexpr int kP = kGn + B * DS, kdS = kP + B * BS, kLse = kdS + B * BS, kDv = kLse + B;
-  static constexpr int total = kDv + B;
+  static constexpr int kAk = kDv + B;  // PaTH-FoX: A_j log2(e) of the key chunk
+  static constexpr int total = kAk + B;
   static constexpr size_t bytes = (size_t)total * 4;
 };
 
 // Persistent CTAs; tile n (heaviest first) is query chunk b = nc-1 - n/BH of head n%BH.
-template <typename T, int B>
+template <typename T, int B, bool FOX>
 __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     Geom g, const T* __restrict__ v, const float* __restrict__ lse, const T* __restrict__ dO,
     const float* __restrict__ Dv, const float* __restrict__ ql, const float* __restrict__ kr,
     const float* __restrict__ f, float* __restrict__ dql, float* __restrict__ dkr,
-    float* __restrict__ dvacc, float* __restrict__ dfacc, float* __restrict__ zs) {
+    float* __restrict__ dvacc, float* __restrict__ dfacc, float* __restrict__ zs,
+    const float* __restrict__ fxa, float* __restrict__ fxcs) {
   extern __shared__ float sm[];
   using S = BwdMainSmem<B>;
   constexpr int BS = S::BS;
@@ -113,6 +118,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
   float* sdS = sm + S::kdS;
   float* sLse = sm + S::kLse;
   float* sDv = sm + S::kDv;
+  float* sAk = sm + S::kAk;
 
   const int tid = threadIdx.x;
   float* myz = zs + (size_t)blockIdx.x * g.Lp * D;
@@ -154,9 +160,12 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     }
     for (int i = tid; i < B; i += NT) {
       const int gi = b * B + i;
-      sLse[i] = gi < g.L ? lse[(size_t)bh * g.L + gi] * kLog2e : INFINITY;  // padded rows: P = 0
+      float l2 = gi < g.L ? lse[(size_t)bh * g.L + gi] * kLog2e : INFINITY;  // padded rows: P = 0
+      if constexpr (FOX) l2 = fmaf(-fxa[brow + i], kLog2e, l2);                 // the + A_i of the bias
+      sLse[i] = l2;
       sDv[i] = Dv[brow + i];
     }
+    float fox_rowsum = 0.f;  // PaTH-FoX: row tid's sum of dS' over the off-diagonal key chunks
     __syncthreads();  // also orders pass-1 scratch writes before the reads below
     for (int c = 0; c < b; ++c) {
       const size_t crow = (size_t)bh * g.Lp + (size_t)c * B;
@@ -169,6 +178,8 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       }
       const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
       for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
+      if constexpr (FOX)
+        for (int j = tid; j < B; j += NT) sAk[j] = fxa[crow + j] * kLog2e;
       __syncthreads();
       // P and dS
       for (int idx = tid; idx < B * B; idx += NT) {
@@ -178,11 +189,21 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
           s += sZ[i * DS + kk] * sK[j * DS + kk];
           dp += sdO[i * DS + kk] * sV[j * DS + kk];
         }
-        const float p = fast_exp2(s * scl2 - sLse[i]);
+        const float p = fast_exp2(s * scl2 - sLse[i] - (FOX ? sAk[j] : 0.f));
         sP[i * BS + j] = p;
         sdS[i * BS + j] = p * (dp - sDv[i]);
       }
       __syncthreads();
+      if constexpr (FOX) {  // dS' row sums kept per thread; column sums of key chunk c into fxcs
+        if (tid < B) {
+          for (int j = 0; j < B; ++j) fox_rowsum += sdS[tid * BS + j];
+        } else if (tid < 2 * B) {
+          const int j = tid - B;
+          float cs = 0.f;
+          for (int i = 0; i < B; ++i) cs += sdS[i * BS + j];
+          atomicAdd(fxcs + crow + j, cs);
+        }
+      }
       // dV_c += P^T dO ; dK->_c += scale dS^T Z ; G_new = scale dS K + G F_c
       for (int idx = tid; idx < B * D; idx += NT) {
         const int j = idx / D, cc = idx % D;
@@ -216,6 +237,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       float* t = sG; sG = sGn; sGn = t;
     }
     for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = sG[(idx / D) * DS + idx % D];
+    if (FOX && tid < B) atomicAdd(fxcs + brow + tid, -fox_rowsum);
     __syncthreads();
   }
 }
@@ -226,21 +248,21 @@ struct PrepBwdSmem {
   static constexpr int nBD = 8, nBB = 11;
   static constexpr int kBD = 0, kBB = kBD + nBD * B * DS;
   static constexpr int kVec = kBB + nBB * B * BS;
-  static constexpr int total = kVec + 4 * B;
+  static constexpr int total = kVec + 7 * B;  // beta, lse, D, dbeta; PaTH-FoX: A, dS' row / column sums
   static constexpr size_t bytes = (size_t)total * 4;
 };
 
 // One CTA per (chunk c, head bh): diagonal-chunk attention backward and the chain rule through
 // Q<- = Q - lower(QW^T) U W, K-> = K - X^T W, F = I - W^T U^T W, X = U strictLower(W K^T),
 // S_d = lower(QK^T) - lower(QW^T) X, U = Y D with Y = (I + strictLower(D W W^T))^{-1}.
-template <typename T, int B>
+template <typename T, int B, bool FOX>
 __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ lse,
     const T* __restrict__ dO, const float* __restrict__ Dv, const float* __restrict__ dql,
     const float* __restrict__ dkr, const float* __restrict__ dvacc, const float* __restrict__ dfacc,
     T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, T* __restrict__ dw,
-    float* __restrict__ dbeta) {
+    float* __restrict__ dbeta, const float* __restrict__ fxa, float* __restrict__ fxcs) {
   extern __shared__ float sm[];
   using S = PrepBwdSmem<B>;
   constexpr int BS = S::BS;
@@ -271,6 +293,9 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   float* sLse = sBeta + B;
   float* sDv = sLse + B;
   float* sgB = sDv + B;
+  float* sFa = sgB + B;  // PaTH-FoX: A_i log2(e)
+  float* sFr = sFa + B;  // PaTH-FoX: row sums of dS'
+  float* sFc = sFr + B;  // PaTH-FoX: column sums of dS'
 
   const int c = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
   const int row0 = c * B;
@@ -300,6 +325,10 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     sLse[r] = ok ? lse[in_row + gi] * kLog2e : INFINITY;
     sDv[r] = Dv[ws_row + r];
     sgB[r] = 0.f;
+    if constexpr (FOX) {
+      sFa[r] = fxa[ws_row + r] * kLog2e;
+      sFr[r] = sFc[r] = 0.f;
+    }
   }
   __syncthreads();
 
@@ -364,14 +393,22 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
   smem_mm<B, D, B, false, false, TC>(sU, BS, sW, DS, [&](int i, int cc, float x) { sY1[i * DS + cc] = x; });
   __syncthreads();
 
-  // P5. S_d = QK^T - M1 X ; P = exp(scale S_d - lse) on j <= i ; dS = scale P (dP - D)
+  // P5. S_d = QK^T - M1 X ; P = exp(scale S_d (+ A_i - A_j) - lse) on j <= i ; dS = scale P (dP - D)
   smem_mm<B, B, B, false, false, TC>(sM1, BS, sX, BS, [&](int i, int j, float x) {
     float p = 0.f;
-    if (j <= i && row0 + i < g.L) p = fast_exp2((sT1[i * BS + j] - x) * scl2 - sLse[i]);
+    const bool live = j <= i && row0 + i < g.L;
+    if (live) p = fast_exp2((sT1[i * BS + j] - x) * scl2 - sLse[i] + (FOX ? sFa[i] - sFa[j] : 0.f));
+    const float ds = p * (sT2[i * BS + j] - sDv[i]);
     sT1[i * BS + j] = p;
-    sdS[i * BS + j] = g.scale * p * (sT2[i * BS + j] - sDv[i]);
+    sdS[i * BS + j] = g.scale * ds;
+    if (FOX && live) {
+      atomicAdd(&sFr[i], ds);
+      atomicAdd(&sFc[j], ds);
+    }
   });
   __syncthreads();
+  if constexpr (FOX)
+    for (int r = tid; r < B; r += NT) atomicAdd(fxcs + ws_row + r, sFc[r] - sFr[r]);
 
   // P6. dv (final) = dV acc + P^T dO ; gQ = dQ<- + dS K ; gK = dK-> + dS^T Q ;
   //     gM1 = lower(-dS X^T - dQ<- Y1^T) (sT2) ; gX = -M1^T dS - W dK->^T
@@ -456,10 +493,16 @@ template <typename T, int B>
 cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                   const float* beta, const void* o, const float* lse, const void* dO, void* dq,
                   void* dk, void* dv, void* dw, float* dbeta, char* ws, const BwdWs& lay,
-                  int phases, cudaStream_t st) {
+                  int phases, cudaStream_t st, const float* logf, float* dlogf) {
   cudaError_t e;
   const size_t rows = (size_t)g.BH * g.Lp;
+  float* fxa = (float*)(ws + lay.fxa);
+  float* fxcs = (float*)(ws + lay.fxcs);
   if (phases & 1) {
+  if (logf) {  // PaTH-FoX: prefix sums of log f, zeroed dS' sums
+    if ((e = launch_fox_prefix(g, logf, fxa, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(fxcs, 0, rows * 4, st)) != cudaSuccess) return e;
+  }
   if ((e = cudaMemsetAsync(ws + lay.dkr, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.df, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
@@ -470,24 +513,27 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
     return e;
   }
   if (phases & 2) {
-    auto kern = bwd_main_simt_kernel<T, B>;
+    auto kern = logf ? bwd_main_simt_kernel<T, B, true> : bwd_main_simt_kernel<T, B, false>;
     const size_t smem = BwdMainSmem<B>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<lay.nctas, NT, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
                                       (const float*)(ws + lay.fw.ql), (const float*)(ws + lay.fw.kr),
                                       (const float*)(ws + lay.fw.f), (float*)(ws + lay.dql),
                                       (float*)(ws + lay.dkr), (float*)(ws + lay.dv), (float*)(ws + lay.df),
-                                      (float*)(ws + lay.zs));
+                                      (float*)(ws + lay.zs), fxa, fxcs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {
-    auto kern = prep_bwd_simt_kernel<T, B>;
+    auto kern = logf ? prep_bwd_simt_kernel<T, B, true> : prep_bwd_simt_kernel<T, B, false>;
     const size_t smem = PrepBwdSmem<B>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<dim3(g.nc, g.BH), NT, smem, st>>>(
         g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, lse, (const T*)dO,
         (const float*)(ws + lay.Dv), (const float*)(ws + lay.dql), (const float*)(ws + lay.dkr),
-        (const float*)(ws + lay.dv), (const float*)(ws + lay.df), (T*)dq, (T*)dk, (T*)dv, (T*)dw, dbeta);
+        (const float*)(ws + lay.dv), (const float*)(ws + lay.df), (T*)dq, (T*)dk, (T*)dv, (T*)dw, dbeta,
+        fxa, fxcs);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (dlogf && (e = launch_fox_dlogf(g, fxcs, dlogf, st)) != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -504,10 +550,12 @@ cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const vo
                             const void* v, const void* w, const float* beta, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
-                            cudaStream_t st) {
-  if (g.B != 32) return cudaErrorInvalidValue;
-  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st)
-                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st);
+                            cudaStream_t st, const float* logf, float* dlogf) {
+  if (g.B != 32 || (dlogf && !logf)) return cudaErrorInvalidValue;
+  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases,
+                                            st, logf, dlogf)
+                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st,
+                                    logf, dlogf);
 }
 
 }  // namespace pathattn

@@ -109,12 +109,15 @@ def test_bwd_argument_errors(pa):
     # order: q,k,v,w,beta,log_f,o,lse,dO,dq,dk,dv,dw,dbeta,dlog_f,ws,ws_bytes,stream
     base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE]
     assert pa.path_attn_bwd(d, *base, n - 1, None) == 3
-    # forget gate: dlog f without log f is an argument error; the fp32 path and a zero scale have
-    # no forget-gate backward (every check runs before any launch: the pointers here are fake)
+    # forget gate: dlog f without log f, or a misaligned log f, is an argument error; the bf16
+    # tensor-core path has no forget-gate backward at a zero scale (every check runs before any
+    # launch: the pointers here are fake)
     with_dlogf = list(base); with_dlogf[14] = FAKE
     assert pa.path_attn_bwd(d, *with_dlogf, n, None) == 1
     with_logf = list(base); with_logf[5] = FAKE
-    assert pa.path_attn_bwd(d, *with_logf, n, None) == 2  # d is an fp32 descriptor
+    assert pa.path_attn_bwd(d, *with_logf, n - 1, None) == 3  # d is an fp32 descriptor
+    odd_logf = list(with_logf); odd_logf[5] = FAKE + 4
+    assert pa.path_attn_bwd(d, *odd_logf, n, None) == 1
     d0 = pa.path_attn_desc_t(d.batch, d.heads, d.seqlen, d.head_dim, pa.PATH_BF16, 0.0, d.chunk)
     assert pa.path_attn_bwd(d0, *with_logf, pa.path_attn_workspace_size(d0, 1), None) == 2
     null_dw = list(base); null_dw[12] = None

@@ -167,15 +167,31 @@ def test_fwd_bf16_more_heads_than_a_schedule_group(cuda_lib):
     check(flat(lse), lse_ref, 2e-2, "lse")
 
 
-def test_fp32_bwd_rejects_forget_gate(cuda_lib):
-    """The fp32 (SIMT) backward has no forget-gate gradient: it refuses log_f."""
+@pytest.mark.parametrize("L,scale", [(1, 1.0), (31, 1.0), (33, 1.0), (129, 0.7), (200, 0.0)])
+def test_bwd_fp32_fox(cuda_lib, L, scale):
+    """Forget-gate backward on the fp32 path (32-row chunks): every gradient including dlog f
+    within 1e-4 of the oracle, at a lone partial chunk, one chunk and one row, ragged tails and a
+    zero scale (only the forget bias shapes the attention)."""
     from softmax_attention_chunk_gb300 import path_attn as pa
 
-    inp = gen_path_inputs(1, 1, 64, 64, "fp32", seed=3, with_dO=True, fox=True)
-    t = {k: v.to(DEV) for k, v in inp.items()}
-    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"])
-    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
-        pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], log_f=t["log_f"])
+    inp = gen_path_inputs(1, 2, L, 64, "fp32", seed=600 + L, with_dO=True, near2_frac=0.1, fox=True)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=scale)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=scale, log_f=t["log_f"])
+    torch.cuda.synchronize()
+    check_grads_fox(inp, g, scale, 1e-4, None)
+
+
+def test_bwd_bf16_chunk32_fox(cuda_lib):
+    """bf16 inputs on the 32-row-chunk (SIMT) path with the forget gate, within the bf16 bound."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(2, 2, 150, 64, "bf16", seed=611, with_dO=True, near2_frac=0.05, fox=True)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=1.0, chunk=32)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=1.0, chunk=32, log_f=t["log_f"])
+    torch.cuda.synchronize()
+    check_grads_fox(inp, g, 1.0, 2e-2, 3e-2)
 
 
 @pytest.mark.parametrize("dtype,t0,steps,tol", [("fp32", 0, 40, 1e-4), ("fp32", 3000, 5, 1e-4),
