@@ -50,7 +50,7 @@ UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule 
 # dram__bytes_write.sum) of a 16-head launch (batch 1, 16 heads) divided by 16 — the kernel takes
 # heads 16 at a time, so a launch over more heads repeats that traffic per group.  To be retaken
 # whenever the kernel changes.
-BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (426225408 + 80330496) / 16
+BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (425917440 + 80140288) / 16
 
 
 def tiles_steps(L):
