@@ -178,5 +178,136 @@ __device__ __forceinline__ void ut_solve_column(const float* sl, int cc, float (
   }
 }
 
+// Named barrier 2 over the 128 threads of a per-chunk UT kernel (the block-inversion routine
+// below synchronises through it).
+__device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// U = (I + L)^{-1} diag(beta) for one 64-row chunk, by two-level block inversion over the row
+// halves t (0-31) and b (32-63):
+//   (I + L)^{-1} = [[Y_tt, 0], [-Y_bb L_bt Y_tt, Y_bb]],  Y_tt = (I + L_tt)^{-1}, Y_bb = (I + L_bb)^{-1}.
+// Phase 1: warp 0 solves the columns of Y_tt, warp 1 those of Y_bb (one column per thread, 32
+// rows by forward substitution), written over L_tt / L_bb.  Phase 2: all 128 threads form
+// T = L_bt Y_tt (into the unused upper-right block of sl), then Y_bt = -Y_bb T, each thread a
+// 2 x 4 block.  sl: the fp32 L of the chunk (f32_idx layout over two tile slots, strictly
+// lower; overwritten); beta: the chunk's clamped beta; U is written as bf16 into the swizzled
+// tile u (LO: with u_lo, U = u + u_lo with both parts bf16).  Called by threads 0-127 together;
+// ends with the tiles written by generic stores (the caller fences them for the tensor core).
+// (The UT backward keeps the column solve above: there warps 2-3 convert the gradient tiles while
+// warps 0-1 substitute, and a phase that needs all four warps lengthened its chain.)
+template <bool LO>
+__device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, uint8_t* u, uint8_t* u_lo,
+                                                 int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  auto put_u = [&](int r, int col, float yv, float bc) {
+    const float val = yv * bc;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(val);
+    *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(r, col)) = hi;
+    if constexpr (LO)
+      *reinterpret_cast<__nv_bfloat16*>(u_lo + sw128_offset(r, col)) = __float2bfloat16_rn(val - __bfloat162float(hi));
+  };
+  // ---- phase 1: diagonal 32 x 32 blocks ----
+  float y[32];
+  if (warp < 2) {
+    const float* sh = sl + 65 * 32 * warp;  // block (32 warp, 32 warp): element (r, m) at sh[f32_idx(r, m)]
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float acc[16];
+      if (b == 1) {
+        uint64_t s2[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+          const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sh + f32_idx(16 + rr, m));
+            s2[rr] = f2_fma(lv.x, y01, s2[rr]);
+            s2[rr] = f2_fma(lv.y, y23, s2[rr]);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float lo, hi;
+          f2_split(s2[rr], lo, hi);
+          acc[rr] = lo + hi;
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * b + rr;
+        float a = acc[rr];
+#pragma unroll
+        for (int m = 16 * b; m < r; m += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
+          a = fmaf(lv.x, y[m], a);
+          if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
+          if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
+          if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
+        }
+        y[r] = (lane == r ? 1.f : 0.f) - a;
+      }
+    }
+  }
+  ut_sync();  // every read of L_tt / L_bb is done
+  if (warp < 2) {
+    const int o = 32 * warp, col = o + lane;
+    const float bc = beta[col];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      sl[65 * o + f32_idx(r, lane)] = y[r];
+      put_u(o + r, col, y[r], bc);
+    }
+    if (warp == 1) {  // upper-right block of U is zero
+#pragma unroll
+      for (int r = 0; r < 32; ++r) put_u(r, col, 0.f, 0.f);
+    }
+  }
+  ut_sync();
+  // ---- phase 2: rows 2 rg, 2 rg + 1 and columns 4 cg .. 4 cg + 3 of a 32 x 32 product ----
+  const int rg = tid >> 3, cg = tid & 7;
+  float acc[2][4];
+  auto product = [&](int a_row0, int a_col0, int b_row0, int b_col0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      const float4 a0 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg, a_col0 + m));
+      const float4 a1 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg + 1, a_col0 + m));
+      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(b_row0 + m + kk, b_col0 + 4 * cg));
+        acc[0][0] = fmaf(av0[kk], bv.x, acc[0][0]);
+        acc[0][1] = fmaf(av0[kk], bv.y, acc[0][1]);
+        acc[0][2] = fmaf(av0[kk], bv.z, acc[0][2]);
+        acc[0][3] = fmaf(av0[kk], bv.w, acc[0][3]);
+        acc[1][0] = fmaf(av1[kk], bv.x, acc[1][0]);
+        acc[1][1] = fmaf(av1[kk], bv.y, acc[1][1]);
+        acc[1][2] = fmaf(av1[kk], bv.z, acc[1][2]);
+        acc[1][3] = fmaf(av1[kk], bv.w, acc[1][3]);
+      }
+    }
+  };
+  product(32, 0, 0, 0);  // T = L_bt Y_tt
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+    *reinterpret_cast<float4*>(sl + f32_idx(2 * rg + e, 32 + 4 * cg)) =
+        make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
+  ut_sync();
+  product(32, 32, 0, 32);  // Y_bb T
+  const float4 bq = *reinterpret_cast<const float4*>(beta + 4 * cg);
+  const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) put_u(32 + 2 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
+}
+
 }  // namespace tc
 }  // namespace pathattn

@@ -1,18 +1,21 @@
-// Per-chunk UT preparation on tcgen05 (bf16 operands, fp32 accumulation in TMEM), chunk B = 64.
+// Per-chunk UT preparation on tcgen05 (bf16 operands, fp32 accumulation in TMEM), chunk B = 64:
+// one CTA of 128 threads per chunk.
 //
 // Method: PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6 (UT representation) and §2.7
 // (boundary-adjusted queries/keys, chunk transform):
 //   G = strictLower(W W^T), M1 = lower(Q W^T), N2 = strictLower(W K^T)
-//   U = (I + strictLower(D G))^{-1} D        (forward substitution, fp32, two warps)
+//   U = (I + strictLower(D G))^{-1} D        (fp32, two-level block inversion)
 //   A = M1 U,  X = U N2,  Y = U^T W
 //   Q<- = Q - A W,  K-> = K - X^T W,  F = I - W^T Y,  S_d = Q K^T - M1 X (masked j <= i)
 // and the diagonal chunk's softmax partial state (m, l, acc = P V).
-// Every product is one M=64 N=64 K=64 MMA whose operands are 64x64 bf16 tiles in the 128-byte
-// swizzled layout (TMA-loaded inputs or tiles written by the warps), K-major or MN-major as the
-// product needs.  Accumulators are read with the 16x32bx2 TMEM shape: each thread of warp w
-// holds 32 columns (half h = lane / 16) of row 16w + lane % 16, so all 128 threads work in every
-// epilogue; the two halves of a row meet through one shuffle where a row reduction is needed.
-// Inputs come through 3-D tensor maps ([heads][L][64]) that read rows >= L as zero.
+// Every product is an M=64 MMA whose operands are 64x64 bf16 tiles in the 128-byte swizzled layout
+// (TMA-loaded inputs or tiles written by the warps), K-major or MN-major as the product needs; the
+// four products of the first phase share their B operands two by two, so they run as two N=128
+// MMAs over the stacked [W; K] tile.  Accumulators are read with the 16x32bx2 TMEM shape: each
+// thread of warp w holds 32 columns (half h = lane / 16) of row 16w + lane % 16, so all 128
+// threads work in every epilogue; the two halves of a row meet through one shuffle where a row
+// reduction is needed.  Inputs come through 3-D tensor maps ([heads][L][64]) that read rows >= L
+// as zero.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
@@ -28,18 +31,8 @@ bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t
 namespace {
 using namespace tc;
 
-constexpr int B = 64;
-constexpr int D = kHeadDim;
-constexpr uint32_t TILE = 64 * 128;  // one 64x64 bf16 tile
-
-struct __align__(1024) UtSmem {
-  uint8_t w[TILE], q[TILE], k[TILE], v[TILE];   // inputs (rows >= L read as zero)
-  uint8_t m1[TILE], n2[TILE], u[TILE];          // lower(QW^T), strictLower(WK^T), U
-  uint8_t a[TILE], x[TILE], y[TILE], p[TILE];   // M1 U, U N2, U^T W, P; a..x hold fp32 L in P1-P2
-  float beta[B], pre[B];
-  uint64_t bar_in, bar_mma;
-  uint32_t tmem_base;
-};
+constexpr uint32_t kUtTile = 64 * 128;  // one 64x64 bf16 tile
+constexpr uint32_t kUtSlotBytes = 11 * kUtTile;
 
 struct UtParams {
   int L, Lp, nc, BH;
@@ -59,16 +52,43 @@ struct UtParams {
   int* err;
 };
 
+// Shared memory of one chunk's preparation: eleven 1024-byte aligned tiles in this order (w and k
+// adjacent: the stacked B operand of the first phase; a and x adjacent: the fp32 L of the
+// substitution), beta and the forget-gate prefix (16-byte aligned), and two mbarriers.
+struct UtSlots {
+  uint8_t *w, *k, *q, *v, *m1, *n2, *u, *a, *x, *y, *p;
+  float* beta;
+  float* pre;
+  uint64_t* bar_in;
+  uint64_t* bar_mma;
+};
+__device__ __forceinline__ UtSlots ut_slots(uint8_t* base, float* beta, float* pre, uint64_t* bar_in,
+                                            uint64_t* bar_mma) {
+  UtSlots s;
+  uint8_t** t[11] = {&s.w, &s.k, &s.q, &s.v, &s.m1, &s.n2, &s.u, &s.a, &s.x, &s.y, &s.p};
+#pragma unroll
+  for (int j = 0; j < 11; ++j) *t[j] = base + j * kUtTile;
+  s.beta = beta;
+  s.pre = pre;
+  s.bar_in = bar_in;
+  s.bar_mma = bar_mma;
+  return s;
+}
+
+// Prepares chunk c of head bh.  Run by the CTA's 128 threads together; thread 0 issues the TMA
+// loads and the MMAs.  tb: 256 TMEM columns of the CTA; in_par / mph: phases of
+// bar_in (one completion per call) and bar_mma (advanced here).  zimg (optional): a swizzled
+// 64-row bf16 tile image that also receives Q<- of the chunk.  The mbarriers are initialised by
+// the caller; on return every TMEM access and every MMA of the chunk has completed, and the
+// slots may be reused.
 template <bool F32>
-__global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                        const __grid_constant__ CUtensorMap tm_k,
-                                                        const __grid_constant__ CUtensorMap tm_v,
-                                                        const __grid_constant__ CUtensorMap tm_w,
-                                                        const UtParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, const CUtensorMap* tm_q,
+                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                              const CUtensorMap* tm_w, const UtParams& p, int bh, int c,
+                                              uint32_t in_par, uint32_t& mph, uint8_t* zimg) {
+  constexpr int B = 64;
+  constexpr int D = kHeadDim;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, bh = blockIdx.y;
   const int row0 = c * B;
   const size_t in_row = (size_t)bh * p.L;
   const size_t ws_row = (size_t)bh * p.Lp + row0;
@@ -76,44 +96,32 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
   // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
   const int i = 16 * warp + (lane & 15), h = lane >> 4;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  float* sg = reinterpret_cast<float*>(s.a);  // fp32 L = strictLower(D G) over the a and x slots (P1 epilogue - P2)
-
-  if (lead) {
-    mbar_init(&s.bar_in, 1);
-    mbar_init(&s.bar_mma, 1);
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(&s.tmem_base, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = s.tmem_base;
+  float* sg = reinterpret_cast<float*>(s.a);  // fp32 L = strictLower(D G) over the a and x slots
   const uint32_t aw = smem_u32(s.w), aq = smem_u32(s.q), ak = smem_u32(s.k), av = smem_u32(s.v);
   const uint32_t am1 = smem_u32(s.m1), an2 = smem_u32(s.n2), au = smem_u32(s.u);
   const uint32_t aa = smem_u32(s.a), ax = smem_u32(s.x), ay = smem_u32(s.y), ap = smem_u32(s.p);
-  uint32_t mph = 0;  // phase of bar_mma
   auto run = [&](auto issue, int code) {  // lead issues one phase's MMAs; every thread waits
     if (lead) {
       tc_fence_after();
       issue();
-      mma_commit(&s.bar_mma);
+      mma_commit(s.bar_mma);
     }
-    mbar_wait(&s.bar_mma, mph, p.err, code);
+    mbar_wait(s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
   };
   auto publish = [&]() {  // tiles written by the threads -> visible to the next MMAs
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    ut_sync();
   };
 
   if (lead) {
-    mbar_arrive_expect_tx(&s.bar_in, (p.with_diag ? 4 : 3) * TILE);
-    tma_load_3d(s.w, &tm_w, 0, row0, bh, &s.bar_in);
-    tma_load_3d(s.q, &tm_q, 0, row0, bh, &s.bar_in);
-    tma_load_3d(s.k, &tm_k, 0, row0, bh, &s.bar_in);
-    if (p.with_diag) tma_load_3d(s.v, &tm_v, 0, row0, bh, &s.bar_in);
+    mbar_arrive_expect_tx(s.bar_in, (p.with_diag ? 4 : 3) * kUtTile);
+    tma_load_3d(s.w, tm_w, 0, row0, bh, s.bar_in);
+    tma_load_3d(s.q, tm_q, 0, row0, bh, s.bar_in);
+    tma_load_3d(s.k, tm_k, 0, row0, bh, s.bar_in);
+    if (p.with_diag) tma_load_3d(s.v, tm_v, 0, row0, bh, s.bar_in);
   }
   if (tid < B) {
     const int gi = row0 + tid;
@@ -132,15 +140,18 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
     s.pre[lane] = a;
     s.pre[32 + lane] = b2 + tot_a;
   }
-  mbar_wait(&s.bar_in, 0, p.err, 31);
-  __syncthreads();
+  mbar_wait(s.bar_in, in_par, p.err, 31);
+  ut_sync();
 
-  // ---- P1: G = W W^T, M1 = Q W^T, N2 = W K^T, Q K^T ----
+  // ---- P1: [G | N2] = W [W; K]^T, [M1 | Q K^T] = Q [W; K]^T ----
   run([&] {
-    mma64(tb + 0, aw, 0, aw, 0, 0);
-    mma64(tb + 64, aq, 0, aw, 0, 0);
-    mma64(tb + 128, aw, 0, ak, 0, 0);
-    mma64(tb + 192, aq, 0, ak, 0, 0);
+    const uint32_t idesc = idesc_bf16(64, 128, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t bd = sdesc_sw128(aw + 32u * kk, 1024, 16);  // 128 rows: the w tile, then the k tile
+      mma_ss(tb + 0, sdesc_sw128(aw + 32u * kk, 1024, 16), bd, idesc, kk > 0 ? 1u : 0u);
+      mma_ss(tb + 128, sdesc_sw128(aq + 32u * kk, 1024, 16), bd, idesc, kk > 0 ? 1u : 0u);
+    }
   }, 32);
   {
     float x[32];
@@ -153,40 +164,20 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
           make_float4(j < i ? bi * x[4 * q] : 0.f, j + 1 < i ? bi * x[4 * q + 1] : 0.f,
                       j + 2 < i ? bi * x[4 * q + 2] : 0.f, j + 3 < i ? bi * x[4 * q + 3] : 0.f);
     }
-    ld_half(tb, lane_off, 64, x);
+    ld_half(tb, lane_off, 128, x);  // M1 = lower(Q W^T)
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
     put_half(s.m1, i, h, x);
-    ld_half(tb, lane_off, 128, x);
+    ld_half(tb, lane_off, 64, x);  // N2 = strictLower(W K^T)
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
     put_half(s.n2, i, h, x);
   }
-  __syncthreads();
+  ut_sync();
 
-
-  // ---- P2: U = (I + strictLower(D G))^{-1} D = Y diag(beta): one column of Y per thread of
-  //      warps 0-1 (columns 32-63 are zero above row 32) ----
-  if (warp < 2) {
-    const int cc = 32 * warp + lane;
-    float y[64];
-    if (warp == 0) ut_solve_column<0>(sg, cc, y);
-    else ut_solve_column<2>(sg, cc, y);
-    const float bc = s.beta[cc];
-    if constexpr (F32) {  // fp32 F: U = U_hi + U_lo, both bf16 (U_lo in P's slot, unused without the diagonal state)
-#pragma unroll
-      for (int r = 0; r < 64; ++r) {
-        const float uv = y[r] * bc;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(uv);
-        *reinterpret_cast<__nv_bfloat16*>(s.u + sw128_offset(r, cc)) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(s.p + sw128_offset(r, cc)) = __float2bfloat16_rn(uv - __bfloat162float(hi));
-      }
-    } else {
-#pragma unroll
-      for (int r = 0; r < 64; ++r)
-        *reinterpret_cast<__nv_bfloat16*>(s.u + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r] * bc);
-    }
-  }
+  // ---- P2: U = (I + strictLower(D G))^{-1} D (with an fp32 F: U = U_hi + U_lo, U_lo in P's
+  //      slot, unused without the diagonal state) ----
+  ut_solve_blocked<F32>(sg, s.beta, s.u, s.p, tid);
   publish();
 
   // ---- P3: A = M1 U, X = U N2, Y = U^T W (+ U_lo^T W for an fp32 F) ----
@@ -233,6 +224,7 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
 #pragma unroll
     for (int j = 0; j < 32; ++j) src[j] -= x[j];
     store_bf16_half(p.ql + orow * D + 32 * h, src);
+    if (zimg) put_half(zimg, i, h, src);
     ld_half(tb, lane_off, 64, x);  // K-> = K - X^T W
     get_half(s.k, i, h, src);
 #pragma unroll
@@ -292,6 +284,42 @@ __global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ 
 #pragma unroll
     for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
   }
+  // every thread's TMEM loads are complete (tcgen05.wait::ld in ld_half); the slots and the TMEM
+  // columns may be reused after the caller's next barrier
+  tc_fence_before();
+  ut_sync();
+  tc_fence_after();
+}
+
+struct __align__(1024) UtSmem {
+  uint8_t tiles[kUtSlotBytes];  // the eleven preparation slots (ut_slots order)
+  float beta[64], pre[64];
+  uint64_t bar_in, bar_mma;
+  uint32_t tmem_base;
+};
+
+template <bool F32>
+__global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                        const __grid_constant__ CUtensorMap tm_k,
+                                                        const __grid_constant__ CUtensorMap tm_v,
+                                                        const __grid_constant__ CUtensorMap tm_w,
+                                                        const UtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&s.bar_in, 1);
+    mbar_init(&s.bar_mma, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&s.tmem_base, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  const UtSlots sl = ut_slots(s.tiles, s.beta, s.pre, &s.bar_in, &s.bar_mma);
+  uint32_t mph = 0;
+  ut_prep_chunk<F32>(sl, tb, &tm_q, &tm_k, &tm_v, &tm_w, p, (int)blockIdx.y, (int)blockIdx.x, 0, mph, nullptr);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
