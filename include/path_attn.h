@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   PATH_OK = 0,
   PATH_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer, bad enum */
-  PATH_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim != 64, chunk value, ...) */
+  PATH_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim not 64 or 128, chunk value, ...) */
   PATH_ERR_WORKSPACE = 3,    /* ws_bytes smaller than the required workspace */
   PATH_ERR_CAPACITY = 4,     /* decode: t + 1 > capacity */
   PATH_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
@@ -57,7 +57,9 @@ typedef struct {
   int batch;      /* > 0 */
   int heads;      /* > 0 */
   int seqlen;     /* L > 0 */
-  int head_dim;   /* d; 64 is supported */
+  int head_dim;   /* d: 64 or 128.  bf16 at 64 runs the tcgen05 kernels (chunk 64); 128 (and fp32)
+                     runs the fp32 CUDA-core kernels, at 128 with 32-row chunks only (chunk 0 or
+                     32; 64 is PATH_ERR_UNSUPPORTED) */
   int dtype;      /* path_dtype_t of q,k,v,w,o (and dO,dq,dk,dv,dw in the backward) */
   float scale;    /* multiplies the Householder-path logit; the forget bias is added unscaled */
   int chunk;      /* UT chunk size B; 0 lets the library choose (see path_attn_chunk) */
@@ -66,7 +68,7 @@ typedef struct {
 typedef struct {
   int batch;       /* > 0 */
   int heads;       /* > 0 */
-  int head_dim;    /* 64 */
+  int head_dim;    /* 64 or 128 (path_decode_prefill and path_decode_step_noalloc: 64 only) */
   int capacity;    /* rows allocated per (batch, head) in each cache */
   int cache_dtype; /* path_dtype_t of the caches and of q_t,k_t,v_t,w_t,o_t */
   float scale;     /* logit multiplier */
@@ -214,7 +216,8 @@ size_t path_decode_prefill_workspace_size(const path_decode_desc_t* desc, int pr
  *   v_cache row j = v_j,
  * i.e. exactly what prompt_len calls of path_decode_step from an empty cache would leave there.
  * Computed blockwise in fp32 (64-row chunks: each key moved to its chunk's end, then through the
- * later chunks' transforms right to left) and rounded once to cache_dtype.
+ * later chunks' transforms right to left) and rounded once to cache_dtype.  head_dim 64 only
+ * (128 is PATH_ERR_UNSUPPORTED).
  * k, v, w: [batch][heads][prompt_len][head_dim] in cache_dtype; beta: [batch][heads][prompt_len]
  * float32 (clamped to [0, 2]).  Caches: [batch][heads][capacity][head_dim]; rows >= prompt_len
  * are not touched.  Requires 0 <= prompt_len <= capacity (else PATH_ERR_CAPACITY); prompt_len = 0

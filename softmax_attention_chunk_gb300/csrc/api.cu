@@ -12,10 +12,10 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// bf16 with the default (or 64) chunk runs the tcgen05 kernels; fp32 and chunk 32 run the
-// SIMT kernels.
+// bf16 at head dim 64 with the default (or 64) chunk runs the tcgen05 kernels; fp32, chunk 32
+// and head dim 128 run the SIMT kernels.
 bool uses_tensor_cores(const path_attn_desc_t* d, int /*for_backward*/) {
-  return d->dtype == PATH_BF16 && (d->chunk == 0 || d->chunk == 64);
+  return d->dtype == PATH_BF16 && d->head_dim == kHeadDim && (d->chunk == 0 || d->chunk == 64);
 }
 
 // Validates a descriptor; on success fills g for the requested pass.
@@ -24,11 +24,13 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
   if (d->batch <= 0 || d->heads <= 0 || d->seqlen <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
   if (d->dtype != PATH_BF16 && d->dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
   if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
-  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  if (d->head_dim != kHeadDim && d->head_dim != kHeadDimWide) return PATH_ERR_UNSUPPORTED;
   const long long BH = (long long)d->batch * d->heads;
   if (BH > 65535) return PATH_ERR_UNSUPPORTED;
   if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
-  int B = for_backward ? 32 : (d->chunk ? d->chunk : 64);
+  // head dim 128: the SIMT kernels' shared memory holds 32-row chunks only
+  if (d->head_dim == kHeadDimWide && d->chunk == 64) return PATH_ERR_UNSUPPORTED;
+  int B = for_backward ? 32 : (d->chunk ? d->chunk : (d->head_dim == kHeadDimWide ? 32 : 64));
   // The tensor-core path scans 64-row key chunks and 128-row query tiles.
   if (uses_tensor_cores(d, for_backward)) B = 64;
   long long nc = (d->seqlen + B - 1) / B;
@@ -41,6 +43,7 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
     g->nc = (int)nc;
     g->Lp = (int)(nc * B);
     g->scale = d->scale;
+    g->D = d->head_dim;
   }
   return PATH_OK;
 }
@@ -188,11 +191,12 @@ PATH_API int path_attn_bwd(const path_attn_desc_t* desc, const void* q, const vo
 }
 
 PATH_API size_t path_decode_workspace_size(const path_decode_desc_t* d) {
-  if (!d || d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim != kHeadDim) return 0;
+  if (!d || d->batch <= 0 || d->heads <= 0 || d->capacity <= 0) return 0;
+  if (d->head_dim != kHeadDim && d->head_dim != kHeadDimWide) return 0;
   if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return 0;
   const long long BH = (long long)d->batch * d->heads;
   if (BH > 65535) return 0;
-  return decode_ws_bytes((int)BH);
+  return decode_ws_bytes((int)BH, d->head_dim);
 }
 
 PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* v_cache, int t,
@@ -202,7 +206,7 @@ PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* 
   if (d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
   if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
   if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
-  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  if (d->head_dim != kHeadDim && d->head_dim != kHeadDimWide) return PATH_ERR_UNSUPPORTED;
   const long long BH = (long long)d->batch * d->heads;
   if (BH > 65535) return PATH_ERR_UNSUPPORTED;
   if (t < 0) return PATH_ERR_INVALID_ARG;
@@ -210,10 +214,10 @@ PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* 
   CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(q_t); CHECK_PTR(k_t); CHECK_PTR(v_t);
   CHECK_PTR(w_t); CHECK_PTR(beta_t); CHECK_PTR(o_t);
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
-  if (ws_bytes < decode_ws_bytes((int)BH)) return PATH_ERR_WORKSPACE;
+  if (ws_bytes < decode_ws_bytes((int)BH, d->head_dim)) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_decode(d->cache_dtype == PATH_BF16, (int)BH, d->capacity, t, d->scale,
                                    k_cache, v_cache, q_t, k_t, v_t, w_t, beta_t, o_t, (float*)ws,
-                                   (cudaStream_t)stream));
+                                   (cudaStream_t)stream, nullptr, nullptr, d->head_dim));
 }
 
 // Geometry of the prompt of a prefill hand-off: 64-row chunks over prompt_len rows.
@@ -233,13 +237,14 @@ static int check_decode_desc(const path_decode_desc_t* d) {
   if (d->batch <= 0 || d->heads <= 0 || d->capacity <= 0 || d->head_dim <= 0) return PATH_ERR_INVALID_ARG;
   if (d->cache_dtype != PATH_BF16 && d->cache_dtype != PATH_FP32) return PATH_ERR_INVALID_ARG;
   if (!isfinite(d->scale)) return PATH_ERR_INVALID_ARG;
-  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;
+  if (d->head_dim != kHeadDim && d->head_dim != kHeadDimWide) return PATH_ERR_UNSUPPORTED;
   if ((long long)d->batch * d->heads > 65535) return PATH_ERR_UNSUPPORTED;
   return PATH_OK;
 }
 
 PATH_API size_t path_decode_prefill_workspace_size(const path_decode_desc_t* d, int prompt_len) {
   if (check_decode_desc(d) != PATH_OK || prompt_len < 0 || prompt_len > d->capacity) return 0;
+  if (d->head_dim != kHeadDim) return 0;
   return prefill_ws_bytes(prefill_geom(d, prompt_len), d->cache_dtype == PATH_BF16);
 }
 
@@ -248,6 +253,7 @@ PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, voi
                                  const float* log_f, float* a_cache, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_decode_desc(d);
   if (rc != PATH_OK) return rc;
+  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;  // the hand-off walk is written for d = 64
   if (prompt_len < 0) return PATH_ERR_INVALID_ARG;
   if (prompt_len > d->capacity) return PATH_ERR_CAPACITY;
   CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta);
@@ -274,10 +280,10 @@ PATH_API int path_decode_step_fox(const path_decode_desc_t* d, void* k_cache, vo
   CHECK_PTR(w_t); CHECK_PTR(beta_t); CHECK_PTR(log_f_t); CHECK_PTR(o_t);
   const int BH = d->batch * d->heads;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
-  if (ws_bytes < decode_ws_bytes(BH)) return PATH_ERR_WORKSPACE;
+  if (ws_bytes < decode_ws_bytes(BH, d->head_dim)) return PATH_ERR_WORKSPACE;
   return cuda_status(launch_decode(d->cache_dtype == PATH_BF16, BH, d->capacity, t, d->scale, k_cache, v_cache,
                                    q_t, k_t, v_t, w_t, beta_t, o_t, (float*)ws, (cudaStream_t)stream, a_cache,
-                                   log_f_t));
+                                   log_f_t, d->head_dim));
 }
 
 }  // extern "C"

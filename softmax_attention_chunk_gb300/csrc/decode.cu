@@ -13,10 +13,7 @@
 namespace pathattn {
 namespace {
 
-constexpr int NT = 256;          // 32 key groups x 8 lanes
-constexpr int D = kHeadDim;
-constexpr int LANES = 8;         // lanes per key; each owns 8 consecutive elements
-constexpr int GROUPS = NT / LANES;
+constexpr int NT = 256;          // key groups x (head dim / 8) lanes
 constexpr int UNROLL = 4;        // keys in flight per group
 
 template <typename T> struct Vec8;
@@ -58,17 +55,21 @@ template <> struct Vec8<float> {
   }
 };
 
-// grid (nsplit, BH).  Split s covers rows [s*per, min((s+1)*per, t+1)) of its head.
-// Writes partial (m [log2 domain], l, acc[64]) to partials[(bh*kDecodeMaxSplits + s)*(D+2)].
+// grid (nsplit, BH).  Split s covers rows [s*per, min((s+1)*per, t+1)) of its head.  A key is
+// read by D / 8 lanes, each owning 8 consecutive elements (one 16-byte vector in bf16), so the
+// CTA streams 256 / (D / 8) keys at a time (32 at D = 64, 16 at D = 128).
+// Writes partial (m [log2 domain], l, acc[D]) to partials[(bh*kDecodeMaxSplits + s)*(D+2)].
 // FOX (PaTH-FoX, notes §2.5): the logit of key j gains sum_{s=j+1..t} log f_s = A_t - a_j, with
 // ac[bh][j] = a_j the prefix sums of log f kept beside the cache; A_t = a_{t-1} + log f_t is
 // stored as row t.
-template <typename T, bool FOX>
+template <typename T, bool FOX, int D>
 __global__ void __launch_bounds__(NT) decode_split_kernel(
     int cap, int t, int per, float scale, T* __restrict__ kc, T* __restrict__ vc,
     const T* __restrict__ qt, const T* __restrict__ kt, const T* __restrict__ vt,
     const T* __restrict__ wt, const float* __restrict__ beta_t, float* __restrict__ partials,
     float* __restrict__ ac, const float* __restrict__ logf_t) {
+  constexpr int LANES = D / 8;  // lanes per key; each owns 8 consecutive elements
+  constexpr int GROUPS = NT / LANES;
   __shared__ float s_m[GROUPS], s_l[GROUPS];
   __shared__ float s_acc[GROUPS][D + 1];
 
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int j = base + grp + u * GROUPS;
-      const bool valid = j < j1;  // uniform within the 8-lane group
+      const bool valid = j < j1;  // uniform within the lane group
       float kf[8];
       kv[u].to_float(kf);
       float a = 0.f, qk = 0.f;
@@ -192,8 +193,8 @@ __global__ void __launch_bounds__(NT) decode_split_kernel(
   }
 }
 
-// grid BH, block 64: merge the per-split states of one head and write o_t.
-template <typename T>
+// grid BH, block D: merge the per-split states of one head and write o_t.
+template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(int nsplit, const float* __restrict__ partials,
                                                            T* __restrict__ o) {
   const int bh = blockIdx.x, c = threadIdx.x;
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(int nsplit, const flo
   o[(size_t)bh * D + c] = from_f<T>(a / l);
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, const void* q,
                      const void* k, const void* v, const void* w, const float* beta, void* o,
                      float* partials, float* ac, const float* logf_t, cudaStream_t st) {
@@ -224,14 +225,14 @@ cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, co
   const int per = (n + nsplit - 1) / nsplit;
   nsplit = (n + per - 1) / per;
   if (ac)
-    decode_split_kernel<T, true><<<dim3(nsplit, BH), NT, 0, st>>>(
+    decode_split_kernel<T, true, D><<<dim3(nsplit, BH), NT, 0, st>>>(
         cap, t, per, scale, (T*)kc, (T*)vc, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta,
         partials, ac, logf_t);
   else
-    decode_split_kernel<T, false><<<dim3(nsplit, BH), NT, 0, st>>>(
+    decode_split_kernel<T, false, D><<<dim3(nsplit, BH), NT, 0, st>>>(
         cap, t, per, scale, (T*)kc, (T*)vc, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta,
         partials, nullptr, nullptr);
-  decode_combine_kernel<T><<<BH, D, 0, st>>>(nsplit, partials, (T*)o);
+  decode_combine_kernel<T, D><<<BH, D, 0, st>>>(nsplit, partials, (T*)o);
   return cudaGetLastError();
 }
 
@@ -240,9 +241,15 @@ cudaError_t decode_t(int BH, int cap, int t, float scale, void* kc, void* vc, co
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
                           const void* q, const void* k, const void* v, const void* w,
                           const float* beta, void* o, float* partials, cudaStream_t st, float* ac,
-                          const float* logf_t) {
-  return is_bf16 ? decode_t<__nv_bfloat16>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st)
-                 : decode_t<float>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st);
+                          const float* logf_t, int D) {
+  if (D == kHeadDim)
+    return is_bf16 ? decode_t<__nv_bfloat16, kHeadDim>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st)
+                   : decode_t<float, kHeadDim>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st);
+  if (D == kHeadDimWide)
+    return is_bf16 ? decode_t<__nv_bfloat16, kHeadDimWide>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac,
+                                                           logf_t, st)
+                   : decode_t<float, kHeadDimWide>(BH, cap, t, scale, kc, vc, q, k, v, w, beta, o, partials, ac, logf_t, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pathattn

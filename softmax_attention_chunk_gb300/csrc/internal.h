@@ -8,7 +8,8 @@
 
 namespace pathattn {
 
-constexpr int kHeadDim = 64;
+constexpr int kHeadDim = 64;      // head dim of the tensor-core path (and the default)
+constexpr int kHeadDimWide = 128;  // the other head dim: fp32 SIMT kernels and decode
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -28,6 +29,7 @@ struct Geom {
   int nc;       // number of chunks = ceil(L / B)
   int Lp;       // padded length nc * B
   float scale;
+  int D = kHeadDim;  // head dim (kHeadDim or kHeadDimWide)
 };
 
 // Byte offsets of the forward workspace.  Element type "E" of ql/kr/f is float32 for the SIMT
@@ -45,12 +47,12 @@ inline FwdWs fwd_ws_layout(const Geom& g, size_t esize, size_t base = 0) {
   size_t off = base;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t rows = (size_t)g.BH * g.Lp;
-  w.ql = take(rows * kHeadDim * esize);
-  w.kr = take(rows * kHeadDim * esize);
-  w.f = take((size_t)g.BH * g.nc * kHeadDim * kHeadDim * esize);
+  w.ql = take(rows * g.D * esize);
+  w.kr = take(rows * g.D * esize);
+  w.f = take((size_t)g.BH * g.nc * g.D * g.D * esize);
   w.dm = take(rows * 4);
   w.dl = take(rows * 4);
-  w.dacc = take(rows * kHeadDim * 4);
+  w.dacc = take(rows * g.D * 4);
   w.fa = take(rows * 4);
   w.fr = take(rows * 4);
   w.ft = take((size_t)g.BH * g.nc * 4);
@@ -84,12 +86,12 @@ inline BwdWs bwd_ws_layout(const Geom& g) {
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t rows = (size_t)g.BH * g.Lp;
   w.Dv = take(rows * 4);
-  w.dql = take(rows * kHeadDim * 4);
-  w.dkr = take(rows * kHeadDim * 4);
-  w.dv = take(rows * kHeadDim * 4);
-  w.df = take((size_t)g.BH * g.nc * kHeadDim * kHeadDim * 4);
+  w.dql = take(rows * g.D * 4);
+  w.dkr = take(rows * g.D * 4);
+  w.dv = take(rows * g.D * 4);
+  w.df = take((size_t)g.BH * g.nc * g.D * g.D * 4);
   w.nctas = bwd_num_ctas(g);
-  w.zs = take((size_t)w.nctas * g.Lp * kHeadDim * 4);
+  w.zs = take((size_t)w.nctas * g.Lp * g.D * 4);
   w.fxa = take(rows * 4);
   w.fxcs = take(rows * 4);
   w.total = off;
@@ -144,8 +146,8 @@ inline TcWs tc_ws_layout(int BH, int L, float scale, bool for_backward) {
   return w;
 }
 
-inline size_t decode_ws_bytes(int BH) {
-  return align_up((size_t)BH * kDecodeMaxSplits * (kHeadDim + 2) * 4, 256);
+inline size_t decode_ws_bytes(int BH, int D = kHeadDim) {
+  return align_up((size_t)BH * kDecodeMaxSplits * (D + 2) * 4, 256);
 }
 
 // ---- launchers (return cudaGetLastError() of their launches) ----
@@ -155,7 +157,8 @@ inline size_t decode_ws_bytes(int BH) {
 cudaError_t launch_fox_prefix(const Geom& g, const float* logf, float* A, cudaStream_t st);
 cudaError_t launch_fox_dlogf(const Geom& g, const float* cs, float* dlogf, cudaStream_t st);
 
-// SIMT (fp32 arithmetic) forward.  is_bf16 selects the input element type.
+// SIMT (fp32 arithmetic) forward.  is_bf16 selects the input element type; g.D is 64 (chunk 32
+// or 64) or 128 (chunk 32).
 cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                              const void* v, const void* w, const float* beta, const float* logf,
                              char* ws, const FwdWs& lay, bool with_diag, cudaStream_t st);
@@ -214,9 +217,10 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
 // Decode step.
 // ac / logf_t (PaTH-FoX, both set or both null): prefix sums of log f beside the cache
 // ([BH][cap] fp32, rows 0..t-1 valid, row t written) and this step's log f ([BH]).
+// D: head dim (kHeadDim or kHeadDimWide); partials hold decode_ws_bytes(BH, D) bytes.
 cudaError_t launch_decode(bool is_bf16, int BH, int cap, int t, float scale, void* kc, void* vc,
                           const void* q, const void* k, const void* v, const void* w,
                           const float* beta, void* o, float* partials, cudaStream_t st, float* ac = nullptr,
-                          const float* logf_t = nullptr);
+                          const float* logf_t = nullptr, int D = kHeadDim);
 
 }  // namespace pathattn

@@ -21,8 +21,7 @@ namespace pathattn {
 namespace {
 
 constexpr int NT = 256;
-constexpr int D = kHeadDim;
-constexpr int DS = D + 1;
+// D (template parameter): head dim, 64 or 128; DS = D + 1 is the padded smem row stride.
 
 // D_i = dO_i . o_i; padded rows get 0.  A row is read by a group of D / VEC lanes with 16-byte
 // loads (VEC elements each), a warp covers DOT_PASSES row groups with all loads issued before the
@@ -47,7 +46,7 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b) {
     return acc;
   }
 }
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(NT) bwd_dot_kernel(Geom g, const T* __restrict__ o,
                                                      const T* __restrict__ dO, float* __restrict__ Dv) {
   constexpr int VEC = 16 / (int)sizeof(T);
@@ -78,15 +77,16 @@ __global__ void __launch_bounds__(NT) bwd_dot_kernel(Geom g, const T* __restrict
     if (l == 0 && row < rows) Dv[row] = acc;
   }
 }
-template <typename T>
+template <typename T, int D>
 unsigned dot_blocks(const Geom& g) {
   constexpr int rows_per_block = (NT / 32) * (32 / (D / (16 / (int)sizeof(T)))) * DOT_PASSES;
   const long rows = (long)g.BH * g.Lp;
   return (unsigned)((rows + rows_per_block - 1) / rows_per_block);
 }
 
-template <int B>
+template <int B, int D>
 struct BwdMainSmem {
+  static constexpr int DS = D + 1;
   static constexpr int BS = B + 1;
   static constexpr int kZ = 0, kK = kZ + B * DS, kV = kK + B * DS, kF = kV + B * DS;
   static constexpr int kdO = kF + D * DS, kG = kdO + B * DS, kGn = kG + B * DS;
@@ -97,7 +97,7 @@ struct BwdMainSmem {
 };
 
 // Persistent CTAs; tile n (heaviest first) is query chunk b = nc-1 - n/BH of head n%BH.
-template <typename T, int B, bool FOX>
+template <typename T, int B, bool FOX, int D>
 __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     Geom g, const T* __restrict__ v, const float* __restrict__ lse, const T* __restrict__ dO,
     const float* __restrict__ Dv, const float* __restrict__ ql, const float* __restrict__ kr,
@@ -105,8 +105,8 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     float* __restrict__ dvacc, float* __restrict__ dfacc, float* __restrict__ zs,
     const float* __restrict__ fxa, float* __restrict__ fxcs) {
   extern __shared__ float sm[];
-  using S = BwdMainSmem<B>;
-  constexpr int BS = S::BS;
+  using S = BwdMainSmem<B, D>;
+  constexpr int BS = S::BS, DS = S::DS;
   float* sZ = sm + S::kZ;
   float* sK = sm + S::kK;
   float* sV = sm + S::kV;
@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
   }
 }
 
-template <int B>
+template <int B, int D>
 struct PrepBwdSmem {
+  static constexpr int DS = D + 1;
   static constexpr int BS = B + 1;
   static constexpr int nBD = 8, nBB = 11;
   static constexpr int kBD = 0, kBB = kBD + nBD * B * DS;
@@ -255,7 +256,7 @@ struct PrepBwdSmem {
 // One CTA per (chunk c, head bh): diagonal-chunk attention backward and the chain rule through
 // Q<- = Q - lower(QW^T) U W, K-> = K - X^T W, F = I - W^T U^T W, X = U strictLower(W K^T),
 // S_d = lower(QK^T) - lower(QW^T) X, U = Y D with Y = (I + strictLower(D W W^T))^{-1}.
-template <typename T, int B, bool FOX>
+template <typename T, int B, bool FOX, int D>
 __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ lse,
@@ -264,8 +265,8 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, T* __restrict__ dw,
     float* __restrict__ dbeta, const float* __restrict__ fxa, float* __restrict__ fxcs) {
   extern __shared__ float sm[];
-  using S = PrepBwdSmem<B>;
-  constexpr int BS = S::BS;
+  using S = PrepBwdSmem<B, D>;
+  constexpr int BS = S::BS, DS = S::DS;
   float* bd = sm + S::kBD;
   float* sW = bd + 0 * B * DS;
   float* sQ = bd + 1 * B * DS;
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(NT) prep_bwd_simt_kernel(
     if (row0 + r < g.L) dbeta[in_row + row0 + r] = sgB[r];
 }
 
-template <typename T, int B>
+template <typename T, int B, int D>
 cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                   const float* beta, const void* o, const float* lse, const void* dO, void* dq,
                   void* dk, void* dv, void* dw, float* dbeta, char* ws, const BwdWs& lay,
@@ -506,15 +507,15 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
   if ((e = cudaMemsetAsync(ws + lay.dkr, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws + lay.df, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
-  bwd_dot_kernel<T><<<dot_blocks<T>(g), NT, 0, st>>>(g, (const T*)o, (const T*)dO, (float*)(ws + lay.Dv));
+  bwd_dot_kernel<T, D><<<dot_blocks<T, D>(g), NT, 0, st>>>(g, (const T*)o, (const T*)dO, (float*)(ws + lay.Dv));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prep_simt(std::is_same<T, __nv_bfloat16>::value, g, q, k, v, w, beta, nullptr, ws,
                             lay.fw, false, st)) != cudaSuccess)
     return e;
   }
   if (phases & 2) {
-    auto kern = logf ? bwd_main_simt_kernel<T, B, true> : bwd_main_simt_kernel<T, B, false>;
-    const size_t smem = BwdMainSmem<B>::bytes;
+    auto kern = logf ? bwd_main_simt_kernel<T, B, true, D> : bwd_main_simt_kernel<T, B, false, D>;
+    const size_t smem = BwdMainSmem<B, D>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<lay.nctas, NT, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
                                       (const float*)(ws + lay.fw.ql), (const float*)(ws + lay.fw.kr),
@@ -524,8 +525,8 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (phases & 4) {
-    auto kern = logf ? prep_bwd_simt_kernel<T, B, true> : prep_bwd_simt_kernel<T, B, false>;
-    const size_t smem = PrepBwdSmem<B>::bytes;
+    auto kern = logf ? prep_bwd_simt_kernel<T, B, true, D> : prep_bwd_simt_kernel<T, B, false, D>;
+    const size_t smem = PrepBwdSmem<B, D>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<dim3(g.nc, g.BH), NT, smem, st>>>(
         g, (const T*)q, (const T*)k, (const T*)v, (const T*)w, beta, lse, (const T*)dO,
@@ -541,7 +542,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
 }  // namespace
 
 cudaError_t launch_bwd_dot(const Geom& g, const void* o, const void* dO, float* Dv, cudaStream_t st) {
-  bwd_dot_kernel<__nv_bfloat16><<<dot_blocks<__nv_bfloat16>(g), NT, 0, st>>>(
+  bwd_dot_kernel<__nv_bfloat16, kHeadDim><<<dot_blocks<__nv_bfloat16, kHeadDim>(g), NT, 0, st>>>(
       g, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, Dv);
   return cudaGetLastError();
 }
@@ -552,10 +553,16 @@ cudaError_t launch_bwd_simt(bool is_bf16, const Geom& g, const void* q, const vo
                             void* dw, float* dbeta, char* ws, const BwdWs& lay, int phases,
                             cudaStream_t st, const float* logf, float* dlogf) {
   if (g.B != 32 || (dlogf && !logf)) return cudaErrorInvalidValue;
-  return is_bf16 ? bwd_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases,
-                                            st, logf, dlogf)
-                 : bwd_t<float, 32>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases, st,
-                                    logf, dlogf);
+  if (g.D == kHeadDimWide)
+    return is_bf16 ? bwd_t<__nv_bfloat16, 32, kHeadDimWide>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws,
+                                                            lay, phases, st, logf, dlogf)
+                   : bwd_t<float, 32, kHeadDimWide>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay,
+                                                    phases, st, logf, dlogf);
+  if (g.D != kHeadDim) return cudaErrorInvalidValue;
+  return is_bf16 ? bwd_t<__nv_bfloat16, 32, kHeadDim>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay,
+                                                      phases, st, logf, dlogf)
+                 : bwd_t<float, 32, kHeadDim>(g, q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta, ws, lay, phases,
+                                              st, logf, dlogf);
 }
 
 }  // namespace pathattn

@@ -13,11 +13,11 @@ namespace pathattn {
 namespace {
 
 constexpr int NT = 256;
-constexpr int D = kHeadDim;
-constexpr int DS = D + 1;  // padded smem row stride of [rows][64] matrices
 
-template <int B>
+// D: head dim (64 or 128); DS = D + 1 is the padded smem row stride of [rows][D] matrices.
+template <int B, int D>
 struct PrepSmem {
+  static constexpr int DS = D + 1;
   static constexpr int BS = B + 1;
   static constexpr int kW = 0, kQ = kW + B * DS, kK = kQ + B * DS, kV = kK + B * DS;
   static constexpr int kU = kV + B * DS, kM1 = kU + B * BS, kX = kM1 + B * BS, kT = kX + B * BS;
@@ -31,7 +31,7 @@ struct PrepSmem {
 // One CTA per (chunk c, head bh).  Writes Q<-, K->, F, the diagonal-chunk softmax state and
 // the chunk-local forget-gate sums.  Rows beyond L are padding with q=k=v=w=0, beta=0
 // (H = I), log f = 0.
-template <typename T, int B, typename OutT>
+template <typename T, int B, typename OutT, int D>
 __global__ void __launch_bounds__(NT) prep_simt_kernel(
     Geom g, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ logf,
@@ -39,8 +39,8 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
     float* __restrict__ dl, float* __restrict__ dacc, float* __restrict__ fa,
     float* __restrict__ fr, float* __restrict__ ft, int with_diag) {
   extern __shared__ float sm[];
-  using S = PrepSmem<B>;
-  constexpr int BS = S::BS;
+  using S = PrepSmem<B, D>;
+  constexpr int BS = S::BS, DS = S::DS;
   float* sW = sm + S::kW;
   float* sQ = sm + S::kQ;
   float* sK = sm + S::kK;
@@ -193,8 +193,9 @@ __global__ void __launch_bounds__(NT) prep_simt_kernel(
   }
 }
 
-template <int B>
+template <int B, int D>
 struct MainSmem {
+  static constexpr int DS = D + 1;
   static constexpr int BS = B + 1;
   static constexpr int kZ = 0, kZn = kZ + B * DS, kK = kZn + B * DS, kV = kK + B * DS;
   static constexpr int kF = kV + B * DS, kP = kF + D * DS, kR = kP + B * BS;
@@ -204,15 +205,15 @@ struct MainSmem {
 
 // One CTA per (query chunk b, head bh): starts from the diagonal-chunk state and scans the
 // earlier chunks right to left: S = Z K->_c^T, online softmax, O += P V_c, Z <- Z F_c^T.
-template <typename T, int B>
+template <typename T, int B, int D>
 __global__ void __launch_bounds__(NT) main_simt_kernel(
     Geom g, const T* __restrict__ v, const float* __restrict__ ql, const float* __restrict__ kr,
     const float* __restrict__ f, const float* __restrict__ dm, const float* __restrict__ dl,
     const float* __restrict__ dacc, const float* __restrict__ fa, const float* __restrict__ fr,
     const float* __restrict__ ft, int fox, T* __restrict__ o, float* __restrict__ lse) {
   extern __shared__ float sm[];
-  using S = MainSmem<B>;
-  constexpr int BS = S::BS;
+  using S = MainSmem<B, D>;
+  constexpr int BS = S::BS, DS = S::DS;
   constexpr int NSUB = NT / B;
   constexpr int OC = D / NSUB;
   constexpr int SC = B / NSUB;
@@ -312,12 +313,12 @@ __global__ void __launch_bounds__(NT) main_simt_kernel(
   }
 }
 
-template <typename T, int B, typename OutT = float>
+template <typename T, int B, int D, typename OutT = float>
 cudaError_t prep_t(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                    const float* beta, const float* logf, char* ws, const FwdWs& lay,
                    bool with_diag, cudaStream_t st) {
-  auto kern = prep_simt_kernel<T, B, OutT>;
-  const size_t smem = PrepSmem<B>::bytes;
+  auto kern = prep_simt_kernel<T, B, OutT, D>;
+  const size_t smem = PrepSmem<B, D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(g.nc, g.BH);
@@ -329,11 +330,11 @@ cudaError_t prep_t(const Geom& g, const void* q, const void* k, const void* v, c
   return cudaGetLastError();
 }
 
-template <typename T, int B>
+template <typename T, int B, int D>
 cudaError_t main_t(const Geom& g, const void* v, const float* logf, char* ws, const FwdWs& lay,
                    void* o, float* lse, cudaStream_t st) {
-  auto kern = main_simt_kernel<T, B>;
-  const size_t smem = MainSmem<B>::bytes;
+  auto kern = main_simt_kernel<T, B, D>;
+  const size_t smem = MainSmem<B, D>::bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(g.nc, g.BH);
@@ -350,23 +351,35 @@ cudaError_t main_t(const Geom& g, const void* v, const float* logf, char* ws, co
 cudaError_t launch_prep_simt(bool is_bf16, const Geom& g, const void* q, const void* k,
                              const void* v, const void* w, const float* beta, const float* logf,
                              char* ws, const FwdWs& lay, bool with_diag, cudaStream_t st) {
+  if (g.D == kHeadDimWide) {
+    if (g.B != 32) return cudaErrorInvalidValue;
+    return is_bf16 ? prep_t<__nv_bfloat16, 32, kHeadDimWide>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
+                   : prep_t<float, 32, kHeadDimWide>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
+  }
+  if (g.D != kHeadDim) return cudaErrorInvalidValue;
   if (g.B == 32)
-    return is_bf16 ? prep_t<__nv_bfloat16, 32>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
-                   : prep_t<float, 32>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
+    return is_bf16 ? prep_t<__nv_bfloat16, 32, kHeadDim>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
+                   : prep_t<float, 32, kHeadDim>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
   if (g.B == 64)
-    return is_bf16 ? prep_t<__nv_bfloat16, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
-                   : prep_t<float, 64>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
+    return is_bf16 ? prep_t<__nv_bfloat16, 64, kHeadDim>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st)
+                   : prep_t<float, 64, kHeadDim>(g, q, k, v, w, beta, logf, ws, lay, with_diag, st);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const float* logf,
                              char* ws, const FwdWs& lay, void* o, float* lse, cudaStream_t st) {
+  if (g.D == kHeadDimWide) {
+    if (g.B != 32) return cudaErrorInvalidValue;
+    return is_bf16 ? main_t<__nv_bfloat16, 32, kHeadDimWide>(g, v, logf, ws, lay, o, lse, st)
+                   : main_t<float, 32, kHeadDimWide>(g, v, logf, ws, lay, o, lse, st);
+  }
+  if (g.D != kHeadDim) return cudaErrorInvalidValue;
   if (g.B == 32)
-    return is_bf16 ? main_t<__nv_bfloat16, 32>(g, v, logf, ws, lay, o, lse, st)
-                   : main_t<float, 32>(g, v, logf, ws, lay, o, lse, st);
+    return is_bf16 ? main_t<__nv_bfloat16, 32, kHeadDim>(g, v, logf, ws, lay, o, lse, st)
+                   : main_t<float, 32, kHeadDim>(g, v, logf, ws, lay, o, lse, st);
   if (g.B == 64)
-    return is_bf16 ? main_t<__nv_bfloat16, 64>(g, v, logf, ws, lay, o, lse, st)
-                   : main_t<float, 64>(g, v, logf, ws, lay, o, lse, st);
+    return is_bf16 ? main_t<__nv_bfloat16, 64, kHeadDim>(g, v, logf, ws, lay, o, lse, st)
+                   : main_t<float, 64, kHeadDim>(g, v, logf, ws, lay, o, lse, st);
   return cudaErrorInvalidValue;
 }
 

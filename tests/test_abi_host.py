@@ -62,7 +62,13 @@ def test_descriptor_validation(pa):
     assert pa.path_attn_chunk(desc(pa), 0) == 64
     assert pa.path_attn_chunk(desc(pa, chunk=32), 0) == 32
     assert pa.path_attn_chunk(desc(pa), 1) > 0
-    assert pa.path_attn_chunk(desc(pa, head_dim=128), 0) == -2          # unsupported
+    assert pa.path_attn_chunk(desc(pa, head_dim=96), 0) == -2           # unsupported head dim
+    # head dim 128 runs the fp32 SIMT kernels, whose shared memory holds 32-row chunks
+    assert pa.path_attn_chunk(desc(pa, head_dim=128), 0) == 32
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16), 0) == 32
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, chunk=64), 0) == -2
+    assert pa.path_attn_chunk(desc(pa, head_dim=128), 1) == 32
+    assert pa.path_attn_workspace_size(desc(pa, head_dim=128), 1) > pa.path_attn_workspace_size(desc(pa), 1)
     assert pa.path_attn_chunk(desc(pa, head_dim=0), 0) == -1            # invalid
     assert pa.path_attn_chunk(desc(pa, seqlen=0), 0) == -1
     assert pa.path_attn_chunk(desc(pa, dtype=7), 0) == -1
@@ -95,7 +101,9 @@ def test_fwd_argument_errors(pa):
     assert call_fwd(pa, d, **fwd_args(pa, d, k=FAKE + 8, ws_bytes=0)) == 1         # misaligned
     assert call_fwd(pa, d, **fwd_args(pa, d, ws=FAKE + 16, ws_bytes=0)) == 1       # ws not 256-aligned
     assert call_fwd(pa, d, **fwd_args(pa, d, log_f=FAKE + 4, ws_bytes=0)) == 1
-    assert call_fwd(pa, desc(pa, head_dim=128), **fwd_args(pa, d)) == 2
+    assert call_fwd(pa, desc(pa, head_dim=96), **fwd_args(pa, d)) == 2
+    d128 = desc(pa, head_dim=128)
+    assert call_fwd(pa, d128, **fwd_args(pa, d128, ws_bytes=pa.path_attn_workspace_size(d128, 0) - 1)) == 3
     assert pa._lib.path_attn_fwd(None, *([FAKE] * 8), FAKE, 0, None) == 1
     for bad in (0, 4, 8):
         assert pa.path_attn_fwd_phases(bad, d, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 0, None) in (1, 3)
@@ -135,9 +143,14 @@ def test_decode_argument_errors(pa):
     assert pa.path_decode_step(dd, FAKE, FAKE, -1, *vec, FAKE, n, None) == 1
     assert pa.path_decode_step(dd, FAKE, FAKE, 5, *vec, FAKE, n - 1, None) == 3
     assert pa.path_decode_step(dd, None, FAKE, 5, *vec, FAKE, n, None) == 1
-    bad = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
+    bad = pa.path_decode_desc_t(2, 2, 96, 100, pa.PATH_BF16, 1.0)
     assert pa.path_decode_workspace_size(bad) == 0
     assert pa.path_decode_step(bad, FAKE, FAKE, 5, *vec, FAKE, n, None) == 2
+    # head dim 128: partials of 128 + 2 floats per split
+    wide = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
+    n128 = pa.path_decode_workspace_size(wide)
+    assert n128 > n
+    assert pa.path_decode_step(wide, FAKE, FAKE, 5, *vec, FAKE, n128 - 1, None) == 3
 
 
 def test_prefill_argument_errors(pa):

@@ -423,3 +423,105 @@ def test_bwd_bf16_fox_training_step_reuse(cuda_lib):
                phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
     torch.cuda.synchronize()
     check_grads_fox(inp, g, 0.7, 2e-2, 3e-2)
+
+
+# ---------------- head dim 128 (fp32 SIMT kernels, 32-row chunks; decode) ----------------
+
+@pytest.mark.parametrize("L,fox", [(1, False), (33, False), (100, False), (200, True)])
+def test_fwd_d128_fp32(cuda_lib, L, fox):
+    """Head dim 128 in the fp32 mode: outputs and lse within 1e-4 of the oracle (F is 128 x 128)."""
+    inp = gen_path_inputs(1, 2, L, 128, "fp32", seed=700 + L, near2_frac=0.1, fox=fox)
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(flat(o), o_ref, 1e-4, "o")
+    check(flat(lse), lse_ref, 1e-4, "lse")
+
+
+def test_fwd_d128_bf16(cuda_lib):
+    inp = gen_path_inputs(2, 2, 300, 128, "bf16", seed=710, near2_frac=0.05)
+    o, lse = run_fwd(inp, 1.0)
+    o_ref, lse_ref = oracle_fwd(inp, 1.0)
+    check(flat(o), o_ref, 2e-2, "o", rel=2e-2)
+    check(flat(lse), lse_ref, 2e-2, "lse")
+
+
+@pytest.mark.parametrize("L", [31, 100])
+def test_bwd_d128_fp32(cuda_lib, L):
+    inp = gen_path_inputs(1, 2, L, 128, "fp32", seed=720 + L, with_dO=True, near2_frac=0.1)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 1e-4)
+
+
+def test_bwd_d128_fp32_fox(cuda_lib):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    inp = gen_path_inputs(1, 2, 90, 128, "fp32", seed=731, with_dO=True, near2_frac=0.1, fox=True)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=1.0)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=1.0, log_f=t["log_f"])
+    torch.cuda.synchronize()
+    check_grads_fox(inp, g, 1.0, 1e-4, None)
+
+
+def test_bwd_d128_bf16(cuda_lib):
+    inp = gen_path_inputs(1, 2, 200, 128, "bf16", seed=740, with_dO=True, near2_frac=0.05)
+    g = run_bwd(inp, 1.0)
+    check_grads(inp, g, 1.0, 2e-2, rel=3e-2)
+
+
+@pytest.mark.parametrize("dtype,t0,steps,tol", [("fp32", 0, 20, 1e-4), ("fp32", 3000, 4, 1e-4),
+                                                ("bf16", 4000, 4, 2e-2)])
+def test_decode_d128_steps(cuda_lib, dtype, t0, steps, tol):
+    """Decode at head dim 128 (16 lanes per key) against the oracle step by step."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    B, H, d = 2, 2, 128
+    di = gen_decode_inputs(B, H, d, t0=t0, steps=steps, dtype=dtype, seed=750 + t0)
+    kc, vc = di["k_cache"].to(DEV), di["v_cache"].to(DEV)
+    kref = np64(di["k_cache"]).reshape(B * H, -1, d).copy()
+    vref = np64(di["v_cache"]).reshape(B * H, -1, d).copy()
+    for s in range(steps):
+        args = [di[n][s].to(DEV) for n in ("q", "k", "v", "w", "beta")]
+        o_t = pa.decode_step(kc, vc, t0 + s, *args, scale=1.0)
+        torch.cuda.synchronize()
+        o_r = orc.decode_step(kref, vref, t0 + s, *[flat(di[n][s]) for n in ("q", "k", "v", "w", "beta")], 1.0)
+        check(o_t.reshape(B * H, d), o_r, tol, f"o_t step {s}", rel=2e-2 if dtype == "bf16" else None)
+    n = t0 + steps
+    check(kc.reshape(B * H, -1, d)[:, :n], kref[:, :n], tol, "rewritten keys")
+    check(vc.reshape(B * H, -1, d)[:, :n], vref[:, :n], 0.0, "values")
+
+
+def test_fox_decode_d128_steps(cuda_lib):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    t0, steps = 2000, 4
+    di = gen_decode_inputs(1, 3, 128, t0=t0, steps=steps, dtype="fp32", seed=761, fox=True)
+    kc, vc, ac = di["k_cache"].to(DEV), di["v_cache"].to(DEV), di["a_cache"].to(DEV)
+    kref, vref = np64(flat(di["k_cache"])).copy(), np64(flat(di["v_cache"])).copy()
+    aref = np64(flat(di["a_cache"])).copy()
+    for s in range(steps):
+        x = {n: di[n][s].to(DEV) for n in ("q", "k", "v", "w", "beta", "log_f")}
+        o = pa.decode_step_fox(kc, vc, ac, t0 + s, x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], scale=1.0)
+        torch.cuda.synchronize()
+        o_r = orc.decode_step_fox(kref, vref, aref, t0 + s, *(flat(di[n][s]) for n in ("q", "k", "v", "w", "beta")),
+                                  flat(di["log_f"][s]), 1.0)
+        check(flat(o), o_r, 1e-4, f"o[{s}]")
+    check(flat(kc)[:, :t0 + steps], kref[:, :t0 + steps], 1e-4, "k_cache")
+
+
+def test_decode_d128_matches_forward_rows(cuda_lib):
+    """At head dim 128 too, decoding token by token from an empty cache gives the forward's rows."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    L = 40
+    inp = gen_path_inputs(1, 2, L, 128, "fp32", seed=771)
+    o_f, _ = run_fwd(inp, 1.0)
+    kc = torch.zeros(1, 2, L, 128, device=DEV)
+    vc = torch.zeros_like(kc)
+    rows = []
+    for t in range(L):
+        sl = lambda x: x[:, :, t].contiguous().to(DEV)
+        rows.append(pa.decode_step(kc, vc, t, sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["w"]),
+                                   sl(inp["beta"]), scale=1.0))
+    o_d = torch.stack(rows, 2)
+    assert (o_d - o_f).abs().max().item() <= 1e-4

@@ -54,7 +54,7 @@ def softmax_attend(S, v):
 
 
 @pytest.mark.parametrize("L,d,fox,scale", [(1, 3, False, 1.0), (7, 4, False, 0.7), (12, 8, True, 1.3),
-                                           (11, 5, True, 2.0)])
+                                           (11, 5, True, 2.0), (9, 128, True, 1.0)])
 def test_logits_and_outputs_match_explicit_products(L, d, fox, scale):
     rng = np.random.default_rng(L * 100 + d)
     q, k, v, w, beta, logf = rand_problem(rng, L, d, fox=fox)
