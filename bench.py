@@ -86,6 +86,7 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-d128", action="store_true", help="skip the head-dim-128 measurements")
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
@@ -104,7 +105,7 @@ def peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
-                    src="measured")
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
@@ -444,6 +445,8 @@ def run_ours(args):
     torch.cuda.empty_cache()
     handoff = None if args.no_decode else run_prefill_handoff(args, pa, dev, pk)
     torch.cuda.empty_cache()
+    d128 = None if (args.no_decode or args.no_d128) else run_head_dim_128(args, pa, dev, pk)
+    torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(dict(CONFIGS[FWD_CFG]), B_f, B_b)
@@ -460,7 +463,8 @@ def run_ours(args):
                 "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward,
                 "fox_train": fox_train, "e2e": e2e,
                 "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 5 * args.steps,
-                "peaks": pk, "decode": dec, "prefill_handoff": handoff, "cpu_baseline": cpu}
+                "peaks": pk, "decode": dec, "prefill_handoff": handoff, "head_dim_128": d128,
+                "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -563,6 +567,81 @@ def run_prefill_handoff(args, pa, dev, pk):
             "bound": "latency: the per-chunk tcgen05 UT preparation (fp32 F from split bf16 products) and the "
                      "per-head fp32 suffix walk (one CTA per head, chunks right to left)",
             "gpu_launches": 2, "workload": "prefill -> decode hand-off, batch 32, 32 heads, d=64, prompt 32768 bf16"}
+
+
+def run_head_dim_128(args, pa, dev, pk):
+    """Head dim 128: the decode step (batch 32, 32 heads, bf16 cache of 32768 entries, 32 steps;
+    HBM bound, against the copy peak) and a training step on the fp32 CUDA-core kernels (batch 4,
+    16 heads, L 2048, bf16 inputs, 32-row chunks; against the FP32 FMA peak 152 SMs x 128 lanes x
+    2 flop x the maximum SM clock).  Inputs drawn on the device."""
+    g = torch.Generator(device=dev).manual_seed(4242)
+    sd = 1.0 / math.sqrt(128)
+    # ---- decode ----
+    Bt, H, d, t0, steps = 32, 32, 128, 32768, 32
+    kc = (torch.randn(Bt, H, t0 + steps, d, device=dev, generator=g) * sd).to(torch.bfloat16)
+    vc = (torch.randn(Bt, H, t0 + steps, d, device=dev, generator=g) * sd).to(torch.bfloat16)
+
+    def unit(*shape):
+        x = torch.randn(*shape, device=dev, generator=g)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    sx = {"q": (torch.randn(steps, Bt, H, d, device=dev, generator=g) * sd).to(torch.bfloat16),
+          "k": (torch.randn(steps, Bt, H, d, device=dev, generator=g) * sd).to(torch.bfloat16),
+          "v": (torch.randn(steps, Bt, H, d, device=dev, generator=g) * sd).to(torch.bfloat16),
+          "w": unit(steps, Bt, H, d),
+          "beta": 2.0 * torch.sigmoid(torch.randn(steps, Bt, H, device=dev, generator=g))}
+    desc = pa.make_decode_desc(kc, 1.0)
+    wsd = pa.decode_workspace(desc, dev)
+    o = torch.empty(Bt, H, d, dtype=torch.bfloat16, device=dev)
+    for s in range(3):  # warm-up on scratch positions, then the timed steps from t0
+        pa.decode_step(kc, vc, t0 - 3 + s, *(sx[n][s] for n in ("q", "k", "v", "w", "beta")), ws=wsd, out=o)
+    torch.cuda.synchronize()
+    marks = [ev()]
+    for s in range(steps):
+        pa.decode_step(kc, vc, t0 + s, *(sx[n][s] for n in ("q", "k", "v", "w", "beta")), ws=wsd, out=o)
+        marks.append(ev())
+    torch.cuda.synchronize()
+    dms = sum(marks[i].elapsed_time(marks[i + 1]) for i in range(steps))
+    nbytes = sum(Bt * H * 3 * (t0 + s) * d * 2 for s in range(steps))
+    dgbs = nbytes / (dms * 1e-3) / 1e9
+    decode = {"value": dgbs, "unit": "GB/s", "ms_per_step": dms / steps, "frac_of_hbm": dgbs / pk["hbm"],
+              "tokens_per_s": Bt * steps / (dms * 1e-3), "gpu_launches": 2 * steps,
+              "workload": "decode, batch 32, 32 heads, d=128, cache 32768 -> 32799 bf16, 32 steps"}
+    del kc, vc, sx
+    torch.cuda.empty_cache()
+    # ---- training step (fp32 CUDA-core kernels) ----
+    Bt, H, L, B = 4, 16, 2048, 32
+    x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16) for n in ("q", "k", "v")}
+    x["w"] = unit(Bt, H, L, d)
+    x["beta"] = 2.0 * torch.sigmoid(torch.randn(Bt, H, L, device=dev, generator=g))
+    x["dO"] = torch.randn(Bt, H, L, d, device=dev, generator=g).to(torch.bfloat16)
+    dsc = pa.make_desc(x["q"], 1.0)
+    wsf, wsb = pa.workspace(dsc, 0, dev), pa.workspace(dsc, 1, dev)
+    o2, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+    grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["q"]), dv=torch.empty_like(x["q"]),
+                 dw=torch.empty_like(x["q"]), dbeta=torch.empty_like(x["beta"]))
+
+    def tstep():
+        pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, 1.0, ws=wsf, out=(o2, lse))
+        pa.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], o2, lse, x["dO"], 1.0, ws=wsb, out=grads)
+    for _ in range(2):
+        tstep()
+    torch.cuda.synchronize()
+    reps = 3
+    a = ev()
+    for _ in range(reps):
+        tstep()
+    b = ev()
+    torch.cuda.synchronize()
+    tms = a.elapsed_time(b) / reps
+    flops = Bt * H * (fwd_flops_per_head(L, d, B) + bwd_flops_per_head(L, d, B))
+    tf = flops / (tms * 1e-3) / 1e12
+    clk = pk.get("sm_max_mhz", 2070.0)
+    fp32_peak = 152 * 128 * 2 * clk * 1e6 / 1e12
+    train = {"ms_per_step": tms, "tflops": tf, "bound": "alu", "peak": fp32_peak, "unit": "TFLOP/s",
+             "frac": tf / fp32_peak, "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {clk:.0f} MHz",
+             "flops_per_step": flops, "chunk": B,
+             "workload": "fwd+bwd, batch 4, 16 heads, d=128, L=2048, bf16 inputs, fp32 CUDA-core kernels"}
+    return {"decode": decode, "train": train}
 
 
 def main():
