@@ -356,9 +356,21 @@ def run_ours(args):
             fx.append((a, b))
     torch.cuda.synchronize()
     fox_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in fx), ws)
+    ff = []  # the forget-gate forward alone (inference: no transported-query store)
+    for i in range(args.warmup + args.steps):
+        a = ev()
+        pa.fwd(q, k, v, w, beta, log_f, cfg["scale"], ws=ws_b, out=(o, lse))
+        b = ev()
+        if i >= args.warmup:
+            ff.append((a, b))
+    torch.cuda.synchronize()
+    fox_fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ff)
+    fox_fwd_tf = BH * fwd_flops_per_head(L, cfg["head_dim"], B_f) / (fox_fwd_ms * 1e-3) / 1e12
     fox_train = {"ms_per_step": fox_ms, "tflops": ws * flops_step / (fox_ms * 1e-3) / 1e12,
                  "frac_of_bf16_peak": flops_step / (fox_ms * 1e-3) / 1e12 / pk["bf16"],
-                 "note": "PaTH-FoX training step (forget gate; dlog f included), same workload, same flop count"}
+                 "forward_ms": fox_fwd_ms, "forward_frac_of_bf16_peak": fox_fwd_tf / pk["bf16"],
+                 "note": "PaTH-FoX training step (forget gate; dlog f included), same workload, same flop count; "
+                         "forward_ms: the forget-gate inference forward alone"}
     del log_f, dlog_f, fox_out
 
     # the forward on its own (inference: no transported-query store), against the bf16 peak

@@ -55,6 +55,7 @@ struct __align__(1024) ScanSmem {
   uint8_t v[NSTAGE][BK * 128];        // V_c
   uint8_t zout[BQ * 128];             // image buffer of the odd Z tiles on their way to the Z store
   float xm[2][BQ];                    // per-half row maxima / sums exchanged between the halves
+  float frs[NSTAGE][BK];              // PaTH-FoX: the chunk's suffix sums of log f (with K->_c, F_c, V_c)
   uint64_t full[NSTAGE], empty[NSTAGE];
   uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done, zbuf_free[2];
   uint32_t tmem_base;
@@ -159,10 +160,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const int st = n % NSTAGE;
         if (n >= NSTAGE && !mbar_wait(&s.empty[st], ((n / NSTAGE) - 1) & 1, p.err, 1)) break;
         const int c = has_partial ? 2 * T - n : 2 * T - 1 - n;
-        mbar_arrive_expect_tx(&s.full[st], 128 * 128 + BK * 128);
+        mbar_arrive_expect_tx(&s.full[st], 128 * 128 + BK * 128 + (FOX ? BK * 4 : 0));
         tma_load_2d(s.kf[st], &tm_kr, 0, bh * p.Lp + c * BK, &s.full[st]);
         tma_load_2d(s.kf[st] + 64 * 128, &tm_f, 0, (bh * p.nc + c) * D, &s.full[st]);
         tma_load_2d(s.v[st], &tm_v, 0, bh * p.L + c * BK, &s.full[st]);
+        if constexpr (FOX) bulk_load(s.frs[st], p.fr + (size_t)bh * p.Lp + (size_t)c * BK, BK * 4, &s.full[st]);
       }
     }
   } else if (warp == 9) {
@@ -300,16 +302,32 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       // maximum (minimum for a negative scale) and x itself is folded into the exponent below
       float mxh;
       if (FOX) {
+        // the keys' suffix sums came with the chunk's stage (its barrier completed before S was
+        // issued; the stage is refilled only after this step's P V)
+        ok = ok && mbar_wait(&s.full[n % NSTAGE], (n / NSTAGE) & 1, p.err, 11);
+        // x = scl s + (A_i + R) log2(e) + r_j log2(e), two keys per paired instruction
         const float rb = (arow + R) * kLog2e;
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const uint64_t rb2 = f2(rb, rb), l2e2 = f2(kLog2e, kLog2e), sc2 = f2(p.scl, p.scl);
+        const ulonglong2* f4 = reinterpret_cast<const ulonglong2*>(s.frs[n % NSTAGE] + 32 * h);
+        float e0 = -INFINITY, e1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float xv = fmaf(__uint_as_float(x[j]), p.scl, rb);
-          xv += __ldg(p.fr + (size_t)bh * p.Lp + (size_t)c * BK + 32 * h + j) * kLog2e;
-          mx4[j & 3] = fmaxf(mx4[j & 3], xv);
-          x[j] = __float_as_uint(xv);
+        for (int q = 0; q < 8; ++q) {
+          const ulonglong2 fv = f4[q];
+          const uint64_t x01 = f2_fma(f2(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1])), sc2,
+                                      f2_fma(fv.x, l2e2, rb2));
+          const uint64_t x23 = f2_fma(f2(__uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3])), sc2,
+                                      f2_fma(fv.y, l2e2, rb2));
+          float a0, a1, a2, a3;
+          f2_split(x01, a0, a1);
+          f2_split(x23, a2, a3);
+          e0 = max3(e0, a0, a1);
+          e1 = max3(e1, a2, a3);
+          x[4 * q] = __float_as_uint(a0);
+          x[4 * q + 1] = __float_as_uint(a1);
+          x[4 * q + 2] = __float_as_uint(a2);
+          x[4 * q + 3] = __float_as_uint(a3);
         }
-        mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        mxh = fmaxf(e0, e1);
       } else {
         float e0, e1;
         if (p.scl >= 0.f) {
