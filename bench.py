@@ -239,15 +239,31 @@ def ev():
 def barrier(ws):
     if ws > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x, ws):
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_config(rank):
+    """The training workload of one rank: the same shape on every rank, its own (batch, head)
+    problems (weak scaling: the seed moves with the rank)."""
+    cfg = dict(CONFIGS[FWD_CFG])
+    cfg["seed"] = cfg["seed"] + 7919 * rank
+    return cfg
+
+
+def job_value(flops_per_rank, ms_max, ws):
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's time."""
+    return ws * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def run_ours(args):
@@ -258,8 +274,7 @@ def run_ours(args):
     from softmax_attention_chunk_gb300 import path_attn as pa
 
     pk = peaks()
-    cfg = dict(CONFIGS[FWD_CFG])
-    cfg["seed"] = cfg["seed"] + 7919 * rank  # each rank owns its own (batch, head) problems
+    cfg = rank_config(rank)  # each rank owns its own (batch, head) problems
     if args.batch:
         cfg["batch"] = args.batch
     if args.heads:
@@ -317,7 +332,7 @@ def run_ours(args):
     ms_step = total_ms / args.steps
     flops_step = BH * (fwd_flops_per_head(L, d, B_f) + bwd_flops_per_head(L, d, B_b))
     fa_flops_step = BH * 7 * L * L * d
-    value = ws * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_value(flops_step, ms_step, ws)
 
     # roofline per phase; the dominant phase is reported as "roofline"
     pr = phase_roofline(L, BH, pk)
