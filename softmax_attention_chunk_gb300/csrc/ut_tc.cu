@@ -1,5 +1,5 @@
 // Per-chunk UT preparation on tcgen05 (bf16 operands, fp32 accumulation in TMEM), chunk B = 64:
-// one CTA of 128 threads per chunk.
+// one CTA of 128 threads per chunk, three CTAs per SM.
 //
 // Method: PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6 (UT representation) and §2.7
 // (boundary-adjusted queries/keys, chunk transform):
@@ -8,14 +8,26 @@
 //   A = M1 U,  X = U N2,  Y = U^T W
 //   Q<- = Q - A W,  K-> = K - X^T W,  F = I - W^T Y,  S_d = Q K^T - M1 X (masked j <= i)
 // and the diagonal chunk's softmax partial state (m, l, acc = P V).
-// Every product is an M=64 MMA whose operands are 64x64 bf16 tiles in the 128-byte swizzled layout
-// (TMA-loaded inputs or tiles written by the warps), K-major or MN-major as the product needs; the
-// four products of the first phase share their B operands two by two, so they run as two N=128
-// MMAs over the stacked [W; K] tile.  Accumulators are read with the 16x32bx2 TMEM shape: each
-// thread of warp w holds 32 columns (half h = lane / 16) of row 16w + lane % 16, so all 128
-// threads work in every epilogue; the two halves of a row meet through one shuffle where a row
-// reduction is needed.  Inputs come through 3-D tensor maps ([heads][L][64]) that read rows >= L
-// as zero.
+//
+// Every product is an M=64 MMA whose operands are 64x64 bf16 tiles in the 128-byte swizzled
+// layout (TMA-loaded inputs or tiles written by the warps), K-major or MN-major as the product
+// needs.  Accumulators are read with the 16x32bx2 TMEM shape: each thread of warp w holds 32
+// columns (half h = lane / 16) of row 16w + lane % 16, so all 128 threads work in every epilogue;
+// the two halves of a row meet through one shuffle where a row reduction is needed.  Inputs come
+// through 3-D tensor maps ([heads][L][64]) that read rows >= L as zero.
+//
+// The kernel is latency bound (a chain of product rounds, each an MMA -> TMEM -> registers ->
+// shared-memory tile round trip, and the substitution), so it is laid out for three CTAs per SM:
+// 128 TMEM columns (two 64-column accumulators per round) and nine 8 KB tile slots, reused as
+// their tenants die:
+//   slot 0 W          P1 .. R4           slot 5 M1 (M1 epilogue .. R2), then Y (R2 .. R4)
+//   slot 1 K          P1 .. R3 epilogue  slot 6 N2 (P1 .. R1), then P (R2 .. R4) or Y_lo (fp32 F)
+//   slot 2 Q          P1 .. R3 epilogue  slot 7 U (P2 .. R2), then V (loaded once R2 has read U)
+//   slots 3-4 fp32 L (P1 .. P2), then A (slot 3) and X (slot 4) (R1 .. R3)
+//   slot 8 U_lo (fp32 F only)
+// W and K are adjacent: the first round's two products share the stacked [W; K] tile as one N=128
+// B operand.  Rounds: P1 [G | N2]; M1 (its MMA runs during the substitution P2); R1 A, X;
+// R2 Y, S_d; R3 A W, X^T W; R4 W^T Y, P V.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
@@ -31,8 +43,13 @@ bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t
 namespace {
 using namespace tc;
 
-constexpr uint32_t kUtTile = 64 * 128;  // one 64x64 bf16 tile
-constexpr uint32_t kUtSlotBytes = 11 * kUtTile;
+constexpr int B = 64;
+constexpr int D = kHeadDim;
+constexpr uint32_t TILE = 64 * 128;  // one 64x64 bf16 tile
+constexpr int NSLOT = 9;
+constexpr uint32_t TMEM_COLS = 128;
+enum { S_W = 0, S_K, S_Q, S_L, S_X, S_M1, S_N2, S_U, S_ULO };
+constexpr int S_A = S_L, S_Y = S_M1, S_P = S_N2, S_YLO = S_N2, S_V = S_U;
 
 struct UtParams {
   int L, Lp, nc, BH;
@@ -52,76 +69,69 @@ struct UtParams {
   int* err;
 };
 
-// Shared memory of one chunk's preparation: eleven 1024-byte aligned tiles in this order (w and k
-// adjacent: the stacked B operand of the first phase; a and x adjacent: the fp32 L of the
-// substitution), beta and the forget-gate prefix (16-byte aligned), and two mbarriers.
-struct UtSlots {
-  uint8_t *w, *k, *q, *v, *m1, *n2, *u, *a, *x, *y, *p;
-  float* beta;
-  float* pre;
-  uint64_t* bar_in;
-  uint64_t* bar_mma;
+struct __align__(1024) UtSmem {
+  uint8_t t[NSLOT][TILE];
+  float beta[B], pre[B];
+  uint64_t bar_in, bar_v, bar_mma;
+  uint32_t tmem_base;
 };
-__device__ __forceinline__ UtSlots ut_slots(uint8_t* base, float* beta, float* pre, uint64_t* bar_in,
-                                            uint64_t* bar_mma) {
-  UtSlots s;
-  uint8_t** t[11] = {&s.w, &s.k, &s.q, &s.v, &s.m1, &s.n2, &s.u, &s.a, &s.x, &s.y, &s.p};
-#pragma unroll
-  for (int j = 0; j < 11; ++j) *t[j] = base + j * kUtTile;
-  s.beta = beta;
-  s.pre = pre;
-  s.bar_in = bar_in;
-  s.bar_mma = bar_mma;
-  return s;
-}
 
-// Prepares chunk c of head bh.  Run by the CTA's 128 threads together; thread 0 issues the TMA
-// loads and the MMAs.  tb: 256 TMEM columns of the CTA; in_par / mph: phases of
-// bar_in (one completion per call) and bar_mma (advanced here).  zimg (optional): a swizzled
-// 64-row bf16 tile image that also receives Q<- of the chunk.  The mbarriers are initialised by
-// the caller; on return every TMEM access and every MMA of the chunk has completed, and the
-// slots may be reused.
 template <bool F32>
-__device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, const CUtensorMap* tm_q,
-                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                              const CUtensorMap* tm_w, const UtParams& p, int bh, int c,
-                                              uint32_t in_par, uint32_t& mph, uint8_t* zimg) {
-  constexpr int B = 64;
-  constexpr int D = kHeadDim;
+__global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                           const __grid_constant__ CUtensorMap tm_k,
+                                                           const __grid_constant__ CUtensorMap tm_v,
+                                                           const __grid_constant__ CUtensorMap tm_w,
+                                                           const UtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, bh = blockIdx.y;
   const int row0 = c * B;
   const size_t in_row = (size_t)bh * p.L;
   const size_t ws_row = (size_t)bh * p.Lp + row0;
   const bool lead = tid == 0;
+  const bool diag = p.with_diag != 0;
   // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
   const int i = 16 * warp + (lane & 15), h = lane >> 4;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  float* sg = reinterpret_cast<float*>(s.a);  // fp32 L = strictLower(D G) over the a and x slots
-  const uint32_t aw = smem_u32(s.w), aq = smem_u32(s.q), ak = smem_u32(s.k), av = smem_u32(s.v);
-  const uint32_t am1 = smem_u32(s.m1), an2 = smem_u32(s.n2), au = smem_u32(s.u);
-  const uint32_t aa = smem_u32(s.a), ax = smem_u32(s.x), ay = smem_u32(s.y), ap = smem_u32(s.p);
-  auto run = [&](auto issue, int code) {  // lead issues one phase's MMAs; every thread waits
+  auto ta = [&](int slot) { return smem_u32(s.t[slot]); };
+  float* sg = reinterpret_cast<float*>(s.t[S_L]);  // fp32 L = strictLower(D G) over slots 3 and 4
+
+  if (lead) {
+    mbar_init(&s.bar_in, 1);
+    mbar_init(&s.bar_v, 1);
+    mbar_init(&s.bar_mma, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&s.tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s.tmem_base;
+  uint32_t mph = 0;  // phase of bar_mma
+  auto issue = [&](auto fn) {  // lead issues one round's MMAs and commits them
     if (lead) {
       tc_fence_after();
-      issue();
-      mma_commit(s.bar_mma);
+      fn();
+      mma_commit(&s.bar_mma);
     }
-    mbar_wait(s.bar_mma, mph, p.err, code);
+  };
+  auto wait_mma = [&](int code) {
+    mbar_wait(&s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
   };
-  auto publish = [&]() {  // tiles written by the threads -> visible to the next MMAs
+  auto publish = [&]() {  // tiles written by the threads -> visible to the next MMAs; TMEM reads done
     fence_proxy_async_smem();
     tc_fence_before();
-    ut_sync();
+    __syncthreads();
   };
 
   if (lead) {
-    mbar_arrive_expect_tx(s.bar_in, (p.with_diag ? 4 : 3) * kUtTile);
-    tma_load_3d(s.w, tm_w, 0, row0, bh, s.bar_in);
-    tma_load_3d(s.q, tm_q, 0, row0, bh, s.bar_in);
-    tma_load_3d(s.k, tm_k, 0, row0, bh, s.bar_in);
-    if (p.with_diag) tma_load_3d(s.v, tm_v, 0, row0, bh, s.bar_in);
+    mbar_arrive_expect_tx(&s.bar_in, 3 * TILE);
+    tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
+    tma_load_3d(s.t[S_K], &tm_k, 0, row0, bh, &s.bar_in);
   }
   if (tid < B) {
     const int gi = row0 + tid;
@@ -133,26 +143,26 @@ __device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, con
     float b2 = (p.logf && gb < p.L) ? p.logf[in_row + gb] : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float ta = __shfl_up_sync(0xffffffffu, a, o), tb2 = __shfl_up_sync(0xffffffffu, b2, o);
-      if (lane >= o) { a += ta; b2 += tb2; }
+      const float ta2 = __shfl_up_sync(0xffffffffu, a, o), tb2 = __shfl_up_sync(0xffffffffu, b2, o);
+      if (lane >= o) { a += ta2; b2 += tb2; }
     }
     const float tot_a = __shfl_sync(0xffffffffu, a, 31);
     s.pre[lane] = a;
     s.pre[32 + lane] = b2 + tot_a;
   }
-  mbar_wait(s.bar_in, in_par, p.err, 31);
-  ut_sync();
+  mbar_wait(&s.bar_in, 0, p.err, 31);
+  __syncthreads();
 
-  // ---- P1: [G | N2] = W [W; K]^T, [M1 | Q K^T] = Q [W; K]^T ----
-  run([&] {
+  // ---- P1: [G | N2] = W [W; K]^T (one N=128 MMA: the w and k slots are adjacent) ----
+  issue([&] {
     const uint32_t idesc = idesc_bf16(64, 128, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t bd = sdesc_sw128(aw + 32u * kk, 1024, 16);  // 128 rows: the w tile, then the k tile
-      mma_ss(tb + 0, sdesc_sw128(aw + 32u * kk, 1024, 16), bd, idesc, kk > 0 ? 1u : 0u);
-      mma_ss(tb + 128, sdesc_sw128(aq + 32u * kk, 1024, 16), bd, idesc, kk > 0 ? 1u : 0u);
+      const uint64_t d = sdesc_sw128(ta(S_W) + 32u * kk, 1024, 16);
+      mma_ss(tb + 0, d, d, idesc, kk > 0 ? 1u : 0u);
     }
-  }, 32);
+  });
+  wait_mma(32);
   {
     float x[32];
     ld_half(tb, lane_off, 0, x);  // L = strictLower(diag(beta) G), fp32
@@ -164,37 +174,62 @@ __device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, con
           make_float4(j < i ? bi * x[4 * q] : 0.f, j + 1 < i ? bi * x[4 * q + 1] : 0.f,
                       j + 2 < i ? bi * x[4 * q + 2] : 0.f, j + 3 < i ? bi * x[4 * q + 3] : 0.f);
     }
-    ld_half(tb, lane_off, 128, x);  // M1 = lower(Q W^T)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
-    put_half(s.m1, i, h, x);
     ld_half(tb, lane_off, 64, x);  // N2 = strictLower(W K^T)
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
-    put_half(s.n2, i, h, x);
+    put_half(s.t[S_N2], i, h, x);
   }
-  ut_sync();
+  // every thread has read P1's accumulators: M1 = Q W^T goes to the tensor core while the
+  // threads substitute
+  tc_fence_before();
+  __syncthreads();
+  issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
 
-  // ---- P2: U = (I + strictLower(D G))^{-1} D (with an fp32 F: U = U_hi + U_lo, U_lo in P's
-  //      slot, unused without the diagonal state) ----
-  ut_solve_blocked<F32>(sg, s.beta, s.u, s.p, tid);
+  // ---- P2: U = (I + strictLower(D G))^{-1} D (fp32 F: U = U_hi + U_lo) ----
+  ut_solve_blocked<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);
+  wait_mma(33);
+  {
+    float x[32];
+    ld_half(tb, lane_off, 0, x);  // M1 = lower(Q W^T)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
+    put_half(s.t[S_M1], i, h, x);
+  }
   publish();
 
-  // ---- P3: A = M1 U, X = U N2, Y = U^T W (+ U_lo^T W for an fp32 F) ----
-  run([&] {
-    mma64(tb + 0, am1, 0, au, 1, 0);
-    mma64(tb + 64, au, 0, an2, 1, 0);
-    mma64(tb + 128, au, 1, aw, 1, 0);
-    if constexpr (F32) mma64(tb + 128, ap, 1, aw, 1, 1);
-  }, 33);
+  // ---- R1: A = M1 U, X = U N2 ----
+  issue([&] {
+    mma64(tb + 0, ta(S_M1), 0, ta(S_U), 1, 0);
+    mma64(tb + 64, ta(S_U), 0, ta(S_N2), 1, 0);
+  });
+  wait_mma(34);
   {
     float x[32];
     ld_half(tb, lane_off, 0, x);
-    put_half(s.a, i, h, x);
+    put_half(s.t[S_A], i, h, x);
     ld_half(tb, lane_off, 64, x);
-    put_half(s.x, i, h, x);
-    ld_half(tb, lane_off, 128, x);
-    if constexpr (F32) {  // Y = Y_hi + Y_lo, both bf16 (Y_lo in V's slot, never loaded without the diagonal state)
+    put_half(s.t[S_X], i, h, x);
+  }
+  publish();
+
+  // ---- R2: Y = U^T W (+ U_lo^T W for an fp32 F), S_d = Q K^T - M1 X; then V into U's slot ----
+  issue([&] {
+    mma64(tb + 0, ta(S_U), 1, ta(S_W), 1, 0);
+    if constexpr (F32) mma64(tb + 0, ta(S_ULO), 1, ta(S_W), 1, 1);
+    if (diag) {
+      mma64(tb + 64, ta(S_Q), 0, ta(S_K), 0, 0);
+      mma64(tb + 64, ta(S_M1), 0, ta(S_X), 1, 1, /*neg_a=*/1);
+    }
+  });
+  wait_mma(35);
+  if (lead && diag) {  // U has been read by R2's products: its slot takes V
+    mbar_arrive_expect_tx(&s.bar_v, TILE);
+    tma_load_3d(s.t[S_V], &tm_v, 0, row0, bh, &s.bar_v);
+  }
+  {
+    float x[32];
+    ld_half(tb, lane_off, 0, x);
+    if constexpr (F32) {  // Y = Y_hi + Y_lo, both bf16
       float lo[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -202,47 +237,11 @@ __device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, con
         lo[j] = x[j] - hi;
         x[j] = hi;
       }
-      put_half(s.v, i, h, lo);
+      put_half(s.t[S_YLO], i, h, lo);
     }
-    put_half(s.y, i, h, x);
-  }
-  publish();
-
-  // ---- P4: A W, X^T W, S_d = QK^T - M1 X (accumulated onto QK^T), W^T Y ----
-  run([&] {
-    mma64(tb + 0, aa, 0, aw, 1, 0);
-    mma64(tb + 64, ax, 1, aw, 1, 0);
-    mma64(tb + 192, am1, 0, ax, 1, 1, /*neg_a=*/1);
-    mma64(tb + 128, aw, 1, ay, 1, 0);
-    if constexpr (F32) mma64(tb + 128, aw, 1, av, 1, 1);
-  }, 34);
-  {
-    float x[32], src[32];
-    const size_t orow = ws_row + i;
-    ld_half(tb, lane_off, 0, x);  // Q<- = Q - A W
-    get_half(s.q, i, h, src);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) src[j] -= x[j];
-    store_bf16_half(p.ql + orow * D + 32 * h, src);
-    if (zimg) put_half(zimg, i, h, src);
-    ld_half(tb, lane_off, 64, x);  // K-> = K - X^T W
-    get_half(s.k, i, h, src);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) src[j] -= x[j];
-    store_bf16_half(p.kr + orow * D + 32 * h, src);
-    ld_half(tb, lane_off, 128, x);  // F = I - W^T Y, row i
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
-    if constexpr (F32) {
-      // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
-      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.f) + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-    } else {
-      store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
-    }
-    if (p.with_diag) {
-      ld_half(tb, lane_off, 192, x);  // S_d: the diagonal chunk's softmax partial state
+    put_half(s.t[S_Y], i, h, x);
+    if (diag) {
+      ld_half(tb, lane_off, 64, x);  // S_d: the diagonal chunk's softmax partial state
       const float pi = s.pre[i];
       float mx = -INFINITY;
 #pragma unroll
@@ -261,10 +260,10 @@ __device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, con
         l += pj;
       }
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      put_half(s.p, i, h, x);
+      put_half(s.t[S_P], i, h, x);
       if (h == 0) {
-        p.dm[orow] = mx;
-        p.dl[orow] = l;
+        p.dm[ws_row + i] = mx;
+        p.dl[ws_row + i] = l;
       }
     }
   }
@@ -274,57 +273,64 @@ __device__ __forceinline__ void ut_prep_chunk(const UtSlots& s, uint32_t tb, con
     p.fr[ws_row + tid] = tot - s.pre[tid];
     if (tid == 0) p.ft[(size_t)bh * p.nc + c] = tot;
   }
-  if (p.with_diag) {
-    publish();
-    // ---- P5: acc = P V ----
-    run([&] { mma64(tb + 0, ap, 0, av, 1, 0); }, 35);
-    float x[32];
+  publish();
+
+  // ---- R3: A W, X^T W -> Q<- = Q - A W, K-> = K - X^T W ----
+  issue([&] {
+    mma64(tb + 0, ta(S_A), 0, ta(S_W), 1, 0);
+    mma64(tb + 64, ta(S_X), 1, ta(S_W), 1, 0);
+  });
+  wait_mma(36);
+  {
+    float x[32], src[32];
+    const size_t orow = ws_row + i;
     ld_half(tb, lane_off, 0, x);
-    float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
+    get_half(s.t[S_Q], i, h, src);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    for (int j = 0; j < 32; ++j) src[j] -= x[j];
+    store_bf16_half(p.ql + orow * D + 32 * h, src);
+    ld_half(tb, lane_off, 64, x);
+    get_half(s.t[S_K], i, h, src);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) src[j] -= x[j];
+    store_bf16_half(p.kr + orow * D + 32 * h, src);
   }
-  // every thread's TMEM loads are complete (tcgen05.wait::ld in ld_half); the slots and the TMEM
-  // columns may be reused after the caller's next barrier
-  tc_fence_before();
-  ut_sync();
-  tc_fence_after();
-}
-
-struct __align__(1024) UtSmem {
-  uint8_t tiles[kUtSlotBytes];  // the eleven preparation slots (ut_slots order)
-  float beta[64], pre[64];
-  uint64_t bar_in, bar_mma;
-  uint32_t tmem_base;
-};
-
-template <bool F32>
-__global__ void __launch_bounds__(128) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                        const __grid_constant__ CUtensorMap tm_k,
-                                                        const __grid_constant__ CUtensorMap tm_v,
-                                                        const __grid_constant__ CUtensorMap tm_w,
-                                                        const UtParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (tid == 0) {
-    mbar_init(&s.bar_in, 1);
-    mbar_init(&s.bar_mma, 1);
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(&s.tmem_base, 256);
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = s.tmem_base;
-  const UtSlots sl = ut_slots(s.tiles, s.beta, s.pre, &s.bar_in, &s.bar_mma);
-  uint32_t mph = 0;
-  ut_prep_chunk<F32>(sl, tb, &tm_q, &tm_k, &tm_v, &tm_w, p, (int)blockIdx.y, (int)blockIdx.x, 0, mph, nullptr);
+
+  // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
+  if (diag) mbar_wait(&s.bar_v, 0, p.err, 37);
+  issue([&] {
+    mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
+    if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);
+    if (diag) mma64(tb + 64, ta(S_P), 0, ta(S_V), 1, 0);
+  });
+  wait_mma(38);
+  {
+    float x[32];
+    ld_half(tb, lane_off, 0, x);  // F = I - W^T Y, row i
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
+    if constexpr (F32) {
+      // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.f) + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else {
+      store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
+    }
+    if (diag) {
+      ld_half(tb, lane_off, 64, x);
+      float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tb, 256);
+    tmem_dealloc(tb, TMEM_COLS);
   }
 }
 
