@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   }
   publish();
 
-  // ---- P3: dP = dO V^T goes to the tensor core first (its accumulator is free).  Warps 0-1 solve
-  //      Y = (I + strictLower(D G))^{-1} by forward substitution (lane = column; columns 32-63
-  //      are zero above row 32) and write Y and U = Y D as bf16 tiles; meanwhile warps 2-3
+  // ---- P3: dP = dO V^T goes to the tensor core first (its accumulator is free).  Warps 0-1 form
+  //      Y = (I + strictLower(D G))^{-1} by two-level block inversion and write Y and U = Y D as
+  //      bf16 tiles; meanwhile warps 2-3
   //      (thread = row) write dQ<- and dK-> (zero past L) and, once dP has read V, dF into V's
   //      slot as bf16 operand tiles ----
   if (tid == 64) {
@@ -251,18 +251,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     mma64(tb + C2, ta(S_DO), 0, ta(S_V), 0, 0);
     mma_commit(&s.bar_mma);
   }
-  if (warp < 2) {
-    const int cc = 32 * warp + lane;
-    float y[64];
-    if (warp == 0) ut_solve_column<0>(sg, cc, y);
-    else ut_solve_column<2>(sg, cc, y);
-    const float bc = s.beta[cc];
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      *reinterpret_cast<__nv_bfloat16*>(s.t[S_Y] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r]);
-      *reinterpret_cast<__nv_bfloat16*>(s.t[S_U] + sw128_offset(r, cc)) = __float2bfloat16_rn(y[r] * bc);
-    }
-  }
+  if (warp < 2) ut_solve_blocked64(sg, s.beta, s.t[S_U], s.t[S_Y], tid);
   if (warp >= 2) {
     const int r = tid - 64;
     const bool ok = row0 + r < p.L;

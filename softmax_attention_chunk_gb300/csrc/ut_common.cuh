@@ -120,64 +120,6 @@ __device__ __forceinline__ void load_f32_half(const float* src, float* x) {
   }
 }
 
-// Forward substitution for the UT transform, one column per thread of two warps: returns in y
-// the column cc of Y = (I + L)^{-1}, L = strictLower(diag(beta) G), i.e. row by row
-//   Y_rc = delta_rc - sum_{m<r} L_rm Y_mc,
-// with L the fp32 matrix at sl (f32_idx layout, strictly lower: entries with m >= r are zero).
-// Rows go in blocks of 16: the earlier blocks enter through 16 independent accumulations
-// (16-byte broadcast loads of L), the block itself is substituted row by row.  Everything is
-// unrolled so that y stays in registers.  B0 is the first row block that can be nonzero for
-// every column of the calling warp (Y is unit lower triangular: 0 for columns 0-31, 2 for
-// columns 32-63), so a warp skips the blocks above it.  The sums over the earlier blocks use
-// paired fp32 FMAs (even and odd m in the two lanes of a 64-bit register, added at the end).
-template <int B0>
-__device__ __forceinline__ void ut_solve_column(const float* sl, int cc, float (&y)[64]) {
-#pragma unroll
-  for (int r = 0; r < 16 * B0; ++r) y[r] = 0.f;
-#pragma unroll
-  for (int b = B0; b < 4; ++b) {
-    float acc[16];
-    if (b > B0) {
-      uint64_t s2[16];
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
-#pragma unroll
-      for (int m = 16 * B0; m < 16 * b; m += 4) {
-        const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sl + f32_idx(16 * b + rr, m));
-          s2[rr] = f2_fma(lv.x, y01, s2[rr]);
-          s2[rr] = f2_fma(lv.y, y23, s2[rr]);
-        }
-      }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        float lo, hi;
-        f2_split(s2[rr], lo, hi);
-        acc[rr] = lo + hi;
-      }
-    } else {
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
-    }
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = 16 * b + rr;
-      float a = acc[rr];
-#pragma unroll
-      for (int m = 16 * b; m < r; m += 4) {
-        const float4 lv = *reinterpret_cast<const float4*>(sl + f32_idx(r, m));
-        a = fmaf(lv.x, y[m], a);
-        if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
-        if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
-        if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
-      }
-      y[r] = (cc == r ? 1.f : 0.f) - a;
-    }
-  }
-}
-
 // Named barrier 2 over the 128 threads of a per-chunk UT kernel (the block-inversion routine
 // below synchronises through it).
 __device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
@@ -192,8 +134,8 @@ __device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 2, 128;" ::: 
 // lower; overwritten); beta: the chunk's clamped beta; U is written as bf16 into the swizzled
 // tile u (LO: with u_lo, U = u + u_lo with both parts bf16).  Called by threads 0-127 together;
 // ends with the tiles written by generic stores (the caller fences them for the tensor core).
-// (The UT backward keeps the column solve above: there warps 2-3 convert the gradient tiles while
-// warps 0-1 substitute, and a phase that needs all four warps lengthened its chain.)
+// (The UT backward uses the 64-thread variant below: there warps 2-3 convert the gradient tiles
+// meanwhile, and a phase that needs all four warps lengthened its chain.)
 template <bool LO>
 __device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, uint8_t* u, uint8_t* u_lo,
                                                  int tid) {
@@ -307,6 +249,126 @@ __device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, u
   for (int e = 0; e < 2; ++e)
 #pragma unroll
     for (int j = 0; j < 4; ++j) put_u(32 + 2 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
+}
+
+// The same block inversion on warps 0-1 alone (threads 0-63, named barrier 3), writing Y =
+// (I + L)^{-1} and U = Y diag(beta) as bf16 tiles yt and u; the off-diagonal block's two 32 x 32
+// products give each thread a 4 x 4 block.  For the UT backward, whose warps 2-3 convert the
+// gradient tiles meanwhile.  sl is overwritten.
+__device__ __forceinline__ void ut_sync64() { asm volatile("bar.sync 3, 64;" ::: "memory"); }
+__device__ __forceinline__ void ut_solve_blocked64(float* sl, const float* beta, uint8_t* u, uint8_t* yt, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  auto put = [&](int r, int col, float yv, float bc) {
+    *reinterpret_cast<__nv_bfloat16*>(yt + sw128_offset(r, col)) = __float2bfloat16_rn(yv);
+    *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(r, col)) = __float2bfloat16_rn(yv * bc);
+  };
+  // ---- phase 1: diagonal 32 x 32 blocks, warp 0 the top one, warp 1 the bottom one ----
+  float y[32];
+  {
+    const float* sh = sl + 65 * 32 * warp;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float acc[16];
+      if (b == 1) {
+        uint64_t s2[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+          const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sh + f32_idx(16 + rr, m));
+            s2[rr] = f2_fma(lv.x, y01, s2[rr]);
+            s2[rr] = f2_fma(lv.y, y23, s2[rr]);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float lo, hi;
+          f2_split(s2[rr], lo, hi);
+          acc[rr] = lo + hi;
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * b + rr;
+        float a = acc[rr];
+#pragma unroll
+        for (int m = 16 * b; m < r; m += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
+          a = fmaf(lv.x, y[m], a);
+          if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
+          if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
+          if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
+        }
+        y[r] = (lane == r ? 1.f : 0.f) - a;
+      }
+    }
+  }
+  ut_sync64();  // every read of L_tt / L_bb is done
+  {
+    const int o = 32 * warp, col = o + lane;
+    const float bc = beta[col];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      sl[65 * o + f32_idx(r, lane)] = y[r];
+      put(o + r, col, y[r], bc);
+    }
+    if (warp == 1) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) put(r, col, 0.f, 0.f);
+    }
+  }
+  ut_sync64();
+  // ---- phase 2: rows 4 rg .. 4 rg + 3, columns 4 cg .. 4 cg + 3 of a 32 x 32 product ----
+  const int rg = tid >> 3, cg = tid & 7;
+  float acc[4][4];
+  auto product = [&](int a_row0, int a_col0, int b_row0, int b_col0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      float av[4][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 a4 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 4 * rg + e, a_col0 + m));
+        av[e][0] = a4.x;
+        av[e][1] = a4.y;
+        av[e][2] = a4.z;
+        av[e][3] = a4.w;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(b_row0 + m + kk, b_col0 + 4 * cg));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[e][0] = fmaf(av[e][kk], bv.x, acc[e][0]);
+          acc[e][1] = fmaf(av[e][kk], bv.y, acc[e][1]);
+          acc[e][2] = fmaf(av[e][kk], bv.z, acc[e][2]);
+          acc[e][3] = fmaf(av[e][kk], bv.w, acc[e][3]);
+        }
+      }
+    }
+  };
+  product(32, 0, 0, 0);  // T = L_bt Y_tt
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    *reinterpret_cast<float4*>(sl + f32_idx(4 * rg + e, 32 + 4 * cg)) =
+        make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
+  ut_sync64();
+  product(32, 32, 0, 32);  // Y_bb T
+  const float4 bq = *reinterpret_cast<const float4*>(beta + 4 * cg);
+  const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) put(32 + 4 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
 }
 
 }  // namespace tc
