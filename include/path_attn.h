@@ -68,7 +68,7 @@ typedef struct {
 typedef struct {
   int batch;       /* > 0 */
   int heads;       /* > 0 */
-  int head_dim;    /* 64 or 128 (path_decode_prefill and path_decode_step_noalloc: 64 only) */
+  int head_dim;    /* 64 or 128 (path_decode_step_noalloc: 64 only) */
   int capacity;    /* rows allocated per (batch, head) in each cache */
   int cache_dtype; /* path_dtype_t of the caches and of q_t,k_t,v_t,w_t,o_t */
   float scale;     /* logit multiplier */
@@ -216,8 +216,8 @@ size_t path_decode_prefill_workspace_size(const path_decode_desc_t* desc, int pr
  *   v_cache row j = v_j,
  * i.e. exactly what prompt_len calls of path_decode_step from an empty cache would leave there.
  * Computed blockwise in fp32 (64-row chunks: each key moved to its chunk's end, then through the
- * later chunks' transforms right to left) and rounded once to cache_dtype.  head_dim 64 only
- * (128 is PATH_ERR_UNSUPPORTED).
+ * later chunks' transforms right to left; 32-row chunks at head_dim 128) and rounded once to
+ * cache_dtype.
  * k, v, w: [batch][heads][prompt_len][head_dim] in cache_dtype; beta: [batch][heads][prompt_len]
  * float32 (clamped to [0, 2]).  Caches: [batch][heads][capacity][head_dim]; rows >= prompt_len
  * are not touched.  Requires 0 <= prompt_len <= capacity (else PATH_ERR_CAPACITY); prompt_len = 0

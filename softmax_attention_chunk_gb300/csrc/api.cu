@@ -220,14 +220,16 @@ PATH_API int path_decode_step(const path_decode_desc_t* d, void* k_cache, void* 
                                    (cudaStream_t)stream, nullptr, nullptr, d->head_dim));
 }
 
-// Geometry of the prompt of a prefill hand-off: 64-row chunks over prompt_len rows.
+// Geometry of the prompt of a prefill hand-off: 64-row chunks over prompt_len rows (32-row chunks
+// at head dim 128).
 static Geom prefill_geom(const path_decode_desc_t* d, int prompt_len) {
   Geom g;
   g.BH = d->batch * d->heads;
   g.L = prompt_len;
-  g.B = 64;
-  g.nc = (prompt_len + 63) / 64;
-  g.Lp = g.nc * 64;
+  g.D = d->head_dim;
+  g.B = g.D == kHeadDimWide ? 32 : 64;
+  g.nc = (prompt_len + g.B - 1) / g.B;
+  g.Lp = g.nc * g.B;
   g.scale = d->scale;
   return g;
 }
@@ -244,7 +246,6 @@ static int check_decode_desc(const path_decode_desc_t* d) {
 
 PATH_API size_t path_decode_prefill_workspace_size(const path_decode_desc_t* d, int prompt_len) {
   if (check_decode_desc(d) != PATH_OK || prompt_len < 0 || prompt_len > d->capacity) return 0;
-  if (d->head_dim != kHeadDim) return 0;
   return prefill_ws_bytes(prefill_geom(d, prompt_len), d->cache_dtype == PATH_BF16);
 }
 
@@ -253,7 +254,6 @@ PATH_API int path_decode_prefill(const path_decode_desc_t* d, void* k_cache, voi
                                  const float* log_f, float* a_cache, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_decode_desc(d);
   if (rc != PATH_OK) return rc;
-  if (d->head_dim != kHeadDim) return PATH_ERR_UNSUPPORTED;  // the hand-off walk is written for d = 64
   if (prompt_len < 0) return PATH_ERR_INVALID_ARG;
   if (prompt_len > d->capacity) return PATH_ERR_CAPACITY;
   CHECK_PTR(k_cache); CHECK_PTR(v_cache); CHECK_PTR(k); CHECK_PTR(v); CHECK_PTR(w); CHECK_PTR(beta);

@@ -10,11 +10,12 @@
 //   F_c = I - W_c^T U_c^T W_c = H_{s(c)} ... H_{e(c)}, so H_{e(c)} ... H_{s(c)} = F_c^T,
 // hence k~_j = F_{nc-1}^T ... F_{c+1}^T K->_c row j.  With the suffix products
 //   S_{nc-1} = I,   S_{c-1} = S_c F_c^T,
-// the cache rows of chunk c are K->_c S_c^T.  For a bf16 cache, K-> (bf16) and F (fp32, from
-// split-precision bf16 products: the long suffix chain must not accumulate bf16 rounding) come
-// from the tcgen05 UT preparation (ut_tc.cu); for an fp32 cache both come from the fp32 SIMT
-// preparation (simt_fwd.cu).  One CTA per head then walks the chunks right to left, keeping S in
-// shared memory, in fp32: 2 * 64^3 multiply-adds per chunk.
+// the cache rows of chunk c are K->_c S_c^T.  At head dim 64, for a bf16 cache, K-> (bf16) and F
+// (fp32, from split-precision bf16 products: the long suffix chain must not accumulate bf16
+// rounding) come from the tcgen05 UT preparation (ut_tc.cu) on 64-row chunks; for an fp32 cache,
+// and at head dim 128 for both cache types, both come from the fp32 SIMT preparation
+// (simt_fwd.cu), at head dim 128 on 32-row chunks.  One CTA per head then walks the chunks right
+// to left, keeping S (d x d) in shared memory, in fp32: per chunk CB d^2 + d^3 multiply-adds.
 #include "internal.h"
 #include "dev_common.cuh"
 
@@ -23,16 +24,12 @@
 namespace pathattn {
 namespace {
 
-constexpr int D = kHeadDim;
-constexpr int CB = 64;       // chunk rows
-constexpr int LD = D + 1;    // padded row stride of the shared-memory matrices
-constexpr int PT = 256;      // threads: each owns a 4 x 4 block of a 64 x 64 product
+constexpr int PT = 256;      // threads: each owns one or more 4 x 4 blocks of a product
 
-struct PrefillSmem {
-  float s[D * LD];   // S_c
-  float a[CB * LD];  // K->_c, then F_c
-  float t[D * LD];   // S_c F_c^T before it replaces S
-};
+// Shared memory of the walk at head dim D (chunk rows CB <= D), rows padded to LD = D + 1 floats:
+// S_c, then K->_c or F_c, then S_c F_c^T before it replaces S.
+template <int D>
+constexpr size_t prefill_smem_bytes() { return (size_t)3 * D * (D + 1) * sizeof(float); }
 
 // Asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned) from global memory into L2.
 __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
@@ -40,7 +37,9 @@ __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
                : "memory");
 }
 
-// out[r][n] = sum_m A[r][m] * B[n][m] for the thread's 4 x 4 block (A B^T).
+// out[r][n] = sum_m A[r][m] * B[n][m] for one 4 x 4 block (A B^T), both operands with row stride
+// LD and D columns.
+template <int D, int LD>
 __device__ __forceinline__ void mm_abt(const float* A, const float* Bm, int r0, int n0, float (&acc)[4][4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -60,16 +59,19 @@ __device__ __forceinline__ void mm_abt(const float* A, const float* Bm, int r0, 
   }
 }
 
-template <typename T, typename KR>
+template <typename T, typename KR, int D, int CB>
 __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, int nc, int cap,
                                                                const KR* __restrict__ kr,
                                                                const float* __restrict__ f,
                                                                T* __restrict__ k_cache) {
+  constexpr int LD = D + 1;
+  constexpr int NB = D / 4;  // 4-column blocks of an output row
   extern __shared__ float smem_f[];
-  PrefillSmem& s = *reinterpret_cast<PrefillSmem*>(smem_f);
+  float* ss = smem_f;            // S_c
+  float* sa = ss + D * LD;       // K->_c, then F_c
+  float* st = sa + D * LD;       // S_c F_c^T
   const int tid = threadIdx.x, bh = blockIdx.x;
-  const int r0 = 4 * (tid / 16), n0 = 4 * (tid % 16);
-  for (int e = tid; e < D * D; e += PT) s.s[(e / D) * LD + e % D] = (e / D == e % D) ? 1.f : 0.f;
+  for (int e = tid; e < D * D; e += PT) ss[(e / D) * LD + e % D] = (e / D == e % D) ? 1.f : 0.f;
   for (int c = nc - 1; c >= 0; --c) {
     const int rows = min(CB, L - c * CB);
     const KR* src = kr + ((size_t)bh * Lp + (size_t)c * CB) * D;
@@ -77,30 +79,37 @@ __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, in
       l2_prefetch(f + ((size_t)bh * nc + c) * D * D, D * D * sizeof(float));
       l2_prefetch(kr + ((size_t)bh * Lp + (size_t)(c - 1) * CB) * D, CB * D * sizeof(KR));
     }
-    for (int e = tid; e < CB * D; e += PT) s.a[(e / D) * LD + e % D] = e / D < rows ? to_f(src[e]) : 0.f;
+    for (int e = tid; e < CB * D; e += PT) sa[(e / D) * LD + e % D] = e / D < rows ? to_f(src[e]) : 0.f;
     __syncthreads();
-    float acc[4][4];
-    mm_abt(s.a, s.s, r0, n0, acc);  // K->_c S_c^T
+    for (int blk = tid; blk < (CB / 4) * NB; blk += PT) {  // K->_c S_c^T
+      const int r0 = 4 * (blk / NB), n0 = 4 * (blk % NB);
+      float acc[4][4];
+      mm_abt<D, LD>(sa, ss, r0, n0, acc);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (r0 + i < rows) {
-        T* dst = k_cache + ((size_t)bh * cap + (size_t)c * CB + r0 + i) * D + n0;
+      for (int i = 0; i < 4; ++i) {
+        if (r0 + i < rows) {
+          T* dst = k_cache + ((size_t)bh * cap + (size_t)c * CB + r0 + i) * D + n0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = from_f<T>(acc[i][j]);
+          for (int j = 0; j < 4; ++j) dst[j] = from_f<T>(acc[i][j]);
+        }
       }
     }
     if (c == 0) break;
     __syncthreads();  // every thread has read K->_c
     const float* fc = f + ((size_t)bh * nc + c) * D * D;
-    for (int e = tid; e < D * D; e += PT) s.a[(e / D) * LD + e % D] = fc[e];
+    for (int e = tid; e < D * D; e += PT) sa[(e / D) * LD + e % D] = fc[e];
     __syncthreads();
-    mm_abt(s.s, s.a, r0, n0, acc);  // S_c F_c^T
+    for (int blk = tid; blk < NB * NB; blk += PT) {  // S_c F_c^T
+      const int r0 = 4 * (blk / NB), n0 = 4 * (blk % NB);
+      float acc[4][4];
+      mm_abt<D, LD>(ss, sa, r0, n0, acc);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s.t[(r0 + i) * LD + n0 + j] = acc[i][j];
+        for (int j = 0; j < 4; ++j) st[(r0 + i) * LD + n0 + j] = acc[i][j];
+    }
     __syncthreads();
-    for (int e = tid; e < D * D; e += PT) s.s[(e / D) * LD + e % D] = s.t[(e / D) * LD + e % D];
+    for (int e = tid; e < D * D; e += PT) ss[(e / D) * LD + e % D] = st[(e / D) * LD + e % D];
     __syncthreads();
   }
 }
@@ -111,11 +120,15 @@ struct PrefillWs {
   FwdWs lay;
   size_t f32, total;
 };
+// The tcgen05 preparation (bf16 cache, head dim 64) writes bf16 K-> and a separate fp32 F; the SIMT
+// preparation writes both in fp32.
+bool prefill_tc(const Geom& g, bool is_bf16) { return is_bf16 && g.D == kHeadDim; }
 PrefillWs prefill_ws(const Geom& g, bool is_bf16) {
   PrefillWs w;
-  w.lay = fwd_ws_layout(g, is_bf16 ? 2 : 4);
+  const bool tcp = prefill_tc(g, is_bf16);
+  w.lay = fwd_ws_layout(g, tcp ? 2 : 4);
   w.f32 = align_up(w.lay.total, 256);
-  w.total = is_bf16 ? w.f32 + (size_t)g.BH * g.nc * D * D * 4 : w.lay.total;
+  w.total = tcp ? w.f32 + (size_t)g.BH * g.nc * g.D * g.D * 4 : w.lay.total;
   return w;
 }
 
@@ -146,13 +159,13 @@ __global__ void __launch_bounds__(PT) prefill_logf_prefix_kernel(int L, int cap,
   }
 }
 
-template <typename T, typename KR>
+template <typename T, typename KR, int D, int CB>
 cudaError_t transport(const Geom& g, int cap, const KR* kr, const float* f, void* k_cache, cudaStream_t st) {
-  const size_t smem = sizeof(PrefillSmem);
-  cudaError_t e = cudaFuncSetAttribute(prefill_transport_kernel<T, KR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const size_t smem = prefill_smem_bytes<D>();
+  auto kern = prefill_transport_kernel<T, KR, D, CB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  prefill_transport_kernel<T, KR><<<(unsigned)g.BH, PT, smem, st>>>(g.L, g.Lp, g.nc, cap, kr, f, (T*)k_cache);
+  kern<<<(unsigned)g.BH, PT, smem, st>>>(g.L, g.Lp, g.nc, cap, kr, f, (T*)k_cache);
   return cudaGetLastError();
 }
 
@@ -163,19 +176,28 @@ size_t prefill_ws_bytes(const Geom& g, bool is_bf16) { return prefill_ws(g, is_b
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
                            const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st,
                            const float* logf, float* a_cache) {
-  if (g.B != CB || (!logf) != (!a_cache)) return cudaErrorInvalidValue;
+  if ((!logf) != (!a_cache)) return cudaErrorInvalidValue;
+  if (!((g.D == kHeadDim && g.B == 64) || (g.D == kHeadDimWide && g.B == 32))) return cudaErrorInvalidValue;
   const PrefillWs pw = prefill_ws(g, is_bf16);
   cudaError_t e;
   // K-> and F of every chunk (the query input is unused here: k stands in for it)
-  if (is_bf16) {
+  if (g.D == kHeadDimWide) {
+    if ((e = launch_prep_simt(is_bf16, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
+    const float* kr = (const float*)(ws + pw.lay.kr);
+    const float* f = (const float*)(ws + pw.lay.f);
+    e = is_bf16 ? transport<__nv_bfloat16, float, kHeadDimWide, 32>(g, cap, kr, f, k_cache, st)
+                : transport<float, float, kHeadDimWide, 32>(g, cap, kr, f, k_cache, st);
+  } else if (is_bf16) {
     FwdWs lay = pw.lay;
     lay.f = pw.f32;  // F in fp32
     if ((e = cudaMemsetAsync(ws + lay.err, 0, sizeof(int), st)) != cudaSuccess) return e;
     if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, lay, false, st, true)) != cudaSuccess) return e;
-    e = transport<__nv_bfloat16>(g, cap, (const __nv_bfloat16*)(ws + lay.kr), (const float*)(ws + pw.f32), k_cache, st);
+    e = transport<__nv_bfloat16, __nv_bfloat16, kHeadDim, 64>(g, cap, (const __nv_bfloat16*)(ws + lay.kr),
+                                                              (const float*)(ws + pw.f32), k_cache, st);
   } else {
     if ((e = launch_prep_simt(false, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
-    e = transport<float>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f), k_cache, st);
+    e = transport<float, float, kHeadDim, 64>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f),
+                                              k_cache, st);
   }
   if (e != cudaSuccess) return e;
   if (logf) {
@@ -183,7 +205,7 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // values are appended unchanged: rows 0..L-1 of every (batch, head) slab of the cache
-  const size_t row = (size_t)D * (is_bf16 ? 2 : 4);
+  const size_t row = (size_t)g.D * (is_bf16 ? 2 : 4);
   return cudaMemcpy2DAsync(v_cache, (size_t)cap * row, v, (size_t)g.L * row, (size_t)g.L * row, (size_t)g.BH,
                            cudaMemcpyDeviceToDevice, st);
 }

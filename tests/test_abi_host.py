@@ -170,9 +170,13 @@ def test_prefill_argument_errors(pa):
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec[:4], FAKE, None, FAKE, n, None) == 1  # log_f alone
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 70, *vec[:4], None, FAKE, FAKE, n, None) == 1  # a_cache alone
     assert pa.path_decode_prefill(dd, FAKE, FAKE, 0, *vec, FAKE, n, None) == 0     # nothing to do
-    bad = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)
+    bad = pa.path_decode_desc_t(2, 2, 96, 100, pa.PATH_BF16, 1.0)
     assert pa.path_decode_prefill_workspace_size(bad, 10) == 0
     assert pa.path_decode_prefill(bad, FAKE, FAKE, 10, *vec, FAKE, n, None) == 2
+    wide = pa.path_decode_desc_t(2, 2, 128, 100, pa.PATH_BF16, 1.0)   # head dim 128: fp32 preparation
+    n128 = pa.path_decode_prefill_workspace_size(wide, 70)
+    assert n128 > n
+    assert pa.path_decode_prefill(wide, FAKE, FAKE, 70, *vec, FAKE, n128 - 1, None) == 3
 
 
 def test_fox_decode_argument_errors(pa):

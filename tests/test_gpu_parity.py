@@ -525,3 +525,36 @@ def test_decode_d128_matches_forward_rows(cuda_lib):
                                    sl(inp["beta"]), scale=1.0))
     o_d = torch.stack(rows, 2)
     assert (o_d - o_f).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("dtype,L", [("fp32", 1), ("fp32", 33), ("fp32", 200), ("bf16", 150)])
+def test_prefill_d128_cache_matches_oracle(cuda_lib, dtype, L):
+    """Hand-off at head dim 128 (fp32 preparation on 32-row chunks, 128 x 128 suffix products):
+    keys transported to the prompt end, values copied, rows >= L untouched."""
+    inp = gen_path_inputs(1, 2, L, 128, dtype, seed=800 + L, near2_frac=0.05)
+    cap = L + 5
+    kc, vc = run_prefill(inp, dtype, cap)
+    kref, vref = orc.prefill_cache(flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]), cap)
+    if dtype == "fp32":
+        check(flat(kc)[:, :L], kref[:, :L], 1e-4, "k_cache")
+    else:
+        check(flat(kc)[:, :L], kref[:, :L], 2e-2 * np.abs(kref).max(), "k_cache", rel=2e-2)
+    check(flat(vc)[:, :L], vref[:, :L], 0.0, "v_cache")
+    assert bool((flat(kc)[:, L:] == 7).all()) and bool((flat(vc)[:, L:] == 7).all())
+
+
+def test_prefill_d128_then_decode_matches_forward(cuda_lib):
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    L, steps = 70, 3
+    inp = gen_path_inputs(1, 2, L + steps, 128, "fp32", seed=811, near2_frac=0.05)
+    head = {n: inp[n][:, :, :L].contiguous() for n in ("k", "v", "w", "beta")}
+    kc, vc = run_prefill(head, "fp32", L + steps)
+    o_ref, _ = orc.fwd(flat(inp["q"]), flat(inp["k"]), flat(inp["v"]), flat(inp["w"]), flat(inp["beta"]), None, 1.0)
+    t = {n: inp[n].to(DEV) for n in ("q", "k", "v", "w", "beta")}
+    for s in range(steps):
+        pos = L + s
+        o = pa.decode_step(kc, vc, pos, *(t[n][:, :, pos].contiguous() for n in ("q", "k", "v", "w", "beta")),
+                           scale=1.0)
+        torch.cuda.synchronize()
+        check(flat(o), o_ref[:, pos], 1e-4, f"o[{pos}]")
