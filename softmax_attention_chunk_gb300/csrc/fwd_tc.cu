@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       // forget gate x is a plain multiple of the raw score, so its maximum comes from the raw
       // maximum (minimum for a negative scale) and x itself is folded into the exponent below
       float mxh;
+      uint64_t v2[FOX ? 16 : 1];  // FoX: the biased log2-domain scores, key pairs (kept packed)
       if (FOX) {
         // the keys' suffix sums came with the chunk's stage (its barrier completed before S was
         // issued; the stage is refilled only after this step's P V)
@@ -313,19 +314,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const ulonglong2 fv = f4[q];
-          const uint64_t x01 = f2_fma(f2(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1])), sc2,
-                                      f2_fma(fv.x, l2e2, rb2));
-          const uint64_t x23 = f2_fma(f2(__uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3])), sc2,
-                                      f2_fma(fv.y, l2e2, rb2));
+          v2[2 * q] = f2_fma(f2(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1])), sc2,
+                             f2_fma(fv.x, l2e2, rb2));
+          v2[2 * q + 1] = f2_fma(f2(__uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3])), sc2,
+                                 f2_fma(fv.y, l2e2, rb2));
           float a0, a1, a2, a3;
-          f2_split(x01, a0, a1);
-          f2_split(x23, a2, a3);
+          f2_split(v2[2 * q], a0, a1);
+          f2_split(v2[2 * q + 1], a2, a3);
           e0 = max3(e0, a0, a1);
           e1 = max3(e1, a2, a3);
-          x[4 * q] = __float_as_uint(a0);
-          x[4 * q + 1] = __float_as_uint(a1);
-          x[4 * q + 2] = __float_as_uint(a2);
-          x[4 * q + 3] = __float_as_uint(a3);
         }
         mxh = fmaxf(e0, e1);
       } else {
@@ -378,9 +375,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const uint64_t nm = f2(-m, -m), sc = f2(p.scl, p.scl);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const uint64_t xx = f2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
           float a0, a1;
-          f2_split(FOX ? f2_add(xx, nm) : f2_fma(xx, sc, nm), a0, a1);
+          if constexpr (FOX) {
+            f2_split(f2_add(v2[j], nm), a0, a1);
+          } else {
+            f2_split(f2_fma(f2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1])), sc, nm), a0, a1);
+          }
           const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
           acc[j & 1] = f2_add(acc[j & 1], f2(p0, p1));
           pk[j] = pack_bf16(p0, p1);
