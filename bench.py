@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -87,6 +88,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-d128", action="store_true", help="skip the head-dim-128 measurements")
+    ap.add_argument("--clocks-dir", default=None, help="where to keep the raw nvidia-smi clock samples "
+                                                        "(default: the system temporary directory)")
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
@@ -124,10 +127,10 @@ class Clocks:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, directory=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(directory or tempfile.gettempdir(), f"clocks_{os.getpid()}_{index}.csv")
 
     def start(self):
         try:
@@ -317,7 +320,7 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         step()
-    clocks = Clocks(local)
+    clocks = Clocks(local, args.clocks_dir)
     barrier(ws)
     clocks.start()
     evs = []
@@ -516,7 +519,7 @@ def run_decode(args, pa, dev, rank, ws, pk):
                        ws=wsd, out=o)
     kc.copy_(kc0)
     vc.copy_(vc0)
-    clocks = Clocks(dev.index)
+    clocks = Clocks(dev.index, args.clocks_dir)
     barrier(ws)
     clocks.start()
     marks = [ev()]
