@@ -347,10 +347,10 @@ def _loss(q, k, v, w, beta, logf, scale, dO):
     return float((o[0] * dO).sum())
 
 
-@pytest.mark.parametrize("fox", [False, True])
-def test_gradients_match_central_differences(fox):
-    rng = np.random.default_rng(23 + fox)
-    L, d, scale = 9, 4, 1.3
+@pytest.mark.parametrize("fox,L,d", [(False, 9, 4), (True, 9, 4), (True, 5, 128)])
+def test_gradients_match_central_differences(fox, L, d):
+    rng = np.random.default_rng(23 + fox + d)
+    scale = 1.3
     q, k, v, w, beta, logf = rand_problem(rng, L, d, beta_lo=0.2, beta_hi=1.8, fox=fox)
     dO = rng.standard_normal((L, d))
     g = orc.bwd(q[None], k[None], v[None], w[None], beta[None], None if logf is None else logf[None],
@@ -375,10 +375,11 @@ def test_gradients_match_central_differences(fox):
         assert err < 1e-6, (name, err)
 
 
-def test_gradients_match_autograd_of_explicit_products():
+@pytest.mark.parametrize("L,d", [(16, 8), (7, 128)])
+def test_gradients_match_autograd_of_explicit_products(L, d):
     """Reverse mode of an independent brute-force PyTorch fp64 formulation (explicit H matrices)."""
-    rng = np.random.default_rng(29)
-    L, d, scale = 16, 8, 0.8
+    rng = np.random.default_rng(29 + d)
+    scale = 0.8
     q, k, v, w, beta, logf = rand_problem(rng, L, d, fox=True)
     dO = rng.standard_normal((L, d))
     T = {n: torch.tensor(a, requires_grad=True) for n, a in
