@@ -32,7 +32,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from softmax_attention_chunk_gb300.inputs import CONFIGS, gen_decode_inputs, gen_path_inputs  # noqa: E402
+from softmax_attention_chunk_gb300.inputs import (BETA_MAX_BELOW_2, CONFIGS, gen_decode_inputs,  # noqa: E402
+                                                  gen_path_inputs)
 
 METRIC = "PaTH fwd+bwd TFLOP/s (B32 H32 d64 L4K) vs bf16 peak; decode HBM GB/s"
 FWD_CFG = "fig1_fwd_l4096"
@@ -52,6 +53,10 @@ UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule 
 # heads 16 at a time, so a launch over more heads repeats that traffic per group.  To be retaken
 # whenever the kernel changes.
 BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (425917440 + 80140288) / 16
+# DRAM bytes per head of one decode step at t = 32768 (split + combine kernels): ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum) of a batch-4 x 32-head step divided by 128 heads.
+# None until captured.
+DECODE_DRAM_BYTES_PER_HEAD_T32768 = None
 
 
 def tiles_steps(L):
@@ -93,6 +98,12 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="override the decode workload's batch (profiling on a smaller case)")
+    ap.add_argument("--only", default=None, choices=["train", "decode", "configs"],
+                    help="run one leg alone (profiling): the training step, the decode step or the "
+                         "per-workload forward/training legs")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload legs")
     return ap.parse_args()
 
 
@@ -196,8 +207,7 @@ def run_reference(args):
     from oracle import oracle as orc
 
     cfg = dict(CONFIGS[FWD_CFG])
-    from softmax_attention_chunk_gb300 import build_lib  # noqa: F401  (chunk sizes only; no GPU)
-    B_f, B_b = chunk_sizes()
+    B_f, B_b = TC_CHUNK, TC_CHUNK  # the flop count of the tensor-core path (this arm loads only the oracle)
     L, d = cfg["seqlen"], cfg["head_dim"]
     per_step = fwd_flops_per_head(L, d, B_f) + bwd_flops_per_head(L, d, B_b)
 
@@ -222,6 +232,11 @@ def run_reference(args):
                              "sample": "one (batch, head) of the B32 H32 L4096 workload per step, fwd+bwd fp64"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# Key chunk of the bf16 tensor-core path at head dim 64 (what path_attn_chunk reports for the
+# workloads below); the reference arm counts flops with it without loading the library.
+TC_CHUNK = 64
 
 
 def chunk_sizes():
@@ -277,6 +292,15 @@ def run_ours(args):
     from softmax_attention_chunk_gb300 import path_attn as pa
 
     pk = peaks()
+    dev = torch.device("cuda", local)
+    if args.only == "decode":
+        print(json.dumps({"decode": run_decode(args, pa, dev, rank, ws, pk)}), flush=True)
+        return
+    if args.only == "configs":
+        print(json.dumps({"configs": run_configs(args, pa, dev, pk, False)}), flush=True)
+        return
+    if args.only == "train":
+        args.no_decode = args.no_configs = args.no_cpu_baseline = True
     cfg = rank_config(rank)  # each rank owns its own (batch, head) problems
     if args.batch:
         cfg["batch"] = args.batch
@@ -285,7 +309,6 @@ def run_ours(args):
     Bt, H, L, d = cfg["batch"], cfg["heads"], cfg["seqlen"], cfg["head_dim"]
     BH = Bt * H
     B_f, B_b = chunk_sizes()
-    dev = torch.device("cuda", local)
 
     host = gen_path_inputs(**cfg, with_dO=True)
     host = {k: v.pin_memory() for k, v in host.items() if v is not None}
@@ -471,6 +494,9 @@ def run_ours(args):
     del ws_b, grads, x, host, outs_h
     torch.cuda.empty_cache()
 
+    confs = None if args.no_configs else run_configs(args, pa, dev, pk, rank == 0 and ws == 1 and
+                                                     not args.no_cpu_baseline)
+    torch.cuda.empty_cache()
     dec = None if args.no_decode else run_decode(args, pa, dev, rank, ws, pk)
     torch.cuda.empty_cache()
     handoff = None if args.no_decode else run_prefill_handoff(args, pa, dev, pk)
@@ -492,17 +518,164 @@ def run_ours(args):
                 "fa_convention_tflops": ws * fa_flops_step / (ms_step * 1e-3) / 1e12,
                 "phases": phases, "roofline": roofline, "scan_roofline": scan_roofline, "forward": forward,
                 "fox_train": fox_train, "e2e": e2e,
-                "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 5 * args.steps,
+                "clocks": clocks_rec, "gpu_launches": 5 * args.steps, "memset_ops": 4 * args.steps,
                 "peaks": pk, "decode": dec, "prefill_handoff": handoff, "head_dim_128": d128,
-                "cpu_baseline": cpu}
+                "configs": confs, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
 
+def device_inputs(Bt, H, L, d, gen, near2_frac=0.0, fox=False, with_dO=False):
+    """One workload's inputs drawn on the device with the distributions of inputs.py: q, k, v ~
+    N(0, 1)/sqrt(d) and w unit (bf16), beta = 2 sigmoid(N(0, 1)) with a fraction near2_frac in
+    [1.95, 2) (fp32), log f = log sigmoid(N(2, 1)) (fp32), dO ~ N(0, 1) (bf16)."""
+    sd = 1.0 / math.sqrt(d)
+    dev = gen.device
+    x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=gen) * sd).to(torch.bfloat16) for n in ("q", "k", "v")}
+    w = torch.randn(Bt, H, L, d, device=dev, generator=gen)
+    x["w"] = (w / w.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    beta = 2.0 * torch.sigmoid(torch.randn(Bt, H, L, device=dev, generator=gen))
+    if near2_frac > 0:
+        m = torch.rand(Bt, H, L, device=dev, generator=gen) < near2_frac
+        beta = torch.where(m, 1.95 + 0.05 * torch.rand(Bt, H, L, device=dev, generator=gen), beta)
+    x["beta"] = beta.clamp(max=BETA_MAX_BELOW_2).contiguous()
+    x["log_f"] = (torch.nn.functional.logsigmoid(torch.randn(Bt, H, L, device=dev, generator=gen) + 2.0)
+                  if fox else None)
+    x["dO"] = torch.randn(Bt, H, L, d, device=dev, generator=gen).to(torch.bfloat16) if with_dO else None
+    return x
+
+
+def time_events(fn, warmup, reps):
+    """Mean ms of fn over reps calls after warmup calls (CUDA events on the current stream)."""
+    for _ in range(warmup):
+        fn()
+    marks = [ev()]
+    for _ in range(reps):
+        fn()
+        marks.append(ev())
+    torch.cuda.synchronize()
+    return statistics.mean(marks[i].elapsed_time(marks[i + 1]) for i in range(reps))
+
+
+def oracle_rate(fn, work_per_call, budget_s, max_calls):
+    """(work per second, calls, seconds) of fn run on the host cores until budget_s or max_calls."""
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_calls and (n == 0 or time.perf_counter() - t0 < budget_s):
+        fn(n)
+        n += 1
+    dt = time.perf_counter() - t0
+    return work_per_call * n / dt, n, dt
+
+
+def run_configs(args, pa, dev, pk, with_cpu):
+    """The other workloads, one leg each, with inputs drawn on the device (same distributions as
+    the parity tests' CPU generator): the inference forward at batch 32 x 32 heads, L 2048 and
+    4096; the training step at batch 8 x 16 heads, L 4096; the PaTH-FoX inference forward at
+    batch 1 x 32 heads, L 16384; the fp32 tiny forward (batch 1 x 2 heads, L 128).  Each reports
+    ms, TFLOP/s (per-head flops of the metric, chunk 64) against the bf16 peak and tokens/s; with
+    with_cpu also the oracle timed on whole heads of the same shape on the host cores, in the same
+    unit."""
+    from oracle import oracle as orc
+
+    g = torch.Generator(device=dev).manual_seed(9001)
+    reps = max(3, args.steps)
+    out = {}
+    ffl = lambda L: fwd_flops_per_head(L, D, TC_CHUNK)
+    bfl = lambda L: bwd_flops_per_head(L, D, TC_CHUNK)
+
+    def cpu_fwd(Bt, H, L, fox, near2, flops_head, bwd=False):
+        if not with_cpu:
+            return None
+        seeds = dict(seed=4242, batch=Bt, heads=H, seqlen=L, head_dim=D, dtype="bf16", near2_frac=near2, fox=fox)
+
+        def one(n):
+            x = gen_path_inputs(**seeds, with_dO=bwd, heads_subset=[n])
+            orc.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], 1.0)
+            if bwd:
+                orc.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], 1.0, x["dO"])
+        rate, n, dt = oracle_rate(one, flops_head, 4.0, 8)
+        return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                "sample": f"{n} whole head(s) of this shape, {'fwd+bwd' if bwd else 'fwd'} fp64 (input generation "
+                          f"included), {dt:.1f} s"}
+
+    for name, (Bt, H, L, near2) in {"fig1_fwd_l2048": (32, 32, 2048, 0.05),
+                                     "fig1_fwd_l4096": (32, 32, 4096, 0.05)}.items():
+        x = device_inputs(Bt, H, L, D, g, near2_frac=near2)
+        desc = pa.make_desc(x["q"], 1.0)
+        wsf = pa.workspace(desc, 0, dev)
+        o, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+        ms = time_events(lambda: pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, 1.0, ws=wsf,
+                                        out=(o, lse)), args.warmup, reps)
+        tf = Bt * H * ffl(L) / (ms * 1e-3) / 1e12
+        out[name] = {"workload": f"inference forward, batch {Bt}, {H} heads, d=64, L={L}, bf16, 5% near-reflection "
+                                 "beta", "ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16"],
+                     "tokens_per_s": Bt * L / (ms * 1e-3),
+                     "fa_convention_tflops": Bt * H * 2 * L * L * D / (ms * 1e-3) / 1e12,
+                     "cpu_oracle": cpu_fwd(Bt, H, L, False, near2, ffl(L))}
+        del x, wsf, o, lse
+        torch.cuda.empty_cache()
+
+    # training step, batch 8 x 16 heads, L 4096 (the bench's reuse path)
+    Bt, H, L = 8, 16, 4096
+    x = device_inputs(Bt, H, L, D, g, with_dO=True)
+    desc = pa.make_desc(x["q"], 1.0)
+    wsb = pa.workspace(desc, 1, dev)
+    o, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+    gr = dict(dq=torch.empty_like(o), dk=torch.empty_like(o), dv=torch.empty_like(o), dw=torch.empty_like(o),
+              dbeta=torch.empty_like(x["beta"]))
+
+    def train():
+        a = (x["q"], x["k"], x["v"], x["w"], x["beta"])
+        pa.fwd(*a, None, 1.0, ws=wsb, out=(o, lse), phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z)
+        pa.bwd(*a, o, lse, x["dO"], 1.0, ws=wsb, out=gr,
+               phases=pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD)
+    ms = time_events(train, args.warmup, reps)
+    fl = Bt * H * (ffl(L) + bfl(L))
+    out["train_b8h16_l4096"] = {"workload": "training step (fwd storing Z + bwd reusing it), batch 8, 16 heads, d=64, "
+                                            "L=4096, bf16", "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / pk["bf16"],
+                                "tokens_per_s": Bt * L / (ms * 1e-3),
+                                "cpu_oracle": cpu_fwd(Bt, H, L, False, 0.0, ffl(L) + bfl(L), bwd=True)}
+    del x, wsb, o, lse, gr
+    torch.cuda.empty_cache()
+
+    # PaTH-FoX inference forward, batch 1 x 32 heads, L 16384
+    Bt, H, L = 1, 32, 16384
+    x = device_inputs(Bt, H, L, D, g, fox=True)
+    desc = pa.make_desc(x["q"], 1.0)
+    wsf = pa.workspace(desc, 0, dev)
+    o, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+    ms = time_events(lambda: pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], 1.0, ws=wsf,
+                                    out=(o, lse)), args.warmup, reps)
+    tf = Bt * H * ffl(L) / (ms * 1e-3) / 1e12
+    out["fox_long_l16384"] = {"workload": "PaTH-FoX inference forward, batch 1, 32 heads, d=64, L=16384, bf16",
+                              "ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16"],
+                              "tokens_per_s": Bt * L / (ms * 1e-3),
+                              "cpu_oracle": cpu_fwd(Bt, H, L, True, 0.0, ffl(L))}
+    del x, wsf, o, lse
+    torch.cuda.empty_cache()
+
+    # fp32 tiny forward (the 1e-4 mode), batch 1 x 2 heads, L 128: launch bound
+    Bt, H, L = 1, 2, 128
+    x = {n: (t.float() if t is not None and t.dtype == torch.bfloat16 else t)
+         for n, t in device_inputs(Bt, H, L, D, g).items()}
+    desc = pa.make_desc(x["q"], 1.0)
+    wsf = pa.workspace(desc, 0, dev)
+    o, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+    ms = time_events(lambda: pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, 1.0, ws=wsf, out=(o, lse)),
+                     args.warmup, 20)
+    out["pr1_tiny_fwd"] = {"workload": "forward, batch 1, 2 heads, d=64, L=128, fp32 CUDA-core kernels", "ms": ms,
+                           "tokens_per_s": Bt * L / (ms * 1e-3), "bound": "launch latency (two small launches)"}
+    return out
+
+
 def run_decode(args, pa, dev, rank, ws, pk):
     cfg = dict(CONFIGS[DEC_CFG])
     cfg["seed"] += 7919 * rank
+    if args.decode_batch:
+        cfg["batch"] = args.decode_batch
     Bt, H, d, t0 = cfg["batch"], cfg["heads"], cfg["head_dim"], cfg["t0"]
     steps = args.decode_steps
     di = gen_decode_inputs(**{**cfg, "steps": steps})
@@ -553,12 +726,32 @@ def run_decode(args, pa, dev, rank, ws, pk):
     fox_ms = max_over_ranks(sum(fmarks[i].elapsed_time(fmarks[i + 1]) for i in range(steps)), ws)
     fox_bytes = nbytes + sum(Bt * H * (t0 + s) * 4 for s in range(steps))  # + the prefix cache
     fox_gbs = ws * fox_bytes / (fox_ms * 1e-3) / 1e9
+    traffic = (DECODE_DRAM_BYTES_PER_HEAD_T32768 * Bt * H
+               if DECODE_DRAM_BYTES_PER_HEAD_T32768 is not None and t0 == 32768 else None)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as orc
+
+        sub = gen_decode_inputs(**{**cfg, "steps": 8}, heads_subset=[0, 1])
+        kref = sub["k_cache"].double().numpy().copy()
+        vref = sub["v_cache"].double().numpy().copy()
+
+        def one(s):
+            orc.decode_step(kref, vref, t0 + s, *(sub[n][s] for n in ("q", "k", "v", "w", "beta")), cfg["scale"])
+        rate, n, dt = oracle_rate(one, 2 * 3 * t0 * d * 2, 4.0, 8)
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+               "sample": f"{n} decode steps of 2 heads at t = {t0}..{t0 + n - 1} (fp64 caches; bytes counted as the "
+                         f"GPU's 3 t d 2 per head), {dt:.1f} s"}
     return {"value": gbs, "unit": "GB/s", "tokens_per_s": ws * Bt * steps / (total_ms * 1e-3),
             "ms_per_step": total_ms / steps, "steps": steps, "frac_of_hbm": gbs / ws / pk["hbm"],
             "roofline": {"kernel": "decode step (split + combine)", "bound": "hbm", "achieved": gbs / ws,
-                         "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / ws / pk["hbm"], "traffic": None},
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / ws / pk["hbm"], "traffic": traffic,
+                         "traffic_note": "DRAM bytes of one step at t = 32768 (decode_split_kernel + "
+                                         "decode_combine_kernel), scaled by heads from an ncu capture of a "
+                                         "4-batch step"},
+            "cpu_oracle": cpu,
             "clocks": crec, "gpu_launches": 2 * steps,
-            "workload": "decode, batch 32, 32 heads, d=64, cache 32768 -> 33023 bf16, 256 steps",
+            "workload": f"decode, batch {Bt}, {H} heads, d=64, cache {t0} -> {t0 + steps - 1} bf16, {steps} steps",
             "fox": {"value": fox_gbs, "unit": "GB/s", "ms_per_step": fox_ms / steps,
                     "frac_of_hbm": fox_gbs / ws / pk["hbm"], "gpu_launches": 2 * steps,
                     "workload": "PaTH-FoX decode, same cache and steps, forget-gate prefix sums beside the cache"}}

@@ -27,7 +27,8 @@
  *    notes §2.1/§2.2).  Inputs already in range are used unchanged; dbeta is the gradient with
  *    respect to the clamped value.  w is used as given (it is not renormalised).
  *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).  Work is
- *    enqueued asynchronously; faults inside kernels surface at the caller's next sync.
+ *    enqueued asynchronously; faults inside kernels surface at the caller's next sync, and a
+ *    tensor-core kernel whose internal wait gave up is reported by path_attn_workspace_status.
  *  - Errors: every argument is validated before any CUDA call; on a validation error nothing
  *    is launched and a status below is returned.  Launch failures return PATH_ERR_CUDA.
  *    No exception crosses the ABI.
@@ -186,24 +187,6 @@ int path_decode_step(const path_decode_desc_t* desc, void* k_cache, void* v_cach
                      const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                      const float* beta_t, void* o_t, void* ws, size_t ws_bytes, void* stream);
 
-/*
- * path_decode_step without a workspace argument.  The paper has no counterpart: this exists
- * for callers that cannot allocate device memory when they decode — code running inside
- * another runtime's memory pool without access to its allocator, plugins that may only use
- * the buffers handed to them, or serving loops that forbid allocation after start-up.
- *
- * Same arguments, semantics and results as path_decode_step, minus ws/ws_bytes.  The per-split
- * partial softmax states live in a fixed 16 MiB array inside the library, present on every
- * GPU that loads it until the process exits.  Limit: batch * heads <= PATH_DECODE_NOALLOC_MAX_HEADS,
- * otherwise PATH_ERR_WORKSPACE is returned and nothing runs.  The call itself allocates
- * nothing (no cudaMalloc, no library allocator).
- *  - The first call made with a given device current looks up the array's device address
- *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
- *  - All calls on a device share the one array: calls that may overlap on the GPU (different
- *    streams without ordering between them) race and give wrong results.  Calls ordered on one
- *    stream are safe.  Nothing in the array needs to start at zero: each call overwrites the
- *    parts it reads.
- */
 /* Bytes of workspace path_decode_prefill needs for a prompt of prompt_len tokens (the fp32
  * chunk transforms of the prompt); 0 if the descriptor or prompt_len is invalid. Host only. */
 size_t path_decode_prefill_workspace_size(const path_decode_desc_t* desc, int prompt_len);
@@ -247,9 +230,63 @@ int path_decode_step_fox(const path_decode_desc_t* desc, void* k_cache, void* v_
                          const float* log_f_t, void* o_t, void* ws, size_t ws_bytes, void* stream);
 
 #define PATH_DECODE_NOALLOC_MAX_HEADS 496
+/*
+ * path_decode_step without a workspace argument.  The paper has no counterpart: this exists
+ * for callers that cannot allocate device memory when they decode — code running inside
+ * another runtime's memory pool without access to its allocator, plugins that may only use
+ * the buffers handed to them, or serving loops that forbid allocation after start-up.
+ *
+ * Same arguments, semantics and results as path_decode_step, minus ws/ws_bytes.  The per-split
+ * partial softmax states live in a fixed 16 MiB array inside the library, present on every
+ * GPU that loads it until the process exits.  Limit: batch * heads <= PATH_DECODE_NOALLOC_MAX_HEADS,
+ * otherwise PATH_ERR_WORKSPACE is returned and nothing runs.  The call itself allocates
+ * nothing (no cudaMalloc, no library allocator).
+ *  - The first call made with a given device current looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *    The cached address belongs to that device's current context: after cudaDeviceReset (or
+ *    anything else that destroys the primary context) it is stale, and this entry point must
+ *    not be called again in that process.
+ *  - All calls on a device share the one array: calls that may overlap on the GPU (different
+ *    streams without ordering between them) race and give wrong results.  Calls ordered on one
+ *    stream are safe.  Nothing in the array needs to start at zero: each call overwrites the
+ *    parts it reads.
+ */
 int path_decode_step_noalloc(const path_decode_desc_t* desc, void* k_cache, void* v_cache, int t,
                              const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                              const float* beta_t, void* o_t, void* stream);
+
+/*
+ * Device-side status of the passes that ran on a workspace.  (The pages have no failure
+ * machinery; this is the library's own.)  Every wait of the tensor-core kernels on their internal
+ * pipeline barriers is bounded (about 2 s); a wait that gives up writes a nonzero code into an int
+ * inside the workspace (the first code wins) and its kernel ends early, so the outputs of that
+ * call are incomplete even though the call returned PATH_OK (kernels run after it returns).
+ * This call waits for all work queued on `stream` (it synchronises the stream), then reads that
+ * word through a 4-byte copy into host memory.
+ *   desc, for_backward: the descriptor and the pass the workspace was sized for (they fix where the
+ *     word lives); ws, ws_bytes: that workspace.
+ * Returns PATH_OK (no wait gave up), PATH_ERR_INTERNAL (one did; *code, when code is not NULL,
+ * receives the first recorded code), PATH_ERR_CUDA (the synchronisation or the copy failed, e.g.
+ * after a kernel fault), or an argument error as the passes would return it.  Passes that run the
+ * fp32 CUDA-core kernels have no such waits: the call returns PATH_OK for them without touching
+ * the device.
+ * The word is cleared by the forward's PREPARE phase and by the backward's PREPARE phase (except
+ * with PATH_BWD_REUSE_FWD or PATH_BWD_Z_FROM_FWD, where it keeps the forward's code), so it covers
+ * every tensor-core kernel since the last clearing.
+ * Test hook: with the environment variable PATH_ATTN_DEBUG_STALL_NS set to n > 0 at the time of
+ * a call, the forward's PREPARE phase on the tensor-core path makes every CTA wait on a barrier
+ * that nothing arrives at, give up after n ns (at most 1 s), record code 99 and end without
+ * writing anything; the workspace status then reads PATH_ERR_INTERNAL with code 99.  The context
+ * stays usable: a later call without the variable runs normally.
+ */
+int path_attn_workspace_status(const path_attn_desc_t* desc, int for_backward, const void* ws, size_t ws_bytes,
+                               int* code, void* stream);
+
+/* The same for the workspace of path_decode_prefill (desc and prompt_len as given to it): the
+ * tcgen05 preparation of bf16 caches at head dim 64 has bounded waits; the other hand-off paths
+ * have none (PATH_OK).  Synchronises `stream`. */
+int path_decode_prefill_status(const path_decode_desc_t* desc, int prompt_len, const void* ws, size_t ws_bytes,
+                               int* code, void* stream);
 
 #ifdef __cplusplus
 }

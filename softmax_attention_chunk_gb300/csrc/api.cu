@@ -5,6 +5,7 @@
 
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 using namespace pathattn;
 
@@ -65,6 +66,26 @@ size_t fwd_ws_total(const path_attn_desc_t* d, const Geom& g) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA; }
 
+// Test hook of the failure path: PATH_ATTN_DEBUG_STALL_NS=<n> (n > 0) in the environment makes
+// the forward's PREPARE phase on the tensor-core path give up a wait after n ns in every CTA (see
+// launch_ut_prep64).  Read at every call; unset (the normal case) it is 0.
+uint32_t debug_stall_ns() {
+  const char* v = getenv("PATH_ATTN_DEBUG_STALL_NS");
+  if (!v || !*v) return 0;
+  const long long n = atoll(v);
+  return n <= 0 ? 0u : (n > 1000000000LL ? 1000000000u : (uint32_t)n);
+}
+
+// Reads the int error word at dev_word after the work queued on st; PATH_ERR_INTERNAL if it is set.
+int read_error_word(const void* dev_word, int* code, cudaStream_t st) {
+  int h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, dev_word, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return PATH_ERR_CUDA;
+  if (code) *code = h;
+  return h == 0 ? PATH_OK : PATH_ERR_INTERNAL;
+}
+
 }  // namespace
 
 #define PATH_API __attribute__((visibility("default")))
@@ -121,7 +142,9 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
     }
     if (phases & PATH_FWD_PREPARE) {
       rc = cuda_status(cudaMemsetAsync(wsb + tw.p64.err, 0, sizeof(int), st));
-      if (rc == PATH_OK) rc = cuda_status(launch_ut_prep64(tw.g64, q, k, v, w, beta, log_f, wsb, tw.p64, true, st));
+      if (rc == PATH_OK)
+        rc = cuda_status(launch_ut_prep64(tw.g64, q, k, v, w, beta, log_f, wsb, tw.p64, true, st, false,
+                                          debug_stall_ns()));
       if (rc != PATH_OK) return rc;
     }
     if (phases & PATH_FWD_SCAN) {
@@ -284,6 +307,35 @@ PATH_API int path_decode_step_fox(const path_decode_desc_t* d, void* k_cache, vo
   return cuda_status(launch_decode(d->cache_dtype == PATH_BF16, BH, d->capacity, t, d->scale, k_cache, v_cache,
                                    q_t, k_t, v_t, w_t, beta_t, o_t, (float*)ws, (cudaStream_t)stream, a_cache,
                                    log_f_t, d->head_dim));
+}
+
+PATH_API int path_attn_workspace_status(const path_attn_desc_t* desc, int for_backward, const void* ws,
+                                        size_t ws_bytes, int* code, void* stream) {
+  Geom g;
+  int rc = check_desc(desc, for_backward ? 1 : 0, &g);
+  if (rc != PATH_OK) return rc;
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  if (code) *code = 0;
+  if (!uses_tensor_cores(desc, for_backward)) return PATH_OK;  // no bounded waits on the fp32 path
+  const TcWs tw = tc_layout(desc, for_backward != 0);
+  if (ws_bytes < tw.total) return PATH_ERR_WORKSPACE;
+  return read_error_word((const char*)ws + tw.p64.err, code, (cudaStream_t)stream);
+}
+
+PATH_API int path_decode_prefill_status(const path_decode_desc_t* d, int prompt_len, const void* ws,
+                                        size_t ws_bytes, int* code, void* stream) {
+  int rc = check_decode_desc(d);
+  if (rc != PATH_OK) return rc;
+  if (prompt_len < 0) return PATH_ERR_INVALID_ARG;
+  if (prompt_len > d->capacity) return PATH_ERR_CAPACITY;
+  if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
+  if (code) *code = 0;
+  const Geom g = prefill_geom(d, prompt_len);
+  const bool bf = d->cache_dtype == PATH_BF16;
+  if (ws_bytes < prefill_ws_bytes(g, bf)) return PATH_ERR_WORKSPACE;
+  const size_t off = prefill_err_offset(g, bf);
+  if (prompt_len == 0 || off == (size_t)-1) return PATH_OK;  // nothing ran / no bounded waits
+  return read_error_word((const char*)ws + off, code, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -701,7 +701,9 @@ cudaError_t launch_bwd_tc(const TcWs& w, const void* q, const void* k, const voi
     if ((e = cudaMemsetAsync(ws + w.dkr64, 0, rows * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(ws + w.dv, 0, rows * D * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(ws + w.df64, 0, (size_t)g.BH * g.nc * D * D * 4, st)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
+    // the error word starts afresh unless the backward builds on the forward's state, whose
+    // timeouts it then keeps
+    if (!(phases & (8 | 16)) && (e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
     if ((e = launch_bwd_dot(g, o, dO, (float*)(ws + w.Dv), st)) != cudaSuccess) return e;
     if (logf) {  // PaTH-FoX: prefix sums of log f, zeroed column sums of dS'
       if ((e = launch_fox_prefix(g, logf, (float*)(ws + w.fxa), st)) != cudaSuccess) return e;

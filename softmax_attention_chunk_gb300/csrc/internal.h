@@ -171,6 +171,9 @@ cudaError_t launch_main_simt(bool is_bf16, const Geom& g, const void* v, const f
 // With logf and a_cache set (PaTH-FoX), rows 0..g.L-1 of a_cache ([g.BH][cap] fp32) get the
 // inclusive prefix sums of logf ([g.BH][g.L]).
 size_t prefill_ws_bytes(const Geom& g, bool is_bf16);
+// Byte offset in that workspace of the int error word of the tcgen05 preparation (bf16 caches at
+// head dim 64), or (size_t)-1 when the hand-off runs no kernel with bounded waits.
+size_t prefill_err_offset(const Geom& g, bool is_bf16);
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
                            const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st,
                            const float* logf = nullptr, float* a_cache = nullptr);
@@ -179,10 +182,12 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
 // tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32_f
 // (and no diagonal state) F is written in fp32 ([BH][nc][64][64]) at lay.f, which must then have
 // room for it, from products whose bf16 operands U and U^T W are split into high and low bf16
-// parts (about 16 significant bits).
+// parts (about 16 significant bits).  stall_ns (test hook of the failure path): nonzero makes every
+// CTA give up a wait on a barrier nothing arrives at after that many ns, recording code 99 in
+// lay.err, and end without writing anything.
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, bool f32_f = false);
+                             cudaStream_t st, bool f32_f = false, uint32_t stall_ns = 0);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

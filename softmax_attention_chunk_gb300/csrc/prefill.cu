@@ -173,6 +173,10 @@ cudaError_t transport(const Geom& g, int cap, const KR* kr, const float* f, void
 
 size_t prefill_ws_bytes(const Geom& g, bool is_bf16) { return prefill_ws(g, is_bf16).total; }
 
+size_t prefill_err_offset(const Geom& g, bool is_bf16) {
+  return (is_bf16 && g.D == kHeadDim) ? prefill_ws(g, is_bf16).lay.err : (size_t)-1;
+}
+
 cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, const void* v, const void* w,
                            const float* beta, void* k_cache, void* v_cache, char* ws, cudaStream_t st,
                            const float* logf, float* a_cache) {

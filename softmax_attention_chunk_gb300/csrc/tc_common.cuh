@@ -41,18 +41,23 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 // Waits for the phase with the given parity to complete, spinning on try_wait (which itself
-// suspends the thread in hardware for a while).  Gives up after about 2 s (global timer; a
-// hard cap on the polls as well), records `code` in *err and returns false, so that a broken
-// pipeline ends the kernel instead of hanging the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+// suspends the thread in hardware for a while).  Gives up after limit_ns of global time (a hard
+// cap on the polls as well), records `code` in *err (first code wins) and returns false, so that
+// a broken pipeline ends the kernel instead of hanging the GPU.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, int* err, int code,
+                                             uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 0 && global_ns() - t0 > 2000000000ull) break;
+    if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) break;
   }
   if (err) atomicCAS(err, 0, code);
   return false;
+}
+// The pipeline waits of the tensor-core kernels: about 2 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+  return mbar_wait_ns(bar, parity, err, code, 2000000000ull);
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

@@ -67,6 +67,7 @@ struct UtParams {
   float* ft;
   int with_diag;
   int* err;
+  uint32_t stall_ns;  // test hook: nonzero makes every CTA give up a wait (see the kernel's start)
 };
 
 struct __align__(1024) UtSmem {
@@ -108,6 +109,19 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
+  if (p.stall_ns) {
+    // Test hook of the failure path: a wait on a barrier that nothing arrives at runs out after
+    // stall_ns, records code 99 and ends the CTA before any copy or MMA has been issued, with its
+    // TMEM freed, as a pipeline wait that gives up does.
+    if (lead) mbar_wait_ns(&s.bar_v, 0, p.err, 99, p.stall_ns);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tb, TMEM_COLS);
+    }
+    return;
+  }
   uint32_t mph = 0;  // phase of bar_mma
   auto issue = [&](auto fn) {  // lead issues one round's MMAs and commits them
     if (lead) {
@@ -338,7 +352,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
 
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, bool f32_f) {
+                             cudaStream_t st, bool f32_f, uint32_t stall_ns) {
   if (g.B != 64 || (f32_f && with_diag)) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv, mw;
   if (!make_map_head_rows64(&mq, q, g.L, g.BH) || !make_map_head_rows64(&mk, k, g.L, g.BH) ||
@@ -363,6 +377,7 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
   p.ft = (float*)(ws + lay.ft);
   p.with_diag = with_diag ? 1 : 0;
   p.err = (int*)(ws + lay.err);
+  p.stall_ns = stall_ns;
   const size_t smem = sizeof(UtSmem) + 1024;
   auto kern = f32_f ? ut_prep64_kernel<true> : ut_prep64_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

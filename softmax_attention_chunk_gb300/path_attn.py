@@ -67,7 +67,12 @@ _lib.path_decode_prefill.restype = _i
 _lib.path_decode_prefill.argtypes = [_DDP, _vp, _vp, _i] + [_vp] * 6 + [_vp, _sz, _vp]
 _lib.path_decode_step_fox.restype = _i
 _lib.path_decode_step_fox.argtypes = [_DDP, _vp, _vp, _vp, _i] + [_vp] * 7 + [_vp, _sz, _vp]
+_lib.path_attn_workspace_status.restype = _i
+_lib.path_attn_workspace_status.argtypes = [_DP, _i, _vp, _sz, ctypes.POINTER(_i), _vp]
+_lib.path_decode_prefill_status.restype = _i
+_lib.path_decode_prefill_status.argtypes = [_DDP, _i, _vp, _sz, ctypes.POINTER(_i), _vp]
 PATH_DECODE_NOALLOC_MAX_HEADS = 496
+PATH_ERR_INTERNAL = 6
 
 PATH_FWD_PREPARE, PATH_FWD_SCAN, PATH_FWD_ALL = 1, 2, 3
 PATH_BWD_PREPARE, PATH_BWD_SCAN, PATH_BWD_FINISH, PATH_BWD_ALL = 1, 2, 4, 7
@@ -78,7 +83,8 @@ PATH_BWD_Z_FROM_FWD = 16
 EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size", "path_attn_fwd",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
             "path_decode_step", "path_decode_step_noalloc", "path_decode_prefill_workspace_size",
-            "path_decode_prefill", "path_decode_step_fox")
+            "path_decode_prefill", "path_decode_step_fox", "path_attn_workspace_status",
+            "path_decode_prefill_status")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -146,6 +152,23 @@ def path_decode_step_fox(desc, k_cache, v_cache, a_cache, t, q_t, k_t, v_t, w_t,
                                      beta_t, log_f_t, o_t, ws, ws_bytes, stream)
 
 
+def path_attn_workspace_status(desc, for_backward, ws, ws_bytes, stream):
+    """(status, first recorded device code) of the passes that ran on the workspace; synchronises
+    the stream."""
+    code = _i(0)
+    rc = _lib.path_attn_workspace_status(ctypes.byref(desc), int(for_backward), ws, ws_bytes, ctypes.byref(code),
+                                         stream)
+    return rc, code.value
+
+
+def path_decode_prefill_status(desc, prompt_len, ws, ws_bytes, stream):
+    """(status, first recorded device code) of a prefill hand-off's workspace; synchronises the stream."""
+    code = _i(0)
+    rc = _lib.path_decode_prefill_status(ctypes.byref(desc), int(prompt_len), ws, ws_bytes, ctypes.byref(code),
+                                         stream)
+    return rc, code.value
+
+
 # ---------------- torch-tensor wrappers ----------------
 
 _DT = {torch.bfloat16: PATH_BF16, torch.float32: PATH_FP32}
@@ -184,8 +207,17 @@ def workspace(desc, for_backward, device):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None, phases=PATH_FWD_ALL):
-    """o [B,H,L,d] (dtype of q) and lse [B,H,L] float32."""
+def check_workspace(desc, for_backward, ws):
+    """Raises RuntimeError if a tensor-core kernel that ran on `ws` gave up one of its bounded
+    waits (its outputs are then incomplete).  Synchronises the current stream."""
+    rc, code = path_attn_workspace_status(desc, for_backward, _p(ws), ws.numel(), _stream())
+    if rc != PATH_OK:
+        raise RuntimeError(f"device status of the workspace: {path_status_string(rc)} (code {code})")
+
+
+def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None, phases=PATH_FWD_ALL, check=False):
+    """o [B,H,L,d] (dtype of q) and lse [B,H,L] float32.  check=True synchronises and raises if a
+    kernel gave up a bounded wait (the workspace status)."""
     desc = make_desc(q, scale, chunk)
     for name, t in (("k", k), ("v", v), ("w", w)):
         _need(t, q.dtype, q.shape, name)
@@ -200,13 +232,15 @@ def fwd(q, k, v, w, beta, log_f=None, scale=1.0, chunk=0, ws=None, out=None, pha
     rc = path_attn_fwd_phases(phases, desc, _p(q), _p(k), _p(v), _p(w), _p(beta), _p(log_f), _p(o), _p(lse),
                               _p(ws), ws.numel(), _stream())
     _check(rc, "path_attn_fwd")
+    if check:
+        check_workspace(desc, 1 if ws.numel() >= path_attn_workspace_size(desc, 1) else 0, ws)
     return o, lse
 
 
 def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, out=None,
-        phases=PATH_BWD_ALL):
+        phases=PATH_BWD_ALL, check=False):
     """Gradients dict dq, dk, dv, dw (dtype of q) and dbeta (float32); with log_f (PaTH-FoX) also
-    dlog_f (float32)."""
+    dlog_f (float32).  check=True synchronises and raises if a kernel gave up a bounded wait."""
     desc = make_desc(q, scale, chunk)
     for name, t in (("k", k), ("v", v), ("w", w), ("o", o), ("dO", dO)):
         _need(t, q.dtype, q.shape, name)
@@ -225,6 +259,8 @@ def bwd(q, k, v, w, beta, o, lse, dO, scale=1.0, chunk=0, ws=None, log_f=None, o
                               _p(dO), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]), _p(out["dw"]),
                               _p(out["dbeta"]), _p(out.get("dlog_f")), _p(ws), ws.numel(), _stream())
     _check(rc, "path_attn_bwd")
+    if check:
+        check_workspace(desc, 1, ws)
     return out
 
 

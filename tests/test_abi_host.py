@@ -234,3 +234,28 @@ def test_training_step_bits_are_validated(pa):
     assert bwd(pa.PATH_BWD_ALL | pa.PATH_BWD_REUSE_FWD | pa.PATH_BWD_Z_FROM_FWD, b_bytes - 1) == 3
     assert bwd(pa.PATH_BWD_Z_FROM_FWD, b_bytes) == 1
     assert bwd(pa.PATH_BWD_ALL | 32, b_bytes) == 1
+
+
+def test_workspace_status_argument_errors(pa):
+    """The status calls validate their arguments before any CUDA call; on the fp32 path (no bounded
+    waits) and for an empty prompt they answer PATH_OK without touching the device."""
+    code = ctypes.c_int(-1)
+    d32 = desc(pa, dtype=pa.PATH_FP32)
+    n32 = pa.path_attn_workspace_size(d32, 1)
+    assert pa.path_attn_workspace_status(d32, 1, FAKE, n32, None) == (0, 0)   # fp32: nothing to read
+    assert pa.path_attn_workspace_status(desc(pa, head_dim=96), 0, FAKE, n32, None)[0] == 2
+    assert pa.path_attn_workspace_status(d32, 0, None, n32, None)[0] == 1
+    assert pa.path_attn_workspace_status(d32, 0, FAKE + 16, n32, None)[0] == 1  # not 256-byte aligned
+    dbf = desc(pa, dtype=pa.PATH_BF16)
+    nb = pa.path_attn_workspace_size(dbf, 0)
+    assert pa.path_attn_workspace_status(dbf, 0, FAKE, nb - 1, None)[0] == 3
+    assert pa._lib.path_attn_workspace_status(None, 0, FAKE, nb, ctypes.byref(code), None) == 1
+    dd = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_BF16, 1.0)
+    n = pa.path_decode_prefill_workspace_size(dd, 70)
+    assert pa.path_decode_prefill_status(dd, 0, FAKE, n, None) == (0, 0)      # an empty prompt ran nothing
+    assert pa.path_decode_prefill_status(dd, 101, FAKE, n, None)[0] == 4
+    assert pa.path_decode_prefill_status(dd, 70, FAKE, n - 1, None)[0] == 3
+    assert pa.path_decode_prefill_status(dd, 70, None, n, None)[0] == 1
+    d32c = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_FP32, 1.0)          # fp32 caches: SIMT preparation
+    assert pa.path_decode_prefill_status(d32c, 70, FAKE, pa.path_decode_prefill_workspace_size(d32c, 70),
+                                         None) == (0, 0)

@@ -111,6 +111,32 @@ def _transported_queries(q, w, beta):
     return Z
 
 
+def test_out_of_range_beta_is_clamped_to_the_parameterisation_range():
+    """beta = 2 sigmoid(x) lives in (0, 2) (notes §2.1); values outside are read as clamped to
+    [0, 2].  Logits and outputs at beta = -0.5 / 2.5 are the explicit products at beta = 0 / 2 (and
+    differ from the unclamped products), and every gradient, dbeta included, is the one at the
+    clamped value."""
+    rng = np.random.default_rng(31)
+    L, d = 10, 6
+    q, k, v, w, beta, _ = rand_problem(rng, L, d)
+    beta[[1, 4, 8]] = [-0.5, 2.5, 2.5]
+    clamped = np.clip(beta, 0.0, 2.0)
+    assert clamped[1] == 0.0 and clamped[4] == 2.0
+    S = orc.logits(q, k, w, beta, None, 1.0)
+    np.testing.assert_allclose(S, explicit_logits(q, k, w, clamped, None, 1.0), rtol=0, atol=1e-12)
+    low = np.tril_indices(L)
+    assert np.abs(S[low] - explicit_logits(q, k, w, beta, None, 1.0)[low]).max() > 1e-3
+    o, lse = orc.fwd(q[None], k[None], v[None], w[None], beta[None], None, 1.0)
+    o_ref, lse_ref = softmax_attend(explicit_logits(q, k, w, clamped, None, 1.0), v)
+    np.testing.assert_allclose(o[0], o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0], lse_ref, rtol=0, atol=1e-12)
+    dO = rng.standard_normal((L, d))
+    g_out = orc.bwd(q[None], k[None], v[None], w[None], beta[None], None, 1.0, dO[None])
+    g_in = orc.bwd(q[None], k[None], v[None], w[None], clamped[None], None, 1.0, dO[None])
+    for key in ("dq", "dk", "dv", "dw", "dbeta"):
+        np.testing.assert_allclose(g_out[key], g_in[key], rtol=0, atol=1e-12, err_msg=key)
+
+
 def test_beta_two_preserves_norm_and_smaller_beta_contracts():
     rng = np.random.default_rng(5)
     L, d = 10, 6
