@@ -54,9 +54,10 @@ UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule 
 # whenever the kernel changes.
 BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (425917440 + 80140288) / 16
 # DRAM bytes per head of one decode step at t = 32768 (split + combine kernels): ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum) of a batch-4 x 32-head step divided by 128 heads.
-# None until captured.
-DECODE_DRAM_BYTES_PER_HEAD_T32768 = None
+# (dram__bytes_read.sum + dram__bytes_write.sum) of a batch-4 x 32-head step divided by 128 heads
+# (the step's traffic grows in proportion to the heads it processes).  To be retaken whenever the
+# kernel changes.
+DECODE_DRAM_BYTES_PER_HEAD_T32768 = (1074203392 + 494862592 + 1309440) / 128
 
 
 def tiles_steps(L):
