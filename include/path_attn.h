@@ -288,6 +288,77 @@ int path_attn_workspace_status(const path_attn_desc_t* desc, int for_backward, c
 int path_decode_prefill_status(const path_decode_desc_t* desc, int prompt_len, const void* ws, size_t ws_bytes,
                                int* code, void* stream);
 
+/*
+ * Context parallelism (sequence sharding) of the forward pass.  The reading notes §2.8, last
+ * paragraph (the paper's Sec. 3.5), sketch it: pass the transported keys and values and the block
+ * transforms between devices and accumulate right to left.  The sequence of L tokens is cut into
+ * consecutive shards, one per device, each a multiple of 128 tokens.  For a query i of shard r and
+ * a key j of an earlier shard r':
+ *   logit(i, j) = scale * k~_j^T (M_{r'+1} ... M_{r-1}) z^_i + a_i + b_j
+ * with k~_j = H_{e(r')} ... H_{j+1} k_j (the key moved to the end of its shard), z^_i =
+ * H_{s(r)} ... H_i q_i (the query moved to the start of its shard), M_s = H_{s(s)} ... H_{e(s)}
+ * (the product over shard s) and, with a forget gate, a_i = sum_{t=s(r)..i} log f_t and
+ * b_j = sum_{t=j+1..e(r')} log f_t plus the totals of the shards in between.  Each device then:
+ *   1. runs path_attn_fwd_phases(PATH_FWD_PREPARE) on its shard (fwd_ws) and
+ *      path_cp_shard_prepare (its keys moved to its end, its queries moved to its start, M^T, and
+ *      the forget-gate terms);
+ *   2. for every earlier shard, receives that shard's key block (already moved to the end of the
+ *      previous shard), its values and key biases, merges them into its queries' softmax state
+ *      with path_cp_attend_block, moves the block through its own shard with path_cp_pass_block
+ *      and sends it on to the next device;
+ *   3. runs path_attn_fwd_phases(PATH_FWD_SCAN): o and lse over the whole prefix.
+ * The order in which blocks are merged does not change the result (up to rounding).  Scope: bf16
+ * at head dim 64 (the tensor-core path), seqlen and block_len multiples of 128, forward only (the
+ * backward is not sharded).  desc is always the local shard's descriptor (seqlen = its length).
+ */
+
+/* Bytes of workspace path_cp_shard_prepare needs; 0 if desc is invalid or outside the scope. */
+size_t path_cp_prepare_workspace_size(const path_attn_desc_t* desc);
+
+/*
+ * Per-shard transports.  Inputs q, k, w ([batch][heads][seqlen][64] bf16), beta (fp32), log_f
+ * (fp32 or NULL).  Outputs (caller-owned device memory):
+ *   k_end   [batch][heads][seqlen][64] fp32: row j = k~_j, the key moved to the shard's end;
+ *   q_start [batch][heads][seqlen][64] bf16: row i = z^_i, the query moved to the shard's start;
+ *   t_shard [batch][heads][64][64] fp32: M^T, the transpose of the shard's product (row-major);
+ *   with log_f (all three or none): a_q [batch][heads][seqlen] = inclusive prefix sums of log f,
+ *   b_k = total - a_q, f_tot [batch][heads] = the total.
+ * Computed from the UT preparation (split-precision fp32 chunk transforms, as the prefill hand-off)
+ * by two fp32 walks over the chunks.  ws: path_cp_prepare_workspace_size bytes, 256-byte aligned,
+ * contents unspecified on exit (a bounded wait of its preparation that gives up is recorded there
+ * but not reported by a status call).
+ * Errors: PATH_ERR_UNSUPPORTED outside the scope above; argument errors as elsewhere.
+ */
+int path_cp_shard_prepare(const path_attn_desc_t* desc, const void* q, const void* k, const void* w,
+                          const float* beta, const float* log_f, float* k_end, void* q_start, float* t_shard,
+                          float* a_q, float* b_k, float* f_tot, void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of block scratch path_cp_attend_block needs for blocks of block_len keys; 0 if invalid. */
+size_t path_cp_block_workspace_size(const path_attn_desc_t* desc, int block_len);
+
+/*
+ * Merges one earlier shard's key block into the softmax state that the forward's PREPARE phase left
+ * in fwd_ws (path_attn_workspace_size(desc, 0 or 1) bytes, the same workspace the later SCAN phase
+ * uses): for every local query i (row of q_start) and every block key j,
+ *   s_ij = scale * k_block_j . q_start_i (+ a_q_i + b_k_j),
+ * added to the query's running maximum, sum and weighted values with v_block_j.  k_block
+ * [batch][heads][block_len][64] fp32 (rounded to bf16 for the tensor-core product), v_block the
+ * same shape in bf16, a_q [..][seqlen] and b_k [..][block_len] fp32 or both NULL.  blk_ws:
+ * path_cp_block_workspace_size bytes, 256-byte aligned.  Runs the forward scan kernel in its block
+ * mode (tcgen05); its bounded waits report through path_attn_workspace_status on fwd_ws.
+ */
+int path_cp_attend_block(const path_attn_desc_t* desc, int block_len, const void* q_start, const float* k_block,
+                         const void* v_block, const float* a_q, const float* b_k, void* fwd_ws, size_t fwd_ws_bytes,
+                         void* blk_ws, size_t blk_ws_bytes, void* stream);
+
+/*
+ * Moves a key block through the local shard, in place: rows k_block <- k_block M (k_block
+ * [batch][heads][block_len][64] fp32, t_shard = M^T from path_cp_shard_prepare), and with a forget
+ * gate b_k += f_tot (b_k [batch][heads][block_len], f_tot [batch][heads]; both or neither).
+ */
+int path_cp_pass_block(const path_attn_desc_t* desc, int block_len, float* k_block, float* b_k,
+                       const float* t_shard, const float* f_tot, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -63,10 +63,12 @@ struct __align__(1024) ScanSmem {
 
 struct ScanParams {
   int L, Lp, nc, BH, ntiles;
+  int Lk;     // rows per head of the K-> (and, in block mode, V) tensor: Lp, or the block's length
+  int nkc;    // block mode: key chunks of the block
   float scl;  // scale * log2(e)
-  const float* dm;
-  const float* dl;
-  const float* dacc;
+  float* dm;  // diagonal-chunk softmax state (read; block mode also writes it back)
+  float* dl;
+  float* dacc;
   const float* fa;
   const float* fr;
   const float* ft;
@@ -113,7 +115,11 @@ __device__ __forceinline__ bool softmax_any(bool q) {
 }
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <bool FOX>
+// BLOCK (context-parallel block mode): every query tile visits every 64-row chunk of a separate
+// key block (K-> = the block's keys, F = one identity tile, V = the block's values; FoX: fa holds
+// the queries' bias, fr the keys'), starting from and writing back the softmax state in dm, dl,
+// dacc (unnormalised), instead of the causal chunk range and the o / lse epilogue.
+template <bool FOX, bool BLOCK>
 __global__ void __launch_bounds__(NTHREADS, 2)
     fwd_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_ql, const __grid_constant__ CUtensorMap tm_kr,
                        const __grid_constant__ CUtensorMap tm_f, const __grid_constant__ CUtensorMap tm_v,
@@ -122,9 +128,15 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   ScanSmem& s = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bh, T;
-  tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
-  const bool has_partial = (2 * T + 1) * BK < p.L;
-  const int nsteps = (has_partial ? 1 : 0) + 2 * T;
+  if constexpr (BLOCK) {
+    bh = (int)blockIdx.x / p.ntiles;
+    T = (int)blockIdx.x % p.ntiles;
+  } else {
+    tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
+  }
+  const bool has_partial = !BLOCK && (2 * T + 1) * BK < p.L;
+  const int nsteps = BLOCK ? p.nkc : (has_partial ? 1 : 0) + 2 * T;
+  auto step_chunk = [&](int n) { return BLOCK ? p.nkc - 1 - n : (has_partial ? 2 * T - n : 2 * T - 1 - n); };
 
   if (tid == 0) {
     for (int k = 0; k < NSTAGE; ++k) {
@@ -159,12 +171,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       for (int n = 0; n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (n >= NSTAGE && !mbar_wait(&s.empty[st], ((n / NSTAGE) - 1) & 1, p.err, 1)) break;
-        const int c = has_partial ? 2 * T - n : 2 * T - 1 - n;
+        const int c = step_chunk(n);
         mbar_arrive_expect_tx(&s.full[st], 128 * 128 + BK * 128 + (FOX ? BK * 4 : 0));
-        tma_load_2d(s.kf[st], &tm_kr, 0, bh * p.Lp + c * BK, &s.full[st]);
-        tma_load_2d(s.kf[st] + 64 * 128, &tm_f, 0, (bh * p.nc + c) * D, &s.full[st]);
-        tma_load_2d(s.v[st], &tm_v, 0, bh * p.L + c * BK, &s.full[st]);
-        if constexpr (FOX) bulk_load(s.frs[st], p.fr + (size_t)bh * p.Lp + (size_t)c * BK, BK * 4, &s.full[st]);
+        tma_load_2d(s.kf[st], &tm_kr, 0, bh * p.Lk + c * BK, &s.full[st]);
+        tma_load_2d(s.kf[st] + 64 * 128, &tm_f, 0, BLOCK ? 0 : (bh * p.nc + c) * D, &s.full[st]);
+        tma_load_2d(s.v[st], &tm_v, 0, bh * (BLOCK ? p.Lk : p.L) + c * BK, &s.full[st]);
+        if constexpr (FOX) bulk_load(s.frs[st], p.fr + (size_t)bh * p.Lk + (size_t)c * BK, BK * 4, &s.full[st]);
       }
     }
   } else if (warp == 9) {
@@ -262,7 +274,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     for (int n = 0; n < nsteps; ++n) {
       ok = ok && mbar_wait(&s.s_full, n & 1, p.err, 6);
       tc_fence_after();
-      const int c = has_partial ? 2 * T - n : 2 * T - 1 - n;
+      const int c = step_chunk(n);
       const bool active = !(has_partial && n == 0 && r < 64);
       // transport first: Z <- bf16(Z F_c^T) into TMEM, so that the next MMAs can start
       if (n + 1 < nsteps && active) {
@@ -389,7 +401,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         f2_split(acc[0], s0, s1);
         f2_split(acc[1], s2, s3);
         l += (s0 + s1) + (s2 + s3);
-        if (FOX) R += p.ft[(size_t)bh * p.nc + c];
+        if (FOX && !BLOCK) R += p.ft[(size_t)bh * p.nc + c];
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = 0u;
@@ -409,26 +421,42 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     s.xm[h][r] = l;
     softmax_sync();
     const float lt = s.xm[0][r] + s.xm[1][r];
-    const float inv = 1.f / lt;
-    if (nsteps > 0) {
-      tmem_ld32(c_o, x);
-      tmem_ld_wait();
-    } else {
+    if constexpr (BLOCK) {  // the merged state goes back where it came from (rows padded to Lp)
+      if (nsteps > 0) {
+        tmem_ld32(c_o, x);
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(p.dacc + wrow * D + 32 * h);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
-    }
-    if (grow < p.L) {
-      uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.L + grow) * D + 32 * h);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 pk;
-        pk.x = pack_bf16(__uint_as_float(x[8 * q]) * inv, __uint_as_float(x[8 * q + 1]) * inv);
-        pk.y = pack_bf16(__uint_as_float(x[8 * q + 2]) * inv, __uint_as_float(x[8 * q + 3]) * inv);
-        pk.z = pack_bf16(__uint_as_float(x[8 * q + 4]) * inv, __uint_as_float(x[8 * q + 5]) * inv);
-        pk.w = pack_bf16(__uint_as_float(x[8 * q + 6]) * inv, __uint_as_float(x[8 * q + 7]) * inv);
-        dst[q] = pk;
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(x[4 * q]), __uint_as_float(x[4 * q + 1]),
+                               __uint_as_float(x[4 * q + 2]), __uint_as_float(x[4 * q + 3]));
+        if (h == 0) {
+          p.dm[wrow] = m;
+          p.dl[wrow] = lt;
+        }
       }
-      if (h == 0) p.lse[(size_t)bh * p.L + grow] = (m + log2f(lt)) * kLn2;
+    } else {
+      const float inv = 1.f / lt;
+      if (nsteps > 0) {
+        tmem_ld32(c_o, x);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(p.dacc[wrow * D + h * 32 + j]);
+      }
+      if (grow < p.L) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * p.L + grow) * D + 32 * h);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 pk;
+          pk.x = pack_bf16(__uint_as_float(x[8 * q]) * inv, __uint_as_float(x[8 * q + 1]) * inv);
+          pk.y = pack_bf16(__uint_as_float(x[8 * q + 2]) * inv, __uint_as_float(x[8 * q + 3]) * inv);
+          pk.z = pack_bf16(__uint_as_float(x[8 * q + 4]) * inv, __uint_as_float(x[8 * q + 5]) * inv);
+          pk.w = pack_bf16(__uint_as_float(x[8 * q + 6]) * inv, __uint_as_float(x[8 * q + 7]) * inv);
+          dst[q] = pk;
+        }
+        if (h == 0) p.lse[(size_t)bh * p.L + grow] = (m + log2f(lt)) * kLn2;
+      }
     }
   }
   tc_fence_before();
@@ -510,10 +538,12 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   p.nc = g.nc;
   p.BH = g.BH;
   p.ntiles = g.nc / 2;
+  p.Lk = g.Lp;
+  p.nkc = 0;
   p.scl = g.scale * kLog2e;
-  p.dm = (const float*)(ws + lay.dm);
-  p.dl = (const float*)(ws + lay.dl);
-  p.dacc = (const float*)(ws + lay.dacc);
+  p.dm = (float*)(ws + lay.dm);
+  p.dl = (float*)(ws + lay.dl);
+  p.dacc = (float*)(ws + lay.dacc);
   p.fa = (const float*)(ws + lay.fa);
   p.fr = (const float*)(ws + lay.fr);
   p.ft = (const float*)(ws + lay.ft);
@@ -522,11 +552,42 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   p.zs = (uint8_t*)zstore;
   p.err = (int*)(ws + lay.err);
   const size_t smem = sizeof(ScanSmem) + 1024;
-  auto kern = logf ? fwd_scan_tc_kernel<true> : fwd_scan_tc_kernel<false>;
+  auto kern = logf ? fwd_scan_tc_kernel<true, false> : fwd_scan_tc_kernel<false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long ntiles = (long)p.ntiles * g.BH;
   kern<<<(unsigned)ntiles, NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void* kb, const void* vb, const void* ident,
+                              const float* aq, const float* bk, char* ws, const FwdWs& lay, cudaStream_t st) {
+  if (g.B != BK || g.Lp != g.L || (g.L % BQ) || Lb <= 0 || (Lb % BK) || ((aq == nullptr) != (bk == nullptr)))
+    return cudaErrorInvalidValue;
+  CUtensorMap m_ql, m_kr, m_f, m_v;
+  if (!make_map_rows64(&m_ql, zq, (uint64_t)g.BH * g.Lp, BQ) || !make_map_rows64(&m_kr, kb, (uint64_t)g.BH * Lb, BK) ||
+      !make_map_rows64(&m_f, ident, D, D) || !make_map_rows64(&m_v, vb, (uint64_t)g.BH * Lb, BK))
+    return cudaErrorInvalidValue;
+  ScanParams p{};
+  p.L = g.L;
+  p.Lp = g.Lp;
+  p.nc = g.nc;
+  p.BH = g.BH;
+  p.ntiles = g.Lp / BQ;
+  p.Lk = Lb;
+  p.nkc = Lb / BK;
+  p.scl = g.scale * kLog2e;
+  p.dm = (float*)(ws + lay.dm);
+  p.dl = (float*)(ws + lay.dl);
+  p.dacc = (float*)(ws + lay.dacc);
+  p.fa = aq;
+  p.fr = bk;
+  p.err = (int*)(ws + lay.err);
+  const size_t smem = sizeof(ScanSmem) + 1024;
+  auto kern = aq ? fwd_scan_tc_kernel<true, true> : fwd_scan_tc_kernel<false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)((long)p.ntiles * g.BH), NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
   return cudaGetLastError();
 }
 

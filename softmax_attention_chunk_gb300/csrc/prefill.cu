@@ -18,6 +18,7 @@
 // to left, keeping S (d x d) in shared memory, in fp32: per chunk CB d^2 + d^3 multiply-adds.
 #include "internal.h"
 #include "dev_common.cuh"
+#include "walk_common.cuh"
 
 #include <type_traits>
 
@@ -30,34 +31,6 @@ constexpr int PT = 256;      // threads: each owns one or more 4 x 4 blocks of a
 // S_c, then K->_c or F_c, then S_c F_c^T before it replaces S.
 template <int D>
 constexpr size_t prefill_smem_bytes() { return (size_t)3 * D * (D + 1) * sizeof(float); }
-
-// Asynchronous copy of `bytes` (a multiple of 16, 16-byte aligned) from global memory into L2.
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
-}
-
-// out[r][n] = sum_m A[r][m] * B[n][m] for one 4 x 4 block (A B^T), both operands with row stride
-// LD and D columns.
-template <int D, int LD>
-__device__ __forceinline__ void mm_abt(const float* A, const float* Bm, int r0, int n0, float (&acc)[4][4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 4
-  for (int m = 0; m < D; ++m) {
-    float a[4], b[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = A[(r0 + i) * LD + m];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) b[j] = Bm[(n0 + j) * LD + m];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-  }
-}
 
 template <typename T, typename KR, int D, int CB>
 __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, int nc, int cap,

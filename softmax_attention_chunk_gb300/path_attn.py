@@ -71,6 +71,16 @@ _lib.path_attn_workspace_status.restype = _i
 _lib.path_attn_workspace_status.argtypes = [_DP, _i, _vp, _sz, ctypes.POINTER(_i), _vp]
 _lib.path_decode_prefill_status.restype = _i
 _lib.path_decode_prefill_status.argtypes = [_DDP, _i, _vp, _sz, ctypes.POINTER(_i), _vp]
+_lib.path_cp_prepare_workspace_size.restype = _sz
+_lib.path_cp_prepare_workspace_size.argtypes = [_DP]
+_lib.path_cp_shard_prepare.restype = _i
+_lib.path_cp_shard_prepare.argtypes = [_DP] + [_vp] * 11 + [_vp, _sz, _vp]
+_lib.path_cp_block_workspace_size.restype = _sz
+_lib.path_cp_block_workspace_size.argtypes = [_DP, _i]
+_lib.path_cp_attend_block.restype = _i
+_lib.path_cp_attend_block.argtypes = [_DP, _i] + [_vp] * 5 + [_vp, _sz, _vp, _sz, _vp]
+_lib.path_cp_pass_block.restype = _i
+_lib.path_cp_pass_block.argtypes = [_DP, _i] + [_vp] * 4 + [_vp]
 PATH_DECODE_NOALLOC_MAX_HEADS = 496
 PATH_ERR_INTERNAL = 6
 
@@ -84,7 +94,8 @@ EXPORTED = ("path_status_string", "path_attn_chunk", "path_attn_workspace_size",
             "path_attn_bwd", "path_attn_fwd_phases", "path_attn_bwd_phases", "path_decode_workspace_size",
             "path_decode_step", "path_decode_step_noalloc", "path_decode_prefill_workspace_size",
             "path_decode_prefill", "path_decode_step_fox", "path_attn_workspace_status",
-            "path_decode_prefill_status")
+            "path_decode_prefill_status", "path_cp_prepare_workspace_size", "path_cp_shard_prepare",
+            "path_cp_block_workspace_size", "path_cp_attend_block", "path_cp_pass_block")
 
 
 # ---------------- raw entry points (same names as the C ABI) ----------------
@@ -167,6 +178,30 @@ def path_decode_prefill_status(desc, prompt_len, ws, ws_bytes, stream):
     rc = _lib.path_decode_prefill_status(ctypes.byref(desc), int(prompt_len), ws, ws_bytes, ctypes.byref(code),
                                          stream)
     return rc, code.value
+
+
+def path_cp_prepare_workspace_size(desc) -> int:
+    return _lib.path_cp_prepare_workspace_size(ctypes.byref(desc))
+
+
+def path_cp_shard_prepare(desc, q, k, w, beta, log_f, k_end, q_start, t_shard, a_q, b_k, f_tot, ws, ws_bytes,
+                          stream) -> int:
+    return _lib.path_cp_shard_prepare(ctypes.byref(desc), q, k, w, beta, log_f, k_end, q_start, t_shard, a_q, b_k,
+                                      f_tot, ws, ws_bytes, stream)
+
+
+def path_cp_block_workspace_size(desc, block_len) -> int:
+    return _lib.path_cp_block_workspace_size(ctypes.byref(desc), int(block_len))
+
+
+def path_cp_attend_block(desc, block_len, q_start, k_block, v_block, a_q, b_k, fwd_ws, fwd_ws_bytes, blk_ws,
+                         blk_ws_bytes, stream) -> int:
+    return _lib.path_cp_attend_block(ctypes.byref(desc), int(block_len), q_start, k_block, v_block, a_q, b_k, fwd_ws,
+                                     fwd_ws_bytes, blk_ws, blk_ws_bytes, stream)
+
+
+def path_cp_pass_block(desc, block_len, k_block, b_k, t_shard, f_tot, stream) -> int:
+    return _lib.path_cp_pass_block(ctypes.byref(desc), int(block_len), k_block, b_k, t_shard, f_tot, stream)
 
 
 # ---------------- torch-tensor wrappers ----------------

@@ -259,3 +259,38 @@ def test_workspace_status_argument_errors(pa):
     d32c = pa.path_decode_desc_t(2, 2, 64, 100, pa.PATH_FP32, 1.0)          # fp32 caches: SIMT preparation
     assert pa.path_decode_prefill_status(d32c, 70, FAKE, pa.path_decode_prefill_workspace_size(d32c, 70),
                                          None) == (0, 0)
+
+
+def test_context_parallel_argument_errors(pa):
+    """The context-parallel calls check scope and arguments before any CUDA call."""
+    d = desc(pa, dtype=pa.PATH_BF16, seqlen=256)
+    assert pa.path_cp_prepare_workspace_size(desc(pa, dtype=pa.PATH_FP32, seqlen=256)) == 0   # bf16 only
+    assert pa.path_cp_prepare_workspace_size(desc(pa, dtype=pa.PATH_BF16, seqlen=200)) == 0   # not a 128 multiple
+    n = pa.path_cp_prepare_workspace_size(d)
+    assert n > 0
+    F = [FAKE] * 7
+    assert pa.path_cp_shard_prepare(desc(pa, dtype=pa.PATH_FP32, seqlen=256), *F[:4], None, *F[4:], None, None,
+                                    None, FAKE, n, None) == 2
+    assert pa.path_cp_shard_prepare(desc(pa, dtype=pa.PATH_BF16, seqlen=200), *F[:4], None, *F[4:], None, None,
+                                    None, FAKE, n, None) == 2
+    assert pa.path_cp_shard_prepare(desc(pa, dtype=pa.PATH_BF16, seqlen=256, head_dim=128), *F[:4], None, *F[4:],
+                                    None, None, None, FAKE, n, None) == 2
+    assert pa.path_cp_shard_prepare(d, None, *F[1:4], None, *F[4:], None, None, None, FAKE, n, None) == 1
+    assert pa.path_cp_shard_prepare(d, *F[:4], FAKE, *F[4:], None, None, None, FAKE, n, None) == 1  # log_f alone
+    assert pa.path_cp_shard_prepare(d, *F[:4], None, *F[4:], FAKE, None, None, FAKE, n, None) == 1  # a_q alone
+    assert pa.path_cp_shard_prepare(d, *F[:4], None, *F[4:], None, None, None, FAKE, n - 1, None) == 3
+    assert pa.path_cp_shard_prepare(d, *F[:4], None, *F[4:], None, None, None, FAKE + 16, n, None) == 1
+    assert pa.path_cp_block_workspace_size(d, 100) == 0
+    nb = pa.path_cp_block_workspace_size(d, 384)
+    nf = pa.path_attn_workspace_size(d, 0)
+    assert nb > 0
+    att = lambda bl, a, b, fw, bw: pa.path_cp_attend_block(d, bl, FAKE, FAKE, FAKE, a, b, FAKE, fw, FAKE, bw, None)
+    assert att(100, None, None, nf, nb) == 2
+    assert att(0, None, None, nf, nb) == 1
+    assert att(384, FAKE, None, nf, nb) == 1
+    assert att(384, None, None, nf - 1, nb) == 3
+    assert att(384, None, None, nf, nb - 1) == 3
+    assert pa.path_cp_pass_block(d, 0, FAKE, None, FAKE, None, None) == 1
+    assert pa.path_cp_pass_block(d, 100, FAKE, None, FAKE, None, None) == 2
+    assert pa.path_cp_pass_block(d, 384, FAKE, FAKE, FAKE, None, None) == 1   # b_k without f_tot
+    assert pa.path_cp_pass_block(d, 384, None, None, FAKE, None, None) == 1
