@@ -362,14 +362,12 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         mbar_arrive_expect_tx(&s.vfull[vi], BK * 128);
         tma_load_2d(s.v[vi], &tm_v, 0, bh * p.L + c * BK, &s.vfull[vi]);
       }
-    } else if (lane == 16) {  // Z_n: read once, so it should not push the chunk operands and the
-                              // accumulators that other tiles reuse out of L2
-      const uint64_t pol = l2_evict_first();
+    } else if (lane == 16) {  // Z_n
       for (int k = 0; k < nsteps; ++k) {
         const int zi = k % BS_ZSTAGE;
         if (k >= BS_ZSTAGE && !mbar_wait(&s.zempty[zi], ((k / BS_ZSTAGE) - 1) & 1, p.err, 20)) break;
         mbar_arrive_expect_tx(&s.zfull[zi], ZTILE);
-        bulk_load_hint(s.z[zi], zbase + (size_t)(nsteps - 1 - k) * ZTILE, ZTILE, &s.zfull[zi], pol);
+        bulk_load(s.z[zi], zbase + (size_t)(nsteps - 1 - k) * ZTILE, ZTILE, &s.zfull[zi]);
       }
     }
   } else if (warp == 5) {

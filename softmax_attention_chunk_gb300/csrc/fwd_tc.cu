@@ -203,16 +203,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       // Z store of this tile: tile n of the tile's sequence at n * 16 KB (the tiles of earlier query
       // tiles of the head come first: sum_{t<T} (2t+1) = T^2)
       uint8_t* zstore = p.zs ? p.zs + ((size_t)bh * p.ntiles * p.ntiles + (size_t)T * T) * (BQ * 128) : nullptr;
-      // the Z store is read again only by the backward: it should not push the chunk operands that
-      // other tiles of the head group reuse out of L2
-      const uint64_t zpol = l2_evict_first();
       for (int n = 0; ok && n < nsteps; ++n) {
         const int st = n % NSTAGE;
         if (!mbar_wait(&s.full[st], (n / NSTAGE) & 1, p.err, 3)) { ok = false; break; }
         if (!mbar_wait(&s.z_ready, n & 1, p.err, 4)) { ok = false; break; }
         tc_fence_after();
         if (zstore) {  // Z_n from image buffer n % 2 (Z_0 is the Q<- tile itself)
-          bulk_store_hint(zstore + (size_t)n * (BQ * 128), (n & 1) ? s.zout : s.z0, BQ * 128, zpol);
+          bulk_store(zstore + (size_t)n * (BQ * 128), (n & 1) ? s.zout : s.z0, BQ * 128);
           bulk_commit();
         }
         const uint64_t d0 = dkf0 + (uint64_t)(1024 * st);
