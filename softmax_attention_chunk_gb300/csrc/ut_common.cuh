@@ -181,16 +181,18 @@ __device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, u
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * b + rr;
-        float a = acc[rr];
+        // four independent partial sums (one per float4 lane) keep the dependent chain of row r
+        // at about r / 4 FMAs
+        float a0 = acc[rr], a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int m = 16 * b; m < r; m += 4) {
           const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
-          a = fmaf(lv.x, y[m], a);
-          if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
-          if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
-          if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
+          a0 = fmaf(lv.x, y[m], a0);
+          if (m + 1 < r) a1 = fmaf(lv.y, y[m + 1], a1);
+          if (m + 2 < r) a2 = fmaf(lv.z, y[m + 2], a2);
+          if (m + 3 < r) a3 = fmaf(lv.w, y[m + 3], a3);
         }
-        y[r] = (lane == r ? 1.f : 0.f) - a;
+        y[r] = (lane == r ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
       }
     }
   }
@@ -251,6 +253,150 @@ __device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, u
     for (int j = 0; j < 4; ++j) put_u(32 + 2 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
 }
 
+// The same block inversion writing U transposed: U^T (and U_lo^T) as swizzled bf16 tiles, so that
+// a thread, which holds one column of a diagonal block of U, writes it as one contiguous tile row
+// (four 16-byte stores instead of 32 scalar ones); Y is kept transposed in sl the same way (row j
+// of the block = column j of Y, eight 16-byte stores), and the off-diagonal block comes from
+//   T = L_bt Y_tt:  T[i][j] = sum_m L[32+i][m] Yt[j][m]   (rows of L times rows of Yt)
+//   Y_bt = -Y_bb T: Y_bt[i][j] = -sum_m Yt_bb[m][i] T[m][j]   (T kept in the unused upper-right block)
+// written to U^T rows j, columns 32 + i as bf16 pairs.  The MMAs read U^T with the opposite
+// operand major-ness.  Same arguments and phases as ut_solve_blocked.
+template <bool LO>
+__device__ __forceinline__ void ut_solve_blocked_t(float* sl, const float* beta, uint8_t* ut, uint8_t* ut_lo,
+                                                   int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  // ---- phase 1: diagonal 32 x 32 blocks (as ut_solve_blocked) ----
+  float y[32];
+  if (warp < 2) {
+    const float* sh = sl + 65 * 32 * warp;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float acc[16];
+      if (b == 1) {
+        uint64_t s2[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+          const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) {
+            const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sh + f32_idx(16 + rr, m));
+            s2[rr] = f2_fma(lv.x, y01, s2[rr]);
+            s2[rr] = f2_fma(lv.y, y23, s2[rr]);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          float lo, hi;
+          f2_split(s2[rr], lo, hi);
+          acc[rr] = lo + hi;
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * b + rr;
+        float a0 = acc[rr], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int m = 16 * b; m < r; m += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
+          a0 = fmaf(lv.x, y[m], a0);
+          if (m + 1 < r) a1 = fmaf(lv.y, y[m + 1], a1);
+          if (m + 2 < r) a2 = fmaf(lv.z, y[m + 2], a2);
+          if (m + 3 < r) a3 = fmaf(lv.w, y[m + 3], a3);
+        }
+        y[r] = (lane == r ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
+      }
+    }
+  }
+  ut_sync();  // every read of L_tt / L_bb is done
+  if (warp < 2) {
+    const int o = 32 * warp, col = o + lane;
+    const float bc = beta[col];
+    // Yt row col (the column of Y), columns o .. o+31
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(sl + f32_idx(col, o + 4 * q)) = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+    float uv[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) uv[r] = y[r] * bc;
+    put_half(ut, col, warp, uv);  // U^T row col, columns o .. o+31
+    if constexpr (LO) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) uv[r] -= __bfloat162float(__float2bfloat16_rn(uv[r]));
+      put_half(ut_lo, col, warp, uv);
+    }
+    if (warp == 1) {  // U^T rows 32-63, columns 0-31 (the zero upper-right block of U)
+#pragma unroll
+      for (int r = 0; r < 32; ++r) uv[r] = 0.f;
+      put_half(ut, col, 0, uv);
+      if constexpr (LO) put_half(ut_lo, col, 0, uv);
+    }
+  }
+  ut_sync();
+  // ---- phase 2: rows 2 rg, 2 rg + 1 and columns 4 cg .. 4 cg + 3 of a 32 x 32 product ----
+  const int rg = tid >> 3, cg = tid & 7;
+  float acc[2][4];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
+  // T = L_bt Y_tt: rows 32 + 2 rg + e of L against rows cg + 8 j of Yt_tt (the eight rows a warp
+  // reads in one load sit on eight different swizzle positions)
+#pragma unroll
+  for (int m = 0; m < 32; m += 4) {
+    const float4 a0 = *reinterpret_cast<const float4*>(sl + f32_idx(32 + 2 * rg, m));
+    const float4 a1 = *reinterpret_cast<const float4*>(sl + f32_idx(32 + 2 * rg + 1, m));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(cg + 8 * j, m));
+      acc[0][j] = fmaf(a0.x, bv.x, fmaf(a0.y, bv.y, fmaf(a0.z, bv.z, fmaf(a0.w, bv.w, acc[0][j]))));
+      acc[1][j] = fmaf(a1.x, bv.x, fmaf(a1.y, bv.y, fmaf(a1.z, bv.z, fmaf(a1.w, bv.w, acc[1][j]))));
+    }
+  }
+  // T into the unused upper-right block of sl (rows 0-31, columns 32-63)
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sl[f32_idx(2 * rg + e, 32 + cg + 8 * j)] = acc[e][j];
+  ut_sync();
+  // Y_bt = -Y_bb T: Yt_bb rows m (columns 32 + 2 rg, + 1) times T rows m (columns 4 cg ..)
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
+#pragma unroll 8
+  for (int m = 0; m < 32; ++m) {
+    const float2 av = *reinterpret_cast<const float2*>(sl + f32_idx(32 + m, 32 + 2 * rg));
+    const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(m, 32 + 4 * cg));
+    acc[0][0] = fmaf(av.x, bv.x, acc[0][0]);
+    acc[0][1] = fmaf(av.x, bv.y, acc[0][1]);
+    acc[0][2] = fmaf(av.x, bv.z, acc[0][2]);
+    acc[0][3] = fmaf(av.x, bv.w, acc[0][3]);
+    acc[1][0] = fmaf(av.y, bv.x, acc[1][0]);
+    acc[1][1] = fmaf(av.y, bv.y, acc[1][1]);
+    acc[1][2] = fmaf(av.y, bv.z, acc[1][2]);
+    acc[1][3] = fmaf(av.y, bv.w, acc[1][3]);
+  }
+  // U[32 + i][j] = Y_bt[i][j] beta_j  ->  U^T row j, columns 32 + 2 rg, + 1 (a bf16 pair)
+  const float4 bq = *reinterpret_cast<const float4*>(beta + 4 * cg);
+  const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float u0 = -acc[0][j] * bv[j], u1 = -acc[1][j] * bv[j];
+    const int row = 4 * cg + j, colp = 32 + 2 * rg;
+    *reinterpret_cast<uint32_t*>(ut + sw128_offset(row, colp)) = pack_bf16(u0, u1);
+    if constexpr (LO) {
+      const float l0 = u0 - __bfloat162float(__float2bfloat16_rn(u0));
+      const float l1 = u1 - __bfloat162float(__float2bfloat16_rn(u1));
+      *reinterpret_cast<uint32_t*>(ut_lo + sw128_offset(row, colp)) = pack_bf16(l0, l1);
+    }
+  }
+}
+
 // The same block inversion on warps 0-1 alone (threads 0-63, named barrier 3), writing Y =
 // (I + L)^{-1} and U = Y diag(beta) as bf16 tiles yt and u; the off-diagonal block's two 32 x 32
 // products give each thread a 4 x 4 block.  For the UT backward, whose warps 2-3 convert the
@@ -296,16 +442,18 @@ __device__ __forceinline__ void ut_solve_blocked64(float* sl, const float* beta,
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * b + rr;
-        float a = acc[rr];
+        // four independent partial sums (one per float4 lane) keep the dependent chain of row r
+        // at about r / 4 FMAs
+        float a0 = acc[rr], a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int m = 16 * b; m < r; m += 4) {
           const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
-          a = fmaf(lv.x, y[m], a);
-          if (m + 1 < r) a = fmaf(lv.y, y[m + 1], a);
-          if (m + 2 < r) a = fmaf(lv.z, y[m + 2], a);
-          if (m + 3 < r) a = fmaf(lv.w, y[m + 3], a);
+          a0 = fmaf(lv.x, y[m], a0);
+          if (m + 1 < r) a1 = fmaf(lv.y, y[m + 1], a1);
+          if (m + 2 < r) a2 = fmaf(lv.z, y[m + 2], a2);
+          if (m + 3 < r) a3 = fmaf(lv.w, y[m + 3], a3);
         }
-        y[r] = (lane == r ? 1.f : 0.f) - a;
+        y[r] = (lane == r ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
       }
     }
   }

@@ -22,9 +22,11 @@
 // their tenants die:
 //   slot 0 W          P1 .. R4           slot 5 M1 (M1 epilogue .. R2), then Y (R2 .. R4)
 //   slot 1 K          P1 .. R3 epilogue  slot 6 N2 (P1 .. R1), then P (R2 .. R4) or Y_lo (fp32 F)
-//   slot 2 Q          P1 .. R3 epilogue  slot 7 U (P2 .. R2), then V (loaded once R2 has read U)
+//   slot 2 Q          P1 .. R3 epilogue  slot 7 U^T (P2 .. R2), then V (loaded once R2 has read it)
 //   slots 3-4 fp32 L (P1 .. P2), then A (slot 3) and X (slot 4) (R1 .. R3)
-//   slot 8 U_lo (fp32 F only)
+//   slot 8 U_lo^T (fp32 F only)
+// U is stored transposed (the block inversion writes each column it holds as a contiguous row), and
+// the products read it with the matching operand major-ness.
 // W and K are adjacent: the first round's two products share the stacked [W; K] tile as one N=128
 // B operand.  Rounds: P1 [G | N2]; M1 (its MMA runs during the substitution P2); R1 A, X;
 // R2 Y, S_d; R3 A W, X^T W; R4 W^T Y, P V.
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
   issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
 
   // ---- P2: U = (I + strictLower(D G))^{-1} D (fp32 F: U = U_hi + U_lo) ----
-  ut_solve_blocked<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);
+  ut_solve_blocked_t<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);  // U^T (and U_lo^T) tiles
   wait_mma(33);
   {
     float x[32];
@@ -213,8 +215,8 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
 
   // ---- R1: A = M1 U, X = U N2 ----
   issue([&] {
-    mma64(tb + 0, ta(S_M1), 0, ta(S_U), 1, 0);
-    mma64(tb + 64, ta(S_U), 0, ta(S_N2), 1, 0);
+    mma64(tb + 0, ta(S_M1), 0, ta(S_U), 0, 0);   // B = U read from U^T (K-major)
+    mma64(tb + 64, ta(S_U), 1, ta(S_N2), 1, 0);  // A = U read from U^T (MN-major)
   });
   wait_mma(34);
   {
@@ -228,8 +230,8 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
 
   // ---- R2: Y = U^T W (+ U_lo^T W for an fp32 F), S_d = Q K^T - M1 X; then V into U's slot ----
   issue([&] {
-    mma64(tb + 0, ta(S_U), 1, ta(S_W), 1, 0);
-    if constexpr (F32) mma64(tb + 0, ta(S_ULO), 1, ta(S_W), 1, 1);
+    mma64(tb + 0, ta(S_U), 0, ta(S_W), 1, 0);  // A = U^T (K-major)
+    if constexpr (F32) mma64(tb + 0, ta(S_ULO), 0, ta(S_W), 1, 1);
     if (diag) {
       mma64(tb + 64, ta(S_Q), 0, ta(S_K), 0, 0);
       mma64(tb + 64, ta(S_M1), 0, ta(S_X), 1, 1, /*neg_a=*/1);
