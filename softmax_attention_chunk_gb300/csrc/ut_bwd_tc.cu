@@ -241,46 +241,34 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   }
   publish();
 
-  // ---- P3: dP = dO V^T goes to the tensor core first (its accumulator is free).  Warps 0-1 form
-  //      Y = (I + strictLower(D G))^{-1} by two-level block inversion and write Y and U = Y D as
-  //      bf16 tiles; meanwhile warps 2-3
-  //      (thread = row) write dQ<- and dK-> (zero past L) and, once dP has read V, dF into V's
-  //      slot as bf16 operand tiles ----
+  // ---- P3: dP = dO V^T goes to the tensor core first (its accumulator is free).  Warps 0-1 solve
+  //      the diagonal blocks of Y = (I + strictLower(D G))^{-1} and write them (and U = Y D) as bf16
+  //      tiles while warps 2-3 write dQ<- and dK-> as bf16 operand tiles (coalesced loads) and dF into
+  //      V's slot once dP has read V; then all
+  //      four warps form the off-diagonal block ----
   if (tid == 64) {
     tc_fence_after();
     mma64(tb + C2, ta(S_DO), 0, ta(S_V), 0, 0);
     mma_commit(&s.bar_mma);
   }
-  if (warp < 2) ut_solve_blocked64(sg, s.beta, s.t[S_U], s.t[S_Y], tid);
-  if (warp >= 2) {
-    const int r = tid - 64;
-    const bool ok = row0 + r < p.L;
-    float x[32];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (ok) {
-        load_f32_half(p.dql + (ws_row + r) * D + 32 * hh, x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = 0.f;
-      }
-      put_half(s.t[S_DQ], r, hh, x);
-      if (ok) {
-        load_f32_half(p.dkr + (ws_row + r) * D + 32 * hh, x);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = 0.f;
-      }
-      put_half(s.t[S_DK], r, hh, x);
+  if (warp < 2) {
+    ut_inv_diag64(sg, s.beta, s.t[S_U], s.t[S_Y], tid);
+  } else {
+    {  // dQ<- and dK-> (prefetched into L2 at the start), zero past L
+      RowsToTile<2> t;
+      t.load(p.dql + ws_row * D, min(B, p.L - row0), warp - 2, lane);
+      t.store(s.t[S_DQ], warp - 2, lane);
+      t.load(p.dkr + ws_row * D, min(B, p.L - row0), warp - 2, lane);
+      t.store(s.t[S_DK], warp - 2, lane);
     }
-    float f0[32], f1[32];
-    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D, f0);
-    load_f32_half(p.df + (((size_t)bh * p.nc + c) * D + r) * D + 32, f1);
+    RowsToTile<2> f;
+    f.load(p.df + ((size_t)bh * p.nc + c) * D * D, B, warp - 2, lane);
     mbar_wait(&s.bar_mma, mph, p.err, 52);  // dP has read V
-    put_half(s.t[S_DF], r, 0, f0);
-    put_half(s.t[S_DF], r, 1, f1);
+    f.store(s.t[S_DF], warp - 2, lane);
   }
   mph ^= 1;
+  ut_sync();  // the diagonal blocks of Y are in sl
+  ut_inv_offdiag128(sg, s.beta, s.t[S_U], s.t[S_Y], tid);
   publish();
 
   // ---- P4: X = U N2, Y1 = U W ----

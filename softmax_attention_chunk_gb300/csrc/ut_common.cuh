@@ -99,6 +99,33 @@ __device__ __forceinline__ void ld_half(uint32_t tb, uint32_t lane_off, uint32_t
 // rows of a warp's 16-byte stores fall on different banks, 4-column groups stay contiguous.
 __device__ __forceinline__ int f32_idx(int r, int m) { return r * 64 + (m ^ ((r & 7) << 2)); }
 
+// Coalesced conversion of fp32 rows [64 columns] into a swizzled bf16 tile by the threads of
+// NW warps: warp w takes rows w * (64 / NW) ..; each warp-wide 16-byte load covers two whole rows
+// (lane l: row + l / 16, columns 4 (l % 16) .. + 3), all loads are issued before the first
+// store, and each thread stores its four values as one 8-byte piece of the tile row.  Rows >= nvalid
+// are stored as zero.  load() and store() are separate so that a caller can wait in between.
+template <int NW>
+struct RowsToTile {
+  static constexpr int kLoads = 32 / NW;  // loads per thread (two rows each)
+  float4 v[kLoads];
+  __device__ __forceinline__ void load(const float* src, int nvalid, int w, int lane) {
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+      const int r = w * (64 / NW) + 2 * k + (lane >> 4);
+      v[k] = r < nvalid ? reinterpret_cast<const float4*>(src + (size_t)r * 64)[lane & 15]
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __device__ __forceinline__ void store(uint8_t* tile, int w, int lane) const {
+#pragma unroll
+    for (int k = 0; k < kLoads; ++k) {
+      const int r = w * (64 / NW) + 2 * k + (lane >> 4), col = 4 * (lane & 15);
+      *reinterpret_cast<uint2*>(tile + sw128_offset(r, col)) =
+          make_uint2(pack_bf16(v[k].x, v[k].y), pack_bf16(v[k].z, v[k].w));
+    }
+  }
+};
+
 // 32 fp32 values as bf16 to global memory (64 bytes, 16-byte aligned).
 __device__ __forceinline__ void store_bf16_half(__nv_bfloat16* dst, const float* x) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -124,148 +151,29 @@ __device__ __forceinline__ void load_f32_half(const float* src, float* x) {
 // below synchronises through it).
 __device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// U = (I + L)^{-1} diag(beta) for one 64-row chunk, by two-level block inversion over the row
-// halves t (0-31) and b (32-63):
+// The block inversion of the UT transform: U = (I + L)^{-1} diag(beta) for one 64-row chunk, by
+// two-level block inversion over the row halves t (0-31) and b (32-63):
 //   (I + L)^{-1} = [[Y_tt, 0], [-Y_bb L_bt Y_tt, Y_bb]],  Y_tt = (I + L_tt)^{-1}, Y_bb = (I + L_bb)^{-1}.
-// Phase 1: warp 0 solves the columns of Y_tt, warp 1 those of Y_bb (one column per thread, 32
-// rows by forward substitution), written over L_tt / L_bb.  Phase 2: all 128 threads form
-// T = L_bt Y_tt (into the unused upper-right block of sl), then Y_bt = -Y_bb T, each thread a
-// 2 x 4 block.  sl: the fp32 L of the chunk (f32_idx layout over two tile slots, strictly
-// lower; overwritten); beta: the chunk's clamped beta; U is written as bf16 into the swizzled
-// tile u (LO: with u_lo, U = u + u_lo with both parts bf16).  Called by threads 0-127 together;
-// ends with the tiles written by generic stores (the caller fences them for the tensor core).
-// (The UT backward uses the 64-thread variant below: there warps 2-3 convert the gradient tiles
-// meanwhile, and a phase that needs all four warps lengthened its chain.)
-template <bool LO>
-__device__ __forceinline__ void ut_solve_blocked(float* sl, const float* beta, uint8_t* u, uint8_t* u_lo,
-                                                 int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  auto put_u = [&](int r, int col, float yv, float bc) {
-    const float val = yv * bc;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(val);
-    *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(r, col)) = hi;
-    if constexpr (LO)
-      *reinterpret_cast<__nv_bfloat16*>(u_lo + sw128_offset(r, col)) = __float2bfloat16_rn(val - __bfloat162float(hi));
-  };
-  // ---- phase 1: diagonal 32 x 32 blocks ----
-  float y[32];
-  if (warp < 2) {
-    const float* sh = sl + 65 * 32 * warp;  // block (32 warp, 32 warp): element (r, m) at sh[f32_idx(r, m)]
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      float acc[16];
-      if (b == 1) {
-        uint64_t s2[16];
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) s2[rr] = 0ull;
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-          const uint64_t y01 = f2(y[m], y[m + 1]), y23 = f2(y[m + 2], y[m + 3]);
-#pragma unroll
-          for (int rr = 0; rr < 16; ++rr) {
-            const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(sh + f32_idx(16 + rr, m));
-            s2[rr] = f2_fma(lv.x, y01, s2[rr]);
-            s2[rr] = f2_fma(lv.y, y23, s2[rr]);
-          }
-        }
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          float lo, hi;
-          f2_split(s2[rr], lo, hi);
-          acc[rr] = lo + hi;
-        }
-      } else {
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
-      }
-#pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const int r = 16 * b + rr;
-        // four independent partial sums (one per float4 lane) keep the dependent chain of row r
-        // at about r / 4 FMAs
-        float a0 = acc[rr], a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int m = 16 * b; m < r; m += 4) {
-          const float4 lv = *reinterpret_cast<const float4*>(sh + f32_idx(r, m));
-          a0 = fmaf(lv.x, y[m], a0);
-          if (m + 1 < r) a1 = fmaf(lv.y, y[m + 1], a1);
-          if (m + 2 < r) a2 = fmaf(lv.z, y[m + 2], a2);
-          if (m + 3 < r) a3 = fmaf(lv.w, y[m + 3], a3);
-        }
-        y[r] = (lane == r ? 1.f : 0.f) - ((a0 + a1) + (a2 + a3));
-      }
-    }
-  }
-  ut_sync();  // every read of L_tt / L_bb is done
-  if (warp < 2) {
-    const int o = 32 * warp, col = o + lane;
-    const float bc = beta[col];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      sl[65 * o + f32_idx(r, lane)] = y[r];
-      put_u(o + r, col, y[r], bc);
-    }
-    if (warp == 1) {  // upper-right block of U is zero
-#pragma unroll
-      for (int r = 0; r < 32; ++r) put_u(r, col, 0.f, 0.f);
-    }
-  }
-  ut_sync();
-  // ---- phase 2: rows 2 rg, 2 rg + 1 and columns 4 cg .. 4 cg + 3 of a 32 x 32 product ----
-  const int rg = tid >> 3, cg = tid & 7;
-  float acc[2][4];
-  auto product = [&](int a_row0, int a_col0, int b_row0, int b_col0) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 32; m += 4) {
-      const float4 a0 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg, a_col0 + m));
-      const float4 a1 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg + 1, a_col0 + m));
-      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(b_row0 + m + kk, b_col0 + 4 * cg));
-        acc[0][0] = fmaf(av0[kk], bv.x, acc[0][0]);
-        acc[0][1] = fmaf(av0[kk], bv.y, acc[0][1]);
-        acc[0][2] = fmaf(av0[kk], bv.z, acc[0][2]);
-        acc[0][3] = fmaf(av0[kk], bv.w, acc[0][3]);
-        acc[1][0] = fmaf(av1[kk], bv.x, acc[1][0]);
-        acc[1][1] = fmaf(av1[kk], bv.y, acc[1][1]);
-        acc[1][2] = fmaf(av1[kk], bv.z, acc[1][2]);
-        acc[1][3] = fmaf(av1[kk], bv.w, acc[1][3]);
-      }
-    }
-  };
-  product(32, 0, 0, 0);  // T = L_bt Y_tt
-#pragma unroll
-  for (int e = 0; e < 2; ++e)
-    *reinterpret_cast<float4*>(sl + f32_idx(2 * rg + e, 32 + 4 * cg)) =
-        make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
-  ut_sync();
-  product(32, 32, 0, 32);  // Y_bb T
-  const float4 bq = *reinterpret_cast<const float4*>(beta + 4 * cg);
-  const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-  for (int e = 0; e < 2; ++e)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) put_u(32 + 2 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
-}
-
-// The same block inversion writing U transposed: U^T (and U_lo^T) as swizzled bf16 tiles, so that
-// a thread, which holds one column of a diagonal block of U, writes it as one contiguous tile row
-// (four 16-byte stores instead of 32 scalar ones); Y is kept transposed in sl the same way (row j
-// of the block = column j of Y, eight 16-byte stores), and the off-diagonal block comes from
-//   T = L_bt Y_tt:  T[i][j] = sum_m L[32+i][m] Yt[j][m]   (rows of L times rows of Yt)
-//   Y_bt = -Y_bb T: Y_bt[i][j] = -sum_m Yt_bb[m][i] T[m][j]   (T kept in the unused upper-right block)
-// written to U^T rows j, columns 32 + i as bf16 pairs.  The MMAs read U^T with the opposite
-// operand major-ness.  Same arguments and phases as ut_solve_blocked.
+// Phase 1: warp 0 solves the columns of Y_tt, warp 1 those of Y_bb (one column per thread, 32 rows
+// by forward substitution, four partial sums per row).  Phase 2: all 128 threads form T = L_bt Y_tt
+// (into the unused upper-right block of sl), then Y_bt = -Y_bb T, each thread a 2 x 4 block.
+// sl: the fp32 L of the chunk (f32_idx layout over two tile slots, strictly lower; overwritten).
+// ut_solve_blocked_t writes U transposed: U^T (and, LO, U_lo^T with U = U_hi + U_lo, both bf16)
+// as swizzled bf16 tiles, so that a thread, which holds one column of a diagonal block, writes it
+// as one contiguous tile row (four 16-byte stores instead of 32 scalar ones); Y is kept transposed
+// in sl the same way (row j of a diagonal block = column j of Y), and phase 2 reads
+//   T = L_bt Y_tt:   T[i][j] = sum_m L[32+i][m] Yt[j][m]   (rows of L against rows of Yt; each
+//                    thread's columns interleaved, cg + 8 j, so that the eight Yt rows of a warp's
+//                    load sit on eight different swizzle positions)
+//   Y_bt = -Y_bb T:  Y_bt[i][j] = -sum_m Yt_bb[m][i] T[m][j]
+// writing U^T rows j, columns 32 + i as bf16 pairs.  The MMAs read U^T with the opposite operand
+// major-ness.  Called by threads 0-127 together; ends with the tiles written by generic stores
+// (the caller fences them for the tensor core).
 template <bool LO>
 __device__ __forceinline__ void ut_solve_blocked_t(float* sl, const float* beta, uint8_t* ut, uint8_t* ut_lo,
                                                    int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  // ---- phase 1: diagonal 32 x 32 blocks (as ut_solve_blocked) ----
+  // ---- phase 1: diagonal 32 x 32 blocks ----
   float y[32];
   if (warp < 2) {
     const float* sh = sl + 65 * 32 * warp;
@@ -397,18 +305,17 @@ __device__ __forceinline__ void ut_solve_blocked_t(float* sl, const float* beta,
   }
 }
 
-// The same block inversion on warps 0-1 alone (threads 0-63, named barrier 3), writing Y =
-// (I + L)^{-1} and U = Y diag(beta) as bf16 tiles yt and u; the off-diagonal block's two 32 x 32
-// products give each thread a 4 x 4 block.  For the UT backward, whose warps 2-3 convert the
-// gradient tiles meanwhile.  sl is overwritten.
+// Named barrier 3 over threads 0-63 (warps 0-1).
 __device__ __forceinline__ void ut_sync64() { asm volatile("bar.sync 3, 64;" ::: "memory"); }
-__device__ __forceinline__ void ut_solve_blocked64(float* sl, const float* beta, uint8_t* u, uint8_t* yt, int tid) {
+// The same block inversion in two parts, U and Y stored untransposed, for a caller whose warps 2-3
+// have their own work during the diagonal solves but are free for the off-diagonal products:
+//   ut_inv_diag64 (warps 0-1, named barrier 3): Y_tt, Y_bb into sl and the tiles yt (Y) and u
+//     (U = Y diag(beta)), the zero upper-right blocks included;
+//   ut_inv_offdiag128 (all 128 threads, after a barrier that makes ut_inv_diag64's stores
+//     visible): T = L_bt Y_tt, then Y_bt = -Y_bb T into yt and u; rows 2 rg, 2 rg + 1 and columns
+//     4 cg .. 4 cg + 3 of each 32 x 32 product per thread.
+__device__ __forceinline__ void ut_inv_diag64(float* sl, const float* beta, uint8_t* u, uint8_t* yt, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  auto put = [&](int r, int col, float yv, float bc) {
-    *reinterpret_cast<__nv_bfloat16*>(yt + sw128_offset(r, col)) = __float2bfloat16_rn(yv);
-    *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(r, col)) = __float2bfloat16_rn(yv * bc);
-  };
-  // ---- phase 1: diagonal 32 x 32 blocks, warp 0 the top one, warp 1 the bottom one ----
   float y[32];
   {
     const float* sh = sl + 65 * 32 * warp;
@@ -442,8 +349,6 @@ __device__ __forceinline__ void ut_solve_blocked64(float* sl, const float* beta,
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * b + rr;
-        // four independent partial sums (one per float4 lane) keep the dependent chain of row r
-        // at about r / 4 FMAs
         float a0 = acc[rr], a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int m = 16 * b; m < r; m += 4) {
@@ -458,66 +363,71 @@ __device__ __forceinline__ void ut_solve_blocked64(float* sl, const float* beta,
     }
   }
   ut_sync64();  // every read of L_tt / L_bb is done
-  {
-    const int o = 32 * warp, col = o + lane;
-    const float bc = beta[col];
+  const int o = 32 * warp, col = o + lane;
+  const float bc = beta[col];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    sl[65 * o + f32_idx(r, lane)] = y[r];
+    *reinterpret_cast<__nv_bfloat16*>(yt + sw128_offset(o + r, col)) = __float2bfloat16_rn(y[r]);
+    *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(o + r, col)) = __float2bfloat16_rn(y[r] * bc);
+  }
+  if (warp == 1) {  // the upper-right blocks of Y and U are zero
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      sl[65 * o + f32_idx(r, lane)] = y[r];
-      put(o + r, col, y[r], bc);
-    }
-    if (warp == 1) {
-#pragma unroll
-      for (int r = 0; r < 32; ++r) put(r, col, 0.f, 0.f);
+      *reinterpret_cast<__nv_bfloat16*>(yt + sw128_offset(r, col)) = __float2bfloat16_rn(0.f);
+      *reinterpret_cast<__nv_bfloat16*>(u + sw128_offset(r, col)) = __float2bfloat16_rn(0.f);
     }
   }
-  ut_sync64();
-  // ---- phase 2: rows 4 rg .. 4 rg + 3, columns 4 cg .. 4 cg + 3 of a 32 x 32 product ----
+}
+
+__device__ __forceinline__ void ut_inv_offdiag128(float* sl, const float* beta, uint8_t* u, uint8_t* yt, int tid) {
   const int rg = tid >> 3, cg = tid & 7;
-  float acc[4][4];
+  float acc[2][4];
   auto product = [&](int a_row0, int a_col0, int b_row0, int b_col0) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < 2; ++e)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[e][j] = 0.f;
 #pragma unroll
     for (int m = 0; m < 32; m += 4) {
-      float av[4][4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 a4 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 4 * rg + e, a_col0 + m));
-        av[e][0] = a4.x;
-        av[e][1] = a4.y;
-        av[e][2] = a4.z;
-        av[e][3] = a4.w;
-      }
+      const float4 a0 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg, a_col0 + m));
+      const float4 a1 = *reinterpret_cast<const float4*>(sl + f32_idx(a_row0 + 2 * rg + 1, a_col0 + m));
+      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const float4 bv = *reinterpret_cast<const float4*>(sl + f32_idx(b_row0 + m + kk, b_col0 + 4 * cg));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[e][0] = fmaf(av[e][kk], bv.x, acc[e][0]);
-          acc[e][1] = fmaf(av[e][kk], bv.y, acc[e][1]);
-          acc[e][2] = fmaf(av[e][kk], bv.z, acc[e][2]);
-          acc[e][3] = fmaf(av[e][kk], bv.w, acc[e][3]);
-        }
+        acc[0][0] = fmaf(av0[kk], bv.x, acc[0][0]);
+        acc[0][1] = fmaf(av0[kk], bv.y, acc[0][1]);
+        acc[0][2] = fmaf(av0[kk], bv.z, acc[0][2]);
+        acc[0][3] = fmaf(av0[kk], bv.w, acc[0][3]);
+        acc[1][0] = fmaf(av1[kk], bv.x, acc[1][0]);
+        acc[1][1] = fmaf(av1[kk], bv.y, acc[1][1]);
+        acc[1][2] = fmaf(av1[kk], bv.z, acc[1][2]);
+        acc[1][3] = fmaf(av1[kk], bv.w, acc[1][3]);
       }
     }
   };
-  product(32, 0, 0, 0);  // T = L_bt Y_tt
+  product(32, 0, 0, 0);  // T = L_bt Y_tt, into the unused upper-right block of sl
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    *reinterpret_cast<float4*>(sl + f32_idx(4 * rg + e, 32 + 4 * cg)) =
+  for (int e = 0; e < 2; ++e)
+    *reinterpret_cast<float4*>(sl + f32_idx(2 * rg + e, 32 + 4 * cg)) =
         make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
-  ut_sync64();
+  ut_sync();
   product(32, 32, 0, 32);  // Y_bb T
   const float4 bq = *reinterpret_cast<const float4*>(beta + 4 * cg);
   const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
+  for (int e = 0; e < 2; ++e) {
+    const int r = 32 + 2 * rg + e;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) put(32 + 4 * rg + e, 4 * cg + j, -acc[e][j], bv[j]);
+    for (int j = 0; j < 4; j += 2) {  // bf16 pairs of columns 4 cg + j, + 1
+      const int cj = 4 * cg + j;
+      *reinterpret_cast<uint32_t*>(yt + sw128_offset(r, cj)) = pack_bf16(-acc[e][j], -acc[e][j + 1]);
+      *reinterpret_cast<uint32_t*>(u + sw128_offset(r, cj)) = pack_bf16(-acc[e][j] * bv[j], -acc[e][j + 1] * bv[j + 1]);
+    }
+  }
 }
+
 
 }  // namespace tc
 }  // namespace pathattn
