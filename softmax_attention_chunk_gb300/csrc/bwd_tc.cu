@@ -242,17 +242,19 @@ __device__ __forceinline__ void store_box_quarter(uint8_t* box, int r, int q, co
         make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
 }
 
-__device__ __forceinline__ void store_row_bf16_sw(uint8_t* tile, int r, const float* x) {
+// 32 bf16 pairs (column 2j in the low half) as row r of a 128-byte swizzled bf16 tile.
+__device__ __forceinline__ void put_row_packed(uint8_t* tile, int r, const uint32_t* pk) {
   uint8_t* row = tile + r * 128;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint4 pk;
-    pk.x = pack_bf16(x[8 * q], x[8 * q + 1]);
-    pk.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
-    pk.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
-    pk.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
-    *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = pk;
-  }
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<uint4*>(row + ((q ^ (r & 7)) * 16)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+// 16 bf16 pairs as columns 32h .. 32h+31 of row r of a 128-byte swizzled bf16 tile.
+__device__ __forceinline__ void put_half_packed(uint8_t* tile, int r, int h, const uint32_t* pk) {
+  uint8_t* row = tile + r * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(row + (((4 * h + q) ^ (r & 7)) * 16)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 // 64 fp32 values as 32 bf16 pairs (column 2j in the low half), the TMEM A-operand layout.
 __device__ __forceinline__ void pack_row_pairs(const float* x, uint32_t (&pk)[32]) {
@@ -540,11 +542,19 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
           }
         }
       } else {
+        // key pairs through paired fp32 instructions: x = scl s - lse (log2 units), P = 2^x,
+        // dS = scale P (dP - D); the exponentials stay scalar
+        const uint64_t scl2 = f2(p.scl, p.scl), nl2 = f2(-lse2, -lse2), nd2 = f2(-Dr, -Dr), sc2 = f2(p.scale, p.scale);
+        const uint64_t z2 = f2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, -lse2)) : 0.f;
-          pv[j] = p0;
-          dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+        for (int j = 0; j < 16; ++j) {
+          float x0, x1;
+          f2_split(f2_fma(f2(__uint_as_float(sa[2 * j]), __uint_as_float(sa[2 * j + 1])), scl2, nl2), x0, x1);
+          const float p0 = active ? fast_exp2(x0) : 0.f, p1 = active ? fast_exp2(x1) : 0.f;
+          pv[2 * j] = p0;
+          pv[2 * j + 1] = p1;
+          const uint64_t dd = f2_add(f2(__uint_as_float(da[2 * j]), __uint_as_float(da[2 * j + 1])), nd2);
+          f2_split(f2_fma(f2_fma(f2(p0, p1), sc2, z2), dd, z2), dsv[2 * j], dsv[2 * j + 1]);
         }
       }
       uint32_t pk[16];
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
       if (k > 0) ok = ok && mbar_wait(&s.g_full, (k - 1) & 1, p.err, 36) && mbar_wait(&s.acc_full, (k - 1) & 1, p.err, 26);
       tc_fence_after();
       put_half(s.ps, r, h, pv);
-      put_half(s.ds, r, h, dsv);
+      put_half_packed(s.ds, r, h, pk);  // the pairs already packed for TMEM
       tmem_st16(tb + lane_off + TM_DSG + 16 * h, pk);
       fence_proxy_async_smem();
       tmem_st_wait();
@@ -636,9 +646,9 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < 16; ++j) dst[j] = make_float4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
         } else {
-          store_row_bf16_sw(s.gs, rg, g);
           uint32_t pk[32];
           pack_row_pairs(g, pk);
+          put_row_packed(s.gs, rg, pk);  // the same pairs for shared memory and TMEM
           tmem_st32(tb + lane_off + TM_DSG + 32, pk);
           fence_proxy_async_smem();
           tmem_st_wait();
