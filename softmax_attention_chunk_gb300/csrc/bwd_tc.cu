@@ -527,18 +527,25 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
         // the stage of this step's chunk holds its A_j (its barrier completed before S was issued)
         const int si = k % BS_KSTAGE;
         ok = ok && mbar_wait(&s.full[si], (k / BS_KSTAGE) & 1, p.err, 39);
-        const float4* a4 = reinterpret_cast<const float4*>(s.fxa[si] + 32 * h);
+        // key pairs through paired fp32 instructions: x = scl s - A_j log2(e) + (A_i log2(e) - lse),
+        // P = 2^x, dS = scale P (dP - D)
+        const ulonglong2* a4 = reinterpret_cast<const ulonglong2*>(s.fxa[si] + 32 * h);
+        const uint64_t scl2 = f2(p.scl, p.scl), nle2 = f2(-kLog2e, -kLog2e), fr2 = f2(fox_row, fox_row);
+        const uint64_t nd2 = f2(-Dr, -Dr), sc2 = f2(p.scale, p.scale), z2 = f2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 av = a4[q];
-          const float aj[4] = {av.x, av.y, av.z, av.w};
+          const ulonglong2 av = a4[q];  // A_j of keys 4q .. 4q+3 as two pairs
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * q + e;
-            const float p0 = active ? fast_exp2(fmaf(__uint_as_float(sa[j]), p.scl, fmaf(-aj[e], kLog2e, fox_row)))
-                                    : 0.f;
+          for (int e = 0; e < 2; ++e) {
+            const int j = 4 * q + 2 * e;
+            const uint64_t off = f2_fma(e ? av.y : av.x, nle2, fr2);
+            float x0, x1;
+            f2_split(f2_fma(f2(__uint_as_float(sa[j]), __uint_as_float(sa[j + 1])), scl2, off), x0, x1);
+            const float p0 = active ? fast_exp2(x0) : 0.f, p1 = active ? fast_exp2(x1) : 0.f;
             pv[j] = p0;
-            dsv[j] = p.scale * p0 * (__uint_as_float(da[j]) - Dr);
+            pv[j + 1] = p1;
+            const uint64_t dd = f2_add(f2(__uint_as_float(da[j]), __uint_as_float(da[j + 1])), nd2);
+            f2_split(f2_fma(f2_fma(f2(p0, p1), sc2, z2), dd, z2), dsv[j], dsv[j + 1]);
           }
         }
       } else {
