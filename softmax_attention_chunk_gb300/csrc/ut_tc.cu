@@ -1,5 +1,5 @@
 // Per-chunk UT preparation on tcgen05 (bf16 operands, fp32 accumulation in TMEM), chunk B = 64:
-// one CTA of 128 threads per chunk, three CTAs per SM.
+// persistent CTAs of 128 threads, three per SM, each taking chunk after chunk.
 //
 // Method: PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6 (UT representation) and §2.7
 // (boundary-adjusted queries/keys, chunk transform):
@@ -37,6 +37,8 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 namespace pathattn {
 
@@ -88,10 +90,6 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, bh = blockIdx.y;
-  const int row0 = c * B;
-  const size_t in_row = (size_t)bh * p.L;
-  const size_t ws_row = (size_t)bh * p.Lp + row0;
   const bool lead = tid == 0;
   const bool diag = p.with_diag != 0;
   // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
@@ -143,211 +141,221 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
     __syncthreads();
   };
 
-  if (lead) {
-    mbar_arrive_expect_tx(&s.bar_in, 3 * TILE);
-    tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
-    tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
-    tma_load_3d(s.t[S_K], &tm_k, 0, row0, bh, &s.bar_in);
-  }
-  if (tid < B) {
-    const int gi = row0 + tid;
-    s.beta[tid] = gi < p.L ? clamp_beta(p.beta[in_row + gi]) : 0.f;
-  }
-  if (warp == 3) {  // chunk-local inclusive prefix of log f
-    const int ga = row0 + lane, gb = row0 + 32 + lane;
-    float a = (p.logf && ga < p.L) ? p.logf[in_row + ga] : 0.f;
-    float b2 = (p.logf && gb < p.L) ? p.logf[in_row + gb] : 0.f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float ta2 = __shfl_up_sync(0xffffffffu, a, o), tb2 = __shfl_up_sync(0xffffffffu, b2, o);
-      if (lane >= o) { a += ta2; b2 += tb2; }
+  // Persistent: the CTA takes chunks blockIdx.x, blockIdx.x + gridDim.x, ... (chunk c of head bh at
+  // index bh * nc + c), keeping its barriers (phases carried over) and its TMEM.
+  const int nchunks = p.BH * p.nc;
+  uint32_t it = 0;  // chunks done by this CTA: the phase of bar_in and bar_v
+  for (int idx = blockIdx.x; idx < nchunks; idx += gridDim.x, ++it) {
+    const int c = idx % p.nc, bh = idx / p.nc;
+    const int row0 = c * B;
+    const size_t in_row = (size_t)bh * p.L;
+    const size_t ws_row = (size_t)bh * p.Lp + row0;
+    if (lead) {
+      fence_proxy_async_smem();  // the previous chunk's reads of the slots come before the copies
+      mbar_arrive_expect_tx(&s.bar_in, 3 * TILE);
+      tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
+      tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
+      tma_load_3d(s.t[S_K], &tm_k, 0, row0, bh, &s.bar_in);
     }
-    const float tot_a = __shfl_sync(0xffffffffu, a, 31);
-    s.pre[lane] = a;
-    s.pre[32 + lane] = b2 + tot_a;
-  }
-  mbar_wait(&s.bar_in, 0, p.err, 31);
-  __syncthreads();
-
-  // ---- P1: [G | N2] = W [W; K]^T (one N=128 MMA: the w and k slots are adjacent) ----
-  issue([&] {
-    const uint32_t idesc = idesc_bf16(64, 128, 0, 0);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t d = sdesc_sw128(ta(S_W) + 32u * kk, 1024, 16);
-      mma_ss(tb + 0, d, d, idesc, kk > 0 ? 1u : 0u);
+    if (tid < B) {
+      const int gi = row0 + tid;
+      s.beta[tid] = gi < p.L ? clamp_beta(p.beta[in_row + gi]) : 0.f;
     }
-  });
-  wait_mma(32);
-  {
-    float x[32];
-    ld_half(tb, lane_off, 0, x);  // L = strictLower(diag(beta) G), fp32
-    const float bi = s.beta[i];
+    if (warp == 3) {  // chunk-local inclusive prefix of log f
+      const int ga = row0 + lane, gb = row0 + 32 + lane;
+      float a = (p.logf && ga < p.L) ? p.logf[in_row + ga] : 0.f;
+      float b2 = (p.logf && gb < p.L) ? p.logf[in_row + gb] : 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = 32 * h + 4 * q;
-      *reinterpret_cast<float4*>(sg + f32_idx(i, j)) =
-          make_float4(j < i ? bi * x[4 * q] : 0.f, j + 1 < i ? bi * x[4 * q + 1] : 0.f,
-                      j + 2 < i ? bi * x[4 * q + 2] : 0.f, j + 3 < i ? bi * x[4 * q + 3] : 0.f);
-    }
-    ld_half(tb, lane_off, 64, x);  // N2 = strictLower(W K^T)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
-    put_half(s.t[S_N2], i, h, x);
-  }
-  // every thread has read P1's accumulators: M1 = Q W^T goes to the tensor core while the
-  // threads substitute
-  tc_fence_before();
-  __syncthreads();
-  issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
-
-  // ---- P2: U = (I + strictLower(D G))^{-1} D (fp32 F: U = U_hi + U_lo) ----
-  ut_solve_blocked_t<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);  // U^T (and U_lo^T) tiles
-  wait_mma(33);
-  {
-    float x[32];
-    ld_half(tb, lane_off, 0, x);  // M1 = lower(Q W^T)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
-    put_half(s.t[S_M1], i, h, x);
-  }
-  publish();
-
-  // ---- R1: A = M1 U, X = U N2 ----
-  issue([&] {
-    mma64(tb + 0, ta(S_M1), 0, ta(S_U), 0, 0);   // B = U read from U^T (K-major)
-    mma64(tb + 64, ta(S_U), 1, ta(S_N2), 1, 0);  // A = U read from U^T (MN-major)
-  });
-  wait_mma(34);
-  {
-    float x[32];
-    ld_half(tb, lane_off, 0, x);
-    put_half(s.t[S_A], i, h, x);
-    ld_half(tb, lane_off, 64, x);
-    put_half(s.t[S_X], i, h, x);
-  }
-  publish();
-
-  // ---- R2: Y = U^T W (+ U_lo^T W for an fp32 F), S_d = Q K^T - M1 X; then V into U's slot ----
-  issue([&] {
-    mma64(tb + 0, ta(S_U), 0, ta(S_W), 1, 0);  // A = U^T (K-major)
-    if constexpr (F32) mma64(tb + 0, ta(S_ULO), 0, ta(S_W), 1, 1);
-    if (diag) {
-      mma64(tb + 64, ta(S_Q), 0, ta(S_K), 0, 0);
-      mma64(tb + 64, ta(S_M1), 0, ta(S_X), 1, 1, /*neg_a=*/1);
-    }
-  });
-  wait_mma(35);
-  if (lead && diag) {  // U has been read by R2's products: its slot takes V
-    mbar_arrive_expect_tx(&s.bar_v, TILE);
-    tma_load_3d(s.t[S_V], &tm_v, 0, row0, bh, &s.bar_v);
-  }
-  {
-    float x[32];
-    ld_half(tb, lane_off, 0, x);
-    if constexpr (F32) {  // Y = Y_hi + Y_lo, both bf16
-      float lo[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(x[j]));
-        lo[j] = x[j] - hi;
-        x[j] = hi;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float ta2 = __shfl_up_sync(0xffffffffu, a, o), tb2 = __shfl_up_sync(0xffffffffu, b2, o);
+        if (lane >= o) { a += ta2; b2 += tb2; }
       }
-      put_half(s.t[S_YLO], i, h, lo);
+      const float tot_a = __shfl_sync(0xffffffffu, a, 31);
+      s.pre[lane] = a;
+      s.pre[32 + lane] = b2 + tot_a;
     }
-    put_half(s.t[S_Y], i, h, x);
-    if (diag) {
-      ld_half(tb, lane_off, 64, x);  // S_d: the diagonal chunk's softmax partial state
-      const float pi = s.pre[i];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int jj = 32 * h + j;
-        const float sv = (jj <= i && row0 + jj < p.L) ? fmaf(x[j], p.scl, (pi - s.pre[jj]) * kLog2e) : -INFINITY;
-        x[j] = sv;
-        mx = fmaxf(mx, sv);
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      float l = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float pj = x[j] == -INFINITY ? 0.f : fast_exp2(x[j] - mx);
-        x[j] = pj;
-        l += pj;
-      }
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      put_half(s.t[S_P], i, h, x);
-      if (h == 0) {
-        p.dm[ws_row + i] = mx;
-        p.dl[ws_row + i] = l;
-      }
-    }
-  }
-  if (p.logf && tid < B) {
-    const float tot = s.pre[B - 1];
-    p.fa[ws_row + tid] = s.pre[tid];
-    p.fr[ws_row + tid] = tot - s.pre[tid];
-    if (tid == 0) p.ft[(size_t)bh * p.nc + c] = tot;
-  }
-  publish();
+    mbar_wait(&s.bar_in, it & 1, p.err, 31);
+    __syncthreads();
 
-  // ---- R3: A W, X^T W -> Q<- = Q - A W, K-> = K - X^T W ----
-  issue([&] {
-    mma64(tb + 0, ta(S_A), 0, ta(S_W), 1, 0);
-    mma64(tb + 64, ta(S_X), 1, ta(S_W), 1, 0);
-  });
-  wait_mma(36);
-  {
-    float x[32], src[32];
-    const size_t orow = ws_row + i;
-    ld_half(tb, lane_off, 0, x);
-    get_half(s.t[S_Q], i, h, src);
+    // ---- P1: [G | N2] = W [W; K]^T (one N=128 MMA: the w and k slots are adjacent) ----
+    issue([&] {
+      const uint32_t idesc = idesc_bf16(64, 128, 0, 0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) src[j] -= x[j];
-    store_bf16_half(p.ql + orow * D + 32 * h, src);
-    ld_half(tb, lane_off, 64, x);
-    get_half(s.t[S_K], i, h, src);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t d = sdesc_sw128(ta(S_W) + 32u * kk, 1024, 16);
+        mma_ss(tb + 0, d, d, idesc, kk > 0 ? 1u : 0u);
+      }
+    });
+    wait_mma(32);
+    {
+      float x[32];
+      ld_half(tb, lane_off, 0, x);  // L = strictLower(diag(beta) G), fp32
+      const float bi = s.beta[i];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) src[j] -= x[j];
-    store_bf16_half(p.kr + orow * D + 32 * h, src);
-  }
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
-  if (diag) mbar_wait(&s.bar_v, 0, p.err, 37);
-  issue([&] {
-    mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
-    if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);
-    if (diag) mma64(tb + 64, ta(S_P), 0, ta(S_V), 1, 0);
-  });
-  wait_mma(38);
-  {
-    float x[32];
-    ld_half(tb, lane_off, 0, x);  // F = I - W^T Y, row i
+      for (int q = 0; q < 8; ++q) {
+        const int j = 32 * h + 4 * q;
+        *reinterpret_cast<float4*>(sg + f32_idx(i, j)) =
+            make_float4(j < i ? bi * x[4 * q] : 0.f, j + 1 < i ? bi * x[4 * q + 1] : 0.f,
+                        j + 2 < i ? bi * x[4 * q + 2] : 0.f, j + 3 < i ? bi * x[4 * q + 3] : 0.f);
+      }
+      ld_half(tb, lane_off, 64, x);  // N2 = strictLower(W K^T)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
-    if constexpr (F32) {
-      // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
-      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.f) + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-    } else {
-      store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
+      for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < i ? x[j] : 0.f;
+      put_half(s.t[S_N2], i, h, x);
     }
-    if (diag) {
+    // every thread has read P1's accumulators: M1 = Q W^T goes to the tensor core while the
+    // threads substitute
+    tc_fence_before();
+    __syncthreads();
+    issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
+
+    // ---- P2: U = (I + strictLower(D G))^{-1} D (fp32 F: U = U_hi + U_lo) ----
+    ut_solve_blocked_t<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);  // U^T (and U_lo^T) tiles
+    wait_mma(33);
+    {
+      float x[32];
+      ld_half(tb, lane_off, 0, x);  // M1 = lower(Q W^T)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = 32 * h + j <= i ? x[j] : 0.f;
+      put_half(s.t[S_M1], i, h, x);
+    }
+    publish();
+
+    // ---- R1: A = M1 U, X = U N2 ----
+    issue([&] {
+      mma64(tb + 0, ta(S_M1), 0, ta(S_U), 0, 0);   // B = U read from U^T (K-major)
+      mma64(tb + 64, ta(S_U), 1, ta(S_N2), 1, 0);  // A = U read from U^T (MN-major)
+    });
+    wait_mma(34);
+    {
+      float x[32];
+      ld_half(tb, lane_off, 0, x);
+      put_half(s.t[S_A], i, h, x);
       ld_half(tb, lane_off, 64, x);
-      float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      put_half(s.t[S_X], i, h, x);
     }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
+    publish();
+
+    // ---- R2: Y = U^T W (+ U_lo^T W for an fp32 F), S_d = Q K^T - M1 X; then V into U's slot ----
+    issue([&] {
+      mma64(tb + 0, ta(S_U), 0, ta(S_W), 1, 0);  // A = U^T (K-major)
+      if constexpr (F32) mma64(tb + 0, ta(S_ULO), 0, ta(S_W), 1, 1);
+      if (diag) {
+        mma64(tb + 64, ta(S_Q), 0, ta(S_K), 0, 0);
+        mma64(tb + 64, ta(S_M1), 0, ta(S_X), 1, 1, /*neg_a=*/1);
+      }
+    });
+    wait_mma(35);
+    if (lead && diag) {  // U has been read by R2's products: its slot takes V
+      mbar_arrive_expect_tx(&s.bar_v, TILE);
+      tma_load_3d(s.t[S_V], &tm_v, 0, row0, bh, &s.bar_v);
+    }
+    {
+      float x[32];
+      ld_half(tb, lane_off, 0, x);
+      if constexpr (F32) {  // Y = Y_hi + Y_lo, both bf16
+        float lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float hi = __bfloat162float(__float2bfloat16_rn(x[j]));
+          lo[j] = x[j] - hi;
+          x[j] = hi;
+        }
+        put_half(s.t[S_YLO], i, h, lo);
+      }
+      put_half(s.t[S_Y], i, h, x);
+      if (diag) {
+        ld_half(tb, lane_off, 64, x);  // S_d: the diagonal chunk's softmax partial state
+        const float pi = s.pre[i];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int jj = 32 * h + j;
+          const float sv = (jj <= i && row0 + jj < p.L) ? fmaf(x[j], p.scl, (pi - s.pre[jj]) * kLog2e) : -INFINITY;
+          x[j] = sv;
+          mx = fmaxf(mx, sv);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float pj = x[j] == -INFINITY ? 0.f : fast_exp2(x[j] - mx);
+          x[j] = pj;
+          l += pj;
+        }
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        put_half(s.t[S_P], i, h, x);
+        if (h == 0) {
+          p.dm[ws_row + i] = mx;
+          p.dl[ws_row + i] = l;
+        }
+      }
+    }
+    if (p.logf && tid < B) {
+      const float tot = s.pre[B - 1];
+      p.fa[ws_row + tid] = s.pre[tid];
+      p.fr[ws_row + tid] = tot - s.pre[tid];
+      if (tid == 0) p.ft[(size_t)bh * p.nc + c] = tot;
+    }
+    publish();
+
+    // ---- R3: A W, X^T W -> Q<- = Q - A W, K-> = K - X^T W ----
+    issue([&] {
+      mma64(tb + 0, ta(S_A), 0, ta(S_W), 1, 0);
+      mma64(tb + 64, ta(S_X), 1, ta(S_W), 1, 0);
+    });
+    wait_mma(36);
+    {
+      float x[32], src[32];
+      const size_t orow = ws_row + i;
+      ld_half(tb, lane_off, 0, x);
+      get_half(s.t[S_Q], i, h, src);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) src[j] -= x[j];
+      store_bf16_half(p.ql + orow * D + 32 * h, src);
+      ld_half(tb, lane_off, 64, x);
+      get_half(s.t[S_K], i, h, src);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) src[j] -= x[j];
+      store_bf16_half(p.kr + orow * D + 32 * h, src);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
+    if (diag) mbar_wait(&s.bar_v, it & 1, p.err, 37);
+    issue([&] {
+      mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
+      if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);
+      if (diag) mma64(tb + 64, ta(S_P), 0, ta(S_V), 1, 0);
+    });
+    wait_mma(38);
+    {
+      float x[32];
+      ld_half(tb, lane_off, 0, x);  // F = I - W^T Y, row i
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
+      if constexpr (F32) {
+        // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
+        float* f32 = reinterpret_cast<float*>(p.f);
+        float4* dst = reinterpret_cast<float4*>(f32 + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      } else {
+        store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
+      }
+      if (diag) {
+        ld_half(tb, lane_off, 64, x);
+        float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // TMEM and the slots are read out before the next chunk reuses them
     tc_fence_after();
-    tmem_dealloc(tb, TMEM_COLS);
   }
+  if (warp == 1) tmem_dealloc(tb, TMEM_COLS);
 }
 
 }  // namespace
@@ -384,7 +392,17 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
   auto kern = f32_f ? ut_prep64_kernel<true> : ut_prep64_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(g.nc, g.BH), 128, smem, st>>>(mq, mk, mv, mw, p);
+  // one wave of persistent CTAs: as many as the SMs hold at once, by shared memory (with the
+  // per-block reservation) and by TMEM columns (three per SM on a GB300)
+  int dev = 0, nsm = 0, smem_sm = 0, reserved = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  const int per_sm = std::max(1, std::min(smem_sm / (int)(smem + reserved), (int)(512 / TMEM_COLS)));
+  const long nchunks = (long)g.nc * g.BH;
+  const long grid = std::min(nchunks, (long)nsm * per_sm);
+  kern<<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mw, p);
   return cudaGetLastError();
 }
 
