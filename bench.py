@@ -103,9 +103,9 @@ def parse():
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode workload's batch (profiling on a smaller case)")
-    ap.add_argument("--only", default=None, choices=["train", "decode", "configs"],
-                    help="run one leg alone (profiling): the training step, the decode step or the "
-                         "per-workload forward/training legs")
+    ap.add_argument("--only", default=None, choices=["train", "decode", "configs", "handoff"],
+                    help="run one leg alone (profiling): the training step, the decode step, the "
+                         "per-workload forward/training legs or the prefill -> decode hand-off")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload legs")
     return ap.parse_args()
 
@@ -301,6 +301,9 @@ def run_ours(args):
         return
     if args.only == "configs":
         print(json.dumps({"configs": run_configs(args, pa, dev, pk, False)}), flush=True)
+        return
+    if args.only == "handoff":
+        print(json.dumps({"prefill_handoff": run_prefill_handoff(args, pa, dev, pk)}), flush=True)
         return
     if args.only == "train":
         args.no_decode = args.no_configs = args.no_cpu_baseline = True
@@ -765,7 +768,9 @@ def run_decode(args, pa, dev, rank, ws, pk):
 def run_prefill_handoff(args, pa, dev, pk):
     """Prefill -> decode hand-off of a prompt as long as the decode workload's cache (batch 32,
     32 heads, 32768 tokens, bf16), inputs drawn on the device; CUDA events around the call."""
-    cfg = CONFIGS[DEC_CFG]
+    cfg = dict(CONFIGS[DEC_CFG])
+    if args.decode_batch:
+        cfg["batch"] = args.decode_batch
     Bt, H, d, L = cfg["batch"], cfg["heads"], cfg["head_dim"], cfg["t0"]
     g = torch.Generator(device=dev).manual_seed(cfg["seed"] + 11)
     sd = 1.0 / math.sqrt(d)
@@ -792,9 +797,10 @@ def run_prefill_handoff(args, pa, dev, pk):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"ms": ms, "tokens_per_s": Bt * L / (ms * 1e-3), "compulsory_bytes": nbytes, "achieved_gbs": gbs,
             "frac_of_hbm": gbs / pk["hbm"],
-            "bound": "latency: the per-chunk tcgen05 UT preparation (fp32 F from split bf16 products) and the "
-                     "per-head fp32 suffix walk (one CTA per head, chunks right to left)",
-            "gpu_launches": 2, "workload": "prefill -> decode hand-off, batch 32, 32 heads, d=64, prompt 32768 bf16"}
+            "bound": "latency: the per-chunk tcgen05 UT preparation (split F from split bf16 products) and the "
+                     "per-head tcgen05 suffix walk (one CTA per head, chunks right to left)",
+            "gpu_launches": 2,
+            "workload": f"prefill -> decode hand-off, batch {Bt}, {H} heads, d={d}, prompt {L} bf16"}
 
 
 def run_head_dim_128(args, pa, dev, pk):

@@ -17,8 +17,9 @@
 // A key block at the end of shard r' reaches the end of shard r by k^ <- M_r^T k^, i.e. the rows
 // K^ <- K^ M_r.  Forget gate (§2.5): bias(i, j) = a_i + b_j with a_i = sum_{t = s(r)..i} log f_t
 // (shard-local inclusive prefix) and b_j = (T_{r'} - a_j) + the totals T of the shards passed.
-// The walks run in fp32, one CTA per head (like the prefill hand-off, with the same fp32 F from
-// split-precision products); the merge is the forward scan's block mode (fwd_tc.cu).
+// The walks are the hand-off's tensor-core chunk walk (walk_tc.cu: one CTA per head, the running
+// product and F split into bf16 high and low parts); the merge is the forward scan's block mode
+// (fwd_tc.cu).
 #include "../../include/path_attn.h"
 #include "internal.h"
 #include "dev_common.cuh"
@@ -39,67 +40,6 @@ constexpr int CB = 64;  // chunk rows of the tcgen05 preparation
 constexpr int LD = D + 1;
 constexpr int NB = D / 4;
 constexpr int WT = 256;  // threads of the walk and pass kernels
-
-// One head per CTA.  ASC = false: keys to the shard end (fp32 rows out) and M^T; ASC = true:
-// queries to the shard start (bf16 rows out).  rows: the chunk-aligned K-> or Q<- rows [BH][L][D]
-// (bf16); f: fp32 chunk transforms [BH][nc][D][D].
-template <bool ASC, typename TOut>
-__global__ void __launch_bounds__(WT) cp_walk_kernel(int L, int nc, const __nv_bfloat16* __restrict__ rows,
-                                                     const float* __restrict__ f, TOut* __restrict__ out,
-                                                     float* __restrict__ t_out) {
-  extern __shared__ float smem_f[];
-  float* ss = smem_f;       // S_c (right to left) or P_c^T (left to right)
-  float* sa = ss + D * LD;  // the chunk's rows, then F_c (right to left) or F_c^T (left to right)
-  float* st = sa + D * LD;  // the next S or P^T
-  const int tid = threadIdx.x, bh = blockIdx.x;
-  for (int e = tid; e < D * D; e += WT) ss[(e / D) * LD + e % D] = (e / D == e % D) ? 1.f : 0.f;
-  for (int n = 0; n < nc; ++n) {
-    const int c = ASC ? n : nc - 1 - n;
-    const bool last = n + 1 == nc;
-    if (tid == 0 && !last) {  // this chunk's transform and the next chunk's rows into L2
-      const int cn = ASC ? c + 1 : c - 1;
-      l2_prefetch(f + ((size_t)bh * nc + c) * D * D, D * D * sizeof(float));
-      l2_prefetch(rows + ((size_t)bh * L + (size_t)cn * CB) * D, CB * D * 2);
-    }
-    const __nv_bfloat16* src = rows + ((size_t)bh * L + (size_t)c * CB) * D;
-    for (int e = tid; e < CB * D; e += WT) sa[(e / D) * LD + e % D] = __bfloat162float(src[e]);
-    __syncthreads();
-    for (int blk = tid; blk < (CB / 4) * NB; blk += WT) {  // rows_c times S_c^T (or P_c)
-      const int r0 = 4 * (blk / NB), n0 = 4 * (blk % NB);
-      float acc[4][4];
-      mm_abt<D, LD>(sa, ss, r0, n0, acc);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        TOut* dst = out + ((size_t)bh * L + (size_t)c * CB + r0 + i) * D + n0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = from_f<TOut>(acc[i][j]);
-      }
-    }
-    if (ASC && last) break;  // the left-to-right walk needs no product past the last chunk
-    __syncthreads();         // every thread has read the chunk's rows
-    const float* fc = f + ((size_t)bh * nc + c) * D * D;
-    if (ASC) {
-      for (int e = tid; e < D * D; e += WT) sa[(e % D) * LD + e / D] = fc[e];  // F_c^T
-    } else {
-      for (int e = tid; e < D * D; e += WT) sa[(e / D) * LD + e % D] = fc[e];  // F_c
-    }
-    __syncthreads();
-    for (int blk = tid; blk < NB * NB; blk += WT) {  // S_c F_c^T, or P_c^T F_c
-      const int r0 = 4 * (blk / NB), n0 = 4 * (blk % NB);
-      float acc[4][4];
-      mm_abt<D, LD>(ss, sa, r0, n0, acc);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) st[(r0 + i) * LD + n0 + j] = acc[i][j];
-    }
-    __syncthreads();
-    for (int e = tid; e < D * D; e += WT) ss[(e / D) * LD + e % D] = st[(e / D) * LD + e % D];
-    __syncthreads();
-  }
-  if (!ASC)  // S_{-1} = M^T
-    for (int e = tid; e < D * D; e += WT) t_out[(size_t)bh * D * D + e] = ss[(e / D) * LD + e % D];
-}
 
 // Forget gate of a shard, one CTA per head: a = inclusive prefix sums of log f, T = the total,
 // b = T - a (fp32; segment sums, then a block scan of the segment totals).
@@ -181,7 +121,7 @@ int check_cp_desc(const path_attn_desc_t* d) {
 bool al(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct CpPrepWs {
-  FwdWs lay;  // the tcgen05 preparation's outputs (bf16 Q<-, K->; the F slot unused)
+  FwdWs lay;  // the tcgen05 preparation's outputs (bf16 Q<-, K->; the F slot unused; split F at f32)
   size_t f32, total;
 };
 CpPrepWs cp_prep_ws(const Geom& g) {
@@ -230,23 +170,17 @@ PATH_API int path_cp_shard_prepare(const path_attn_desc_t* desc, const void* q, 
   cudaStream_t st = (cudaStream_t)stream;
   char* wsb = (char*)ws;
   FwdWs lay = pw.lay;
-  lay.f = pw.f32;  // F in fp32
-  if ((rc = cuda_rc(cudaMemsetAsync(wsb + lay.err, 0, sizeof(int), st))) != PATH_OK) return rc;
-  // K->, Q<- (bf16) and the fp32 chunk transforms of every chunk (the values are not needed: k
+  lay.f = pw.f32;  // split F
+  int* err = (int*)(wsb + lay.err);
+  if ((rc = cuda_rc(cudaMemsetAsync(err, 0, sizeof(int), st))) != PATH_OK) return rc;
+  // K->, Q<- (bf16) and the split chunk transforms of every chunk (the values are not needed: k
   // stands in for them)
   if ((rc = cuda_rc(launch_ut_prep64(g, q, k, k, w, beta, nullptr, wsb, lay, false, st, true))) != PATH_OK) return rc;
-  const size_t smem = (size_t)3 * D * LD * sizeof(float);
-  auto kd = cp_walk_kernel<false, float>;
-  auto ka = cp_walk_kernel<true, __nv_bfloat16>;
-  if ((rc = cuda_rc(cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) != PATH_OK ||
-      (rc = cuda_rc(cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) != PATH_OK)
+  const void* fs = wsb + pw.f32;
+  if ((rc = cuda_rc(launch_walk_tc(g, false, true, wsb + lay.kr, fs, k_end, g.L, t_shard, err, st))) != PATH_OK)
     return rc;
-  const float* f = (const float*)(wsb + pw.f32);
-  kd<<<(unsigned)g.BH, WT, smem, st>>>(g.L, g.nc, (const __nv_bfloat16*)(wsb + lay.kr), f, k_end, t_shard);
-  if ((rc = cuda_rc(cudaGetLastError())) != PATH_OK) return rc;
-  ka<<<(unsigned)g.BH, WT, smem, st>>>(g.L, g.nc, (const __nv_bfloat16*)(wsb + lay.ql), f,
-                                       (__nv_bfloat16*)q_start, nullptr);
-  if ((rc = cuda_rc(cudaGetLastError())) != PATH_OK) return rc;
+  if ((rc = cuda_rc(launch_walk_tc(g, true, false, wsb + lay.ql, fs, q_start, g.L, nullptr, err, st))) != PATH_OK)
+    return rc;
   if (fox) {
     cp_fox_kernel<<<(unsigned)g.BH, WT, 0, st>>>(g.L, log_f, a_q, b_k, f_tot);
     if ((rc = cuda_rc(cudaGetLastError())) != PATH_OK) return rc;

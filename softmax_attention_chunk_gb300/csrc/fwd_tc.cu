@@ -510,17 +510,21 @@ bool make_map_f32_rows64(CUtensorMap* m, const void* base, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [heads][L][64] bf16 tensor seen in 64-row boxes of one head; rows >= L read as zero.
-bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads) {
+// [heads][L][64] bf16 tensor (head_rows rows between heads) seen in 64-row boxes of one head; rows
+// >= L read as zero and are not written by stores.
+bool make_map_head_rows64_pitch(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads, uint64_t head_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {64, L, heads};
-  cuuint64_t strides[2] = {128, L * 128};
+  cuuint64_t strides[2] = {128, head_rows * 128};
   cuuint32_t box[3] = {64, 64, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads) {
+  return make_map_head_rows64_pitch(m, base, L, heads, L);
 }
 
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,

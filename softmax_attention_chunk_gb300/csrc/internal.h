@@ -180,14 +180,29 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
 
 // tcgen05 UT preparation at chunk 64 (bf16 inputs): writes the chunk-64 operands of the
 // tensor-core scans (bf16 Q<-, K->, F) and, with_diag, the diagonal softmax state.  With f32_f
-// (and no diagonal state) F is written in fp32 ([BH][nc][64][64]) at lay.f, which must then have
-// room for it, from products whose bf16 operands U and U^T W are split into high and low bf16
-// parts (about 16 significant bits).  stall_ns (test hook of the failure path): nonzero makes every
-// CTA give up a wait on a barrier nothing arrives at after that many ns, recording code 99 in
-// lay.err, and end without writing anything.
+// (and no diagonal state) F is written split, F = F_hi + F_lo, as two bf16 64 x 64 tiles in the
+// 128-byte swizzled layout per chunk ([BH][nc][2][64 x 64], 16 KB per chunk) at lay.f, which must
+// then have room for it, from products whose bf16 operands U and U^T W are split into high and
+// low bf16 parts (about 16 significant bits).  with_q = false (with f32_f) runs the keys-only
+// instance of the hand-off: Q<- is not written, q is not read, and rows 0..g.L-1 of v are copied
+// to v_cache ([g.BH][cap][64] bf16, cap >= g.L).  stall_ns (test hook of the failure path): nonzero makes every CTA give
+// up a wait on a barrier nothing arrives at after that many ns, recording code 99 in lay.err, and
+// end without writing anything.
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, bool f32_f = false, uint32_t stall_ns = 0);
+                             cudaStream_t st, bool f32_f = false, uint32_t stall_ns = 0, bool with_q = true,
+                             void* v_cache = nullptr, int cap = 0);
+
+// Chunk walk on tcgen05 at head dim 64 over 64-row chunks, one CTA per head: with M = I at the
+// first chunk visited, out_c = X_c M_c^T for every chunk and the next M = M_c F_c^T (right to
+// left, asc = false: M_c = S_c, the suffix product) or M_c F_c (left to right, asc = true:
+// M_c = P_c^T), M held as a bf16 high/low pair and every product split-precision.  x: chunk-aligned
+// bf16 rows [g.BH][g.Lp][64]; fs: the split chunk transforms of launch_ut_prep64 with f32_f; out:
+// rows [g.BH][out_head][64] (fp32 with out_f32, else bf16), rows >= g.L not written; t_out (right to
+// left only, may be null): the final M = S_{-1} [g.BH][64][64] fp32.  err: the int that a wait
+// that gives up records its code in.
+cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x, const void* fs, void* out,
+                           size_t out_head, float* t_out, int* err, cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

@@ -11,11 +11,13 @@
 // hence k~_j = F_{nc-1}^T ... F_{c+1}^T K->_c row j.  With the suffix products
 //   S_{nc-1} = I,   S_{c-1} = S_c F_c^T,
 // the cache rows of chunk c are K->_c S_c^T.  At head dim 64, for a bf16 cache, K-> (bf16) and F
-// (fp32, from split-precision bf16 products: the long suffix chain must not accumulate bf16
-// rounding) come from the tcgen05 UT preparation (ut_tc.cu) on 64-row chunks; for an fp32 cache,
-// and at head dim 128 for both cache types, both come from the fp32 SIMT preparation
-// (simt_fwd.cu), at head dim 128 on 32-row chunks.  One CTA per head then walks the chunks right
-// to left, keeping S (d x d) in shared memory, in fp32: per chunk CB d^2 + d^3 multiply-adds.
+// (split into bf16 high and low tiles, from split-precision products: the long suffix chain must
+// not accumulate bf16 rounding) come from the tcgen05 UT preparation (ut_tc.cu, without its query
+// side) on 64-row chunks, and the walk runs on the tensor cores with S split the same way
+// (walk_tc.cu).  For an fp32 cache, and at head dim 128 for both cache types, both come from the
+// fp32 SIMT preparation (simt_fwd.cu), at head dim 128 on 32-row chunks, and one CTA per head
+// walks the chunks right to left on the CUDA cores, keeping S (d x d) in shared memory, in fp32:
+// per chunk CB d^2 + d^3 multiply-adds.
 #include "internal.h"
 #include "dev_common.cuh"
 #include "walk_common.cuh"
@@ -88,13 +90,13 @@ __global__ void __launch_bounds__(PT) prefill_transport_kernel(int L, int Lp, in
 }
 
 // Workspace of the hand-off: the forward layout of the chosen preparation (bf16 tcgen05 or fp32
-// SIMT), plus the fp32 F array of the bf16 path.
+// SIMT), plus the split F array of the bf16 path (two bf16 tiles, 16 KB per chunk).
 struct PrefillWs {
   FwdWs lay;
   size_t f32, total;
 };
-// The tcgen05 preparation (bf16 cache, head dim 64) writes bf16 K-> and a separate fp32 F; the SIMT
-// preparation writes both in fp32.
+// The tcgen05 preparation (bf16 cache, head dim 64) writes bf16 K-> and a separate split F; the
+// SIMT preparation writes both in fp32.
 bool prefill_tc(const Geom& g, bool is_bf16) { return is_bf16 && g.D == kHeadDim; }
 PrefillWs prefill_ws(const Geom& g, bool is_bf16) {
   PrefillWs w;
@@ -157,6 +159,7 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
   if (!((g.D == kHeadDim && g.B == 64) || (g.D == kHeadDimWide && g.B == 32))) return cudaErrorInvalidValue;
   const PrefillWs pw = prefill_ws(g, is_bf16);
   cudaError_t e;
+  bool values_done = false;
   // K-> and F of every chunk (the query input is unused here: k stands in for it)
   if (g.D == kHeadDimWide) {
     if ((e = launch_prep_simt(is_bf16, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
@@ -166,11 +169,15 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
                 : transport<float, float, kHeadDimWide, 32>(g, cap, kr, f, k_cache, st);
   } else if (is_bf16) {
     FwdWs lay = pw.lay;
-    lay.f = pw.f32;  // F in fp32
+    lay.f = pw.f32;  // split F
     if ((e = cudaMemsetAsync(ws + lay.err, 0, sizeof(int), st)) != cudaSuccess) return e;
-    if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, lay, false, st, true)) != cudaSuccess) return e;
-    e = transport<__nv_bfloat16, __nv_bfloat16, kHeadDim, 64>(g, cap, (const __nv_bfloat16*)(ws + lay.kr),
-                                                              (const float*)(ws + pw.f32), k_cache, st);
+    // K->, the split F and the values (copied to the cache by the preparation on the way)
+    if ((e = launch_ut_prep64(g, k, k, v, w, beta, nullptr, ws, lay, false, st, true, 0, false, v_cache, cap)) !=
+        cudaSuccess)
+      return e;
+    e = launch_walk_tc(g, false, false, ws + lay.kr, ws + pw.f32, k_cache, (size_t)cap, nullptr, (int*)(ws + lay.err),
+                       st);
+    values_done = true;
   } else {
     if ((e = launch_prep_simt(false, g, k, k, v, w, beta, nullptr, ws, pw.lay, false, st)) != cudaSuccess) return e;
     e = transport<float, float, kHeadDim, 64>(g, cap, (const float*)(ws + pw.lay.kr), (const float*)(ws + pw.lay.f),
@@ -181,6 +188,7 @@ cudaError_t launch_prefill(bool is_bf16, const Geom& g, int cap, const void* k, 
     prefill_logf_prefix_kernel<<<(unsigned)g.BH, PT, 0, st>>>(g.L, cap, logf, a_cache);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (values_done) return cudaSuccess;
   // values are appended unchanged: rows 0..L-1 of every (batch, head) slab of the cache
   const size_t row = (size_t)g.D * (is_bf16 ? 2 : 4);
   return cudaMemcpy2DAsync(v_cache, (size_t)cap * row, v, (size_t)g.L * row, (size_t)g.L * row, (size_t)g.BH,

@@ -21,10 +21,14 @@
 // 128 TMEM columns (two 64-column accumulators per round) and nine 8 KB tile slots, reused as
 // their tenants die:
 //   slot 0 W          P1 .. R4           slot 5 M1 (M1 epilogue .. R2), then Y (R2 .. R4)
-//   slot 1 K          P1 .. R3 epilogue  slot 6 N2 (P1 .. R1), then P (R2 .. R4) or Y_lo (fp32 F)
+//   slot 1 K          P1 .. R3 epilogue  slot 6 N2 (P1 .. R1), then P (R2 .. R4) or Y_lo (split F)
 //   slot 2 Q          P1 .. R3 epilogue  slot 7 U^T (P2 .. R2), then V (loaded once R2 has read it)
 //   slots 3-4 fp32 L (P1 .. P2), then A (slot 3) and X (slot 4) (R1 .. R3)
-//   slot 8 U_lo^T (fp32 F only)
+//   slot 8 U_lo^T (split F only)
+// The split-F instances (the walks of the hand-off and of the context-parallel shards) write F as
+// F_hi + F_lo, two bf16 tiles of about 16 significant bits together.  The keys-only instance (the
+// hand-off) loads no Q, skips M1, A, X and Q<-, and forms K-> = K - N2^T Y (X^T W = N2^T U^T W)
+// and F = I - W^T Y in one round, with Y_lo in Q's slot (N2 stays in its own until then).
 // U is stored transposed (the block inversion writes each column it holds as a contiguous row), and
 // the products read it with the matching operand major-ness.
 // W and K are adjacent: the first round's two products share the stacked [W; K] tile as one N=128
@@ -43,6 +47,7 @@
 namespace pathattn {
 
 bool make_map_head_rows64(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads);  // fwd_tc.cu
+bool make_map_head_rows64_pitch(CUtensorMap* m, const void* base, uint64_t L, uint64_t heads, uint64_t head_rows);
 
 namespace {
 using namespace tc;
@@ -81,11 +86,16 @@ struct __align__(1024) UtSmem {
   uint32_t tmem_base;
 };
 
-template <bool F32>
+// F32: F split into bf16 high and low tiles.  KO (keys only, with F32; the hand-off): no query
+// side and no diagonal state: K-> = K - N2^T Y and F = I - W^T Y both come from Y = U^T W in one
+// round; the chunk's values are copied to the value cache (tm_vc) on the way, through the fp32 L
+// slots once the substitution is done with them (TMA load, then TMA store: rows >= L are clipped).
+template <bool F32, bool KO>
 __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                            const __grid_constant__ CUtensorMap tm_k,
                                                            const __grid_constant__ CUtensorMap tm_v,
                                                            const __grid_constant__ CUtensorMap tm_w,
+                                                           const __grid_constant__ CUtensorMap tm_vc,
                                                            const UtParams p) {
   extern __shared__ uint8_t smem_raw[];
   UtSmem& s = *reinterpret_cast<UtSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,9 +162,9 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
     const size_t ws_row = (size_t)bh * p.Lp + row0;
     if (lead) {
       fence_proxy_async_smem();  // the previous chunk's reads of the slots come before the copies
-      mbar_arrive_expect_tx(&s.bar_in, 3 * TILE);
+      mbar_arrive_expect_tx(&s.bar_in, (KO ? 2 : 3) * TILE);
       tma_load_3d(s.t[S_W], &tm_w, 0, row0, bh, &s.bar_in);
-      tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
+      if (!KO) tma_load_3d(s.t[S_Q], &tm_q, 0, row0, bh, &s.bar_in);
       tma_load_3d(s.t[S_K], &tm_k, 0, row0, bh, &s.bar_in);
     }
     if (tid < B) {
@@ -207,12 +217,12 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
     // threads substitute
     tc_fence_before();
     __syncthreads();
-    issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
+    if constexpr (!KO) issue([&] { mma64(tb + 0, ta(S_Q), 0, ta(S_W), 0, 0); });
 
-    // ---- P2: U = (I + strictLower(D G))^{-1} D (fp32 F: U = U_hi + U_lo) ----
+    // ---- P2: U = (I + strictLower(D G))^{-1} D (split F: U = U_hi + U_lo) ----
     ut_solve_blocked_t<F32>(sg, s.beta, s.t[S_U], s.t[S_ULO], tid);  // U^T (and U_lo^T) tiles
-    wait_mma(33);
-    {
+    if constexpr (!KO) {
+      wait_mma(33);
       float x[32];
       ld_half(tb, lane_off, 0, x);  // M1 = lower(Q W^T)
 #pragma unroll
@@ -220,21 +230,25 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
       put_half(s.t[S_M1], i, h, x);
     }
     publish();
+    if (KO && lead) {  // the values through slot 3 (free once the substitution has read L)
+      mbar_arrive_expect_tx(&s.bar_v, TILE);
+      tma_load_3d(s.t[S_A], &tm_v, 0, row0, bh, &s.bar_v);
+    }
 
     // ---- R1: A = M1 U, X = U N2 ----
-    issue([&] {
-      mma64(tb + 0, ta(S_M1), 0, ta(S_U), 0, 0);   // B = U read from U^T (K-major)
-      mma64(tb + 64, ta(S_U), 1, ta(S_N2), 1, 0);  // A = U read from U^T (MN-major)
-    });
-    wait_mma(34);
-    {
+    if constexpr (!KO) {
+      issue([&] {
+        mma64(tb + 0, ta(S_M1), 0, ta(S_U), 0, 0);   // B = U read from U^T (K-major)
+        mma64(tb + 64, ta(S_U), 1, ta(S_N2), 1, 0);  // A = U read from U^T (MN-major)
+      });
+      wait_mma(34);
       float x[32];
       ld_half(tb, lane_off, 0, x);
       put_half(s.t[S_A], i, h, x);
       ld_half(tb, lane_off, 64, x);
       put_half(s.t[S_X], i, h, x);
+      publish();
     }
-    publish();
 
     // ---- R2: Y = U^T W (+ U_lo^T W for an fp32 F), S_d = Q K^T - M1 X; then V into U's slot ----
     issue([&] {
@@ -261,7 +275,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
           lo[j] = x[j] - hi;
           x[j] = hi;
         }
-        put_half(s.t[S_YLO], i, h, lo);
+        put_half(s.t[KO ? S_Q : S_YLO], i, h, lo);  // keys only: N2 stays for K->
       }
       put_half(s.t[S_Y], i, h, x);
       if (diag) {
@@ -299,62 +313,101 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
     }
     publish();
 
-    // ---- R3: A W, X^T W -> Q<- = Q - A W, K-> = K - X^T W ----
-    issue([&] {
-      mma64(tb + 0, ta(S_A), 0, ta(S_W), 1, 0);
-      mma64(tb + 64, ta(S_X), 1, ta(S_W), 1, 0);
-    });
-    wait_mma(36);
-    {
-      float x[32], src[32];
-      const size_t orow = ws_row + i;
-      ld_half(tb, lane_off, 0, x);
-      get_half(s.t[S_Q], i, h, src);
+    // F (row i, half h) as F_hi + F_lo, two bf16 tiles in the 128-byte swizzled layout, 16 KB per
+    // chunk at the F pointer (the caller's layout gives it room), for the chunk walks to load as
+    // they are
+    auto store_split_f = [&](float (&fv)[32]) {
+      float lo[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) src[j] -= x[j];
-      store_bf16_half(p.ql + orow * D + 32 * h, src);
+      for (int j = 0; j < 32; ++j) {
+        const float v = fv[j];
+        fv[j] = __bfloat162float(__float2bfloat16_rn(v));
+        lo[j] = v - fv[j];
+      }
+      uint8_t* ft = reinterpret_cast<uint8_t*>(p.f + ((size_t)bh * p.nc + c) * 2 * D * D);
+      put_half(ft, i, h, fv);
+      put_half(ft + TILE, i, h, lo);
+    };
+    if constexpr (KO) {
+      // ---- R3': W^T Y (+ W^T Y_lo), N2^T Y (+ N2^T Y_lo) -> F = I - W^T Y, K-> = K - N2^T Y
+      // (X^T W = N2^T U^T W) ----
+      issue([&] {
+        mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
+        mma64(tb + 0, ta(S_W), 1, ta(S_Q), 1, 1);
+        mma64(tb + 64, ta(S_N2), 1, ta(S_Y), 1, 0);
+        mma64(tb + 64, ta(S_N2), 1, ta(S_Q), 1, 1);
+      });
+      wait_mma(36);
+      if (lead && mbar_wait(&s.bar_v, it & 1, p.err, 37)) {
+        tma_store_3d(&tm_vc, s.t[S_A], 0, row0, bh);
+        bulk_commit();
+      }
+      float x[32], src[32];
       ld_half(tb, lane_off, 64, x);
       get_half(s.t[S_K], i, h, src);
 #pragma unroll
       for (int j = 0; j < 32; ++j) src[j] -= x[j];
-      store_bf16_half(p.kr + orow * D + 32 * h, src);
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
-    if (diag) mbar_wait(&s.bar_v, it & 1, p.err, 37);
-    issue([&] {
-      mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
-      if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);
-      if (diag) mma64(tb + 64, ta(S_P), 0, ta(S_V), 1, 0);
-    });
-    wait_mma(38);
-    {
-      float x[32];
-      ld_half(tb, lane_off, 0, x);  // F = I - W^T Y, row i
+      store_bf16_half(p.kr + (ws_row + i) * D + 32 * h, src);
+      ld_half(tb, lane_off, 0, x);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
-      if constexpr (F32) {
-        // fp32 F at the same F pointer (the caller's layout gives it room for fp32)
-        float* f32 = reinterpret_cast<float*>(p.f);
-        float4* dst = reinterpret_cast<float4*>(f32 + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h);
+      for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];  // F = I - W^T Y, row i
+      store_split_f(x);
+    } else {
+      // ---- R3: A W, X^T W -> Q<- = Q - A W, K-> = K - X^T W ----
+      issue([&] {
+        mma64(tb + 0, ta(S_A), 0, ta(S_W), 1, 0);
+        mma64(tb + 64, ta(S_X), 1, ta(S_W), 1, 0);
+      });
+      wait_mma(36);
+      {
+        float x[32], src[32];
+        const size_t orow = ws_row + i;
+        ld_half(tb, lane_off, 0, x);
+        get_half(s.t[S_Q], i, h, src);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-      } else {
-        store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
-      }
-      if (diag) {
+        for (int j = 0; j < 32; ++j) src[j] -= x[j];
+        store_bf16_half(p.ql + orow * D + 32 * h, src);
         ld_half(tb, lane_off, 64, x);
-        float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
+        get_half(s.t[S_K], i, h, src);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int j = 0; j < 32; ++j) src[j] -= x[j];
+        store_bf16_half(p.kr + orow * D + 32 * h, src);
+      }
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
+      if (diag) mbar_wait(&s.bar_v, it & 1, p.err, 37);
+      issue([&] {
+        mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
+        if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);
+        if (diag) mma64(tb + 64, ta(S_P), 0, ta(S_V), 1, 0);
+      });
+      wait_mma(38);
+      {
+        float x[32];
+        ld_half(tb, lane_off, 0, x);  // F = I - W^T Y, row i
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (32 * h + j == i ? 1.f : 0.f) - x[j];
+        if constexpr (F32) {
+          store_split_f(x);
+        } else {
+          store_bf16_half(p.f + (((size_t)bh * p.nc + c) * D + i) * D + 32 * h, x);
+        }
+        if (diag) {
+          ld_half(tb, lane_off, 64, x);
+          float4* dst = reinterpret_cast<float4*>(p.dacc + (ws_row + i) * D + 32 * h);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
       }
     }
+    if (KO && lead) bulk_wait_read0();  // the value store has read slot 3
     tc_fence_before();
     __syncthreads();  // TMEM and the slots are read out before the next chunk reuses them
     tc_fence_after();
   }
+  if (KO && lead) bulk_wait0();
   if (warp == 1) tmem_dealloc(tb, TMEM_COLS);
 }
 
@@ -362,12 +415,15 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
 
 cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const void* v, const void* w,
                              const float* beta, const float* logf, char* ws, const FwdWs& lay, bool with_diag,
-                             cudaStream_t st, bool f32_f, uint32_t stall_ns) {
-  if (g.B != 64 || (f32_f && with_diag)) return cudaErrorInvalidValue;
-  CUtensorMap mq, mk, mv, mw;
+                             cudaStream_t st, bool f32_f, uint32_t stall_ns, bool with_q, void* v_cache,
+                             int cap) {
+  if (g.B != 64 || (f32_f && with_diag) || (!with_q && (!f32_f || !v_cache || cap < g.L))) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv, mw, mvc;
   if (!make_map_head_rows64(&mq, q, g.L, g.BH) || !make_map_head_rows64(&mk, k, g.L, g.BH) ||
       !make_map_head_rows64(&mv, v, g.L, g.BH) || !make_map_head_rows64(&mw, w, g.L, g.BH))
     return cudaErrorInvalidValue;
+  if (with_q) mvc = mv;  // unused
+  else if (!make_map_head_rows64_pitch(&mvc, v_cache, g.L, g.BH, cap)) return cudaErrorInvalidValue;
   UtParams p;
   p.L = g.L;
   p.Lp = g.Lp;
@@ -389,7 +445,8 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
   p.err = (int*)(ws + lay.err);
   p.stall_ns = stall_ns;
   const size_t smem = sizeof(UtSmem) + 1024;
-  auto kern = f32_f ? ut_prep64_kernel<true> : ut_prep64_kernel<false>;
+  auto kern = !with_q ? ut_prep64_kernel<true, true>
+                      : (f32_f ? ut_prep64_kernel<true, false> : ut_prep64_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // one wave of persistent CTAs: as many as the SMs hold at once, by shared memory (with the
@@ -402,7 +459,7 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
   const int per_sm = std::max(1, std::min(smem_sm / (int)(smem + reserved), (int)(512 / TMEM_COLS)));
   const long nchunks = (long)g.nc * g.BH;
   const long grid = std::min(nchunks, (long)nsm * per_sm);
-  kern<<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mw, p);
+  kern<<<(unsigned)grid, 128, smem, st>>>(mq, mk, mv, mw, mvc, p);
   return cudaGetLastError();
 }
 
