@@ -676,7 +676,68 @@ def run_configs(args, pa, dev, pk, with_cpu):
                      args.warmup, 20)
     out["pr1_tiny_fwd"] = {"workload": "forward, batch 1, 2 heads, d=64, L=128, fp32 CUDA-core kernels", "ms": ms,
                            "tokens_per_s": Bt * L / (ms * 1e-3), "bound": "launch latency (two small launches)"}
+    del x, wsf, o, lse
+    torch.cuda.empty_cache()
+    out["cp_fox_l16384_4shards"] = run_cp(args, pa, g, pk)
     return out
+
+
+def run_cp(args, pa, g, pk):
+    """Context-parallel forward of the PaTH-FoX long sequence (batch 1 x 32 heads, L 16384, bf16) cut
+    into 4 shards of 4096, the ranks emulated on this one GPU (the chain's schedule and C-ABI
+    calls, messages as device copies, no collective): the whole chain (every shard's preparation,
+    the 6 block merges and 3 block passes, every shard's scan) against the single-device forward
+    of the same sequence, and the time of each kind of shard operation (one instrumented run)."""
+    from softmax_attention_chunk_gb300.context_parallel import ShardOps, emulate_ring
+
+    Bt, H, L, world = 1, 32, 16384, 4
+    Ls = L // world
+    x = device_inputs(Bt, H, L, D, g, fox=True)
+    sh = [{n: (None if t is None else t[:, :, r * Ls:(r + 1) * Ls].contiguous()) for n, t in x.items() if n != "dO"}
+          for r in range(world)]
+
+    def chain():
+        ops = [ShardOps(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"], 1.0) for s in sh]
+        return emulate_ring(ops)
+
+    reps = max(3, args.steps)
+    ms = time_events(chain, args.warmup, reps)
+    desc = pa.make_desc(x["q"], 1.0)
+    wsf = pa.workspace(desc, 0, g.device)
+    o, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=g.device)
+    ms1 = time_events(lambda: pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["log_f"], 1.0, ws=wsf,
+                                     out=(o, lse)), args.warmup, reps)
+    # one instrumented chain: events around each kind of operation
+    parts = {"prepare": 0.0, "merge_block": 0.0, "pass_block": 0.0, "scan": 0.0}
+
+    def timed(kind, fn):
+        a = ev()
+        r = fn()
+        b = ev()
+        torch.cuda.synchronize()
+        parts[kind] += a.elapsed_time(b)
+        return r
+
+    ops = [timed("prepare", lambda s=s: ShardOps(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"], 1.0))
+           for s in sh]
+    held = [op.own_block() for op in ops]
+    from softmax_attention_chunk_gb300.context_parallel import step_roles
+    for st in range(1, world):
+        sent = [held[r] if step_roles(r, world, st)[0] else None for r in range(world)]
+        for r in range(world):
+            if step_roles(r, world, st)[1]:
+                got = {k: (None if t is None else t.clone()) for k, t in sent[r - 1].items()}
+                timed("merge_block", lambda: ops[r].attend(got))
+                held[r] = timed("pass_block", lambda: ops[r].pass_block(got)) if r <= world - 2 else None
+    res = [timed("scan", op.finish) for op in ops]
+    err = max((torch.cat([q[0] for q in res], dim=2).float() - o.float()).abs().max().item(),
+              (torch.cat([q[1] for q in res], dim=2) - lse).abs().max().item())
+    fl = Bt * H * fwd_flops_per_head(L, D, TC_CHUNK)
+    return {"workload": f"context-parallel PaTH-FoX forward, batch {Bt}, {H} heads, d=64, L={L} bf16, {world} shards "
+                        f"of {Ls} emulated on one GPU (no collectives)",
+            "ms": ms, "single_device_fwd_ms": ms1, "work_ratio": ms / ms1,
+            "tflops_at_the_forward_flop_count": fl / (ms * 1e-3) / 1e12, "parts_ms": parts,
+            "max_abs_diff_vs_single_device": err}
 
 
 def run_decode(args, pa, dev, rank, ws, pk):

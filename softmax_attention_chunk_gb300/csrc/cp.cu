@@ -30,7 +30,7 @@
 
 namespace pathattn {
 
-cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void* kb, const void* vb, const void* ident,
+cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void* kb, const void* vb,
                               const float* aq, const float* bk, char* ws, const FwdWs& lay, cudaStream_t st);
 
 namespace {
@@ -90,13 +90,10 @@ __global__ void __launch_bounds__(WT) cp_pass_kernel(int Lb, float* __restrict__
   if (bk && tid < CB) bk[(size_t)bh * Lb + (size_t)c * CB + tid] += tot[bh];
 }
 
-// The block's keys rounded to bf16 (the MMA operand) and the identity tile that stands for F in the
-// scan's block mode.
-__global__ void cp_block_operands_kernel(size_t n, const float* __restrict__ kh, __nv_bfloat16* __restrict__ kb,
-                                         __nv_bfloat16* __restrict__ ident) {
+// The block's keys rounded to bf16 (the MMA operand of the scan's block mode).
+__global__ void cp_block_operands_kernel(size_t n, const float* __restrict__ kh, __nv_bfloat16* __restrict__ kb) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) kb[i] = __float2bfloat16_rn(kh[i]);
-  if (i < (size_t)D * D) ident[i] = __float2bfloat16_rn((i / D) == (i % D) ? 1.f : 0.f);
 }
 
 // Shard geometry: 64-row chunks, L a multiple of 128 (the scan's query tiles).
@@ -132,7 +129,7 @@ CpPrepWs cp_prep_ws(const Geom& g) {
   return w;
 }
 
-size_t cp_block_ws(const Geom& g, int Lb) { return align_up((size_t)g.BH * Lb * D * 2, 256) + D * D * 2; }
+size_t cp_block_ws(const Geom& g, int Lb) { return align_up((size_t)g.BH * Lb * D * 2, 256); }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA; }
 
@@ -176,10 +173,8 @@ PATH_API int path_cp_shard_prepare(const path_attn_desc_t* desc, const void* q, 
   // K->, Q<- (bf16) and the split chunk transforms of every chunk (the values are not needed: k
   // stands in for them)
   if ((rc = cuda_rc(launch_ut_prep64(g, q, k, k, w, beta, nullptr, wsb, lay, false, st, true))) != PATH_OK) return rc;
-  const void* fs = wsb + pw.f32;
-  if ((rc = cuda_rc(launch_walk_tc(g, false, true, wsb + lay.kr, fs, k_end, g.L, t_shard, err, st))) != PATH_OK)
-    return rc;
-  if ((rc = cuda_rc(launch_walk_tc(g, true, false, wsb + lay.ql, fs, q_start, g.L, nullptr, err, st))) != PATH_OK)
+  if ((rc = cuda_rc(launch_walk_tc_pair(g, wsb + lay.kr, wsb + lay.ql, wsb + pw.f32, k_end, q_start, g.L, t_shard, err,
+                                        st))) != PATH_OK)
     return rc;
   if (fox) {
     cp_fox_kernel<<<(unsigned)g.BH, WT, 0, st>>>(g.L, log_f, a_q, b_k, f_tot);
@@ -216,11 +211,10 @@ PATH_API int path_cp_attend_block(const path_attn_desc_t* desc, int block_len, c
   cudaStream_t st = (cudaStream_t)stream;
   char* bw = (char*)blk_ws;
   __nv_bfloat16* kb = (__nv_bfloat16*)bw;
-  __nv_bfloat16* ident = (__nv_bfloat16*)(bw + align_up((size_t)g.BH * block_len * D * 2, 256));
   const size_t n = (size_t)g.BH * block_len * D;
-  cp_block_operands_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, k_block, kb, ident);
+  cp_block_operands_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n, k_block, kb);
   if ((rc = cuda_rc(cudaGetLastError())) != PATH_OK) return rc;
-  return cuda_rc(launch_scan_block(tw.g64, block_len, q_start, kb, v_block, ident, a_q, b_k, (char*)fwd_ws, tw.p64, st));
+  return cuda_rc(launch_scan_block(tw.g64, block_len, q_start, kb, v_block, a_q, b_k, (char*)fwd_ws, tw.p64, st));
 }
 
 PATH_API int path_cp_pass_block(const path_attn_desc_t* desc, int block_len, float* k_block, float* b_k,

@@ -116,7 +116,8 @@ __device__ __forceinline__ bool softmax_any(bool q) {
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // BLOCK (context-parallel block mode): every query tile visits every 64-row chunk of a separate
-// key block (K-> = the block's keys, F = one identity tile, V = the block's values; FoX: fa holds
+// key block (K-> = the block's keys, V = the block's values, no transport: the queries stay where
+// the shard start put them, so no F is loaded, the MMA forms S alone and Z is never rewritten; FoX: fa holds
 // the queries' bias, fr the keys'), starting from and writing back the softmax state in dm, dl,
 // dacc (unnormalised), instead of the causal chunk range and the o / lse epilogue.
 template <bool FOX, bool BLOCK>
@@ -172,9 +173,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         const int st = n % NSTAGE;
         if (n >= NSTAGE && !mbar_wait(&s.empty[st], ((n / NSTAGE) - 1) & 1, p.err, 1)) break;
         const int c = step_chunk(n);
-        mbar_arrive_expect_tx(&s.full[st], 128 * 128 + BK * 128 + (FOX ? BK * 4 : 0));
+        mbar_arrive_expect_tx(&s.full[st], (BLOCK ? 64 : 128) * 128 + BK * 128 + (FOX ? BK * 4 : 0));
         tma_load_2d(s.kf[st], &tm_kr, 0, bh * p.Lk + c * BK, &s.full[st]);
-        tma_load_2d(s.kf[st] + 64 * 128, &tm_f, 0, BLOCK ? 0 : (bh * p.nc + c) * D, &s.full[st]);
+        if (!BLOCK) tma_load_2d(s.kf[st] + 64 * 128, &tm_f, 0, (bh * p.nc + c) * D, &s.full[st]);
         tma_load_2d(s.v[st], &tm_v, 0, bh * (BLOCK ? p.Lk : p.L) + c * BK, &s.full[st]);
         if constexpr (FOX) bulk_load(s.frs[st], p.fr + (size_t)bh * p.Lk + (size_t)c * BK, BK * 4, &s.full[st]);
       }
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       // S and Z' come from one N=128 MMA: the stage tile stacks K->_c (rows 0-63) over F_c, and
       // the S and Z' TMEM blocks are adjacent.  Descriptors advance by plain 64-bit adds (the
       // start-address field counts 16-byte units).
-      const uint32_t idesc_sz = idesc_bf16(128, 128, 0, 0);
+      const uint32_t idesc_sz = idesc_bf16(128, BLOCK ? 64 : 128, 0, 0);  // block mode: S alone
       const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
       // stage st of the kf / v rings lies st * 16 KB / st * 8 KB after stage 0
       const uint64_t dkf0 = sdesc_sw128(smem_u32(s.kf[0]), 1024, 16);
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       const int c = step_chunk(n);
       const bool active = !(has_partial && n == 0 && r < 64);
       // transport first: Z <- bf16(Z F_c^T) into TMEM, so that the next MMAs can start
-      if (n + 1 < nsteps && active) {
+      if (!BLOCK && n + 1 < nsteps && active) {
         tmem_ld32(c_zp, x);
         tmem_ld_wait();
         uint32_t z16[16];
@@ -564,13 +565,14 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   return cudaGetLastError();
 }
 
-cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void* kb, const void* vb, const void* ident,
+cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void* kb, const void* vb,
                               const float* aq, const float* bk, char* ws, const FwdWs& lay, cudaStream_t st) {
   if (g.B != BK || g.Lp != g.L || (g.L % BQ) || Lb <= 0 || (Lb % BK) || ((aq == nullptr) != (bk == nullptr)))
     return cudaErrorInvalidValue;
   CUtensorMap m_ql, m_kr, m_f, m_v;
   if (!make_map_rows64(&m_ql, zq, (uint64_t)g.BH * g.Lp, BQ) || !make_map_rows64(&m_kr, kb, (uint64_t)g.BH * Lb, BK) ||
-      !make_map_rows64(&m_f, ident, D, D) || !make_map_rows64(&m_v, vb, (uint64_t)g.BH * Lb, BK))
+      !make_map_rows64(&m_f, kb, (uint64_t)g.BH * Lb, BK) ||  // not read in block mode
+      !make_map_rows64(&m_v, vb, (uint64_t)g.BH * Lb, BK))
     return cudaErrorInvalidValue;
   ScanParams p{};
   p.L = g.L;

@@ -203,6 +203,10 @@ cudaError_t launch_ut_prep64(const Geom& g, const void* q, const void* k, const 
 // that gives up records its code in.
 cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x, const void* fs, void* out,
                            size_t out_head, float* t_out, int* err, cudaStream_t st);
+// Both walks of a context-parallel shard in one launch: xk (K->) right to left into fp32 k_out and
+// t_out, xq (Q<-) left to right into bf16 q_out (both [g.BH][out_head][64]).
+cudaError_t launch_walk_tc_pair(const Geom& g, const void* xk, const void* xq, const void* fs, float* k_out,
+                                void* q_out, size_t out_head, float* t_out, int* err, cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

@@ -62,7 +62,7 @@ struct __align__(1024) WalkSmem {
 };
 
 template <bool ASC, bool OUT_F32>
-__global__ void __launch_bounds__(128, 3) walk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const WalkParams p) {
+__device__ __forceinline__ void walk_head(const CUtensorMap& tm_x, const WalkParams& p, int bh) {
   extern __shared__ uint8_t smem_raw[];
   WalkSmem& s = *reinterpret_cast<WalkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(128, 3) walk_tc_kernel(const __grid_constant__
   // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
   const int i = 16 * warp + (lane & 15), h = lane >> 4;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const int bh = blockIdx.x, nc = p.nc;
+  const int nc = p.nc;
 
   if (lead) {
     for (int st = 0; st < NSTAGE; ++st) mbar_init(&s.full[st], 1);
@@ -187,14 +187,22 @@ __global__ void __launch_bounds__(128, 3) walk_tc_kernel(const __grid_constant__
   }
 }
 
-}  // namespace
+template <bool ASC, bool OUT_F32>
+__global__ void __launch_bounds__(128, 3) walk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const WalkParams p) {
+  walk_head<ASC, OUT_F32>(tm_x, p, (int)blockIdx.x);
+}
 
-cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x, const void* fs, void* out,
-                           size_t out_head, float* t_out, int* err, cudaStream_t st) {
-  if (g.B != 64 || g.D != D || g.Lp != g.nc * 64 || (asc && t_out) || g.nc <= 0) return cudaErrorInvalidValue;
-  if (out_head < (size_t)g.L) return cudaErrorInvalidValue;
-  CUtensorMap mx;
-  if (!make_map_head_rows64(&mx, x, g.Lp, g.BH)) return cudaErrorInvalidValue;
+// Both walks of a context-parallel shard in one launch (they are independent): CTAs 0 .. BH-1
+// move the keys right to left (fp32 rows and the shard product), CTAs BH .. 2BH-1 the queries
+// left to right (bf16 rows).
+__global__ void __launch_bounds__(128, 3) walk_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                              const __grid_constant__ CUtensorMap tm_q,
+                                                              const WalkParams pk, const WalkParams pq, int BH) {
+  if ((int)blockIdx.x < BH) walk_head<false, true>(tm_k, pk, (int)blockIdx.x);
+  else walk_head<true, false>(tm_q, pq, (int)blockIdx.x - BH);
+}
+
+WalkParams walk_params(const Geom& g, const void* fs, void* out, size_t out_head, float* t_out, int* err) {
   WalkParams p;
   p.nc = g.nc;
   p.nrows = g.L;
@@ -203,12 +211,43 @@ cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x,
   p.out_head = out_head;
   p.t_out = t_out;
   p.err = err;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x, const void* fs, void* out,
+                           size_t out_head, float* t_out, int* err, cudaStream_t st) {
+  if (g.B != 64 || g.D != D || g.Lp != g.nc * 64 || (asc && t_out) || g.nc <= 0) return cudaErrorInvalidValue;
+  if (out_head < (size_t)g.L) return cudaErrorInvalidValue;
+  CUtensorMap mx;
+  if (!make_map_head_rows64(&mx, x, g.Lp, g.BH)) return cudaErrorInvalidValue;
+  const WalkParams p = walk_params(g, fs, out, out_head, t_out, err);
   const size_t smem = sizeof(WalkSmem) + 1024;
   auto kern = asc ? (out_f32 ? walk_tc_kernel<true, true> : walk_tc_kernel<true, false>)
                   : (out_f32 ? walk_tc_kernel<false, true> : walk_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)g.BH, 128, smem, st>>>(mx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pathattn
+
+namespace pathattn {
+
+cudaError_t launch_walk_tc_pair(const Geom& g, const void* xk, const void* xq, const void* fs, float* k_out,
+                                void* q_out, size_t out_head, float* t_out, int* err, cudaStream_t st) {
+  if (g.B != 64 || g.D != D || g.Lp != g.nc * 64 || g.nc <= 0 || out_head < (size_t)g.L) return cudaErrorInvalidValue;
+  CUtensorMap mk, mq;
+  if (!make_map_head_rows64(&mk, xk, g.Lp, g.BH) || !make_map_head_rows64(&mq, xq, g.Lp, g.BH))
+    return cudaErrorInvalidValue;
+  const WalkParams pk = walk_params(g, fs, k_out, out_head, t_out, err);
+  const WalkParams pq = walk_params(g, fs, q_out, out_head, nullptr, err);
+  const size_t smem = sizeof(WalkSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(walk_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  walk_tc_pair_kernel<<<(unsigned)(2 * g.BH), 128, smem, st>>>(mk, mq, pk, pq, g.BH);
   return cudaGetLastError();
 }
 
