@@ -49,10 +49,10 @@ D = 64
 UT_PREP64_MMAS = 12  # G, M1, N2, QK^T; M1 U, U N2, U^T W; A W, X^T W, M1 X, W^T Y; P V
 UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule through U, X, M1, N2, G
 # DRAM bytes per head of one bwd_scan_tc_kernel launch at L = 4096: ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum) of a 16-head launch (batch 1, 16 heads) divided by 16 — the kernel takes
-# heads 16 at a time, so a launch over more heads repeats that traffic per group.  To be retaken
-# whenever the kernel changes.
-BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (425917440 + 80140288) / 16
+# dram__bytes_write.sum) of a 64-head launch (batch 4 x 16 heads: four head groups, a working set
+# above L2) divided by 64 — the kernel takes heads 16 at a time, so a launch over more heads repeats
+# that traffic per group.  To be retaken whenever the kernel changes.
+BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (1712006144 + 436957952) / 64
 # DRAM bytes per head of one decode step at t = 32768 (split + combine kernels): ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum) of a batch-4 x 32-head step divided by 128 heads
 # (the step's traffic grows in proportion to the heads it processes).  To be retaken whenever the
