@@ -53,13 +53,20 @@ struct __align__(1024) ScanSmem {
                                       // step 0 the image buffer of the even Z tiles
   uint8_t kf[NSTAGE][128 * 128];      // rows 0-63: K->_c, rows 64-127: F_c
   uint8_t v[NSTAGE][BK * 128];        // V_c
-  uint8_t zout[BQ * 128];             // image buffer of the odd Z tiles on their way to the Z store
   float xm[2][BQ];                    // per-half row maxima / sums exchanged between the halves
   float frs[NSTAGE][BK];              // PaTH-FoX: the chunk's suffix sums of log f (with K->_c, F_c, V_c)
   uint64_t full[NSTAGE], empty[NSTAGE];
   uint64_t z_init, z_ready, s_full, p_ready, pv_done, o_done, zbuf_free[2];
   uint32_t tmem_base;
+  // last, so that a launch without the Z store leaves it out of its shared memory (16 KB less
+  // per CTA: more of the SM's unified memory stays L1)
+  alignas(1024) uint8_t zout[BQ * 128];  // image buffer of the odd Z tiles on their way to the Z store
 };
+// Dynamic shared memory of a launch (with the 1 KB alignment slack): without the Z store the
+// buffer that only the store uses is not allocated.
+constexpr size_t scan_smem_bytes(bool zstore) {
+  return (zstore ? sizeof(ScanSmem) : offsetof(ScanSmem, zout)) + 1024;
+}
 
 struct ScanParams {
   int L, Lp, nc, BH, ntiles;
@@ -556,9 +563,9 @@ cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char
   p.lse = lse;
   p.zs = (uint8_t*)zstore;
   p.err = (int*)(ws + lay.err);
-  const size_t smem = sizeof(ScanSmem) + 1024;
+  const size_t smem = scan_smem_bytes(p.zs != nullptr);  // the attribute below is the maximum of both
   auto kern = logf ? fwd_scan_tc_kernel<true, false> : fwd_scan_tc_kernel<false, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem_bytes(true));
   if (e != cudaSuccess) return e;
   const long ntiles = (long)p.ntiles * g.BH;
   kern<<<(unsigned)ntiles, NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
@@ -589,9 +596,9 @@ cudaError_t launch_scan_block(const Geom& g, int Lb, const void* zq, const void*
   p.fa = aq;
   p.fr = bk;
   p.err = (int*)(ws + lay.err);
-  const size_t smem = sizeof(ScanSmem) + 1024;
+  const size_t smem = scan_smem_bytes(p.zs != nullptr);  // the attribute below is the maximum of both
   auto kern = aq ? fwd_scan_tc_kernel<true, true> : fwd_scan_tc_kernel<false, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem_bytes(true));
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)((long)p.ntiles * g.BH), NTHREADS, smem, st>>>(m_ql, m_kr, m_f, m_v, p);
   return cudaGetLastError();
