@@ -103,9 +103,10 @@ def parse():
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode workload's batch (profiling on a smaller case)")
-    ap.add_argument("--only", default=None, choices=["train", "decode", "configs", "handoff"],
+    ap.add_argument("--only", default=None, choices=["train", "decode", "configs", "handoff", "d128"],
                     help="run one leg alone (profiling): the training step, the decode step, the "
-                         "per-workload forward/training legs or the prefill -> decode hand-off")
+                         "per-workload forward/training legs, the prefill -> decode hand-off or the "
+                         "head-dim-128 legs")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload legs")
     return ap.parse_args()
 
@@ -304,6 +305,9 @@ def run_ours(args):
         return
     if args.only == "handoff":
         print(json.dumps({"prefill_handoff": run_prefill_handoff(args, pa, dev, pk)}), flush=True)
+        return
+    if args.only == "d128":
+        print(json.dumps({"head_dim_128": run_head_dim_128(args, pa, dev, pk)}), flush=True)
         return
     if args.only == "train":
         args.no_decode = args.no_configs = args.no_cpu_baseline = True
@@ -866,9 +870,11 @@ def run_prefill_handoff(args, pa, dev, pk):
 
 def run_head_dim_128(args, pa, dev, pk):
     """Head dim 128: the decode step (batch 32, 32 heads, bf16 cache of 32768 entries, 32 steps;
-    HBM bound, against the copy peak) and a training step on the fp32 CUDA-core kernels (batch 4,
-    16 heads, L 2048, bf16 inputs, 32-row chunks; against the FP32 FMA peak 152 SMs x 128 lanes x
-    2 flop x the maximum SM clock).  Inputs drawn on the device."""
+    HBM bound, against the copy peak); the bf16 forward on the head-dim-128 tensor-core kernels
+    (batch 4 x 16 heads x 2048 and batch 16 x 32 heads x 4096; TFLOP/s at chunk 64 against the bf16
+    peak); a training step (batch 4, 16 heads, L 2048, bf16 inputs): that forward plus the backward
+    on the fp32 CUDA-core kernels (32-row chunks), the backward also timed alone against the FP32
+    FMA peak 152 SMs x 128 lanes x 2 flop x the maximum SM clock.  Inputs drawn on the device."""
     g = torch.Generator(device=dev).manual_seed(4242)
     sd = 1.0 / math.sqrt(128)
     # ---- decode ----
@@ -903,7 +909,25 @@ def run_head_dim_128(args, pa, dev, pk):
               "workload": "decode, batch 32, 32 heads, d=128, cache 32768 -> 32799 bf16, 32 steps"}
     del kc, vc, sx
     torch.cuda.empty_cache()
-    # ---- training step (fp32 CUDA-core kernels) ----
+    # ---- forward on the tensor cores ----
+    fwd = {}
+    for Bt, H, L in ((4, 16, 2048), (16, 32, 4096)):
+        x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16) for n in ("q", "k", "v")}
+        x["w"] = unit(Bt, H, L, d)
+        x["beta"] = 2.0 * torch.sigmoid(torch.randn(Bt, H, L, device=dev, generator=g))
+        dsc = pa.make_desc(x["q"], 1.0)
+        wsf = pa.workspace(dsc, 0, dev)
+        o2, lse = torch.empty_like(x["q"]), torch.empty(Bt, H, L, device=dev)
+        ms = time_events(lambda: pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, 1.0, ws=wsf, out=(o2, lse)),
+                         args.warmup, max(3, args.steps))
+        tf = Bt * H * fwd_flops_per_head(L, d, TC_CHUNK) / (ms * 1e-3) / 1e12
+        fwd[f"b{Bt}h{H}_l{L}"] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16"],
+                                  "tokens_per_s": Bt * L / (ms * 1e-3), "gpu_launches": 2,
+                                  "workload": f"inference forward, batch {Bt}, {H} heads, d=128, L={L}, bf16, "
+                                              "tcgen05 (chunk 64)"}
+        del x, wsf, o2, lse
+        torch.cuda.empty_cache()
+    # ---- training step (tensor-core forward, fp32 CUDA-core backward) ----
     Bt, H, L, B = 4, 16, 2048, 32
     x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16) for n in ("q", "k", "v")}
     x["w"] = unit(Bt, H, L, d)
@@ -928,15 +952,19 @@ def run_head_dim_128(args, pa, dev, pk):
     b = ev()
     torch.cuda.synchronize()
     tms = a.elapsed_time(b) / reps
-    flops = Bt * H * (fwd_flops_per_head(L, d, B) + bwd_flops_per_head(L, d, B))
-    tf = flops / (tms * 1e-3) / 1e12
+    bms = time_events(lambda: pa.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], o2, lse, x["dO"], 1.0, ws=wsb,
+                                     out=grads), 1, reps)
+    ffl, bfl = Bt * H * fwd_flops_per_head(L, d, TC_CHUNK), Bt * H * bwd_flops_per_head(L, d, B)
     clk = pk.get("sm_max_mhz", 2070.0)
     fp32_peak = 152 * 128 * 2 * clk * 1e6 / 1e12
-    train = {"ms_per_step": tms, "tflops": tf, "bound": "alu", "peak": fp32_peak, "unit": "TFLOP/s",
-             "frac": tf / fp32_peak, "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {clk:.0f} MHz",
-             "flops_per_step": flops, "chunk": B,
-             "workload": "fwd+bwd, batch 4, 16 heads, d=128, L=2048, bf16 inputs, fp32 CUDA-core kernels"}
-    return {"decode": decode, "train": train}
+    btf = bfl / (bms * 1e-3) / 1e12
+    train = {"ms_per_step": tms, "tflops": (ffl + bfl) / (tms * 1e-3) / 1e12, "flops_per_step": ffl + bfl,
+             "backward": {"ms": bms, "tflops": btf, "bound": "alu", "peak": fp32_peak, "unit": "TFLOP/s",
+                          "frac": btf / fp32_peak, "chunk": B,
+                          "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {clk:.0f} MHz"},
+             "workload": "fwd+bwd, batch 4, 16 heads, d=128, L=2048, bf16 inputs: tcgen05 forward (chunk 64), "
+                         "fp32 CUDA-core backward (chunk 32)"}
+    return {"decode": decode, "forward": fwd, "train": train}
 
 
 def main():

@@ -58,9 +58,10 @@ typedef struct {
   int batch;      /* > 0 */
   int heads;      /* > 0 */
   int seqlen;     /* L > 0 */
-  int head_dim;   /* d: 64 or 128.  bf16 at 64 runs the tcgen05 kernels (chunk 64); 128 (and fp32)
-                     runs the fp32 CUDA-core kernels, at 128 with 32-row chunks only (chunk 0 or
-                     32; 64 is PATH_ERR_UNSUPPORTED) */
+  int head_dim;   /* d: 64 or 128.  bf16 at 64 runs the tcgen05 kernels (chunk 64); the bf16
+                     forward at 128 runs the head-dim-128 tcgen05 kernels (chunk 0 or 64: 64-row
+                     chunks); fp32 and the backward at 128 run the fp32 CUDA-core kernels with
+                     32-row chunks (fp32 chunk 64 at 128 is PATH_ERR_UNSUPPORTED) */
   int dtype;      /* path_dtype_t of q,k,v,w,o (and dO,dq,dk,dv,dw in the backward) */
   float scale;    /* multiplies the Householder-path logit; the forget bias is added unscaled */
   int chunk;      /* UT chunk size B; 0 lets the library choose (see path_attn_chunk) */
@@ -151,7 +152,7 @@ enum { PATH_BWD_REUSE_FWD = 8 };
  * training step): ws must be backward-sized (path_attn_workspace_size(desc, 1), else
  * PATH_ERR_WORKSPACE), and the scan also stores every transported query tile Z_n (§2.7: the
  * queries carried across earlier chunks) in ws, which the backward needs.  The bf16
- * tensor-core path only; ignored by the fp32 path. */
+ * tensor-core path at head_dim 64 only; ignored otherwise. */
 enum { PATH_FWD_STORE_Z = 4 };
 /* Optional bit for path_attn_bwd_phases(PREPARE): the workspace already holds the transported
  * query tiles because the forward ran with PATH_FWD_STORE_Z on it (same inputs, descriptor and

@@ -13,10 +13,15 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// bf16 at head dim 64 with the default (or 64) chunk runs the tcgen05 kernels; fp32, chunk 32
-// and head dim 128 run the SIMT kernels.
+// bf16 at head dim 64 with the default (or 64) chunk runs the tcgen05 kernels; fp32 and chunk 32
+// run the SIMT kernels.
 bool uses_tensor_cores(const path_attn_desc_t* d, int /*for_backward*/) {
   return d->dtype == PATH_BF16 && d->head_dim == kHeadDim && (d->chunk == 0 || d->chunk == 64);
+}
+// bf16 at head dim 128 with the default (or 64) chunk: the forward runs the head-dim-128 tcgen05
+// kernels (64-row chunks, 128-row query tiles); the backward runs the SIMT kernels (32-row chunks).
+bool uses_tc128(const path_attn_desc_t* d, int for_backward) {
+  return !for_backward && d->dtype == PATH_BF16 && d->head_dim == kHeadDimWide && (d->chunk == 0 || d->chunk == 64);
 }
 
 // Validates a descriptor; on success fills g for the requested pass.
@@ -29,13 +34,15 @@ int check_desc(const path_attn_desc_t* d, int for_backward, Geom* g) {
   const long long BH = (long long)d->batch * d->heads;
   if (BH > 65535) return PATH_ERR_UNSUPPORTED;
   if (d->chunk != 0 && d->chunk != 32 && d->chunk != 64) return PATH_ERR_UNSUPPORTED;
-  // head dim 128: the SIMT kernels' shared memory holds 32-row chunks only
-  if (d->head_dim == kHeadDimWide && d->chunk == 64) return PATH_ERR_UNSUPPORTED;
+  // head dim 128: the SIMT kernels' shared memory holds 32-row chunks only (bf16 forwards run the
+  // tensor-core kernels on 64-row chunks; their backward takes 32-row chunks whatever the descriptor)
+  if (d->head_dim == kHeadDimWide && d->chunk == 64 && d->dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
   int B = for_backward ? 32 : (d->chunk ? d->chunk : (d->head_dim == kHeadDimWide ? 32 : 64));
-  // The tensor-core path scans 64-row key chunks and 128-row query tiles.
-  if (uses_tensor_cores(d, for_backward)) B = 64;
+  // The tensor-core paths scan 64-row key chunks and 128-row query tiles.
+  const bool tc = uses_tensor_cores(d, for_backward) || uses_tc128(d, for_backward);
+  if (tc) B = 64;
   long long nc = (d->seqlen + B - 1) / B;
-  if (uses_tensor_cores(d, for_backward)) nc = (d->seqlen + 127) / 128 * 2;
+  if (tc) nc = (d->seqlen + 127) / 128 * 2;
   if (nc * (B / 32) > 65535 || nc * B > (1LL << 30)) return PATH_ERR_UNSUPPORTED;
   if (g) {
     g->BH = (int)BH;
@@ -55,6 +62,7 @@ TcWs tc_layout(const path_attn_desc_t* d, bool for_backward) {
 
 // Forward workspace size of the path this descriptor takes.
 size_t fwd_ws_total(const path_attn_desc_t* d, const Geom& g) {
+  if (uses_tc128(d, 0)) return fwd_ws_layout(g, 2).total;
   return uses_tensor_cores(d, 0) ? tc_layout(d, false).total : fwd_ws_layout(g, 4).total;
 }
 
@@ -149,6 +157,19 @@ PATH_API int path_attn_fwd_phases(int phases, const path_attn_desc_t* desc, cons
     }
     if (phases & PATH_FWD_SCAN) {
       rc = cuda_status(launch_scan_tc(tw.g64, v, log_f, wsb, tw.p64, o, lse, zstore, st));
+      if (rc != PATH_OK) return rc;
+    }
+    return PATH_OK;
+  }
+  if (uses_tc128(desc, 0)) {  // (no Z store: the head-dim-128 backward recomputes its own operands)
+    const FwdWs lay = fwd_ws_layout(g, 2);
+    if (phases & PATH_FWD_PREPARE) {
+      rc = cuda_status(cudaMemsetAsync(wsb + lay.err, 0, sizeof(int), st));
+      if (rc == PATH_OK) rc = cuda_status(launch_ut_prep128(g, q, k, v, w, beta, log_f, wsb, lay, st));
+      if (rc != PATH_OK) return rc;
+    }
+    if (phases & PATH_FWD_SCAN) {
+      rc = cuda_status(launch_scan128_tc(g, v, log_f, wsb, lay, o, lse, st));
       if (rc != PATH_OK) return rc;
     }
     return PATH_OK;
@@ -316,6 +337,11 @@ PATH_API int path_attn_workspace_status(const path_attn_desc_t* desc, int for_ba
   if (rc != PATH_OK) return rc;
   if (!ws || !aligned(ws, 256)) return PATH_ERR_INVALID_ARG;
   if (code) *code = 0;
+  if (uses_tc128(desc, for_backward)) {
+    const FwdWs lay = fwd_ws_layout(g, 2);
+    if (ws_bytes < lay.total) return PATH_ERR_WORKSPACE;
+    return read_error_word((const char*)ws + lay.err, code, (cudaStream_t)stream);
+  }
   if (!uses_tensor_cores(desc, for_backward)) return PATH_OK;  // no bounded waits on the fp32 path
   const TcWs tw = tc_layout(desc, for_backward != 0);
   if (ws_bytes < tw.total) return PATH_ERR_WORKSPACE;

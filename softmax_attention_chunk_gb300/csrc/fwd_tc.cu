@@ -28,6 +28,7 @@
 #include "internal.h"
 #include "dev_common.cuh"
 #include "tc_common.cuh"
+#include "scan_common.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -95,32 +96,6 @@ __device__ __forceinline__ void put_tile_quarter(uint8_t* tile, int r, int h, co
         make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-// 3-input max/min.
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-__device__ __forceinline__ float min3(float a, float b, float c) {
-  float r;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Barrier 1 over the softmax threads; returns whether q held for any of them.
-__device__ __forceinline__ bool softmax_any(bool q) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pq, pr;\n\t"
-      "setp.ne.u32 pq, %1, 0;\n\t"
-      "bar.red.or.pred pr, 1, 256, pq;\n\t"
-      "selp.u32 %0, 1, 0, pr;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)q)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // BLOCK (context-parallel block mode): every query tile visits every 64-row chunk of a separate
 // key block (K-> = the block's keys, V = the block's values, no transport: the queries stay where

@@ -207,6 +207,13 @@ cudaError_t launch_walk_tc(const Geom& g, bool asc, bool out_f32, const void* x,
 // t_out, xq (Q<-) left to right into bf16 q_out (both [g.BH][out_head][64]).
 cudaError_t launch_walk_tc_pair(const Geom& g, const void* xk, const void* xq, const void* fs, float* k_out,
                                 void* q_out, size_t out_head, float* t_out, int* err, cudaStream_t st);
+// Head dim 128 (bf16): the tcgen05 UT preparation of every 64-row chunk (Q<-, K->, F = 128 x 128
+// in bf16, the diagonal softmax state) into lay = fwd_ws_layout(g, 2) with g.D = 128, g.B = 64, and
+// the tcgen05 forward scan over 128-row query tiles from it (g.nc even).
+cudaError_t launch_ut_prep128(const Geom& g, const void* q, const void* k, const void* v, const void* w,
+                              const float* beta, const float* logf, char* ws, const FwdWs& lay, cudaStream_t st);
+cudaError_t launch_scan128_tc(const Geom& g, const void* v, const float* logf, char* ws, const FwdWs& lay, void* o,
+                              float* lse, cudaStream_t st);
 // tcgen05 forward scan over 128-row query tiles (pairs of 64-row chunks); g.nc must be even.
 cudaError_t launch_scan_tc(const Geom& g, const void* v, const float* logf, char* ws,
                            const FwdWs& lay, void* o, float* lse, void* zstore, cudaStream_t st);

@@ -63,9 +63,13 @@ def test_descriptor_validation(pa):
     assert pa.path_attn_chunk(desc(pa, chunk=32), 0) == 32
     assert pa.path_attn_chunk(desc(pa), 1) > 0
     assert pa.path_attn_chunk(desc(pa, head_dim=96), 0) == -2           # unsupported head dim
-    # head dim 128 runs the fp32 SIMT kernels, whose shared memory holds 32-row chunks
+    # head dim 128: fp32 (and every backward) runs the SIMT kernels, whose shared memory holds
+    # 32-row chunks; the bf16 forward runs the head-dim-128 tensor-core kernels on 64-row chunks
     assert pa.path_attn_chunk(desc(pa, head_dim=128), 0) == 32
-    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16), 0) == 32
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16), 0) == 64
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16, chunk=32), 0) == 32
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16, chunk=64), 0) == 64
+    assert pa.path_attn_chunk(desc(pa, head_dim=128, dtype=pa.PATH_BF16), 1) == 32
     assert pa.path_attn_chunk(desc(pa, head_dim=128, chunk=64), 0) == -2
     assert pa.path_attn_chunk(desc(pa, head_dim=128), 1) == 32
     assert pa.path_attn_workspace_size(desc(pa, head_dim=128), 1) > pa.path_attn_workspace_size(desc(pa), 1)
