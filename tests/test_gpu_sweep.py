@@ -2,7 +2,8 @@
 length (ragged, one to several query tiles), scale (either sign), near-reflection fraction and
 forget gate drawn from one generator, the forward and every gradient compared in full.  Head
 counts are chosen so that the scans' 16-head groups end in a partial group.  Also the head-dim-128
-forward across a partial head group and the one-shard (degenerate) context-parallel chain."""
+forward across a partial head group, the one-shard (degenerate) context-parallel chain, and a
+backward with more query tiles than SMs (several tiles per persistent CTA)."""
 import numpy as np
 import pytest
 import torch
@@ -91,3 +92,33 @@ def test_one_shard_chain_is_the_plain_forward(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(o, o1)
     assert torch.equal(lse, l1)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_backward_with_several_tiles_per_cta(cuda_lib, record_margin, fox):
+    """Batch 2 x 20 heads x 1024: 320 query tiles, more than the SMs, so the persistent backward
+    scan runs two or three tiles per CTA (its rings and barrier phases carried from tile to tile);
+    three whole heads against the oracle."""
+    from softmax_attention_chunk_gb300 import path_attn as pa
+
+    B, H, L = 2, 20, 1024
+    cfg = dict(batch=B, heads=H, seqlen=L, head_dim=64, dtype="bf16", seed=3301 + fox, with_dO=True, near2_frac=0.05,
+               fox=fox)
+    inp = gen_path_inputs(**cfg)
+    t = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
+    o, lse = pa.fwd(t["q"], t["k"], t["v"], t["w"], t["beta"], t["log_f"], scale=1.0)
+    g = pa.bwd(t["q"], t["k"], t["v"], t["w"], t["beta"], o, lse, t["dO"], scale=1.0, log_f=t["log_f"])
+    torch.cuda.synchronize()
+    heads = [0, 17, B * H - 1]
+    sub = gen_path_inputs(**cfg, heads_subset=heads)
+    ref = orc.bwd(sub["q"], sub["k"], sub["v"], sub["w"], sub["beta"], sub["log_f"], 1.0, sub["dO"], want_dlogf=fox)
+    keys = ("dq", "dk", "dv", "dw", "dbeta") + (("dlog_f",) if fox else ())
+    case = f"backward B{B} H{H} L{L}{' FoX' if fox else ''}, several tiles per CTA (heads {heads})"
+    for key in keys:
+        got = np64(flat(g[key])[heads])
+        r = ref[key]
+        bound = 2e-2 * max(1.0, np.abs(r).max())
+        e = np.abs(got - r).max()
+        rr = np.linalg.norm(got - r) / max(np.linalg.norm(r), 1e-30)
+        record_margin(case, key, e, bound, rel=rr)
+        assert e <= bound and rr <= 3e-2, (key, e, bound, rr)
