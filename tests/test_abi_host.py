@@ -298,3 +298,16 @@ def test_context_parallel_argument_errors(pa):
     assert pa.path_cp_pass_block(d, 100, FAKE, None, FAKE, None, None) == 2
     assert pa.path_cp_pass_block(d, 384, FAKE, FAKE, FAKE, None, None) == 1   # b_k without f_tot
     assert pa.path_cp_pass_block(d, 384, None, None, FAKE, None, None) == 1
+
+
+def test_autograd_binding_rejects_host_tensors_before_any_launch(pa):
+    """The autograd wrapper marshals through the same checks: CPU tensors are refused on the host."""
+    import pytest as _pytest
+    import torch as _torch
+
+    from softmax_attention_chunk_gb300.autograd import path_attention
+
+    q = _torch.zeros(1, 2, 64, 64, dtype=_torch.bfloat16)
+    beta = _torch.zeros(1, 2, 64, dtype=_torch.float32)
+    with _pytest.raises(ValueError):
+        path_attention(q, q, q, q, beta)
