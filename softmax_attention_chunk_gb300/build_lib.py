@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(16, len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".{os.getpid()}.tmp"
     r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
