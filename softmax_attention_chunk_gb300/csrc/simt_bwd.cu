@@ -14,6 +14,7 @@
 #include "internal.h"
 #include "dev_common.cuh"
 #include "smem_mm.cuh"
+#include "tc_common.cuh"
 
 #include <type_traits>
 
@@ -204,17 +205,12 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
           atomicAdd(fxcs + crow + j, cs);
         }
       }
-      // dV_c += P^T dO ; dK->_c += scale dS^T Z ; G_new = scale dS K + G F_c
-      for (int idx = tid; idx < B * D; idx += NT) {
-        const int j = idx / D, cc = idx % D;
-        float a = 0.f, bk = 0.f;
-        for (int i = 0; i < B; ++i) {
-          a += sP[i * BS + j] * sdO[i * DS + cc];
-          bk += sdS[i * BS + j] * sZ[i * DS + cc];
-        }
-        atomicAdd(dvacc + (crow + j) * D + cc, a);
-        atomicAdd(dkr + (crow + j) * D + cc, g.scale * bk);
-      }
+      // G_new = scale dS K + G F_c first (the last read of K), then dV_c += P^T dO and
+      // dK->_c += scale dS^T Z into the dead K and V buffers as dense 32 x D fp32 blocks, added to
+      // the accumulators by one bulk reduction each (contiguous rows of chunk c), and dF_c +=
+      // G_{b,c-1}^T Z_{b,c} in 32-row pieces through the same two buffers.  One thread issues the
+      // reductions; it waits for a buffer's previous reduction to have read it before the buffer
+      // is written again.
       for (int idx = tid; idx < B * D; idx += NT) {
         const int i = idx / D, nn = idx % D;
         float a = 0.f;
@@ -224,15 +220,45 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
           for (int kk = 0; kk < D; ++kk) a += sG[i * DS + kk] * sF[kk * DS + nn];
         sGn[i * DS + nn] = a;
       }
-      if (c > 0) {  // dF_c += G_{b,c-1}^T Z_{b,c}
+      __syncthreads();  // K and V are dead
+      for (int idx = tid; idx < B * D; idx += NT) {
+        const int j = idx / D, cc = idx % D;
+        float a = 0.f, bk = 0.f;
+        for (int i = 0; i < B; ++i) {
+          a += sP[i * BS + j] * sdO[i * DS + cc];
+          bk += sdS[i * BS + j] * sZ[i * DS + cc];
+        }
+        sV[idx] = a;
+        sK[idx] = g.scale * bk;
+      }
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::bulk_reduce_add_f32(dvacc + crow * D, sV, B * D * 4);
+        tc::bulk_reduce_add_f32(dkr + crow * D, sK, B * D * 4);
+        tc::bulk_commit();
+      }
+      if (c > 0) {  // dF_c += G_{b,c-1}^T Z_{b,c}, rows 32 q .. 32 q + 31 per piece
         float* dfc = dfacc + ((size_t)bh * g.nc + c) * D * D;
-        for (int idx = tid; idx < D * D; idx += NT) {
-          const int nn = idx / D, cc = idx % D;
-          float a = 0.f;
-          for (int i = 0; i < B; ++i) a += sG[i * DS + nn] * sZ[i * DS + cc];
-          atomicAdd(dfc + idx, a);
+        for (int q = 0; q < D / 32; ++q) {
+          float* buf = (q & 1) ? sK : sV;
+          if (tid == 0) tc::bulk_wait_read0();  // every earlier reduction has read its buffer
+          __syncthreads();
+          for (int idx = tid; idx < 32 * D; idx += NT) {
+            const int nn = 32 * q + idx / D, cc = idx % D;
+            float a = 0.f;
+            for (int i = 0; i < B; ++i) a += sG[i * DS + nn] * sZ[i * DS + cc];
+            buf[idx] = a;
+          }
+          tc::fence_proxy_async_smem();
+          __syncthreads();
+          if (tid == 0) {
+            tc::bulk_reduce_add_f32(dfc + (size_t)32 * q * D, buf, 32 * D * 4);
+            tc::bulk_commit();
+          }
         }
       }
+      if (tid == 0) tc::bulk_wait_read0();  // K and V are reloaded next step
       __syncthreads();
       float* t = sG; sG = sGn; sGn = t;
     }
@@ -240,6 +266,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     if (FOX && tid < B) atomicAdd(fxcs + brow + tid, -fox_rowsum);
     __syncthreads();
   }
+  if (tid == 0) tc::bulk_wait0();  // the reductions are complete before the CTA exits
 }
 
 template <int B, int D>
