@@ -302,13 +302,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         softmax_sync();
         const float mnew = fmaxf(m, fmaxf(s.xm[0][r], s.xm[1][r]));
         softmax_sync();
-        if (mnew > m + kTau) {
+        // the TMEM loads and stores of O are warp-wide instructions: a warp with any row to
+        // rescale rescales all 32 of its rows, by 1 where the reference stays
+        const bool resc = mnew > m + kTau;
+        if (__any_sync(0xffffffffu, resc)) {
           // O holds P(n-1) V(n-1) only once that MMA has completed
           if (n > 0) ok = ok && mbar_wait(&s.pv_done, (n - 1) & 1, p.err, 8);
           tc_fence_after();
-          const float corr = fast_exp2(m - mnew);
-          m = mnew;
-          l *= corr;
+          const float corr = resc ? fast_exp2(m - mnew) : 1.f;
+          if (resc) {
+            m = mnew;
+            l *= corr;
+          }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             uint32_t ob[32];
