@@ -927,7 +927,7 @@ def run_head_dim_128(args, pa, dev, pk):
                                               "tcgen05 (chunk 64)"}
         del x, wsf, o2, lse
         torch.cuda.empty_cache()
-    # ---- training step (tensor-core forward, fp32 CUDA-core backward) ----
+    # ---- training step (tcgen05 forward; backward on TF32 warp MMAs with fp32 accumulation) ----
     Bt, H, L, B = 4, 16, 2048, 32
     x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=g) * sd).to(torch.bfloat16) for n in ("q", "k", "v")}
     x["w"] = unit(Bt, H, L, d)
@@ -957,13 +957,15 @@ def run_head_dim_128(args, pa, dev, pk):
     ffl, bfl = Bt * H * fwd_flops_per_head(L, d, TC_CHUNK), Bt * H * bwd_flops_per_head(L, d, B)
     clk = pk.get("sm_max_mhz", 2070.0)
     fp32_peak = 152 * 128 * 2 * clk * 1e6 / 1e12
+    tf32_peak = pk["bf16"] * 1.1 / 2.25
     btf = bfl / (bms * 1e-3) / 1e12
     train = {"ms_per_step": tms, "tflops": (ffl + bfl) / (tms * 1e-3) / 1e12, "flops_per_step": ffl + bfl,
-             "backward": {"ms": bms, "tflops": btf, "bound": "alu", "peak": fp32_peak, "unit": "TFLOP/s",
-                          "frac": btf / fp32_peak, "chunk": B,
-                          "peak_source": f"FP32 FMA: 152 SMs x 128 lanes x 2 flop x {clk:.0f} MHz"},
+             "backward": {"ms": bms, "tflops": btf, "bound": "tensor", "peak": tf32_peak, "unit": "TFLOP/s",
+                          "frac": btf / tf32_peak, "chunk": B,
+                          "peak_source": f"tf32 dense: measured bf16 {pk['bf16']:.1f} x nominal tf32/bf16 (1.1/2.25)",
+                          "fp32_fma_peak": fp32_peak, "frac_of_fp32_fma_peak": btf / fp32_peak},
              "workload": "fwd+bwd, batch 4, 16 heads, d=128, L=2048, bf16 inputs: tcgen05 forward (chunk 64), "
-                         "fp32 CUDA-core backward (chunk 32)"}
+                         "backward (chunk 32) on TF32 warp MMAs (mma.sync, fp32 accumulation)"}
     return {"decode": decode, "forward": fwd, "train": train}
 
 

@@ -85,10 +85,14 @@ unsigned dot_blocks(const Geom& g) {
   return (unsigned)((rows + rows_per_block - 1) / rows_per_block);
 }
 
-template <int B, int D>
+// Row strides padded for the products' operand reads: + 4 floats (stride = 4 mod 32 banks) for
+// the TF32 warp MMAs, whose fragment loads then hit 32 distinct banks in either operand
+// orientation; + 1 for the plain fp32 loops, whose threads walk a row or a column.
+template <int B, int D, bool TC>
 struct BwdMainSmem {
-  static constexpr int DS = D + 1;
-  static constexpr int BS = B + 1;
+  static constexpr int PAD = TC ? 4 : 1;
+  static constexpr int DS = D + PAD;
+  static constexpr int BS = B + PAD;
   static constexpr int kZ = 0, kK = kZ + B * DS, kV = kK + B * DS, kF = kV + B * DS;
   static constexpr int kdO = kF + D * DS, kG = kdO + B * DS, kGn = kG + B * DS;
   static constexpr int kP = kGn + B * DS, kdS = kP + B * BS, kLse = kdS + B * BS, kDv = kLse + B;
@@ -106,7 +110,9 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     float* __restrict__ dvacc, float* __restrict__ dfacc, float* __restrict__ zs,
     const float* __restrict__ fxa, float* __restrict__ fxcs) {
   extern __shared__ float sm[];
-  using S = BwdMainSmem<B, D>;
+  // bf16 inputs: the products run as TF32 warp MMAs (fp32 accumulation); fp32 inputs: plain fp32
+  constexpr bool TC = std::is_same<T, __nv_bfloat16>::value;
+  using S = BwdMainSmem<B, D, TC>;
   constexpr int BS = S::BS, DS = S::DS;
   float* sZ = sm + S::kZ;
   float* sK = sm + S::kK;
@@ -143,12 +149,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
       for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
       __syncthreads();
-      for (int idx = tid; idx < B * D; idx += NT) {
-        const int i = idx / D, nn = idx % D;
-        float a = 0.f;
-        for (int kk = 0; kk < D; ++kk) a += sZ[i * DS + kk] * sF[nn * DS + kk];
-        sGn[i * DS + nn] = a;
-      }
+      smem_mm<B, D, D, false, true, TC>(sZ, DS, sF, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] = x; });
       __syncthreads();
       for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = sGn[(idx / D) * DS + idx % D];
       __syncthreads();
@@ -182,18 +183,14 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       if constexpr (FOX)
         for (int j = tid; j < B; j += NT) sAk[j] = fxa[crow + j] * kLog2e;
       __syncthreads();
-      // P and dS
-      for (int idx = tid; idx < B * B; idx += NT) {
-        const int i = idx / B, j = idx % B;
-        float s = 0.f, dp = 0.f;
-        for (int kk = 0; kk < D; ++kk) {
-          s += sZ[i * DS + kk] * sK[j * DS + kk];
-          dp += sdO[i * DS + kk] * sV[j * DS + kk];
-        }
-        const float p = fast_exp2(s * scl2 - sLse[i] - (FOX ? sAk[j] : 0.f));
-        sP[i * BS + j] = p;
-        sdS[i * BS + j] = p * (dp - sDv[i]);
-      }
+      // P and dS (the two products share their output mapping: the thread that writes P(i, j)
+      // reads it back)
+      smem_mm<B, B, D, false, true, TC>(sZ, DS, sK, DS, [&](int i, int j, float x) {
+        sP[i * BS + j] = fast_exp2(x * scl2 - sLse[i] - (FOX ? sAk[j] : 0.f));
+      });
+      smem_mm<B, B, D, false, true, TC>(sdO, DS, sV, DS, [&](int i, int j, float x) {
+        sdS[i * BS + j] = sP[i * BS + j] * (x - sDv[i]);
+      });
       __syncthreads();
       if constexpr (FOX) {  // dS' row sums kept per thread; column sums of key chunk c into fxcs
         if (tid < B) {
@@ -211,26 +208,12 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       // G_{b,c-1}^T Z_{b,c} in 32-row pieces through the same two buffers.  One thread issues the
       // reductions; it waits for a buffer's previous reduction to have read it before the buffer
       // is written again.
-      for (int idx = tid; idx < B * D; idx += NT) {
-        const int i = idx / D, nn = idx % D;
-        float a = 0.f;
-        for (int j = 0; j < B; ++j) a += sdS[i * BS + j] * sK[j * DS + nn];
-        a *= g.scale;
-        if (c > 0)
-          for (int kk = 0; kk < D; ++kk) a += sG[i * DS + kk] * sF[kk * DS + nn];
-        sGn[i * DS + nn] = a;
-      }
+      smem_mm<B, D, B, false, false, TC>(sdS, BS, sK, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] = g.scale * x; });
+      if (c > 0)
+        smem_mm<B, D, D, false, false, TC>(sG, DS, sF, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] += x; });
       __syncthreads();  // K and V are dead
-      for (int idx = tid; idx < B * D; idx += NT) {
-        const int j = idx / D, cc = idx % D;
-        float a = 0.f, bk = 0.f;
-        for (int i = 0; i < B; ++i) {
-          a += sP[i * BS + j] * sdO[i * DS + cc];
-          bk += sdS[i * BS + j] * sZ[i * DS + cc];
-        }
-        sV[idx] = a;
-        sK[idx] = g.scale * bk;
-      }
+      smem_mm<B, D, B, true, false, TC>(sP, BS, sdO, DS, [&](int j, int cc, float x) { sV[j * D + cc] = x; });
+      smem_mm<B, D, B, true, false, TC>(sdS, BS, sZ, DS, [&](int j, int cc, float x) { sK[j * D + cc] = g.scale * x; });
       tc::fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {
@@ -244,12 +227,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
           float* buf = (q & 1) ? sK : sV;
           if (tid == 0) tc::bulk_wait_read0();  // every earlier reduction has read its buffer
           __syncthreads();
-          for (int idx = tid; idx < 32 * D; idx += NT) {
-            const int nn = 32 * q + idx / D, cc = idx % D;
-            float a = 0.f;
-            for (int i = 0; i < B; ++i) a += sG[i * DS + nn] * sZ[i * DS + cc];
-            buf[idx] = a;
-          }
+          smem_mm<32, D, B, true, false, TC>(sG + 32 * q, DS, sZ, DS, [&](int r, int cc, float x) { buf[r * D + cc] = x; });
           tc::fence_proxy_async_smem();
           __syncthreads();
           if (tid == 0) {
@@ -542,7 +520,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
   }
   if (phases & 2) {
     auto kern = logf ? bwd_main_simt_kernel<T, B, true, D> : bwd_main_simt_kernel<T, B, false, D>;
-    const size_t smem = BwdMainSmem<B, D>::bytes;
+    const size_t smem = BwdMainSmem<B, D, std::is_same<T, __nv_bfloat16>::value>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<lay.nctas, NT, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
                                       (const float*)(ws + lay.fw.ql), (const float*)(ws + lay.fw.kr),
