@@ -88,18 +88,45 @@ unsigned dot_blocks(const Geom& g) {
 // Row strides padded for the products' operand reads: + 4 floats (stride = 4 mod 32 banks) for
 // the TF32 warp MMAs, whose fragment loads then hit 32 distinct banks in either operand
 // orientation; + 1 for the plain fp32 loops, whose threads walk a row or a column.
+// K, V, dO and G are adjacent: the Z-chain pass, in which all four are dead, holds its second F
+// buffer there.  With the TF32 padding every buffer starts on a 16-byte boundary and every row
+// is 16-byte aligned, so the fp32 operands arrive by asynchronous 16-byte copies.
 template <int B, int D, bool TC>
 struct BwdMainSmem {
   static constexpr int PAD = TC ? 4 : 1;
   static constexpr int DS = D + PAD;
   static constexpr int BS = B + PAD;
-  static constexpr int kZ = 0, kK = kZ + B * DS, kV = kK + B * DS, kF = kV + B * DS;
-  static constexpr int kdO = kF + D * DS, kG = kdO + B * DS, kGn = kG + B * DS;
+  static constexpr int kZ = 0, kF = kZ + B * DS, kK = kF + D * DS, kV = kK + B * DS;
+  static constexpr int kdO = kV + B * DS, kG = kdO + B * DS, kGn = kG + B * DS;
   static constexpr int kP = kGn + B * DS, kdS = kP + B * BS, kLse = kdS + B * BS, kDv = kLse + B;
   static constexpr int kAk = kDv + B;  // PaTH-FoX: A_j log2(e) of the key chunk
   static constexpr int total = kAk + B;
   static constexpr size_t bytes = (size_t)total * 4;
+  static_assert(D * DS <= kGn - kK, "the second F buffer fits over K, V, dO and G");
+  static_assert(!TC || (DS % 4 == 0 && BS % 4 == 0), "16-byte aligned rows");
 };
+
+// A 16-byte global -> shared copy that bypasses the registers; cp_async_wait_all() waits for the
+// calling thread's copies (a barrier then publishes them to the block).
+__device__ __forceinline__ void cp_async16(float* sdst, const float* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// `rows` fp32 rows of D (global row stride D) into shared rows of stride DS: asynchronous 16-byte
+// copies (ASYNC, 16-byte aligned rows) or plain loads and stores.
+template <int D, int DS, bool ASYNC>
+__device__ __forceinline__ void load_rows(float* dst, const float* src, int rows, int tid) {
+  if constexpr (ASYNC) {
+    constexpr int Q = D / 4;
+    for (int idx = tid; idx < rows * Q; idx += NT) {
+      const int r = idx / Q, q = idx % Q;
+      cp_async16(dst + r * DS + 4 * q, src + (size_t)r * D + 4 * q);
+    }
+  } else {
+    for (int idx = tid; idx < rows * D; idx += NT) dst[(idx / D) * DS + idx % D] = src[idx];
+  }
+}
 
 // Persistent CTAs; tile n (heaviest first) is query chunk b = nc-1 - n/BH of head n%BH.
 template <typename T, int B, bool FOX, int D>
@@ -140,19 +167,32 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = 0.f;
       continue;
     }
-    // ---- pass 1: Z_{b,c} for c = b-1 .. 0, stored in this CTA's scratch slab ----
-    for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = ql[brow * D + idx];
-    __syncthreads();
-    for (int c = b - 1; c >= 0; --c) {
-      for (int idx = tid; idx < B * D; idx += NT) myz[(size_t)c * B * D + idx] = sZ[(idx / D) * DS + idx % D];
-      if (c == 0) break;
-      const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
-      for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
+    // ---- pass 1: Z_{b,c} for c = b-1 .. 0, stored in this CTA's scratch slab; F_{c-1} arrives
+    // during the product with F_c (two F buffers), the two Z buffers alternate ----
+    {
+      float* za = sm + S::kZ;   // Z_{b,c}
+      float* zb = sm + S::kGn;  // Z_{b,c-1}
+      float* fa = sm + S::kF;  // F_c
+      float* fn = sm + S::kK;  // F_{c-1}
+      load_rows<D, DS, TC>(za, ql + brow * D, B, tid);
+      if (b >= 2) load_rows<D, DS, TC>(fa, f + ((size_t)bh * g.nc + (b - 1)) * D * D, D, tid);
+      if constexpr (TC) cp_async_wait_all();
       __syncthreads();
-      smem_mm<B, D, D, false, true, TC>(sZ, DS, sF, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] = x; });
-      __syncthreads();
-      for (int idx = tid; idx < B * D; idx += NT) sZ[(idx / D) * DS + idx % D] = sGn[(idx / D) * DS + idx % D];
-      __syncthreads();
+      for (int c = b - 1; c >= 0; --c) {
+        for (int idx = tid; idx < B * D; idx += NT) myz[(size_t)c * B * D + idx] = za[(idx / D) * DS + idx % D];
+        if (c == 0) break;
+        if (c >= 2) load_rows<D, DS, TC>(fn, f + ((size_t)bh * g.nc + (c - 1)) * D * D, D, tid);
+        smem_mm<B, D, D, false, true, TC>(za, DS, fa, DS, [&](int i, int nn, float x) { zb[i * DS + nn] = x; });
+        if constexpr (TC) cp_async_wait_all();
+        __syncthreads();
+        float* t = za;
+        za = zb;
+        zb = t;
+        t = fa;
+        fa = fn;
+        fn = t;
+      }
+      __syncthreads();  // the last Z has been stored before its buffer (possibly G's) is reused
     }
     // ---- pass 2: ascending adjoint scan ----
     for (int idx = tid; idx < B * D; idx += NT) {
@@ -169,19 +209,31 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     }
     float fox_rowsum = 0.f;  // PaTH-FoX: row tid's sum of dS' over the off-diagonal key chunks
     __syncthreads();  // also orders pass-1 scratch writes before the reads below
+    // F_c (read by step c > 0 only) is fetched during step c - 1, once that step's G product has
+    // read F_{c-1}; Z_c and K_c are fetched at the step's start (their buffers serve until the
+    // previous step's end)
     for (int c = 0; c < b; ++c) {
       const size_t crow = (size_t)bh * g.Lp + (size_t)c * B;
-      const size_t vrow = (size_t)bh * g.L + (size_t)c * B;
-      for (int idx = tid; idx < B * D; idx += NT) {
-        const int r = idx / D, cc = idx % D;
-        sZ[r * DS + cc] = myz[(size_t)c * B * D + idx];
-        sK[r * DS + cc] = kr[crow * D + idx];
-        sV[r * DS + cc] = to_f(v[vrow * D + idx]);
+      const size_t vrow = (size_t)bh * g.L + (size_t)c * B;  // rows of chunk c < b are all < L
+      load_rows<D, DS, TC>(sZ, myz + (size_t)c * B * D, B, tid);
+      load_rows<D, DS, TC>(sK, kr + crow * D, B, tid);
+      if constexpr (TC) {  // bf16 V: 8 values per 16-byte load (tensor pointers are 16-byte aligned)
+        for (int idx = tid; idx < B * D / 8; idx += NT) {
+          const int r = idx / (D / 8), q = idx % (D / 8);
+          const uint4 u = *reinterpret_cast<const uint4*>(v + (vrow + r) * D + 8 * q);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+          const float2 a0 = __bfloat1622float2(h2[0]), a1 = __bfloat1622float2(h2[1]);
+          const float2 a2 = __bfloat1622float2(h2[2]), a3 = __bfloat1622float2(h2[3]);
+          float4* dst = reinterpret_cast<float4*>(sV + r * DS + 8 * q);
+          dst[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+          dst[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+        }
+      } else {
+        for (int idx = tid; idx < B * D; idx += NT) sV[(idx / D) * DS + idx % D] = to_f(v[vrow * D + idx]);
       }
-      const float* fc = f + ((size_t)bh * g.nc + c) * D * D;
-      for (int idx = tid; idx < D * D; idx += NT) sF[(idx / D) * DS + idx % D] = fc[idx];
       if constexpr (FOX)
         for (int j = tid; j < B; j += NT) sAk[j] = fxa[crow + j] * kLog2e;
+      if constexpr (TC) cp_async_wait_all();
       __syncthreads();
       // P and dS (the two products share their output mapping: the thread that writes P(i, j)
       // reads it back)
@@ -211,7 +263,8 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       smem_mm<B, D, B, false, false, TC>(sdS, BS, sK, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] = g.scale * x; });
       if (c > 0)
         smem_mm<B, D, D, false, false, TC>(sG, DS, sF, DS, [&](int i, int nn, float x) { sGn[i * DS + nn] += x; });
-      __syncthreads();  // K and V are dead
+      __syncthreads();  // K, V and F are dead
+      if (c + 1 < b) load_rows<D, DS, TC>(sF, f + ((size_t)bh * g.nc + c + 1) * D * D, D, tid);
       smem_mm<B, D, B, true, false, TC>(sP, BS, sdO, DS, [&](int j, int cc, float x) { sV[j * D + cc] = x; });
       smem_mm<B, D, B, true, false, TC>(sdS, BS, sZ, DS, [&](int j, int cc, float x) { sK[j * D + cc] = g.scale * x; });
       tc::fence_proxy_async_smem();

@@ -35,20 +35,27 @@ __device__ __forceinline__ void smem_mm(const float* A, int lda, const float* B,
   auto LB = [&](int k, int j) { return TB ? B[j * ldb + k] : B[k * ldb + j]; };
   const int tid = threadIdx.x;
   if constexpr (TC) {
-    static_assert(M % 16 == 0 && N % 8 == 0 && K % 8 == 0, "tile shape");
+    static_assert(M % 16 == 0 && N % 8 == 0 && K % 16 == 0, "tile shape");
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int nwarps = blockDim.x >> 5;
     constexpr int TN = N / 8, NT = (M / 16) * TN;
     for (int tile = warp; tile < NT; tile += nwarps) {
       const int i0 = (tile / TN) * 16, j0 = (tile % TN) * 8;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int k0 = 0; k0 < K; k0 += 8) {
+      // two accumulators over alternate 8-wide K slices: two independent MMA chains
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+      for (int k0 = 0; k0 < K; k0 += 16) {
         const uint32_t a[4] = {to_tf32(LA(i0 + g, k0 + t)), to_tf32(LA(i0 + g + 8, k0 + t)),
                                to_tf32(LA(i0 + g, k0 + t + 4)), to_tf32(LA(i0 + g + 8, k0 + t + 4))};
         const uint32_t b[2] = {to_tf32(LB(k0 + t, j0 + g)), to_tf32(LB(k0 + t + 4, j0 + g))};
+        const uint32_t a2[4] = {to_tf32(LA(i0 + g, k0 + 8 + t)), to_tf32(LA(i0 + g + 8, k0 + 8 + t)),
+                                to_tf32(LA(i0 + g, k0 + 12 + t)), to_tf32(LA(i0 + g + 8, k0 + 12 + t))};
+        const uint32_t b2[2] = {to_tf32(LB(k0 + 8 + t, j0 + g)), to_tf32(LB(k0 + 12 + t, j0 + g))};
         mma_m16n8k8_tf32(c, a, b);
+        mma_m16n8k8_tf32(c2, a2, b2);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] += c2[e];
       epi(i0 + g, j0 + 2 * t, c[0]);
       epi(i0 + g, j0 + 2 * t + 1, c[1]);
       epi(i0 + g + 8, j0 + 2 * t, c[2]);
