@@ -38,6 +38,46 @@ __device__ __forceinline__ void smem_mm(const float* A, int lda, const float* B,
     static_assert(M % 16 == 0 && N % 8 == 0 && K % 16 == 0, "tile shape");
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int nwarps = blockDim.x >> 5;
+    // Products with at least eight 16 x 16 tiles give each warp 16 x 16 tiles: one A fragment
+    // serves two MMAs, and two N halves x two K parities make four independent chains.
+    constexpr bool WIDE = N % 16 == 0 && (M / 16) * (N / 16) >= 8;
+    if constexpr (WIDE) {
+      constexpr int TN = N / 16, NTW = (M / 16) * TN;
+      for (int tile = warp; tile < NTW; tile += nwarps) {
+        const int i0 = (tile / TN) * 16, j0 = (tile % TN) * 16;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 16) {
+          const uint32_t a[4] = {to_tf32(LA(i0 + g, k0 + t)), to_tf32(LA(i0 + g + 8, k0 + t)),
+                                 to_tf32(LA(i0 + g, k0 + t + 4)), to_tf32(LA(i0 + g + 8, k0 + t + 4))};
+          const uint32_t b0[2] = {to_tf32(LB(k0 + t, j0 + g)), to_tf32(LB(k0 + t + 4, j0 + g))};
+          const uint32_t b1[2] = {to_tf32(LB(k0 + t, j0 + 8 + g)), to_tf32(LB(k0 + t + 4, j0 + 8 + g))};
+          const uint32_t a2[4] = {to_tf32(LA(i0 + g, k0 + 8 + t)), to_tf32(LA(i0 + g + 8, k0 + 8 + t)),
+                                  to_tf32(LA(i0 + g, k0 + 12 + t)), to_tf32(LA(i0 + g + 8, k0 + 12 + t))};
+          const uint32_t e0[2] = {to_tf32(LB(k0 + 8 + t, j0 + g)), to_tf32(LB(k0 + 12 + t, j0 + g))};
+          const uint32_t e1[2] = {to_tf32(LB(k0 + 8 + t, j0 + 8 + g)), to_tf32(LB(k0 + 12 + t, j0 + 8 + g))};
+          mma_m16n8k8_tf32(c0, a, b0);
+          mma_m16n8k8_tf32(c1, a, b1);
+          mma_m16n8k8_tf32(d0, a2, e0);
+          mma_m16n8k8_tf32(d1, a2, e1);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          c0[e] += d0[e];
+          c1[e] += d1[e];
+        }
+        epi(i0 + g, j0 + 2 * t, c0[0]);
+        epi(i0 + g, j0 + 2 * t + 1, c0[1]);
+        epi(i0 + g + 8, j0 + 2 * t, c0[2]);
+        epi(i0 + g + 8, j0 + 2 * t + 1, c0[3]);
+        epi(i0 + g, j0 + 8 + 2 * t, c1[0]);
+        epi(i0 + g, j0 + 8 + 2 * t + 1, c1[1]);
+        epi(i0 + g + 8, j0 + 8 + 2 * t, c1[2]);
+        epi(i0 + g + 8, j0 + 8 + 2 * t + 1, c1[3]);
+      }
+      return;
+    }
     constexpr int TN = N / 8, NT = (M / 16) * TN;
     for (int tile = warp; tile < NT; tile += nwarps) {
       const int i0 = (tile / TN) * 16, j0 = (tile % TN) * 8;
