@@ -22,6 +22,7 @@ namespace pathattn {
 namespace {
 
 constexpr int NT = 256;
+constexpr int NTM = 512;  // threads of the backward scan (one CTA per SM: 16 warps hide the latencies)
 // D (template parameter): head dim, 64 or 128; DS = D + 1 is the padded smem row stride.
 
 // D_i = dO_i . o_i; padded rows get 0.  A row is read by a group of D / VEC lanes with 16-byte
@@ -119,18 +120,18 @@ template <int D, int DS, bool ASYNC>
 __device__ __forceinline__ void load_rows(float* dst, const float* src, int rows, int tid) {
   if constexpr (ASYNC) {
     constexpr int Q = D / 4;
-    for (int idx = tid; idx < rows * Q; idx += NT) {
+    for (int idx = tid; idx < rows * Q; idx += NTM) {
       const int r = idx / Q, q = idx % Q;
       cp_async16(dst + r * DS + 4 * q, src + (size_t)r * D + 4 * q);
     }
   } else {
-    for (int idx = tid; idx < rows * D; idx += NT) dst[(idx / D) * DS + idx % D] = src[idx];
+    for (int idx = tid; idx < rows * D; idx += NTM) dst[(idx / D) * DS + idx % D] = src[idx];
   }
 }
 
 // Persistent CTAs; tile n (heaviest first) is query chunk b = nc-1 - n/BH of head n%BH.
 template <typename T, int B, bool FOX, int D>
-__global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
+__global__ void __launch_bounds__(NTM, 1) bwd_main_simt_kernel(
     Geom g, const T* __restrict__ v, const float* __restrict__ lse, const T* __restrict__ dO,
     const float* __restrict__ Dv, const float* __restrict__ ql, const float* __restrict__ kr,
     const float* __restrict__ f, float* __restrict__ dql, float* __restrict__ dkr,
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
     const int bh = (int)(n % g.BH);
     const size_t brow = (size_t)bh * g.Lp + (size_t)b * B;
     if (b == 0) {
-      for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = 0.f;
+      for (int idx = tid; idx < B * D; idx += NTM) dql[brow * D + idx] = 0.f;
       continue;
     }
     // ---- pass 1: Z_{b,c} for c = b-1 .. 0, stored in this CTA's scratch slab; F_{c-1} arrives
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       if constexpr (TC) cp_async_wait_all();
       __syncthreads();
       for (int c = b - 1; c >= 0; --c) {
-        for (int idx = tid; idx < B * D; idx += NT) myz[(size_t)c * B * D + idx] = za[(idx / D) * DS + idx % D];
+        for (int idx = tid; idx < B * D; idx += NTM) myz[(size_t)c * B * D + idx] = za[(idx / D) * DS + idx % D];
         if (c == 0) break;
         if (c >= 2) load_rows<D, DS, TC>(fn, f + ((size_t)bh * g.nc + (c - 1)) * D * D, D, tid);
         smem_mm<B, D, D, false, true, TC>(za, DS, fa, DS, [&](int i, int nn, float x) { zb[i * DS + nn] = x; });
@@ -195,12 +196,12 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       __syncthreads();  // the last Z has been stored before its buffer (possibly G's) is reused
     }
     // ---- pass 2: ascending adjoint scan ----
-    for (int idx = tid; idx < B * D; idx += NT) {
+    for (int idx = tid; idx < B * D; idx += NTM) {
       const int i = idx / D, cc = idx % D, gi = b * B + i;
       sdO[i * DS + cc] = gi < g.L ? to_f(dO[((size_t)bh * g.L + gi) * D + cc]) : 0.f;
       sG[i * DS + cc] = 0.f;
     }
-    for (int i = tid; i < B; i += NT) {
+    for (int i = tid; i < B; i += NTM) {
       const int gi = b * B + i;
       float l2 = gi < g.L ? lse[(size_t)bh * g.L + gi] * kLog2e : INFINITY;  // padded rows: P = 0
       if constexpr (FOX) l2 = fmaf(-fxa[brow + i], kLog2e, l2);                 // the + A_i of the bias
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       load_rows<D, DS, TC>(sZ, myz + (size_t)c * B * D, B, tid);
       load_rows<D, DS, TC>(sK, kr + crow * D, B, tid);
       if constexpr (TC) {  // bf16 V: 8 values per 16-byte load (tensor pointers are 16-byte aligned)
-        for (int idx = tid; idx < B * D / 8; idx += NT) {
+        for (int idx = tid; idx < B * D / 8; idx += NTM) {
           const int r = idx / (D / 8), q = idx % (D / 8);
           const uint4 u = *reinterpret_cast<const uint4*>(v + (vrow + r) * D + 8 * q);
           const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -229,10 +230,10 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
           dst[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
         }
       } else {
-        for (int idx = tid; idx < B * D; idx += NT) sV[(idx / D) * DS + idx % D] = to_f(v[vrow * D + idx]);
+        for (int idx = tid; idx < B * D; idx += NTM) sV[(idx / D) * DS + idx % D] = to_f(v[vrow * D + idx]);
       }
       if constexpr (FOX)
-        for (int j = tid; j < B; j += NT) sAk[j] = fxa[crow + j] * kLog2e;
+        for (int j = tid; j < B; j += NTM) sAk[j] = fxa[crow + j] * kLog2e;
       if constexpr (TC) cp_async_wait_all();
       __syncthreads();
       // P and dS (the two products share their output mapping: the thread that writes P(i, j)
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(NT) bwd_main_simt_kernel(
       __syncthreads();
       float* t = sG; sG = sGn; sGn = t;
     }
-    for (int idx = tid; idx < B * D; idx += NT) dql[brow * D + idx] = sG[(idx / D) * DS + idx % D];
+    for (int idx = tid; idx < B * D; idx += NTM) dql[brow * D + idx] = sG[(idx / D) * DS + idx % D];
     if (FOX && tid < B) atomicAdd(fxcs + brow + tid, -fox_rowsum);
     __syncthreads();
   }
@@ -575,7 +576,7 @@ cudaError_t bwd_t(const Geom& g, const void* q, const void* k, const void* v, co
     auto kern = logf ? bwd_main_simt_kernel<T, B, true, D> : bwd_main_simt_kernel<T, B, false, D>;
     const size_t smem = BwdMainSmem<B, D, std::is_same<T, __nv_bfloat16>::value>::bytes;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-    kern<<<lay.nctas, NT, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
+    kern<<<lay.nctas, NTM, smem, st>>>(g, (const T*)v, lse, (const T*)dO, (const float*)(ws + lay.Dv),
                                       (const float*)(ws + lay.fw.ql), (const float*)(ws + lay.fw.kr),
                                       (const float*)(ws + lay.fw.f), (float*)(ws + lay.dql),
                                       (float*)(ws + lay.dkr), (float*)(ws + lay.dv), (float*)(ws + lay.df),
