@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
                                                         const ZcParams p) {
   extern __shared__ uint8_t smem_raw[];
   ZcSmem& s = *reinterpret_cast<ZcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int err0 = threadIdx.x == 0 ? peek_err(p.err) : 0;  // consumed at the setup barrier
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bh, T;
   tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
@@ -80,9 +81,14 @@ __global__ void __launch_bounds__(160) zchain_tc_kernel(const __grid_constant__ 
   }
   if (warp == 4) tmem_alloc(&s.tmem_base, 64);
   tc_fence_before();
-  __syncthreads();
+  // a wait of an earlier CTA of the launch has given up: end at once (the pipeline is broken)
+  const bool launch_err = __syncthreads_or(err0 != 0) != 0;
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
+  if (launch_err) {
+    if (warp == 4) tmem_dealloc(tb, 64);
+    return;
+  }
 
   if (warp == 4) {
     if (lane == 0) {
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
                                                             const BsParams p) {
   extern __shared__ uint8_t smem_raw[];
   BsSmem& s = *reinterpret_cast<BsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int err0 = threadIdx.x == 0 ? peek_err(p.err) : 0;  // consumed at the setup barrier
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bh, T;
   tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
@@ -337,9 +344,14 @@ __global__ void __launch_bounds__(BS_THREADS, 1) bwd_scan_tc_kernel(const __grid
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, 512);
   tc_fence_before();
-  __syncthreads();
+  // a wait of an earlier CTA of the launch has given up: end at once (the pipeline is broken)
+  const bool launch_err = __syncthreads_or(err0 != 0) != 0;
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
+  if (launch_err) {
+    if (warp == 5) tmem_dealloc(tb, 512);
+    return;
+  }
 
   if (warp == 4) {
     // ---------------- producers ----------------

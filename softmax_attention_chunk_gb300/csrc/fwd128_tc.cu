@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                           const Scan128Params p) {
   extern __shared__ uint8_t smem_raw[];
   Scan128Smem& s = *reinterpret_cast<Scan128Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int err0 = threadIdx.x == 0 ? peek_err(p.err) : 0;  // consumed at the setup barrier
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bh, T;
   tile_of_block((int)blockIdx.x, p.ntiles, p.BH, bh, T);
@@ -104,9 +105,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   if (warp == 9) tmem_alloc(&s.tmem_base, TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  // a wait of an earlier CTA of the launch has given up: end at once (the pipeline is broken)
+  const bool launch_err = __syncthreads_or(err0 != 0) != 0;
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
+  if (launch_err) {
+    if (warp == 9) tmem_dealloc(tb, TMEM_COLS);
+    return;
+  }
 
   if (warp == 8) {
     // ---------------- TMA producer ----------------

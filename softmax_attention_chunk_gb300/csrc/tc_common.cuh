@@ -59,6 +59,39 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, int
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   return mbar_wait_ns(bar, parity, err, code, 2000000000ull);
 }
+// Whether a wait of this launch (or of an earlier launch on the same workspace) has given up.  A
+// CTA of a kernel with few waves calls it first thing and returns when it holds.  Thread 0
+// reads, the block agrees (through the barrier's reduction: no shared memory).
+__device__ __forceinline__ bool launch_failed(const int* err) {
+  return __syncthreads_or(threadIdx.x == 0 && err && *reinterpret_cast<const volatile int*>(err) != 0) != 0;
+}
+// The error word as it stands, read without waiting for it: a kernel issues this load first and
+// consumes the value at its setup barrier, so that the load's latency overlaps the setup.
+__device__ __forceinline__ int peek_err(const int* err) {
+  return err ? *reinterpret_cast<const volatile int*>(err) : 0;
+}
+// The same wait with its polling loop out of line, for the per-chunk kernels at their register
+// cap (their wait sites keep only the first try_wait; the call falls on the slow path).  A wait
+// still open after 1 ms (healthy ones complete in microseconds) also watches the error word:
+// once another wait of the launch (or of an earlier launch on the same workspace) has given up,
+// the pipeline is broken and this one gives up too, so that a failed launch of these persistent
+// or many-CTA kernels ends after about 1 ms per remaining wait instead of 2 s.
+static __device__ __noinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, int* err, int code) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      const uint64_t dt = global_ns() - t0;
+      if (dt > 2000000000ull) break;
+      if (dt > 1000000ull && err && *reinterpret_cast<volatile int*>(err) != 0) return false;
+    }
+  }
+  if (err) atomicCAS(err, 0, code);
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_lean(uint64_t* bar, uint32_t parity, int* err, int code) {
+  return mbar_try_wait(bar, parity) || mbar_wait_poll(bar, parity, err, code);
+}
 
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

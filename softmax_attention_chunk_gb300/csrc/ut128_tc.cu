@@ -73,7 +73,6 @@ struct __align__(1024) Ut128Smem {
   float beta[B], pre[B];
   uint64_t bar_in, bar_v, bar_mma;
   uint32_t tmem_base;
-  int stop;  // set once a wait of this CTA or of the launch has given up: the CTA leaves its loop
 };
 
 
@@ -104,21 +103,15 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tb = s.tmem_base;
   uint32_t mph = 0;  // phase of bar_mma
-  // After a wait of this thread has given up (code recorded in *err), its later waits are skipped,
-  // so that the chunk runs out without another 2 s per wait; at the chunk's end the CTA stops.
-  bool dead = false;
-  auto wait_bar = [&](uint64_t* bar, uint32_t parity, int code) {
-    if (!dead && !mbar_wait(bar, parity, p.err, code)) dead = true;
-  };
   auto issue = [&](auto fn) {  // lead issues one round's MMAs and commits them
-    if (lead && !dead) {
+    if (lead) {
       tc_fence_after();
       fn();
       mma_commit(&s.bar_mma);
     }
   };
   auto wait_mma = [&](int code) {
-    wait_bar(&s.bar_mma, mph, code);
+    mbar_wait_lean(&s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
   };
@@ -137,7 +130,7 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
     const int row0 = c * B;
     const size_t in_row = (size_t)bh * p.L;
     const size_t ws_row = (size_t)bh * p.Lp + row0;
-    if (lead && !dead) {
+    if (lead) {
       fence_proxy_async_smem();  // the previous chunk's reads of the slots come before the copies
       mbar_arrive_expect_tx(&s.bar_in, 7 * TILE);
       tma_load_3d(s.t[S_WA], &tm_w, 0, row0, bh, &s.bar_in);
@@ -165,7 +158,7 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
       s.pre[lane] = a;
       s.pre[32 + lane] = b2 + tot_a;
     }
-    wait_bar(&s.bar_in, it & 1, 31);
+    mbar_wait_lean(&s.bar_in, it & 1, p.err, 31);
     __syncthreads();
 
     // ---- P1: [G | N2] = W_a [W_a; K_a]^T + W_b [W_b; K_b]^T (two N=128 MMAs over adjacent slots) ----
@@ -243,7 +236,7 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
       mma64(tb + 128, ta(S_M1), 0, ta(S_X), 1, 1, /*neg_a=*/1);
     });
     wait_mma(35);
-    if (lead && !dead) {  // U has been read by R2's products: its slot takes V_a
+    if (lead) {  // U has been read by R2's products: its slot takes V_a
       mbar_arrive_expect_tx(&s.bar_v, TILE);
       tma_load_3d(s.t[S_VA], &tm_v, 0, row0, bh, &s.bar_v);
     }
@@ -337,7 +330,7 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
     __syncthreads();
 
     // ---- R5: P V_x -> acc ----
-    wait_bar(&s.bar_v, it & 1, 38);
+    mbar_wait_lean(&s.bar_v, it & 1, p.err, 38);
     issue([&] {
       mma64(tb + 0, ta(S_P), 0, ta(S_VA), 1, 0);
       mma64(tb + 64, ta(S_P), 0, ta(S_VB), 1, 0);
@@ -353,11 +346,9 @@ __global__ void __launch_bounds__(128, 2) ut_prep128_kernel(const __grid_constan
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
       }
     }
-    if (lead) s.stop = dead || *reinterpret_cast<volatile int*>(p.err) != 0;
     tc_fence_before();
     __syncthreads();  // TMEM and the slots are read out before the next chunk reuses them
     tc_fence_after();
-    if (s.stop) break;
   }
   if (warp == 1) tmem_dealloc(tb, TMEM_COLS);
 }

@@ -151,14 +151,14 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     }
   };
   auto wait_mma2 = [&](int code) {
-    mbar_wait(&s.bar_mma, mph, p.err, code);
-    mbar_wait(&s.bar_mma2, mph2, p.err, code);
+    mbar_wait_lean(&s.bar_mma, mph, p.err, code);
+    mbar_wait_lean(&s.bar_mma2, mph2, p.err, code);
     mph ^= 1;
     mph2 ^= 1;
     tc_fence_after();
   };
   auto wait_mma = [&](int code) {
-    mbar_wait(&s.bar_mma, mph, p.err, code);
+    mbar_wait_lean(&s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
   };
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
       s.pre[32 + lane] = b2 + tot_a;
     }
   }
-  mbar_wait(&s.bar_in, 0, p.err, 41);
+  mbar_wait_lean(&s.bar_in, 0, p.err, 41);
   publish();
 
   // ---- P2: G = W W^T, M1 = Q W^T, N2 = W K^T, Q K^T ----
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
     }
     RowsToTile<2> f;
     f.load(p.df + ((size_t)bh * p.nc + c) * D * D, B, warp - 2, lane);
-    mbar_wait(&s.bar_mma, mph, p.err, 52);  // dP has read V
+    mbar_wait_lean(&s.bar_mma, mph, p.err, 52);  // dP has read V
     f.store(s.t[S_DF], warp - 2, lane);
   }
   mph ^= 1;
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(128, 2) ut_bwd64_kernel(const __grid_constant_
   publish();
 
   // ---- P7: gQ = dS K + gM1 W ; E3 = M1^T dQ<- + W dF^T ; gN2 = U^T gX ; gW += gM1^T Q ----
-  if (lead || tid == 32) mbar_wait(&s.bar_in, 1, p.err, 46);  // both issuers read Q and K again
+  if (lead || tid == 32) mbar_wait_lean(&s.bar_in, 1, p.err, 46);  // both issuers read Q and K again
   issue2([&] {
     mma64(tb + C0, ta(S_DS), 0, ta(S_K2), 1, 0);
     mma64(tb + C0, ta(S_GM1), 0, ta(S_W), 1, 1);

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
     }
   };
   auto wait_mma = [&](int code) {
-    mbar_wait(&s.bar_mma, mph, p.err, code);
+    mbar_wait_lean(&s.bar_mma, mph, p.err, code);
     mph ^= 1;
     tc_fence_after();
   };
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
       s.pre[lane] = a;
       s.pre[32 + lane] = b2 + tot_a;
     }
-    mbar_wait(&s.bar_in, it & 1, p.err, 31);
+    mbar_wait_lean(&s.bar_in, it & 1, p.err, 31);
     __syncthreads();
 
     // ---- P1: [G | N2] = W [W; K]^T (one N=128 MMA: the w and k slots are adjacent) ----
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
         mma64(tb + 64, ta(S_N2), 1, ta(S_Q), 1, 1);
       });
       wait_mma(36);
-      if (lead && mbar_wait(&s.bar_v, it & 1, p.err, 37)) {
+      if (lead && mbar_wait_lean(&s.bar_v, it & 1, p.err, 37)) {
         tma_store_3d(&tm_vc, s.t[S_A], 0, row0, bh);
         bulk_commit();
       }
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(128, 3) ut_prep64_kernel(const __grid_constant
       __syncthreads();
 
       // ---- R4: W^T Y (+ W^T Y_lo) -> F = I - W^T Y; P V -> acc ----
-      if (diag) mbar_wait(&s.bar_v, it & 1, p.err, 37);
+      if (diag) mbar_wait_lean(&s.bar_v, it & 1, p.err, 37);
       issue([&] {
         mma64(tb + 0, ta(S_W), 1, ta(S_Y), 1, 0);
         if constexpr (F32) mma64(tb + 0, ta(S_W), 1, ta(S_YLO), 1, 1);

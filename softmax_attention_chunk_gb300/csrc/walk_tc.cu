@@ -65,6 +65,7 @@ template <bool ASC, bool OUT_F32>
 __device__ __forceinline__ void walk_head(const CUtensorMap& tm_x, const WalkParams& p, int bh) {
   extern __shared__ uint8_t smem_raw[];
   WalkSmem& s = *reinterpret_cast<WalkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (launch_failed(p.err)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool lead = tid == 0;
   // this thread's half row of the M=64 accumulators: row i, columns 32h .. 32h+31
