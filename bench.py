@@ -52,7 +52,7 @@ UT_BWD64_MMAS = 31   # the diagonal-chunk attention backward and the chain rule 
 # dram__bytes_write.sum) of a 64-head launch (batch 4 x 16 heads: four head groups, a working set
 # above L2) divided by 64 — the kernel takes heads 16 at a time, so a launch over more heads repeats
 # that traffic per group.  To be retaken whenever the kernel changes.
-BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (1712006144 + 436957952) / 64
+BWD_SCAN_DRAM_BYTES_PER_HEAD_L4096 = (1713337088 + 439145472) / 64
 # DRAM bytes per head of one decode step at t = 32768 (split + combine kernels): ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum) of a batch-4 x 32-head step divided by 128 heads
 # (the step's traffic grows in proportion to the heads it processes).  To be retaken whenever the
@@ -103,10 +103,12 @@ def parse():
     ap.add_argument("--heads", type=int, default=None, help="override the heads (profiling on a smaller case)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode workload's batch (profiling on a smaller case)")
-    ap.add_argument("--only", default=None, choices=["train", "decode", "configs", "handoff", "d128"],
+    ap.add_argument("--only", default=None, choices=["train", "decode", "configs", "handoff", "d128",
+                                                     "d128_train_small"],
                     help="run one leg alone (profiling): the training step, the decode step, the "
-                         "per-workload forward/training legs, the prefill -> decode hand-off or the "
-                         "head-dim-128 legs")
+                         "per-workload forward/training legs, the prefill -> decode hand-off, the "
+                         "head-dim-128 legs, or a small head-dim-128 training step (batch 1 x 8 heads x "
+                         "2048 unless --batch / --heads say otherwise) for profiler captures")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload legs")
     return ap.parse_args()
 
@@ -308,6 +310,9 @@ def run_ours(args):
         return
     if args.only == "d128":
         print(json.dumps({"head_dim_128": run_head_dim_128(args, pa, dev, pk)}), flush=True)
+        return
+    if args.only == "d128_train_small":
+        print(json.dumps({"d128_train_small": run_d128_train_small(args, pa, dev)}), flush=True)
         return
     if args.only == "train":
         args.no_decode = args.no_configs = args.no_cpu_baseline = True
@@ -967,6 +972,42 @@ def run_head_dim_128(args, pa, dev, pk):
              "workload": "fwd+bwd, batch 4, 16 heads, d=128, L=2048, bf16 inputs: tcgen05 forward (chunk 64), "
                          "backward (chunk 32) on TF32 warp MMAs (mma.sync, fp32 accumulation)"}
     return {"decode": decode, "forward": fwd, "train": train}
+
+
+def run_d128_train_small(args, pa, dev):
+    """A small head-dim-128 training step (tcgen05 forward + the backward's three phases) for
+    profiler captures: batch 1 x 8 heads x 2048 unless --batch / --heads override; each backward
+    phase also timed alone with CUDA events."""
+    Bt, H, L, d = args.batch or 1, args.heads or 8, 2048, 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    x = {n: (torch.randn(Bt, H, L, d, device=dev, generator=g) / math.sqrt(d)).to(torch.bfloat16)
+         for n in ("q", "k", "v")}
+    wr = torch.randn(Bt, H, L, d, device=dev, generator=g)
+    x["w"] = (wr / wr.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    x["beta"] = 2.0 * torch.sigmoid(torch.randn(Bt, H, L, device=dev, generator=g))
+    x["dO"] = torch.randn(Bt, H, L, d, device=dev, generator=g).to(torch.bfloat16)
+    o, lse = pa.fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, 1.0)
+    wsb = pa.workspace(pa.make_desc(x["q"], 1.0), 1, dev)
+    grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["q"]), dv=torch.empty_like(x["q"]),
+                 dw=torch.empty_like(x["q"]), dbeta=torch.empty_like(x["beta"]))
+
+    def bwd(phases):
+        pa.bwd(x["q"], x["k"], x["v"], x["w"], x["beta"], o, lse, x["dO"], 1.0, ws=wsb, out=grads, phases=phases)
+    out = {"workload": f"fwd+bwd, batch {Bt}, {H} heads, d=128, L={L}, bf16"}
+    for name, ph in (("prepare", 1), ("scan", 2), ("finish", 4)):
+        ms = []
+        for _ in range(max(1, args.steps)):
+            if ph > 1:
+                bwd(ph - 1)  # the phases before this one, untimed
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            bwd(ph)
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        out[f"{name}_ms"] = min(ms)
+    return out
 
 
 def main():
