@@ -8,7 +8,8 @@ cases use a large score scale (score standard deviation 5 to 10 nats): rows whos
 keys then meet far larger scores in earlier chunks, at different steps for different rows of
 one warp.  Each case first counts, from the oracle's explicit logits of one head, the rows that
 must rescale, then compares the tensor-core forward (head dims 64 and 128, either sign of the
-scale, with and without the forget gate, and the training forward that stores Z) with the oracle.
+scale, with and without the forget gate, the training forward that stores Z, and the
+context-parallel chain whose scan runs over the other shards' key blocks) with the oracle.
 
 Tolerance: the scores here are |scale| times those of the same inputs at scale 1, and the bf16
 rounding of the transported queries and keys perturbs each score by a relative amount, so the
@@ -99,3 +100,26 @@ def test_training_forward_lazy_rescale(cuda_lib, record_margin):
                     phases=pa.PATH_FWD_ALL | pa.PATH_FWD_STORE_Z, check=True)
     torch.cuda.synchronize()
     check_fwd(inp, o, lse, scale, f"lazy rescale, training forward (Z stored), scale {scale}", record_margin)
+
+
+def test_context_parallel_chain_lazy_rescale(cuda_lib, record_margin):
+    """The context-parallel chain (the scan in its block mode over the other shards' key blocks)."""
+    from softmax_attention_chunk_gb300.context_parallel import ShardOps, emulate_ring
+
+    B, H, L, world, scale = 1, 2, 512, 4, 40.0
+    inp = gen_path_inputs(B, H, L, 64, "bf16", seed=3421, near2_frac=0.05)
+    assert rows_that_rescale(inp, 0, scale) >= 8
+    Ls = L // world
+    ops = []
+    for r in range(world):
+        sl = slice(r * Ls, (r + 1) * Ls)
+        s = {n: (None if t is None else t[:, :, sl].contiguous().to(DEV)) for n, t in inp.items()}
+        ops.append(ShardOps(s["q"], s["k"], s["v"], s["w"], s["beta"], s["log_f"], scale))
+    res = emulate_ring(ops)
+    torch.cuda.synchronize()
+    for op in ops:
+        cuda_lib.check_workspace(op.desc, 0, op.ws)
+    o = torch.cat([r[0] for r in res], dim=2)
+    lse = torch.cat([r[1] for r in res], dim=2)
+    check_fwd(inp, o, lse, scale, f"lazy rescale, context-parallel chain over {world} shards, scale {scale}",
+              record_margin)
