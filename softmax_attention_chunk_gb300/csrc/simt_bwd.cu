@@ -1,4 +1,6 @@
-// SIMT (fp32 CUDA-core) backward of PaTH attention.
+// CUDA-core backward of PaTH attention: plain fp32 loops for fp32 inputs; for bf16 inputs (head
+// dim 128, and chunk 32 at head dim 64) the same kernels run their small products as TF32 warp
+// MMAs (smem_mm.cuh) with fp32 accumulation.
 //
 // The pages give no backward; this is the exact derivative of the blockwise forward of the
 // PaTH reading notes (cc.laoqi.cc/papers/2505.16381), §2.6–§2.7.  With Z_{b,c} the query chunk b
@@ -23,7 +25,8 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int NTM = 512;  // threads of the backward scan (one CTA per SM: 16 warps hide the latencies)
-// D (template parameter): head dim, 64 or 128; DS = D + 1 is the padded smem row stride.
+// D (template parameter): head dim, 64 or 128; DS is the padded shared-memory row stride (D + 1,
+// or D + 4 for the backward scan's TF32 products: see BwdMainSmem).
 
 // D_i = dO_i . o_i; padded rows get 0.  A row is read by a group of D / VEC lanes with 16-byte
 // loads (VEC elements each), a warp covers DOT_PASSES row groups with all loads issued before the

@@ -1,5 +1,6 @@
-// Block-level product of small fp32 matrices held in shared memory, used by the per-chunk UT
-// kernels (32x32, 32x64, 64x64 operands).  C = op(A) op(B) with
+// Block-level product of small fp32 matrices held in shared memory, used by the CUDA-core per-chunk
+// UT kernels (32x32, 32x64, 64x64 operands) and the CUDA-core backward scan (32- or 64-row chunks
+// against head-dim-wide operands up to 128 x 128).  C = op(A) op(B) with
 //   op(A)(i,k) = TA ? A[k*lda + i] : A[i*lda + k]    (M x K)
 //   op(B)(k,j) = TB ? B[j*ldb + k] : B[k*ldb + j]    (K x N)
 // and every result element handed to epi(i, j, value).  The operands' zeros encode the
@@ -7,7 +8,8 @@
 //
 // TC = true runs 16x8x8 TF32 warp MMAs (fp32 accumulate; operands rounded to TF32, relative
 // 2^-11), the bf16 path's choice: these products are too small and too dependent for tcgen05's
-// 64/128-row tiles and TMEM round trips.  TC = false is a plain fp32 loop (fp32 mode).
+// 64/128-row tiles and TMEM round trips (the head-dim-128 backward keeps them here because its
+// accumulators exceed the SM's TMEM).  TC = false is a plain fp32 loop (fp32 mode).
 #pragma once
 
 #include <cuda_runtime.h>
